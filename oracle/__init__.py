@@ -1,0 +1,25 @@
+"""CPU oracle for one speculative-decoding draft round: TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, obviously-correct NumPy restatement of what the round computes,
+written from hf2q 0.1.1's source pages (`models/qwen35/mtp.rs`,
+`spec_decode/dflash/tensors.rs`, `spec_decode/dflash/qwen35_orchestrator.rs`).
+Floating point is F32 over BF16-decoded weights, as those pages fix it
+(BF16 projection weights, F32 activations/residuals/logits); every function
+also runs in float64 (`dt=np.float64`) as a shadow to bound rounding.
+
+Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s cpu_baseline /
+reference arm may import this package. The CUDA library never does, and this
+package never imports the CUDA library: they share no code.
+
+Pin status (what each function is checked against, in tests/test_oracle_*.py):
+  decode_bf16            canonical round trip, odd length, misread signature, all 65536 patterns
+  rmsnorm / head_rmsnorm closed forms (constant vector, hand example), scale invariance, unit RMS
+  rope                   hand example, norm preservation, R(p)R(q)=R(p+q), relative-position property
+  sdpa                   brute-force float64 loops, one key, equal keys, GQA == MHA with repeated heads
+  silu / sigmoid         special values
+  argmax_top2            planted maxima, ties to the lowest index, brute-force scan
+  accept_walk            hand examples + brute force over all short draft/target pairs
+  kv_rollback            hand examples, overflow rejection
+  dflash forward / mtp   special cases with closed forms (zero projections, one key), float64 shadow
+  moe routing            hand example, top-k weights sum to one, one-expert reduction to dense
+"""

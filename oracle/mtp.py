@@ -1,0 +1,110 @@
+"""Oracle MTP (NextN) single-token draft step, dense or MoE FFN, chained 1..N steps.
+
+Test infrastructure only (see the package docstring).
+
+mtp.rs (hf2q 0.1.1), `MtpWeights::forward_draft_with_hidden`:
+    x      = eh_embed . rmsnorm(embed_t, enorm, 1e-6) + eh_hidden . rmsnorm(prev_hidden, hnorm, 1e-6)
+                                                         (`project_embedding_and_hidden`)
+    xn     = rmsnorm(x, attn_norm)
+    q,k,v  = xn Wq^T, xn Wk^T, xn Wv^T;  gate = xn Wgate^T (when present)
+    q, k   = rope(headnorm(q), pos), rope(headnorm(k), pos)
+    K/V appended at pos; o = softmax(q K[0..pos]^T / sqrt(d)) V[0..pos]
+    o      = o * sigmoid(gate)                           (`apply_sigmoid_gate_multiply`)
+    h1     = x + o Wo^T                                   (fused residual + post-attn norm)
+    hidden = h1 + FFN(rmsnorm(h1, post_attn_norm))        (`forward_ffn_residual`)
+    logits = rmsnorm(hidden, shared_head_norm) lm_head^T  (`forward_shared_head`)
+Chained steps feed (hidden, embedding of the step's argmax) into the next step at
+pos + 1 (`forward_draft_with_hidden` doc: K=N chaining).
+
+MoE FFN (mtp.rs `MtpFfnWeightsGpu::Moe`; routing details are not on the page, read
+as): router softmax over all experts, the top-k by probability (lower index first on
+ties) renormalised to sum one, weighted sum of the chosen experts' SwiGLU, plus one
+shared SwiGLU expert scaled by sigmoid(x . w_shared_gate).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .core import (OracleError, decode_bf16, head_rmsnorm, linear, lm_head_argmax, rmsnorm, rope,
+                   sdpa, sigmoid, silu, swiglu)
+
+
+def moe_route(x, router_bits, top_k, dt=np.float32):
+    """(expert ids, weights): softmax over router logits, top-k, renormalised."""
+    logits = linear(x, router_bits, dt)
+    m = np.max(logits)
+    p = np.exp(logits - m)
+    p = p / np.sum(p)
+    order = sorted(range(p.shape[0]), key=lambda e: (-float(p[e]), e))[:top_k]
+    sel = np.array(order, dtype=np.int64)
+    wsel = p[sel] / np.sum(p[sel])
+    return sel, wsel.astype(dt)
+
+
+def moe_ffn(x, w, top_k, dt=np.float32):
+    sel, ws = moe_route(x, w["router"], top_k, dt)
+    out = np.zeros_like(np.asarray(x, dt))
+    for e, we in zip(sel, ws):
+        out = out + we * swiglu(x, w["exp_g"][e], w["exp_u"][e], w["exp_d"][e], dt)
+    sg = sigmoid(linear(x, w["sh_gate"], dt), dt)            # [1]
+    out = out + sg[0] * swiglu(x, w["sh_g"], w["sh_u"], w["sh_d"], dt)
+    return out, sel, ws
+
+
+def mtp_step(cfg, w, k_cache, v_cache, pos, prev_hidden, token, dt=np.float32):
+    """One MTP draft step for one sequence. k_cache/v_cache [n_kv, cap, d] are updated
+    at `pos`. Returns (hidden [H], argmax id, top1, top2, logits-free info dict)."""
+    H, nq, nkv, d = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    eps, theta, rot = cfg.rms_eps, cfg.rope_theta, cfg.rot
+    if pos + 1 > k_cache.shape[1]:
+        raise OracleError("MTP KV slot capacity exceeded")
+    e = decode_bf16(w["embed"][int(token)], dt)
+    x = (linear(rmsnorm(e, w["enorm"], 1e-6, dt), w["eh_embed"], dt)
+         + linear(rmsnorm(np.asarray(prev_hidden, dt), w["hnorm"], 1e-6, dt), w["eh_hidden"], dt))
+    xn = rmsnorm(x, w["attn_norm"], eps, dt)
+    q = head_rmsnorm(linear(xn, w["wq"], dt), w["q_norm"], nq, d, eps, dt)
+    k = head_rmsnorm(linear(xn, w["wk"], dt), w["k_norm"], nkv, d, eps, dt)
+    v = linear(xn, w["wv"], dt)
+    q = rope(q.reshape(1, nq, d), [pos], rot, theta, dt)
+    k = rope(k.reshape(1, nkv, d), [pos], rot, theta, dt)
+    k_cache[:, pos, :] = k[0]
+    v_cache[:, pos, :] = v.reshape(nkv, d)
+    keys = np.asarray(k_cache[:, :pos + 1, :], dt).transpose(1, 0, 2)
+    vals = np.asarray(v_cache[:, :pos + 1, :], dt).transpose(1, 0, 2)
+    o = sdpa(q, keys, vals, None, dt).reshape(nq * d)
+    if w.get("w_gate") is not None:
+        o = o * sigmoid(linear(xn, w["w_gate"], dt), dt)
+    h1 = x + linear(o, w["wo"], dt)
+    fin = rmsnorm(h1, w["post_norm"], eps, dt)
+    info = {}
+    if w.get("router") is not None:
+        f, sel, ws = moe_ffn(fin, w, cfg.top_k, dt)
+        info["experts"], info["expert_w"] = sel, ws
+    else:
+        f = swiglu(fin, w["wg"], w["wu"], w["wd"], dt)
+    hidden = h1 + f
+    xh = rmsnorm(hidden, w["shared_head_norm"], eps, dt)
+    idx, t1, t2 = lm_head_argmax(xh[None, :], w["lm_head"], dt)
+    return hidden, int(idx[0]), float(t1[0]), float(t2[0]), info
+
+
+def mtp_forward_draft(cfg, w, cache_k, cache_v, seq_len, prev_hidden, tokens, n_steps,
+                      dt=np.float32):
+    """Chained MTP draft: n_steps steps per sequence. cache_k/cache_v [B, n_kv, cap, d]
+    (updated), seq_len [B]. Returns hidden [n_steps, B, H], argmax [n_steps, B],
+    top1/top2 [n_steps, B], new seq_len, per-step info."""
+    B = len(tokens)
+    hid = np.zeros((n_steps, B, cfg.hidden), dtype=dt)
+    am = np.zeros((n_steps, B), dtype=np.int64)
+    t1s = np.zeros((n_steps, B))
+    t2s = np.zeros((n_steps, B))
+    seq = np.asarray(seq_len, dtype=np.int64).copy()
+    infos = []
+    for b in range(B):
+        h, tok = np.asarray(prev_hidden[b], dt), int(tokens[b])
+        for s in range(n_steps):
+            h, tok, t1, t2, info = mtp_step(cfg, w, cache_k[b], cache_v[b], int(seq[b]), h, tok, dt)
+            seq[b] += 1
+            hid[s, b], am[s, b], t1s[s, b], t2s[s, b] = h, tok, t1, t2
+            infos.append(info)
+    return hid, am, t1s, t2s, seq, infos
