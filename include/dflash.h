@@ -1,0 +1,289 @@
+/*
+ * dflash.h — C ABI of the GB300 speculative-decoding draft-round library (libdflash.so).
+ *
+ * One draft round, as hf2q 0.1.1's `spec_decode/dflash/qwen35_orchestrator.rs` runs it
+ * (module doc, "Per-round loop", steps 1-9): a drafter forward over a block of K+1
+ * positions, a per-position argmax over the vocabulary, the greedy accept-prefix walk
+ * against the verifier's argmaxes and the KV rollback of the rejected positions. The
+ * Qwen3.5 MTP (NextN) draft step of `models/qwen35/mtp.rs` (`forward_draft_with_hidden`)
+ * is the second drafter.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer is caller-owned. Device pointers are CUDA global memory on the current
+ *    device; "host" is marked where a pointer is host memory. The library allocates and frees
+ *    nothing and keeps no state between calls besides the thread-local error text.
+ *  - BF16 tensors are passed as `const uint16_t *` holding BF16 bit patterns (little-endian,
+ *    row-major `[out, in]`, as tensors.rs `upload_bf16` copies them: no transpose, no
+ *    dequantisation). RMSNorm weights are F32 (tensors.rs `upload_bf16_as_f32`: a BF16 buffer
+ *    read as F32 is the misinterpretation bug that file's tests guard against).
+ *    Activations, residuals, logits and the KV cache are F32.
+ *  - Calls are asynchronous on `stream` (a `cudaStream_t`; NULL = legacy default stream). A
+ *    call returns after host-side validation and kernel launches; nothing synchronises except
+ *    `df_draft_round_host`. Return value: DF_OK or a negative `df_status`; `df_last_error()`
+ *    then holds a message. Host-detected errors launch nothing and modify nothing.
+ *  - Conditions only the device can see (a sequence's `n_new` above `n_new_max`, a cache that
+ *    would overflow, a token id outside [0, vocab), a rollback longer than the cache) are
+ *    clamped so no access leaves its buffer, and the failing `df_status` code is written to the
+ *    optional device word `d_status` (int32, may be NULL). A kernel never traps.
+ *  - `ws` is a device workspace of at least the size the matching `*_workspace_bytes` query
+ *    returns (256-byte aligned). Its counter region must be zero before the first call that
+ *    uses it (allocate it zeroed); every call leaves it zero again. Calls sharing one workspace
+ *    must be ordered on the GPU (the same stream, or events).
+ *  - Dimensions: every K dimension of a projection (hidden, intermediate, n_q_heads*head_dim,
+ *    n_target_layers*hidden) must be a multiple of 8; head_dim a multiple of 32 and <= 256;
+ *    rotary_dim even and <= head_dim; n_q_heads a multiple of n_kv_heads.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *df_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    DF_OK = 0,
+    DF_EINVAL = -1,      /* null pointer, bad flag, id outside [0, vocab) */
+    DF_ESHAPE = -2,      /* dimension out of range or misaligned; n_new above n_new_max */
+    DF_ECAPACITY = -3,   /* KV cache would overflow, or a rollback exceeds seq_len */
+    DF_EWORKSPACE = -4,  /* workspace missing, misaligned or too small */
+    DF_ECUDA = -5,       /* a CUDA runtime call or launch failed */
+    DF_ETIMEOUT = -6     /* a bounded device-side wait gave up */
+} df_status;
+
+/* Thread-local text of the last error returned on this thread ("" if none). */
+const char *df_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int df_version(void);
+
+/* ------------------------------------------------------------------------------------------
+ * DFlash drafter (tensors.rs `DFlashLayerTensors`, `DFlashModelTensors`; dflash config fields
+ * seen in qwen35_orchestrator.rs: target_layer_ids, mask_token_id, hidden_size, head_dim).
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t hidden;           /* H */
+    int32_t n_layers;         /* decoder layers */
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;         /* d */
+    int32_t intermediate;     /* SwiGLU I */
+    int32_t vocab;            /* V (shared embed / lm_head rows) */
+    int32_t n_target_layers;  /* fc input = n_target_layers * H */
+    int32_t rotary_dim;       /* 0 = head_dim */
+    int32_t mask_token_id;    /* id of the K mask positions of the block */
+    int32_t causal_block;     /* 0: block positions attend to each other freely; 1: causal */
+    float rms_eps;
+    float rope_theta;
+    float embed_scale;        /* multiplies gathered embedding rows (1.0) */
+} df_dflash_config;
+
+typedef struct {
+    const float *input_norm;      /* [H] F32, before attention */
+    const float *post_attn_norm;  /* [H] F32, before the SwiGLU */
+    const float *q_norm;          /* [d] F32, per-head RMSNorm of q */
+    const float *k_norm;          /* [d] F32, per-head RMSNorm of k */
+    const uint16_t *wq;           /* [n_q*d, H] BF16 */
+    const uint16_t *wk;           /* [n_kv*d, H] BF16 */
+    const uint16_t *wv;           /* [n_kv*d, H] BF16 */
+    const uint16_t *wo;           /* [H, n_q*d] BF16 */
+    const uint16_t *w_gate;       /* [I, H] BF16 */
+    const uint16_t *w_up;         /* [I, H] BF16 */
+    const uint16_t *w_down;       /* [H, I] BF16 */
+} df_layer_weights;
+
+typedef struct {
+    const uint16_t *fc;              /* [H, n_target_layers*H] BF16 */
+    const float *hidden_norm;        /* [H] F32, RMSNorm of the fc output */
+    const float *final_norm;         /* [H] F32 */
+    const df_layer_weights *layers;  /* HOST array [n_layers] */
+    const uint16_t *embed;           /* [V, H] BF16 token embedding (the target's, borrowed) */
+    const uint16_t *lm_head;         /* [V, H] BF16 (the target's, borrowed) */
+} df_dflash_weights;
+
+/* Per-layer F32 KV cache. Row p of sequence b, KV head h lives at
+ * k[l] + ((b * n_kv + h) * cap + p) * head_dim. seq_len[b] counts the valid rows. */
+typedef struct {
+    float *const *k;     /* HOST array [n_layers] of device pointers [batch, n_kv, cap, d] */
+    float *const *v;     /* HOST array [n_layers], same layout */
+    int32_t *seq_len;    /* device [batch] */
+    int32_t cap;         /* rows per sequence and head */
+    int32_t batch;
+    int32_t n_layers;
+} df_kv_cache;
+
+/* Workspace bytes for dflash_block_forward / df_draft_round at batch B, block = K+1 and
+ * at most n_new_max new context rows per sequence. 0 on invalid arguments. */
+size_t df_dflash_workspace_bytes(const df_dflash_config *cfg, int B, int block, int n_new_max);
+
+/*
+ * dflash_block_forward — the drafter forward of one round (qwen35_orchestrator.rs steps 2-4,
+ * `dispatch_dflash_model_forward`; tensors.rs for the tensors it reads).
+ *   block_ids          device int32 [B, block]: [last_token, mask_token_id x K] per sequence
+ *   target_hidden_new  device F32 [B, n_new_max, n_target_layers*H]: the target hidden rows of
+ *                      the n_new[b] context positions committed since the last round
+ *   n_new              device int32 [B], each in [0, n_new_max]
+ *   h_final            device F32 [B, block, H] out: final-normed hidden of every block row
+ * For every layer the n_new[b] context rows' K/V (per-head k-norm, RoPE at their absolute
+ * positions seq_len[b] + j) are appended at cache rows seq_len[b] + j; the block rows (at
+ * positions seq_len[b] + n_new[b] + i) attend over the whole cache plus the block and their
+ * own K/V are not kept. On return seq_len[b] has advanced by n_new[b].
+ * Device status: DF_ESHAPE (n_new out of range), DF_ECAPACITY (append beyond cap),
+ * DF_EINVAL (block id outside [0, vocab)).
+ */
+int dflash_block_forward(const df_dflash_config *cfg, const df_dflash_weights *w,
+                         const df_kv_cache *cache, const int32_t *block_ids,
+                         const float *target_hidden_new, const int32_t *n_new, int n_new_max,
+                         int B, int block, float *h_final, void *ws, size_t ws_bytes,
+                         int32_t *d_status, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * lm_head + per-row argmax (qwen35_orchestrator.rs step 5,
+ * `per_position_argmax_from_normed_hidden`; mtp.rs `forward_shared_head`), fused so the
+ * logits never reach global memory.
+ * ---------------------------------------------------------------------------------------- */
+size_t df_lm_head_workspace_bytes(int rows, int H, int V);
+
+/*   W     device BF16 [V, H];  X device F32 [rows, H] (already normed)
+ *   idx   device int32 [rows] out: argmax, the lowest index among exactly equal maxima
+ *   top1  device F32 [rows] out or NULL: the largest logit
+ *   top2  device F32 [rows] out or NULL: the second largest (== top1 when the max is tied) */
+int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
+                   float *top1, float *top2, void *ws, size_t ws_bytes, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Greedy accept walk (qwen35_orchestrator.rs module doc "Greedy accept-walk consistency
+ * invariant" and steps 7-9: `step_round_from_argmaxes`, rollback = K - accept_count).
+ * ---------------------------------------------------------------------------------------- */
+/*   drafts       device int32, row b at drafts + b*drafts_ld, K entries (block positions 1..K)
+ *   target       device int32 [B, K+1]: verifier argmaxes over [last_token, drafts...]
+ *   eos          device int32 [n_eos] (may be NULL when n_eos == 0)
+ *   committed    device int32 [B, K+1] out: accepted drafts + the free token, cut after the
+ *                first EOS id; entries past n_committed[b] are set to -1
+ *   n_committed, accept_count, hit_eos, rollback   device int32 [B] out
+ * accept_count = longest prefix with drafts == target; rollback = K - accept_count
+ * (independent of the EOS cut); 1 <= n_committed <= K+1. */
+int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
+                         int K, const int32_t *eos, int n_eos, int32_t *committed,
+                         int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                         int32_t *rollback, df_stream_t stream);
+
+/* Same walk on the host for one sequence (all pointers HOST memory). Synchronous. */
+int accept_prefix_argmax_host(const int32_t *drafts, const int32_t *target, int K,
+                              const int32_t *eos, int n_eos, int32_t *committed,
+                              int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                              int32_t *rollback);
+
+/* ------------------------------------------------------------------------------------------
+ * KV rollback (qwen35_orchestrator.rs step 8, `rollback_kv`): seq_len[b] -= n[b]. Cache rows
+ * are not touched. If n[b] < 0 or n[b] > seq_len[b], seq_len[b] is left unchanged and
+ * DF_ECAPACITY is written to d_status.
+ * ---------------------------------------------------------------------------------------- */
+int kv_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *d_status,
+                df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Whole DFlash draft round on the device: the benchmark unit. Steps: block build
+ * [last_token, mask x K] + embed gather, dflash_block_forward, lm_head argmax of every block
+ * row, drafts = argmax[1..K], accept walk against target_argmax, rollback of the verifier's
+ * KV length target_seq_len[b] by K - accept_count[b].
+ *   last_token      device int32 [B]
+ *   target_argmax   device int32 [B, K+1]
+ *   target_seq_len  device int32 [B] in/out (verifier cache length after its K+1 positions)
+ *   argmax_out      device int32 [B, K+1] out (position 0 = the drafter's own guess for
+ *                   last_token's successor; 1..K = the drafts)
+ *   committed, n_committed, accept_count, hit_eos, rollback: as accept_prefix_argmax
+ * The drafter cache advances by n_new[b] exactly as in dflash_block_forward.
+ * ---------------------------------------------------------------------------------------- */
+int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
+                   const df_kv_cache *cache, const int32_t *last_token,
+                   const float *target_hidden_new, const int32_t *n_new, int n_new_max, int B,
+                   int K, const int32_t *target_argmax, const int32_t *eos, int n_eos,
+                   int32_t *target_seq_len, int32_t *argmax_out, int32_t *committed,
+                   int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                   int32_t *rollback, void *ws, size_t ws_bytes, int32_t *d_status,
+                   df_stream_t stream);
+
+/* Bytes of the host-buffer round's staging area (device), in addition to the round's own. */
+size_t df_draft_round_host_workspace_bytes(const df_dflash_config *cfg, int B, int K,
+                                           int n_new_max, int n_eos);
+
+/*
+ * df_draft_round_host — the same round with HOST inputs and outputs: copies last_token,
+ * target_hidden_new, n_new, target_argmax, eos and target_seq_len into device staging carved
+ * from `ws`, runs df_draft_round, copies the results back, and synchronises `stream`.
+ * Host buffers should be pinned for asynchronous copies. Outputs (host): target_seq_len
+ * (in/out), argmax_out [B, K+1], committed [B, K+1], n_committed, accept_count, hit_eos,
+ * rollback [B], status (the device status word). ws must hold
+ * df_dflash_workspace_bytes(cfg, B, K+1, n_new_max) + df_draft_round_host_workspace_bytes().
+ */
+int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
+                        const df_kv_cache *cache, const int32_t *last_token,
+                        const float *target_hidden_new, const int32_t *n_new, int n_new_max,
+                        int B, int K, const int32_t *target_argmax, const int32_t *eos,
+                        int n_eos, int32_t *target_seq_len, int32_t *argmax_out,
+                        int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                        int32_t *hit_eos, int32_t *rollback, int32_t *status, void *ws,
+                        size_t ws_bytes, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * MTP (NextN) draft step, mtp.rs `MtpWeights::forward_draft_with_hidden`, chained n_steps
+ * times (the returned hidden feeds the next step with the embedding of the step's argmax).
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t hidden, n_q_heads, n_kv_heads, head_dim, vocab;
+    int32_t intermediate;   /* dense SwiGLU I (0 when MoE) */
+    int32_t n_experts;      /* 0 = dense FFN */
+    int32_t top_k;          /* experts chosen per token (MoE) */
+    int32_t expert_inter;   /* per-expert SwiGLU intermediate (MoE) */
+    int32_t shared_inter;   /* shared-expert SwiGLU intermediate (MoE) */
+    int32_t rotary_dim;     /* 0 = head_dim */
+    float rms_eps, rope_theta;
+} df_mtp_config;
+
+typedef struct {
+    const float *enorm, *hnorm;             /* [H] F32 (eps fixed at 1e-6) */
+    const uint16_t *eh_embed, *eh_hidden;   /* [H, H] BF16 each (eh_proj halves) */
+    const float *attn_norm, *post_attn_norm, *q_norm, *k_norm;   /* F32 */
+    const uint16_t *wq, *wk, *wv;           /* [n_q*d, H], [n_kv*d, H], [n_kv*d, H] */
+    const uint16_t *w_gate;                 /* [n_q*d, H] or NULL (no output gate) */
+    const uint16_t *wo;                     /* [H, n_q*d] */
+    const float *shared_head_norm;          /* [H] */
+    const uint16_t *embed, *lm_head;        /* [V, H] */
+    /* dense FFN */
+    const uint16_t *w_gate_mlp, *w_up, *w_down;   /* [I, H], [I, H], [H, I] */
+    /* MoE FFN */
+    const uint16_t *router;                 /* [E, H] */
+    const uint16_t *exp_gate, *exp_up;      /* [E, Ie, H] */
+    const uint16_t *exp_down;               /* [E, H, Ie] */
+    const uint16_t *sh_gate_mlp, *sh_up;    /* [Is, H] */
+    const uint16_t *sh_down;                /* [H, Is] */
+    const uint16_t *sh_expert_gate;         /* [1, H]: sigmoid gate of the shared expert */
+} df_mtp_weights;
+
+size_t df_mtp_workspace_bytes(const df_mtp_config *cfg, int B);
+
+/*   cache        one-layer KV slot (n_layers = 1); step s of sequence b writes row
+ *                seq_len[b] + s and attends over rows [0, seq_len[b] + s]; seq_len advances
+ *                by n_steps
+ *   prev_hidden  device F32 [B, H]: hidden state of the verifier for the previous token
+ *   token        device int32 [B]: the just-accepted token (its embedding is embed[token])
+ *   hidden_out   device F32 [n_steps, B, H] out: pre-head hidden of every step
+ *   argmax_out   device int32 [n_steps, B] out: the draft token of every step
+ *   logits_out   device F32 [B, V] or NULL: dense logits of the last step, only if asked */
+int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
+                      const df_kv_cache *cache, const float *prev_hidden, const int32_t *token,
+                      int B, int n_steps, float *hidden_out, int32_t *argmax_out,
+                      float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
+                      df_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

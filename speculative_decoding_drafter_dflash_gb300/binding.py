@@ -1,0 +1,315 @@
+"""Thin ctypes binding of libdflash.so: same names as the C ABI in include/dflash.h.
+
+Argument marshalling only: torch tensors become device pointers, Python shapes become
+the C structs, the current torch CUDA stream becomes the `cudaStream_t`. Every step of
+the draft round runs in the library's CUDA kernels. There is no fallback: if the
+library is missing, importing a call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int, c_int32, c_size_t, c_void_p
+from typing import List, Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdflash.so")
+
+DF_OK, DF_EINVAL, DF_ESHAPE, DF_ECAPACITY, DF_EWORKSPACE, DF_ECUDA, DF_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+STATUS_NAMES = {0: "DF_OK", -1: "DF_EINVAL", -2: "DF_ESHAPE", -3: "DF_ECAPACITY",
+                -4: "DF_EWORKSPACE", -5: "DF_ECUDA", -6: "DF_ETIMEOUT"}
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class DFlashConfig(ctypes.Structure):
+    _fields_ = [("hidden", c_int32), ("n_layers", c_int32), ("n_q_heads", c_int32),
+                ("n_kv_heads", c_int32), ("head_dim", c_int32), ("intermediate", c_int32),
+                ("vocab", c_int32), ("n_target_layers", c_int32), ("rotary_dim", c_int32),
+                ("mask_token_id", c_int32), ("causal_block", c_int32), ("rms_eps", c_float),
+                ("rope_theta", c_float), ("embed_scale", c_float)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("input_norm", "post_attn_norm", "q_norm", "k_norm", "wq",
+                                        "wk", "wv", "wo", "w_gate", "w_up", "w_down")]
+
+
+class DFlashWeights(ctypes.Structure):
+    _fields_ = [("fc", c_void_p), ("hidden_norm", c_void_p), ("final_norm", c_void_p),
+                ("layers", POINTER(LayerWeights)), ("embed", c_void_p), ("lm_head", c_void_p)]
+
+
+class KvCache(ctypes.Structure):
+    _fields_ = [("k", POINTER(c_void_p)), ("v", POINTER(c_void_p)), ("seq_len", c_void_p),
+                ("cap", c_int32), ("batch", c_int32), ("n_layers", c_int32)]
+
+
+class MtpConfig(ctypes.Structure):
+    _fields_ = [("hidden", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32),
+                ("head_dim", c_int32), ("vocab", c_int32), ("intermediate", c_int32),
+                ("n_experts", c_int32), ("top_k", c_int32), ("expert_inter", c_int32),
+                ("shared_inter", c_int32), ("rotary_dim", c_int32), ("rms_eps", c_float),
+                ("rope_theta", c_float)]
+
+
+class MtpWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in (
+        "enorm", "hnorm", "eh_embed", "eh_hidden", "attn_norm", "post_attn_norm", "q_norm",
+        "k_norm", "wq", "wk", "wv", "w_gate", "wo", "shared_head_norm", "embed", "lm_head",
+        "w_gate_mlp", "w_up", "w_down", "router", "exp_gate", "exp_up", "exp_down",
+        "sh_gate_mlp", "sh_up", "sh_down", "sh_expert_gate")]
+
+
+_lib = None
+
+# (name, restype, argtypes)
+_SIGS = [
+    ("df_last_error", ctypes.c_char_p, []),
+    ("df_version", c_int, []),
+    ("df_dflash_workspace_bytes", c_size_t, [POINTER(DFlashConfig), c_int, c_int, c_int]),
+    ("dflash_block_forward", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), POINTER(KvCache),
+                                     c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
+                                     c_void_p, c_size_t, c_void_p, c_void_p]),
+    ("df_lm_head_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
+    ("lm_head_argmax", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                               c_void_p, c_void_p, c_size_t, c_void_p]),
+    ("accept_prefix_argmax", c_int, [c_void_p, c_int, c_void_p, c_int, c_int, c_void_p, c_int,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("accept_prefix_argmax_host", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p,
+                                          c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("kv_rollback", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
+    ("df_draft_round", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), POINTER(KvCache),
+                               c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
+                               c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                               c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
+    ("df_draft_round_host_workspace_bytes", c_size_t, [POINTER(DFlashConfig), c_int, c_int, c_int,
+                                                       c_int]),
+    ("df_draft_round_host", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights),
+                                    POINTER(KvCache), c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                    c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_size_t, c_void_p]),
+    ("df_mtp_workspace_bytes", c_size_t, [POINTER(MtpConfig), c_int]),
+    ("mtp_forward_draft", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), POINTER(KvCache),
+                                  c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_size_t, c_void_p, c_void_p]),
+]
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m speculative_decoding_drafter_dflash_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in _SIGS:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().df_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != DF_OK:
+        raise DFlashError(rc, last_error())
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ----------------------------------------------------------------------------- structs
+class DFlashModel:
+    """C structs for a DFlash drafter: config, weight pointers, KV cache. Keeps the tensors
+    and ctypes arrays alive for the lifetime of the object."""
+
+    def __init__(self, shape, weights, cache, embed_scale: float = 1.0):
+        self.shape = shape
+        self.cfg = DFlashConfig(shape.hidden, shape.n_layers, shape.n_q_heads, shape.n_kv_heads,
+                                shape.head_dim, shape.intermediate, shape.vocab,
+                                shape.n_target_layers, shape.rotary_dim, shape.mask_id,
+                                shape.causal_block, shape.rms_eps, shape.rope_theta, embed_scale)
+        L = len(weights.layers)
+        self._layers = (LayerWeights * L)()
+        for i, lw in enumerate(weights.layers):
+            self._layers[i] = LayerWeights(*(t.data_ptr() for t in (
+                lw.input_norm, lw.post_norm, lw.q_norm, lw.k_norm, lw.wq, lw.wk, lw.wv, lw.wo,
+                lw.wg, lw.wu, lw.wd)))
+        self.weights = DFlashWeights(weights.fc.data_ptr(), weights.hidden_norm.data_ptr(),
+                                     weights.final_norm.data_ptr(), self._layers,
+                                     weights.embed.data_ptr(), weights.lm_head.data_ptr())
+        self._w = weights
+        self.set_cache(cache)
+
+    def set_cache(self, cache):
+        L = len(cache.k)
+        self._k = (c_void_p * L)(*[t.data_ptr() for t in cache.k])
+        self._v = (c_void_p * L)(*[t.data_ptr() for t in cache.v])
+        self.cache_c = KvCache(self._k, self._v, cache.seq_len.data_ptr(), cache.cap,
+                               cache.seq_len.shape[0], L)
+        self._cache = cache
+
+    def workspace_bytes(self, B: int, block: int, n_new_max: int) -> int:
+        return int(lib().df_dflash_workspace_bytes(ctypes.byref(self.cfg), B, block, n_new_max))
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zeroed device workspace, 256-byte aligned (the caching allocator aligns to 512)."""
+    t = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    assert t.data_ptr() % 256 == 0
+    return t
+
+
+# ----------------------------------------------------------------------------- calls
+def dflash_block_forward(model: DFlashModel, block_ids, target_hidden_new, n_new, n_new_max: int,
+                         h_final, ws, d_status=None, stream=None):
+    B, block = block_ids.shape
+    _check(lib().dflash_block_forward(ctypes.byref(model.cfg), ctypes.byref(model.weights),
+                                      ctypes.byref(model.cache_c), _p(block_ids),
+                                      _p(target_hidden_new), _p(n_new), n_new_max, B, block,
+                                      _p(h_final), _p(ws), ws.numel(), _p(d_status),
+                                      _stream(stream)))
+
+
+def lm_head_workspace_bytes(rows: int, H: int, V: int) -> int:
+    return int(lib().df_lm_head_workspace_bytes(rows, H, V))
+
+
+def lm_head_argmax(W, X, idx, top1=None, top2=None, ws=None, stream=None):
+    rows, H = X.shape
+    V = W.shape[0]
+    _check(lib().lm_head_argmax(_p(W), _p(X), rows, H, V, _p(idx), _p(top1), _p(top2), _p(ws),
+                                ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def accept_prefix_argmax(drafts, drafts_ld: int, target, K: int, eos, committed, n_committed,
+                         accept_count, hit_eos, rollback, stream=None):
+    B = target.shape[0]
+    n_eos = 0 if eos is None else eos.numel()
+    _check(lib().accept_prefix_argmax(_p(drafts), drafts_ld, _p(target), B, K, _p(eos), n_eos,
+                                      _p(committed), _p(n_committed), _p(accept_count),
+                                      _p(hit_eos), _p(rollback), _stream(stream)))
+
+
+def accept_prefix_argmax_host(drafts: Sequence[int], target: Sequence[int], eos: Sequence[int]):
+    """Host walk of one sequence; returns (committed list, accept_count, hit_eos, rollback)."""
+    K = len(drafts)
+    D = (c_int32 * max(K, 1))(*drafts)
+    T = (c_int32 * (K + 1))(*target)
+    E = (c_int32 * max(len(eos), 1))(*eos)
+    C = (c_int32 * (K + 1))()
+    nc, ac, he, rb = c_int32(), c_int32(), c_int32(), c_int32()
+    _check(lib().accept_prefix_argmax_host(D, T, K, E if eos else None, len(eos), C,
+                                           ctypes.byref(nc), ctypes.byref(ac), ctypes.byref(he),
+                                           ctypes.byref(rb)))
+    return list(C[:nc.value]), ac.value, he.value, rb.value
+
+
+def kv_rollback(seq_len, n, d_status=None, stream=None):
+    _check(lib().kv_rollback(_p(seq_len), _p(n), seq_len.shape[0], _p(d_status), _stream(stream)))
+
+
+class RoundOutputs:
+    """Device outputs of one draft round for B sequences and K drafts."""
+
+    def __init__(self, B: int, K: int, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        self.argmax = torch.zeros((B, K + 1), **i32)
+        self.committed = torch.zeros((B, K + 1), **i32)
+        self.n_committed = torch.zeros(B, **i32)
+        self.accept = torch.zeros(B, **i32)
+        self.hit_eos = torch.zeros(B, **i32)
+        self.rollback = torch.zeros(B, **i32)
+
+
+def df_draft_round(model: DFlashModel, last_token, target_hidden_new, n_new, n_new_max: int, K: int,
+                   target_argmax, eos, target_seq_len, out: RoundOutputs, ws, d_status=None,
+                   stream=None):
+    B = last_token.shape[0]
+    n_eos = 0 if eos is None else eos.numel()
+    _check(lib().df_draft_round(ctypes.byref(model.cfg), ctypes.byref(model.weights),
+                                ctypes.byref(model.cache_c), _p(last_token), _p(target_hidden_new),
+                                _p(n_new), n_new_max, B, K, _p(target_argmax), _p(eos), n_eos,
+                                _p(target_seq_len), _p(out.argmax), _p(out.committed),
+                                _p(out.n_committed), _p(out.accept), _p(out.hit_eos),
+                                _p(out.rollback), _p(ws), ws.numel(), _p(d_status),
+                                _stream(stream)))
+
+
+def draft_round_host_workspace_bytes(model: DFlashModel, B: int, K: int, n_new_max: int,
+                                     n_eos: int) -> int:
+    return int(model.workspace_bytes(B, K + 1, n_new_max)
+               + lib().df_draft_round_host_workspace_bytes(ctypes.byref(model.cfg), B, K,
+                                                           n_new_max, n_eos))
+
+
+def df_draft_round_host(model: DFlashModel, last_token, target_hidden_new, n_new, n_new_max: int,
+                        K: int, target_argmax, eos, target_seq_len, host_out: dict, ws,
+                        stream=None):
+    """All tensor arguments are (pinned) HOST tensors; host_out holds host int32 tensors
+    argmax/committed [B, K+1], n_committed/accept/hit_eos/rollback [B], status [1]."""
+    B = last_token.shape[0]
+    n_eos = 0 if eos is None else eos.numel()
+    _check(lib().df_draft_round_host(
+        ctypes.byref(model.cfg), ctypes.byref(model.weights), ctypes.byref(model.cache_c),
+        _p(last_token), _p(target_hidden_new), _p(n_new), n_new_max, B, K, _p(target_argmax),
+        _p(eos), n_eos, _p(target_seq_len), _p(host_out["argmax"]), _p(host_out["committed"]),
+        _p(host_out["n_committed"]), _p(host_out["accept"]), _p(host_out["hit_eos"]),
+        _p(host_out["rollback"]), _p(host_out["status"]), _p(ws), ws.numel(), _stream(stream)))
+
+
+class MtpModel:
+    """C structs of an MTP block: config + weight pointers + the one-layer KV slot."""
+
+    def __init__(self, shape, w, cache):
+        self.shape = shape
+        self.cfg = MtpConfig(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
+                             shape.vocab, shape.intermediate, shape.n_experts, shape.top_k,
+                             shape.expert_inter, shape.shared_inter, shape.rotary_dim,
+                             shape.rms_eps, shape.rope_theta)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        self.weights = MtpWeights(*[ptr(getattr(w, n)) for n in (
+            "enorm", "hnorm", "eh_embed", "eh_hidden", "attn_norm", "post_norm", "q_norm",
+            "k_norm", "wq", "wk", "wv", "w_gate", "wo", "shared_head_norm", "embed", "lm_head",
+            "wg", "wu", "wd", "router", "exp_g", "exp_u", "exp_d", "sh_g", "sh_u", "sh_d",
+            "sh_gate")])
+        self._w = w
+        self._k = (c_void_p * 1)(cache.k[0].data_ptr())
+        self._v = (c_void_p * 1)(cache.v[0].data_ptr())
+        self.cache_c = KvCache(self._k, self._v, cache.seq_len.data_ptr(), cache.cap,
+                               cache.seq_len.shape[0], 1)
+        self._cache = cache
+
+    def workspace_bytes(self, B: int) -> int:
+        return int(lib().df_mtp_workspace_bytes(ctypes.byref(self.cfg), B))
+
+
+def mtp_forward_draft(model: MtpModel, prev_hidden, token, n_steps: int, hidden_out, argmax_out,
+                      ws, logits_out=None, d_status=None, stream=None):
+    B = token.shape[0]
+    _check(lib().mtp_forward_draft(ctypes.byref(model.cfg), ctypes.byref(model.weights),
+                                   ctypes.byref(model.cache_c), _p(prev_hidden), _p(token), B,
+                                   n_steps, _p(hidden_out), _p(argmax_out), _p(logits_out), _p(ws),
+                                   ws.numel(), _p(d_status), _stream(stream)))

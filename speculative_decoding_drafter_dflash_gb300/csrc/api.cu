@@ -1,0 +1,1013 @@
+// C ABI entry points: host-side validation, workspace carving and the launch sequence of a
+// draft round. Every arithmetic step runs in the kernels of the other translation units.
+//
+// The launch sequence follows hf2q 0.1.1 spec_decode/dflash/qwen35_orchestrator.rs
+// (per-round loop, steps 1-9) for DFlash and models/qwen35/mtp.rs
+// (`forward_draft_with_hidden`) for MTP.
+#include <algorithm>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "df_internal.cuh"
+
+namespace df {
+
+static thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_check(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DF_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return DF_OK;
+}
+
+namespace {
+
+constexpr int kArgmaxGridMax = 4 * kNumSMs;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQ(cond, code, ...)                         \
+    do {                                             \
+        if (!(cond)) return fail(code, __VA_ARGS__); \
+    } while (0)
+
+int check_bf16(const void *p, const char *name) {
+    REQ(p != nullptr, DF_EINVAL, "%s is NULL", name);
+    REQ(aligned16(p), DF_EINVAL, "%s is not 16-byte aligned", name);
+    return DF_OK;
+}
+
+int check_f32(const void *p, const char *name) {
+    REQ(p != nullptr, DF_EINVAL, "%s is NULL", name);
+    REQ((reinterpret_cast<uintptr_t>(p) & 3u) == 0, DF_EINVAL, "%s is not 4-byte aligned", name);
+    return DF_OK;
+}
+
+int check_cfg(const df_dflash_config *c) {
+    REQ(c, DF_EINVAL, "config is NULL");
+    REQ(c->hidden > 0 && c->hidden % 8 == 0, DF_ESHAPE, "hidden=%d must be a positive multiple of 8",
+        c->hidden);
+    REQ(c->n_layers > 0, DF_ESHAPE, "n_layers=%d", c->n_layers);
+    REQ(c->n_q_heads > 0 && c->n_kv_heads > 0 && c->n_q_heads % c->n_kv_heads == 0, DF_ESHAPE,
+        "n_q_heads=%d must be a positive multiple of n_kv_heads=%d", c->n_q_heads, c->n_kv_heads);
+    REQ(c->head_dim >= 32 && c->head_dim <= 256 && c->head_dim % 32 == 0, DF_ESHAPE,
+        "head_dim=%d must be a multiple of 32 in [32, 256]", c->head_dim);
+    int rot = c->rotary_dim ? c->rotary_dim : c->head_dim;
+    REQ(rot > 0 && rot <= c->head_dim && rot % 2 == 0, DF_ESHAPE, "rotary_dim=%d", c->rotary_dim);
+    REQ(c->intermediate > 0 && c->intermediate % 8 == 0, DF_ESHAPE, "intermediate=%d",
+        c->intermediate);
+    REQ(c->vocab > 1, DF_ESHAPE, "vocab=%d", c->vocab);
+    REQ(c->n_target_layers > 0, DF_ESHAPE, "n_target_layers=%d", c->n_target_layers);
+    REQ((long long)c->n_target_layers * c->hidden < (1LL << 30), DF_ESHAPE, "fc input too wide");
+    REQ(c->mask_token_id >= 0 && c->mask_token_id < c->vocab, DF_EINVAL,
+        "mask_token_id=%d outside [0, vocab)", c->mask_token_id);
+    REQ(c->causal_block == 0 || c->causal_block == 1, DF_EINVAL, "causal_block=%d", c->causal_block);
+    REQ(c->rms_eps >= 0.f && c->rope_theta > 0.f, DF_EINVAL, "rms_eps / rope_theta");
+    return DF_OK;
+}
+
+int check_weights(const df_dflash_config *c, const df_dflash_weights *w) {
+    REQ(w, DF_EINVAL, "weights is NULL");
+    DF_TRY(check_bf16(w->fc, "fc"));
+    DF_TRY(check_f32(w->hidden_norm, "hidden_norm"));
+    DF_TRY(check_f32(w->final_norm, "final_norm"));
+    DF_TRY(check_bf16(w->embed, "embed"));
+    DF_TRY(check_bf16(w->lm_head, "lm_head"));
+    REQ(w->layers, DF_EINVAL, "layers is NULL");
+    for (int l = 0; l < c->n_layers; ++l) {
+        const df_layer_weights &L = w->layers[l];
+        DF_TRY(check_f32(L.input_norm, "input_norm"));
+        DF_TRY(check_f32(L.post_attn_norm, "post_attn_norm"));
+        DF_TRY(check_f32(L.q_norm, "q_norm"));
+        DF_TRY(check_f32(L.k_norm, "k_norm"));
+        DF_TRY(check_bf16(L.wq, "wq"));
+        DF_TRY(check_bf16(L.wk, "wk"));
+        DF_TRY(check_bf16(L.wv, "wv"));
+        DF_TRY(check_bf16(L.wo, "wo"));
+        DF_TRY(check_bf16(L.w_gate, "w_gate"));
+        DF_TRY(check_bf16(L.w_up, "w_up"));
+        DF_TRY(check_bf16(L.w_down, "w_down"));
+    }
+    return DF_OK;
+}
+
+int check_cache(const df_kv_cache *k, int n_layers, int B, int d) {
+    REQ(k, DF_EINVAL, "cache is NULL");
+    REQ(k->n_layers == n_layers, DF_ESHAPE, "cache has %d layers, expected %d", k->n_layers,
+        n_layers);
+    REQ(k->batch == B, DF_ESHAPE, "cache batch %d != B %d", k->batch, B);
+    REQ(k->cap > 0, DF_ESHAPE, "cache cap=%d", k->cap);
+    REQ(k->k && k->v && k->seq_len, DF_EINVAL, "cache arrays are NULL");
+    for (int l = 0; l < n_layers; ++l) {
+        REQ(k->k[l] && k->v[l], DF_EINVAL, "cache layer %d is NULL", l);
+        REQ(aligned16(k->k[l]) && aligned16(k->v[l]), DF_EINVAL, "cache layer %d misaligned", l);
+    }
+    (void)d;
+    return DF_OK;
+}
+
+// ---------------------------------------------------------------- DFlash workspace
+struct DFlashWs {
+    float *h, *hctx, *qkv, *q, *kb, *vb, *cos_t, *sin_t, *part_o, *part_ml, *h_final;
+    uint16_t *xp_ctx, *xp_qkv, *xp_o, *xp_ffn, *xp_act, *xp_head;
+    ArgTop *amax_part;
+    int32_t *idx;
+    AttnArgs plan;
+};
+
+void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int blk, int n_new_max,
+                  int cap, bool round) {
+    const int H = c->hidden, d = c->head_dim, nq = c->n_q_heads, nkv = c->n_kv_heads;
+    const int rot = c->rotary_dim ? c->rotary_dim : d;
+    const size_t T_blk = (size_t)B * blk, T_ctx = (size_t)B * n_new_max, T_all = T_blk + T_ctx;
+    const size_t fc_in = (size_t)c->n_target_layers * H, qt = (size_t)nq * d, kt = (size_t)nkv * d;
+    w.h = cv.take<float>(T_blk * H);
+    w.hctx = cv.take<float>(std::max<size_t>(T_ctx, 1) * H);
+    w.qkv = cv.take<float>(T_all * (qt + 2 * kt));
+    w.q = cv.take<float>(T_blk * qt);
+    w.kb = cv.take<float>(T_blk * kt);
+    w.vb = cv.take<float>(T_blk * kt);
+    w.cos_t = cv.take<float>((size_t)B * (blk + n_new_max) * (rot / 2));
+    w.sin_t = cv.take<float>((size_t)B * (blk + n_new_max) * (rot / 2));
+    w.plan = AttnArgs{};
+    w.plan.B = B;
+    w.plan.blk = blk;
+    w.plan.nq = nq;
+    w.plan.nkv = nkv;
+    w.plan.d = d;
+    attn_plan(w.plan, cap + blk);
+    size_t pf = attn_part_floats(B, nkv, w.plan.n_groups, w.plan.n_chunks, w.plan.rows_per_group, d);
+    w.part_o = cv.take<float>(pf);
+    w.part_ml = cv.take<float>(pf / (d + 2) * 2);
+    w.xp_ctx = cv.take<uint16_t>(2 * std::max<size_t>(T_ctx, 1) * fc_in);
+    w.xp_qkv = cv.take<uint16_t>(2 * T_all * H);
+    w.xp_o = cv.take<uint16_t>(2 * T_blk * qt);
+    w.xp_ffn = cv.take<uint16_t>(2 * T_blk * H);
+    w.xp_act = cv.take<uint16_t>(2 * T_blk * c->intermediate);
+    if (round) {
+        w.h_final = cv.take<float>(T_blk * H);
+        w.xp_head = cv.take<uint16_t>(2 * T_blk * H);
+        w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * T_blk);
+    } else {
+        w.h_final = nullptr;
+        w.xp_head = nullptr;
+        w.amax_part = nullptr;
+    }
+}
+
+int get_ws(void *ws, size_t ws_bytes, size_t need) {
+    REQ(ws != nullptr, DF_EWORKSPACE, "workspace is NULL (need %zu bytes)", need);
+    REQ((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, DF_EWORKSPACE,
+        "workspace is not 256-byte aligned");
+    REQ(ws_bytes >= need, DF_EWORKSPACE, "workspace of %zu bytes is smaller than %zu", ws_bytes,
+        need);
+    return DF_OK;
+}
+
+// The drafter forward. Either block_ids or (last_token, mask id) provides the block tokens.
+int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
+                        const df_kv_cache *cache, const int32_t *block_ids,
+                        const int32_t *last_token, const float *target_hidden,
+                        const int32_t *n_new, int n_new_max, int B, int blk, float *h_final,
+                        uint16_t *final_pack, DFlashWs &ws, int32_t *st, cudaStream_t s) {
+    const int H = c->hidden, d = c->head_dim, nq = c->n_q_heads, nkv = c->n_kv_heads;
+    const int rot = c->rotary_dim ? c->rotary_dim : d;
+    const int I = c->intermediate;
+    const int T_blk = B * blk, T_ctx = B * n_new_max, T_all = T_blk + T_ctx;
+    const int fc_in = c->n_target_layers * H, qt = nq * d, kt = nkv * d, Nqkv = qt + 2 * kt;
+
+    DF_TRY(launch_rope_table(ws.cos_t, ws.sin_t, cache->seq_len, n_new, n_new_max, B, blk, 0, rot,
+                             c->rope_theta, st, s));
+    if (T_ctx > 0) {
+        // Context stream: h_ctx = rmsnorm(X_new fc^T) * hidden_norm, packed after the block rows.
+        PackArgs p;
+        p.src = target_hidden;
+        p.lds = fc_in;
+        p.pack = ws.xp_ctx;
+        p.ldp = fc_in;
+        p.T = T_ctx;
+        p.K = fc_in;
+        p.nvalid = n_new;
+        p.rows_per_seq = n_new_max;
+        p.status = st;
+        DF_TRY(launch_pack(p, s));
+        GemmArgs g;
+        g.W0 = W->fc;
+        g.n0 = H;
+        g.N = H;
+        g.K = fc_in;
+        g.X = ws.xp_ctx;
+        g.ldx = fc_in;
+        g.T = T_ctx;
+        g.epi = EPI_STORE;
+        g.out = ws.hctx;
+        g.ldo = H;
+        DF_TRY(launch_gemm(g, s));
+        PackArgs q;
+        q.src = ws.hctx;
+        q.lds = H;
+        q.norm_w = W->hidden_norm;
+        q.eps = c->rms_eps;
+        q.pack = ws.xp_qkv + (size_t)2 * T_blk * H;
+        q.ldp = H;
+        q.T = T_ctx;
+        q.K = H;
+        q.nvalid = n_new;
+        q.rows_per_seq = n_new_max;
+        q.status = st;
+        DF_TRY(launch_pack(q, s));
+    }
+    for (int l = 0; l < c->n_layers; ++l) {
+        const df_layer_weights &L = W->layers[l];
+        PackArgs p;
+        if (l == 0) {
+            p.gather = W->embed;
+            p.ids = block_ids;
+            p.last_token = last_token;
+            p.mask_id = c->mask_token_id;
+            p.vocab = c->vocab;
+            p.scale = c->embed_scale;
+            p.h_out = ws.h;
+            p.ldh = H;
+            p.rows_per_seq = blk;
+        } else {
+            p.src = ws.h;
+            p.lds = H;
+        }
+        p.norm_w = L.input_norm;
+        p.eps = c->rms_eps;
+        p.pack = ws.xp_qkv;
+        p.ldp = H;
+        p.T = T_blk;
+        p.K = H;
+        p.status = st;
+        DF_TRY(launch_pack(p, s));
+
+        GemmArgs g;
+        g.W0 = L.wq;
+        g.n0 = qt;
+        g.W1 = L.wk;
+        g.n1 = kt;
+        g.W2 = L.wv;
+        g.n2 = kt;
+        g.N = Nqkv;
+        g.K = H;
+        g.X = ws.xp_qkv;
+        g.ldx = H;
+        g.T = T_all;
+        g.epi = EPI_STORE;
+        g.out = ws.qkv;
+        g.ldo = Nqkv;
+        DF_TRY(launch_gemm(g, s));
+
+        QkArgs qa;
+        qa.qkv = ws.qkv;
+        qa.ldq = Nqkv;
+        qa.B = B;
+        qa.blk = blk;
+        qa.n_new_max = n_new_max;
+        qa.nq = nq;
+        qa.nkv = nkv;
+        qa.d = d;
+        qa.rot = rot;
+        qa.q_norm = L.q_norm;
+        qa.k_norm = L.k_norm;
+        qa.eps = c->rms_eps;
+        qa.cos_t = ws.cos_t;
+        qa.sin_t = ws.sin_t;
+        qa.q_out = ws.q;
+        qa.kb = ws.kb;
+        qa.vb = ws.vb;
+        qa.cache_k = cache->k[l];
+        qa.cache_v = cache->v[l];
+        qa.cap = cache->cap;
+        qa.seq_len = cache->seq_len;
+        qa.n_new = n_new;
+        qa.append_block = 0;
+        qa.pos_off = 0;
+        qa.status = st;
+        DF_TRY(launch_qk_rope(qa, s));
+
+        AttnArgs at = ws.plan;
+        at.q = ws.q;
+        at.cache_k = cache->k[l];
+        at.cache_v = cache->v[l];
+        at.cap = cache->cap;
+        at.kb = ws.kb;
+        at.vb = ws.vb;
+        at.seq_len = cache->seq_len;
+        at.n_new = n_new;
+        at.n_new_max = n_new_max;
+        at.extra_rows = 0;
+        at.causal_block = c->causal_block;
+        at.part_o = ws.part_o;
+        at.part_ml = ws.part_ml;
+        at.gate = nullptr;
+        at.ldg = 0;
+        at.pack = ws.xp_o;
+        at.status = st;
+        DF_TRY(launch_attn(at, s));
+
+        GemmArgs go;
+        go.W0 = L.wo;
+        go.n0 = H;
+        go.N = H;
+        go.K = qt;
+        go.X = ws.xp_o;
+        go.ldx = qt;
+        go.T = T_blk;
+        go.epi = EPI_RESID;
+        go.out = ws.h;
+        go.ldo = H;
+        go.resid = ws.h;
+        go.ldr = H;
+        DF_TRY(launch_gemm(go, s));
+
+        PackArgs pf;
+        pf.src = ws.h;
+        pf.lds = H;
+        pf.norm_w = L.post_attn_norm;
+        pf.eps = c->rms_eps;
+        pf.pack = ws.xp_ffn;
+        pf.ldp = H;
+        pf.T = T_blk;
+        pf.K = H;
+        pf.status = st;
+        DF_TRY(launch_pack(pf, s));
+
+        GemmArgs gu;
+        gu.W0 = L.w_gate;
+        gu.n0 = I;
+        gu.W1 = L.w_up;
+        gu.n1 = I;
+        gu.N = I;
+        gu.K = H;
+        gu.X = ws.xp_ffn;
+        gu.ldx = H;
+        gu.T = T_blk;
+        gu.epi = EPI_SWIGLU;
+        gu.pack_out = ws.xp_act;
+        gu.ldpo = I;
+        DF_TRY(launch_gemm(gu, s));
+
+        GemmArgs gd;
+        gd.W0 = L.w_down;
+        gd.n0 = H;
+        gd.N = H;
+        gd.K = I;
+        gd.X = ws.xp_act;
+        gd.ldx = I;
+        gd.T = T_blk;
+        gd.epi = EPI_RESID;
+        gd.out = ws.h;
+        gd.ldo = H;
+        gd.resid = ws.h;
+        gd.ldr = H;
+        DF_TRY(launch_gemm(gd, s));
+    }
+    PackArgs pfin;
+    pfin.src = ws.h;
+    pfin.lds = H;
+    pfin.norm_w = W->final_norm;
+    pfin.eps = c->rms_eps;
+    pfin.y_out = h_final;
+    pfin.ldy = H;
+    pfin.pack = final_pack;
+    pfin.ldp = H;
+    pfin.T = T_blk;
+    pfin.K = H;
+    pfin.status = st;
+    DF_TRY(launch_pack(pfin, s));
+    return launch_seq_advance(cache->seq_len, n_new, B, 0, cache->cap, st, s);
+}
+
+int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
+                 int32_t *idx, float *top1, float *top2, cudaStream_t s) {
+    GemmArgs g;
+    g.W0 = Wlm;
+    g.n0 = V;
+    g.N = V;
+    g.K = H;
+    g.X = xp;
+    g.ldx = H;
+    g.T = rows;
+    g.epi = EPI_ARGMAX;
+    g.part = part;
+    int G = 0;
+    DF_TRY(launch_gemm(g, s, &G));
+    return launch_argmax_final(part, G, rows, idx, top1, top2, nullptr, 1, 0, s);
+}
+
+}  // namespace
+}  // namespace df
+
+using namespace df;
+
+extern "C" {
+
+const char *df_last_error(void) { return g_err; }
+
+int df_version(void) { return 100; }
+
+size_t df_dflash_workspace_bytes(const df_dflash_config *cfg, int B, int block, int n_new_max) {
+    if (check_cfg(cfg) != DF_OK || B <= 0 || block < 2 || n_new_max < 0) return 0;
+    // The attention partials depend on the cache capacity; size for the largest plan.
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    DFlashWs w;
+    carve_dflash(cv, w, cfg, B, block, n_new_max, 1 << 20, true);
+    return cv.off;
+}
+
+int dflash_block_forward(const df_dflash_config *cfg, const df_dflash_weights *w,
+                         const df_kv_cache *cache, const int32_t *block_ids,
+                         const float *target_hidden_new, const int32_t *n_new, int n_new_max,
+                         int B, int block, float *h_final, void *ws, size_t ws_bytes,
+                         int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_cfg(cfg));
+    DF_TRY(check_weights(cfg, w));
+    REQ(B > 0 && block >= 2, DF_ESHAPE, "B=%d, block=%d (block must be >= 2)", B, block);
+    REQ(n_new_max >= 0, DF_ESHAPE, "n_new_max=%d", n_new_max);
+    DF_TRY(check_cache(cache, cfg->n_layers, B, cfg->head_dim));
+    REQ(block_ids && h_final, DF_EINVAL, "block_ids / h_final is NULL");
+    REQ(n_new_max == 0 || (target_hidden_new && n_new), DF_EINVAL,
+        "target_hidden_new / n_new is NULL");
+    REQ(n_new_max <= cache->cap, DF_ECAPACITY, "n_new_max=%d exceeds cap=%d", n_new_max, cache->cap);
+    size_t need = df_dflash_workspace_bytes(cfg, B, block, n_new_max);
+    DF_TRY(get_ws(ws, ws_bytes, need));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    DFlashWs W;
+    carve_dflash(cv, W, cfg, B, block, n_new_max, cache->cap, false);
+    return dflash_forward_impl(cfg, w, cache, block_ids, nullptr, target_hidden_new, n_new,
+                               n_new_max, B, block, h_final, nullptr, W, d_status,
+                               (cudaStream_t)stream);
+}
+
+size_t df_lm_head_workspace_bytes(int rows, int H, int V) {
+    if (rows <= 0 || H <= 0 || V <= 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    cv.take<uint16_t>((size_t)2 * rows * H);
+    cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    return cv.off;
+}
+
+int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
+                   float *top1, float *top2, void *ws, size_t ws_bytes, df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(rows > 0 && H > 0 && H % 8 == 0 && V > 0, DF_ESHAPE, "rows=%d H=%d V=%d (H %% 8 == 0)",
+        rows, H, V);
+    DF_TRY(check_bf16(W, "W"));
+    DF_TRY(check_f32(X, "X"));
+    REQ(idx, DF_EINVAL, "idx is NULL");
+    DF_TRY(get_ws(ws, ws_bytes, df_lm_head_workspace_bytes(rows, H, V)));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    uint16_t *xp = cv.take<uint16_t>((size_t)2 * rows * H);
+    ArgTop *part = cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    cudaStream_t s = (cudaStream_t)stream;
+    PackArgs p;
+    p.src = X;
+    p.lds = H;
+    p.pack = xp;
+    p.ldp = H;
+    p.T = rows;
+    p.K = H;
+    DF_TRY(launch_pack(p, s));
+    return lm_head_impl(W, xp, rows, H, V, part, idx, top1, top2, s);
+}
+
+int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
+                         int K, const int32_t *eos, int n_eos, int32_t *committed,
+                         int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                         int32_t *rollback, df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(B > 0 && K >= 1, DF_ESHAPE, "B=%d K=%d (K >= 1)", B, K);
+    REQ(drafts_ld >= K, DF_ESHAPE, "drafts_ld=%d < K=%d", drafts_ld, K);
+    REQ(n_eos >= 0 && (n_eos == 0 || eos), DF_EINVAL, "eos list");
+    REQ(drafts && target && committed && n_committed && accept_count && hit_eos && rollback,
+        DF_EINVAL, "NULL output or input");
+    return launch_accept(drafts, drafts_ld, target, B, K, eos, n_eos, committed, n_committed,
+                         accept_count, hit_eos, rollback, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+int accept_prefix_argmax_host(const int32_t *drafts, const int32_t *target, int K,
+                              const int32_t *eos, int n_eos, int32_t *committed,
+                              int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                              int32_t *rollback) {
+    g_err[0] = 0;
+    REQ(K >= 1, DF_ESHAPE, "K=%d (K >= 1)", K);
+    REQ(n_eos >= 0 && (n_eos == 0 || eos), DF_EINVAL, "eos list");
+    REQ(drafts && target && committed && n_committed && accept_count && hit_eos && rollback,
+        DF_EINVAL, "NULL output or input");
+    int a = 0;
+    while (a < K && drafts[a] == target[a]) ++a;
+    int n = 0, hit = 0;
+    for (int i = 0; i <= a; ++i) {
+        int tok = i < a ? drafts[i] : target[a];
+        committed[n++] = tok;
+        bool is_eos = false;
+        for (int e = 0; e < n_eos; ++e) is_eos |= (tok == eos[e]);
+        if (is_eos) {
+            hit = 1;
+            break;
+        }
+    }
+    for (int i = n; i <= K; ++i) committed[i] = -1;
+    *n_committed = n;
+    *accept_count = a;
+    *hit_eos = hit;
+    *rollback = K - a;
+    return DF_OK;
+}
+
+int kv_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(B > 0, DF_ESHAPE, "B=%d", B);
+    REQ(seq_len && n, DF_EINVAL, "seq_len / n is NULL");
+    return launch_rollback(seq_len, n, B, d_status, (cudaStream_t)stream);
+}
+
+int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
+                   const df_kv_cache *cache, const int32_t *last_token,
+                   const float *target_hidden_new, const int32_t *n_new, int n_new_max, int B,
+                   int K, const int32_t *target_argmax, const int32_t *eos, int n_eos,
+                   int32_t *target_seq_len, int32_t *argmax_out, int32_t *committed,
+                   int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                   int32_t *rollback, void *ws, size_t ws_bytes, int32_t *d_status,
+                   df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_cfg(cfg));
+    DF_TRY(check_weights(cfg, w));
+    REQ(B > 0 && K >= 1, DF_ESHAPE, "B=%d K=%d (K >= 1)", B, K);
+    const int blk = K + 1;
+    REQ(n_new_max >= 0 && n_new_max <= (cache ? cache->cap : 0), DF_ESHAPE, "n_new_max=%d",
+        n_new_max);
+    DF_TRY(check_cache(cache, cfg->n_layers, B, cfg->head_dim));
+    REQ(last_token && target_argmax && target_seq_len && argmax_out && committed && n_committed &&
+            accept_count && hit_eos && rollback,
+        DF_EINVAL, "NULL round input or output");
+    REQ(n_new_max == 0 || (target_hidden_new && n_new), DF_EINVAL,
+        "target_hidden_new / n_new is NULL");
+    REQ(n_eos >= 0 && (n_eos == 0 || eos), DF_EINVAL, "eos list");
+    size_t need = df_dflash_workspace_bytes(cfg, B, blk, n_new_max);
+    DF_TRY(get_ws(ws, ws_bytes, need));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    DFlashWs W;
+    carve_dflash(cv, W, cfg, B, blk, n_new_max, cache->cap, true);
+    cudaStream_t s = (cudaStream_t)stream;
+    DF_TRY(dflash_forward_impl(cfg, w, cache, nullptr, last_token, target_hidden_new, n_new,
+                               n_new_max, B, blk, W.h_final, W.xp_head, W, d_status, s));
+    DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
+                        argmax_out, nullptr, nullptr, s));
+    return launch_accept(argmax_out + 1, blk, target_argmax, B, K, eos, n_eos, committed,
+                         n_committed, accept_count, hit_eos, rollback, target_seq_len, d_status, s);
+}
+
+size_t df_draft_round_host_workspace_bytes(const df_dflash_config *cfg, int B, int K,
+                                           int n_new_max, int n_eos) {
+    if (check_cfg(cfg) != DF_OK || B <= 0 || K < 1 || n_new_max < 0 || n_eos < 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    const size_t fc_in = (size_t)cfg->n_target_layers * cfg->hidden;
+    cv.take<float>((size_t)B * std::max(n_new_max, 1) * fc_in);   // target hidden rows
+    cv.take<int32_t>((size_t)B * 9 * (K + 2) + n_eos + 8);         // ints in and out
+    return cv.off;
+}
+
+int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
+                        const df_kv_cache *cache, const int32_t *last_token,
+                        const float *target_hidden_new, const int32_t *n_new, int n_new_max,
+                        int B, int K, const int32_t *target_argmax, const int32_t *eos,
+                        int n_eos, int32_t *target_seq_len, int32_t *argmax_out,
+                        int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                        int32_t *hit_eos, int32_t *rollback, int32_t *status, void *ws,
+                        size_t ws_bytes, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_cfg(cfg));
+    REQ(B > 0 && K >= 1 && n_new_max >= 0 && n_eos >= 0, DF_ESHAPE, "B=%d K=%d n_new_max=%d", B,
+        K, n_new_max);
+    REQ(last_token && target_argmax && target_seq_len && argmax_out && committed && n_committed &&
+            accept_count && hit_eos && rollback && status,
+        DF_EINVAL, "NULL host buffer");
+    REQ(n_new_max == 0 || (target_hidden_new && n_new), DF_EINVAL, "target_hidden_new / n_new");
+    const int blk = K + 1;
+    size_t need_round = df_dflash_workspace_bytes(cfg, B, blk, n_new_max);
+    size_t need_stage = df_draft_round_host_workspace_bytes(cfg, B, K, n_new_max, n_eos);
+    DF_TRY(get_ws(ws, ws_bytes, need_round + need_stage));
+    char *stage = static_cast<char *>(ws) + need_round;
+    Carve cv{stage, 0, need_stage, true};
+    const size_t fc_in = (size_t)cfg->n_target_layers * cfg->hidden;
+    float *d_th = cv.take<float>((size_t)B * std::max(n_new_max, 1) * fc_in);
+    int32_t *ip = cv.take<int32_t>((size_t)B * 9 * (K + 2) + n_eos + 8);
+    int32_t *d_last = ip;
+    int32_t *d_nnew = d_last + B;
+    int32_t *d_tgt = d_nnew + B;
+    int32_t *d_tsl = d_tgt + (size_t)B * blk;
+    int32_t *d_am = d_tsl + B;
+    int32_t *d_com = d_am + (size_t)B * blk;
+    int32_t *d_nc = d_com + (size_t)B * blk;
+    int32_t *d_ac = d_nc + B;
+    int32_t *d_he = d_ac + B;
+    int32_t *d_rb = d_he + B;
+    int32_t *d_eos = d_rb + B;
+    int32_t *d_st = d_eos + n_eos;
+    cudaStream_t s = (cudaStream_t)stream;
+    auto h2d = [&](void *dst, const void *src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) : cudaSuccess;
+    };
+    auto d2h = [&](void *dst, const void *src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s) : cudaSuccess;
+    };
+    cudaError_t e = cudaSuccess;
+    e = e ? e : h2d(d_last, last_token, sizeof(int32_t) * B);
+    if (n_new_max > 0) {
+        e = e ? e : h2d(d_th, target_hidden_new, sizeof(float) * B * n_new_max * fc_in);
+        e = e ? e : h2d(d_nnew, n_new, sizeof(int32_t) * B);
+    }
+    e = e ? e : h2d(d_tgt, target_argmax, sizeof(int32_t) * B * blk);
+    e = e ? e : h2d(d_tsl, target_seq_len, sizeof(int32_t) * B);
+    e = e ? e : h2d(d_eos, eos, sizeof(int32_t) * n_eos);
+    e = e ? e : cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return fail(DF_ECUDA, "host round staging: %s", cudaGetErrorString(e));
+    DF_TRY(df_draft_round(cfg, w, cache, d_last, n_new_max ? d_th : nullptr,
+                          n_new_max ? d_nnew : nullptr, n_new_max, B, K, d_tgt, d_eos, n_eos,
+                          d_tsl, d_am, d_com, d_nc, d_ac, d_he, d_rb, ws, need_round, d_st,
+                          stream));
+    e = d2h(target_seq_len, d_tsl, sizeof(int32_t) * B);
+    e = e ? e : d2h(argmax_out, d_am, sizeof(int32_t) * B * blk);
+    e = e ? e : d2h(committed, d_com, sizeof(int32_t) * B * blk);
+    e = e ? e : d2h(n_committed, d_nc, sizeof(int32_t) * B);
+    e = e ? e : d2h(accept_count, d_ac, sizeof(int32_t) * B);
+    e = e ? e : d2h(hit_eos, d_he, sizeof(int32_t) * B);
+    e = e ? e : d2h(rollback, d_rb, sizeof(int32_t) * B);
+    e = e ? e : d2h(status, d_st, sizeof(int32_t));
+    e = e ? e : cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(DF_ECUDA, "host round readback: %s", cudaGetErrorString(e));
+    return DF_OK;
+}
+
+}  // extern "C"
+
+// ================================================================ MTP draft step
+namespace df {
+namespace {
+
+int check_mtp_cfg(const df_mtp_config *c) {
+    REQ(c, DF_EINVAL, "MTP config is NULL");
+    REQ(c->hidden > 0 && c->hidden % 8 == 0, DF_ESHAPE, "hidden=%d", c->hidden);
+    REQ(c->n_q_heads > 0 && c->n_kv_heads > 0 && c->n_q_heads % c->n_kv_heads == 0, DF_ESHAPE,
+        "heads %d / %d", c->n_q_heads, c->n_kv_heads);
+    REQ(c->head_dim >= 32 && c->head_dim <= 256 && c->head_dim % 32 == 0, DF_ESHAPE,
+        "head_dim=%d", c->head_dim);
+    int rot = c->rotary_dim ? c->rotary_dim : c->head_dim;
+    REQ(rot > 0 && rot <= c->head_dim && rot % 2 == 0, DF_ESHAPE, "rotary_dim=%d", c->rotary_dim);
+    REQ(c->vocab > 1, DF_ESHAPE, "vocab=%d", c->vocab);
+    if (c->n_experts == 0) {
+        REQ(c->intermediate > 0 && c->intermediate % 8 == 0, DF_ESHAPE, "intermediate=%d",
+            c->intermediate);
+    } else {
+        REQ(c->n_experts > 0 && c->top_k >= 1 && c->top_k <= c->n_experts && c->top_k <= 16,
+            DF_ESHAPE, "n_experts=%d top_k=%d (top_k <= 16)", c->n_experts, c->top_k);
+        REQ(c->expert_inter > 0 && c->expert_inter % 8 == 0 && c->shared_inter > 0 &&
+                c->shared_inter % 8 == 0,
+            DF_ESHAPE, "expert_inter=%d shared_inter=%d", c->expert_inter, c->shared_inter);
+    }
+    REQ(c->rms_eps >= 0.f && c->rope_theta > 0.f, DF_EINVAL, "rms_eps / rope_theta");
+    return DF_OK;
+}
+
+int check_mtp_weights(const df_mtp_config *c, const df_mtp_weights *w) {
+    REQ(w, DF_EINVAL, "MTP weights is NULL");
+    DF_TRY(check_f32(w->enorm, "enorm"));
+    DF_TRY(check_f32(w->hnorm, "hnorm"));
+    DF_TRY(check_bf16(w->eh_embed, "eh_embed"));
+    DF_TRY(check_bf16(w->eh_hidden, "eh_hidden"));
+    DF_TRY(check_f32(w->attn_norm, "attn_norm"));
+    DF_TRY(check_f32(w->post_attn_norm, "post_attn_norm"));
+    DF_TRY(check_f32(w->q_norm, "q_norm"));
+    DF_TRY(check_f32(w->k_norm, "k_norm"));
+    DF_TRY(check_bf16(w->wq, "wq"));
+    DF_TRY(check_bf16(w->wk, "wk"));
+    DF_TRY(check_bf16(w->wv, "wv"));
+    if (w->w_gate) DF_TRY(check_bf16(w->w_gate, "w_gate"));
+    DF_TRY(check_bf16(w->wo, "wo"));
+    DF_TRY(check_f32(w->shared_head_norm, "shared_head_norm"));
+    DF_TRY(check_bf16(w->embed, "embed"));
+    DF_TRY(check_bf16(w->lm_head, "lm_head"));
+    if (c->n_experts == 0) {
+        DF_TRY(check_bf16(w->w_gate_mlp, "w_gate_mlp"));
+        DF_TRY(check_bf16(w->w_up, "w_up"));
+        DF_TRY(check_bf16(w->w_down, "w_down"));
+    } else {
+        DF_TRY(check_bf16(w->router, "router"));
+        DF_TRY(check_bf16(w->exp_gate, "exp_gate"));
+        DF_TRY(check_bf16(w->exp_up, "exp_up"));
+        DF_TRY(check_bf16(w->exp_down, "exp_down"));
+        DF_TRY(check_bf16(w->sh_gate_mlp, "sh_gate_mlp"));
+        DF_TRY(check_bf16(w->sh_up, "sh_up"));
+        DF_TRY(check_bf16(w->sh_down, "sh_down"));
+        DF_TRY(check_bf16(w->sh_expert_gate, "sh_expert_gate"));
+    }
+    return DF_OK;
+}
+
+struct MtpWs {
+    float *x, *qkv, *gate, *q, *h1, *cos_t, *sin_t, *part_o, *part_ml, *moe_out, *router_logits;
+    uint16_t *xp_eh, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
+    ArgTop *amax_part;
+    int32_t *moe_sel;
+    float *moe_w;
+    AttnArgs plan;
+};
+
+void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
+    const int H = c->hidden, d = c->head_dim, nq = c->n_q_heads, nkv = c->n_kv_heads;
+    const int rot = c->rotary_dim ? c->rotary_dim : d;
+    const size_t qt = (size_t)nq * d, kt = (size_t)nkv * d;
+    const size_t I = c->n_experts ? (size_t)std::max(c->expert_inter * c->top_k, c->shared_inter)
+                                  : (size_t)c->intermediate;
+    w.x = cv.take<float>((size_t)B * H);
+    w.qkv = cv.take<float>((size_t)B * (qt + 2 * kt));
+    w.gate = cv.take<float>((size_t)B * qt);
+    w.q = cv.take<float>((size_t)B * qt);
+    w.h1 = cv.take<float>((size_t)B * H);
+    w.cos_t = cv.take<float>((size_t)B * (rot / 2));
+    w.sin_t = cv.take<float>((size_t)B * (rot / 2));
+    w.plan = AttnArgs{};
+    w.plan.B = B;
+    w.plan.blk = 1;
+    w.plan.nq = nq;
+    w.plan.nkv = nkv;
+    w.plan.d = d;
+    attn_plan(w.plan, cap);
+    size_t pf = attn_part_floats(B, nkv, w.plan.n_groups, w.plan.n_chunks, w.plan.rows_per_group, d);
+    w.part_o = cv.take<float>(pf);
+    w.part_ml = cv.take<float>(pf / (d + 2) * 2);
+    w.moe_out = cv.take<float>((size_t)B * H);
+    w.router_logits = cv.take<float>((size_t)B * std::max(c->n_experts, 1));
+    w.xp_eh = cv.take<uint16_t>((size_t)2 * B * 2 * H);
+    w.xp_attn = cv.take<uint16_t>((size_t)2 * B * H);
+    w.xp_o = cv.take<uint16_t>((size_t)2 * B * qt);
+    w.xp_ffn = cv.take<uint16_t>((size_t)2 * B * H);
+    w.xp_act = cv.take<uint16_t>((size_t)2 * B * I);
+    w.xp_sh = cv.take<uint16_t>((size_t)2 * B * std::max(c->shared_inter, 1));
+    w.xp_head = cv.take<uint16_t>((size_t)2 * B * H);
+    w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * B);
+    w.moe_sel = cv.take<int32_t>((size_t)B * std::max(c->top_k, 1));
+    w.moe_w = cv.take<float>((size_t)B * std::max(c->top_k, 1));
+}
+
+}  // namespace
+}  // namespace df
+
+extern "C" {
+
+size_t df_mtp_workspace_bytes(const df_mtp_config *cfg, int B) {
+    if (check_mtp_cfg(cfg) != DF_OK || B <= 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    MtpWs w;
+    carve_mtp(cv, w, cfg, B, 1 << 20);
+    return cv.off;
+}
+
+int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
+                      const df_kv_cache *cache, const float *prev_hidden, const int32_t *token,
+                      int B, int n_steps, float *hidden_out, int32_t *argmax_out,
+                      float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
+                      df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_mtp_cfg(cfg));
+    DF_TRY(check_mtp_weights(cfg, w));
+    REQ(B > 0 && n_steps >= 1, DF_ESHAPE, "B=%d n_steps=%d", B, n_steps);
+    DF_TRY(check_cache(cache, 1, B, cfg->head_dim));
+    REQ(prev_hidden && token && hidden_out && argmax_out, DF_EINVAL, "NULL MTP input or output");
+    REQ(cfg->n_experts == 0, DF_EINVAL, "MoE MTP FFN is not available in this build");
+    DF_TRY(get_ws(ws, ws_bytes, df_mtp_workspace_bytes(cfg, B)));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    MtpWs W;
+    carve_mtp(cv, W, cfg, B, cache->cap);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int H = cfg->hidden, d = cfg->head_dim, nq = cfg->n_q_heads, nkv = cfg->n_kv_heads;
+    const int rot = cfg->rotary_dim ? cfg->rotary_dim : d;
+    const int qt = nq * d, kt = nkv * d, Nqkv = qt + 2 * kt, I = cfg->intermediate;
+
+    for (int st = 0; st < n_steps; ++st) {
+        const float *hprev = st == 0 ? prev_hidden : hidden_out + (size_t)(st - 1) * B * H;
+        const int32_t *tok = st == 0 ? token : argmax_out + (size_t)(st - 1) * B;
+        float *hid = hidden_out + (size_t)st * B * H;
+        // x = eh_embed . enorm(embed[tok]) + eh_hidden . hnorm(prev): one projection over the
+        // concatenation [enorm(e); hnorm(h)] (mtp.rs `project_embedding_and_hidden`).
+        PackArgs pe;
+        pe.gather = w->embed;
+        pe.ids = tok;
+        pe.vocab = cfg->vocab;
+        pe.rows_per_seq = 1;
+        pe.norm_w = w->enorm;
+        pe.eps = 1e-6f;
+        pe.pack = W.xp_eh;
+        pe.ldp = 2 * H;
+        pe.T = B;
+        pe.K = H;
+        pe.status = d_status;
+        DF_TRY(launch_pack(pe, s));
+        PackArgs ph;
+        ph.src = hprev;
+        ph.lds = H;
+        ph.norm_w = w->hnorm;
+        ph.eps = 1e-6f;
+        ph.pack = W.xp_eh + H;
+        ph.ldp = 2 * H;
+        ph.T = B;
+        ph.K = H;
+        DF_TRY(launch_pack(ph, s));
+        GemmArgs ge;
+        ge.W0 = w->eh_embed;
+        ge.n0 = H;
+        ge.Wk2 = w->eh_hidden;
+        ge.K1 = H;
+        ge.N = H;
+        ge.K = 2 * H;
+        ge.X = W.xp_eh;
+        ge.ldx = 2 * H;
+        ge.T = B;
+        ge.epi = EPI_STORE;
+        ge.out = W.x;
+        ge.ldo = H;
+        DF_TRY(launch_gemm(ge, s));
+
+        PackArgs pa;
+        pa.src = W.x;
+        pa.lds = H;
+        pa.norm_w = w->attn_norm;
+        pa.eps = cfg->rms_eps;
+        pa.pack = W.xp_attn;
+        pa.ldp = H;
+        pa.T = B;
+        pa.K = H;
+        DF_TRY(launch_pack(pa, s));
+        GemmArgs gq;
+        gq.W0 = w->wq;
+        gq.n0 = qt;
+        gq.W1 = w->wk;
+        gq.n1 = kt;
+        gq.W2 = w->wv;
+        gq.n2 = kt;
+        gq.N = Nqkv;
+        gq.K = H;
+        gq.X = W.xp_attn;
+        gq.ldx = H;
+        gq.T = B;
+        gq.epi = EPI_STORE;
+        gq.out = W.qkv;
+        gq.ldo = Nqkv;
+        DF_TRY(launch_gemm(gq, s));
+        if (w->w_gate) {
+            GemmArgs gg = gq;
+            gg.W0 = w->w_gate;
+            gg.n0 = qt;
+            gg.W1 = gg.W2 = nullptr;
+            gg.n1 = gg.n2 = 0;
+            gg.N = qt;
+            gg.out = W.gate;
+            gg.ldo = qt;
+            DF_TRY(launch_gemm(gg, s));
+        }
+        DF_TRY(launch_rope_table(W.cos_t, W.sin_t, cache->seq_len, nullptr, 0, B, 1, st, rot,
+                                 cfg->rope_theta, d_status, s));
+        QkArgs qa;
+        qa.qkv = W.qkv;
+        qa.ldq = Nqkv;
+        qa.B = B;
+        qa.blk = 1;
+        qa.n_new_max = 0;
+        qa.nq = nq;
+        qa.nkv = nkv;
+        qa.d = d;
+        qa.rot = rot;
+        qa.q_norm = w->q_norm;
+        qa.k_norm = w->k_norm;
+        qa.eps = cfg->rms_eps;
+        qa.cos_t = W.cos_t;
+        qa.sin_t = W.sin_t;
+        qa.q_out = W.q;
+        qa.kb = nullptr;
+        qa.vb = nullptr;
+        qa.cache_k = cache->k[0];
+        qa.cache_v = cache->v[0];
+        qa.cap = cache->cap;
+        qa.seq_len = cache->seq_len;
+        qa.n_new = nullptr;
+        qa.append_block = 1;
+        qa.pos_off = st;
+        qa.status = d_status;
+        DF_TRY(launch_qk_rope(qa, s));
+        AttnArgs at = W.plan;
+        at.q = W.q;
+        at.cache_k = cache->k[0];
+        at.cache_v = cache->v[0];
+        at.cap = cache->cap;
+        at.kb = nullptr;
+        at.vb = nullptr;
+        at.seq_len = cache->seq_len;
+        at.n_new = nullptr;
+        at.n_new_max = 0;
+        at.extra_rows = st + 1;
+        at.causal_block = 0;
+        at.part_o = W.part_o;
+        at.part_ml = W.part_ml;
+        at.gate = w->w_gate ? W.gate : nullptr;
+        at.ldg = qt;
+        at.pack = W.xp_o;
+        at.status = d_status;
+        DF_TRY(launch_attn(at, s));
+        GemmArgs go;
+        go.W0 = w->wo;
+        go.n0 = H;
+        go.N = H;
+        go.K = qt;
+        go.X = W.xp_o;
+        go.ldx = qt;
+        go.T = B;
+        go.epi = EPI_RESID;
+        go.out = W.h1;
+        go.ldo = H;
+        go.resid = W.x;
+        go.ldr = H;
+        DF_TRY(launch_gemm(go, s));
+        PackArgs pf;
+        pf.src = W.h1;
+        pf.lds = H;
+        pf.norm_w = w->post_attn_norm;
+        pf.eps = cfg->rms_eps;
+        pf.pack = W.xp_ffn;
+        pf.ldp = H;
+        pf.T = B;
+        pf.K = H;
+        DF_TRY(launch_pack(pf, s));
+        GemmArgs gu;
+        gu.W0 = w->w_gate_mlp;
+        gu.n0 = I;
+        gu.W1 = w->w_up;
+        gu.n1 = I;
+        gu.N = I;
+        gu.K = H;
+        gu.X = W.xp_ffn;
+        gu.ldx = H;
+        gu.T = B;
+        gu.epi = EPI_SWIGLU;
+        gu.pack_out = W.xp_act;
+        gu.ldpo = I;
+        DF_TRY(launch_gemm(gu, s));
+        GemmArgs gd;
+        gd.W0 = w->w_down;
+        gd.n0 = H;
+        gd.N = H;
+        gd.K = I;
+        gd.X = W.xp_act;
+        gd.ldx = I;
+        gd.T = B;
+        gd.epi = EPI_RESID;
+        gd.out = hid;
+        gd.ldo = H;
+        gd.resid = W.h1;
+        gd.ldr = H;
+        DF_TRY(launch_gemm(gd, s));
+        // shared head: rmsnorm(hidden) then lm_head argmax (mtp.rs `forward_shared_head`)
+        PackArgs pk;
+        pk.src = hid;
+        pk.lds = H;
+        pk.norm_w = w->shared_head_norm;
+        pk.eps = cfg->rms_eps;
+        pk.pack = W.xp_head;
+        pk.ldp = H;
+        pk.T = B;
+        pk.K = H;
+        DF_TRY(launch_pack(pk, s));
+        DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B, H, cfg->vocab, W.amax_part,
+                            argmax_out + (size_t)st * B, nullptr, nullptr, s));
+        if (logits_out && st == n_steps - 1) {
+            GemmArgs gl;
+            gl.W0 = w->lm_head;
+            gl.n0 = cfg->vocab;
+            gl.N = cfg->vocab;
+            gl.K = H;
+            gl.X = W.xp_head;
+            gl.ldx = H;
+            gl.T = B;
+            gl.epi = EPI_STORE;
+            gl.out = logits_out;
+            gl.ldo = cfg->vocab;
+            DF_TRY(launch_gemm(gl, s));
+        }
+    }
+    return launch_seq_advance(cache->seq_len, nullptr, B, n_steps, cache->cap, d_status, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,219 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dflash.h"
+
+namespace df {
+
+// ---------------------------------------------------------------- host-side errors
+int fail(int code, const char *fmt, ...);   // records the message, returns code
+int cuda_check(const char *what);           // DF_ECUDA if the last launch failed
+
+#define DF_TRY(expr)                 \
+    do {                             \
+        int df_rc_ = (expr);         \
+        if (df_rc_ != DF_OK) return df_rc_; \
+    } while (0)
+
+constexpr int kNumSMs = 152;
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Round-to-nearest-even F32 -> BF16 bits.
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Split y into hi = bf16(y) and lo = bf16(y - hi); hi + lo carries ~16 mantissa bits of y and
+// is exactly representable in F32.
+__device__ __forceinline__ void split_hi_lo(float y, uint16_t &hi, uint16_t &lo) {
+    hi = f32_to_bf16_bits(y);
+    lo = f32_to_bf16_bits(y - bf16_bits_to_f32(hi));
+}
+
+__device__ __forceinline__ void set_status(int32_t *st, int code) {
+    if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+// Streaming 128-bit load that does not allocate in L1 (weights are read once per call).
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Argmax state: best value, its index, and the second-largest value.
+struct ArgTop {
+    float v1;
+    int i1;
+    float v2;
+};
+
+__device__ __forceinline__ ArgTop argtop_empty(int big_index) { return {-INFINITY, big_index, -INFINITY}; }
+
+// Merge two states; the lower index wins an exact tie of the best value.
+__device__ __forceinline__ ArgTop argtop_merge(ArgTop a, ArgTop b) {
+    bool b_wins = (b.v1 > a.v1) || (b.v1 == a.v1 && b.i1 < a.i1);
+    ArgTop r;
+    r.v1 = b_wins ? b.v1 : a.v1;
+    r.i1 = b_wins ? b.i1 : a.i1;
+    float lo = b_wins ? a.v1 : b.v1;           // the loser's best
+    r.v2 = fmaxf(lo, fmaxf(a.v2, b.v2));
+    return r;
+}
+
+__device__ __forceinline__ ArgTop argtop_push(ArgTop a, float v, int i) {
+    ArgTop b = {v, i, -INFINITY};
+    return argtop_merge(a, b);
+}
+
+// ---------------------------------------------------------------- workspace carving
+struct Carve {
+    char *base;
+    size_t off, cap;
+    bool ok;
+    template <class T>
+    T *take(size_t count) {
+        size_t bytes = (count * sizeof(T) + 255) & ~size_t(255);
+        if (off + bytes > cap) ok = false;
+        T *p = ok && base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += bytes;
+        return p;
+    }
+};
+
+// ---------------------------------------------------------------- kernels (launchers)
+
+// Packed activation layout: for token t of a GEMM input, row 2t holds bf16(y) and row 2t+1
+// holds bf16(y - bf16(y)), both [K] BF16 with leading dimension ldp (elements).
+struct PackArgs {
+    const float *src = nullptr;      // F32 rows [T, K], row stride lds
+    int lds = 0;
+    const uint16_t *gather = nullptr;  // gather mode: rows embed[ids[t]] (BF16) instead of src
+    const int32_t *ids = nullptr;
+    const int32_t *last_token = nullptr;  // gather mode alternative: id = i == 0 ? last[b] : mask
+    int mask_id = 0;
+    int vocab = 0;
+    float scale = 1.f;
+    float *h_out = nullptr;          // optional raw (gathered) rows, row stride ldh
+    int ldh = 0;
+    const float *norm_w = nullptr;   // optional RMSNorm weight
+    float eps = 0.f;
+    float *y_out = nullptr;          // optional normalised rows, row stride ldy
+    int ldy = 0;
+    uint16_t *pack = nullptr;        // optional packed output
+    int ldp = 0;
+    int T = 0, K = 0;
+    const int32_t *nvalid = nullptr; // rows t = s*rows_per_seq + j are valid iff j < nvalid[s]
+    int rows_per_seq = 1;
+    int32_t *status = nullptr;
+};
+int launch_pack(const PackArgs &a, cudaStream_t s);
+
+enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
+
+struct GemmArgs {
+    // Weight rows (BF16 [rows, K] row-major). Up to three segments concatenated along the
+    // output dimension: rows [0,n0) of W0, then n1 rows of W1, then n2 rows of W2.
+    // EPI_SWIGLU pairs row j of W0 (gate) with row j of W1 (up): N = n0 = n1.
+    const uint16_t *W0 = nullptr, *W1 = nullptr, *W2 = nullptr;
+    int n0 = 0, n1 = 0, n2 = 0;
+    // Optional split along K for segment 0: columns [K1, K) read from Wk2 [n0, K-K1].
+    const uint16_t *Wk2 = nullptr;
+    int K1 = 0;
+    int N = 0, K = 0;
+    const uint16_t *X = nullptr;     // packed activations [2T, ldx]
+    int ldx = 0, T = 0;
+    int epi = EPI_STORE;
+    float *out = nullptr;            // EPI_STORE / EPI_RESID: out[t*ldo + n]
+    int ldo = 0;
+    const float *resid = nullptr;    // EPI_RESID: resid[t*ldr + n] (may alias out)
+    int ldr = 0;
+    uint16_t *pack_out = nullptr;    // EPI_SWIGLU: packed [2T, ldpo]
+    int ldpo = 0;
+    ArgTop *part = nullptr;          // EPI_ARGMAX: partial states [grid, T]
+    int *n_part = nullptr;           // EPI_ARGMAX: host-visible count of partial rows written
+};
+int launch_gemm(const GemmArgs &a, cudaStream_t s, int *n_partials_out = nullptr);
+
+// Reduce EPI_ARGMAX partials [G, T] into idx/top1/top2 [T].
+int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1,
+                        float *top2, int32_t *idx_copy, int idx_copy_ld, int idx_copy_skip,
+                        cudaStream_t s);
+
+// RoPE table: cos/sin F32 [B, slots, rot/2] for block slots (pos = seq_len + n_new + i + off)
+// and context slots (pos = seq_len + j).
+int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const int32_t *n_new,
+                      int n_new_max, int B, int blk, int pos_off, int rot, float theta,
+                      int32_t *status, cudaStream_t s);
+
+struct QkArgs {
+    const float *qkv;        // [T_blk + T_ctx, ldq] raw projections (q | k | v)
+    int ldq;
+    int B, blk, n_new_max;
+    int nq, nkv, d, rot;
+    const float *q_norm, *k_norm;   // may be null (no per-head norm)
+    float eps;
+    const float *cos_t, *sin_t;     // [B, blk + n_new_max, rot/2]
+    float *q_out;                   // [B, blk, nq, d]
+    float *kb, *vb;                 // [B, nkv, blk, d] (block K/V) or null
+    float *cache_k, *cache_v;       // [B, nkv, cap, d]
+    int cap;
+    const int32_t *seq_len, *n_new;
+    int append_block;               // 1: block rows are appended to the cache (MTP)
+    int pos_off;                    // added to block positions (MTP chained step)
+    int32_t *status;
+};
+int launch_qk_rope(const QkArgs &a, cudaStream_t s);
+
+struct AttnArgs {
+    const float *q;          // [B, blk, nq, d]
+    const float *cache_k, *cache_v;   // [B, nkv, cap, d]
+    int cap;
+    const float *kb, *vb;    // [B, nkv, blk, d] block keys or null
+    int B, blk, nq, nkv, d;
+    const int32_t *seq_len, *n_new;   // cache rows visible: seq_len + n_new (+ extra)
+    int n_new_max;
+    int extra_rows;          // rows beyond seq_len + n_new that are visible (MTP: step + 1)
+    int causal_block;
+    float *part_o, *part_ml; // workspace partials
+    int n_chunks, chunk, rows_per_group, n_groups;
+    // combine
+    const float *gate;       // optional [B*blk, ldg] gate pre-activation (q_total wide)
+    int ldg;
+    uint16_t *pack;          // packed output [2*B*blk, nq*d]
+    int32_t *status;
+};
+void attn_plan(AttnArgs &a, int max_keys);
+size_t attn_part_floats(int B, int nkv, int n_groups, int n_chunks, int rows_per_group, int d);
+int launch_attn(const AttnArgs &a, cudaStream_t s);
+
+int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
+                       int32_t *status, cudaStream_t s);
+int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
+                  const int32_t *eos, int n_eos, int32_t *committed, int32_t *n_committed,
+                  int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,
+                  int32_t *target_seq_len, int32_t *status, cudaStream_t s);
+int launch_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *status, cudaStream_t s);
+
+}  // namespace df

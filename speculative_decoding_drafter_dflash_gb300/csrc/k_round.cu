@@ -1,0 +1,103 @@
+// Integer tail of the draft round: final argmax reduction, greedy accept walk, KV rollback.
+//
+// hf2q 0.1.1 spec_decode/dflash/qwen35_orchestrator.rs: step 5 (per-position argmax,
+// drafts = argmax[1..]), step 7 (`step_round_from_argmaxes`: accept a draft only while it
+// equals the verifier's argmax; the verifier's argmax at accept_count is the free token; stop
+// at EOS), step 8 (`rollback = drafts.len() - accept_count`, `rollback_kv`).
+#include "df_internal.cuh"
+
+namespace df {
+
+namespace {
+
+// One thread per row: merge the G partial states in increasing partial order.
+__global__ void argmax_final_kernel(const ArgTop *part, int G, int T, int32_t *idx, float *top1,
+                                    float *top2, int32_t *idx_copy, int ld, int skip) {
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    ArgTop r = argtop_empty(0x7fffffff);
+    for (int g = 0; g < G; ++g) r = argtop_merge(r, part[(size_t)g * T + t]);
+    idx[t] = r.i1;
+    if (top1) top1[t] = r.v1;
+    if (top2) top2[t] = r.v2;
+    // Optional copy in a second layout (used to place drafts = rows 1..K of each sequence).
+    if (idx_copy) {
+        int b = t / ld, i = t % ld;
+        if (i >= skip) idx_copy[(size_t)b * (ld - skip) + (i - skip)] = r.i1;
+    }
+}
+
+// One thread per sequence.
+__global__ void accept_kernel(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
+                              const int32_t *eos, int n_eos, int32_t *committed,
+                              int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                              int32_t *rollback, int32_t *target_seq_len, int32_t *status) {
+    int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int32_t *dr = drafts + (size_t)b * ld;
+    const int32_t *tg = target + (size_t)b * (K + 1);
+    int a = 0;
+    while (a < K && dr[a] == tg[a]) ++a;
+    int32_t *out = committed + (size_t)b * (K + 1);
+    int n = 0, hit = 0;
+    for (int i = 0; i <= a; ++i) {
+        int tok = i < a ? dr[i] : tg[a];
+        out[n++] = tok;
+        bool is_eos = false;
+        for (int e = 0; e < n_eos; ++e) is_eos |= (tok == eos[e]);
+        if (is_eos) {
+            hit = 1;
+            break;
+        }
+    }
+    for (int i = n; i <= K; ++i) out[i] = -1;
+    n_committed[b] = n;
+    accept_count[b] = a;
+    hit_eos[b] = hit;
+    rollback[b] = K - a;
+    if (target_seq_len) {
+        int rb = K - a;
+        if (rb > target_seq_len[b]) set_status(status, DF_ECAPACITY);
+        else target_seq_len[b] -= rb;
+    }
+}
+
+__global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32_t *status) {
+    int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int k = n[b];
+    if (k < 0 || k > seq_len[b]) {
+        set_status(status, DF_ECAPACITY);
+        return;
+    }
+    seq_len[b] -= k;
+}
+
+}  // namespace
+
+int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1, float *top2,
+                        int32_t *idx_copy, int idx_copy_ld, int idx_copy_skip, cudaStream_t s) {
+    if (T <= 0) return DF_OK;
+    argmax_final_kernel<<<(T + 127) / 128, 128, 0, s>>>(part, G, T, idx, top1, top2, idx_copy,
+                                                        idx_copy_ld, idx_copy_skip);
+    return cuda_check("argmax_final_kernel");
+}
+
+int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
+                  const int32_t *eos, int n_eos, int32_t *committed, int32_t *n_committed,
+                  int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,
+                  int32_t *target_seq_len, int32_t *status, cudaStream_t s) {
+    if (B <= 0) return DF_OK;
+    accept_kernel<<<(B + 127) / 128, 128, 0, s>>>(drafts, ld, target, B, K, eos, n_eos, committed,
+                                                  n_committed, accept_count, hit_eos, rollback,
+                                                  target_seq_len, status);
+    return cuda_check("accept_kernel");
+}
+
+int launch_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *status, cudaStream_t s) {
+    if (B <= 0) return DF_OK;
+    rollback_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, n, B, status);
+    return cuda_check("rollback_kernel");
+}
+
+}  // namespace df
