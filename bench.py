@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Benchmark: DFlash-shaped draft rounds per second on GB300 (K=15, block 16, H=2816, 5
+layers, 16q/8kv x 128, SwiGLU 8192, vocab 262144, context 4096), batch 1 per GPU.
+
+One step = one whole draft round through the C ABI (`df_draft_round`: embed gather, fc +
+hidden_norm of the new context rows, 5 drafter layers, final norm, lm_head + fused argmax of
+the 16 block rows, greedy accept walk, verifier KV rollback) followed by `kv_rollback` of the
+drafter cache, so every replay sees the same state (stateless replays of 8 seeded round
+variants whose new-context-row counts follow geometric acceptance, p = 0.6).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line (rank 0). N > 1 runs under torchrun: one replica per GPU (the round
+does not shard; no collective on the data path), value = all ranks' rounds / max elapsed.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft rounds/s (DFlash shape, K=15) & achieved HBM GB/s vs 8 TB/s"
+N_VARIANTS = 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="bound on the oracle's CPU sample time")
+    ap.add_argument("--skip-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def round_bytes(s, n_new: int) -> int:
+    """Algorithmic HBM bytes of one round: every weight once, KV read of the cache plus the
+    appended rows, KV write of the appended rows, the new target hidden rows, embed rows."""
+    H, d, nkv, L = s.hidden, s.head_dim, s.n_kv_heads, s.n_layers
+    kv_row = nkv * d * 4 * 2                       # K and V, F32
+    w = s.weight_bytes() + 2 * s.vocab * H         # drafter + lm_head
+    kv_read = L * (s.ctx + n_new) * kv_row
+    kv_write = L * n_new * kv_row
+    return w + kv_read + kv_write + n_new * s.fc_in * 4 + s.block * H * 2
+
+
+def lm_head_bytes(s, rows: int) -> int:
+    return 2 * s.vocab * s.hidden + 2 * 2 * rows * s.hidden
+
+
+def variants(s):
+    """Seeded round variants: accept counts a_v (geometric) and n_new_v = a_{v-1} + 1."""
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    acc = synth.accept_lengths(N_VARIANTS, s.K, s.accept_p, seed=123)
+    n_new = [int(acc[(v - 1) % N_VARIANTS]) + 1 for v in range(N_VARIANTS)]
+    return acc, n_new
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_round_setup(s, w, cache, inputs):
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    h = synth.host
+    hw = dict(fc=h(w.fc), hidden_norm=h(w.hidden_norm), final_norm=h(w.final_norm),
+              embed=h(w.embed), lm_head=h(w.lm_head),
+              layers=[dict(input_norm=h(l.input_norm), post_norm=h(l.post_norm), q_norm=h(l.q_norm),
+                           k_norm=h(l.k_norm), wq=h(l.wq), wk=h(l.wk), wv=h(l.wv), wo=h(l.wo),
+                           wg=h(l.wg), wu=h(l.wu), wd=h(l.wd)) for l in w.layers])
+    ks = [h(k) for k in cache.k]
+    vs = [h(v) for v in cache.v]
+    seq = h(cache.seq_len).copy()
+    return hw, ks, vs, seq, [(h(i.block_ids), h(i.target_hidden), h(i.n_new)) for i in inputs]
+
+
+def oracle_rounds(s, hw, ks, vs, seq, host_inputs, targets, n: int, budget_s: float):
+    """Time up to n oracle rounds (stopping once budget_s is spent); returns (rounds, seconds)."""
+    from oracle import dflash as odf
+    done, t0 = 0, time.perf_counter()
+    while done < n:
+        v = done % len(host_inputs)
+        ids, th, nn = host_inputs[v]
+        odf.draft_round(s, hw, ks, vs, seq, ids, th, nn, targets[v], s.eos_ids, [1 << 30])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- native
+def run_native(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+
+    B.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    s = DFLASH_K15
+    acc, n_new = variants(s)
+    nmax = s.block
+    w = synth.dflash_weights(s, seed=0, device=dev)
+    cache = synth.dflash_cache(s, seed=1, device=dev)
+    inputs = []
+    for v in range(N_VARIANTS):
+        inp = synth.dflash_round_inputs(s, [nmax], seed=10 + 100 * rank + v, device=dev)
+        inp.n_new = torch.tensor([n_new[v]], dtype=torch.int32, device=dev)
+        inputs.append(inp)
+    model = B.DFlashModel(s, w, cache)
+    ws = B.alloc_workspace(model.workspace_bytes(1, s.block, nmax), dev)
+    out = B.RoundOutputs(1, s.K, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
+    tsl = torch.full((1,), 1 << 30, dtype=torch.int32, device=dev)
+    zero_tgt = torch.zeros((1, s.block), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(v, tgt):
+        inp = inputs[v]
+        B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, nmax, s.K, tgt, eos,
+                         tsl, out, ws, st, stream=stream)
+        B.kv_rollback(cache.seq_len, inp.n_new, st, stream=stream)
+
+    # Untimed pass: each variant's drafts define its synthetic target argmaxes.
+    targets, drafts = [], []
+    with torch.cuda.stream(stream):
+        for v in range(N_VARIANTS):
+            step(v, zero_tgt)
+            stream.synchronize()
+            d = out.argmax[0, 1:].cpu().numpy()
+            drafts.append(d)
+            t = synth.targets_from_drafts(d[None, :], np.array([acc[v]]), s.vocab, seed=50 + v)
+            targets.append(torch.tensor(t, device=dev))
+        # Check pass: drafts repeat bit-exactly and the accept walk lands on a_v.
+        ok = True
+        l0 = B.kernel_launches()
+        for v in range(N_VARIANTS):
+            step(v, targets[v])
+            stream.synchronize()
+            ok &= bool(np.array_equal(out.argmax[0, 1:].cpu().numpy(), drafts[v]))
+            ok &= int(out.accept[0]) == int(acc[v]) and int(st.item()) == 0
+        launches_per_step = (B.kernel_launches() - l0) // N_VARIANTS
+    if not ok:
+        raise RuntimeError("replayed rounds did not reproduce their drafts / accept counts")
+
+    graphs = []
+    if not args.no_graph:
+        for v in range(N_VARIANTS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(v, targets[v])
+            graphs.append(g)
+
+    def run(i):
+        v = i % N_VARIANTS
+        if graphs:
+            graphs[v].replay()
+        else:
+            step(v, targets[v])
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            run(i)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            run(i)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    assert int(st.item()) == 0, "device status set during the timed region"
+    rounds = args.steps * world
+    value = rounds / elapsed
+    ms = elapsed / args.steps * 1e3
+    avg_bytes = sum(round_bytes(s, n_new[i % N_VARIANTS]) for i in range(args.steps)) / args.steps
+    hbm_peak, peak_kind = peaks()
+
+    # Dominant kernel (lm_head + fused argmax over the 16 block rows): CUDA events around each
+    # call on its launching stream, inputs resident, weights (1.48 GB) far larger than L2.
+    rows = s.block
+    X = torch.randn((rows, s.hidden), device=dev)
+    idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    ws_lm = B.alloc_workspace(B.lm_head_workspace_bytes(rows, s.hidden, s.vocab), dev)
+    durs = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            B.lm_head_argmax(w.lm_head, X, idx, ws=ws_lm, stream=stream)
+        for i in range(max(args.steps, 10)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            B.lm_head_argmax(w.lm_head, X, idx, ws=ws_lm, stream=stream)
+            b.record(stream)
+            durs.append((a, b))
+    torch.cuda.synchronize(dev)
+    lm_s = statistics.mean(a.elapsed_time(b) for a, b in durs) / 1e3
+    lm_ach = lm_head_bytes(s, rows) / lm_s / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "lm_head_argmax_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        if tj.get("kernel_source_hash") == kernel_hash():
+            traffic = tj.get("dram_bytes_per_launch")
+
+    # End to end through the host-buffer entry point: pinned host inputs copied in, the round,
+    # results copied back and the stream synchronised, every step.
+    e2e = None
+    if True:
+        hin = []
+        for v in range(N_VARIANTS):
+            inp = inputs[v]
+            hin.append(dict(last=inp.last_token.cpu().pin_memory(),
+                            th=inp.target_hidden.cpu().pin_memory(),
+                            nn=inp.n_new.cpu().pin_memory(), tgt=targets[v].cpu().pin_memory()))
+        heos = eos.cpu().pin_memory()
+        htsl = torch.full((1,), 1 << 30, dtype=torch.int32).pin_memory()
+        hout = {k: torch.zeros(shape, dtype=torch.int32).pin_memory() for k, shape in (
+            ("argmax", (1, s.block)), ("committed", (1, s.block)), ("n_committed", (1,)),
+            ("accept", (1,)), ("hit_eos", (1,)), ("rollback", (1,)), ("status", (1,)))}
+        ws_h = B.alloc_workspace(B.draft_round_host_workspace_bytes(model, 1, s.K, nmax, 1), dev)
+
+        def host_step(i):
+            v = i % N_VARIANTS
+            h = hin[v]
+            B.df_draft_round_host(model, h["last"], h["th"], h["nn"], nmax, s.K, h["tgt"], heos,
+                                  htsl, hout, ws_h, stream=stream)
+            B.kv_rollback(cache.seq_len, inputs[v].n_new, st, stream=stream)
+
+        for i in range(args.warmup):
+            host_step(i)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            host_step(i)
+        torch.cuda.synchronize(dev)
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        assert int(hout["status"][0]) == 0
+        h2d = sum(hin[i % N_VARIANTS]["last"].numel() * 4 + hin[i % N_VARIANTS]["th"].numel() * 4
+                  + 4 + hin[i % N_VARIANTS]["tgt"].numel() * 4 + 4 + 4
+                  for i in range(args.steps)) // args.steps
+        d2h = sum(t.numel() * 4 for t in hout.values())
+        e2e = {"value": round(rounds / e2e_s, 3), "unit": "rounds/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        hw, ks, vs, seq, hinp = oracle_round_setup(s, w, cache, inputs)
+        tg = [t.cpu().numpy() for t in targets]
+        oracle_rounds(s, hw, ks, vs, seq, hinp, tg, 1, 1e9)      # warm the BLAS / page cache
+        n, secs = oracle_rounds(s, hw, ks, vs, seq, hinp, tg, 50, args.cpu_seconds)
+        cpu = {"value": round(n / secs, 4), "unit": "rounds/s", "cores": cores(), "kind": "oracle",
+               "sample": f"{n} full rounds of this workload by the NumPy F32 oracle ({secs:.1f} s)"}
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "rounds/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": s.name, "batch_per_gpu": 1, "K": s.K, "block": s.block,
+                   "ctx": s.ctx, "hidden": s.hidden, "layers": s.n_layers, "heads": "16q/8kv x 128",
+                   "intermediate": s.intermediate, "vocab": s.vocab,
+                   "weights": "bf16", "activations_kv": "f32", "accumulate": "f32",
+                   "n_new_per_variant": n_new, "accept_per_variant": [int(a) for a in acc],
+                   "l2": "no flush: each round streams 2.6 GB of weights, 20x the 129 MB L2",
+                   "cuda_graph": not args.no_graph, "parallelism": f"replicas x{world}"},
+        "positions_per_s": round(value * s.block, 1),
+        "drafts_per_s": round(value * s.K, 1),
+        "round_bytes": int(avg_bytes),
+        "round_hbm_gbs": round(avg_bytes / (ms / 1e3) / 1e9, 1),
+        "round_frac_of_8tbs": round(avg_bytes / (ms / 1e3) / 8e12, 4),
+        "round_frac_of_measured_hbm": round(avg_bytes / (ms / 1e3) / 1e9 / hbm_peak, 4),
+        "roofline": {"kernel": "lm_head_argmax (lm_head rows x 16 block rows, fused argmax)",
+                     "bound": "hbm", "achieved": round(lm_ach, 1), "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(lm_ach / hbm_peak, 4),
+                     "traffic": traffic, "bytes_per_launch": lm_head_bytes(s, rows),
+                     "avg_launch_us": round(lm_s * 1e6, 2)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_step * args.steps),
+        "launches_per_step": int(launches_per_step),
+        "clocks": clk,
+    }
+
+
+def kernel_hash():
+    """Hash of the CUDA sources: a stored traffic figure is only used for the kernels it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_drafter_dflash_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The oracle, as it stands, timed on this machine's host cores on the same workload."""
+    if rank != 0:
+        return None
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+    s = DFLASH_K15
+    dev = "cuda" if torch.cuda.is_available() else "cpu"       # generation only
+    acc, n_new = variants(s)
+    w = synth.dflash_weights(s, seed=0, device=dev)
+    cache = synth.dflash_cache(s, seed=1, device=dev)
+    inputs = []
+    for v in range(N_VARIANTS):
+        inp = synth.dflash_round_inputs(s, [s.block], seed=10 + v, device=dev)
+        inp.n_new = torch.tensor([n_new[v]], dtype=torch.int32, device=dev)
+        inputs.append(inp)
+    hw, ks, vs, seq, hinp = oracle_round_setup(s, w, cache, inputs)
+    del w, cache, inputs
+    # Each step is one full oracle round. The target row only steers the integer walk at the
+    # end, so a fixed one leaves the timed arithmetic the same as with per-variant targets.
+    tg = [np.zeros((1, s.block), dtype=np.int32)] * N_VARIANTS
+    for i in range(args.warmup):
+        oracle_rounds(s, hw, ks, vs, seq, [hinp[i % N_VARIANTS]], tg, 1, 1e9)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_rounds(s, hw, ks, vs, seq, [hinp[i % N_VARIANTS]], tg, 1, 1e9)
+    secs = time.perf_counter() - t0
+    value = args.steps / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "rounds/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": s.name, "batch_per_gpu": 1, "K": s.K, "ctx": s.ctx},
+        "cpu_baseline": {"value": round(value, 4), "unit": "rounds/s", "cores": cores(),
+                         "kind": "oracle",
+                         "sample": "one full round of the workload per step (NumPy F32 oracle)"},
+        "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, rank, world)
+        else:
+            res = run_native(args, rank, world, local_rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

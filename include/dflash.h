@@ -62,6 +62,10 @@ const char *df_last_error(void);
 /* Library ABI version (major * 100 + minor). */
 int df_version(void);
 
+/* Number of kernels this process has launched through the library so far (all threads).
+ * Launches recorded into a CUDA graph count once, at capture. */
+uint64_t df_kernel_launches(void);
+
 /* ------------------------------------------------------------------------------------------
  * DFlash drafter (tensors.rs `DFlashLayerTensors`, `DFlashModelTensors`; dflash config fields
  * seen in qwen35_orchestrator.rs: target_layer_ids, mask_token_id, hidden_size, head_dim).

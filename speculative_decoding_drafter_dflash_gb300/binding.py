@@ -73,6 +73,7 @@ _lib = None
 _SIGS = [
     ("df_last_error", ctypes.c_char_p, []),
     ("df_version", c_int, []),
+    ("df_kernel_launches", ctypes.c_uint64, []),
     ("df_dflash_workspace_bytes", c_size_t, [POINTER(DFlashConfig), c_int, c_int, c_int]),
     ("dflash_block_forward", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), POINTER(KvCache),
                                      c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
@@ -117,6 +118,10 @@ def lib():
             fn.argtypes = args
         _lib = L
     return _lib
+
+
+def kernel_launches() -> int:
+    return int(lib().df_kernel_launches())
 
 
 def last_error() -> str:

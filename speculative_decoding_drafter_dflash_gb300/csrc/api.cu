@@ -5,6 +5,7 @@
 // (per-round loop, steps 1-9) for DFlash and models/qwen35/mtp.rs
 // (`forward_draft_with_hidden`) for MTP.
 #include <algorithm>
+#include <atomic>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -14,6 +15,7 @@
 namespace df {
 
 static thread_local char g_err[512] = "";
+static std::atomic<uint64_t> g_launches{0};
 
 int fail(int code, const char *fmt, ...) {
     va_list ap;
@@ -24,6 +26,7 @@ int fail(int code, const char *fmt, ...) {
 }
 
 int cuda_check(const char *what) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DF_ECUDA, "%s: %s", what, cudaGetErrorString(e));
     return DF_OK;
@@ -417,6 +420,8 @@ extern "C" {
 const char *df_last_error(void) { return g_err; }
 
 int df_version(void) { return 100; }
+
+uint64_t df_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t df_dflash_workspace_bytes(const df_dflash_config *cfg, int B, int block, int n_new_max) {
     if (check_cfg(cfg) != DF_OK || B <= 0 || block < 2 || n_new_max < 0) return 0;

@@ -12,7 +12,7 @@ namespace df {
 
 // ---------------------------------------------------------------- host-side errors
 int fail(int code, const char *fmt, ...);   // records the message, returns code
-int cuda_check(const char *what);           // DF_ECUDA if the last launch failed
+int cuda_check(const char *what);           // DF_ECUDA if the last launch failed; counts launches
 
 #define DF_TRY(expr)                 \
     do {                             \

@@ -21,7 +21,7 @@ def L():
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "dflash.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char|void)\s*\*?\s*(\w+)\s*\(", src, re.M)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char|void|uint64_t)\s*\*?\s*(\w+)\s*\(", src, re.M)
     return sorted(set(names))
 
 
