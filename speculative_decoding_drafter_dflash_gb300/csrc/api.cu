@@ -125,7 +125,18 @@ struct DFlashWs {
     ArgTop *amax_part;
     int32_t *idx;
     AttnArgs plan;
+    TcScratch tc;
 };
+
+int n_counters_for(long long rows) { return (int)(rows / 64 + 256); }
+
+void carve_tc(Carve &cv, TcScratch &tc, int max_tokens, long long max_rows) {
+    tc.partial_floats = tc_partial_floats(max_tokens);
+    tc.partials = cv.take<float>(tc.partial_floats);
+    tc.n_counters = n_counters_for(max_rows);
+    tc.counters = cv.take<int>((size_t)tc.n_counters);
+    tc.max_ctas = kNumSMs;
+}
 
 void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int blk, int n_new_max,
                   int cap, bool round) {
@@ -156,6 +167,11 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     w.xp_o = cv.take<uint16_t>(2 * T_blk * qt);
     w.xp_ffn = cv.take<uint16_t>(2 * T_blk * H);
     w.xp_act = cv.take<uint16_t>(2 * T_blk * c->intermediate);
+    {
+        long long rows = std::max<long long>({(long long)c->vocab, 2LL * c->intermediate,
+                                              (long long)(qt + 2 * kt), (long long)H});
+        carve_tc(cv, w.tc, (int)T_all, rows);
+    }
     if (round) {
         w.h_final = cv.take<float>(T_blk * H);
         w.xp_head = cv.take<uint16_t>(2 * T_blk * H);
@@ -214,7 +230,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.epi = EPI_STORE;
         g.out = ws.hctx;
         g.ldo = H;
-        DF_TRY(launch_gemm(g, s));
+        g.status = st;
+        DF_TRY(launch_gemm_tc(g, ws.tc, s));
         PackArgs q;
         q.src = ws.hctx;
         q.lds = H;
@@ -270,7 +287,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.epi = EPI_STORE;
         g.out = ws.qkv;
         g.ldo = Nqkv;
-        DF_TRY(launch_gemm(g, s));
+        g.status = st;
+        DF_TRY(launch_gemm_tc(g, ws.tc, s));
 
         QkArgs qa;
         qa.qkv = ws.qkv;
@@ -333,7 +351,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         go.ldo = H;
         go.resid = ws.h;
         go.ldr = H;
-        DF_TRY(launch_gemm(go, s));
+        go.status = st;
+        DF_TRY(launch_gemm_tc(go, ws.tc, s));
 
         PackArgs pf;
         pf.src = ws.h;
@@ -360,7 +379,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gu.epi = EPI_SWIGLU;
         gu.pack_out = ws.xp_act;
         gu.ldpo = I;
-        DF_TRY(launch_gemm(gu, s));
+        gu.status = st;
+        DF_TRY(launch_gemm_tc(gu, ws.tc, s));
 
         GemmArgs gd;
         gd.W0 = L.w_down;
@@ -375,7 +395,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gd.ldo = H;
         gd.resid = ws.h;
         gd.ldr = H;
-        DF_TRY(launch_gemm(gd, s));
+        gd.status = st;
+        DF_TRY(launch_gemm_tc(gd, ws.tc, s));
     }
     PackArgs pfin;
     pfin.src = ws.h;
@@ -394,7 +415,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
 }
 
 int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
-                 int32_t *idx, float *top1, float *top2, cudaStream_t s) {
+                 int32_t *idx, float *top1, float *top2, const TcScratch &tc, cudaStream_t s) {
     GemmArgs g;
     g.W0 = Wlm;
     g.n0 = V;
@@ -406,7 +427,7 @@ int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V
     g.epi = EPI_ARGMAX;
     g.part = part;
     int G = 0;
-    DF_TRY(launch_gemm(g, s, &G));
+    DF_TRY(launch_gemm_tc(g, tc, s, &G));
     return launch_argmax_final(part, G, rows, idx, top1, top2, nullptr, 1, 0, s);
 }
 
@@ -459,17 +480,20 @@ int dflash_block_forward(const df_dflash_config *cfg, const df_dflash_weights *w
 
 size_t df_lm_head_workspace_bytes(int rows, int H, int V) {
     if (rows <= 0 || H <= 0 || V <= 0) return 0;
+    if (rows > kMaxTcTokens) return 0;
     Carve cv{nullptr, 0, ~size_t(0), true};
     cv.take<uint16_t>((size_t)2 * rows * H);
     cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    TcScratch tc;
+    carve_tc(cv, tc, rows, V);
     return cv.off;
 }
 
 int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
                    float *top1, float *top2, void *ws, size_t ws_bytes, df_stream_t stream) {
     g_err[0] = 0;
-    REQ(rows > 0 && H > 0 && H % 8 == 0 && V > 0, DF_ESHAPE, "rows=%d H=%d V=%d (H %% 8 == 0)",
-        rows, H, V);
+    REQ(rows > 0 && rows <= kMaxTcTokens && H > 0 && H % 8 == 0 && V > 0, DF_ESHAPE,
+        "rows=%d (1..%d) H=%d V=%d (H %% 8 == 0)", rows, kMaxTcTokens, H, V);
     DF_TRY(check_bf16(W, "W"));
     DF_TRY(check_f32(X, "X"));
     REQ(idx, DF_EINVAL, "idx is NULL");
@@ -477,6 +501,8 @@ int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, in
     Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
     uint16_t *xp = cv.take<uint16_t>((size_t)2 * rows * H);
     ArgTop *part = cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    TcScratch tc;
+    carve_tc(cv, tc, rows, V);
     cudaStream_t s = (cudaStream_t)stream;
     PackArgs p;
     p.src = X;
@@ -486,7 +512,7 @@ int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, in
     p.T = rows;
     p.K = H;
     DF_TRY(launch_pack(p, s));
-    return lm_head_impl(W, xp, rows, H, V, part, idx, top1, top2, s);
+    return lm_head_impl(W, xp, rows, H, V, part, idx, top1, top2, tc, s);
 }
 
 int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
@@ -571,7 +597,7 @@ int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
     DF_TRY(dflash_forward_impl(cfg, w, cache, nullptr, last_token, target_hidden_new, n_new,
                                n_new_max, B, blk, W.h_final, W.xp_head, W, d_status, s));
     DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
-                        argmax_out, nullptr, nullptr, s));
+                        argmax_out, nullptr, nullptr, W.tc, s));
     return launch_accept(argmax_out + 1, blk, target_argmax, B, K, eos, n_eos, committed,
                          n_committed, accept_count, hit_eos, rollback, target_seq_len, d_status, s);
 }
@@ -725,11 +751,12 @@ int check_mtp_weights(const df_mtp_config *c, const df_mtp_weights *w) {
 
 struct MtpWs {
     float *x, *qkv, *gate, *q, *h1, *cos_t, *sin_t, *part_o, *part_ml, *moe_out, *router_logits;
-    uint16_t *xp_eh, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
+    uint16_t *xp_e, *xp_h, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
     ArgTop *amax_part;
     int32_t *moe_sel;
     float *moe_w;
     AttnArgs plan;
+    TcScratch tc;
 };
 
 void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
@@ -757,7 +784,8 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     w.part_ml = cv.take<float>(pf / (d + 2) * 2);
     w.moe_out = cv.take<float>((size_t)B * H);
     w.router_logits = cv.take<float>((size_t)B * std::max(c->n_experts, 1));
-    w.xp_eh = cv.take<uint16_t>((size_t)2 * B * 2 * H);
+    w.xp_e = cv.take<uint16_t>((size_t)2 * B * H);
+    w.xp_h = cv.take<uint16_t>((size_t)2 * B * H);
     w.xp_attn = cv.take<uint16_t>((size_t)2 * B * H);
     w.xp_o = cv.take<uint16_t>((size_t)2 * B * qt);
     w.xp_ffn = cv.take<uint16_t>((size_t)2 * B * H);
@@ -767,6 +795,10 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * B);
     w.moe_sel = cv.take<int32_t>((size_t)B * std::max(c->top_k, 1));
     w.moe_w = cv.take<float>((size_t)B * std::max(c->top_k, 1));
+    long long rows = std::max<long long>({(long long)c->vocab, 2LL * (long long)I,
+                                          (long long)(qt + 2 * kt), (long long)H,
+                                          (long long)std::max(c->n_experts, 1)});
+    carve_tc(cv, w.tc, B, rows);
 }
 
 }  // namespace
@@ -816,8 +848,8 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         pe.rows_per_seq = 1;
         pe.norm_w = w->enorm;
         pe.eps = 1e-6f;
-        pe.pack = W.xp_eh;
-        pe.ldp = 2 * H;
+        pe.pack = W.xp_e;
+        pe.ldp = H;
         pe.T = B;
         pe.K = H;
         pe.status = d_status;
@@ -827,8 +859,8 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         ph.lds = H;
         ph.norm_w = w->hnorm;
         ph.eps = 1e-6f;
-        ph.pack = W.xp_eh + H;
-        ph.ldp = 2 * H;
+        ph.pack = W.xp_h;
+        ph.ldp = H;
         ph.T = B;
         ph.K = H;
         DF_TRY(launch_pack(ph, s));
@@ -839,13 +871,15 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         ge.K1 = H;
         ge.N = H;
         ge.K = 2 * H;
-        ge.X = W.xp_eh;
-        ge.ldx = 2 * H;
+        ge.X = W.xp_e;
+        ge.ldx = H;
+        ge.X2 = W.xp_h;
+        ge.ldx2 = H;
         ge.T = B;
         ge.epi = EPI_STORE;
         ge.out = W.x;
         ge.ldo = H;
-        DF_TRY(launch_gemm(ge, s));
+        DF_TRY(launch_gemm_tc(ge, W.tc, s));
 
         PackArgs pa;
         pa.src = W.x;
@@ -872,7 +906,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         gq.epi = EPI_STORE;
         gq.out = W.qkv;
         gq.ldo = Nqkv;
-        DF_TRY(launch_gemm(gq, s));
+        DF_TRY(launch_gemm_tc(gq, W.tc, s));
         if (w->w_gate) {
             GemmArgs gg = gq;
             gg.W0 = w->w_gate;
@@ -882,7 +916,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
             gg.N = qt;
             gg.out = W.gate;
             gg.ldo = qt;
-            DF_TRY(launch_gemm(gg, s));
+            DF_TRY(launch_gemm_tc(gg, W.tc, s));
         }
         DF_TRY(launch_rope_table(W.cos_t, W.sin_t, cache->seq_len, nullptr, 0, B, 1, st, rot,
                                  cfg->rope_theta, d_status, s));
@@ -945,7 +979,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         go.ldo = H;
         go.resid = W.x;
         go.ldr = H;
-        DF_TRY(launch_gemm(go, s));
+        DF_TRY(launch_gemm_tc(go, W.tc, s));
         PackArgs pf;
         pf.src = W.h1;
         pf.lds = H;
@@ -969,7 +1003,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         gu.epi = EPI_SWIGLU;
         gu.pack_out = W.xp_act;
         gu.ldpo = I;
-        DF_TRY(launch_gemm(gu, s));
+        DF_TRY(launch_gemm_tc(gu, W.tc, s));
         GemmArgs gd;
         gd.W0 = w->w_down;
         gd.n0 = H;
@@ -983,7 +1017,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         gd.ldo = H;
         gd.resid = W.h1;
         gd.ldr = H;
-        DF_TRY(launch_gemm(gd, s));
+        DF_TRY(launch_gemm_tc(gd, W.tc, s));
         // shared head: rmsnorm(hidden) then lm_head argmax (mtp.rs `forward_shared_head`)
         PackArgs pk;
         pk.src = hid;
@@ -996,7 +1030,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         pk.K = H;
         DF_TRY(launch_pack(pk, s));
         DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B, H, cfg->vocab, W.amax_part,
-                            argmax_out + (size_t)st * B, nullptr, nullptr, s));
+                            argmax_out + (size_t)st * B, nullptr, nullptr, W.tc, s));
         if (logits_out && st == n_steps - 1) {
             GemmArgs gl;
             gl.W0 = w->lm_head;
@@ -1009,7 +1043,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
             gl.epi = EPI_STORE;
             gl.out = logits_out;
             gl.ldo = cfg->vocab;
-            DF_TRY(launch_gemm(gl, s));
+            DF_TRY(launch_gemm_tc(gl, W.tc, s));
         }
     }
     return launch_seq_advance(cache->seq_len, nullptr, B, n_steps, cache->cap, d_status, s);

@@ -144,6 +144,9 @@ struct GemmArgs {
     int N = 0, K = 0;
     const uint16_t *X = nullptr;     // packed activations [2T, ldx]
     int ldx = 0, T = 0;
+    const uint16_t *X2 = nullptr;    // with Wk2: packed activations of columns [K1, K)
+    int ldx2 = 0;
+    int32_t *status = nullptr;
     int epi = EPI_STORE;
     float *out = nullptr;            // EPI_STORE / EPI_RESID: out[t*ldo + n]
     int ldo = 0;
@@ -154,7 +157,23 @@ struct GemmArgs {
     ArgTop *part = nullptr;          // EPI_ARGMAX: partial states [grid, T]
     int *n_part = nullptr;           // EPI_ARGMAX: host-visible count of partial rows written
 };
-int launch_gemm(const GemmArgs &a, cudaStream_t s, int *n_partials_out = nullptr);
+
+// Scratch of the tensor-core projections: partial tiles of tiles shared by several CTAs, and
+// one arrival counter per tile (zero between calls).
+constexpr int kMaxTcTokens = 128;
+struct TcScratch {
+    float *partials = nullptr;
+    size_t partial_floats = 0;
+    int *counters = nullptr;
+    int n_counters = 0;
+    int max_ctas = kNumSMs;
+};
+inline size_t tc_partial_floats(int max_tokens) {
+    int t = max_tokens < kMaxTcTokens ? max_tokens : kMaxTcTokens;
+    return (size_t)kNumSMs * 2 * 128 * (size_t)(t > 0 ? t : 1);
+}
+int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s,
+                   int *n_partials_out = nullptr);
 
 // Reduce EPI_ARGMAX partials [G, T] into idx/top1/top2 [T].
 int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1,

@@ -1,0 +1,708 @@
+// Projections on the 5th-generation tensor cores: y[t, n] = sum_k x[t, k] W[n, k] for BF16
+// weights W [N, K] (row-major) and F32 activations x packed as two BF16 rows per token
+// (hi = bf16(x), lo = bf16(x - hi)), so one kind::f16 MMA with N = 2T columns carries the
+// activations to ~16 mantissa bits and the two columns of a token are summed in F32 in the
+// epilogue.
+//
+//   A (weights, M = 128 rows x K)   TMA, 128-byte swizzle, K-major, 64-wide K blocks
+//   B (packed x, N = 2T rows x K)   TMA, same layout; rows past 2T are zero-filled by TMA
+//   D (F32, 128 lanes x N columns)  TMEM, two accumulators so the epilogue of one tile
+//                                   overlaps the MMAs of the next
+//
+// One persistent CTA per SM, warp-specialised: warp 0 issues TMA loads, warp 1 issues
+// tcgen05.mma (one elected lane) and owns the TMEM allocation, warps 2-5 run the epilogue.
+// Work is split stream-K style: the (tile, K-block) space is cut into equal contiguous ranges,
+// one per CTA, so every SM streams the same number of weight bytes. A tile shared by several
+// CTAs is finished by the last one to arrive, which sums the partial tiles in CTA order (the
+// result does not depend on arrival order).
+//
+// Epilogues: plain store, residual add, SwiGLU (gate rows 0-63 and up rows 64-127 of a tile
+// come from the two weight matrices; silu(g) * u is re-packed hi/lo for the down projection),
+// and a running argmax per token over lm_head rows (logits never leave the SM).
+//
+// Projections of hf2q 0.1.1 spec_decode/dflash/tensors.rs (`DFlashLayerTensors`: BF16
+// row-major [out, in] weights, F32 activations) and models/qwen35/mtp.rs
+// (`apply_linear_projection_f32`, `forward_shared_head`).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "df_internal.cuh"
+
+namespace df {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBK = 64;                    // BF16 elements per K block: one 128-byte row
+constexpr int kABytes = kBM * kBK * 2;     // 16 KB
+constexpr int kTokChunk = 8;               // tokens per TMEM load (16 columns)
+constexpr long long kTimeoutCycles = 4000000000LL;   // ~2 s at 2 GHz
+
+struct TcParams {
+    CUtensorMap amap[4];
+    CUtensorMap bmap[2];
+    int n_seg;
+    int seg_rows[4];
+    int seg_tile0[5];
+    int seg_col0[4];
+    int k_seg;
+    int kb_seg0;
+    int kbt;
+    int pair;
+    int T, NC, acc_cols, alloc_cols;
+    int n_tiles, G, stages;
+    long long total_kb;
+    uint32_t stage_bytes;
+    uint32_t idesc;
+    int epi;
+    int N;
+    float *out;
+    int ldo;
+    const float *resid;
+    int ldr;
+    uint16_t *pack_out;
+    int ldpo;
+    ArgTop *part;
+    float *scratch;
+    int *counters;
+    int32_t *status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a barrier phase. Gives up (returns false) when another role has aborted or
+// after kTimeoutCycles, in which case it raises the CTA's abort flag and DF_ETIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
+    long long t0 = clock64();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kTimeoutCycles) {
+                *abort_flag = 1;
+                set_status(status, DF_ETIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while tearing down after an abort (ignores the abort flag).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kTimeoutCycles) return;
+    }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
+                                            int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// OR of a predicate over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ bool epi_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// Shared-memory matrix descriptor: K-major operand stored as 128-byte rows, 128-byte swizzle,
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;              // leading-dimension offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride between 8-row groups
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+// ------------------------------------------------------------------ work split
+__device__ __forceinline__ long long kb_start(long long c, const TcParams &p) {
+    return c * p.total_kb / p.G;
+}
+
+__device__ __forceinline__ int cta_of(long long x, const TcParams &p) {
+    return (int)(((x + 1) * (long long)p.G - 1) / p.total_kb);
+}
+
+__device__ __forceinline__ int seg_of_tile(int m, const TcParams &p) {
+    int s = 0;
+    while (s + 1 < p.n_seg && m >= p.seg_tile0[s + 1]) ++s;
+    return s;
+}
+
+// Output row and validity of tile row r.
+__device__ __forceinline__ bool tile_row(const TcParams &p, int m, int r, int &n_out, int &s) {
+    if (p.pair) {
+        s = 0;
+        n_out = m * 64 + (r & 63);
+        return n_out < p.seg_rows[0];
+    }
+    s = seg_of_tile(m, p);
+    int local = (m - p.seg_tile0[s]) * kBM + r;
+    n_out = p.seg_col0[s] + local;
+    return local < p.seg_rows[s];
+}
+
+// ------------------------------------------------------------------ epilogue
+struct EpiSmem {
+    float *xs;      // [128][kTokChunk]
+    ArgTop *wst;    // [4][kTokChunk]
+    ArgTop *st;     // [T]
+};
+
+// Apply the epilogue op to tokens [t0, t0 + kTokChunk) of tile m for this thread's row r.
+// Every epilogue thread calls this (the SwiGLU and argmax paths synchronise the 128 threads).
+__device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, int m, int r,
+                                          int q, int lane, int t0, const float (&y)[kTokChunk]) {
+    int n_out, s;
+    const bool valid = tile_row(p, m, r, n_out, s);
+    if (p.epi == EPI_STORE || p.epi == EPI_RESID) {
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < kTokChunk; ++i) {
+                int t = t0 + i;
+                if (t < p.T) {
+                    float v = y[i];
+                    if (p.epi == EPI_RESID) v += p.resid[(size_t)t * p.ldr + n_out];
+                    p.out[(size_t)t * p.ldo + n_out] = v;
+                }
+            }
+        }
+    } else if (p.epi == EPI_SWIGLU) {
+#pragma unroll
+        for (int i = 0; i < kTokChunk; ++i) es.xs[r * kTokChunk + i] = y[i];
+        epi_bar();
+        if (r < 64 && valid) {
+#pragma unroll
+            for (int i = 0; i < kTokChunk; ++i) {
+                int t = t0 + i;
+                if (t < p.T) {
+                    float g = es.xs[r * kTokChunk + i];
+                    float u = es.xs[(r + 64) * kTokChunk + i];
+                    float act = g / (1.f + expf(-g)) * u;
+                    uint16_t hi, lo;
+                    split_hi_lo(act, hi, lo);
+                    p.pack_out[(size_t)(2 * t) * p.ldpo + n_out] = hi;
+                    p.pack_out[(size_t)(2 * t + 1) * p.ldpo + n_out] = lo;
+                }
+            }
+        }
+        epi_bar();
+    } else {   // EPI_ARGMAX
+#pragma unroll
+        for (int i = 0; i < kTokChunk; ++i) {
+            ArgTop a = valid ? ArgTop{y[i], n_out, -INFINITY} : argtop_empty(0x7fffffff);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                ArgTop b;
+                b.v1 = __shfl_xor_sync(0xffffffffu, a.v1, o);
+                b.i1 = __shfl_xor_sync(0xffffffffu, a.i1, o);
+                b.v2 = __shfl_xor_sync(0xffffffffu, a.v2, o);
+                a = argtop_merge(a, b);
+            }
+            if (lane == 0) es.wst[q * kTokChunk + i] = a;
+        }
+        epi_bar();
+        const int tid = r;   // any distinct id in [0, 128)
+        if (tid < kTokChunk && t0 + tid < p.T) {
+            ArgTop acc = es.st[t0 + tid];
+            for (int w = 0; w < 4; ++w) acc = argtop_merge(acc, es.wst[w * kTokChunk + tid]);
+            es.st[t0 + tid] = acc;
+        }
+        epi_bar();
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *stage_base = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)p.stages * p.stage_bytes);
+    uint64_t *empty = full + p.stages;
+    uint64_t *tfull = empty + p.stages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *s_last = reinterpret_cast<int *>(tmem_slot + 2);
+    EpiSmem es;
+    es.xs = reinterpret_cast<float *>(tmem_slot + 4);
+    es.wst = reinterpret_cast<ArgTop *>(es.xs + kBM * kTokChunk);
+    es.st = es.wst + 4 * kTokChunk;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, p.alloc_cols);
+        tmem_relinquish();
+    }
+    if (warp >= 2) {
+        for (int t = threadIdx.x - 64; t < p.T; t += 128) es.st[t] = argtop_empty(0x7fffffff);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const long long my_begin = kb_start(blockIdx.x, p), my_end = kb_start(blockIdx.x + 1, p);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (long long x = my_begin; x < my_end && ok;) {
+                const int m = (int)(x / p.kbt);
+                const int k0 = (int)(x - (long long)m * p.kbt);
+                const int k1 = (int)min((long long)p.kbt, my_end - (long long)m * p.kbt);
+                x = (long long)m * p.kbt + k1;
+                int s = 0, row0 = 0;
+                if (!p.pair) {
+                    s = seg_of_tile(m, p);
+                    row0 = (m - p.seg_tile0[s]) * kBM;
+                }
+                for (int kb = k0; kb < k1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full[stage], p.stage_bytes);
+                    uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
+                    uint8_t *b = a + kABytes;
+                    const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
+                    const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
+                    if (p.pair) {
+                        tma_load_2d(a, &p.amap[0], &full[stage], kx, m * 64, pol_w);
+                        tma_load_2d(a + kABytes / 2, &p.amap[1], &full[stage], kx, m * 64, pol_w);
+                    } else {
+                        tma_load_2d(a, &p.amap[ks ? 1 : s], &full[stage], kx, row0, pol_w);
+                    }
+                    tma_load_2d(b, &p.bmap[ks], &full[stage], kx, 0, pol_x);
+                    ++issued;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every load already issued land before the CTA can exit.
+                long long first = issued > p.stages ? issued - p.stages : 0;
+                for (long long j = first; j < issued; ++j)
+                    mbar_drain(&full[j % p.stages], (uint32_t)((j / p.stages) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (long long x = my_begin; x < my_end && ok;) {
+                const int m = (int)(x / p.kbt);
+                const int k0 = (int)(x - (long long)m * p.kbt);
+                const int k1 = (int)min((long long)p.kbt, my_end - (long long)m * p.kbt);
+                x = (long long)m * p.kbt + k1;
+                if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * p.acc_cols);
+                for (int kb = k0; kb < k1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(stage_base + (size_t)stage * p.stage_bytes);
+                    const uint64_t adesc = sw128_desc(a_addr);
+                    const uint64_t bdesc = sw128_desc(a_addr + kABytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // advance 16 BF16 (32 bytes) along K inside the swizzled 128-byte row
+                        mma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), p.idesc,
+                                 (kb > k0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aphase ^= 1u;
+                }
+            }
+            // Every MMA this thread issued has completed once the drain barrier flips.
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        const int q = warp & 3;          // TMEM lane quadrant this warp may access
+        const int r = q * 32 + lane;     // tile row of this thread
+        int acc = 0;
+        uint32_t aphase = 0;
+        for (long long x = my_begin; x < my_end;) {
+            const int m = (int)(x / p.kbt);
+            const int k0 = (int)(x - (long long)m * p.kbt);
+            const int k1 = (int)min((long long)p.kbt, my_end - (long long)m * p.kbt);
+            x = (long long)m * p.kbt + k1;
+            const bool whole = (k0 == 0 && k1 == p.kbt);
+            const int slot = (kb_start(blockIdx.x, p) / p.kbt == m) ? 0 : 1;
+            const bool got = mbar_wait(&tfull[acc], aphase, abort_flag, p.status);
+            if (epi_any(!got)) break;   // all four epilogue warps leave together
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.acc_cols);
+            const int n_chunks = (p.T + kTokChunk - 1) / kTokChunk;
+            float *slot_base = p.scratch + ((size_t)blockIdx.x * 2 + slot) * (size_t)p.T * kBM;
+            for (int c = 0; c < n_chunks; ++c) {
+                uint32_t v[16];
+                tmem_ld16(taddr + (uint32_t)(c * 2 * kTokChunk), v);
+                if (c == n_chunks - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                }
+                float y[kTokChunk];
+#pragma unroll
+                for (int i = 0; i < kTokChunk; ++i)
+                    y[i] = __uint_as_float(v[2 * i]) + __uint_as_float(v[2 * i + 1]);
+                if (whole) {
+                    epi_apply(p, es, m, r, q, lane, c * kTokChunk, y);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTokChunk; ++i) {
+                        int t = c * kTokChunk + i;
+                        if (t < p.T) slot_base[(size_t)t * kBM + r] = y[i];
+                    }
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+            if (!whole) {
+                // Stream-K fixup: the last CTA of this tile sums the partials in CTA order.
+                __threadfence();
+                epi_bar();
+                const long long lo = (long long)m * p.kbt, hi = lo + p.kbt - 1;
+                const int c_lo = cta_of(lo, p), c_hi = cta_of(hi, p);
+                if (r == 0) {
+                    int prev = atomicAdd(&p.counters[m], 1);
+                    *s_last = (prev == c_hi - c_lo) ? 1 : 0;
+                }
+                epi_bar();
+                const int last = *s_last;
+                epi_bar();
+                if (last) {
+                    __threadfence();
+                    for (int c = 0; c < n_chunks; ++c) {
+                        float y[kTokChunk];
+#pragma unroll
+                        for (int i = 0; i < kTokChunk; ++i) y[i] = 0.f;
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
+                            const int sl = (kb_start(cc, p) / p.kbt == m) ? 0 : 1;
+                            const float *src = p.scratch + ((size_t)cc * 2 + sl) * (size_t)p.T * kBM;
+#pragma unroll
+                            for (int i = 0; i < kTokChunk; ++i) {
+                                int t = c * kTokChunk + i;
+                                if (t < p.T) y[i] += __ldcg(src + (size_t)t * kBM + r);
+                            }
+                        }
+                        epi_apply(p, es, m, r, q, lane, c * kTokChunk, y);
+                    }
+                    if (r == 0) p.counters[m] = 0;
+                }
+            }
+        }
+        if (p.epi == EPI_ARGMAX) {
+            epi_bar();
+            for (int t = threadIdx.x - 64; t < p.T; t += 128)
+                p.part[(size_t)blockIdx.x * p.T + t] = es.st[t];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.alloc_cols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encode() {
+    if (g_encode) return DF_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(DF_ECUDA, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return DF_OK;
+}
+
+// 2-D BF16 map over rows x cols (row stride ld elements), box box_cols x box_rows, 128B swizzle.
+int make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
+             uint32_t box_cols, uint32_t box_rows) {
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (ld * 2) % 16 != 0)
+        return fail(DF_EINVAL, "TMA operand misaligned (base %p, row stride %llu elements)", base,
+                    (unsigned long long)ld);
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DF_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return DF_OK;
+}
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_out) {
+    DF_TRY(get_encode());
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    const int T = a.T;
+    int NC = ((2 * T + 15) / 16) * 16;
+    if (NC < 16) NC = 16;
+    p.T = T;
+    p.NC = NC;
+    int alloc = 32;
+    while (alloc < 2 * NC) alloc <<= 1;
+    p.alloc_cols = alloc;
+    p.acc_cols = alloc / 2;          // each accumulator starts on a power-of-two column
+    p.pair = a.epi == EPI_SWIGLU;
+    p.k_seg = a.Wk2 ? 2 : 1;
+    const int K0 = a.Wk2 ? a.K1 : a.K;
+    const int K1 = a.K - K0;
+    p.kb_seg0 = ceil_div(K0, kBK);
+    p.kbt = p.kb_seg0 + (a.Wk2 ? ceil_div(K1, kBK) : 0);
+    if (p.pair) {
+        p.n_seg = 1;
+        p.seg_rows[0] = a.N;
+        p.n_tiles = ceil_div(a.N, 64);
+        DF_TRY(make_map(&p.amap[0], a.W0, a.K, a.N, a.K, kBK, 64));
+        DF_TRY(make_map(&p.amap[1], a.W1, a.K, a.N, a.K, kBK, 64));
+    } else if (a.Wk2) {
+        p.n_seg = 1;
+        p.seg_rows[0] = a.n0;
+        p.seg_tile0[0] = 0;
+        p.seg_col0[0] = 0;
+        p.n_tiles = ceil_div(a.n0, kBM);
+        DF_TRY(make_map(&p.amap[0], a.W0, K0, a.n0, K0, kBK, kBM));
+        DF_TRY(make_map(&p.amap[1], a.Wk2, K1, a.n0, K1, kBK, kBM));
+    } else {
+        const uint16_t *W[3] = {a.W0, a.W1, a.W2};
+        const int rows[3] = {a.n0, a.n1, a.n2};
+        int tiles = 0, col = 0, ns = 0;
+        for (int i = 0; i < 3; ++i) {
+            if (rows[i] <= 0 || W[i] == nullptr) continue;
+            p.seg_rows[ns] = rows[i];
+            p.seg_tile0[ns] = tiles;
+            p.seg_col0[ns] = col;
+            DF_TRY(make_map(&p.amap[ns], W[i], a.K, rows[i], a.K, kBK, kBM));
+            tiles += ceil_div(rows[i], kBM);
+            col += rows[i];
+            ++ns;
+        }
+        p.n_seg = ns;
+        p.n_tiles = tiles;
+    }
+    p.seg_tile0[p.n_seg] = p.n_tiles;
+    DF_TRY(make_map(&p.bmap[0], a.X, K0, 2 * T, a.ldx, kBK, NC));
+    if (a.Wk2) DF_TRY(make_map(&p.bmap[1], a.X2, K1, 2 * T, a.ldx2, kBK, NC));
+    p.total_kb = (long long)p.n_tiles * p.kbt;
+    p.G = (int)std::min<long long>(sc.max_ctas, p.total_kb);
+    p.stage_bytes = kABytes + NC * 128;
+    p.stages = std::min(8, (int)((200 * 1024) / p.stage_bytes));
+    p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NC >> 3) << 17) |
+              ((uint32_t)(kBM >> 4) << 24);
+    p.epi = a.epi;
+    p.N = a.N;
+    p.out = a.out;
+    p.ldo = a.ldo;
+    p.resid = a.resid;
+    p.ldr = a.ldr;
+    p.pack_out = a.pack_out;
+    p.ldpo = a.ldpo;
+    p.part = a.part;
+    p.scratch = sc.partials;
+    p.counters = sc.counters;
+    p.status = a.status;
+    if ((size_t)p.G * 2 * T * kBM > sc.partial_floats)
+        return fail(DF_EWORKSPACE, "GEMM scratch too small (%d tokens)", T);
+    if (p.n_tiles > sc.n_counters)
+        return fail(DF_EWORKSPACE, "GEMM tile counters too few (%d tiles)", p.n_tiles);
+    size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 5) * 8 + 16 +
+                  (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
+                  (size_t)T * sizeof(ArgTop) + 64;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    if (G_out) *G_out = p.G;
+    gemm_tc_kernel<<<p.G, kThreads, smem, s>>>(p);
+    return cuda_check("gemm_tc_kernel");
+}
+
+}  // namespace
+
+int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *n_partials_out) {
+    if (a.N <= 0 || a.T <= 0) {
+        if (n_partials_out) *n_partials_out = 0;
+        return DF_OK;
+    }
+    if (a.T <= kMaxTcTokens) return launch_chunk(a, sc, s, n_partials_out);
+    if (a.epi == EPI_ARGMAX) return fail(DF_ESHAPE, "argmax over more than %d rows", kMaxTcTokens);
+    for (int t0 = 0; t0 < a.T; t0 += kMaxTcTokens) {
+        GemmArgs c = a;
+        c.T = std::min(kMaxTcTokens, a.T - t0);
+        c.X = a.X + (size_t)2 * t0 * a.ldx;
+        if (a.X2) c.X2 = a.X2 + (size_t)2 * t0 * a.ldx2;
+        if (a.out) c.out = a.out + (size_t)t0 * a.ldo;
+        if (a.resid) c.resid = a.resid + (size_t)t0 * a.ldr;
+        if (a.pack_out) c.pack_out = a.pack_out + (size_t)2 * t0 * a.ldpo;
+        DF_TRY(launch_chunk(c, sc, s, nullptr));
+    }
+    return DF_OK;
+}
+
+}  // namespace df
