@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--profile-case", choices=["lm_head", "round"], default=None,
+                    help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
 
 
@@ -435,8 +437,39 @@ def run_reference(args, rank, world):
     }
 
 
+def profile_case(args):
+    """A small, self-contained case for ncu: the full-size lm_head argmax (1.48 GB of weights,
+    larger than L2) over the 16 block rows, 2 warm-up launches then 3 profiled ones; or one
+    eager round of the workload."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+    s = DFLASH_K15
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    if args.profile_case == "lm_head":
+        W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
+        X = torch.randn((s.block, s.hidden), generator=g, device=dev)
+        idx = torch.empty(s.block, dtype=torch.int32, device=dev)
+        ws = B.alloc_workspace(B.lm_head_workspace_bytes(s.block, s.hidden, s.vocab), dev)
+        for _ in range(5):
+            B.lm_head_argmax(W, X, idx, ws=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "lm_head", "idx0": int(idx[0])}))
+    else:
+        args.no_graph = True
+        args.skip_cpu = True
+        args.steps, args.warmup = 1, 1
+        run_native(args, 0, 1, 0)
+        print(json.dumps({"profile_case": "round"}))
+
+
 def main():
     args = parse()
+    if args.profile_case:
+        profile_case(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
