@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["lm_head", "round"], default=None,
+    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms"], default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
 
@@ -457,6 +457,32 @@ def profile_case(args):
             B.lm_head_argmax(W, X, idx, ws=ws)
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": "lm_head", "idx0": int(idx[0])}))
+    elif args.profile_case == "gemms":
+        # Every projection shape of one drafter layer (+ fc) timed alone with CUDA events.
+        H, I, qt, kt = s.hidden, s.intermediate, s.q_total, s.kv_total
+        shapes = [("fc", 16, H, s.fc_in), ("qkv", 32, qt + 2 * kt, H), ("o", 16, H, qt),
+                  ("gate_up", 16, 2 * I, H), ("down", 16, H, I), ("lm_head_store", 16, s.vocab, H)]
+        res = {}
+        for name, T, N, K in shapes:
+            W = (torch.randn((N, K), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
+            X = torch.randn((T, K), generator=g, device=dev)
+            Y = torch.empty((T, N), device=dev)
+            ws = B.alloc_workspace(B.linear_workspace_bytes(T, N, K), dev)
+            for _ in range(3):
+                B.df_linear(W, X, Y, ws)
+            evs = []
+            for _ in range(20):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                B.df_linear(W, X, Y, ws)
+                e1.record()
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+            res[name] = {"T": T, "N": N, "K": K, "us": round(us, 2),
+                         "weight_gbs": round(N * K * 2 / us / 1e3, 1)}
+            del W, X, Y, ws
+        print(json.dumps({"profile_case": "gemms", "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count, **res}))
     else:
         args.no_graph = True
         args.skip_cpu = True

@@ -161,6 +161,17 @@ int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, in
                    float *top1, float *top2, void *ws, size_t ws_bytes, df_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * One BF16-weight x F32-activation projection (mtp.rs `apply_linear_projection_f32`;
+ * tensors.rs: row-major [out, in] BF16 weights consumed with F32 activations):
+ *   Y[t, n] = sum_k X[t, k] * W[n, k],  W device BF16 [N, K], X device F32 [T, K],
+ *   Y device F32 [T, N]; K a multiple of 8. F32 accumulation.
+ * ---------------------------------------------------------------------------------------- */
+size_t df_linear_workspace_bytes(int T, int N, int K);
+
+int df_linear(const uint16_t *W, const float *X, int T, int N, int K, float *Y, void *ws,
+              size_t ws_bytes, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Greedy accept walk (qwen35_orchestrator.rs module doc "Greedy accept-walk consistency
  * invariant" and steps 7-9: `step_round_from_argmaxes`, rollback = K - accept_count).
  * ---------------------------------------------------------------------------------------- */

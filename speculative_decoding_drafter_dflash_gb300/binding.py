@@ -81,6 +81,9 @@ _SIGS = [
     ("df_lm_head_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
     ("lm_head_argmax", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
+    ("df_linear_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
+    ("df_linear", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
+                          c_void_p]),
     ("accept_prefix_argmax", c_int, [c_void_p, c_int, c_void_p, c_int, c_int, c_void_p, c_int,
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("accept_prefix_argmax_host", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p,
@@ -207,6 +210,16 @@ def lm_head_argmax(W, X, idx, top1=None, top2=None, ws=None, stream=None):
     V = W.shape[0]
     _check(lib().lm_head_argmax(_p(W), _p(X), rows, H, V, _p(idx), _p(top1), _p(top2), _p(ws),
                                 ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def linear_workspace_bytes(T: int, N: int, K: int) -> int:
+    return int(lib().df_linear_workspace_bytes(T, N, K))
+
+
+def df_linear(W, X, Y, ws, stream=None):
+    T, K = X.shape
+    N = W.shape[0]
+    _check(lib().df_linear(_p(W), _p(X), T, N, K, _p(Y), _p(ws), ws.numel(), _stream(stream)))
 
 
 def accept_prefix_argmax(drafts, drafts_ld: int, target, K: int, eos, committed, n_committed,

@@ -120,7 +120,8 @@ int check_cache(const df_kv_cache *k, int n_layers, int B, int d) {
 
 // ---------------------------------------------------------------- DFlash workspace
 struct DFlashWs {
-    float *h, *hctx, *qkv, *q, *kb, *vb, *cos_t, *sin_t, *part_o, *part_ml, *h_final;
+    float *h, *hctx, *qkv, *q, *kb, *vb, *cos_t, *sin_t, *attn_part, *h_final;
+    int *attn_counters;
     uint16_t *xp_ctx, *xp_qkv, *xp_o, *xp_ffn, *xp_act, *xp_head;
     ArgTop *amax_part;
     int32_t *idx;
@@ -159,9 +160,8 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     w.plan.nkv = nkv;
     w.plan.d = d;
     attn_plan(w.plan, cap + blk);
-    size_t pf = attn_part_floats(B, nkv, w.plan.n_groups, w.plan.n_chunks, w.plan.rows_per_group, d);
-    w.part_o = cv.take<float>(pf);
-    w.part_ml = cv.take<float>(pf / (d + 2) * 2);
+    w.attn_part = cv.take<float>(attn_part_floats(w.plan));
+    w.attn_counters = cv.take<int>((size_t)B * nkv);
     w.xp_ctx = cv.take<uint16_t>(2 * std::max<size_t>(T_ctx, 1) * fc_in);
     w.xp_qkv = cv.take<uint16_t>(2 * T_all * H);
     w.xp_o = cv.take<uint16_t>(2 * T_blk * qt);
@@ -330,8 +330,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         at.n_new_max = n_new_max;
         at.extra_rows = 0;
         at.causal_block = c->causal_block;
-        at.part_o = ws.part_o;
-        at.part_ml = ws.part_ml;
+        at.part = ws.attn_part;
+        at.counters = ws.attn_counters;
         at.gate = nullptr;
         at.ldg = 0;
         at.pack = ws.xp_o;
@@ -513,6 +513,50 @@ int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, in
     p.K = H;
     DF_TRY(launch_pack(p, s));
     return lm_head_impl(W, xp, rows, H, V, part, idx, top1, top2, tc, s);
+}
+
+size_t df_linear_workspace_bytes(int T, int N, int K) {
+    if (T <= 0 || N <= 0 || K <= 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    cv.take<uint16_t>((size_t)2 * T * K);
+    TcScratch tc;
+    carve_tc(cv, tc, T, N);
+    return cv.off;
+}
+
+int df_linear(const uint16_t *W, const float *X, int T, int N, int K, float *Y, void *ws,
+              size_t ws_bytes, df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(T > 0 && N > 0 && K > 0 && K % 8 == 0, DF_ESHAPE, "T=%d N=%d K=%d (K %% 8 == 0)", T, N, K);
+    DF_TRY(check_bf16(W, "W"));
+    DF_TRY(check_f32(X, "X"));
+    DF_TRY(check_f32(Y, "Y"));
+    DF_TRY(get_ws(ws, ws_bytes, df_linear_workspace_bytes(T, N, K)));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    uint16_t *xp = cv.take<uint16_t>((size_t)2 * T * K);
+    TcScratch tc;
+    carve_tc(cv, tc, T, N);
+    cudaStream_t s = (cudaStream_t)stream;
+    PackArgs p;
+    p.src = X;
+    p.lds = K;
+    p.pack = xp;
+    p.ldp = K;
+    p.T = T;
+    p.K = K;
+    DF_TRY(launch_pack(p, s));
+    GemmArgs g;
+    g.W0 = W;
+    g.n0 = N;
+    g.N = N;
+    g.K = K;
+    g.X = xp;
+    g.ldx = K;
+    g.T = T;
+    g.epi = EPI_STORE;
+    g.out = Y;
+    g.ldo = N;
+    return launch_gemm_tc(g, tc, s);
 }
 
 int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
@@ -750,7 +794,8 @@ int check_mtp_weights(const df_mtp_config *c, const df_mtp_weights *w) {
 }
 
 struct MtpWs {
-    float *x, *qkv, *gate, *q, *h1, *cos_t, *sin_t, *part_o, *part_ml, *moe_out, *router_logits;
+    float *x, *qkv, *gate, *q, *h1, *cos_t, *sin_t, *attn_part, *moe_out, *router_logits;
+    int *attn_counters;
     uint16_t *xp_e, *xp_h, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
     ArgTop *amax_part;
     int32_t *moe_sel;
@@ -779,9 +824,8 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     w.plan.nkv = nkv;
     w.plan.d = d;
     attn_plan(w.plan, cap);
-    size_t pf = attn_part_floats(B, nkv, w.plan.n_groups, w.plan.n_chunks, w.plan.rows_per_group, d);
-    w.part_o = cv.take<float>(pf);
-    w.part_ml = cv.take<float>(pf / (d + 2) * 2);
+    w.attn_part = cv.take<float>(attn_part_floats(w.plan));
+    w.attn_counters = cv.take<int>((size_t)B * nkv);
     w.moe_out = cv.take<float>((size_t)B * H);
     w.router_logits = cv.take<float>((size_t)B * std::max(c->n_experts, 1));
     w.xp_e = cv.take<uint16_t>((size_t)2 * B * H);
@@ -959,8 +1003,8 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         at.n_new_max = 0;
         at.extra_rows = st + 1;
         at.causal_block = 0;
-        at.part_o = W.part_o;
-        at.part_ml = W.part_ml;
+        at.part = W.attn_part;
+        at.counters = W.attn_counters;
         at.gate = w->w_gate ? W.gate : nullptr;
         at.ldg = qt;
         at.pack = W.xp_o;

@@ -215,16 +215,16 @@ struct AttnArgs {
     int n_new_max;
     int extra_rows;          // rows beyond seq_len + n_new that are visible (MTP: step + 1)
     int causal_block;
-    float *part_o, *part_ml; // workspace partials
-    int n_chunks, chunk, rows_per_group, n_groups;
-    // combine
+    float *part;             // [B, nkv, n_chunks, R, d + 2] per-CTA partial (o, m, l)
+    int *counters;           // [B * nkv] arrival counters, zero between calls
+    int n_chunks, chunk;     // key chunks per (sequence, KV head); keys per chunk
     const float *gate;       // optional [B*blk, ldg] gate pre-activation (q_total wide)
     int ldg;
     uint16_t *pack;          // packed output [2*B*blk, nq*d]
     int32_t *status;
 };
 void attn_plan(AttnArgs &a, int max_keys);
-size_t attn_part_floats(int B, int nkv, int n_groups, int n_chunks, int rows_per_group, int d);
+size_t attn_part_floats(const AttnArgs &a);
 int launch_attn(const AttnArgs &a, cudaStream_t s);
 
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,

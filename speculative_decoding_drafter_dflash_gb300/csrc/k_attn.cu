@@ -9,6 +9,8 @@
 // `DFlashLayerTensors::q_norm/k_norm`; the context rows of qwen35_orchestrator.rs step 3.
 #include <math.h>
 
+#include <algorithm>
+
 #include "df_internal.cuh"
 
 namespace df {
@@ -132,215 +134,286 @@ __global__ void qk_rope_kernel(QkArgs a) {
 }
 
 constexpr int kAttnThreads = 256;
-constexpr int kKeyTile = 32;
-constexpr int kMaxOut = 16;      // outputs per thread: rows_per_group * d <= 256 * 16
+constexpr int kAttnStages = 4;
+constexpr int kTileBytes = 32768;          // K + V bytes of one key tile
+constexpr int kKeyGroup = 8;               // keys per online-softmax update
 
-// Split-KV partial attention. Grid (n_chunks, nkv * n_groups, B). Key index space of a
-// sequence: cache rows [0, S_cache) then block keys [S_cache, S_cache + blk).
-__global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(AttnArgs a) {
-    extern __shared__ float sm[];
-    const int d = a.d, dp = d + 4;
-    const int R = a.rows_per_group;
-    const int rep = a.nq / a.nkv;
-    const int chunk = blockIdx.x;
-    const int g = blockIdx.y / a.n_groups, grp = blockIdx.y % a.n_groups;
-    const int b = blockIdx.z;
-    const int rows_total = a.blk * rep;
-    const int r0 = grp * R;
-    const int nr = min(R, rows_total - r0);
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 
-    float *q_s = sm;                        // [R][dp]
-    float *k_s = q_s + R * dp;              // [kKeyTile][dp]
-    float *v_s = k_s + kKeyTile * dp;       // [kKeyTile][dp]
-    float *p_s = v_s + kKeyTile * dp;       // [R][kKeyTile + 1]
-    float *m_s = p_s + R * (kKeyTile + 1);  // [R]
-    float *l_s = m_s + R;                   // [R]
-    float *c_s = l_s + R;                   // [R]
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
 
-    int nn = a.n_new ? min(max(a.n_new[b], 0), a.n_new_max) : 0;
-    long long sc = (long long)a.seq_len[b] + nn + a.extra_rows;
-    const int S_cache = (int)min(max(sc, 0LL), (long long)a.cap);
-    const int S = S_cache + (a.kb ? a.blk : 0);
-    const int k_begin = chunk * a.chunk;
-    const int k_end = min(S, k_begin + a.chunk);
-
-    // query rows of this group: row r -> block token i = r / rep, q head g*rep + r % rep
-    for (int idx = threadIdx.x; idx < nr * d; idx += blockDim.x) {
-        int r = idx / d, e = idx % d;
-        int rr = r0 + r;
-        int i = rr / rep, h = g * rep + rr % rep;
-        q_s[r * dp + e] = a.q[(((size_t)b * a.blk + i) * a.nq + h) * d + e];
-    }
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-        m_s[r] = -INFINITY;
-        l_s[r] = 0.f;
-    }
-    float o[kMaxOut];
-#pragma unroll
-    for (int u = 0; u < kMaxOut; ++u) o[u] = 0.f;
-    const float scale = 1.f / sqrtf((float)d);
-    __syncthreads();
-
-    for (int kt = k_begin; kt < k_end; kt += kKeyTile) {
-        const int nk = min(kKeyTile, k_end - kt);
-        for (int idx = threadIdx.x; idx < kKeyTile * (d / 4); idx += blockDim.x) {
-            int kk = idx / (d / 4), e4 = (idx % (d / 4)) * 4;
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (kk < nk) {
-                int s = kt + kk;
-                const float *kp, *vp;
-                if (s < S_cache) {
-                    size_t off = (((size_t)b * a.nkv + g) * a.cap + s) * d + e4;
-                    kp = a.cache_k + off;
-                    vp = a.cache_v + off;
-                } else {
-                    size_t off = (((size_t)b * a.nkv + g) * a.blk + (s - S_cache)) * d + e4;
-                    kp = a.kb + off;
-                    vp = a.vb + off;
-                }
-                kv = *reinterpret_cast<const float4 *>(kp);
-                vv = *reinterpret_cast<const float4 *>(vp);
-            }
-            *reinterpret_cast<float4 *>(k_s + kk * dp + e4) = kv;
-            *reinterpret_cast<float4 *>(v_s + kk * dp + e4) = vv;
+// Bounded wait for a phase of an mbarrier (~2 s); on timeout DF_ETIMEOUT is raised and the
+// caller continues with whatever the buffer holds (results are then invalid, nothing hangs).
+__device__ __forceinline__ void attn_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
+    const long long t0 = clock64();
+    uint32_t ok = 0;
+    while (true) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return;
+        if (clock64() - t0 > 4000000000LL) {
+            set_status(status, DF_ETIMEOUT);
+            return;
         }
-        __syncthreads();
-        // scores
-        for (int idx = threadIdx.x; idx < nr * kKeyTile; idx += blockDim.x) {
-            int r = idx / kKeyTile, kk = idx % kKeyTile;
-            float sc2 = -INFINITY;
-            if (kk < nk) {
-                const float *qr = q_s + r * dp;
-                const float *kr = k_s + kk * dp;
-                float acc = 0.f;
-                for (int e = 0; e < d; e += 4) {
-                    float4 qa = *reinterpret_cast<const float4 *>(qr + e);
-                    float4 ka = *reinterpret_cast<const float4 *>(kr + e);
-                    acc = fmaf(qa.x, ka.x, acc);
-                    acc = fmaf(qa.y, ka.y, acc);
-                    acc = fmaf(qa.z, ka.z, acc);
-                    acc = fmaf(qa.w, ka.w, acc);
-                }
-                sc2 = acc * scale;
-                int s = kt + kk;
-                if (a.causal_block && s >= S_cache) {
-                    int i = (r0 + r) / rep;
-                    if (s - S_cache > i) sc2 = -INFINITY;
-                }
-            }
-            p_s[r * (kKeyTile + 1) + kk] = sc2;
-        }
-        __syncthreads();
-        // online softmax update, one thread per row
-        for (int r = threadIdx.x; r < nr; r += blockDim.x) {
-            float mo = m_s[r];
-            float mx = mo;
-            for (int kk = 0; kk < kKeyTile; ++kk) mx = fmaxf(mx, p_s[r * (kKeyTile + 1) + kk]);
-            float corr = 1.f, sum = 0.f;
-            if (mx == -INFINITY) {
-                for (int kk = 0; kk < kKeyTile; ++kk) p_s[r * (kKeyTile + 1) + kk] = 0.f;
-            } else {
-                corr = (mo == -INFINITY) ? 0.f : expf(mo - mx);
-                for (int kk = 0; kk < kKeyTile; ++kk) {
-                    float v = p_s[r * (kKeyTile + 1) + kk];
-                    float p = (v == -INFINITY) ? 0.f : expf(v - mx);
-                    p_s[r * (kKeyTile + 1) + kk] = p;
-                    sum += p;
-                }
-            }
-            m_s[r] = mx;
-            l_s[r] = l_s[r] * corr + sum;
-            c_s[r] = corr;
-        }
-        __syncthreads();
-        // o = o * corr + P V
-#pragma unroll
-        for (int u = 0; u < kMaxOut; ++u) {
-            int idx = threadIdx.x + u * blockDim.x;
-            if (idx < nr * d) {
-                int r = idx / d, e = idx % d;
-                float acc = o[u] * c_s[r];
-                const float *pr = p_s + r * (kKeyTile + 1);
-                for (int kk = 0; kk < nk; ++kk) acc = fmaf(pr[kk], v_s[kk * dp + e], acc);
-                o[u] = acc;
-            }
-        }
-        __syncthreads();
-    }
-    // write partials
-    const size_t pbase = ((((size_t)b * a.nkv + g) * a.n_groups + grp) * a.n_chunks + chunk) * R;
-#pragma unroll
-    for (int u = 0; u < kMaxOut; ++u) {
-        int idx = threadIdx.x + u * blockDim.x;
-        if (idx < nr * d) {
-            int r = idx / d, e = idx % d;
-            a.part_o[(pbase + r) * d + e] = o[u];
-        }
-    }
-    for (int r = threadIdx.x; r < nr; r += blockDim.x) {
-        a.part_ml[(pbase + r) * 2 + 0] = m_s[r];
-        a.part_ml[(pbase + r) * 2 + 1] = l_s[r];
     }
 }
 
-// One warp per (sequence, block token, q head): merge the chunk partials, apply the optional
-// sigmoid gate, pack hi/lo BF16 for the O projection.
-__global__ void attn_combine_kernel(AttnArgs a) {
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int rep = a.nq / a.nkv;
-    const long long total = (long long)a.B * a.blk * a.nq;
-    if (gw >= total) return;
-    const int h = (int)(gw % a.nq);
-    const int i = (int)((gw / a.nq) % a.blk);
-    const int b = (int)(gw / ((long long)a.nq * a.blk));
-    const int g = h / rep;
-    const int rr = i * rep + (h % rep);
-    const int grp = rr / a.rows_per_group, r = rr % a.rows_per_group;
-    const int d = a.d, ept = d / 32;
-    const size_t cbase = (((size_t)b * a.nkv + g) * a.n_groups + grp) * a.n_chunks;
+// Split-KV attention for one (key chunk, KV head, sequence). Each lane owns 64 (or D) of the
+// head dimensions of one query row (LPR lanes per row); warps split the query rows into row
+// groups and the keys of every tile into key subsets. Key/value tiles stream into shared
+// memory through bulk copies (4 stages). Scores are kept in log2 units (q is pre-scaled by
+// log2(e)/sqrt(D)). The CTA merges its warps, writes one partial (o, m, l) per query row, and
+// the last CTA of the (sequence, KV head) merges the chunk partials in chunk order, applies the
+// optional sigmoid gate and packs the output for the O projection.
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
+    constexpr int LPR = D >= 64 ? D / 64 : 1;
+    constexpr int DL = D / LPR;
+    constexpr int RPW = 32 / LPR;
+    constexpr int TK = kTileBytes / (2 * D * 4);
+    extern __shared__ __align__(128) uint8_t sm_raw[];
+    float *tiles = reinterpret_cast<float *>(sm_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm_raw + (size_t)kAttnStages * kTileBytes);
+    int *s_flag = reinterpret_cast<int *>(full + kAttnStages);
 
-    float M = -INFINITY;
-    for (int c = lane; c < a.n_chunks; c += 32)
-        M = fmaxf(M, a.part_ml[((cbase + c) * a.rows_per_group + r) * 2]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int c = lane; c < a.n_chunks; c += 32) {
-        float m = a.part_ml[((cbase + c) * a.rows_per_group + r) * 2];
-        float l = a.part_ml[((cbase + c) * a.rows_per_group + r) * 2 + 1];
-        if (m != -INFINITY) L += l * expf(m - M);
-    }
-    L = warp_sum(L);
-    float acc[8];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int rep = a.nq / a.nkv;
+    const int R = a.blk * rep;
+    const int RG = (R + RPW - 1) / RPW;
+    const int KS = RG >= 8 ? 1 : 8 / RG;
+    const int rg = warp % RG, ks = warp / RG;
+    const bool active = ks < KS;
+    const int sub = lane / RPW, row = lane % RPW;
+    const int rr = rg * RPW + row;
+    const bool row_valid = active && rr < R;
+    const int tok = row_valid ? rr / rep : 0;
+    const int qh = g * rep + (row_valid ? rr % rep : 0);
+
+    const int nn = a.n_new ? min(max(a.n_new[b], 0), a.n_new_max) : 0;
+    const long long sc = (long long)a.seq_len[b] + nn + a.extra_rows;
+    const int S_cache = (int)min(max(sc, 0LL), (long long)a.cap);
+    const int S = S_cache + (a.kb ? a.blk : 0);
+    const int c0 = min(S, chunk * a.chunk), c1 = min(S, c0 + a.chunk);
+    const int n_tiles = (c1 - c0 + TK - 1) / TK;
+    const size_t head_off = (size_t)b * a.nkv + g;
+
+    // this lane's q slice, rotated by 4*sub floats so the LPR lanes of a row hit different banks
+    float2 q2[DL / 2];
+    {
+        const float qs = 1.4426950408889634f / sqrtf((float)D);
+        const float *qp = a.q + (((size_t)b * a.blk + tok) * a.nq + qh) * D + sub * DL;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-    for (int c = 0; c < a.n_chunks; ++c) {
-        float m = a.part_ml[((cbase + c) * a.rows_per_group + r) * 2];
-        if (m == -INFINITY) continue;
-        float f = expf(m - M);
-        const float *po = a.part_o + ((cbase + c) * a.rows_per_group + r) * d;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (u < ept) acc[u] = fmaf(f, po[lane + 32 * u], acc[u]);
-    }
-    const float invL = L > 0.f ? 1.f / L : 0.f;
-    const size_t t = (size_t)b * a.blk + i;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        if (u < ept) {
-            int e = lane + 32 * u;
-            float y = acc[u] * invL;
-            if (a.gate) {
-                float z = a.gate[t * a.ldg + h * d + e];
-                y = y * (1.f / (1.f + expf(-z)));
-            }
-            uint16_t hi, lo;
-            split_hi_lo(y, hi, lo);
-            size_t col = (size_t)h * d + e;
-            a.pack[(2 * t) * (size_t)(a.nq * d) + col] = hi;
-            a.pack[(2 * t + 1) * (size_t)(a.nq * d) + col] = lo;
+        for (int j = 0; j < DL / 4; ++j) {
+            float4 v = row_valid ? *reinterpret_cast<const float4 *>(qp + ((4 * j + 4 * sub) % DL))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            q2[2 * j] = make_float2(v.x * qs, v.y * qs);
+            q2[2 * j + 1] = make_float2(v.z * qs, v.w * qs);
         }
     }
+    float2 o2[DL / 2];
+#pragma unroll
+    for (int j = 0; j < DL / 2; ++j) o2[j] = make_float2(0.f, 0.f);
+    float m = -INFINITY, l = 0.f;
+
+    auto issue = [&](int jt) {
+        const int st = jt % kAttnStages;
+        const int t0 = c0 + jt * TK;
+        const int n = min(TK, c1 - t0);
+        const int ncache = max(0, min(n, S_cache - t0));
+        const int nblock = n - ncache;
+        float *kd = tiles + (size_t)st * (kTileBytes / 4);
+        float *vd = kd + TK * D;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&full[st])),
+                     "r"((uint32_t)(2 * n * D * 4))
+                     : "memory");
+        if (ncache > 0) {
+            const size_t off = (head_off * a.cap + t0) * D;
+            bulk_g2s(kd, a.cache_k + off, ncache * D * 4, &full[st]);
+            bulk_g2s(vd, a.cache_v + off, ncache * D * 4, &full[st]);
+        }
+        if (nblock > 0) {
+            const int bs = max(0, t0 - S_cache);
+            const size_t off = (head_off * a.blk + bs) * D;
+            bulk_g2s(kd + ncache * D, a.kb + off, nblock * D * 4, &full[st]);
+            bulk_g2s(vd + ncache * D, a.vb + off, nblock * D * 4, &full[st]);
+        }
+    };
+
+    if (tid == 0) {
+        for (int s2 = 0; s2 < kAttnStages; ++s2)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s2])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int jt = 0; jt < min(kAttnStages, n_tiles); ++jt) issue(jt);
+
+    const int KW = (TK + KS - 1) / KS;
+    for (int jt = 0; jt < n_tiles; ++jt) {
+        const int st = jt % kAttnStages;
+        attn_wait(&full[st], (uint32_t)((jt / kAttnStages) & 1), a.status);
+        const int t0 = c0 + jt * TK;
+        const int n = min(TK, c1 - t0);
+        const float *kt = tiles + (size_t)st * (kTileBytes / 4);
+        const float *vt = kt + TK * D;
+        const int kbeg = ks * KW, kend = min(n, kbeg + KW);
+        if (active) {
+            for (int k0 = kbeg; k0 < kend; k0 += kKeyGroup) {
+                float s[kKeyGroup];
+#pragma unroll
+                for (int u = 0; u < kKeyGroup; ++u) {
+                    const int kk = min(k0 + u, n - 1);
+                    const float *kr = kt + (size_t)kk * D + sub * DL;
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < DL / 4; ++j) {
+                        const float4 kv = *reinterpret_cast<const float4 *>(kr + ((4 * j + 4 * sub) % DL));
+                        acc = __ffma2_rn(q2[2 * j], make_float2(kv.x, kv.y), acc);
+                        acc = __ffma2_rn(q2[2 * j + 1], make_float2(kv.z, kv.w), acc);
+                    }
+                    s[u] = acc.x + acc.y;
+                }
+#pragma unroll
+                for (int u = 0; u < kKeyGroup; ++u) {
+#pragma unroll
+                    for (int o = RPW; o < 32; o <<= 1) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
+                    const int key = t0 + k0 + u;
+                    bool ok = row_valid && (k0 + u) < kend;
+                    if (a.causal_block && key >= S_cache && key - S_cache > tok) ok = false;
+                    if (!ok) s[u] = -INFINITY;
+                }
+                float mt = s[0];
+#pragma unroll
+                for (int u = 1; u < kKeyGroup; ++u) mt = fmaxf(mt, s[u]);
+                const float mn = fmaxf(m, mt);
+                if (mn == -INFINITY) continue;
+                const float corr = exp2f(m - mn);
+                float p[kKeyGroup], ps = 0.f;
+#pragma unroll
+                for (int u = 0; u < kKeyGroup; ++u) {
+                    p[u] = exp2f(s[u] - mn);
+                    ps += p[u];
+                }
+                l = l * corr + ps;
+                m = mn;
+                const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+                for (int j = 0; j < DL / 2; ++j) o2[j] = __fmul2_rn(o2[j], c2);
+#pragma unroll
+                for (int u = 0; u < kKeyGroup; ++u) {
+                    const int kk = min(k0 + u, n - 1);
+                    const float *vr = vt + (size_t)kk * D + sub * DL;
+                    const float2 pu = make_float2(p[u], p[u]);
+#pragma unroll
+                    for (int j = 0; j < DL / 4; ++j) {
+                        const float4 vv = *reinterpret_cast<const float4 *>(vr + ((4 * j + 4 * sub) % DL));
+                        o2[2 * j] = __ffma2_rn(pu, make_float2(vv.x, vv.y), o2[2 * j]);
+                        o2[2 * j + 1] = __ffma2_rn(pu, make_float2(vv.z, vv.w), o2[2 * j + 1]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0 && jt + kAttnStages < n_tiles) issue(jt + kAttnStages);
+    }
+
+    // ---- merge the key subsets of each row group (stage buffers are free now)
+    const int rows_cta = RG * RPW;
+    float *mo = tiles;                                  // [KS][rows_cta][D]
+    float *mm = mo + (size_t)KS * rows_cta * D;         // [KS][rows_cta]
+    float *ml = mm + KS * rows_cta;                     // [KS][rows_cta]
+    if (active) {
+        float *dst = mo + ((size_t)ks * rows_cta + rr) * D + sub * DL;
+#pragma unroll
+        for (int j = 0; j < DL / 4; ++j)
+            *reinterpret_cast<float4 *>(dst + ((4 * j + 4 * sub) % DL)) =
+                make_float4(o2[2 * j].x, o2[2 * j].y, o2[2 * j + 1].x, o2[2 * j + 1].y);
+        if (sub == 0) {
+            mm[ks * rows_cta + rr] = m;
+            ml[ks * rows_cta + rr] = l;
+        }
+    }
+    __syncthreads();
+    float *part = a.part + ((head_off * a.n_chunks + chunk) * (size_t)R) * (D + 2);
+    for (int idx = tid; idx < R * D; idx += kAttnThreads) {
+        const int r2 = idx / D, e = idx % D;
+        float M = -INFINITY;
+        for (int k2 = 0; k2 < KS; ++k2) M = fmaxf(M, mm[k2 * rows_cta + r2]);
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+            for (int k2 = 0; k2 < KS; ++k2) {
+                const float w = exp2f(mm[k2 * rows_cta + r2] - M);
+                O = fmaf(w, mo[((size_t)k2 * rows_cta + r2) * D + e], O);
+                L = fmaf(w, ml[k2 * rows_cta + r2], L);
+            }
+        }
+        part[(size_t)r2 * (D + 2) + e] = O;
+        if (e == 0) {
+            part[(size_t)r2 * (D + 2) + D] = M;
+            part[(size_t)r2 * (D + 2) + D + 1] = L;
+        }
+    }
+
+    // ---- the last CTA of this (sequence, KV head) merges the chunk partials in chunk order
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(&a.counters[head_off], 1);
+        *s_flag = (prev == a.n_chunks - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*s_flag) return;
+    __threadfence();
+    const float *allp = a.part + head_off * a.n_chunks * (size_t)R * (D + 2);
+    float *wts = tiles;                                 // [n_chunks][R] merge weights
+    for (int r2 = tid; r2 < R; r2 += kAttnThreads) {
+        float M = -INFINITY;
+        for (int c = 0; c < a.n_chunks; ++c)
+            M = fmaxf(M, __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D));
+        float L = 0.f;
+        if (M != -INFINITY)
+            for (int c = 0; c < a.n_chunks; ++c) {
+                const float mc = __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D);
+                L = fmaf(__ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D + 1), exp2f(mc - M), L);
+            }
+        for (int c = 0; c < a.n_chunks; ++c) {
+            const float mc = __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D);
+            wts[c * R + r2] = (L > 0.f) ? exp2f(mc - M) / L : 0.f;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < R * D; idx += kAttnThreads) {
+        const int r2 = idx / D, e = idx % D;
+        float y = 0.f;
+        for (int c = 0; c < a.n_chunks; ++c)
+            y = fmaf(wts[c * R + r2], __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + e), y);
+        const int i = r2 / rep, h = g * rep + r2 % rep;
+        const size_t t = (size_t)b * a.blk + i;
+        if (a.gate) {
+            const float z = a.gate[t * a.ldg + (size_t)h * D + e];
+            y = y * (1.f / (1.f + expf(-z)));
+        }
+        uint16_t hi, lo;
+        split_hi_lo(y, hi, lo);
+        const size_t col = (size_t)h * D + e;
+        a.pack[(2 * t) * (size_t)(a.nq * D) + col] = hi;
+        a.pack[(2 * t + 1) * (size_t)(a.nq * D) + col] = lo;
+    }
+    if (tid == 0) a.counters[head_off] = 0;
 }
 
 __global__ void seq_advance_kernel(int32_t *seq_len, const int32_t *n_new, int B, int delta,
@@ -378,47 +451,56 @@ int launch_qk_rope(const QkArgs &a, cudaStream_t s) {
     return cuda_check("qk_rope_kernel");
 }
 
-size_t attn_part_floats(int B, int nkv, int n_groups, int n_chunks, int rows_per_group, int d) {
-    return (size_t)B * nkv * n_groups * n_chunks * rows_per_group * (size_t)(d + 2);
+size_t attn_part_floats(const AttnArgs &a) {
+    const int R = a.blk * (a.nq / a.nkv);
+    return (size_t)a.B * a.nkv * a.n_chunks * R * (size_t)(a.d + 2);
 }
 
-// Rows per CTA group bounded by the per-thread output registers; chunk count aims at about
-// two CTAs per SM for the largest possible key count.
+// Keys per chunk: a whole number of tiles, about one CTA per SM (two waves when sequences x
+// KV heads alone nearly fill the GPU).
 void attn_plan(AttnArgs &a, int max_keys) {
-    const int rep = a.nq / a.nkv;
-    const int rows_total = a.blk * rep;
-    const int max_rows = (kAttnThreads * kMaxOut) / a.d;
-    a.n_groups = (rows_total + max_rows - 1) / max_rows;
-    a.rows_per_group = (rows_total + a.n_groups - 1) / a.n_groups;
-    int ctas_per_chunk = a.B * a.nkv * a.n_groups;
-    int want = max(1, (2 * kNumSMs + ctas_per_chunk - 1) / ctas_per_chunk);
-    int max_chunks = max(1, (max_keys + kKeyTile - 1) / kKeyTile);
-    int n = min(want, max_chunks);
-    int chunk = (max_keys + n - 1) / n;
-    chunk = ((chunk + kKeyTile - 1) / kKeyTile) * kKeyTile;
-    a.chunk = max(chunk, kKeyTile);
-    a.n_chunks = max(1, (max_keys + a.chunk - 1) / a.chunk);
+    const int TK = kTileBytes / (2 * a.d * 4);
+    const int heads = a.B * a.nkv;
+    const int waves = heads > 38 ? 2 : 1;
+    int want = std::max(1, (waves * kNumSMs + heads - 1) / heads);
+    int tiles = std::max(1, (max_keys + TK - 1) / TK);
+    int n = std::min(want, tiles);
+    int per = (tiles + n - 1) / n;
+    a.chunk = per * TK;
+    a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
+}
+
+template <int D>
+int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
+    const int R = a.blk * (a.nq / a.nkv);
+    constexpr int RPW = 32 / (D >= 64 ? D / 64 : 1);
+    if ((R + RPW - 1) / RPW > 8) return fail(DF_ESHAPE, "attention: %d query rows per KV head exceed %d", R, 8 * RPW);
+    size_t smem = (size_t)kAttnStages * kTileBytes + kAttnStages * 8 + 16;
+    size_t need_merge = sizeof(float) * ((size_t)8 * 32 * (D / (D >= 64 ? D / 64 : 1) + 2) + 512);
+    smem = std::max(smem, need_merge);
+    size_t need_w = sizeof(float) * (size_t)a.n_chunks * R;
+    if (need_w > (size_t)kAttnStages * kTileBytes) return fail(DF_ESHAPE, "attention: too many key chunks");
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool set[4][64] = {};
+    const int di = D == 32 ? 0 : D == 64 ? 1 : D == 128 ? 2 : 3;
+    if (dev >= 0 && dev < 64 && !set[di][dev]) {
+        cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set[di][dev] = true;
+    }
+    dim3 grid(a.n_chunks, a.nkv, a.B);
+    attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(a);
+    return cuda_check("attn_kernel");
 }
 
 int launch_attn(const AttnArgs &a, cudaStream_t s) {
-    const int dp = a.d + 4, R = a.rows_per_group;
-    size_t smem = sizeof(float) * ((size_t)R * dp + 2 * kKeyTile * dp + R * (kKeyTile + 1) + 3 * R);
-    if (smem > 48 * 1024) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        static bool attr_set[64] = {};
-        if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-            cudaFuncSetAttribute(attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 200 * 1024);
-            if (dev >= 0 && dev < 64) attr_set[dev] = true;
-        }
+    switch (a.d) {
+        case 32: return launch_attn_d<32>(a, s);
+        case 64: return launch_attn_d<64>(a, s);
+        case 128: return launch_attn_d<128>(a, s);
+        case 256: return launch_attn_d<256>(a, s);
+        default: return fail(DF_ESHAPE, "attention: head_dim %d not in {32, 64, 128, 256}", a.d);
     }
-    dim3 grid(a.n_chunks, a.nkv * a.n_groups, a.B);
-    attn_partial_kernel<<<grid, kAttnThreads, smem, s>>>(a);
-    DF_TRY(cuda_check("attn_partial_kernel"));
-    long long warps = (long long)a.B * a.blk * a.nq;
-    attn_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(a);
-    return cuda_check("attn_combine_kernel");
 }
 
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
