@@ -484,11 +484,50 @@ def profile_case(args):
             del W, X, Y, ws
         print(json.dumps({"profile_case": "gemms", "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count, **res}))
     else:
-        args.no_graph = True
-        args.skip_cpu = True
-        args.steps, args.warmup = 1, 1
-        run_native(args, 0, 1, 0)
-        print(json.dumps({"profile_case": "round"}))
+        # Per-kernel GPU time inside eager rounds of the workload (library event profiler).
+        from speculative_decoding_drafter_dflash_gb300 import synth
+        acc, n_new = variants(s)
+        nmax = s.block
+        w = synth.dflash_weights(s, seed=0, device=dev)
+        cache = synth.dflash_cache(s, seed=1, device=dev)
+        model = B.DFlashModel(s, w, cache)
+        ws = B.alloc_workspace(model.workspace_bytes(1, s.block, nmax), dev)
+        out = B.RoundOutputs(1, s.K, dev)
+        eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
+        tsl = torch.full((1,), 1 << 30, dtype=torch.int32, device=dev)
+        tgt = torch.zeros((1, s.block), dtype=torch.int32, device=dev)
+        inputs = []
+        for v in range(N_VARIANTS):
+            inp = synth.dflash_round_inputs(s, [nmax], seed=10 + v, device=dev)
+            inp.n_new = torch.tensor([n_new[v]], dtype=torch.int32, device=dev)
+            inputs.append(inp)
+
+        def one(v):
+            inp = inputs[v]
+            B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, nmax, s.K, tgt,
+                             eos, tsl, out, ws)
+            B.kv_rollback(cache.seq_len, inp.n_new)
+
+        for v in range(3):
+            one(v)
+        torch.cuda.synchronize()
+        rounds = 8
+        B.profile_enable(True)
+        for i in range(rounds):
+            one(i % N_VARIANTS)
+        rec = B.profile_read()
+        B.profile_enable(False)
+        agg = {}
+        for name, us in rec:
+            a = agg.setdefault(name, [0, 0.0])
+            a[0] += 1
+            a[1] += us
+        total = sum(v[1] for v in agg.values()) / rounds
+        table = {k: {"per_round": v[0] // rounds, "us_per_round": round(v[1] / rounds, 2),
+                     "us_each": round(v[1] / v[0], 2), "share": round(v[1] / rounds / total, 4)}
+                 for k, v in sorted(agg.items(), key=lambda kv: -kv[1][1])}
+        print(json.dumps({"profile_case": "round", "rounds": rounds,
+                          "kernel_us_per_round": round(total, 1), "kernels": table}))
 
 
 def main():

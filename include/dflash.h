@@ -66,6 +66,16 @@ int df_version(void);
  * Launches recorded into a CUDA graph count once, at capture. */
 uint64_t df_kernel_launches(void);
 
+/* Per-kernel GPU time of the library's own launches (the analogue of the pages'
+ * HF2Q_MTP_PROFILE / HF2Q_DFLASH_PROFILE sub-step timers, without their forced syncs): while
+ * enabled, an event pair brackets every kernel on its launching stream; launches recorded into
+ * a CUDA graph capture are not timed. df_profile_enable(1) clears the record (room for 4096
+ * kernels) and starts recording, df_profile_enable(0) stops. df_profile_read synchronises and
+ * writes up to max_entries durations (microseconds) into us and their kernel names, one per
+ * line, into names; it returns the number of entries. */
+int df_profile_enable(int on);
+int df_profile_read(float *us, int max_entries, char *names, size_t names_bytes);
+
 /* ------------------------------------------------------------------------------------------
  * DFlash drafter (tensors.rs `DFlashLayerTensors`, `DFlashModelTensors`; dflash config fields
  * seen in qwen35_orchestrator.rs: target_layer_ids, mask_token_id, hidden_size, head_dim).

@@ -74,6 +74,8 @@ _SIGS = [
     ("df_last_error", ctypes.c_char_p, []),
     ("df_version", c_int, []),
     ("df_kernel_launches", ctypes.c_uint64, []),
+    ("df_profile_enable", c_int, [c_int]),
+    ("df_profile_read", c_int, [c_void_p, c_int, ctypes.c_char_p, c_size_t]),
     ("df_dflash_workspace_bytes", c_size_t, [POINTER(DFlashConfig), c_int, c_int, c_int]),
     ("dflash_block_forward", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), POINTER(KvCache),
                                      c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
@@ -125,6 +127,21 @@ def lib():
 
 def kernel_launches() -> int:
     return int(lib().df_kernel_launches())
+
+
+def profile_enable(on: bool = True):
+    _check(lib().df_profile_enable(1 if on else 0))
+
+
+def profile_read(max_entries: int = 8192):
+    """[(kernel name, microseconds)] of the launches recorded since profile_enable(True)."""
+    us = (ctypes.c_float * max_entries)()
+    buf = ctypes.create_string_buffer(64 * max_entries)
+    n = lib().df_profile_read(us, max_entries, buf, len(buf))
+    if n < 0:
+        _check(n)
+    names = buf.value.decode().split("\n")
+    return [(names[i], float(us[i])) for i in range(n)]
 
 
 def last_error() -> str:

@@ -6,6 +6,8 @@
 // (`forward_draft_with_hidden`) for MTP.
 #include <algorithm>
 #include <atomic>
+#include <mutex>
+#include <vector>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -25,9 +27,44 @@ int fail(int code, const char *fmt, ...) {
     return code;
 }
 
-int cuda_check(const char *what) {
+// ---------------------------------------------------------------- launch profiling
+struct Prof {
+    std::mutex mu;
+    bool on = false;
+    int cap = 0, n = 0;
+    std::vector<cudaEvent_t> ev;
+    std::vector<const char *> names;   // nullptr marks a "before" event
+};
+static Prof g_prof;
+
+static bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
+void prof_begin(cudaStream_t s) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (!g_prof.on || g_prof.n + 2 > g_prof.cap || capturing(s)) return;
+    cudaEventRecord(g_prof.ev[g_prof.n], s);
+    g_prof.names[g_prof.n++] = nullptr;
+}
+
+int cuda_check(const char *what, cudaStream_t s) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = cudaGetLastError();
+    if (g_prof.on) {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        if (g_prof.on && g_prof.n > 0 && g_prof.n < g_prof.cap &&
+            g_prof.names[g_prof.n - 1] == nullptr) {
+            cudaEventRecord(g_prof.ev[g_prof.n], s);
+            g_prof.names[g_prof.n++] = what;
+        }
+    }
     if (e != cudaSuccess) return fail(DF_ECUDA, "%s: %s", what, cudaGetErrorString(e));
     return DF_OK;
 }
@@ -230,6 +267,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.epi = EPI_STORE;
         g.out = ws.hctx;
         g.ldo = H;
+        g.name = "gemm_fc";
         g.status = st;
         DF_TRY(launch_gemm_tc(g, ws.tc, s));
         PackArgs q;
@@ -287,6 +325,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.epi = EPI_STORE;
         g.out = ws.qkv;
         g.ldo = Nqkv;
+        g.name = "gemm_qkv";
         g.status = st;
         DF_TRY(launch_gemm_tc(g, ws.tc, s));
 
@@ -351,6 +390,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         go.ldo = H;
         go.resid = ws.h;
         go.ldr = H;
+        go.name = "gemm_o";
         go.status = st;
         DF_TRY(launch_gemm_tc(go, ws.tc, s));
 
@@ -379,6 +419,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gu.epi = EPI_SWIGLU;
         gu.pack_out = ws.xp_act;
         gu.ldpo = I;
+        gu.name = "gemm_gate_up";
         gu.status = st;
         DF_TRY(launch_gemm_tc(gu, ws.tc, s));
 
@@ -395,6 +436,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gd.ldo = H;
         gd.resid = ws.h;
         gd.ldr = H;
+        gd.name = "gemm_down";
         gd.status = st;
         DF_TRY(launch_gemm_tc(gd, ws.tc, s));
     }
@@ -426,6 +468,7 @@ int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V
     g.T = rows;
     g.epi = EPI_ARGMAX;
     g.part = part;
+    g.name = "gemm_lm_head_argmax";
     int G = 0;
     DF_TRY(launch_gemm_tc(g, tc, s, &G));
     return launch_argmax_final(part, G, rows, idx, top1, top2, nullptr, 1, 0, s);
@@ -443,6 +486,44 @@ const char *df_last_error(void) { return g_err; }
 int df_version(void) { return 100; }
 
 uint64_t df_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int df_profile_enable(int on) {
+    g_err[0] = 0;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (on && g_prof.ev.empty()) {
+        g_prof.cap = 8192;
+        g_prof.ev.resize(g_prof.cap);
+        g_prof.names.resize(g_prof.cap);
+        for (auto &e : g_prof.ev)
+            if (cudaEventCreate(&e) != cudaSuccess)
+                return fail(DF_ECUDA, "profiling events: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    g_prof.n = 0;
+    g_prof.on = on != 0;
+    return DF_OK;
+}
+
+int df_profile_read(float *us, int max_entries, char *names, size_t names_bytes) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (g_prof.n == 0) return 0;
+    if (cudaEventSynchronize(g_prof.ev[g_prof.n - 1]) != cudaSuccess)
+        return fail(DF_ECUDA, "profiling sync: %s", cudaGetErrorString(cudaGetLastError()));
+    int k = 0;
+    size_t off = 0;
+    if (names && names_bytes) names[0] = 0;
+    for (int i = 1; i < g_prof.n && k < max_entries; ++i) {
+        if (g_prof.names[i] == nullptr || g_prof.names[i - 1] != nullptr) continue;
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, g_prof.ev[i - 1], g_prof.ev[i]);
+        if (us) us[k] = ms * 1000.f;
+        if (names && off < names_bytes) {
+            int w = snprintf(names + off, names_bytes - off, "%s\n", g_prof.names[i]);
+            off += w > 0 ? (size_t)w : 0;
+        }
+        ++k;
+    }
+    return k;
+}
 
 size_t df_dflash_workspace_bytes(const df_dflash_config *cfg, int B, int block, int n_new_max) {
     if (check_cfg(cfg) != DF_OK || B <= 0 || block < 2 || n_new_max < 0) return 0;

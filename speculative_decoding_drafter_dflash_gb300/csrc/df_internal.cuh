@@ -12,7 +12,11 @@ namespace df {
 
 // ---------------------------------------------------------------- host-side errors
 int fail(int code, const char *fmt, ...);   // records the message, returns code
-int cuda_check(const char *what);           // DF_ECUDA if the last launch failed; counts launches
+// Kernel launch bookkeeping: prof_begin() before a launch and cuda_check() after it record
+// profiling events on the launching stream (when enabled), count launches, and map a failed
+// launch to DF_ECUDA.
+void prof_begin(cudaStream_t s);
+int cuda_check(const char *what, cudaStream_t s);
 
 #define DF_TRY(expr)                 \
     do {                             \
@@ -147,6 +151,7 @@ struct GemmArgs {
     const uint16_t *X2 = nullptr;    // with Wk2: packed activations of columns [K1, K)
     int ldx2 = 0;
     int32_t *status = nullptr;
+    const char *name = "gemm_tc_kernel";   // label in launch profiles
     int epi = EPI_STORE;
     float *out = nullptr;            // EPI_STORE / EPI_RESID: out[t*ldo + n]
     int ldo = 0;

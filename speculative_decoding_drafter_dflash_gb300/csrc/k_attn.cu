@@ -437,9 +437,10 @@ int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const 
     int total = B * (blk + n_new_max) * (rot / 2);
     if (total <= 0) return DF_OK;
     int threads = 256, grid = min((total + threads - 1) / threads, 4 * kNumSMs);
+    prof_begin(s);
     rope_table_kernel<<<grid, threads, 0, s>>>(cos_t, sin_t, seq_len, n_new, n_new_max, B, blk,
                                                 pos_off, rot, theta, status);
-    return cuda_check("rope_table_kernel");
+    return cuda_check("rope_table_kernel", s);
 }
 
 int launch_qk_rope(const QkArgs &a, cudaStream_t s) {
@@ -447,8 +448,9 @@ int launch_qk_rope(const QkArgs &a, cudaStream_t s) {
     if (warps <= 0) return DF_OK;
     const int wpb = 8;
     long long grid = (warps + wpb - 1) / wpb;
+    prof_begin(s);
     qk_rope_kernel<<<(unsigned)grid, wpb * 32, wpb * a.d * sizeof(float), s>>>(a);
-    return cuda_check("qk_rope_kernel");
+    return cuda_check("qk_rope_kernel", s);
 }
 
 size_t attn_part_floats(const AttnArgs &a) {
@@ -489,8 +491,9 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
         set[di][dev] = true;
     }
     dim3 grid(a.n_chunks, a.nkv, a.B);
+    prof_begin(s);
     attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(a);
-    return cuda_check("attn_kernel");
+    return cuda_check("attn_kernel", s);
 }
 
 int launch_attn(const AttnArgs &a, cudaStream_t s) {
@@ -505,8 +508,9 @@ int launch_attn(const AttnArgs &a, cudaStream_t s) {
 
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
                        int32_t *status, cudaStream_t s) {
+    prof_begin(s);
     seq_advance_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, n_new, B, delta, cap, status);
-    return cuda_check("seq_advance_kernel");
+    return cuda_check("seq_advance_kernel", s);
 }
 
 }  // namespace df

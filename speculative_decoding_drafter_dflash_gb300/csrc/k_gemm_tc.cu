@@ -525,18 +525,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 epi_bar();
                 if (last) {
                     __threadfence();
+                    // Load every partial of a token chunk before summing them, in CTA order, so
+                    // the reduction costs one L2 round trip per chunk rather than one per CTA.
+                    constexpr int kMaxParts = 8;
                     for (int c = 0; c < n_chunks; ++c) {
                         float y[kTokChunk];
 #pragma unroll
                         for (int i = 0; i < kTokChunk; ++i) y[i] = 0.f;
-                        for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            const int sl = (kb_start(cc, p) / p.kbt == m) ? 0 : 1;
-                            const float *src = p.scratch + ((size_t)cc * 2 + sl) * (size_t)p.T * kBM;
+                        for (int cb = c_lo; cb <= c_hi; cb += kMaxParts) {
+                            float v8[kMaxParts][kTokChunk];
 #pragma unroll
-                            for (int i = 0; i < kTokChunk; ++i) {
-                                int t = c * kTokChunk + i;
-                                if (t < p.T) y[i] += __ldcg(src + (size_t)t * kBM + r);
+                            for (int j = 0; j < kMaxParts; ++j) {
+                                const int cc = cb + j;
+                                const float *src = nullptr;
+                                if (cc <= c_hi) {
+                                    const int sl = (kb_start(cc, p) / p.kbt == m) ? 0 : 1;
+                                    src = p.scratch + ((size_t)cc * 2 + sl) * (size_t)p.T * kBM;
+                                }
+#pragma unroll
+                                for (int i = 0; i < kTokChunk; ++i) {
+                                    const int t = c * kTokChunk + i;
+                                    v8[j][i] = (src && t < p.T) ? __ldcg(src + (size_t)t * kBM + r) : 0.f;
+                                }
                             }
+#pragma unroll
+                            for (int j = 0; j < kMaxParts; ++j)
+#pragma unroll
+                                for (int i = 0; i < kTokChunk; ++i) y[i] += v8[j][i];
                         }
                         epi_apply(p, es, m, r, q, lane, c * kTokChunk, y);
                     }
@@ -679,8 +694,9 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     if (G_out) *G_out = p.G;
+    prof_begin(s);
     gemm_tc_kernel<<<p.G, kThreads, smem, s>>>(p);
-    return cuda_check("gemm_tc_kernel");
+    return cuda_check(a.name, s);
 }
 
 }  // namespace

@@ -81,8 +81,9 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
 
 int launch_pack(const PackArgs &a, cudaStream_t s) {
     if (a.T <= 0) return DF_OK;
+    prof_begin(s);
     pack_kernel<<<a.T, kPackThreads, 0, s>>>(a);
-    return cuda_check("pack_kernel");
+    return cuda_check("pack_kernel", s);
 }
 
 }  // namespace df

@@ -10,13 +10,25 @@ namespace df {
 
 namespace {
 
-// One thread per row: merge the G partial states in increasing partial order.
+// One warp per row: lanes merge strided subsets of the G partial states, then a fixed
+// butterfly merges the lanes (the result is independent of the order: the merge keeps the
+// largest value, the lowest index among equal values, and the second-largest value).
 __global__ void argmax_final_kernel(const ArgTop *part, int G, int T, int32_t *idx, float *top1,
                                     float *top2, int32_t *idx_copy, int ld, int skip) {
-    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (t >= T) return;
     ArgTop r = argtop_empty(0x7fffffff);
-    for (int g = 0; g < G; ++g) r = argtop_merge(r, part[(size_t)g * T + t]);
+    for (int g = lane; g < G; g += 32) r = argtop_merge(r, part[(size_t)g * T + t]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        ArgTop b;
+        b.v1 = __shfl_xor_sync(0xffffffffu, r.v1, o);
+        b.i1 = __shfl_xor_sync(0xffffffffu, r.i1, o);
+        b.v2 = __shfl_xor_sync(0xffffffffu, r.v2, o);
+        r = argtop_merge(r, b);
+    }
+    if (lane != 0) return;
     idx[t] = r.i1;
     if (top1) top1[t] = r.v1;
     if (top2) top2[t] = r.v2;
@@ -78,9 +90,10 @@ __global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32
 int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1, float *top2,
                         int32_t *idx_copy, int idx_copy_ld, int idx_copy_skip, cudaStream_t s) {
     if (T <= 0) return DF_OK;
-    argmax_final_kernel<<<(T + 127) / 128, 128, 0, s>>>(part, G, T, idx, top1, top2, idx_copy,
+    prof_begin(s);
+    argmax_final_kernel<<<(T + 3) / 4, 128, 0, s>>>(part, G, T, idx, top1, top2, idx_copy,
                                                         idx_copy_ld, idx_copy_skip);
-    return cuda_check("argmax_final_kernel");
+    return cuda_check("argmax_final_kernel", s);
 }
 
 int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
@@ -88,16 +101,18 @@ int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, i
                   int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,
                   int32_t *target_seq_len, int32_t *status, cudaStream_t s) {
     if (B <= 0) return DF_OK;
+    prof_begin(s);
     accept_kernel<<<(B + 127) / 128, 128, 0, s>>>(drafts, ld, target, B, K, eos, n_eos, committed,
                                                   n_committed, accept_count, hit_eos, rollback,
                                                   target_seq_len, status);
-    return cuda_check("accept_kernel");
+    return cuda_check("accept_kernel", s);
 }
 
 int launch_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *status, cudaStream_t s) {
     if (B <= 0) return DF_OK;
+    prof_begin(s);
     rollback_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, n, B, status);
-    return cuda_check("rollback_kernel");
+    return cuda_check("rollback_kernel", s);
 }
 
 }  // namespace df
