@@ -158,7 +158,6 @@ int check_cache(const df_kv_cache *k, int n_layers, int B, int d) {
 // ---------------------------------------------------------------- DFlash workspace
 struct DFlashWs {
     float *h, *hctx, *qkv, *q, *kb, *vb, *cos_t, *sin_t, *attn_part, *h_final;
-    int *attn_counters;
     uint16_t *xp_ctx, *xp_qkv, *xp_o, *xp_ffn, *xp_act, *xp_head;
     ArgTop *amax_part;
     int32_t *idx;
@@ -198,7 +197,6 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     w.plan.d = d;
     attn_plan(w.plan, cap + blk);
     w.attn_part = cv.take<float>(attn_part_floats(w.plan));
-    w.attn_counters = cv.take<int>((size_t)B * nkv);
     w.xp_ctx = cv.take<uint16_t>(2 * std::max<size_t>(T_ctx, 1) * fc_in);
     w.xp_qkv = cv.take<uint16_t>(2 * T_all * H);
     w.xp_o = cv.take<uint16_t>(2 * T_blk * qt);
@@ -370,7 +368,6 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         at.extra_rows = 0;
         at.causal_block = c->causal_block;
         at.part = ws.attn_part;
-        at.counters = ws.attn_counters;
         at.gate = nullptr;
         at.ldg = 0;
         at.pack = ws.xp_o;
@@ -876,7 +873,6 @@ int check_mtp_weights(const df_mtp_config *c, const df_mtp_weights *w) {
 
 struct MtpWs {
     float *x, *qkv, *gate, *q, *h1, *cos_t, *sin_t, *attn_part, *moe_out, *router_logits;
-    int *attn_counters;
     uint16_t *xp_e, *xp_h, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
     ArgTop *amax_part;
     int32_t *moe_sel;
@@ -906,7 +902,6 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     w.plan.d = d;
     attn_plan(w.plan, cap);
     w.attn_part = cv.take<float>(attn_part_floats(w.plan));
-    w.attn_counters = cv.take<int>((size_t)B * nkv);
     w.moe_out = cv.take<float>((size_t)B * H);
     w.router_logits = cv.take<float>((size_t)B * std::max(c->n_experts, 1));
     w.xp_e = cv.take<uint16_t>((size_t)2 * B * H);
@@ -1085,7 +1080,6 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         at.extra_rows = st + 1;
         at.causal_block = 0;
         at.part = W.attn_part;
-        at.counters = W.attn_counters;
         at.gate = w->w_gate ? W.gate : nullptr;
         at.ldg = qt;
         at.pack = W.xp_o;

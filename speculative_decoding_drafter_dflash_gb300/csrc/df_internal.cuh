@@ -221,7 +221,6 @@ struct AttnArgs {
     int extra_rows;          // rows beyond seq_len + n_new that are visible (MTP: step + 1)
     int causal_block;
     float *part;             // [B, nkv, n_chunks, R, d + 2] per-CTA partial (o, m, l)
-    int *counters;           // [B * nkv] arrival counters, zero between calls
     int n_chunks, chunk;     // key chunks per (sequence, KV head); keys per chunk
     const float *gate;       // optional [B*blk, ldg] gate pre-activation (q_total wide)
     int ldg;

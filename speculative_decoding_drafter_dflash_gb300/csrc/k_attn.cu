@@ -33,11 +33,16 @@ __global__ void rope_table_kernel(float *cos_t, float *sin_t, const int32_t *seq
         if (status && j == 0 && s == 0 && n_new && (n_new[b] < 0 || n_new[b] > n_new_max))
             set_status(status, DF_ESHAPE);
         long long pos = s < blk ? (long long)base + nn + s + pos_off : (long long)base + (s - blk);
-        double inv = pow((double)theta, -2.0 * (double)j / (double)rot);
-        double sn, cs;
-        sincos((double)pos * inv, &sn, &cs);
-        cos_t[i] = (float)cs;
-        sin_t[i] = (float)sn;
+        // inverse frequency theta^(-2j/rot) and the angle in double precision; the angle is
+        // reduced to [-pi, pi] in double, then its sine and cosine are taken in F32.
+        const double inv = exp2(-2.0 * (double)j / (double)rot * log2((double)theta));
+        const double ang = (double)pos * inv;
+        const double two_pi = 6.283185307179586476925286766559;
+        const double red = ang - rint(ang / two_pi) * two_pi;
+        float sn, cs;
+        sincosf((float)red, &sn, &cs);
+        cos_t[i] = cs;
+        sin_t[i] = sn;
     }
 }
 
@@ -187,7 +192,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t sm_raw[];
     float *tiles = reinterpret_cast<float *>(sm_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm_raw + (size_t)kAttnStages * kTileBytes);
-    int *s_flag = reinterpret_cast<int *>(full + kAttnStages);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -368,52 +372,78 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
         }
     }
 
-    // ---- the last CTA of this (sequence, KV head) merges the chunk partials in chunk order
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(&a.counters[head_off], 1);
-        *s_flag = (prev == a.n_chunks - 1) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!*s_flag) return;
-    __threadfence();
+}
+
+// Merge of the chunk partials: one warp per (query row, sequence, KV head) group of rows. Lane c
+// holds chunk c's merge weight exp2(m_c - M) / L; every partial o value of a chunk is loaded
+// before any is summed, and the sum runs in chunk order (the result does not depend on timing).
+template <int D>
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
+    constexpr int RPB = 8;                   // query rows per CTA (one per warp)
+    constexpr int EPL = D / 32;              // output dims per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int rep = a.nq / a.nkv;
+    const int R = a.blk * rep;
+    const int r2 = blockIdx.x * RPB + warp;
+    if (r2 >= R) return;
+    const size_t head_off = (size_t)b * a.nkv + g;
     const float *allp = a.part + head_off * a.n_chunks * (size_t)R * (D + 2);
-    float *wts = tiles;                                 // [n_chunks][R] merge weights
-    for (int r2 = tid; r2 < R; r2 += kAttnThreads) {
-        float M = -INFINITY;
-        for (int c = 0; c < a.n_chunks; ++c)
-            M = fmaxf(M, __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D));
-        float L = 0.f;
-        if (M != -INFINITY)
-            for (int c = 0; c < a.n_chunks; ++c) {
-                const float mc = __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D);
-                L = fmaf(__ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D + 1), exp2f(mc - M), L);
+    const int NC = a.n_chunks;
+    float M = -INFINITY;
+    for (int c = lane; c < NC; c += 32) M = fmaxf(M, allp[((size_t)c * R + r2) * (D + 2) + D]);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int c = lane; c < NC; c += 32) {
+        const float *pc = allp + ((size_t)c * R + r2) * (D + 2);
+        const float mc = pc[D];
+        if (mc != -INFINITY) L += pc[D + 1] * exp2f(mc - M);
+    }
+    L = warp_sum(L);
+    const float invL = L > 0.f ? 1.f / L : 0.f;
+    float y[EPL];
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) y[u] = 0.f;
+    for (int c0 = 0; c0 < NC; c0 += 32) {
+        float wl = 0.f;
+        if (c0 + lane < NC) {
+            const float mc = allp[((size_t)(c0 + lane) * R + r2) * (D + 2) + D];
+            wl = mc == -INFINITY ? 0.f : exp2f(mc - M) * invL;
+        }
+        const int cn = min(32, NC - c0);
+        for (int cb = 0; cb < cn; cb += 8) {
+            float ov[8][EPL];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = c0 + cb + j;
+                const float *pc = allp + ((size_t)min(c, NC - 1) * R + r2) * (D + 2);
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) ov[j][u] = (cb + j < cn) ? pc[lane + 32 * u] : 0.f;
             }
-        for (int c = 0; c < a.n_chunks; ++c) {
-            const float mc = __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + D);
-            wts[c * R + r2] = (L > 0.f) ? exp2f(mc - M) / L : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, wl, (cb + j) & 31);
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) y[u] = fmaf(wj, ov[j][u], y[u]);
+            }
         }
     }
-    __syncthreads();
-    for (int idx = tid; idx < R * D; idx += kAttnThreads) {
-        const int r2 = idx / D, e = idx % D;
-        float y = 0.f;
-        for (int c = 0; c < a.n_chunks; ++c)
-            y = fmaf(wts[c * R + r2], __ldcg(allp + ((size_t)c * R + r2) * (D + 2) + e), y);
-        const int i = r2 / rep, h = g * rep + r2 % rep;
-        const size_t t = (size_t)b * a.blk + i;
+    const int i = r2 / rep, h = g * rep + r2 % rep;
+    const size_t t = (size_t)b * a.blk + i;
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) {
+        const int e = lane + 32 * u;
+        float v = y[u];
         if (a.gate) {
             const float z = a.gate[t * a.ldg + (size_t)h * D + e];
-            y = y * (1.f / (1.f + expf(-z)));
+            v = v * (1.f / (1.f + expf(-z)));
         }
         uint16_t hi, lo;
-        split_hi_lo(y, hi, lo);
+        split_hi_lo(v, hi, lo);
         const size_t col = (size_t)h * D + e;
         a.pack[(2 * t) * (size_t)(a.nq * D) + col] = hi;
         a.pack[(2 * t + 1) * (size_t)(a.nq * D) + col] = lo;
     }
-    if (tid == 0) a.counters[head_off] = 0;
 }
 
 __global__ void seq_advance_kernel(int32_t *seq_len, const int32_t *n_new, int B, int delta,
@@ -480,8 +510,6 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     size_t smem = (size_t)kAttnStages * kTileBytes + kAttnStages * 8 + 16;
     size_t need_merge = sizeof(float) * ((size_t)8 * 32 * (D / (D >= 64 ? D / 64 : 1) + 2) + 512);
     smem = std::max(smem, need_merge);
-    size_t need_w = sizeof(float) * (size_t)a.n_chunks * R;
-    if (need_w > (size_t)kAttnStages * kTileBytes) return fail(DF_ESHAPE, "attention: too many key chunks");
     int dev = 0;
     cudaGetDevice(&dev);
     static bool set[4][64] = {};
@@ -493,7 +521,11 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     dim3 grid(a.n_chunks, a.nkv, a.B);
     prof_begin(s);
     attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(a);
-    return cuda_check("attn_kernel", s);
+    DF_TRY(cuda_check("attn_kernel", s));
+    dim3 cgrid((R + 7) / 8, a.nkv, a.B);
+    prof_begin(s);
+    attn_combine_kernel<D><<<cgrid, 256, 0, s>>>(a);
+    return cuda_check("attn_combine_kernel", s);
 }
 
 int launch_attn(const AttnArgs &a, cudaStream_t s) {

@@ -77,12 +77,104 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
     }
 }
 
+// Register-resident variant for rows of at most 256 * 4 * NV elements: every element is loaded
+// once (128-bit loads, all issued before the reduction), kept in registers for the second
+// pass, and stored as packed 4-element groups.
+template <int NV>
+__global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
+    __shared__ float red[33];
+    const int t = blockIdx.x;
+    const int K = a.K, K4 = K >> 2;
+    const int s = t / a.rows_per_seq, j = t - s * a.rows_per_seq;
+    const bool valid = a.nvalid == nullptr || j < min(max(a.nvalid[s], 0), a.rows_per_seq);
+    int id = 0;
+    if (a.gather) {
+        id = a.ids ? a.ids[t] : (j == 0 ? a.last_token[s] : a.mask_id);
+        if (id < 0 || id >= a.vocab) {
+            if (threadIdx.x == 0) set_status(a.status, DF_EINVAL);
+            id = min(max(id, 0), a.vocab - 1);
+        }
+    }
+    float4 x[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int k4 = threadIdx.x + u * kPackThreads;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid && k4 < K4) {
+            if (a.gather) {
+                const uint2 g = *reinterpret_cast<const uint2 *>(a.gather + (size_t)id * K + 4 * k4);
+                v = make_float4(__uint_as_float(g.x << 16) * a.scale,
+                                __uint_as_float(g.x & 0xffff0000u) * a.scale,
+                                __uint_as_float(g.y << 16) * a.scale,
+                                __uint_as_float(g.y & 0xffff0000u) * a.scale);
+            } else {
+                v = *reinterpret_cast<const float4 *>(a.src + (size_t)t * a.lds + 4 * k4);
+            }
+        }
+        x[u] = v;
+    }
+    float inv = 1.f;
+    if (a.norm_w) {
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < NV; ++u)
+            ss = fmaf(x[u].x, x[u].x, fmaf(x[u].y, x[u].y, fmaf(x[u].z, x[u].z, fmaf(x[u].w, x[u].w, ss))));
+        ss = block_sum(ss, red);
+        inv = 1.f / sqrtf(ss / (float)K + a.eps);
+    }
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int k4 = threadIdx.x + u * kPackThreads;
+        if (k4 >= K4) continue;
+        const int k = 4 * k4;
+        float4 v = x[u];
+        if (a.h_out) *reinterpret_cast<float4 *>(a.h_out + (size_t)t * a.ldh + k) = v;
+        if (a.norm_w) {
+            const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + k);
+            v = make_float4(v.x * inv * w.x, v.y * inv * w.y, v.z * inv * w.z, v.w * inv * w.w);
+        }
+        if (a.y_out) *reinterpret_cast<float4 *>(a.y_out + (size_t)t * a.ldy + k) = v;
+        if (a.pack) {
+            uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
+            split_hi_lo(v.x, h0, l0);
+            split_hi_lo(v.y, h1, l1);
+            split_hi_lo(v.z, h2, l2);
+            split_hi_lo(v.w, h3, l3);
+            *reinterpret_cast<uint2 *>(a.pack + (size_t)(2 * t) * a.ldp + k) =
+                make_uint2(h0 | ((uint32_t)h1 << 16), h2 | ((uint32_t)h3 << 16));
+            *reinterpret_cast<uint2 *>(a.pack + (size_t)(2 * t + 1) * a.ldp + k) =
+                make_uint2(l0 | ((uint32_t)l1 << 16), l2 | ((uint32_t)l3 << 16));
+        }
+    }
+}
+
+bool aligned_for_vec(const PackArgs &a) {
+    auto al = [](const void *p, int bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; };
+    if (a.K % 4) return false;
+    if (a.src && (!al(a.src, 16) || a.lds % 4)) return false;
+    if (a.gather && !al(a.gather, 8)) return false;
+    if (a.h_out && (!al(a.h_out, 16) || a.ldh % 4)) return false;
+    if (a.norm_w && !al(a.norm_w, 16)) return false;
+    if (a.y_out && (!al(a.y_out, 16) || a.ldy % 4)) return false;
+    if (a.pack && (!al(a.pack, 8) || a.ldp % 4)) return false;
+    return true;
+}
+
 }  // namespace
 
 int launch_pack(const PackArgs &a, cudaStream_t s) {
     if (a.T <= 0) return DF_OK;
+    const int nv = (a.K / 4 + kPackThreads - 1) / kPackThreads;
     prof_begin(s);
-    pack_kernel<<<a.T, kPackThreads, 0, s>>>(a);
+    if (aligned_for_vec(a) && nv <= 16) {
+        if (nv <= 1) pack_vec_kernel<1><<<a.T, kPackThreads, 0, s>>>(a);
+        else if (nv <= 2) pack_vec_kernel<2><<<a.T, kPackThreads, 0, s>>>(a);
+        else if (nv <= 4) pack_vec_kernel<4><<<a.T, kPackThreads, 0, s>>>(a);
+        else if (nv <= 8) pack_vec_kernel<8><<<a.T, kPackThreads, 0, s>>>(a);
+        else pack_vec_kernel<16><<<a.T, kPackThreads, 0, s>>>(a);
+    } else {
+        pack_kernel<<<a.T, kPackThreads, 0, s>>>(a);
+    }
     return cuda_check("pack_kernel", s);
 }
 
