@@ -10,6 +10,7 @@
 #include <vector>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "df_internal.cuh"
@@ -25,6 +26,30 @@ int fail(int code, const char *fmt, ...) {
     vsnprintf(g_err, sizeof(g_err), fmt, ap);
     va_end(ap);
     return code;
+}
+
+// ---------------------------------------------------------------- launch set-up
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("DF_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+void prepare_kernel(const void *func, int dyn_smem) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void *, int>> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto &d : done)
+        if (d.first == func && d.second == dev) return;
+    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaGetLastError();
+    done.emplace_back(func, dev);
+    (void)dyn_smem;
 }
 
 // ---------------------------------------------------------------- launch profiling

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dflash.h"
 
 namespace df {
@@ -25,6 +27,41 @@ int cuda_check(const char *what, cudaStream_t s);
     } while (0)
 
 constexpr int kNumSMs = 152;
+
+// ---------------------------------------------------------------- launches
+// Every kernel is launched with programmatic dependent launch: it may start while its
+// predecessor on the stream is still running, does only work that reads no predecessor output
+// (weight prefetch, barrier and TMEM set-up) before pdl_wait(), and lets its own successor
+// launch early with pdl_trigger(). Every kernel executes pdl_wait() before touching memory that
+// another kernel writes, so completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+bool pdl_enabled();
+// One-time per (kernel, device): dynamic shared memory limit and a max-shared carveout, so SMs
+// keep one L1/shared split across the kernels of a round.
+void prepare_kernel(const void *func, int dyn_smem);
+
+template <typename... KArgs, typename... Args>
+int launch_k(const char *name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+             cudaStream_t s, Args &&...args) {
+    prepare_kernel(reinterpret_cast<const void *>(kernel), (int)smem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    prof_begin(s);
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return cuda_check(name, s);
+}
 
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }

@@ -21,6 +21,8 @@ namespace {
 __global__ void rope_table_kernel(float *cos_t, float *sin_t, const int32_t *seq_len,
                                   const int32_t *n_new, int n_new_max, int B, int blk, int pos_off,
                                   int rot, float theta, int32_t *status) {
+    pdl_trigger();
+    pdl_wait();
     const int half = rot / 2;
     const int slots = blk + n_new_max;
     const int total = B * slots * half;
@@ -50,6 +52,8 @@ __global__ void rope_table_kernel(float *cos_t, float *sin_t, const int32_t *seq
 // [nq+nkv, nq+2nkv) v heads. Rows [0, B*blk) are block rows, the rest context rows.
 __global__ void qk_rope_kernel(QkArgs a) {
     extern __shared__ float smem[];
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wpb = blockDim.x >> 5;
     const int slots = a.nq + 2 * a.nkv;
@@ -195,6 +199,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    pdl_trigger();
+    pdl_wait();
     const int rep = a.nq / a.nkv;
     const int R = a.blk * rep;
     const int RG = (R + RPW - 1) / RPW;
@@ -381,6 +387,8 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
     constexpr int RPB = 8;                   // query rows per CTA (one per warp)
     constexpr int EPL = D / 32;              // output dims per lane
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y, b = blockIdx.z;
     const int rep = a.nq / a.nkv;
@@ -448,6 +456,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
 
 __global__ void seq_advance_kernel(int32_t *seq_len, const int32_t *n_new, int B, int delta,
                                    int cap, int32_t *status) {
+    pdl_trigger();
+    pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int add = n_new ? n_new[b] : delta;
@@ -467,10 +477,8 @@ int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const 
     int total = B * (blk + n_new_max) * (rot / 2);
     if (total <= 0) return DF_OK;
     int threads = 256, grid = min((total + threads - 1) / threads, 4 * kNumSMs);
-    prof_begin(s);
-    rope_table_kernel<<<grid, threads, 0, s>>>(cos_t, sin_t, seq_len, n_new, n_new_max, B, blk,
-                                                pos_off, rot, theta, status);
-    return cuda_check("rope_table_kernel", s);
+    return launch_k("rope_table_kernel", rope_table_kernel, dim3(grid), dim3(threads), 0, s, cos_t,
+                    sin_t, seq_len, n_new, n_new_max, B, blk, pos_off, rot, theta, status);
 }
 
 int launch_qk_rope(const QkArgs &a, cudaStream_t s) {
@@ -478,9 +486,8 @@ int launch_qk_rope(const QkArgs &a, cudaStream_t s) {
     if (warps <= 0) return DF_OK;
     const int wpb = 8;
     long long grid = (warps + wpb - 1) / wpb;
-    prof_begin(s);
-    qk_rope_kernel<<<(unsigned)grid, wpb * 32, wpb * a.d * sizeof(float), s>>>(a);
-    return cuda_check("qk_rope_kernel", s);
+    return launch_k("qk_rope_kernel", qk_rope_kernel, dim3((unsigned)grid), dim3(wpb * 32),
+                    wpb * a.d * sizeof(float), s, a);
 }
 
 size_t attn_part_floats(const AttnArgs &a) {
@@ -510,22 +517,10 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     size_t smem = (size_t)kAttnStages * kTileBytes + kAttnStages * 8 + 16;
     size_t need_merge = sizeof(float) * ((size_t)8 * 32 * (D / (D >= 64 ? D / 64 : 1) + 2) + 512);
     smem = std::max(smem, need_merge);
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static bool set[4][64] = {};
-    const int di = D == 32 ? 0 : D == 64 ? 1 : D == 128 ? 2 : 3;
-    if (dev >= 0 && dev < 64 && !set[di][dev]) {
-        cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        set[di][dev] = true;
-    }
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    prof_begin(s);
-    attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(a);
-    DF_TRY(cuda_check("attn_kernel", s));
+    DF_TRY(launch_k("attn_kernel", attn_kernel<D>, grid, dim3(kAttnThreads), smem, s, a));
     dim3 cgrid((R + 7) / 8, a.nkv, a.B);
-    prof_begin(s);
-    attn_combine_kernel<D><<<cgrid, 256, 0, s>>>(a);
-    return cuda_check("attn_combine_kernel", s);
+    return launch_k("attn_combine_kernel", attn_combine_kernel<D>, cgrid, dim3(256), 0, s, a);
 }
 
 int launch_attn(const AttnArgs &a, cudaStream_t s) {
@@ -540,9 +535,8 @@ int launch_attn(const AttnArgs &a, cudaStream_t s) {
 
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
                        int32_t *status, cudaStream_t s) {
-    prof_begin(s);
-    seq_advance_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, n_new, B, delta, cap, status);
-    return cuda_check("seq_advance_kernel", s);
+    return launch_k("seq_advance_kernel", seq_advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s,
+                    seq_len, n_new, B, delta, cap, status);
 }
 
 }  // namespace df

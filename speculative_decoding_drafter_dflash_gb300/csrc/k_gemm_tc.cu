@@ -373,45 +373,57 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     const long long my_begin = kb_start(blockIdx.x, p), my_end = kb_start(blockIdx.x + 1, p);
 
+    pdl_trigger();
     if (warp == 0) {
         if (lane == 0) {
+            // Weights do not depend on earlier kernels: the first stages' weight tiles are
+            // requested before waiting for the predecessor grid, activation tiles after.
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (long long x = my_begin; x < my_end && ok;) {
-                const int m = (int)(x / p.kbt);
-                const int k0 = (int)(x - (long long)m * p.kbt);
-                const int k1 = (int)min((long long)p.kbt, my_end - (long long)m * p.kbt);
-                x = (long long)m * p.kbt + k1;
-                int s = 0, row0 = 0;
-                if (!p.pair) {
-                    s = seg_of_tile(m, p);
-                    row0 = (m - p.seg_tile0[s]) * kBM;
+            const long long count = my_end - my_begin;
+            const int pre = (int)min((long long)p.stages, count);
+            auto load_a = [&](long long x, int stage) {
+                const int m = (int)(x / p.kbt), kb = (int)(x - (long long)m * p.kbt);
+                uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
+                const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
+                const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
+                if (p.pair) {
+                    tma_load_2d(a, &p.amap[0], &full[stage], kx, m * 64, pol_w);
+                    tma_load_2d(a + kABytes / 2, &p.amap[1], &full[stage], kx, m * 64, pol_w);
+                } else {
+                    const int s = seg_of_tile(m, p);
+                    tma_load_2d(a, &p.amap[ks ? 1 : s], &full[stage], kx, (m - p.seg_tile0[s]) * kBM,
+                                pol_w);
                 }
-                for (int kb = k0; kb < k1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(&full[stage], p.stage_bytes);
-                    uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
-                    uint8_t *b = a + kABytes;
-                    const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
-                    const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
-                    if (p.pair) {
-                        tma_load_2d(a, &p.amap[0], &full[stage], kx, m * 64, pol_w);
-                        tma_load_2d(a + kABytes / 2, &p.amap[1], &full[stage], kx, m * 64, pol_w);
-                    } else {
-                        tma_load_2d(a, &p.amap[ks ? 1 : s], &full[stage], kx, row0, pol_w);
-                    }
-                    tma_load_2d(b, &p.bmap[ks], &full[stage], kx, 0, pol_x);
-                    ++issued;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            };
+            auto load_b = [&](long long x, int stage) {
+                const int m = (int)(x / p.kbt), kb = (int)(x - (long long)m * p.kbt);
+                uint8_t *b = stage_base + (size_t)stage * p.stage_bytes + kABytes;
+                const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
+                const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
+                tma_load_2d(b, &p.bmap[ks], &full[stage], kx, 0, pol_x);
+            };
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(&full[i], p.stage_bytes);
+                load_a(my_begin + i, i);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) load_b(my_begin + i, i);
+            int stage = pre % p.stages;
+            uint32_t phase = (pre == p.stages) ? 1u : 0u;
+            long long issued = pre;
+            bool ok = true;
+            for (long long x = my_begin + pre; x < my_end; ++x) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&full[stage], p.stage_bytes);
+                load_a(x, stage);
+                load_b(x, stage);
+                ++issued;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
             if (!ok) {
@@ -467,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             mbar_drain(drain, 0);
         }
     } else {
+        pdl_wait();
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
         const int r = q * 32 + lane;     // tile row of this thread
         int acc = 0;
@@ -686,17 +699,8 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
     size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 5) * 8 + 16 +
                   (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
                   (size_t)T * sizeof(ArgTop) + 64;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
     if (G_out) *G_out = p.G;
-    prof_begin(s);
-    gemm_tc_kernel<<<p.G, kThreads, smem, s>>>(p);
-    return cuda_check(a.name, s);
+    return launch_k(a.name, gemm_tc_kernel, dim3(p.G), dim3(kThreads), smem, s, p);
 }
 
 }  // namespace

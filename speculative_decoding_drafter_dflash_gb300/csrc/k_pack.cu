@@ -34,6 +34,8 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // optionally stores that (y_out), and packs it into two BF16 rows (hi, lo).
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
     __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const int K = a.K;
     const int s = t / a.rows_per_seq, j = t - s * a.rows_per_seq;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
 template <int NV>
 __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
     __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const int K = a.K, K4 = K >> 2;
     const int s = t / a.rows_per_seq, j = t - s * a.rows_per_seq;
@@ -165,17 +169,15 @@ bool aligned_for_vec(const PackArgs &a) {
 int launch_pack(const PackArgs &a, cudaStream_t s) {
     if (a.T <= 0) return DF_OK;
     const int nv = (a.K / 4 + kPackThreads - 1) / kPackThreads;
-    prof_begin(s);
+    const dim3 g(a.T), b(kPackThreads);
     if (aligned_for_vec(a) && nv <= 16) {
-        if (nv <= 1) pack_vec_kernel<1><<<a.T, kPackThreads, 0, s>>>(a);
-        else if (nv <= 2) pack_vec_kernel<2><<<a.T, kPackThreads, 0, s>>>(a);
-        else if (nv <= 4) pack_vec_kernel<4><<<a.T, kPackThreads, 0, s>>>(a);
-        else if (nv <= 8) pack_vec_kernel<8><<<a.T, kPackThreads, 0, s>>>(a);
-        else pack_vec_kernel<16><<<a.T, kPackThreads, 0, s>>>(a);
-    } else {
-        pack_kernel<<<a.T, kPackThreads, 0, s>>>(a);
+        if (nv <= 1) return launch_k("pack_kernel", pack_vec_kernel<1>, g, b, 0, s, a);
+        if (nv <= 2) return launch_k("pack_kernel", pack_vec_kernel<2>, g, b, 0, s, a);
+        if (nv <= 4) return launch_k("pack_kernel", pack_vec_kernel<4>, g, b, 0, s, a);
+        if (nv <= 8) return launch_k("pack_kernel", pack_vec_kernel<8>, g, b, 0, s, a);
+        return launch_k("pack_kernel", pack_vec_kernel<16>, g, b, 0, s, a);
     }
-    return cuda_check("pack_kernel", s);
+    return launch_k("pack_kernel", pack_kernel, g, b, 0, s, a);
 }
 
 }  // namespace df

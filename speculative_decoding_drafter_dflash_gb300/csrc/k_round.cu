@@ -15,6 +15,8 @@ namespace {
 // largest value, the lowest index among equal values, and the second-largest value).
 __global__ void argmax_final_kernel(const ArgTop *part, int G, int T, int32_t *idx, float *top1,
                                     float *top2, int32_t *idx_copy, int ld, int skip) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -44,6 +46,8 @@ __global__ void accept_kernel(const int32_t *drafts, int ld, const int32_t *targ
                               const int32_t *eos, int n_eos, int32_t *committed,
                               int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
                               int32_t *rollback, int32_t *target_seq_len, int32_t *status) {
+    pdl_trigger();
+    pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const int32_t *dr = drafts + (size_t)b * ld;
@@ -75,6 +79,8 @@ __global__ void accept_kernel(const int32_t *drafts, int ld, const int32_t *targ
 }
 
 __global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32_t *status) {
+    pdl_trigger();
+    pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int k = n[b];
@@ -90,10 +96,8 @@ __global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32
 int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1, float *top2,
                         int32_t *idx_copy, int idx_copy_ld, int idx_copy_skip, cudaStream_t s) {
     if (T <= 0) return DF_OK;
-    prof_begin(s);
-    argmax_final_kernel<<<(T + 3) / 4, 128, 0, s>>>(part, G, T, idx, top1, top2, idx_copy,
-                                                        idx_copy_ld, idx_copy_skip);
-    return cuda_check("argmax_final_kernel", s);
+    return launch_k("argmax_final_kernel", argmax_final_kernel, dim3((T + 3) / 4), dim3(128), 0, s,
+                    part, G, T, idx, top1, top2, idx_copy, idx_copy_ld, idx_copy_skip);
 }
 
 int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
@@ -101,18 +105,15 @@ int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, i
                   int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,
                   int32_t *target_seq_len, int32_t *status, cudaStream_t s) {
     if (B <= 0) return DF_OK;
-    prof_begin(s);
-    accept_kernel<<<(B + 127) / 128, 128, 0, s>>>(drafts, ld, target, B, K, eos, n_eos, committed,
-                                                  n_committed, accept_count, hit_eos, rollback,
-                                                  target_seq_len, status);
-    return cuda_check("accept_kernel", s);
+    return launch_k("accept_kernel", accept_kernel, dim3((B + 127) / 128), dim3(128), 0, s, drafts,
+                    ld, target, B, K, eos, n_eos, committed, n_committed, accept_count, hit_eos,
+                    rollback, target_seq_len, status);
 }
 
 int launch_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *status, cudaStream_t s) {
     if (B <= 0) return DF_OK;
-    prof_begin(s);
-    rollback_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, n, B, status);
-    return cuda_check("rollback_kernel", s);
+    return launch_k("rollback_kernel", rollback_kernel, dim3((B + 127) / 128), dim3(128), 0, s,
+                    seq_len, n, B, status);
 }
 
 }  // namespace df
