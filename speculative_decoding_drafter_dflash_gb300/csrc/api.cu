@@ -45,8 +45,13 @@ void prepare_kernel(const void *func, int dyn_smem) {
     std::lock_guard<std::mutex> lk(mu);
     for (auto &d : done)
         if (d.first == func && d.second == dev) return;
+    static const int carveout = [] {
+        const char *e = getenv("DF_CARVEOUT");
+        return e ? atoi(e) : 100;
+    }();
     cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (carveout >= 0)
+        cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
     cudaGetLastError();
     done.emplace_back(func, dev);
     (void)dyn_smem;

@@ -381,33 +381,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             const long long count = my_end - my_begin;
             const int pre = (int)min((long long)p.stages, count);
-            auto load_a = [&](long long x, int stage) {
-                const int m = (int)(x / p.kbt), kb = (int)(x - (long long)m * p.kbt);
-                uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
-                const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
-                const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
-                if (p.pair) {
-                    tma_load_2d(a, &p.amap[0], &full[stage], kx, m * 64, pol_w);
-                    tma_load_2d(a + kABytes / 2, &p.amap[1], &full[stage], kx, m * 64, pol_w);
-                } else {
-                    const int s = seg_of_tile(m, p);
-                    tma_load_2d(a, &p.amap[ks ? 1 : s], &full[stage], kx, (m - p.seg_tile0[s]) * kBM,
-                                pol_w);
+            // (tile, k-block) cursor advanced without divisions: one TMA issue per k-block
+            // must stay far cheaper than the ~700 cycles a 16 KB tile takes to stream per SM.
+            struct Cursor {
+                int m, kb, s, row0;
+            };
+            auto cursor_at = [&](long long x) {
+                Cursor c;
+                c.m = (int)(x / p.kbt);
+                c.kb = (int)(x - (long long)c.m * p.kbt);
+                c.s = p.pair ? 0 : seg_of_tile(c.m, p);
+                c.row0 = p.pair ? c.m * 64 : (c.m - p.seg_tile0[c.s]) * kBM;
+                return c;
+            };
+            auto advance = [&](Cursor &c) {
+                if (++c.kb == p.kbt) {
+                    c.kb = 0;
+                    ++c.m;
+                    if (p.pair) {
+                        c.row0 = c.m * 64;
+                    } else {
+                        if (c.s + 1 < p.n_seg && c.m >= p.seg_tile0[c.s + 1]) ++c.s;
+                        c.row0 = (c.m - p.seg_tile0[c.s]) * kBM;
+                    }
                 }
             };
-            auto load_b = [&](long long x, int stage) {
-                const int m = (int)(x / p.kbt), kb = (int)(x - (long long)m * p.kbt);
+            auto load_a = [&](const Cursor &c, int stage) {
+                uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
+                const int ks = (p.k_seg == 2 && c.kb >= p.kb_seg0) ? 1 : 0;
+                const int kx = (ks ? c.kb - p.kb_seg0 : c.kb) * kBK;
+                if (p.pair) {
+                    tma_load_2d(a, &p.amap[0], &full[stage], kx, c.row0, pol_w);
+                    tma_load_2d(a + kABytes / 2, &p.amap[1], &full[stage], kx, c.row0, pol_w);
+                } else {
+                    tma_load_2d(a, &p.amap[ks ? 1 : c.s], &full[stage], kx, c.row0, pol_w);
+                }
+            };
+            auto load_b = [&](const Cursor &c, int stage) {
                 uint8_t *b = stage_base + (size_t)stage * p.stage_bytes + kABytes;
-                const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
-                const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
+                const int ks = (p.k_seg == 2 && c.kb >= p.kb_seg0) ? 1 : 0;
+                const int kx = (ks ? c.kb - p.kb_seg0 : c.kb) * kBK;
                 tma_load_2d(b, &p.bmap[ks], &full[stage], kx, 0, pol_x);
             };
+            Cursor cur = cursor_at(my_begin);
             for (int i = 0; i < pre; ++i) {
                 mbar_expect_tx(&full[i], p.stage_bytes);
-                load_a(my_begin + i, i);
+                load_a(cur, i);
+                advance(cur);
             }
             pdl_wait();
-            for (int i = 0; i < pre; ++i) load_b(my_begin + i, i);
+            Cursor cb = cursor_at(my_begin);
+            for (int i = 0; i < pre; ++i) {
+                load_b(cb, i);
+                advance(cb);
+            }
             int stage = pre % p.stages;
             uint32_t phase = (pre == p.stages) ? 1u : 0u;
             long long issued = pre;
@@ -418,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     break;
                 }
                 mbar_expect_tx(&full[stage], p.stage_bytes);
-                load_a(x, stage);
-                load_b(x, stage);
+                load_a(cur, stage);
+                load_b(cur, stage);
+                advance(cur);
                 ++issued;
                 if (++stage == p.stages) {
                     stage = 0;
