@@ -187,7 +187,8 @@ int check_cache(const df_kv_cache *k, int n_layers, int B, int d) {
 
 // ---------------------------------------------------------------- DFlash workspace
 struct DFlashWs {
-    float *h, *hctx, *qkv, *q, *kb, *vb, *cos_t, *sin_t, *attn_part, *h_final;
+    float *h, *defer, *q, *kb, *vb, *cos_t, *sin_t, *attn_part, *h_final;
+    size_t defer_floats;
     uint16_t *xp_ctx, *xp_qkv, *xp_o, *xp_ffn, *xp_act, *xp_head;
     ArgTop *amax_part;
     int32_t *idx;
@@ -196,6 +197,12 @@ struct DFlashWs {
 };
 
 int n_counters_for(long long rows) { return (int)(rows / 64 + 256); }
+
+// Room for the split partial sums of a projection with N outputs over T tokens: the splits S
+// satisfy S * ceil(N / 128) <= SMs, so S * N < (SMs + S) * 128.
+size_t defer_floats_for(int T, long long N) {
+    return (size_t)T * (size_t)(2 * kNumSMs * 128 + N);
+}
 
 void carve_tc(Carve &cv, TcScratch &tc, int max_tokens, long long max_rows) {
     tc.partial_floats = tc_partial_floats(max_tokens);
@@ -212,8 +219,9 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     const size_t T_blk = (size_t)B * blk, T_ctx = (size_t)B * n_new_max, T_all = T_blk + T_ctx;
     const size_t fc_in = (size_t)c->n_target_layers * H, qt = (size_t)nq * d, kt = (size_t)nkv * d;
     w.h = cv.take<float>(T_blk * H);
-    w.hctx = cv.take<float>(std::max<size_t>(T_ctx, 1) * H);
-    w.qkv = cv.take<float>(T_all * (qt + 2 * kt));
+    // deferred split-K sums of one projection: S x T x N floats with S * N <= SMs * 128
+    w.defer_floats = defer_floats_for((int)T_all, (long long)std::max<size_t>(qt + 2 * kt, H));
+    w.defer = cv.take<float>(w.defer_floats);
     w.q = cv.take<float>(T_blk * qt);
     w.kb = cv.take<float>(T_blk * kt);
     w.vb = cv.take<float>(T_blk * kt);
@@ -258,6 +266,9 @@ int get_ws(void *ws, size_t ws_bytes, size_t need) {
 }
 
 // The drafter forward. Either block_ids or (last_token, mask id) provides the block tokens.
+// fc, QKV, O and down projections leave split-K partial sums that the next kernel adds in
+// (hidden_norm pack, q/k-norm + RoPE, fused residual + RMSNorm pack); gate/up writes packed
+// SwiGLU activations directly.
 int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
                         const df_kv_cache *cache, const int32_t *block_ids,
                         const int32_t *last_token, const float *target_hidden,
@@ -268,6 +279,18 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
     const int I = c->intermediate;
     const int T_blk = B * blk, T_ctx = B * n_new_max, T_all = T_blk + T_ctx;
     const int fc_in = c->n_target_layers * H, qt = nq * d, kt = nkv * d, Nqkv = qt + 2 * kt;
+
+    // A projection whose split partial sums land in ws.defer; returns the split count.
+    auto deferred = [&](GemmArgs g, int T, int N, const char *name, int *S) -> int {
+        g.epi = EPI_STORE;
+        g.defer = 1;
+        g.out = ws.defer;
+        g.ldo = N;
+        g.part_stride = (size_t)T * N;
+        g.status = st;
+        g.name = name;
+        return launch_gemm_tc(g, ws.tc, s, S);
+    };
 
     DF_TRY(launch_rope_table(ws.cos_t, ws.sin_t, cache->seq_len, n_new, n_new_max, B, blk, 0, rot,
                              c->rope_theta, st, s));
@@ -292,15 +315,13 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.X = ws.xp_ctx;
         g.ldx = fc_in;
         g.T = T_ctx;
-        g.epi = EPI_STORE;
-        g.out = ws.hctx;
-        g.ldo = H;
-        g.name = "gemm_fc";
-        g.status = st;
-        DF_TRY(launch_gemm_tc(g, ws.tc, s));
+        int S = 0;
+        DF_TRY(deferred(g, T_ctx, H, "gemm_fc", &S));
         PackArgs q;
-        q.src = ws.hctx;
-        q.lds = H;
+        q.part = ws.defer;
+        q.n_part = S;
+        q.part_stride = (size_t)T_ctx * H;
+        q.ldpart = H;
         q.norm_w = W->hidden_norm;
         q.eps = c->rms_eps;
         q.pack = ws.xp_qkv + (size_t)2 * T_blk * H;
@@ -312,6 +333,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         q.status = st;
         DF_TRY(launch_pack(q, s));
     }
+    int S_down = 0;   // split count of the previous layer's down projection
     for (int l = 0; l < c->n_layers; ++l) {
         const df_layer_weights &L = W->layers[l];
         PackArgs p;
@@ -322,13 +344,18 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
             p.mask_id = c->mask_token_id;
             p.vocab = c->vocab;
             p.scale = c->embed_scale;
-            p.h_out = ws.h;
-            p.ldh = H;
             p.rows_per_seq = blk;
         } else {
+            // h += down-projection partials of layer l-1, then input RMSNorm of layer l
             p.src = ws.h;
             p.lds = H;
+            p.part = ws.defer;
+            p.n_part = S_down;
+            p.part_stride = (size_t)T_blk * H;
+            p.ldpart = H;
         }
+        p.h_out = ws.h;
+        p.ldh = H;
         p.norm_w = L.input_norm;
         p.eps = c->rms_eps;
         p.pack = ws.xp_qkv;
@@ -350,15 +377,14 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.X = ws.xp_qkv;
         g.ldx = H;
         g.T = T_all;
-        g.epi = EPI_STORE;
-        g.out = ws.qkv;
-        g.ldo = Nqkv;
-        g.name = "gemm_qkv";
-        g.status = st;
-        DF_TRY(launch_gemm_tc(g, ws.tc, s));
+        int S_qkv = 0;
+        DF_TRY(deferred(g, T_all, Nqkv, "gemm_qkv", &S_qkv));
 
         QkArgs qa;
-        qa.qkv = ws.qkv;
+        qa.qkv = nullptr;
+        qa.part = ws.defer;
+        qa.n_part = S_qkv;
+        qa.part_stride = (size_t)T_all * Nqkv;
         qa.ldq = Nqkv;
         qa.B = B;
         qa.blk = blk;
@@ -412,18 +438,19 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         go.X = ws.xp_o;
         go.ldx = qt;
         go.T = T_blk;
-        go.epi = EPI_RESID;
-        go.out = ws.h;
-        go.ldo = H;
-        go.resid = ws.h;
-        go.ldr = H;
-        go.name = "gemm_o";
-        go.status = st;
-        DF_TRY(launch_gemm_tc(go, ws.tc, s));
+        int S_o = 0;
+        DF_TRY(deferred(go, T_blk, H, "gemm_o", &S_o));
 
+        // h += O-projection partials (fused residual add), then post-attention RMSNorm
         PackArgs pf;
         pf.src = ws.h;
         pf.lds = H;
+        pf.part = ws.defer;
+        pf.n_part = S_o;
+        pf.part_stride = (size_t)T_blk * H;
+        pf.ldpart = H;
+        pf.h_out = ws.h;
+        pf.ldh = H;
         pf.norm_w = L.post_attn_norm;
         pf.eps = c->rms_eps;
         pf.pack = ws.xp_ffn;
@@ -446,8 +473,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gu.epi = EPI_SWIGLU;
         gu.pack_out = ws.xp_act;
         gu.ldpo = I;
-        gu.name = "gemm_gate_up";
         gu.status = st;
+        gu.name = "gemm_gate_up";
         DF_TRY(launch_gemm_tc(gu, ws.tc, s));
 
         GemmArgs gd;
@@ -458,18 +485,16 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gd.X = ws.xp_act;
         gd.ldx = I;
         gd.T = T_blk;
-        gd.epi = EPI_RESID;
-        gd.out = ws.h;
-        gd.ldo = H;
-        gd.resid = ws.h;
-        gd.ldr = H;
-        gd.name = "gemm_down";
-        gd.status = st;
-        DF_TRY(launch_gemm_tc(gd, ws.tc, s));
+        DF_TRY(deferred(gd, T_blk, H, "gemm_down", &S_down));
     }
+    // h += last down-projection partials, then the final norm
     PackArgs pfin;
     pfin.src = ws.h;
     pfin.lds = H;
+    pfin.part = ws.defer;
+    pfin.n_part = S_down;
+    pfin.part_stride = (size_t)T_blk * H;
+    pfin.ldpart = H;
     pfin.norm_w = W->final_norm;
     pfin.eps = c->rms_eps;
     pfin.y_out = h_final;
@@ -902,7 +927,7 @@ int check_mtp_weights(const df_mtp_config *c, const df_mtp_weights *w) {
 }
 
 struct MtpWs {
-    float *x, *qkv, *gate, *q, *h1, *cos_t, *sin_t, *attn_part, *moe_out, *router_logits;
+    float *x, *defer, *gate, *q, *h1, *cos_t, *sin_t, *attn_part, *moe_out, *router_logits;
     uint16_t *xp_e, *xp_h, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
     ArgTop *amax_part;
     int32_t *moe_sel;
@@ -918,7 +943,7 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     const size_t I = c->n_experts ? (size_t)std::max(c->expert_inter * c->top_k, c->shared_inter)
                                   : (size_t)c->intermediate;
     w.x = cv.take<float>((size_t)B * H);
-    w.qkv = cv.take<float>((size_t)B * (qt + 2 * kt));
+    w.defer = cv.take<float>(defer_floats_for(B, (long long)std::max<size_t>(2 * qt + 2 * kt, H)));
     w.gate = cv.take<float>((size_t)B * qt);
     w.q = cv.take<float>((size_t)B * qt);
     w.h1 = cv.take<float>((size_t)B * H);
@@ -985,6 +1010,19 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
     const int rot = cfg->rotary_dim ? cfg->rotary_dim : d;
     const int qt = nq * d, kt = nkv * d, Nqkv = qt + 2 * kt, I = cfg->intermediate;
 
+    // A projection whose split partial sums land in W.defer; returns the split count.
+    auto deferred = [&](GemmArgs g, int N, const char *name, int *S) -> int {
+        g.epi = EPI_STORE;
+        g.defer = 1;
+        g.out = W.defer;
+        g.ldo = N;
+        g.part_stride = (size_t)B * N;
+        g.status = d_status;
+        g.name = name;
+        return launch_gemm_tc(g, W.tc, s, S);
+    };
+    const int n_gate = w->w_gate ? nq : 0;
+    const int Nq4 = Nqkv + n_gate * d;
     for (int st = 0; st < n_steps; ++st) {
         const float *hprev = st == 0 ? prev_hidden : hidden_out + (size_t)(st - 1) * B * H;
         const int32_t *tok = st == 0 ? token : argmax_out + (size_t)(st - 1) * B;
@@ -1026,14 +1064,17 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         ge.X2 = W.xp_h;
         ge.ldx2 = H;
         ge.T = B;
-        ge.epi = EPI_STORE;
-        ge.out = W.x;
-        ge.ldo = H;
-        DF_TRY(launch_gemm_tc(ge, W.tc, s));
+        int S_eh = 0;
+        DF_TRY(deferred(ge, H, "gemm_eh_proj", &S_eh));
 
+        // x = sum of the eh partials (kept as the attention residual); attention RMSNorm
         PackArgs pa;
-        pa.src = W.x;
-        pa.lds = H;
+        pa.part = W.defer;
+        pa.n_part = S_eh;
+        pa.part_stride = (size_t)B * H;
+        pa.ldpart = H;
+        pa.h_out = W.x;
+        pa.ldh = H;
         pa.norm_w = w->attn_norm;
         pa.eps = cfg->rms_eps;
         pa.pack = W.xp_attn;
@@ -1048,31 +1089,26 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         gq.n1 = kt;
         gq.W2 = w->wv;
         gq.n2 = kt;
-        gq.N = Nqkv;
+        gq.W3 = w->w_gate;
+        gq.n3 = n_gate * d;
+        gq.N = Nq4;
         gq.K = H;
         gq.X = W.xp_attn;
         gq.ldx = H;
         gq.T = B;
-        gq.epi = EPI_STORE;
-        gq.out = W.qkv;
-        gq.ldo = Nqkv;
-        DF_TRY(launch_gemm_tc(gq, W.tc, s));
-        if (w->w_gate) {
-            GemmArgs gg = gq;
-            gg.W0 = w->w_gate;
-            gg.n0 = qt;
-            gg.W1 = gg.W2 = nullptr;
-            gg.n1 = gg.n2 = 0;
-            gg.N = qt;
-            gg.out = W.gate;
-            gg.ldo = qt;
-            DF_TRY(launch_gemm_tc(gg, W.tc, s));
-        }
+        int S_q = 0;
+        DF_TRY(deferred(gq, Nq4, "gemm_qkv_gate", &S_q));
         DF_TRY(launch_rope_table(W.cos_t, W.sin_t, cache->seq_len, nullptr, 0, B, 1, st, rot,
                                  cfg->rope_theta, d_status, s));
         QkArgs qa;
-        qa.qkv = W.qkv;
-        qa.ldq = Nqkv;
+        qa.qkv = nullptr;
+        qa.part = W.defer;
+        qa.n_part = S_q;
+        qa.part_stride = (size_t)B * Nq4;
+        qa.ldq = Nq4;
+        qa.n_gate_heads = n_gate;
+        qa.gate_out = W.gate;
+        qa.ldg = qt;
         qa.B = B;
         qa.blk = 1;
         qa.n_new_max = 0;
@@ -1123,15 +1159,18 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         go.X = W.xp_o;
         go.ldx = qt;
         go.T = B;
-        go.epi = EPI_RESID;
-        go.out = W.h1;
-        go.ldo = H;
-        go.resid = W.x;
-        go.ldr = H;
-        DF_TRY(launch_gemm_tc(go, W.tc, s));
+        int S_o = 0;
+        DF_TRY(deferred(go, H, "gemm_o", &S_o));
+        // h1 = x + O partials (fused residual add); post-attention RMSNorm
         PackArgs pf;
-        pf.src = W.h1;
+        pf.src = W.x;
         pf.lds = H;
+        pf.part = W.defer;
+        pf.n_part = S_o;
+        pf.part_stride = (size_t)B * H;
+        pf.ldpart = H;
+        pf.h_out = W.h1;
+        pf.ldh = H;
         pf.norm_w = w->post_attn_norm;
         pf.eps = cfg->rms_eps;
         pf.pack = W.xp_ffn;
@@ -1152,6 +1191,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         gu.epi = EPI_SWIGLU;
         gu.pack_out = W.xp_act;
         gu.ldpo = I;
+        gu.name = "gemm_gate_up";
         DF_TRY(launch_gemm_tc(gu, W.tc, s));
         GemmArgs gd;
         gd.W0 = w->w_down;
@@ -1161,16 +1201,19 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         gd.X = W.xp_act;
         gd.ldx = I;
         gd.T = B;
-        gd.epi = EPI_RESID;
-        gd.out = hid;
-        gd.ldo = H;
-        gd.resid = W.h1;
-        gd.ldr = H;
-        DF_TRY(launch_gemm_tc(gd, W.tc, s));
-        // shared head: rmsnorm(hidden) then lm_head argmax (mtp.rs `forward_shared_head`)
+        int S_d = 0;
+        DF_TRY(deferred(gd, H, "gemm_down", &S_d));
+        // hidden = h1 + down partials (the step's output); shared head: RMSNorm then lm_head
+        // argmax (mtp.rs `forward_ffn_residual`, `forward_shared_head`)
         PackArgs pk;
-        pk.src = hid;
+        pk.src = W.h1;
         pk.lds = H;
+        pk.part = W.defer;
+        pk.n_part = S_d;
+        pk.part_stride = (size_t)B * H;
+        pk.ldpart = H;
+        pk.h_out = hid;
+        pk.ldh = H;
         pk.norm_w = w->shared_head_norm;
         pk.eps = cfg->rms_eps;
         pk.pack = W.xp_head;
@@ -1192,6 +1235,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
             gl.epi = EPI_STORE;
             gl.out = logits_out;
             gl.ldo = cfg->vocab;
+            gl.name = "gemm_logits";
             DF_TRY(launch_gemm_tc(gl, W.tc, s));
         }
     }

@@ -168,17 +168,23 @@ struct PackArgs {
     const int32_t *nvalid = nullptr; // rows t = s*rows_per_seq + j are valid iff j < nvalid[s]
     int rows_per_seq = 1;
     int32_t *status = nullptr;
+    // Optional deferred split-K sums added to the row after src, in split order:
+    // x[t, k] = src[t, k] + part[0][t, k] + ... + part[n_part-1][t, k]
+    const float *part = nullptr;
+    int n_part = 0;
+    size_t part_stride = 0;          // floats between splits
+    int ldpart = 0;                  // floats between rows of one split
 };
 int launch_pack(const PackArgs &a, cudaStream_t s);
 
 enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
 
 struct GemmArgs {
-    // Weight rows (BF16 [rows, K] row-major). Up to three segments concatenated along the
-    // output dimension: rows [0,n0) of W0, then n1 rows of W1, then n2 rows of W2.
+    // Weight rows (BF16 [rows, K] row-major). Up to four segments concatenated along the
+    // output dimension: rows [0,n0) of W0, then n1 rows of W1, n2 of W2, n3 of W3.
     // EPI_SWIGLU pairs row j of W0 (gate) with row j of W1 (up): N = n0 = n1.
-    const uint16_t *W0 = nullptr, *W1 = nullptr, *W2 = nullptr;
-    int n0 = 0, n1 = 0, n2 = 0;
+    const uint16_t *W0 = nullptr, *W1 = nullptr, *W2 = nullptr, *W3 = nullptr;
+    int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
     // Optional split along K for segment 0: columns [K1, K) read from Wk2 [n0, K-K1].
     const uint16_t *Wk2 = nullptr;
     int K1 = 0;
@@ -189,6 +195,11 @@ struct GemmArgs {
     int ldx2 = 0;
     int32_t *status = nullptr;
     const char *name = "gemm_tc_kernel";   // label in launch profiles
+    // Deferred split-K (EPI_STORE only): the output is S partial sums, split s of token t at
+    // out[s * part_stride + t * ldo + n]; the consuming kernel adds them in split order.
+    // The number of splits S is returned through launch_gemm_tc's n_partials_out.
+    int defer = 0;
+    size_t part_stride = 0;
     int epi = EPI_STORE;
     float *out = nullptr;            // EPI_STORE / EPI_RESID: out[t*ldo + n]
     int ldo = 0;
@@ -244,6 +255,16 @@ struct QkArgs {
     int append_block;               // 1: block rows are appended to the cache (MTP)
     int pos_off;                    // added to block positions (MTP chained step)
     int32_t *status;
+    // Deferred split-K: when part is set the projections are the sum of n_part splits
+    // part[s * part_stride + row * ldq + col] instead of qkv.
+    const float *part = nullptr;
+    int n_part = 0;
+    size_t part_stride = 0;
+    // Optional sigmoid-gate pre-activations (n_gate_heads heads after q|k|v, block rows only),
+    // reduced like q/k/v and stored to gate_out[row * ldg + h * d + e].
+    int n_gate_heads = 0;
+    float *gate_out = nullptr;
+    int ldg = 0;
 };
 int launch_qk_rope(const QkArgs &a, cudaStream_t s);
 

@@ -56,7 +56,7 @@ __global__ void qk_rope_kernel(QkArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wpb = blockDim.x >> 5;
-    const int slots = a.nq + 2 * a.nkv;
+    const int slots = a.nq + 2 * a.nkv + a.n_gate_heads;
     const int T_blk = a.B * a.blk;
     const int T_all = T_blk + a.B * a.n_new_max;
     const long long gw = (long long)blockIdx.x * wpb + warp;
@@ -74,19 +74,50 @@ __global__ void qk_rope_kernel(QkArgs a) {
     } else {
         b = (row - T_blk) / a.n_new_max;
         i = (row - T_blk) % a.n_new_max;
-        if (slot < a.nq) return;                        // context rows feed only K/V
+        if (slot < a.nq || slot >= a.nq + 2 * a.nkv) return;   // context rows feed only K/V
         int nn = min(max(a.n_new[b], 0), a.n_new_max);
         if (i >= nn) return;
     }
+    const bool is_gate = slot >= a.nq + 2 * a.nkv;
     const bool is_q = slot < a.nq;
     const bool is_k = !is_q && slot < a.nq + a.nkv;
-    const int head = is_q ? slot : (is_k ? slot - a.nq : slot - a.nq - a.nkv);
-    const int col = is_q ? head * d : (is_k ? a.nq * d + head * d : (a.nq + a.nkv) * d + head * d);
-    const float *src = a.qkv + (size_t)row * a.ldq + col;
+    const int head = is_gate ? slot - a.nq - 2 * a.nkv
+                             : (is_q ? slot : (is_k ? slot - a.nq : slot - a.nq - a.nkv));
+    const int col = is_gate ? (a.nq + 2 * a.nkv) * d + head * d
+                            : (is_q ? head * d
+                                    : (is_k ? a.nq * d + head * d : (a.nq + a.nkv) * d + head * d));
 
     float x[8];
+    if (a.part) {
+        // deferred split-K: every split is loaded first, then summed in split order
 #pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = (u < ept) ? src[lane + 32 * u] : 0.f;
+        for (int u = 0; u < 8; ++u) x[u] = 0.f;
+        for (int sp0 = 0; sp0 < a.n_part; sp0 += 4) {
+            float pv[4][8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float *src = a.part + (size_t)(sp0 + j) * a.part_stride + (size_t)row * a.ldq + col;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    pv[j][u] = (sp0 + j < a.n_part && u < ept) ? src[lane + 32 * u] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] += pv[j][u];
+        }
+    } else {
+        const float *src = a.qkv + (size_t)row * a.ldq + col;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = (u < ept) ? src[lane + 32 * u] : 0.f;
+    }
+    if (is_gate) {
+        float *g = a.gate_out + (size_t)row * a.ldg + head * d;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (u < ept) g[lane + 32 * u] = x[u];
+        return;
+    }
 
     if (!(slot >= a.nq + a.nkv)) {   // q or k: per-head RMSNorm, then RoPE
         const float *nw = is_q ? a.q_norm : a.k_norm;
@@ -482,7 +513,7 @@ int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const 
 }
 
 int launch_qk_rope(const QkArgs &a, cudaStream_t s) {
-    long long warps = (long long)(a.B * a.blk + a.B * a.n_new_max) * (a.nq + 2 * a.nkv);
+    long long warps = (long long)(a.B * a.blk + a.B * a.n_new_max) * (a.nq + 2 * a.nkv + a.n_gate_heads);
     if (warps <= 0) return DF_OK;
     const int wpb = 8;
     long long grid = (warps + wpb - 1) / wpb;

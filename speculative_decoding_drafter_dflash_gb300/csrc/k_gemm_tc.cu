@@ -55,6 +55,9 @@ struct TcParams {
     int pair;
     int T, NC, acc_cols, alloc_cols;
     int n_tiles, G, stages;
+    int splits;              // > 0: unit u = (tile u / splits, K split u % splits); 0: stream-K
+    int n_units;
+    size_t part_stride;      // split mode: output of split s starts at out + s * part_stride
     long long total_kb;
     uint32_t stage_bytes;
     uint32_t idesc;
@@ -238,6 +241,39 @@ __device__ __forceinline__ int cta_of(long long x, const TcParams &p) {
     return (int)(((x + 1) * (long long)p.G - 1) / p.total_kb);
 }
 
+// The segments (tile m, K blocks [k0, k1), split index) a CTA works on, in order. Stream-K:
+// one contiguous range of the (tile, K block) space. Split mode: units blockIdx.x + i * G.
+struct Work {
+    long long x, end;
+    int u;
+    __device__ __forceinline__ void init(const TcParams &p) {
+        if (p.splits) {
+            u = blockIdx.x;
+        } else {
+            x = kb_start(blockIdx.x, p);
+            end = kb_start(blockIdx.x + 1, p);
+        }
+    }
+    __device__ __forceinline__ bool next(const TcParams &p, int &m, int &k0, int &k1, int &split) {
+        if (p.splits) {
+            if (u >= p.n_units) return false;
+            m = u / p.splits;
+            split = u - m * p.splits;
+            k0 = split * p.kbt / p.splits;
+            k1 = (split + 1) * p.kbt / p.splits;
+            u += gridDim.x;
+            return true;
+        }
+        if (x >= end) return false;
+        m = (int)(x / p.kbt);
+        k0 = (int)(x - (long long)m * p.kbt);
+        k1 = (int)min((long long)p.kbt, end - (long long)m * p.kbt);
+        split = 0;
+        x = (long long)m * p.kbt + k1;
+        return true;
+    }
+};
+
 __device__ __forceinline__ int seg_of_tile(int m, const TcParams &p) {
     int s = 0;
     while (s + 1 < p.n_seg && m >= p.seg_tile0[s + 1]) ++s;
@@ -267,18 +303,20 @@ struct EpiSmem {
 // Apply the epilogue op to tokens [t0, t0 + kTokChunk) of tile m for this thread's row r.
 // Every epilogue thread calls this (the SwiGLU and argmax paths synchronise the 128 threads).
 __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, int m, int r,
-                                          int q, int lane, int t0, const float (&y)[kTokChunk]) {
+                                          int q, int lane, int t0, const float (&y)[kTokChunk],
+                                          int split) {
     int n_out, s;
     const bool valid = tile_row(p, m, r, n_out, s);
     if (p.epi == EPI_STORE || p.epi == EPI_RESID) {
         if (valid) {
+            float *out = p.out + (size_t)split * p.part_stride;
 #pragma unroll
             for (int i = 0; i < kTokChunk; ++i) {
                 int t = t0 + i;
                 if (t < p.T) {
                     float v = y[i];
                     if (p.epi == EPI_RESID) v += p.resid[(size_t)t * p.ldr + n_out];
-                    p.out[(size_t)t * p.ldo + n_out] = v;
+                    out[(size_t)t * p.ldo + n_out] = v;
                 }
             }
         }
@@ -371,7 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const long long my_begin = kb_start(blockIdx.x, p), my_end = kb_start(blockIdx.x + 1, p);
 
     pdl_trigger();
     if (warp == 0) {
@@ -379,32 +416,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // Weights do not depend on earlier kernels: the first stages' weight tiles are
             // requested before waiting for the predecessor grid, activation tiles after.
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            const long long count = my_end - my_begin;
-            const int pre = (int)min((long long)p.stages, count);
-            // (tile, k-block) cursor advanced without divisions: one TMA issue per k-block
-            // must stay far cheaper than the ~700 cycles a 16 KB tile takes to stream per SM.
+            // (tile, k-block) cursor: one TMA issue per k-block must stay far cheaper than the
+            // ~700 cycles a 16 KB weight tile takes to stream into one SM.
             struct Cursor {
-                int m, kb, s, row0;
+                Work w;
+                int m, kb, k1, split, s, row0;
+                bool valid;
             };
-            auto cursor_at = [&](long long x) {
-                Cursor c;
-                c.m = (int)(x / p.kbt);
-                c.kb = (int)(x - (long long)c.m * p.kbt);
+            auto seg_setup = [&](Cursor &c) {
                 c.s = p.pair ? 0 : seg_of_tile(c.m, p);
                 c.row0 = p.pair ? c.m * 64 : (c.m - p.seg_tile0[c.s]) * kBM;
-                return c;
+            };
+            auto cursor_init = [&](Cursor &c) {
+                c.w.init(p);
+                c.valid = c.w.next(p, c.m, c.kb, c.k1, c.split);
+                while (c.valid && c.kb >= c.k1) c.valid = c.w.next(p, c.m, c.kb, c.k1, c.split);
+                if (c.valid) seg_setup(c);
             };
             auto advance = [&](Cursor &c) {
-                if (++c.kb == p.kbt) {
-                    c.kb = 0;
-                    ++c.m;
-                    if (p.pair) {
-                        c.row0 = c.m * 64;
-                    } else {
-                        if (c.s + 1 < p.n_seg && c.m >= p.seg_tile0[c.s + 1]) ++c.s;
-                        c.row0 = (c.m - p.seg_tile0[c.s]) * kBM;
-                    }
-                }
+                if (++c.kb < c.k1) return;
+                do {
+                    c.valid = c.w.next(p, c.m, c.kb, c.k1, c.split);
+                } while (c.valid && c.kb >= c.k1);
+                if (c.valid) seg_setup(c);
             };
             auto load_a = [&](const Cursor &c, int stage) {
                 uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
@@ -423,23 +457,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int kx = (ks ? c.kb - p.kb_seg0 : c.kb) * kBK;
                 tma_load_2d(b, &p.bmap[ks], &full[stage], kx, 0, pol_x);
             };
-            Cursor cur = cursor_at(my_begin);
-            for (int i = 0; i < pre; ++i) {
-                mbar_expect_tx(&full[i], p.stage_bytes);
-                load_a(cur, i);
+            // Weights do not depend on earlier kernels: the first stages' weight tiles are
+            // requested before waiting for the predecessor grid, activation tiles after.
+            Cursor cur;
+            cursor_init(cur);
+            int pre = 0;
+            while (cur.valid && pre < p.stages) {
+                mbar_expect_tx(&full[pre], p.stage_bytes);
+                load_a(cur, pre);
                 advance(cur);
+                ++pre;
             }
             pdl_wait();
-            Cursor cb = cursor_at(my_begin);
-            for (int i = 0; i < pre; ++i) {
-                load_b(cb, i);
-                advance(cb);
+            {
+                Cursor cb;
+                cursor_init(cb);
+                for (int i = 0; i < pre; ++i) {
+                    load_b(cb, i);
+                    advance(cb);
+                }
             }
             int stage = pre % p.stages;
             uint32_t phase = (pre == p.stages) ? 1u : 0u;
             long long issued = pre;
             bool ok = true;
-            for (long long x = my_begin + pre; x < my_end; ++x) {
+            while (cur.valid) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -466,11 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            for (long long x = my_begin; x < my_end && ok;) {
-                const int m = (int)(x / p.kbt);
-                const int k0 = (int)(x - (long long)m * p.kbt);
-                const int k1 = (int)min((long long)p.kbt, my_end - (long long)m * p.kbt);
-                x = (long long)m * p.kbt + k1;
+            Work w;
+            w.init(p);
+            int m, k0, k1, split;
+            while (ok && w.next(p, m, k0, k1, split)) {
+                if (k0 >= k1) continue;
                 if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * p.acc_cols);
@@ -512,13 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int r = q * 32 + lane;     // tile row of this thread
         int acc = 0;
         uint32_t aphase = 0;
-        for (long long x = my_begin; x < my_end;) {
-            const int m = (int)(x / p.kbt);
-            const int k0 = (int)(x - (long long)m * p.kbt);
-            const int k1 = (int)min((long long)p.kbt, my_end - (long long)m * p.kbt);
-            x = (long long)m * p.kbt + k1;
-            const bool whole = (k0 == 0 && k1 == p.kbt);
-            const int slot = (kb_start(blockIdx.x, p) / p.kbt == m) ? 0 : 1;
+        Work w;
+        w.init(p);
+        int m, k0, k1, split;
+        while (w.next(p, m, k0, k1, split)) {
+            if (k0 >= k1) continue;
+            const bool whole = p.splits || (k0 == 0 && k1 == p.kbt);
+            const int slot = (!p.splits && kb_start(blockIdx.x, p) / p.kbt == m) ? 0 : 1;
             const bool got = mbar_wait(&tfull[acc], aphase, abort_flag, p.status);
             if (epi_any(!got)) break;   // all four epilogue warps leave together
             tc_fence_after();
@@ -538,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 for (int i = 0; i < kTokChunk; ++i)
                     y[i] = __uint_as_float(v[2 * i]) + __uint_as_float(v[2 * i + 1]);
                 if (whole) {
-                    epi_apply(p, es, m, r, q, lane, c * kTokChunk, y);
+                    epi_apply(p, es, m, r, q, lane, c * kTokChunk, y, split);
                 } else {
 #pragma unroll
                     for (int i = 0; i < kTokChunk; ++i) {
@@ -594,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                                 for (int i = 0; i < kTokChunk; ++i) y[i] += v8[j][i];
                         }
-                        epi_apply(p, es, m, r, q, lane, c * kTokChunk, y);
+                        epi_apply(p, es, m, r, q, lane, c * kTokChunk, y, split);
                     }
                     if (r == 0) p.counters[m] = 0;
                 }
@@ -683,10 +725,10 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
         DF_TRY(make_map(&p.amap[0], a.W0, K0, a.n0, K0, kBK, kBM));
         DF_TRY(make_map(&p.amap[1], a.Wk2, K1, a.n0, K1, kBK, kBM));
     } else {
-        const uint16_t *W[3] = {a.W0, a.W1, a.W2};
-        const int rows[3] = {a.n0, a.n1, a.n2};
+        const uint16_t *W[4] = {a.W0, a.W1, a.W2, a.W3};
+        const int rows[4] = {a.n0, a.n1, a.n2, a.n3};
         int tiles = 0, col = 0, ns = 0;
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < 4; ++i) {
             if (rows[i] <= 0 || W[i] == nullptr) continue;
             p.seg_rows[ns] = rows[i];
             p.seg_tile0[ns] = tiles;
@@ -703,7 +745,22 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
     DF_TRY(make_map(&p.bmap[0], a.X, K0, 2 * T, a.ldx, kBK, NC));
     if (a.Wk2) DF_TRY(make_map(&p.bmap[1], a.X2, K1, 2 * T, a.ldx2, kBK, NC));
     p.total_kb = (long long)p.n_tiles * p.kbt;
-    p.G = (int)std::min<long long>(sc.max_ctas, p.total_kb);
+    if (a.defer) {
+        // Uniform K splits of every tile, as many as fill the GPU once; no cross-CTA reduction.
+        int S = std::max(1, sc.max_ctas / p.n_tiles);
+        S = std::min(S, p.kbt);
+        p.splits = S;
+        p.n_units = p.n_tiles * S;
+        p.part_stride = a.part_stride;
+        p.G = std::min(sc.max_ctas, p.n_units);
+    } else if (p.pair && p.n_tiles <= sc.max_ctas) {
+        // SwiGLU with at most one tile per SM: whole tiles, epilogue in place.
+        p.splits = 1;
+        p.n_units = p.n_tiles;
+        p.G = p.n_tiles;
+    } else {
+        p.G = (int)std::min<long long>(sc.max_ctas, p.total_kb);
+    }
     p.stage_bytes = kABytes + NC * 128;
     p.stages = std::min(8, (int)((200 * 1024) / p.stage_bytes));
     p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NC >> 3) << 17) |
@@ -720,14 +777,16 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
     p.scratch = sc.partials;
     p.counters = sc.counters;
     p.status = a.status;
-    if ((size_t)p.G * 2 * T * kBM > sc.partial_floats)
+    if (!p.splits && (size_t)p.G * 2 * T * kBM > sc.partial_floats)
         return fail(DF_EWORKSPACE, "GEMM scratch too small (%d tokens)", T);
+    if (a.defer && (a.epi != EPI_STORE || a.part_stride < (size_t)T * a.ldo))
+        return fail(DF_EINVAL, "deferred split-K needs a plain store into S x T x ldo floats");
     if (p.n_tiles > sc.n_counters)
         return fail(DF_EWORKSPACE, "GEMM tile counters too few (%d tiles)", p.n_tiles);
     size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 5) * 8 + 16 +
                   (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
                   (size_t)T * sizeof(ArgTop) + 64;
-    if (G_out) *G_out = p.G;
+    if (G_out) *G_out = a.defer ? p.splits : p.G;
     return launch_k(a.name, gemm_tc_kernel, dim3(p.G), dim3(kThreads), smem, s, p);
 }
 
@@ -748,7 +807,7 @@ int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *
         if (a.out) c.out = a.out + (size_t)t0 * a.ldo;
         if (a.resid) c.resid = a.resid + (size_t)t0 * a.ldr;
         if (a.pack_out) c.pack_out = a.pack_out + (size_t)2 * t0 * a.ldpo;
-        DF_TRY(launch_chunk(c, sc, s, nullptr));
+        DF_TRY(launch_chunk(c, sc, s, n_partials_out));
     }
     return DF_OK;
 }

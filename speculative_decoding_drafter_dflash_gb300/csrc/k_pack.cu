@@ -52,7 +52,9 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
     auto load = [&](int k) -> float {
         if (!valid) return 0.f;
         if (a.gather) return bf16_bits_to_f32(a.gather[(size_t)id * K + k]) * a.scale;
-        return a.src[(size_t)t * a.lds + k];
+        float x = a.src ? a.src[(size_t)t * a.lds + k] : 0.f;
+        for (int sp = 0; sp < a.n_part; ++sp) x += a.part[sp * a.part_stride + (size_t)t * a.ldpart + k];
+        return x;
     };
 
     float inv = 1.f;
@@ -111,11 +113,37 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
                                 __uint_as_float(g.x & 0xffff0000u) * a.scale,
                                 __uint_as_float(g.y << 16) * a.scale,
                                 __uint_as_float(g.y & 0xffff0000u) * a.scale);
-            } else {
+            } else if (a.src) {
                 v = *reinterpret_cast<const float4 *>(a.src + (size_t)t * a.lds + 4 * k4);
             }
         }
         x[u] = v;
+    }
+    if (a.part && valid) {
+        // every split's values are loaded before any is added; the sum runs in split order
+        for (int sp0 = 0; sp0 < a.n_part; sp0 += 4) {
+            float4 pv[4][NV];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int u = 0; u < NV; ++u) {
+                    const int k4 = threadIdx.x + u * kPackThreads;
+                    pv[j][u] = (sp0 + j < a.n_part && k4 < K4)
+                                   ? *reinterpret_cast<const float4 *>(
+                                         a.part + (size_t)(sp0 + j) * a.part_stride +
+                                         (size_t)t * a.ldpart + 4 * k4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int u = 0; u < NV; ++u) {
+                    x[u].x += pv[j][u].x;
+                    x[u].y += pv[j][u].y;
+                    x[u].z += pv[j][u].z;
+                    x[u].w += pv[j][u].w;
+                }
+        }
     }
     float inv = 1.f;
     if (a.norm_w) {
@@ -156,6 +184,7 @@ bool aligned_for_vec(const PackArgs &a) {
     auto al = [](const void *p, int bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; };
     if (a.K % 4) return false;
     if (a.src && (!al(a.src, 16) || a.lds % 4)) return false;
+    if (a.part && (!al(a.part, 16) || a.ldpart % 4 || a.part_stride % 4)) return false;
     if (a.gather && !al(a.gather, 8)) return false;
     if (a.h_out && (!al(a.h_out, 16) || a.ldh % 4)) return false;
     if (a.norm_w && !al(a.norm_w, 16)) return false;
