@@ -173,7 +173,7 @@ __global__ void qk_rope_kernel(QkArgs a) {
         if (u < ept) dst[lane + 32 * u] = x[u];
 }
 
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 512;
 constexpr int kAttnStages = 4;
 constexpr int kTileBytes = 32768;          // K + V bytes of one key tile
 constexpr int kKeyGroup = 8;               // keys per online-softmax update
@@ -211,18 +211,21 @@ __device__ __forceinline__ void attn_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
-// Split-KV attention for one (key chunk, KV head, sequence). Each lane owns 64 (or D) of the
-// head dimensions of one query row (LPR lanes per row); warps split the query rows into row
-// groups and the keys of every tile into key subsets. Key/value tiles stream into shared
-// memory through bulk copies (4 stages). Scores are kept in log2 units (q is pre-scaled by
-// log2(e)/sqrt(D)). The CTA merges its warps, writes one partial (o, m, l) per query row, and
-// the last CTA of the (sequence, KV head) merges the chunk partials in chunk order, applies the
-// optional sigmoid gate and packs the output for the O projection.
+// Split-KV attention for one (key chunk, KV head, sequence). Each query row is owned by
+// LPR = D/32 lanes; lane sub of a row holds the interleaved head dimensions
+// {4*LPR*j + 4*sub + c} of q and of the running output (32 floats each), so at every step the
+// LPR lanes of a row read adjacent 16-byte words of a key row (no bank conflicts, no index
+// arithmetic in the inner loop) and the rows of a warp share them by broadcast. Warps split
+// the query rows into row groups and every key tile into key subsets. Key/value tiles stream
+// into shared memory through bulk copies (4 stages). Scores are kept in log2 units (q is
+// pre-scaled by log2(e)/sqrt(D)). The CTA merges its key subsets and writes one partial
+// (o, m, l) per query row; attn_combine_kernel merges the chunks.
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
-    constexpr int LPR = D >= 64 ? D / 64 : 1;
-    constexpr int DL = D / LPR;
+    constexpr int LPR = D / 32;
+    constexpr int DL = 32;
     constexpr int RPW = 32 / LPR;
+    constexpr int NW = kAttnThreads / 32;
     constexpr int TK = kTileBytes / (2 * D * 4);
     extern __shared__ __align__(128) uint8_t sm_raw[];
     float *tiles = reinterpret_cast<float *>(sm_raw);
@@ -235,9 +238,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     const int rep = a.nq / a.nkv;
     const int R = a.blk * rep;
     const int RG = (R + RPW - 1) / RPW;
-    const int KS = RG >= 8 ? 1 : 8 / RG;
+    const int KS = RG >= NW ? 1 : NW / RG;
     const int rg = warp % RG, ks = warp / RG;
-    const bool active = ks < KS;
+    const bool active = ks < KS && warp < RG * KS;
     const int sub = lane / RPW, row = lane % RPW;
     const int rr = rg * RPW + row;
     const bool row_valid = active && rr < R;
@@ -252,14 +255,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     const int n_tiles = (c1 - c0 + TK - 1) / TK;
     const size_t head_off = (size_t)b * a.nkv + g;
 
-    // this lane's q slice, rotated by 4*sub floats so the LPR lanes of a row hit different banks
     float2 q2[DL / 2];
     {
         const float qs = 1.4426950408889634f / sqrtf((float)D);
-        const float *qp = a.q + (((size_t)b * a.blk + tok) * a.nq + qh) * D + sub * DL;
+        const float *qp = a.q + (((size_t)b * a.blk + tok) * a.nq + qh) * D + 4 * sub;
 #pragma unroll
         for (int j = 0; j < DL / 4; ++j) {
-            float4 v = row_valid ? *reinterpret_cast<const float4 *>(qp + ((4 * j + 4 * sub) % DL))
+            float4 v = row_valid ? *reinterpret_cast<const float4 *>(qp + 4 * LPR * j)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             q2[2 * j] = make_float2(v.x * qs, v.y * qs);
             q2[2 * j + 1] = make_float2(v.z * qs, v.w * qs);
@@ -309,20 +311,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
         attn_wait(&full[st], (uint32_t)((jt / kAttnStages) & 1), a.status);
         const int t0 = c0 + jt * TK;
         const int n = min(TK, c1 - t0);
-        const float *kt = tiles + (size_t)st * (kTileBytes / 4);
+        const float *kt = tiles + (size_t)st * (kTileBytes / 4) + 4 * sub;
         const float *vt = kt + TK * D;
         const int kbeg = ks * KW, kend = min(n, kbeg + KW);
         if (active) {
             for (int k0 = kbeg; k0 < kend; k0 += kKeyGroup) {
+                const int nk = min(kKeyGroup, kend - k0);
                 float s[kKeyGroup];
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
-                    const int kk = min(k0 + u, n - 1);
-                    const float *kr = kt + (size_t)kk * D + sub * DL;
+                    const float *kr = kt + (size_t)(k0 + min(u, nk - 1)) * D;
                     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int j = 0; j < DL / 4; ++j) {
-                        const float4 kv = *reinterpret_cast<const float4 *>(kr + ((4 * j + 4 * sub) % DL));
+                        const float4 kv = *reinterpret_cast<const float4 *>(kr + 4 * LPR * j);
                         acc = __ffma2_rn(q2[2 * j], make_float2(kv.x, kv.y), acc);
                         acc = __ffma2_rn(q2[2 * j + 1], make_float2(kv.z, kv.w), acc);
                     }
@@ -332,8 +334,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
                 for (int u = 0; u < kKeyGroup; ++u) {
 #pragma unroll
                     for (int o = RPW; o < 32; o <<= 1) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
-                    const int key = t0 + k0 + u;
-                    bool ok = row_valid && (k0 + u) < kend;
+                }
+                const int key0 = t0 + k0;
+#pragma unroll
+                for (int u = 0; u < kKeyGroup; ++u) {
+                    bool ok = row_valid && u < nk;
+                    const int key = key0 + u;
                     if (a.causal_block && key >= S_cache && key - S_cache > tok) ok = false;
                     if (!ok) s[u] = -INFINITY;
                 }
@@ -356,12 +362,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
                 for (int j = 0; j < DL / 2; ++j) o2[j] = __fmul2_rn(o2[j], c2);
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
-                    const int kk = min(k0 + u, n - 1);
-                    const float *vr = vt + (size_t)kk * D + sub * DL;
+                    const float *vr = vt + (size_t)(k0 + min(u, nk - 1)) * D;
                     const float2 pu = make_float2(p[u], p[u]);
 #pragma unroll
                     for (int j = 0; j < DL / 4; ++j) {
-                        const float4 vv = *reinterpret_cast<const float4 *>(vr + ((4 * j + 4 * sub) % DL));
+                        const float4 vv = *reinterpret_cast<const float4 *>(vr + 4 * LPR * j);
                         o2[2 * j] = __ffma2_rn(pu, make_float2(vv.x, vv.y), o2[2 * j]);
                         o2[2 * j + 1] = __ffma2_rn(pu, make_float2(vv.z, vv.w), o2[2 * j + 1]);
                     }
@@ -378,10 +383,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     float *mm = mo + (size_t)KS * rows_cta * D;         // [KS][rows_cta]
     float *ml = mm + KS * rows_cta;                     // [KS][rows_cta]
     if (active) {
-        float *dst = mo + ((size_t)ks * rows_cta + rr) * D + sub * DL;
+        float *dst = mo + ((size_t)ks * rows_cta + rr) * D + 4 * sub;
 #pragma unroll
         for (int j = 0; j < DL / 4; ++j)
-            *reinterpret_cast<float4 *>(dst + ((4 * j + 4 * sub) % DL)) =
+            *reinterpret_cast<float4 *>(dst + 4 * LPR * j) =
                 make_float4(o2[2 * j].x, o2[2 * j].y, o2[2 * j + 1].x, o2[2 * j + 1].y);
         if (sub == 0) {
             mm[ks * rows_cta + rr] = m;
@@ -408,7 +413,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
             part[(size_t)r2 * (D + 2) + D + 1] = L;
         }
     }
-
 }
 
 // Merge of the chunk partials: one warp per (query row, sequence, KV head) group of rows. Lane c
@@ -543,11 +547,15 @@ void attn_plan(AttnArgs &a, int max_keys) {
 template <int D>
 int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     const int R = a.blk * (a.nq / a.nkv);
-    constexpr int RPW = 32 / (D >= 64 ? D / 64 : 1);
-    if ((R + RPW - 1) / RPW > 8) return fail(DF_ESHAPE, "attention: %d query rows per KV head exceed %d", R, 8 * RPW);
+    constexpr int RPW = 32 / (D / 32);
+    constexpr int NW = kAttnThreads / 32;
+    if ((R + RPW - 1) / RPW > NW)
+        return fail(DF_ESHAPE, "attention: %d query rows per KV head exceed %d", R, NW * RPW);
+    // stage buffers, reused at the end for the key-subset merge (KS * rows_cta <= NW * RPW rows)
     size_t smem = (size_t)kAttnStages * kTileBytes + kAttnStages * 8 + 16;
-    size_t need_merge = sizeof(float) * ((size_t)8 * 32 * (D / (D >= 64 ? D / 64 : 1) + 2) + 512);
-    smem = std::max(smem, need_merge);
+    size_t need_merge = sizeof(float) * ((size_t)NW * RPW * (D + 2));
+    if (need_merge > (size_t)kAttnStages * kTileBytes)
+        return fail(DF_ESHAPE, "attention: merge buffer exceeds the stage buffers");
     dim3 grid(a.n_chunks, a.nkv, a.B);
     DF_TRY(launch_k("attn_kernel", attn_kernel<D>, grid, dim3(kAttnThreads), smem, s, a));
     dim3 cgrid((R + 7) / 8, a.nkv, a.B);
