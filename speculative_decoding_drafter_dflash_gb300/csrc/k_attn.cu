@@ -173,7 +173,7 @@ __global__ void qk_rope_kernel(QkArgs a) {
         if (u < ept) dst[lane + 32 * u] = x[u];
 }
 
-constexpr int kAttnThreads = 512;
+constexpr int kAttnThreads = 256;
 constexpr int kAttnStages = 4;
 constexpr int kTileBytes = 32768;          // K + V bytes of one key tile
 constexpr int kKeyGroup = 8;               // keys per online-softmax update
@@ -211,20 +211,22 @@ __device__ __forceinline__ void attn_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
-// Split-KV attention for one (key chunk, KV head, sequence). Each query row is owned by
-// LPR = D/32 lanes; lane sub of a row holds the interleaved head dimensions
-// {4*LPR*j + 4*sub + c} of q and of the running output (32 floats each), so at every step the
-// LPR lanes of a row read adjacent 16-byte words of a key row (no bank conflicts, no index
-// arithmetic in the inner loop) and the rows of a warp share them by broadcast. Warps split
-// the query rows into row groups and every key tile into key subsets. Key/value tiles stream
-// into shared memory through bulk copies (4 stages). Scores are kept in log2 units (q is
+// Split-KV attention for one (key chunk, KV head, sequence). A "row set" is RPL query rows of
+// one block token whose q heads share this KV head (RPL = 2 when the GQA group allows), so
+// every key/value element a lane loads from shared memory feeds RPL rows. Each row set is
+// owned by LPR = D/32 lanes; lane sub of a row set holds the interleaved head dimensions
+// {4*LPR*j + 4*sub + c} of q and of the running outputs (32 floats per row), so at every step
+// the LPR lanes read adjacent 16-byte words of a key row (no bank conflicts, no index
+// arithmetic in the inner loop) and the row sets of a warp share them by broadcast. Warps
+// split the row sets into row groups and every key tile into key subsets. Key/value tiles
+// stream into shared memory through bulk copies. Scores are kept in log2 units (q is
 // pre-scaled by log2(e)/sqrt(D)). The CTA merges its key subsets and writes one partial
 // (o, m, l) per query row; attn_combine_kernel merges the chunks.
-template <int D>
+template <int D, int RPL>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     constexpr int LPR = D / 32;
     constexpr int DL = 32;
-    constexpr int RPW = 32 / LPR;
+    constexpr int RPW = 32 / LPR;                  // row sets per warp
     constexpr int NW = kAttnThreads / 32;
     constexpr int TK = kTileBytes / (2 * D * 4);
     extern __shared__ __align__(128) uint8_t sm_raw[];
@@ -236,16 +238,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     pdl_trigger();
     pdl_wait();
     const int rep = a.nq / a.nkv;
-    const int R = a.blk * rep;
-    const int RG = (R + RPW - 1) / RPW;
+    const int R = a.blk * rep;                     // query rows of this KV head
+    const int NS = R / RPL;                        // row sets
+    const int RG = (NS + RPW - 1) / RPW;
     const int KS = RG >= NW ? 1 : NW / RG;
     const int rg = warp % RG, ks = warp / RG;
     const bool active = ks < KS && warp < RG * KS;
-    const int sub = lane / RPW, row = lane % RPW;
-    const int rr = rg * RPW + row;
-    const bool row_valid = active && rr < R;
-    const int tok = row_valid ? rr / rep : 0;
-    const int qh = g * rep + (row_valid ? rr % rep : 0);
+    const int sub = lane / RPW, rsl = lane % RPW;
+    const int rs = rg * RPW + rsl;                 // row set of this lane
+    const bool set_valid = active && rs < NS;
+    // rows rr = rs * RPL + r: token rr / rep, q head g * rep + rr % rep
+    const int tok = set_valid ? (rs * RPL) / rep : 0;
 
     const int nn = a.n_new ? min(max(a.n_new[b], 0), a.n_new_max) : 0;
     const long long sc = (long long)a.seq_len[b] + nn + a.extra_rows;
@@ -255,22 +258,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     const int n_tiles = (c1 - c0 + TK - 1) / TK;
     const size_t head_off = (size_t)b * a.nkv + g;
 
-    float2 q2[DL / 2];
+    float2 q2[RPL][DL / 2];
     {
         const float qs = 1.4426950408889634f / sqrtf((float)D);
-        const float *qp = a.q + (((size_t)b * a.blk + tok) * a.nq + qh) * D + 4 * sub;
 #pragma unroll
-        for (int j = 0; j < DL / 4; ++j) {
-            float4 v = row_valid ? *reinterpret_cast<const float4 *>(qp + 4 * LPR * j)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-            q2[2 * j] = make_float2(v.x * qs, v.y * qs);
-            q2[2 * j + 1] = make_float2(v.z * qs, v.w * qs);
+        for (int r = 0; r < RPL; ++r) {
+            const int rr = rs * RPL + r;
+            const int qh = g * rep + (set_valid ? rr % rep : 0);
+            const float *qp = a.q + (((size_t)b * a.blk + tok) * a.nq + qh) * D + 4 * sub;
+#pragma unroll
+            for (int j = 0; j < DL / 4; ++j) {
+                float4 v = set_valid ? *reinterpret_cast<const float4 *>(qp + 4 * LPR * j)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                q2[r][2 * j] = make_float2(v.x * qs, v.y * qs);
+                q2[r][2 * j + 1] = make_float2(v.z * qs, v.w * qs);
+            }
         }
     }
-    float2 o2[DL / 2];
+    float2 o2[RPL][DL / 2];
+    float m[RPL], l[RPL];
 #pragma unroll
-    for (int j = 0; j < DL / 2; ++j) o2[j] = make_float2(0.f, 0.f);
-    float m = -INFINITY, l = 0.f;
+    for (int r = 0; r < RPL; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < DL / 2; ++j) o2[r][j] = make_float2(0.f, 0.f);
+    }
 
     auto issue = [&](int jt) {
         const int st = jt % kAttnStages;
@@ -317,58 +330,86 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
         if (active) {
             for (int k0 = kbeg; k0 < kend; k0 += kKeyGroup) {
                 const int nk = min(kKeyGroup, kend - k0);
-                float s[kKeyGroup];
+                float s[kKeyGroup][RPL];
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
                     const float *kr = kt + (size_t)(k0 + min(u, nk - 1)) * D;
-                    float2 acc = make_float2(0.f, 0.f);
+                    float2 acc[RPL];
+#pragma unroll
+                    for (int r = 0; r < RPL; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int j = 0; j < DL / 4; ++j) {
                         const float4 kv = *reinterpret_cast<const float4 *>(kr + 4 * LPR * j);
-                        acc = __ffma2_rn(q2[2 * j], make_float2(kv.x, kv.y), acc);
-                        acc = __ffma2_rn(q2[2 * j + 1], make_float2(kv.z, kv.w), acc);
+                        const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            acc[r] = __ffma2_rn(q2[r][2 * j], k01, acc[r]);
+                            acc[r] = __ffma2_rn(q2[r][2 * j + 1], k23, acc[r]);
+                        }
                     }
-                    s[u] = acc.x + acc.y;
+#pragma unroll
+                    for (int r = 0; r < RPL; ++r) s[u][r] = acc[r].x + acc[r].y;
                 }
 #pragma unroll
-                for (int u = 0; u < kKeyGroup; ++u) {
+                for (int u = 0; u < kKeyGroup; ++u)
 #pragma unroll
-                    for (int o = RPW; o < 32; o <<= 1) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
-                }
+                    for (int r = 0; r < RPL; ++r)
+#pragma unroll
+                        for (int o = RPW; o < 32; o <<= 1)
+                            s[u][r] += __shfl_xor_sync(0xffffffffu, s[u][r], o);
                 const int key0 = t0 + k0;
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
-                    bool ok = row_valid && u < nk;
+                    bool ok = set_valid && u < nk;
                     const int key = key0 + u;
                     if (a.causal_block && key >= S_cache && key - S_cache > tok) ok = false;
-                    if (!ok) s[u] = -INFINITY;
+                    if (!ok)
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) s[u][r] = -INFINITY;
                 }
-                float mt = s[0];
+                float p[kKeyGroup][RPL];
+                bool any = false;
 #pragma unroll
-                for (int u = 1; u < kKeyGroup; ++u) mt = fmaxf(mt, s[u]);
-                const float mn = fmaxf(m, mt);
-                if (mn == -INFINITY) continue;
-                const float corr = exp2f(m - mn);
-                float p[kKeyGroup], ps = 0.f;
+                for (int r = 0; r < RPL; ++r) {
+                    float mt = s[0][r];
 #pragma unroll
-                for (int u = 0; u < kKeyGroup; ++u) {
-                    p[u] = exp2f(s[u] - mn);
-                    ps += p[u];
+                    for (int u = 1; u < kKeyGroup; ++u) mt = fmaxf(mt, s[u][r]);
+                    const float mn = fmaxf(m[r], mt);
+                    if (mn == -INFINITY) {
+#pragma unroll
+                        for (int u = 0; u < kKeyGroup; ++u) p[u][r] = 0.f;
+                        continue;
+                    }
+                    any = true;
+                    const float corr = exp2f(m[r] - mn);
+                    float ps = 0.f;
+#pragma unroll
+                    for (int u = 0; u < kKeyGroup; ++u) {
+                        p[u][r] = exp2f(s[u][r] - mn);
+                        ps += p[u][r];
+                    }
+                    l[r] = l[r] * corr + ps;
+                    m[r] = mn;
+                    const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+                    for (int j = 0; j < DL / 2; ++j) o2[r][j] = __fmul2_rn(o2[r][j], c2);
                 }
-                l = l * corr + ps;
-                m = mn;
-                const float2 c2 = make_float2(corr, corr);
-#pragma unroll
-                for (int j = 0; j < DL / 2; ++j) o2[j] = __fmul2_rn(o2[j], c2);
+                if (!any) continue;
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
                     const float *vr = vt + (size_t)(k0 + min(u, nk - 1)) * D;
-                    const float2 pu = make_float2(p[u], p[u]);
+                    float2 pu[RPL];
+#pragma unroll
+                    for (int r = 0; r < RPL; ++r) pu[r] = make_float2(p[u][r], p[u][r]);
 #pragma unroll
                     for (int j = 0; j < DL / 4; ++j) {
                         const float4 vv = *reinterpret_cast<const float4 *>(vr + 4 * LPR * j);
-                        o2[2 * j] = __ffma2_rn(pu, make_float2(vv.x, vv.y), o2[2 * j]);
-                        o2[2 * j + 1] = __ffma2_rn(pu, make_float2(vv.z, vv.w), o2[2 * j + 1]);
+                        const float2 v01 = make_float2(vv.x, vv.y), v23 = make_float2(vv.z, vv.w);
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            o2[r][2 * j] = __ffma2_rn(pu[r], v01, o2[r][2 * j]);
+                            o2[r][2 * j + 1] = __ffma2_rn(pu[r], v23, o2[r][2 * j + 1]);
+                        }
                     }
                 }
             }
@@ -378,19 +419,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     }
 
     // ---- merge the key subsets of each row group (stage buffers are free now)
-    const int rows_cta = RG * RPW;
+    const int rows_cta = RG * RPW * RPL;
     float *mo = tiles;                                  // [KS][rows_cta][D]
     float *mm = mo + (size_t)KS * rows_cta * D;         // [KS][rows_cta]
     float *ml = mm + KS * rows_cta;                     // [KS][rows_cta]
     if (active) {
-        float *dst = mo + ((size_t)ks * rows_cta + rr) * D + 4 * sub;
 #pragma unroll
-        for (int j = 0; j < DL / 4; ++j)
-            *reinterpret_cast<float4 *>(dst + 4 * LPR * j) =
-                make_float4(o2[2 * j].x, o2[2 * j].y, o2[2 * j + 1].x, o2[2 * j + 1].y);
-        if (sub == 0) {
-            mm[ks * rows_cta + rr] = m;
-            ml[ks * rows_cta + rr] = l;
+        for (int r = 0; r < RPL; ++r) {
+            const int rr = rs * RPL + r;
+            float *dst = mo + ((size_t)ks * rows_cta + rr) * D + 4 * sub;
+#pragma unroll
+            for (int j = 0; j < DL / 4; ++j)
+                *reinterpret_cast<float4 *>(dst + 4 * LPR * j) =
+                    make_float4(o2[r][2 * j].x, o2[r][2 * j].y, o2[r][2 * j + 1].x, o2[r][2 * j + 1].y);
+            if (sub == 0) {
+                mm[ks * rows_cta + rr] = m[r];
+                ml[ks * rows_cta + rr] = l[r];
+            }
         }
     }
     __syncthreads();
@@ -544,30 +589,36 @@ void attn_plan(AttnArgs &a, int max_keys) {
     a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
 }
 
-template <int D>
+template <int D, int RPL>
 int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     const int R = a.blk * (a.nq / a.nkv);
     constexpr int RPW = 32 / (D / 32);
     constexpr int NW = kAttnThreads / 32;
-    if ((R + RPW - 1) / RPW > NW)
-        return fail(DF_ESHAPE, "attention: %d query rows per KV head exceed %d", R, NW * RPW);
-    // stage buffers, reused at the end for the key-subset merge (KS * rows_cta <= NW * RPW rows)
+    if ((R / RPL + RPW - 1) / RPW > NW)
+        return fail(DF_ESHAPE, "attention: %d query rows per KV head exceed %d", R, NW * RPW * RPL);
+    // stage buffers, reused at the end for the key-subset merge (KS * rows_cta <= NW*RPW*RPL rows)
     size_t smem = (size_t)kAttnStages * kTileBytes + kAttnStages * 8 + 16;
-    size_t need_merge = sizeof(float) * ((size_t)NW * RPW * (D + 2));
+    size_t need_merge = sizeof(float) * ((size_t)NW * RPW * RPL * (D + 2));
     if (need_merge > (size_t)kAttnStages * kTileBytes)
         return fail(DF_ESHAPE, "attention: merge buffer exceeds the stage buffers");
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    DF_TRY(launch_k("attn_kernel", attn_kernel<D>, grid, dim3(kAttnThreads), smem, s, a));
+    DF_TRY(launch_k("attn_kernel", attn_kernel<D, RPL>, grid, dim3(kAttnThreads), smem, s, a));
     dim3 cgrid((R + 7) / 8, a.nkv, a.B);
     return launch_k("attn_combine_kernel", attn_combine_kernel<D>, cgrid, dim3(256), 0, s, a);
 }
 
+template <int D>
+int launch_attn_r(const AttnArgs &a, cudaStream_t s) {
+    if ((a.nq / a.nkv) % 2 == 0) return launch_attn_d<D, 2>(a, s);
+    return launch_attn_d<D, 1>(a, s);
+}
+
 int launch_attn(const AttnArgs &a, cudaStream_t s) {
     switch (a.d) {
-        case 32: return launch_attn_d<32>(a, s);
-        case 64: return launch_attn_d<64>(a, s);
-        case 128: return launch_attn_d<128>(a, s);
-        case 256: return launch_attn_d<256>(a, s);
+        case 32: return launch_attn_r<32>(a, s);
+        case 64: return launch_attn_r<64>(a, s);
+        case 128: return launch_attn_r<128>(a, s);
+        case 256: return launch_attn_r<256>(a, s);
         default: return fail(DF_ESHAPE, "attention: head_dim %d not in {32, 64, 128, 256}", a.d);
     }
 }

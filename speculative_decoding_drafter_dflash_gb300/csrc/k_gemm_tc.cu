@@ -754,7 +754,7 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
         p.n_units = p.n_tiles * S;
         p.part_stride = a.part_stride;
         p.G = std::min(sc.max_ctas, p.n_units);
-    } else if (p.pair && p.n_tiles <= sc.max_ctas && getenv("DF_SWIGLU_WHOLE")) {
+    } else if (p.pair && p.n_tiles <= sc.max_ctas) {
         // SwiGLU with at most one tile per SM: whole tiles, epilogue in place.
         p.splits = 1;
         p.n_units = p.n_tiles;
