@@ -366,7 +366,7 @@ __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, 
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -763,16 +763,7 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
         p.G = (int)std::min<long long>(sc.max_ctas, p.total_kb);
     }
     p.stage_bytes = kABytes + NC * 128;
-    // Stream-K runs (the long lm_head) keep one CTA per SM with 8 stages; split/whole-tile runs
-    // use fewer stages so two CTAs fit on an SM and the next projection (launched early by
-    // programmatic dependent launch) can prefetch its weights under this one's tail.
-    static const int split_stages = [] {
-        const char *e = getenv("DF_GEMM_STAGES");
-        return e ? std::max(2, std::min(8, atoi(e))) : 5;
-    }();
-    p.stages = p.splits ? std::min(split_stages, (int)((100 * 1024) / p.stage_bytes))
-                        : std::min(8, (int)((200 * 1024) / p.stage_bytes));
-    p.stages = std::max(p.stages, 2);
+    p.stages = std::min(8, (int)((200 * 1024) / p.stage_bytes));
     p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NC >> 3) << 17) |
               ((uint32_t)(kBM >> 4) << 24);
     p.epi = a.epi;
