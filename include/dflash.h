@@ -170,6 +170,22 @@ size_t df_lm_head_workspace_bytes(int rows, int H, int V);
 int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
                    float *top1, float *top2, void *ws, size_t ws_bytes, df_stream_t stream);
 
+/*
+ * lm_head_argmax_noalloc — lm_head_argmax for callers that cannot allocate device memory:
+ * host code that runs inside an engine or plug-in which owns every allocation, or a loop that
+ * may not take cudaMalloc's implicit synchronisation. The source pages have no counterpart;
+ * the arithmetic and outputs are those of lm_head_argmax.
+ * It takes no workspace: its scratch (about 3.5 MB) is one fixed array in the library's device
+ * memory, which every GPU that loads the library holds until the process exits. Limits:
+ * rows <= 16, H <= 8192 (a multiple of 8), V <= 524288; larger sizes return DF_ESHAPE.
+ * The first call on a device looks up the array's device address with that device current, so
+ * make that first call before any stream capture. All calls share the one array and it keeps
+ * the last call's contents: the call clears the part that must start at zero itself, and calls
+ * that overlap on the GPU (other streams, other host threads) race — order them.
+ */
+int lm_head_argmax_noalloc(const uint16_t *W, const float *X, int rows, int H, int V,
+                           int32_t *idx, float *top1, float *top2, df_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------
  * One BF16-weight x F32-activation projection (mtp.rs `apply_linear_projection_f32`;
  * tensors.rs: row-major [out, in] BF16 weights consumed with F32 activations):

@@ -83,6 +83,8 @@ _SIGS = [
     ("df_lm_head_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
     ("lm_head_argmax", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
+    ("lm_head_argmax_noalloc", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                                       c_void_p, c_void_p]),
     ("df_linear_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
     ("df_linear", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
                           c_void_p]),
@@ -237,6 +239,14 @@ def df_linear(W, X, Y, ws, stream=None):
     T, K = X.shape
     N = W.shape[0]
     _check(lib().df_linear(_p(W), _p(X), T, N, K, _p(Y), _p(ws), ws.numel(), _stream(stream)))
+
+
+def lm_head_argmax_noalloc(W, X, idx, top1=None, top2=None, stream=None):
+    """lm_head_argmax without a workspace (fixed scratch inside the library; see dflash.h)."""
+    rows, H = X.shape
+    V = W.shape[0]
+    _check(lib().lm_head_argmax_noalloc(_p(W), _p(X), rows, H, V, _p(idx), _p(top1), _p(top2),
+                                        _stream(stream)))
 
 
 def accept_prefix_argmax(drafts, drafts_ld: int, target, K: int, eos, committed, n_committed,

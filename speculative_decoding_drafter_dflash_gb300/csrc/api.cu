@@ -1243,3 +1243,48 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
 }
 
 }  // extern "C"
+
+// ================================================================ fixed-scratch lm_head
+// Helpers of lm_head_argmax_noalloc (noalloc.cu): the same steps as lm_head_argmax with the
+// scratch carved from a caller-given region instead of a workspace argument.
+namespace df {
+
+size_t lm_head_scratch_bytes(int rows, int H, int V) {
+    if (rows <= 0 || rows > kMaxTcTokens || H <= 0 || V <= 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    cv.take<uint16_t>((size_t)2 * rows * H);
+    cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    TcScratch tc;
+    carve_tc(cv, tc, rows, V);
+    return cv.off;
+}
+
+int lm_head_run(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
+                float *top1, float *top2, char *scratch, size_t scratch_bytes, bool zero_counters,
+                cudaStream_t s) {
+    g_err[0] = 0;
+    DF_TRY(check_bf16(W, "W"));
+    DF_TRY(check_f32(X, "X"));
+    REQ(idx, DF_EINVAL, "idx is NULL");
+    Carve cv{scratch, 0, scratch_bytes, true};
+    uint16_t *xp = cv.take<uint16_t>((size_t)2 * rows * H);
+    ArgTop *part = cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    TcScratch tc;
+    carve_tc(cv, tc, rows, V);
+    REQ(cv.ok, DF_EWORKSPACE, "scratch of %zu bytes is too small", scratch_bytes);
+    if (zero_counters) {
+        cudaError_t e = cudaMemsetAsync(tc.counters, 0, sizeof(int) * (size_t)tc.n_counters, s);
+        if (e != cudaSuccess) return fail(DF_ECUDA, "clearing tile counters: %s", cudaGetErrorString(e));
+    }
+    PackArgs p;
+    p.src = X;
+    p.lds = H;
+    p.pack = xp;
+    p.ldp = H;
+    p.T = rows;
+    p.K = H;
+    DF_TRY(launch_pack(p, s));
+    return lm_head_impl(W, xp, rows, H, V, part, idx, top1, top2, tc, s);
+}
+
+}  // namespace df
