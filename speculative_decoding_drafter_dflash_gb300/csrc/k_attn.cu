@@ -178,6 +178,13 @@ constexpr int kAttnStages = 4;
 constexpr int kTileBytes = 32768;          // K + V bytes of one key tile
 constexpr int kKeyGroup = 8;               // keys per online-softmax update
 
+// 2^x with the hardware approximation (relative error ~2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -330,10 +337,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
         if (active) {
             for (int k0 = kbeg; k0 < kend; k0 += kKeyGroup) {
                 const int nk = min(kKeyGroup, kend - k0);
+                const bool fullg = nk == kKeyGroup;
                 float s[kKeyGroup][RPL];
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
-                    const float *kr = kt + (size_t)(k0 + min(u, nk - 1)) * D;
+                    const float *kr = kt + (size_t)(k0 + (fullg ? u : min(u, nk - 1))) * D;
                     float2 acc[RPL];
 #pragma unroll
                     for (int r = 0; r < RPL; ++r) acc[r] = make_float2(0.f, 0.f);
@@ -358,14 +366,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
                         for (int o = RPW; o < 32; o <<= 1)
                             s[u][r] += __shfl_xor_sync(0xffffffffu, s[u][r], o);
                 const int key0 = t0 + k0;
+                const bool need_mask = !fullg || !set_valid ||
+                                       (a.causal_block && key0 + kKeyGroup > S_cache);
+                if (need_mask) {
 #pragma unroll
-                for (int u = 0; u < kKeyGroup; ++u) {
-                    bool ok = set_valid && u < nk;
-                    const int key = key0 + u;
-                    if (a.causal_block && key >= S_cache && key - S_cache > tok) ok = false;
-                    if (!ok)
+                    for (int u = 0; u < kKeyGroup; ++u) {
+                        bool ok = set_valid && u < nk;
+                        const int key = key0 + u;
+                        if (a.causal_block && key >= S_cache && key - S_cache > tok) ok = false;
+                        if (!ok)
 #pragma unroll
-                        for (int r = 0; r < RPL; ++r) s[u][r] = -INFINITY;
+                            for (int r = 0; r < RPL; ++r) s[u][r] = -INFINITY;
+                    }
                 }
                 float p[kKeyGroup][RPL];
                 bool any = false;
@@ -381,23 +393,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
                         continue;
                     }
                     any = true;
-                    const float corr = exp2f(m[r] - mn);
                     float ps = 0.f;
 #pragma unroll
                     for (int u = 0; u < kKeyGroup; ++u) {
-                        p[u][r] = exp2f(s[u][r] - mn);
+                        p[u][r] = fast_exp2(s[u][r] - mn);
                         ps += p[u][r];
                     }
-                    l[r] = l[r] * corr + ps;
-                    m[r] = mn;
-                    const float2 c2 = make_float2(corr, corr);
+                    if (mn != m[r]) {          // the running max moved: rescale what is summed so far
+                        const float corr = fast_exp2(m[r] - mn);
+                        l[r] *= corr;
+                        const float2 c2 = make_float2(corr, corr);
 #pragma unroll
-                    for (int j = 0; j < DL / 2; ++j) o2[r][j] = __fmul2_rn(o2[r][j], c2);
+                        for (int j = 0; j < DL / 2; ++j) o2[r][j] = __fmul2_rn(o2[r][j], c2);
+                        m[r] = mn;
+                    }
+                    l[r] += ps;
                 }
                 if (!any) continue;
 #pragma unroll
                 for (int u = 0; u < kKeyGroup; ++u) {
-                    const float *vr = vt + (size_t)(k0 + min(u, nk - 1)) * D;
+                    const float *vr = vt + (size_t)(k0 + (fullg ? u : min(u, nk - 1))) * D;
                     float2 pu[RPL];
 #pragma unroll
                     for (int r = 0; r < RPL; ++r) pu[r] = make_float2(p[u][r], p[u][r]);

@@ -262,3 +262,23 @@ def test_full_size_round_k15_ctx4096():
     if gated == 0:
         assert int(out.accept[0]) == acc and int(out.rollback[0]) == shape.K - acc
         assert int(tsl[0]) == 5000 - (shape.K - acc)
+
+
+@pytest.mark.slow
+def test_batched_round_b8_ctx1024():
+    """The batched sweep shape: 8 sequences x 16 block rows (128 lm_head rows, 256 projection
+    tokens with the context rows), K=15, context 1024, ragged new-row counts."""
+    shape = DFLASH_K15.with_(batch=8, ctx=1024)
+    n_new = [1, 16, 3, 7, 2, 11, 5, 9]
+    r = _run_forward(shape, n_new, seed=5)
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+    assert list(synth.host(r["cache"].seq_len)) == list(r["seq_ref"])
+    # lm_head argmax over all 128 rows
+    rows = r["h_final"].reshape(-1, shape.hidden)
+    idx = torch.empty(rows.shape[0], dtype=torch.int32, device=DEV)
+    ws = B.alloc_workspace(B.lm_head_workspace_bytes(rows.shape[0], shape.hidden, shape.vocab))
+    B.lm_head_argmax(r["w"].lm_head, rows, idx, ws=ws)
+    torch.cuda.synchronize()
+    ri, r1, r2 = ocore.lm_head_argmax(r["ref"].reshape(-1, shape.hidden), r["hw"]["lm_head"])
+    assert_argmax_parity(idx.cpu().numpy(), ri, r1, r2, "B=8 argmax")

@@ -80,3 +80,19 @@ def test_mtp_without_output_gate():
     r = _run(shape, 1, seed=7)
     hid_ref = r["ref"][0]
     assert rel_err(r["hid"][0].cpu().numpy(), hid_ref[0]) <= REL_TOL
+
+
+@pytest.mark.slow
+def test_mtp_dense_full_size_two_steps():
+    """The dense MTP shape at full size (H=5120, 24q/4kv x 256, I=17408, V=248320, KV 8192),
+    two chained steps."""
+    from speculative_decoding_drafter_dflash_gb300.workloads import MTP_DENSE
+    r = _run(MTP_DENSE, 2, seed=21)
+    assert r["st"] == 0
+    hid_ref, am_ref, t1, t2, seq_ref, _ = r["ref"]
+    assert rel_err(r["hid"][0].cpu().numpy(), hid_ref[0]) <= REL_TOL
+    gated = assert_argmax_parity(r["am"][0].cpu().numpy(), am_ref[0], t1[0], t2[0], "step 0")
+    if gated == 0:
+        assert rel_err(r["hid"][1].cpu().numpy(), hid_ref[1]) <= REL_TOL
+        assert_argmax_parity(r["am"][1].cpu().numpy(), am_ref[1], t1[1], t2[1], "step 1")
+    assert list(synth.host(r["cache"].seq_len)) == list(seq_ref)
