@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms"], default=None,
+    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp"],
+                    default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
 
@@ -155,6 +156,23 @@ def oracle_rounds(s, hw, ks, vs, seq, host_inputs, targets, n: int, budget_s: fl
     return done, time.perf_counter() - t0
 
 
+def max_over_ranks(seconds: float, world: int, device=None) -> float:
+    """The slowest rank's elapsed time (all ranks call this; a single rank returns its own)."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(steps_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank's rounds over the slowest rank's time (weak scaling:
+    each rank runs its own replica on its own sequences)."""
+    return steps_per_rank * world / max_seconds
+
+
 def cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -254,15 +272,12 @@ def run_native(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    elapsed = e0.elapsed_time(e1) / 1e3
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
     if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
         dist.barrier()
     assert int(st.item()) == 0, "device status set during the timed region"
     rounds = args.steps * world
-    value = rounds / elapsed
+    value = job_rate(args.steps, world, elapsed)
     ms = elapsed / args.steps * 1e3
     avg_bytes = sum(round_bytes(s, n_new[i % N_VARIANTS]) for i in range(args.steps)) / args.steps
     hbm_peak, peak_kind = peaks()
@@ -325,11 +340,7 @@ def run_native(args, rank, world, local_rank):
         for i in range(args.steps):
             host_step(i)
         torch.cuda.synchronize(dev)
-        e2e_s = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
         assert int(hout["status"][0]) == 0
         h2d = sum(hin[i % N_VARIANTS]["last"].numel() * 4 + hin[i % N_VARIANTS]["th"].numel() * 4
                   + 4 + hin[i % N_VARIANTS]["tgt"].numel() * 4 + 4 + 4
@@ -437,6 +448,111 @@ def run_reference(args, rank, world):
     }
 
 
+def _graph_rate(run_once, steps: int, warmup: int = 3) -> float:
+    """Capture run_once into a CUDA graph, replay it, return replays per second (CUDA events)."""
+    import torch
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run_once(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run_once(stream)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return steps / (e0.elapsed_time(e1) / 1e3)
+
+
+def sweep_case(steps: int):
+    """Draft rounds/s over K x context x batch at the DFlash shape (one line per case)."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+    dev = torch.device("cuda", 0)
+    hbm_peak, _ = peaks()
+    w = synth.dflash_weights(DFLASH_K15, seed=0, device=dev)
+    for ctx in (1024, 8192, 32768):
+        for Bn in (1, 8):
+            cache = None
+            for K in (1, 3, 7, 15):
+                s = DFLASH_K15.with_(K=K, ctx=ctx, batch=Bn)
+                if cache is None or cache.cap < s.ctx + s.block:
+                    cache = None
+                    torch.cuda.empty_cache()
+                    cache = synth.dflash_cache(s.with_(K=15), seed=1, device=dev)
+                cache.seq_len.fill_(ctx)
+                acc = synth.accept_lengths(Bn, K, s.accept_p, seed=7)
+                n_new = [int(a) + 1 for a in acc]
+                inp = synth.dflash_round_inputs(s, n_new, seed=3, device=dev)
+                model = B.DFlashModel(s, w, cache)
+                ws = B.alloc_workspace(model.workspace_bytes(Bn, s.block, inp.n_new_max), dev)
+                out = B.RoundOutputs(Bn, K, dev)
+                eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
+                tsl = torch.full((Bn,), 1 << 30, dtype=torch.int32, device=dev)
+                tgt = torch.zeros((Bn, s.block), dtype=torch.int32, device=dev)
+
+                def once(stream):
+                    B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new,
+                                     inp.n_new_max, K, tgt, eos, tsl, out, ws, stream=stream)
+                    B.kv_rollback(cache.seq_len, inp.n_new, stream=stream)
+
+                rate = _graph_rate(once, steps)
+                nb = sum(round_bytes(s, n) for n in n_new) - (Bn - 1) * (s.weight_bytes() + 2 * s.vocab * s.hidden)
+                print(json.dumps({"profile_case": "sweep", "K": K, "ctx": ctx, "batch": Bn,
+                                  "rounds_per_s": round(rate, 1),
+                                  "positions_per_s": round(rate * Bn * s.block, 1),
+                                  "round_us": round(1e6 / rate, 1), "round_bytes": int(nb),
+                                  "frac_of_measured_hbm": round(nb * rate / 1e9 / hbm_peak, 4)}),
+                      flush=True)
+                del ws, model, out
+
+
+def mtp_case(steps: int):
+    """Dense MTP chained draft (1..3 steps) at full size: steps/s and HBM fraction."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import MTP_DENSE
+    dev = torch.device("cuda", 0)
+    hbm_peak, _ = peaks()
+    s = MTP_DENSE
+    w = synth.mtp_weights(s, seed=0, device=dev)
+    H, I, V, d = s.hidden, s.intermediate, s.vocab, s.head_dim
+    wbytes = 2 * (2 * H * H + 2 * s.q_total * H + 2 * s.kv_total * H + H * s.q_total + 3 * I * H)
+    for n_steps in (1, 2, 3):
+        cache = synth.mtp_cache(s, n_steps, seed=1, device=dev)
+        prev, tok = synth.mtp_inputs(s, seed=2, device=dev)
+        model = B.MtpModel(s, w, cache)
+        ws = B.alloc_workspace(model.workspace_bytes(1), dev)
+        hid = torch.empty((n_steps, 1, H), device=dev)
+        am = torch.empty((n_steps, 1), dtype=torch.int32, device=dev)
+        nback = torch.tensor([n_steps], dtype=torch.int32, device=dev)
+
+        def once(stream):
+            B.mtp_forward_draft(model, prev, tok, n_steps, hid, am, ws, stream=stream)
+            B.kv_rollback(cache.seq_len, nback, stream=stream)
+
+        rate = _graph_rate(once, steps)
+        kv = sum((s.kv_len + i + 1) * s.n_kv_heads * d * 8 for i in range(n_steps))
+        nb = n_steps * (wbytes + 2 * V * H) + kv
+        print(json.dumps({"profile_case": "mtp", "workload": s.name, "n_steps": n_steps,
+                          "drafts_per_s": round(rate * n_steps, 1), "call_us": round(1e6 / rate, 1),
+                          "step_us": round(1e6 / rate / n_steps, 1), "bytes_per_call": int(nb),
+                          "frac_of_measured_hbm": round(nb * rate / 1e9 / hbm_peak, 4)}), flush=True)
+        del ws, model, cache
+
+
 def profile_case(args):
     """A small, self-contained case for ncu: the full-size lm_head argmax (1.48 GB of weights,
     larger than L2) over the 16 block rows, 2 warm-up launches then 3 profiled ones; or one
@@ -448,6 +564,10 @@ def profile_case(args):
     s = DFLASH_K15
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(0)
+    if args.profile_case == "sweep":
+        return sweep_case(args.steps)
+    if args.profile_case == "mtp":
+        return mtp_case(args.steps)
     if args.profile_case == "lm_head":
         W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)
