@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp"],
+    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -517,40 +517,95 @@ def sweep_case(steps: int):
                 del ws, model, out
 
 
+def mtp_step_weight_bytes(s) -> int:
+    """Weight bytes one MTP step streams for one sequence: eh_proj, q/k/v(/gate)/o, the FFN
+    (dense SwiGLU, or router + top_k experts + shared expert and its gate) and lm_head."""
+    H = s.hidden
+    attn = 2 * H * H + s.q_total * H * (3 if s.gate else 2) + 2 * s.kv_total * H
+    if s.moe:
+        ffn = s.n_experts * H + s.top_k * 3 * s.expert_inter * H + 3 * s.shared_inter * H + H
+    else:
+        ffn = 3 * s.intermediate * H
+    return 2 * (attn + ffn + s.vocab * H)
+
+
 def mtp_case(steps: int):
-    """Dense MTP chained draft (1..3 steps) at full size: steps/s and HBM fraction."""
+    """MTP chained draft (1..3 steps) at full size, dense and MoE FFN: steps/s and HBM
+    fraction."""
     import torch
 
     from speculative_decoding_drafter_dflash_gb300 import binding as B
     from speculative_decoding_drafter_dflash_gb300 import synth
-    from speculative_decoding_drafter_dflash_gb300.workloads import MTP_DENSE
+    from speculative_decoding_drafter_dflash_gb300.workloads import MTP_DENSE, MTP_MOE
     dev = torch.device("cuda", 0)
     hbm_peak, _ = peaks()
-    s = MTP_DENSE
-    w = synth.mtp_weights(s, seed=0, device=dev)
-    H, I, V, d = s.hidden, s.intermediate, s.vocab, s.head_dim
-    wbytes = 2 * (2 * H * H + 2 * s.q_total * H + 2 * s.kv_total * H + H * s.q_total + 3 * I * H)
-    for n_steps in (1, 2, 3):
-        cache = synth.mtp_cache(s, n_steps, seed=1, device=dev)
-        prev, tok = synth.mtp_inputs(s, seed=2, device=dev)
-        model = B.MtpModel(s, w, cache)
-        ws = B.alloc_workspace(model.workspace_bytes(1), dev)
-        hid = torch.empty((n_steps, 1, H), device=dev)
-        am = torch.empty((n_steps, 1), dtype=torch.int32, device=dev)
-        nback = torch.tensor([n_steps], dtype=torch.int32, device=dev)
+    for s in (MTP_DENSE, MTP_MOE):
+        w = synth.mtp_weights(s, seed=0, device=dev)
+        H, d = s.hidden, s.head_dim
+        wbytes = mtp_step_weight_bytes(s)
+        for n_steps in (1, 2, 3):
+            cache = synth.mtp_cache(s, n_steps, seed=1, device=dev)
+            prev, tok = synth.mtp_inputs(s, seed=2, device=dev)
+            model = B.MtpModel(s, w, cache)
+            ws = B.alloc_workspace(model.workspace_bytes(1), dev)
+            hid = torch.empty((n_steps, 1, H), device=dev)
+            am = torch.empty((n_steps, 1), dtype=torch.int32, device=dev)
+            nback = torch.tensor([n_steps], dtype=torch.int32, device=dev)
+
+            def once(stream):
+                B.mtp_forward_draft(model, prev, tok, n_steps, hid, am, ws, stream=stream)
+                B.kv_rollback(cache.seq_len, nback, stream=stream)
+
+            rate = _graph_rate(once, steps)
+            kv = sum((s.kv_len + i + 1) * s.n_kv_heads * d * 8 for i in range(n_steps))
+            nb = n_steps * wbytes + kv
+            print(json.dumps({"profile_case": "mtp", "workload": s.name, "n_steps": n_steps,
+                              "drafts_per_s": round(rate * n_steps, 1),
+                              "call_us": round(1e6 / rate, 1),
+                              "step_us": round(1e6 / rate / n_steps, 1), "bytes_per_call": int(nb),
+                              "frac_of_measured_hbm": round(nb * rate / 1e9 / hbm_peak, 4)}),
+                  flush=True)
+            del ws, model, cache
+        del w
+        torch.cuda.empty_cache()
+
+
+def moe_case(steps: int):
+    """The MoE FFN alone at full size (H=2048, 256 experts top-8, SwiGLU 512, shared expert)
+    for 1 and 8 rows: weight bytes streamed over time. One MoE block is 57 MB, under L2, so
+    each timed replay runs four blocks with their own weights (230 MB) in turn."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import MTP_MOE
+    dev = torch.device("cuda", 0)
+    hbm_peak, _ = peaks()
+    s = MTP_MOE.with_(vocab=1024)        # lm_head and embedding are not read here
+    n_sets = 4
+    models = [B.MtpModel(s, synth.mtp_weights(s, seed=i, device=dev),
+                         synth.mtp_cache(s, 1, seed=1, device=dev)) for i in range(n_sets)]
+    H = s.hidden
+    g = torch.Generator(device=dev).manual_seed(5)
+    for T in (1, 8):
+        x = torch.randn((T, H), generator=g, device=dev)
+        out = torch.empty_like(x)
+        ids = [torch.empty((T, s.top_k), dtype=torch.int32, device=dev) for _ in models]
+        ws = [B.alloc_workspace(m.moe_workspace_bytes(T), dev) for m in models]
 
         def once(stream):
-            B.mtp_forward_draft(model, prev, tok, n_steps, hid, am, ws, stream=stream)
-            B.kv_rollback(cache.seq_len, nback, stream=stream)
+            for m, i, w in zip(models, ids, ws):
+                B.moe_ffn(m, x, out, w, i, stream=stream)
 
-        rate = _graph_rate(once, steps)
-        kv = sum((s.kv_len + i + 1) * s.n_kv_heads * d * 8 for i in range(n_steps))
-        nb = n_steps * (wbytes + 2 * V * H) + kv
-        print(json.dumps({"profile_case": "mtp", "workload": s.name, "n_steps": n_steps,
-                          "drafts_per_s": round(rate * n_steps, 1), "call_us": round(1e6 / rate, 1),
-                          "step_us": round(1e6 / rate / n_steps, 1), "bytes_per_call": int(nb),
-                          "frac_of_measured_hbm": round(nb * rate / 1e9 / hbm_peak, 4)}), flush=True)
-        del ws, model, cache
+        rate = _graph_rate(once, steps) * n_sets
+        torch.cuda.synchronize()
+        distinct = sum(len(set(i.cpu().numpy().reshape(-1).tolist())) for i in ids) / n_sets
+        nb = 2 * H * (s.n_experts + 1 + distinct * 3 * s.expert_inter + 3 * s.shared_inter)
+        print(json.dumps({"profile_case": "moe", "workload": "moe-ffn-h2048-e256-top8-i512",
+                          "rows": T, "distinct_experts": distinct, "call_us": round(1e6 / rate, 2),
+                          "weight_bytes": int(nb),
+                          "frac_of_measured_hbm": round(nb * rate / 1e9 / hbm_peak, 4)}),
+              flush=True)
 
 
 def profile_case(args):
@@ -568,6 +623,8 @@ def profile_case(args):
         return sweep_case(args.steps)
     if args.profile_case == "mtp":
         return mtp_case(args.steps)
+    if args.profile_case == "moe":
+        return moe_case(args.steps)
     if args.profile_case == "lm_head":
         W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)

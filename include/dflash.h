@@ -323,6 +323,33 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
                       float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
                       df_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Mixture-of-experts FFN of the MTP block on its own (mtp.rs `MtpFfnWeightsGpu::Moe`; the
+ * same kernels run inside mtp_forward_draft when cfg->n_experts > 0). The page names the
+ * router, the experts and the shared expert with its scalar gate; the routing rule is read as
+ *   p = softmax(x . router^T) over all E experts; sel = the top_k largest p (the lower expert
+ *   index first on equal values), largest first; w_j = p[sel_j] / sum_i p[sel_i]
+ *   out = sum_j w_j * SwiGLU_{sel_j}(x) + sigmoid(x . sh_expert_gate) * SwiGLU_shared(x)
+ * with SwiGLU_e(x) = down_e( silu(gate_e x) * (up_e x) ).
+ * ---------------------------------------------------------------------------------------- */
+/* Workspace of df_moe_ffn for T rows; 0 when cfg has no experts or T is outside 1..16. */
+size_t df_moe_workspace_bytes(const df_mtp_config *cfg, int T);
+
+/*   cfg          n_experts <= 512, top_k <= 16; hidden, expert_inter and shared_inter
+ *                multiples of 8 (attention fields are checked but unused)
+ *   w            only router, exp_*, sh_gate_mlp, sh_up, sh_down and sh_expert_gate are read
+ *   x            device F32 [T, H], 16-byte aligned: the FFN input (already normalised)
+ *   T            1..16 rows
+ *   out          device F32 [T, H] out: the FFN output (no residual)
+ *   expert_ids   device int32 [T, top_k] out, or NULL: the chosen experts, largest weight first
+ *   expert_w     device F32 [T, top_k + 1] out, or NULL: the renormalised weights, then the
+ *                shared expert's sigmoid gate
+ * Errors: DF_ESHAPE for sizes outside the limits, DF_EINVAL for NULL pointers; a NaN router
+ * logit sets *d_status to DF_EINVAL. */
+int df_moe_ffn(const df_mtp_config *cfg, const df_mtp_weights *w, const float *x, int T,
+               float *out, int32_t *expert_ids, float *expert_w, void *ws, size_t ws_bytes,
+               int32_t *d_status, df_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,6 +41,15 @@ def moe_route(x, router_bits, top_k, dt=np.float32):
     return sel, wsel.astype(dt)
 
 
+def route_margin(x, router_bits, top_k, dt=np.float32):
+    """Gap between the top_k-th and (top_k+1)-th largest router logits (inf when every expert
+    is chosen): how far the expert choice is from a tie."""
+    logits = np.sort(np.asarray(linear(x, router_bits, dt), np.float64))[::-1]
+    if top_k >= logits.shape[0]:
+        return float("inf")
+    return float(logits[top_k - 1] - logits[top_k])
+
+
 def moe_ffn(x, w, top_k, dt=np.float32):
     sel, ws = moe_route(x, w["router"], top_k, dt)
     out = np.zeros_like(np.asarray(x, dt))
@@ -80,6 +89,7 @@ def mtp_step(cfg, w, k_cache, v_cache, pos, prev_hidden, token, dt=np.float32):
     if w.get("router") is not None:
         f, sel, ws = moe_ffn(fin, w, cfg.top_k, dt)
         info["experts"], info["expert_w"] = sel, ws
+        info["route_gap"] = route_margin(fin, w["router"], cfg.top_k, dt)
     else:
         f = swiglu(fin, w["wg"], w["wu"], w["wd"], dt)
     hidden = h1 + f

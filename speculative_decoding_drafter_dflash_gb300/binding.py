@@ -108,6 +108,9 @@ _SIGS = [
     ("mtp_forward_draft", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), POINTER(KvCache),
                                   c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_size_t, c_void_p, c_void_p]),
+    ("df_moe_workspace_bytes", c_size_t, [POINTER(MtpConfig), c_int]),
+    ("df_moe_ffn", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), c_void_p, c_int, c_void_p,
+                           c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
 ]
 
 
@@ -350,6 +353,9 @@ class MtpModel:
     def workspace_bytes(self, B: int) -> int:
         return int(lib().df_mtp_workspace_bytes(ctypes.byref(self.cfg), B))
 
+    def moe_workspace_bytes(self, T: int) -> int:
+        return int(lib().df_moe_workspace_bytes(ctypes.byref(self.cfg), T))
+
 
 def mtp_forward_draft(model: MtpModel, prev_hidden, token, n_steps: int, hidden_out, argmax_out,
                       ws, logits_out=None, d_status=None, stream=None):
@@ -358,3 +364,13 @@ def mtp_forward_draft(model: MtpModel, prev_hidden, token, n_steps: int, hidden_
                                    ctypes.byref(model.cache_c), _p(prev_hidden), _p(token), B,
                                    n_steps, _p(hidden_out), _p(argmax_out), _p(logits_out), _p(ws),
                                    ws.numel(), _p(d_status), _stream(stream)))
+
+
+def moe_ffn(model: MtpModel, x, out, ws, expert_ids=None, expert_w=None, d_status=None,
+            stream=None):
+    """The MoE FFN alone: out[T, H] from normalised rows x[T, H]; optional expert_ids
+    [T, top_k] int32 and expert_w [T, top_k + 1] F32 outputs."""
+    T = x.shape[0]
+    _check(lib().df_moe_ffn(ctypes.byref(model.cfg), ctypes.byref(model.weights), _p(x), T,
+                            _p(out), _p(expert_ids), _p(expert_w), _p(ws), ws.numel(),
+                            _p(d_status), _stream(stream)))

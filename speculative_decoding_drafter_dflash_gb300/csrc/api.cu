@@ -881,13 +881,27 @@ int check_mtp_cfg(const df_mtp_config *c) {
         REQ(c->intermediate > 0 && c->intermediate % 8 == 0, DF_ESHAPE, "intermediate=%d",
             c->intermediate);
     } else {
-        REQ(c->n_experts > 0 && c->top_k >= 1 && c->top_k <= c->n_experts && c->top_k <= 16,
-            DF_ESHAPE, "n_experts=%d top_k=%d (top_k <= 16)", c->n_experts, c->top_k);
+        REQ(c->n_experts > 0 && c->n_experts <= kMoeMaxExperts && c->top_k >= 1 &&
+                c->top_k <= c->n_experts && c->top_k <= kMoeMaxTopK,
+            DF_ESHAPE, "n_experts=%d top_k=%d (n_experts <= %d, top_k <= %d)", c->n_experts,
+            c->top_k, kMoeMaxExperts, kMoeMaxTopK);
         REQ(c->expert_inter > 0 && c->expert_inter % 8 == 0 && c->shared_inter > 0 &&
                 c->shared_inter % 8 == 0,
             DF_ESHAPE, "expert_inter=%d shared_inter=%d", c->expert_inter, c->shared_inter);
     }
     REQ(c->rms_eps >= 0.f && c->rope_theta > 0.f, DF_EINVAL, "rms_eps / rope_theta");
+    return DF_OK;
+}
+
+int check_moe_weights(const df_mtp_weights *w) {
+    DF_TRY(check_bf16(w->router, "router"));
+    DF_TRY(check_bf16(w->exp_gate, "exp_gate"));
+    DF_TRY(check_bf16(w->exp_up, "exp_up"));
+    DF_TRY(check_bf16(w->exp_down, "exp_down"));
+    DF_TRY(check_bf16(w->sh_gate_mlp, "sh_gate_mlp"));
+    DF_TRY(check_bf16(w->sh_up, "sh_up"));
+    DF_TRY(check_bf16(w->sh_down, "sh_down"));
+    DF_TRY(check_bf16(w->sh_expert_gate, "sh_expert_gate"));
     return DF_OK;
 }
 
@@ -914,24 +928,63 @@ int check_mtp_weights(const df_mtp_config *c, const df_mtp_weights *w) {
         DF_TRY(check_bf16(w->w_up, "w_up"));
         DF_TRY(check_bf16(w->w_down, "w_down"));
     } else {
-        DF_TRY(check_bf16(w->router, "router"));
-        DF_TRY(check_bf16(w->exp_gate, "exp_gate"));
-        DF_TRY(check_bf16(w->exp_up, "exp_up"));
-        DF_TRY(check_bf16(w->exp_down, "exp_down"));
-        DF_TRY(check_bf16(w->sh_gate_mlp, "sh_gate_mlp"));
-        DF_TRY(check_bf16(w->sh_up, "sh_up"));
-        DF_TRY(check_bf16(w->sh_down, "sh_down"));
-        DF_TRY(check_bf16(w->sh_expert_gate, "sh_expert_gate"));
+        DF_TRY(check_moe_weights(w));
     }
     return DF_OK;
 }
 
+// Scratch of the MoE FFN (router logits, choice, activations, per-slot outputs, counter).
+struct MoeWs {
+    float *logits, *wts, *act, *part;
+    int32_t *sel;
+    int *counter;
+};
+
+void carve_moe(Carve &cv, MoeWs &m, const df_mtp_config *c, int T) {
+    const size_t S = (size_t)c->top_k + 1, Imax = (size_t)std::max(c->expert_inter, c->shared_inter);
+    m.logits = cv.take<float>((size_t)T * (c->n_experts + 1));
+    m.sel = cv.take<int32_t>((size_t)T * c->top_k);
+    m.wts = cv.take<float>((size_t)T * S);
+    m.act = cv.take<float>((size_t)T * S * Imax);
+    m.part = cv.take<float>(S * T * c->hidden);
+    m.counter = cv.take<int>(1);
+}
+
+MoeArgs moe_args(const df_mtp_config *c, const df_mtp_weights *w, const MoeWs &m,
+                 const float *x, int T, int32_t *status) {
+    MoeArgs a;
+    a.x = x;
+    a.ldx = c->hidden;
+    a.T = T;
+    a.H = c->hidden;
+    a.E = c->n_experts;
+    a.k = c->top_k;
+    a.Ie = c->expert_inter;
+    a.Is = c->shared_inter;
+    a.router = w->router;
+    a.sh_gate = w->sh_expert_gate;
+    a.exp_gate = w->exp_gate;
+    a.exp_up = w->exp_up;
+    a.exp_down = w->exp_down;
+    a.sh_g = w->sh_gate_mlp;
+    a.sh_u = w->sh_up;
+    a.sh_d = w->sh_down;
+    a.logits = m.logits;
+    a.sel = m.sel;
+    a.wts = m.wts;
+    a.act = m.act;
+    a.part = m.part;
+    a.ldpart = c->hidden;
+    a.counter = m.counter;
+    a.status = status;
+    return a;
+}
+
 struct MtpWs {
-    float *x, *defer, *gate, *q, *h1, *cos_t, *sin_t, *attn_part, *moe_out, *router_logits;
-    uint16_t *xp_e, *xp_h, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head, *xp_sh;
+    float *x, *defer, *gate, *q, *h1, *xf, *cos_t, *sin_t, *attn_part;
+    uint16_t *xp_e, *xp_h, *xp_attn, *xp_o, *xp_ffn, *xp_act, *xp_head;
     ArgTop *amax_part;
-    int32_t *moe_sel;
-    float *moe_w;
+    MoeWs moe;
     AttnArgs plan;
     TcScratch tc;
 };
@@ -940,13 +993,13 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     const int H = c->hidden, d = c->head_dim, nq = c->n_q_heads, nkv = c->n_kv_heads;
     const int rot = c->rotary_dim ? c->rotary_dim : d;
     const size_t qt = (size_t)nq * d, kt = (size_t)nkv * d;
-    const size_t I = c->n_experts ? (size_t)std::max(c->expert_inter * c->top_k, c->shared_inter)
-                                  : (size_t)c->intermediate;
+    const size_t I = c->n_experts ? 0 : (size_t)c->intermediate;
     w.x = cv.take<float>((size_t)B * H);
     w.defer = cv.take<float>(defer_floats_for(B, (long long)std::max<size_t>(2 * qt + 2 * kt, H)));
     w.gate = cv.take<float>((size_t)B * qt);
     w.q = cv.take<float>((size_t)B * qt);
     w.h1 = cv.take<float>((size_t)B * H);
+    w.xf = cv.take<float>((size_t)B * H);
     w.cos_t = cv.take<float>((size_t)B * (rot / 2));
     w.sin_t = cv.take<float>((size_t)B * (rot / 2));
     w.plan = AttnArgs{};
@@ -957,22 +1010,18 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     w.plan.d = d;
     attn_plan(w.plan, cap);
     w.attn_part = cv.take<float>(attn_part_floats(w.plan));
-    w.moe_out = cv.take<float>((size_t)B * H);
-    w.router_logits = cv.take<float>((size_t)B * std::max(c->n_experts, 1));
     w.xp_e = cv.take<uint16_t>((size_t)2 * B * H);
     w.xp_h = cv.take<uint16_t>((size_t)2 * B * H);
     w.xp_attn = cv.take<uint16_t>((size_t)2 * B * H);
     w.xp_o = cv.take<uint16_t>((size_t)2 * B * qt);
     w.xp_ffn = cv.take<uint16_t>((size_t)2 * B * H);
-    w.xp_act = cv.take<uint16_t>((size_t)2 * B * I);
-    w.xp_sh = cv.take<uint16_t>((size_t)2 * B * std::max(c->shared_inter, 1));
+    w.xp_act = cv.take<uint16_t>((size_t)2 * B * std::max<size_t>(I, 1));
     w.xp_head = cv.take<uint16_t>((size_t)2 * B * H);
     w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * B);
-    w.moe_sel = cv.take<int32_t>((size_t)B * std::max(c->top_k, 1));
-    w.moe_w = cv.take<float>((size_t)B * std::max(c->top_k, 1));
+    if (c->n_experts) carve_moe(cv, w.moe, c, B);
+    else w.moe = MoeWs{};
     long long rows = std::max<long long>({(long long)c->vocab, 2LL * (long long)I,
-                                          (long long)(qt + 2 * kt), (long long)H,
-                                          (long long)std::max(c->n_experts, 1)});
+                                          (long long)(qt + 2 * kt), (long long)H});
     carve_tc(cv, w.tc, B, rows);
 }
 
@@ -1000,7 +1049,8 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
     REQ(B > 0 && n_steps >= 1, DF_ESHAPE, "B=%d n_steps=%d", B, n_steps);
     DF_TRY(check_cache(cache, 1, B, cfg->head_dim));
     REQ(prev_hidden && token && hidden_out && argmax_out, DF_EINVAL, "NULL MTP input or output");
-    REQ(cfg->n_experts == 0, DF_EINVAL, "MoE MTP FFN is not available in this build");
+    REQ(cfg->n_experts == 0 || B <= kMoeMaxRows, DF_ESHAPE, "MoE MTP takes B <= %d (B=%d)",
+        kMoeMaxRows, B);
     DF_TRY(get_ws(ws, ws_bytes, df_mtp_workspace_bytes(cfg, B)));
     Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
     MtpWs W;
@@ -1009,6 +1059,7 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
     const int H = cfg->hidden, d = cfg->head_dim, nq = cfg->n_q_heads, nkv = cfg->n_kv_heads;
     const int rot = cfg->rotary_dim ? cfg->rotary_dim : d;
     const int qt = nq * d, kt = nkv * d, Nqkv = qt + 2 * kt, I = cfg->intermediate;
+    const bool moe = cfg->n_experts > 0;
 
     // A projection whose split partial sums land in W.defer; returns the split count.
     auto deferred = [&](GemmArgs g, int N, const char *name, int *S) -> int {
@@ -1173,45 +1224,19 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         pf.ldh = H;
         pf.norm_w = w->post_attn_norm;
         pf.eps = cfg->rms_eps;
-        pf.pack = W.xp_ffn;
-        pf.ldp = H;
+        if (moe) {
+            pf.y_out = W.xf;
+            pf.ldy = H;
+        } else {
+            pf.pack = W.xp_ffn;
+            pf.ldp = H;
+        }
         pf.T = B;
         pf.K = H;
         DF_TRY(launch_pack(pf, s));
-        GemmArgs gu;
-        gu.W0 = w->w_gate_mlp;
-        gu.n0 = I;
-        gu.W1 = w->w_up;
-        gu.n1 = I;
-        gu.N = I;
-        gu.K = H;
-        gu.X = W.xp_ffn;
-        gu.ldx = H;
-        gu.T = B;
-        gu.epi = EPI_SWIGLU;
-        gu.pack_out = W.xp_act;
-        gu.ldpo = I;
-        gu.name = "gemm_gate_up";
-        DF_TRY(launch_gemm_tc(gu, W.tc, s));
-        GemmArgs gd;
-        gd.W0 = w->w_down;
-        gd.n0 = H;
-        gd.N = H;
-        gd.K = I;
-        gd.X = W.xp_act;
-        gd.ldx = I;
-        gd.T = B;
-        int S_d = 0;
-        DF_TRY(deferred(gd, H, "gemm_down", &S_d));
-        // hidden = h1 + down partials (the step's output); shared head: RMSNorm then lm_head
-        // argmax (mtp.rs `forward_ffn_residual`, `forward_shared_head`)
-        PackArgs pk;
+        PackArgs pk;   // hidden = h1 + FFN output (the step's output); shared-head RMSNorm
         pk.src = W.h1;
         pk.lds = H;
-        pk.part = W.defer;
-        pk.n_part = S_d;
-        pk.part_stride = (size_t)B * H;
-        pk.ldpart = H;
         pk.h_out = hid;
         pk.ldh = H;
         pk.norm_w = w->shared_head_norm;
@@ -1220,6 +1245,45 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         pk.ldp = H;
         pk.T = B;
         pk.K = H;
+        if (moe) {
+            // routed experts + shared expert, one weighted output per slot (mtp.rs
+            // `MtpFfnWeightsGpu::Moe`), summed in slot order by the head pack below
+            DF_TRY(launch_moe(moe_args(cfg, w, W.moe, W.xf, B, d_status), s));
+            pk.part = W.moe.part;
+            pk.n_part = cfg->top_k + 1;
+        } else {
+            GemmArgs gu;
+            gu.W0 = w->w_gate_mlp;
+            gu.n0 = I;
+            gu.W1 = w->w_up;
+            gu.n1 = I;
+            gu.N = I;
+            gu.K = H;
+            gu.X = W.xp_ffn;
+            gu.ldx = H;
+            gu.T = B;
+            gu.epi = EPI_SWIGLU;
+            gu.pack_out = W.xp_act;
+            gu.ldpo = I;
+            gu.name = "gemm_gate_up";
+            DF_TRY(launch_gemm_tc(gu, W.tc, s));
+            GemmArgs gd;
+            gd.W0 = w->w_down;
+            gd.n0 = H;
+            gd.N = H;
+            gd.K = I;
+            gd.X = W.xp_act;
+            gd.ldx = I;
+            gd.T = B;
+            int S_d = 0;
+            DF_TRY(deferred(gd, H, "gemm_down", &S_d));
+            pk.part = W.defer;   // dense SwiGLU: the down projection's split partial sums
+            pk.n_part = S_d;
+        }
+        pk.part_stride = (size_t)B * H;
+        pk.ldpart = H;
+        // shared head: RMSNorm then lm_head argmax (mtp.rs `forward_ffn_residual`,
+        // `forward_shared_head`)
         DF_TRY(launch_pack(pk, s));
         DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B, H, cfg->vocab, W.amax_part,
                             argmax_out + (size_t)st * B, nullptr, nullptr, W.tc, s));
@@ -1240,6 +1304,46 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         }
     }
     return launch_seq_advance(cache->seq_len, nullptr, B, n_steps, cache->cap, d_status, s);
+}
+
+size_t df_moe_workspace_bytes(const df_mtp_config *cfg, int T) {
+    if (check_mtp_cfg(cfg) != DF_OK || cfg->n_experts == 0 || T <= 0 || T > kMoeMaxRows) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    MoeWs m;
+    carve_moe(cv, m, cfg, T);
+    return cv.off;
+}
+
+int df_moe_ffn(const df_mtp_config *cfg, const df_mtp_weights *w, const float *x, int T,
+               float *out, int32_t *expert_ids, float *expert_w, void *ws, size_t ws_bytes,
+               int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_mtp_cfg(cfg));
+    REQ(cfg->n_experts > 0, DF_EINVAL, "df_moe_ffn: the config has no experts");
+    REQ(w, DF_EINVAL, "MTP weights is NULL");
+    DF_TRY(check_moe_weights(w));
+    REQ(T >= 1 && T <= kMoeMaxRows, DF_ESHAPE, "df_moe_ffn: T=%d (1 <= T <= %d)", T, kMoeMaxRows);
+    REQ(x && out, DF_EINVAL, "df_moe_ffn: NULL x or out");
+    REQ(reinterpret_cast<uintptr_t>(x) % 16 == 0, DF_EINVAL, "df_moe_ffn: x not 16-byte aligned");
+    DF_TRY(get_ws(ws, ws_bytes, df_moe_workspace_bytes(cfg, T)));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    MoeWs m;
+    carve_moe(cv, m, cfg, T);
+    cudaStream_t s = (cudaStream_t)stream;
+    MoeArgs a = moe_args(cfg, w, m, x, T, d_status);
+    if (expert_ids) a.sel = expert_ids;
+    if (expert_w) a.wts = expert_w;
+    DF_TRY(launch_moe(a, s));
+    PackArgs p;   // out = sum of the top_k + 1 slot outputs, in slot order
+    p.part = m.part;
+    p.n_part = cfg->top_k + 1;
+    p.part_stride = (size_t)T * cfg->hidden;
+    p.ldpart = cfg->hidden;
+    p.h_out = out;
+    p.ldh = cfg->hidden;
+    p.T = T;
+    p.K = cfg->hidden;
+    return launch_pack(p, s);
 }
 
 }  // extern "C"

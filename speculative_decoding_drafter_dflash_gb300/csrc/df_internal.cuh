@@ -177,6 +177,29 @@ struct PackArgs {
 };
 int launch_pack(const PackArgs &a, cudaStream_t s);
 
+// Mixture-of-experts FFN (router, top-k, routed + shared expert SwiGLUs) over T <= 16 rows.
+constexpr int kMoeMaxRows = 16;
+constexpr int kMoeMaxExperts = 512;
+constexpr int kMoeMaxTopK = 16;
+struct MoeArgs {
+    const float *x = nullptr;        // [T, H] F32 normalised rows, row stride ldx (16-byte aligned)
+    int ldx = 0;
+    int T = 0, H = 0, E = 0, k = 0, Ie = 0, Is = 0;
+    const uint16_t *router = nullptr, *sh_gate = nullptr;          // [E, H], [1, H]
+    const uint16_t *exp_gate = nullptr, *exp_up = nullptr;         // [E, Ie, H]
+    const uint16_t *exp_down = nullptr;                            // [E, H, Ie]
+    const uint16_t *sh_g = nullptr, *sh_u = nullptr, *sh_d = nullptr;  // [Is, H] x2, [H, Is]
+    float *logits = nullptr;         // [T, E + 1] scratch
+    int32_t *sel = nullptr;          // [T, k] chosen experts, largest weight first
+    float *wts = nullptr;            // [T, k + 1]: renormalised weights, then sigmoid(shared gate)
+    float *act = nullptr;            // [T, k + 1, max(Ie, Is)] SwiGLU activations
+    float *part = nullptr;           // [k + 1, T, ldpart] weighted per-slot outputs
+    int ldpart = 0;
+    int *counter = nullptr;          // zero before the call, left zero
+    int32_t *status = nullptr;
+};
+int launch_moe(const MoeArgs &a, cudaStream_t s);
+
 enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
 
 struct GemmArgs {
