@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe"],
+    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe", "attn"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -608,6 +608,54 @@ def moe_case(steps: int):
               flush=True)
 
 
+def attn_case(steps: int):
+    """Split-KV attention alone on the drafter shapes: KV bytes read over time, each call timed
+    with CUDA events after a 256 MB write that evicts L2."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    hbm_peak, _ = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    cases = [("dflash-k15-ctx4096-b1", 1, 16, 16, 8, 128, 4096, True),
+             ("dflash-k15-ctx32768-b1", 1, 16, 16, 8, 128, 32768, True),
+             ("dflash-k15-ctx8192-b8", 8, 16, 16, 8, 128, 8192, True),
+             ("mtp-dense-kv8192", 1, 1, 24, 4, 256, 8192, False),
+             ("mtp-moe-kv16384", 1, 1, 16, 2, 256, 16384, False)]
+    for name, Bn, blk, nq, nkv, d, ctx, blockk in cases:
+        q = torch.randn((Bn, blk, nq, d), generator=g, device=dev)
+        ck = torch.randn((Bn, nkv, ctx, d), generator=g, device=dev)
+        cv = torch.randn((Bn, nkv, ctx, d), generator=g, device=dev)
+        kb = torch.randn((Bn, nkv, blk, d), generator=g, device=dev) if blockk else None
+        vb = torch.randn((Bn, nkv, blk, d), generator=g, device=dev) if blockk else None
+        sl = torch.full((Bn,), ctx, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        ws = B.alloc_workspace(B.attention_workspace_bytes(Bn, blk, nq, nkv, d, ctx), dev)
+        for _ in range(3):
+            B.attention(q, ck, cv, sl, out, ws, kb, vb)
+        times = []
+        for _ in range(steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.attention(q, ck, cv, sl, out, ws, kb, vb)
+            e1.record()
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
+        nb = 2 * Bn * nkv * (ctx + (blk if blockk else 0)) * d * 4 + 2 * q.numel() * 4
+        B.profile_enable(True)
+        B.attention(q, ck, cv, sl, out, ws, kb, vb)
+        ks = [n for n, _ in B.profile_read()]
+        B.profile_enable(False)
+        print(json.dumps({"profile_case": "attn", "workload": name, "us": round(us, 2),
+                          "bytes": int(nb), "gbs": round(nb / us / 1e3, 1),
+                          "frac_of_measured_hbm": round(nb / us / 1e3 / hbm_peak, 4),
+                          "kernels": ks}), flush=True)
+        del q, ck, cv, kb, vb, out, ws
+
+
 def profile_case(args):
     """A small, self-contained case for ncu: the full-size lm_head argmax (1.48 GB of weights,
     larger than L2) over the 16 block rows, 2 warm-up launches then 3 profiled ones; or one
@@ -625,6 +673,8 @@ def profile_case(args):
         return mtp_case(args.steps)
     if args.profile_case == "moe":
         return moe_case(args.steps)
+    if args.profile_case == "attn":
+        return attn_case(args.steps)
     if args.profile_case == "lm_head":
         W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)

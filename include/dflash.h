@@ -198,6 +198,30 @@ int df_linear(const uint16_t *W, const float *X, int T, int N, int K, float *Y, 
               size_t ws_bytes, df_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Split-KV scaled dot-product attention on its own (the attention step of every drafter layer
+ * and of the MTP step: softmax(q k^T / sqrt(d)) v with grouped KV heads, mtp.rs
+ * `forward_full_attention`; the DFlash block attends to the context rows and to all block rows,
+ * qwen35_orchestrator.rs step 4). The same kernels run inside dflash_block_forward and
+ * mtp_forward_draft.
+ * ---------------------------------------------------------------------------------------- */
+/* Workspace for the per-chunk partial outputs; 0 for unsupported sizes. */
+size_t df_attention_workspace_bytes(int B, int blk, int nq, int nkv, int d, int cap);
+
+/*   q            device F32 [B, blk, nq, d]: query rows (RoPE and norms already applied)
+ *   cache_k/v    device F32 [B, nkv, cap, d]; sequence b sees cache rows [0, seq_len[b])
+ *   seq_len      device int32 [B], clamped to [0, cap]
+ *   kb, vb       device F32 [B, nkv, blk, d] block keys/values seen after the cache rows, or
+ *                both NULL
+ *   causal_block 0: every query row sees all block rows; 1: block row i sees block rows <= i
+ *   out          device F32 [B, blk, nq, d] out
+ * Query head h reads KV head h / (nq / nkv). d is 32, 64, 128 or 256; q, the caches and the
+ * block buffers are 16-byte aligned. A row with no visible key gets zeros. */
+int df_attention(const float *q, const float *cache_k, const float *cache_v, int cap,
+                 const int32_t *seq_len, const float *kb, const float *vb, int B, int blk, int nq,
+                 int nkv, int d, int causal_block, float *out, void *ws, size_t ws_bytes,
+                 int32_t *d_status, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Greedy accept walk (qwen35_orchestrator.rs module doc "Greedy accept-walk consistency
  * invariant" and steps 7-9: `step_round_from_argmaxes`, rollback = K - accept_count).
  * ---------------------------------------------------------------------------------------- */

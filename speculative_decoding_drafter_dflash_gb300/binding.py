@@ -108,6 +108,10 @@ _SIGS = [
     ("mtp_forward_draft", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), POINTER(KvCache),
                                   c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_size_t, c_void_p, c_void_p]),
+    ("df_attention_workspace_bytes", c_size_t, [c_int] * 6),
+    ("df_attention", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
+                             c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                             c_size_t, c_void_p, c_void_p]),
     ("df_moe_workspace_bytes", c_size_t, [POINTER(MtpConfig), c_int]),
     ("df_moe_ffn", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), c_void_p, c_int, c_void_p,
                            c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -374,3 +378,18 @@ def moe_ffn(model: MtpModel, x, out, ws, expert_ids=None, expert_w=None, d_statu
     _check(lib().df_moe_ffn(ctypes.byref(model.cfg), ctypes.byref(model.weights), _p(x), T,
                             _p(out), _p(expert_ids), _p(expert_w), _p(ws), ws.numel(),
                             _p(d_status), _stream(stream)))
+
+
+def attention_workspace_bytes(B: int, blk: int, nq: int, nkv: int, d: int, cap: int) -> int:
+    return int(lib().df_attention_workspace_bytes(B, blk, nq, nkv, d, cap))
+
+
+def attention(q, cache_k, cache_v, seq_len, out, ws, kb=None, vb=None, causal_block=False,
+              d_status=None, stream=None):
+    """q [B, blk, nq, d]; cache_k/v [B, nkv, cap, d]; optional block keys kb/vb [B, nkv, blk, d];
+    out [B, blk, nq, d]."""
+    Bn, blk, nq, d = q.shape
+    nkv, cap = cache_k.shape[1], cache_k.shape[2]
+    _check(lib().df_attention(_p(q), _p(cache_k), _p(cache_v), cap, _p(seq_len), _p(kb), _p(vb),
+                              Bn, blk, nq, nkv, d, 1 if causal_block else 0, _p(out), _p(ws),
+                              ws.numel(), _p(d_status), _stream(stream)))

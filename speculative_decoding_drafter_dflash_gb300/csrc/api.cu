@@ -692,6 +692,65 @@ int df_linear(const uint16_t *W, const float *X, int T, int N, int K, float *Y, 
     return launch_gemm_tc(g, tc, s);
 }
 
+// The attention plan of df_attention: key chunks sized for cap cache rows (+ the block rows).
+static AttnArgs attention_plan(int B, int blk, int nq, int nkv, int d, int cap, bool block_keys) {
+    AttnArgs a = AttnArgs{};
+    a.B = B;
+    a.blk = blk;
+    a.nq = nq;
+    a.nkv = nkv;
+    a.d = d;
+    attn_plan(a, cap + (block_keys ? blk : 0));
+    return a;
+}
+
+static int check_attention(int B, int blk, int nq, int nkv, int d, int cap) {
+    REQ(B > 0 && blk > 0 && cap > 0, DF_ESHAPE, "B=%d blk=%d cap=%d", B, blk, cap);
+    REQ(nq > 0 && nkv > 0 && nq % nkv == 0, DF_ESHAPE, "heads %d / %d", nq, nkv);
+    REQ(d == 32 || d == 64 || d == 128 || d == 256, DF_ESHAPE, "head_dim=%d not in {32, 64, 128, 256}", d);
+    return DF_OK;
+}
+
+size_t df_attention_workspace_bytes(int B, int blk, int nq, int nkv, int d, int cap) {
+    if (check_attention(B, blk, nq, nkv, d, cap) != DF_OK) return 0;
+    AttnArgs a = attention_plan(B, blk, nq, nkv, d, cap, true);
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    cv.take<float>(attn_part_floats(a));
+    return cv.off;
+}
+
+int df_attention(const float *q, const float *cache_k, const float *cache_v, int cap,
+                 const int32_t *seq_len, const float *kb, const float *vb, int B, int blk, int nq,
+                 int nkv, int d, int causal_block, float *out, void *ws, size_t ws_bytes,
+                 int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_attention(B, blk, nq, nkv, d, cap));
+    REQ(q && cache_k && cache_v && seq_len && out, DF_EINVAL, "df_attention: NULL q, cache, seq_len or out");
+    REQ((kb == nullptr) == (vb == nullptr), DF_EINVAL, "df_attention: kb and vb go together");
+    DF_TRY(check_bf16(q, "q"));                 // 16-byte alignment (vector and bulk copies)
+    DF_TRY(check_bf16(cache_k, "cache_k"));
+    DF_TRY(check_bf16(cache_v, "cache_v"));
+    if (kb) {
+        DF_TRY(check_bf16(kb, "kb"));
+        DF_TRY(check_bf16(vb, "vb"));
+    }
+    DF_TRY(check_f32(out, "out"));
+    DF_TRY(get_ws(ws, ws_bytes, df_attention_workspace_bytes(B, blk, nq, nkv, d, cap)));
+    AttnArgs a = attention_plan(B, blk, nq, nkv, d, cap, kb != nullptr);
+    a.q = q;
+    a.cache_k = cache_k;
+    a.cache_v = cache_v;
+    a.cap = cap;
+    a.kb = kb;
+    a.vb = vb;
+    a.seq_len = seq_len;
+    a.causal_block = causal_block ? 1 : 0;
+    a.part = static_cast<float *>(ws);
+    a.out = out;
+    a.status = d_status;
+    return launch_attn(a, (cudaStream_t)stream);
+}
+
 int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
                          int K, const int32_t *eos, int n_eos, int32_t *committed,
                          int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,

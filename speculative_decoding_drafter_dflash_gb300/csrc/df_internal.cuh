@@ -303,14 +303,19 @@ struct AttnArgs {
     int causal_block;
     float *part;             // [B, nkv, n_chunks, R, d + 2] per-CTA partial (o, m, l)
     int n_chunks, chunk;     // key chunks per (sequence, KV head); keys per chunk
+    int tc;                  // 1: tensor-core kernel (chunk a multiple of 128 keys)
     const float *gate;       // optional [B*blk, ldg] gate pre-activation (q_total wide)
     int ldg;
-    uint16_t *pack;          // packed output [2*B*blk, nq*d]
+    uint16_t *pack;          // packed output [2*B*blk, nq*d] (or null)
+    float *out;              // F32 output [B*blk, nq*d] (or null)
     int32_t *status;
 };
 void attn_plan(AttnArgs &a, int max_keys);
 size_t attn_part_floats(const AttnArgs &a);
 int launch_attn(const AttnArgs &a, cudaStream_t s);
+bool attn_tc_supported(int d, int rows);
+int attn_tc_max_keys(int d, int rows);
+int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
 
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
                        int32_t *status, cudaStream_t s);

@@ -541,11 +541,14 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
             const float z = a.gate[t * a.ldg + (size_t)h * D + e];
             v = v * (1.f / (1.f + expf(-z)));
         }
-        uint16_t hi, lo;
-        split_hi_lo(v, hi, lo);
         const size_t col = (size_t)h * D + e;
-        a.pack[(2 * t) * (size_t)(a.nq * D) + col] = hi;
-        a.pack[(2 * t + 1) * (size_t)(a.nq * D) + col] = lo;
+        if (a.out) a.out[t * (size_t)(a.nq * D) + col] = v;
+        if (a.pack) {
+            uint16_t hi, lo;
+            split_hi_lo(v, hi, lo);
+            a.pack[(2 * t) * (size_t)(a.nq * D) + col] = hi;
+            a.pack[(2 * t + 1) * (size_t)(a.nq * D) + col] = lo;
+        }
     }
 }
 
@@ -591,17 +594,25 @@ size_t attn_part_floats(const AttnArgs &a) {
 }
 
 // Keys per chunk: a whole number of tiles, about one CTA per SM (two waves when sequences x
-// KV heads alone nearly fill the GPU).
+// KV heads alone nearly fill the GPU). Head dims 128 and 256 with up to 32 query rows per KV
+// head run on the tensor cores when a chunk fits the tensor-core kernel's score memory;
+// everything else runs on the CUDA cores.
 void attn_plan(AttnArgs &a, int max_keys) {
-    const int TK = kTileBytes / (2 * a.d * 4);
+    const int R = a.blk * (a.nq / a.nkv);
     const int heads = a.B * a.nkv;
     const int waves = heads > 38 ? 2 : 1;
-    int want = std::max(1, (waves * kNumSMs + heads - 1) / heads);
-    int tiles = std::max(1, (max_keys + TK - 1) / TK);
-    int n = std::min(want, tiles);
-    int per = (tiles + n - 1) / n;
-    a.chunk = per * TK;
-    a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
+    const int want = std::max(1, (waves * kNumSMs + heads - 1) / heads);
+    for (int tc = attn_tc_supported(a.d, R) ? 1 : 0; tc >= 0; --tc) {
+        const int TK = tc ? 128 : kTileBytes / (2 * a.d * 4);
+        const int tiles = std::max(1, (max_keys + TK - 1) / TK);
+        const int n = std::min(want, tiles);
+        const int per = (tiles + n - 1) / n;
+        if (tc && per * TK > attn_tc_max_keys(a.d, R)) continue;
+        a.tc = tc;
+        a.chunk = per * TK;
+        a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
+        return;
+    }
 }
 
 template <int D, int RPL>
@@ -617,7 +628,8 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     if (need_merge > (size_t)kAttnStages * kTileBytes)
         return fail(DF_ESHAPE, "attention: merge buffer exceeds the stage buffers");
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    DF_TRY(launch_k("attn_kernel", attn_kernel<D, RPL>, grid, dim3(kAttnThreads), smem, s, a));
+    if (a.tc) DF_TRY(launch_attn_tc(a, s));
+    else DF_TRY(launch_k("attn_kernel", attn_kernel<D, RPL>, grid, dim3(kAttnThreads), smem, s, a));
     dim3 cgrid((R + 7) / 8, a.nkv, a.B);
     return launch_k("attn_combine_kernel", attn_combine_kernel<D>, cgrid, dim3(256), 0, s, a);
 }

@@ -31,6 +31,7 @@
 #include <algorithm>
 
 #include "df_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace df {
 
@@ -41,7 +42,6 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;                    // BF16 elements per K block: one 128-byte row
 constexpr int kABytes = kBM * kBK * 2;     // 16 KB
 constexpr int kTokChunk = 8;               // tokens per TMEM load (16 columns)
-constexpr long long kTimeoutCycles = 4000000000LL;   // ~2 s at 2 GHz
 
 struct TcParams {
     CUtensorMap amap[4];
@@ -76,135 +76,6 @@ struct TcParams {
     int32_t *status;
 };
 
-// ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait on a barrier phase. Gives up (returns false) when another role has aborted or
-// after kTimeoutCycles, in which case it raises the CTA's abort flag and DF_ETIMEOUT.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
-    long long t0 = clock64();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
-                *abort_flag = 1;
-                set_status(status, DF_ETIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-// Bounded wait used while tearing down after an abort (ignores the abort flag).
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-    long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kTimeoutCycles) return;
-    }
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
-                                            int y, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
-                 "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // OR of a predicate over the 128 epilogue threads (named barrier 1).
@@ -219,18 +90,6 @@ __device__ __forceinline__ bool epi_any(bool v) {
         : "r"((uint32_t)v)
         : "memory");
     return r != 0;
-}
-
-// Shared-memory matrix descriptor: K-major operand stored as 128-byte rows, 128-byte swizzle,
-// 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;              // leading-dimension offset (unused for this layout)
-    d |= (uint64_t)(1024 >> 4) << 32;    // stride between 8-row groups
-    d |= (uint64_t)1 << 46;              // descriptor version
-    d |= (uint64_t)2 << 61;              // 128-byte swizzle
-    return d;
 }
 
 // ------------------------------------------------------------------ work split
@@ -658,42 +517,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-int get_encode() {
-    if (g_encode) return DF_OK;
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return fail(DF_ECUDA, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return DF_OK;
-}
-
 // 2-D BF16 map over rows x cols (row stride ld elements), box box_cols x box_rows, 128B swizzle.
 int make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
              uint32_t box_cols, uint32_t box_rows) {
-    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (ld * 2) % 16 != 0)
-        return fail(DF_EINVAL, "TMA operand misaligned (base %p, row stride %llu elements)", base,
-                    (unsigned long long)ld);
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(DF_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return DF_OK;
+    return make_tma_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, ld, box_cols,
+                       box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_out) {
-    DF_TRY(get_encode());
     TcParams p;
     memset(&p, 0, sizeof(p));
     const int T = a.T;
@@ -810,6 +643,40 @@ int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *
         if (a.pack_out) c.pack_out = a.pack_out + (size_t)2 * t0 * a.ldpo;
         DF_TRY(launch_chunk(c, sc, s, n_partials_out));
     }
+    return DF_OK;
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encode() {
+    if (g_encode) return DF_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(DF_ECUDA, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return DF_OK;
+}
+}  // namespace
+
+int make_tma_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem_bytes,
+                uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols, uint32_t box_rows,
+                CUtensorMapSwizzle swizzle) {
+    DF_TRY(get_encode());
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (ld * elem_bytes) % 16 != 0)
+        return fail(DF_EINVAL, "TMA operand misaligned (base %p, row stride %llu elements)", base,
+                    (unsigned long long)ld);
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * (uint64_t)elem_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DF_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return DF_OK;
 }
 

@@ -1,0 +1,128 @@
+"""The tensor-core attention kernel (head_dim 128 / 256, up to 32 query rows per KV head)
+against the oracle, through the DFlash forward and the MTP step: ragged context lengths,
+tiles that straddle the cache / block boundary, chunks of several tiles, the causal block
+variant, and a check that the tensor-core kernel is the one that ran."""
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_drafter_dflash_gb300 import binding as B
+from speculative_decoding_drafter_dflash_gb300 import synth
+from speculative_decoding_drafter_dflash_gb300.workloads import MTP_TINY, TINY
+from tests.harness import REL_TOL, rel_err
+from tests.test_gpu_dflash import _run_forward
+from tests.test_gpu_mtp import _run as _run_mtp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_drafter_dflash_gb300 import build
+    build.build()
+    B.lib()
+
+
+def _kernels(fn):
+    B.profile_enable(True)
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+        names = [n for n, _ in B.profile_read()]
+    finally:
+        B.profile_enable(False)
+    return out, names
+
+
+@pytest.mark.parametrize("d,nq,nkv,K,ctx,n_new", [
+    (128, 4, 2, 4, 300, [3]),        # 10 rows per KV head, cache/block boundary inside a tile
+    (128, 4, 2, 15, 250, [0]),       # 32 rows per KV head
+    (256, 4, 2, 15, 130, [5]),       # head_dim 256: two 128-wide halves
+    (256, 8, 8, 7, 64, [1]),         # one query head per KV head, a single partial tile
+])
+def test_dflash_forward_tensor_core_attention(d, nq, nkv, K, ctx, n_new):
+    shape = TINY.with_(head_dim=d, n_q_heads=nq, n_kv_heads=nkv, K=K, ctx=ctx)
+    r, names = _kernels(lambda: _run_forward(shape, n_new, seed=d + ctx))
+    assert "attn_tc_kernel" in names and "attn_kernel" not in names
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+
+
+def test_dflash_tensor_core_attention_multi_tile_chunks_batched_causal():
+    """16 KV heads x 2 sequences leave ~10 chunks per head, so each chunk spans two tiles."""
+    shape = TINY.with_(head_dim=128, n_q_heads=16, n_kv_heads=8, K=15, ctx=2000, batch=2)
+    r, names = _kernels(lambda: _run_forward(shape, [7, 2], seed=31))
+    assert "attn_tc_kernel" in names
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+    rc = _run_forward(shape, [4, 9], seed=32, causal=1)
+    assert rc["st"] == 0
+    assert rel_err(rc["h_final"].cpu().numpy(), rc["ref"]) <= REL_TOL
+
+
+@pytest.mark.parametrize("d,nq,nkv,kv_len,steps", [(256, 4, 2, 300, 2), (128, 6, 1, 700, 1)])
+def test_mtp_tensor_core_attention(d, nq, nkv, kv_len, steps):
+    shape = MTP_TINY.with_(head_dim=d, n_q_heads=nq, n_kv_heads=nkv, kv_len=kv_len)
+    r, names = _kernels(lambda: _run_mtp(shape, steps, seed=d))
+    assert "attn_tc_kernel" in names
+    assert r["st"] == 0
+    hid_ref = r["ref"][0]
+    assert rel_err(r["hid"][0].cpu().numpy(), hid_ref[0]) <= REL_TOL
+    assert list(synth.host(r["cache"].seq_len)) == list(r["ref"][4])
+
+
+# ---------------------------------------------------------------- df_attention on its own
+ATTN_TOL = 1e-4   # hi/lo BF16 operands carry ~16 mantissa bits; the CUDA-core path is plain F32
+
+
+def _attention_case(Bn, blk, nq, nkv, d, seq, cap, block_keys, causal, seed):
+    from oracle import core
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = torch.randn((Bn, blk, nq, d), generator=g, device="cuda")
+    ck = torch.randn((Bn, nkv, cap, d), generator=g, device="cuda")
+    cv = torch.randn((Bn, nkv, cap, d), generator=g, device="cuda")
+    kb = torch.randn((Bn, nkv, blk, d), generator=g, device="cuda") if block_keys else None
+    vb = torch.randn((Bn, nkv, blk, d), generator=g, device="cuda") if block_keys else None
+    sl = torch.tensor(seq, dtype=torch.int32, device="cuda")
+    out = torch.full((Bn, blk, nq, d), float("nan"), device="cuda")
+    ws = B.alloc_workspace(B.attention_workspace_bytes(Bn, blk, nq, nkv, d, cap))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    (_, names) = _kernels(lambda: B.attention(q, ck, cv, sl, out, ws, kb, vb, causal, st))
+    assert int(st) == 0
+    got = out.cpu().numpy()
+    qh, kh, vh = synth.host(q), synth.host(ck), synth.host(cv)
+    for b in range(Bn):
+        keys = kh[b, :, :seq[b]].transpose(1, 0, 2)
+        vals = vh[b, :, :seq[b]].transpose(1, 0, 2)
+        mask = None
+        if block_keys:
+            keys = np.concatenate([keys, synth.host(kb)[b].transpose(1, 0, 2)])
+            vals = np.concatenate([vals, synth.host(vb)[b].transpose(1, 0, 2)])
+            if causal:
+                mask = np.ones((blk, keys.shape[0]), dtype=bool)
+                mask[:, seq[b]:] = np.tril(np.ones((blk, blk), dtype=bool))
+        if keys.shape[0] == 0:
+            assert np.all(got[b] == 0.0)
+            continue
+        ref = core.sdpa(qh[b], keys, vals, mask, np.float64)
+        assert rel_err(got[b], ref) <= ATTN_TOL, f"sequence {b}"
+    return names
+
+
+@pytest.mark.parametrize("Bn,blk,nq,nkv,d,seq,cap,block_keys,causal,kernel", [
+    (2, 16, 16, 8, 128, [1000, 333], 1100, True, False, "attn_tc_kernel"),   # DFlash layout
+    (2, 16, 16, 8, 128, [257, 0], 400, True, True, "attn_tc_kernel"),        # causal, empty cache
+    (1, 1, 24, 4, 256, [2049], 2100, False, False, "attn_tc_kernel"),        # MTP dense GQA
+    (1, 1, 16, 2, 256, [3000], 3000, False, False, "attn_tc_kernel"),        # MTP MoE GQA, full cache
+    (3, 4, 4, 2, 64, [100, 1, 77], 128, True, False, "attn_kernel"),         # CUDA-core path
+    (1, 2, 2, 1, 32, [50], 64, True, True, "attn_kernel"),
+])
+def test_attention_matches_oracle(Bn, blk, nq, nkv, d, seq, cap, block_keys, causal, kernel):
+    names = _attention_case(Bn, blk, nq, nkv, d, seq, cap, block_keys, causal, seed=d + cap)
+    assert kernel in names
+
+
+def test_attention_no_visible_keys_gives_zeros():
+    _attention_case(1, 2, 4, 2, 128, [0], 64, False, False, seed=1)
