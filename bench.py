@@ -391,15 +391,18 @@ def run_native(args, rank, world, local_rank):
     }
 
 
-def kernel_hash():
-    """Hash of the CUDA sources: a stored traffic figure is only used for the kernels it was taken on."""
+LM_HEAD_SOURCES = ("k_gemm_tc.cu", "tc_ptx.cuh")
+
+
+def kernel_hash(files=LM_HEAD_SOURCES):
+    """Hash of the CUDA sources of the lm_head kernel: a stored traffic figure is only used for
+    the kernel code it was taken on."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_drafter_dflash_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -63,6 +63,30 @@ int launch_k(const char *name, void (*kernel)(KArgs...), dim3 grid, dim3 block, 
     return cuda_check(name, s);
 }
 
+// launch_k with a thread-block cluster of cluster_x CTAs along x (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+int launch_kc(const char *name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+              int cluster_x, cudaStream_t s, Args &&...args) {
+    prepare_kernel(reinterpret_cast<const void *>(kernel), (int)smem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    prof_begin(s);
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return cuda_check(name, s);
+}
+
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 

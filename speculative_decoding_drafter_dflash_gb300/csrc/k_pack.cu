@@ -4,7 +4,11 @@
 // RMSNorm follows hf2q 0.1.1 models/qwen35/mtp.rs `rms_norm_with_weight`
 // (y = x * 1/sqrt(mean(x^2) + eps) * w, F32 weight); the embedding gather is
 // qwen35_orchestrator.rs step 1 (`embed_tokens_gpu` of [last_token, mask x K]).
+#include <cooperative_groups.h>
+
 #include "df_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace df {
 
@@ -81,32 +85,35 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
     }
 }
 
-// Register-resident variant for rows of at most 256 * 4 * NV elements: every element is loaded
-// once (128-bit loads, all issued before the reduction), kept in registers for the second
-// pass, and stored as packed 4-element groups.
+// Register-resident variant: a row is split over a cluster of `cl` CTAs (consecutive blockIdx.x),
+// each holding at most 256 * 4 * NV of its elements in registers. Every element and every
+// split partial is loaded once with 128-bit loads, all issued before any is used; the RMSNorm
+// sum of squares is reduced in the CTA and then across the cluster through distributed shared
+// memory, in rank order, so every CTA of a row applies the same factor.
 template <int NV>
-__global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
+__global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a, int cl) {
+    constexpr int G = NV <= 2 ? 8 : 4;   // split partials loaded per round
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
-    const int t = blockIdx.x;
-    const int K = a.K, K4 = K >> 2;
+    const int t = blockIdx.x / cl, rank = blockIdx.x - t * cl;
+    const int K = a.K, K4 = K >> 2, per4 = K4 / cl, base4 = rank * per4;
     const int s = t / a.rows_per_seq, j = t - s * a.rows_per_seq;
     const bool valid = a.nvalid == nullptr || j < min(max(a.nvalid[s], 0), a.rows_per_seq);
     int id = 0;
     if (a.gather) {
         id = a.ids ? a.ids[t] : (j == 0 ? a.last_token[s] : a.mask_id);
         if (id < 0 || id >= a.vocab) {
-            if (threadIdx.x == 0) set_status(a.status, DF_EINVAL);
+            if (threadIdx.x == 0 && rank == 0) set_status(a.status, DF_EINVAL);
             id = min(max(id, 0), a.vocab - 1);
         }
     }
     float4 x[NV];
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        const int k4 = threadIdx.x + u * kPackThreads;
+        const int i4 = threadIdx.x + u * kPackThreads, k4 = base4 + i4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid && k4 < K4) {
+        if (valid && i4 < per4) {
             if (a.gather) {
                 const uint2 g = *reinterpret_cast<const uint2 *>(a.gather + (size_t)id * K + 4 * k4);
                 v = make_float4(__uint_as_float(g.x << 16) * a.scale,
@@ -120,28 +127,29 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
         x[u] = v;
     }
     if (a.part && valid) {
-        // every split's values are loaded before any is added; the sum runs in split order
-        for (int sp0 = 0; sp0 < a.n_part; sp0 += 4) {
-            float4 pv[4][NV];
+        // every split's values of a round are loaded before any is added; the sum runs in
+        // split order
+        for (int sp0 = 0; sp0 < a.n_part; sp0 += G) {
+            float4 pv[G][NV];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int jj = 0; jj < G; ++jj)
 #pragma unroll
                 for (int u = 0; u < NV; ++u) {
-                    const int k4 = threadIdx.x + u * kPackThreads;
-                    pv[j][u] = (sp0 + j < a.n_part && k4 < K4)
-                                   ? *reinterpret_cast<const float4 *>(
-                                         a.part + (size_t)(sp0 + j) * a.part_stride +
-                                         (size_t)t * a.ldpart + 4 * k4)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int i4 = threadIdx.x + u * kPackThreads;
+                    pv[jj][u] = (sp0 + jj < a.n_part && i4 < per4)
+                                    ? *reinterpret_cast<const float4 *>(
+                                          a.part + (size_t)(sp0 + jj) * a.part_stride +
+                                          (size_t)t * a.ldpart + 4 * (base4 + i4))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int jj = 0; jj < G; ++jj)
 #pragma unroll
                 for (int u = 0; u < NV; ++u) {
-                    x[u].x += pv[j][u].x;
-                    x[u].y += pv[j][u].y;
-                    x[u].z += pv[j][u].z;
-                    x[u].w += pv[j][u].w;
+                    x[u].x += pv[jj][u].x;
+                    x[u].y += pv[jj][u].y;
+                    x[u].z += pv[jj][u].z;
+                    x[u].w += pv[jj][u].w;
                 }
         }
     }
@@ -151,14 +159,32 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
 #pragma unroll
         for (int u = 0; u < NV; ++u)
             ss = fmaf(x[u].x, x[u].x, fmaf(x[u].y, x[u].y, fmaf(x[u].z, x[u].z, fmaf(x[u].w, x[u].w, ss))));
-        ss = block_sum(ss, red);
+        ss = warp_sum(ss);
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        if (l == 0) red[w] = ss;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+            for (int i = 0; i < kPackThreads / 32; ++i) tot += red[i];
+            red[32] = tot;
+        }
+        if (cl > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();
+            float tot = 0.f;
+            for (int r = 0; r < cl; ++r) tot += *cluster.map_shared_rank(&red[32], r);
+            ss = tot;
+        } else {
+            __syncthreads();
+            ss = red[32];
+        }
         inv = 1.f / sqrtf(ss / (float)K + a.eps);
     }
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        const int k4 = threadIdx.x + u * kPackThreads;
-        if (k4 >= K4) continue;
-        const int k = 4 * k4;
+        const int i4 = threadIdx.x + u * kPackThreads;
+        if (i4 >= per4) continue;
+        const int k = 4 * (base4 + i4);
         float4 v = x[u];
         if (a.h_out) *reinterpret_cast<float4 *>(a.h_out + (size_t)t * a.ldh + k) = v;
         if (a.norm_w) {
@@ -178,6 +204,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a) {
                 make_uint2(l0 | ((uint32_t)l1 << 16), l2 | ((uint32_t)l3 << 16));
         }
     }
+    // peers may still be reading red[32] through distributed shared memory
+    if (a.norm_w && cl > 1) cg::this_cluster().sync();
 }
 
 bool aligned_for_vec(const PackArgs &a) {
@@ -197,16 +225,30 @@ bool aligned_for_vec(const PackArgs &a) {
 
 int launch_pack(const PackArgs &a, cudaStream_t s) {
     if (a.T <= 0) return DF_OK;
-    const int nv = (a.K / 4 + kPackThreads - 1) / kPackThreads;
-    const dim3 g(a.T), b(kPackThreads);
-    if (aligned_for_vec(a) && nv <= 16) {
-        if (nv <= 1) return launch_k("pack_kernel", pack_vec_kernel<1>, g, b, 0, s, a);
-        if (nv <= 2) return launch_k("pack_kernel", pack_vec_kernel<2>, g, b, 0, s, a);
-        if (nv <= 4) return launch_k("pack_kernel", pack_vec_kernel<4>, g, b, 0, s, a);
-        if (nv <= 8) return launch_k("pack_kernel", pack_vec_kernel<8>, g, b, 0, s, a);
-        return launch_k("pack_kernel", pack_vec_kernel<16>, g, b, 0, s, a);
+    if (aligned_for_vec(a)) {
+        // Split each row over up to 8 CTAs of a cluster, keeping at least 64 4-element groups
+        // per CTA.
+        const int K4 = a.K / 4;
+        int cl = 8;
+        while (cl > 1 && (K4 % cl != 0 || K4 / cl < 64)) cl >>= 1;
+        const int nv = (K4 / cl + kPackThreads - 1) / kPackThreads;
+        const dim3 g(a.T * cl), b(kPackThreads);
+        if (nv <= 16) {
+            if (cl > 1) {
+                if (nv <= 1) return launch_kc("pack_kernel", pack_vec_kernel<1>, g, b, 0, cl, s, a, cl);
+                if (nv <= 2) return launch_kc("pack_kernel", pack_vec_kernel<2>, g, b, 0, cl, s, a, cl);
+                if (nv <= 4) return launch_kc("pack_kernel", pack_vec_kernel<4>, g, b, 0, cl, s, a, cl);
+                if (nv <= 8) return launch_kc("pack_kernel", pack_vec_kernel<8>, g, b, 0, cl, s, a, cl);
+                return launch_kc("pack_kernel", pack_vec_kernel<16>, g, b, 0, cl, s, a, cl);
+            }
+            if (nv <= 1) return launch_k("pack_kernel", pack_vec_kernel<1>, g, b, 0, s, a, cl);
+            if (nv <= 2) return launch_k("pack_kernel", pack_vec_kernel<2>, g, b, 0, s, a, cl);
+            if (nv <= 4) return launch_k("pack_kernel", pack_vec_kernel<4>, g, b, 0, s, a, cl);
+            if (nv <= 8) return launch_k("pack_kernel", pack_vec_kernel<8>, g, b, 0, s, a, cl);
+            return launch_k("pack_kernel", pack_vec_kernel<16>, g, b, 0, s, a, cl);
+        }
     }
-    return launch_k("pack_kernel", pack_kernel, g, b, 0, s, a);
+    return launch_k("pack_kernel", pack_kernel, dim3(a.T), dim3(kPackThreads), 0, s, a);
 }
 
 }  // namespace df
