@@ -49,7 +49,13 @@ void prepare_kernel(const void *func, int dyn_smem) {
         const char *e = getenv("DF_CARVEOUT");
         return e ? atoi(e) : 100;
     }();
-    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    // The dynamic limit is what the device allows per block minus the kernel's static shared
+    // memory (asking for more fails and would leave the 48 KB default in place).
+    int optin = 232448;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, func) == cudaSuccess) optin -= (int)fa.sharedSizeBytes;
+    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (carveout >= 0)
         cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
     cudaGetLastError();
