@@ -22,4 +22,7 @@ Pin status (what each function is checked against, in tests/test_oracle_*.py):
   kv_rollback            hand examples, overflow rejection
   dflash forward / mtp   special cases with closed forms (zero projections, one key), float64 shadow
   moe routing            hand example, top-k weights sum to one, one-expert reduction to dense
+  stochastic accept      hand draws, exact identity (committed token ~ target softmax) with a
+                         planted wrong residual, Monte-Carlo run of the walk, greedy limit at
+                         T -> 0 equals accept_walk, identical distributions accept everything
 """
