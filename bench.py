@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe", "attn"],
+    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe", "attn",
+                                                     "stochastic"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -659,6 +660,49 @@ def attn_case(steps: int):
         del q, ck, cv, kb, vb, out, ws
 
 
+def stochastic_case(steps: int):
+    """The stochastic accept step alone (K=15, V=262144, T=0.8) for 1 and 8 sequences: logit
+    bytes read once over time, each call timed with CUDA events after an L2-evicting write."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    hbm_peak, _ = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    K, V, T = 15, 262144, 0.8
+    for Bn in (1, 8):
+        tl = torch.randn((Bn, K + 1, V), generator=g, device=dev) * 2.0
+        dl = (tl[:, :K] + torch.randn((Bn, K, V), generator=g, device=dev) * 0.5).contiguous()
+        drafts = torch.argmax(dl, dim=-1).to(torch.int32).contiguous()
+        ua = torch.rand((Bn, K), generator=g, device=dev)
+        us = torch.rand((Bn,), generator=g, device=dev)
+        eos = torch.tensor([1], dtype=torch.int32, device=dev)
+        out = {k: torch.empty((Bn,), dtype=torch.int32, device=dev)
+               for k in ("n_committed", "accept", "hit_eos", "rollback")}
+        out["committed"] = torch.empty((Bn, K + 1), dtype=torch.int32, device=dev)
+        ws = B.alloc_workspace(B.accept_stochastic_workspace_bytes(Bn, K, V), dev)
+        for _ in range(3):
+            B.accept_stochastic(dl, tl, drafts, T, ua, us, eos, out, ws)
+        times = []
+        for _ in range(steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.accept_stochastic(dl, tl, drafts, T, ua, us, eos, out, ws)
+            e1.record()
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        us_ = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
+        nb = Bn * (2 * K + 1) * V * 4
+        print(json.dumps({"profile_case": "stochastic", "workload": f"accept-k{K}-v{V}-b{Bn}",
+                          "us": round(us_, 2), "logit_bytes": nb,
+                          "gbs": round(nb / us_ / 1e3, 1),
+                          "frac_of_measured_hbm": round(nb / us_ / 1e3 / hbm_peak, 4),
+                          "mean_accept": float(out["accept"].float().mean())}), flush=True)
+        del tl, dl, ws
+
+
 def profile_case(args):
     """A small, self-contained case for ncu: the full-size lm_head argmax (1.48 GB of weights,
     larger than L2) over the 16 block rows, 2 warm-up launches then 3 profiled ones; or one
@@ -678,6 +722,8 @@ def profile_case(args):
         return moe_case(args.steps)
     if args.profile_case == "attn":
         return attn_case(args.steps)
+    if args.profile_case == "stochastic":
+        return stochastic_case(args.steps)
     if args.profile_case == "lm_head":
         W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)

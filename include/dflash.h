@@ -245,6 +245,42 @@ int accept_prefix_argmax_host(const int32_t *drafts, const int32_t *target, int 
                               int32_t *rollback);
 
 /* ------------------------------------------------------------------------------------------
+ * Non-greedy accept step: speculative sampling at temperature T > 0. qwen35_orchestrator.rs,
+ * module doc "Non-greedy (Metropolis-Hastings) is out of scope here": stochastic acceptance is
+ * wired through the MTP K=1 path and would take the place of `step_round_from_argmaxes` at
+ * step 11 of the DFlash loop. The page gives no formula; the rule is read as the standard
+ * speculative-sampling test. With p_i = softmax(target_logits[b, i] / T) and
+ * q_i = softmax(draft_logits[b, i] / T):
+ *   draft x_i is accepted while u_accept[b, i] * q_i(x_i) < p_i(x_i);
+ *   at the first rejection a the committed token is drawn from max(0, p_a - q_a) (normalised),
+ *   after K acceptances from p_K;
+ *   a draw from weights w with uniform u is the smallest j with w_0 + ... + w_j > u * sum(w).
+ * committed / n_committed / hit_eos / rollback follow the greedy walk: accepted drafts then the
+ * drawn token, cut after the first EOS id, -1 past n_committed, rollback = K - accept_count.
+ * ---------------------------------------------------------------------------------------- */
+/* Workspace (chunk statistics, per-sequence state, draw partial sums, counters); allocate it
+ * zeroed. 0 for unsupported sizes. */
+size_t df_accept_stochastic_workspace_bytes(int B, int K, int V);
+
+/*   draft_logits   device F32 [B, K, V]: drafter logits of block positions 1..K, 16-byte aligned
+ *   target_logits  device F32 [B, K+1, V]: verifier logits at positions 0..K, 16-byte aligned
+ *   V              vocabulary, a positive multiple of 4
+ *   drafts         device int32 [B, K]: the drafted tokens (ids outside [0, V) are clamped and
+ *                  set DF_EINVAL in d_status)
+ *   temperature    > 0 (DF_EINVAL otherwise; temperature 0 is accept_prefix_argmax)
+ *   u_accept       device F32 [B, K] uniforms in [0, 1); u_sample device F32 [B] the same
+ *   eos            device int32 [n_eos] (NULL when n_eos == 0)
+ *   committed      device int32 [B, K+1] out; n_committed, accept_count, hit_eos, rollback
+ *                  device int32 [B] out
+ * 1 <= K <= 64. A draw whose weights sum to zero sets DF_EINVAL in d_status. */
+int accept_stochastic(const float *draft_logits, const float *target_logits, int V,
+                      const int32_t *drafts, int B, int K, float temperature,
+                      const float *u_accept, const float *u_sample, const int32_t *eos, int n_eos,
+                      int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                      int32_t *hit_eos, int32_t *rollback, void *ws, size_t ws_bytes,
+                      int32_t *d_status, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * KV rollback (qwen35_orchestrator.rs step 8, `rollback_kv`): seq_len[b] -= n[b]. Cache rows
  * are not touched. If n[b] < 0 or n[b] > seq_len[b], seq_len[b] is left unchanged and
  * DF_ECAPACITY is written to d_status.

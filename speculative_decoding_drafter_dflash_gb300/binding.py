@@ -108,6 +108,11 @@ _SIGS = [
     ("mtp_forward_draft", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), POINTER(KvCache),
                                   c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_size_t, c_void_p, c_void_p]),
+    ("df_accept_stochastic_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
+    ("accept_stochastic", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
+                                  c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
+                                  c_void_p]),
     ("df_attention_workspace_bytes", c_size_t, [c_int] * 6),
     ("df_attention", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
                              c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
@@ -393,3 +398,21 @@ def attention(q, cache_k, cache_v, seq_len, out, ws, kb=None, vb=None, causal_bl
     _check(lib().df_attention(_p(q), _p(cache_k), _p(cache_v), cap, _p(seq_len), _p(kb), _p(vb),
                               Bn, blk, nq, nkv, d, 1 if causal_block else 0, _p(out), _p(ws),
                               ws.numel(), _p(d_status), _stream(stream)))
+
+
+def accept_stochastic_workspace_bytes(B: int, K: int, V: int) -> int:
+    return int(lib().df_accept_stochastic_workspace_bytes(B, K, V))
+
+
+def accept_stochastic(draft_logits, target_logits, drafts, temperature: float, u_accept,
+                      u_sample, eos, out: dict, ws, d_status=None, stream=None):
+    """draft_logits [B, K, V], target_logits [B, K+1, V], drafts [B, K] int32, u_accept [B, K],
+    u_sample [B]; out holds device int32 committed [B, K+1] and n_committed / accept /
+    hit_eos / rollback [B]."""
+    B, K, V = draft_logits.shape
+    n_eos = 0 if eos is None else eos.numel()
+    _check(lib().accept_stochastic(_p(draft_logits), _p(target_logits), V, _p(drafts), B, K,
+                                   float(temperature), _p(u_accept), _p(u_sample), _p(eos), n_eos,
+                                   _p(out["committed"]), _p(out["n_committed"]), _p(out["accept"]),
+                                   _p(out["hit_eos"]), _p(out["rollback"]), _p(ws), ws.numel(),
+                                   _p(d_status), _stream(stream)))

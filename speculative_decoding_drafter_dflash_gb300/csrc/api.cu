@@ -757,6 +757,64 @@ int df_attention(const float *q, const float *cache_k, const float *cache_v, int
     return launch_attn(a, (cudaStream_t)stream);
 }
 
+static void carve_sample(Carve &cv, SampleArgs &a, int B, int K, int V) {
+    a.n_chunks = sample_chunks(V);
+    a.stats = cv.take<MaxSum>((size_t)B * (2 * K + 1) * a.n_chunks);
+    a.state = cv.take<SampleState>((size_t)B);
+    a.csum = cv.take<float>((size_t)B * a.n_chunks);
+    a.counters = cv.take<int>((size_t)B);
+}
+
+size_t df_accept_stochastic_workspace_bytes(int B, int K, int V) {
+    if (B <= 0 || K < 1 || K > 64 || V <= 0 || V % 4 != 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    SampleArgs a;
+    carve_sample(cv, a, B, K, V);
+    return cv.off;
+}
+
+int accept_stochastic(const float *draft_logits, const float *target_logits, int V,
+                      const int32_t *drafts, int B, int K, float temperature,
+                      const float *u_accept, const float *u_sample, const int32_t *eos, int n_eos,
+                      int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                      int32_t *hit_eos, int32_t *rollback, void *ws, size_t ws_bytes,
+                      int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(B > 0 && K >= 1 && K <= 64, DF_ESHAPE, "B=%d K=%d (1 <= K <= 64)", B, K);
+    REQ(V > 0 && V % 4 == 0, DF_ESHAPE, "V=%d (a positive multiple of 4)", V);
+    REQ(temperature > 0.f, DF_EINVAL, "temperature=%g (the greedy walk is accept_prefix_argmax)",
+        (double)temperature);
+    REQ(draft_logits && target_logits && drafts && u_accept && u_sample && committed &&
+            n_committed && accept_count && hit_eos && rollback,
+        DF_EINVAL, "NULL input or output");
+    REQ(n_eos >= 0 && (n_eos == 0 || eos), DF_EINVAL, "eos is NULL with n_eos=%d", n_eos);
+    DF_TRY(check_bf16(draft_logits, "draft_logits"));      // 16-byte alignment
+    DF_TRY(check_bf16(target_logits, "target_logits"));
+    DF_TRY(get_ws(ws, ws_bytes, df_accept_stochastic_workspace_bytes(B, K, V)));
+    SampleArgs a;
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    carve_sample(cv, a, B, K, V);
+    a.draft = draft_logits;
+    a.target = target_logits;
+    a.V = V;
+    a.B = B;
+    a.K = K;
+    a.T = temperature;
+    a.scale = (float)(1.4426950408889634 / (double)temperature);
+    a.drafts = drafts;
+    a.u_accept = u_accept;
+    a.u_sample = u_sample;
+    a.eos = eos;
+    a.n_eos = n_eos;
+    a.committed = committed;
+    a.n_committed = n_committed;
+    a.accept_count = accept_count;
+    a.hit_eos = hit_eos;
+    a.rollback = rollback;
+    a.status = d_status;
+    return launch_accept_stochastic(a, (cudaStream_t)stream);
+}
+
 int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
                          int K, const int32_t *eos, int n_eos, int32_t *committed,
                          int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,

@@ -341,6 +341,38 @@ bool attn_tc_supported(int d, int rows);
 int attn_tc_max_keys(int d, int rows);
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
 
+// Non-greedy accept step (speculative sampling) over B sequences of K drafts and vocab V.
+constexpr int kSampleMaxK = 64;
+struct MaxSum {
+    float m, s;              // max of x, sum of exp(x - m)
+};
+struct SampleState {
+    int acc;                 // accepted drafts
+    float mp, sp, mq, sq;    // max and 1 / sum of the rows the committed token is drawn from
+};
+struct SampleArgs {
+    const float *draft = nullptr;    // [B, K, V] drafter logits (block positions 1..K)
+    const float *target = nullptr;   // [B, K+1, V] verifier logits (positions 0..K)
+    int V = 0, B = 0, K = 0;
+    float T = 1.f;                   // temperature > 0
+    float scale = 1.f;               // log2(e) / T
+    const int32_t *drafts = nullptr; // [B, K]
+    const float *u_accept = nullptr; // [B, K] uniforms in [0, 1)
+    const float *u_sample = nullptr; // [B]
+    const int32_t *eos = nullptr;
+    int n_eos = 0;
+    int32_t *committed = nullptr, *n_committed = nullptr, *accept_count = nullptr;
+    int32_t *hit_eos = nullptr, *rollback = nullptr;
+    int n_chunks = 0;
+    MaxSum *stats = nullptr;         // [B, 2K+1, n_chunks]
+    SampleState *state = nullptr;    // [B]
+    float *csum = nullptr;           // [B, n_chunks]
+    int *counters = nullptr;         // [B], zero between calls
+    int32_t *status = nullptr;
+};
+int sample_chunks(int V);
+int launch_accept_stochastic(const SampleArgs &a, cudaStream_t s);
+
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
                        int32_t *status, cudaStream_t s);
 int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
