@@ -25,4 +25,7 @@ Pin status (what each function is checked against, in tests/test_oracle_*.py):
   stochastic accept      hand draws, exact identity (committed token ~ target softmax) with a
                          planted wrong residual, Monte-Carlo run of the walk, greedy limit at
                          T -> 0 equals accept_walk, identical distributions accept everything
+  generate loop          capture helpers by hand; output follows the verifier (the reference when
+                         it never agrees), every draft accepted when it always agrees, budget
+                         truncation, EOS stop, max_new_tokens == 0, prefix one behind the output
 """
