@@ -44,7 +44,7 @@ def parse():
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe", "attn",
-                                                     "stochastic"],
+                                                     "stochastic", "generate"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -703,6 +703,65 @@ def stochastic_case(steps: int):
         del tl, dl, ws
 
 
+def generate_case(steps: int):
+    """The device generate loop (one CUDA graph with a while node) on the DFlash K=15 shape:
+    prompt 4096 tokens already in the drafter cache, 256 new tokens, a synthetic verifier that
+    takes a draft with probability 0.6 per position. Tokens/s and time per round, CUDA events
+    around each call (state reset outside the timed region)."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+    dev = torch.device("cuda", 0)
+    s = DFLASH_K15
+    K, prompt, max_new, n_comb = s.K, s.ctx, 256, s.n_target_layers + 1
+    max_len = prompt + max_new + 2 * (K + 2)
+    for Bn in (1, 4):
+        w = synth.dflash_weights(s, seed=0, device=dev) if Bn == 1 else w
+        cache = synth.kv_cache(s.n_layers, Bn, s.n_kv_heads, s.head_dim, prompt, max_len, 1, dev)
+        seq0 = cache.seq_len.clone()
+        g = torch.Generator(device=dev).manual_seed(2)
+        ref = torch.randint(2, s.vocab - 2, (Bn, max_len), generator=g, device=dev,
+                            dtype=torch.int32)
+        agree = (torch.rand((Bn, max_len), generator=g, device=dev) < 0.6).to(torch.uint8)
+        table = torch.randn((Bn, n_comb, max_len, s.hidden), generator=g, device=dev)
+        prior = table.clone()
+        model = B.DFlashModel(s, w, cache)
+        n_new_max = K + 1
+        ws = B.alloc_workspace(B.generate_workspace_bytes(model, Bn, K, n_new_max), dev)
+        out = torch.zeros((Bn, max_len), dtype=torch.int32, device=dev)
+        out[:, :prompt + 1] = ref[:, :prompt + 1]
+        pl = torch.full((Bn,), prompt, dtype=torch.int32, device=dev)
+        out_len, prior_len = pl + 1, pl.clone()
+        rounds = torch.zeros(Bn, dtype=torch.int32, device=dev)
+        eos = torch.tensor([1], dtype=torch.int32, device=dev)
+        max_rounds = max_new
+        times, toks, rnds = [], [], []
+        for it in range(steps + 2):
+            cache.seq_len.copy_(seq0)
+            out_len.copy_(pl + 1)
+            prior_len.copy_(pl)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.generate(model, ref, agree, table, list(range(s.n_target_layers)), prior, prior_len,
+                       out, out_len, pl, max_new, max_rounds, K, n_new_max, eos, rounds, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= 2:                          # the first calls build and warm the graph
+                times.append(e0.elapsed_time(e1))
+                toks.append(int((out_len - pl).sum()))
+                rnds.append(int(rounds.max()))
+        ms = statistics.median(times)
+        print(json.dumps({"profile_case": "generate", "workload": f"dflash-k15-ctx4096-b{Bn}-new256",
+                          "ms_per_call": round(ms, 3), "tokens": toks[-1], "rounds": rnds[-1],
+                          "tokens_per_s": round(toks[-1] / ms * 1e3, 1),
+                          "us_per_round": round(ms * 1e3 / rnds[-1], 1),
+                          "tokens_per_round": round(toks[-1] / Bn / rnds[-1], 3)}), flush=True)
+        del cache, ws, table, prior
+
+
 def profile_case(args):
     """A small, self-contained case for ncu: the full-size lm_head argmax (1.48 GB of weights,
     larger than L2) over the 16 block rows, 2 warm-up launches then 3 profiled ones; or one
@@ -724,6 +783,8 @@ def profile_case(args):
         return attn_case(args.steps)
     if args.profile_case == "stochastic":
         return stochastic_case(args.steps)
+    if args.profile_case == "generate":
+        return generate_case(args.steps)
     if args.profile_case == "lm_head":
         W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)

@@ -333,6 +333,60 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
                         size_t ws_bytes, df_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Multi-round generate loop on the device (qwen35_orchestrator.rs, `dispatch_qwen35_dflash_
+ * generate`, "Multi-round loop (Option A)", steps 1-10 and the final truncation) with a
+ * synthetic verifier standing in for the target model. Per round, for every sequence still
+ * running: n_new = prior_len - drafter cache length new context rows, gathered from the
+ * captured verifier states as the concatenation of the drafter's target layers
+ * (`extract_drafter_concat`); the draft round (df_draft_round's steps); the verifier's greedy
+ * tokens for [last_token, drafts]; the greedy accept walk; the committed tokens appended and
+ * last_token updated; the sequence stops on EOS, when out_len - prompt_len >= max_new_tokens
+ * (then out_len is truncated to prompt_len + max_new_tokens) or when the next round would not
+ * fit max_len; otherwise the first n_committed verify positions are appended to the captured
+ * prefix (`append_capture_positions`). Before the first round a sequence whose last token is an
+ * EOS id, or any sequence when max_new_tokens == 0, is done (the page returns prompt + first
+ * token). The whole loop is one CUDA graph: a while node repeats the round until no sequence is
+ * running or max_rounds rounds have run; no host synchronisation happens in between.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+    const int32_t *ref;     /* device [B, max_len]: the verifier's greedy token after position p
+                               is ref[b, p + 1] ... */
+    const uint8_t *agree;   /* ... unless agree[b, p] != 0 (device [B, max_len], or NULL) for a
+                               drafted position p < p0 + K of a verify starting at p0, where it
+                               is the draft itself */
+    const float *table;     /* device [B, n_comb, max_len, H]: the verifier's captured hidden
+                               state of capture layer c at position p */
+    int32_t n_comb;         /* capture layers */
+    int32_t sel[16];        /* the drafter's target layer l is capture layer sel[l] */
+    int32_t max_len;        /* positions per sequence in ref, agree, table, prior_cap, out */
+} df_synthetic_verifier;
+
+/* Workspace: the round's (df_dflash_workspace_bytes(cfg, B, K+1, n_new_max)) plus the loop's
+ * round scratch; allocate it zeroed. 0 on invalid arguments (n_new_max < K + 1). */
+size_t df_generate_workspace_bytes(const df_dflash_config *cfg, int B, int K, int n_new_max);
+
+/*   prior_cap      device F32 [B, n_comb, max_len, H] in/out: captured verifier states of the
+ *                  committed prefix, positions [0, prior_len[b])
+ *   prior_len      device int32 [B] in/out: must equal out_len - 1 on entry
+ *   out_tokens     device int32 [B, max_len] in/out: prompt + first token on entry (out_len[b]
+ *                  of them), the generated tokens appended
+ *   out_len        device int32 [B] in/out
+ *   prompt_len     device int32 [B]
+ *   rounds         device int32 [B] out: rounds each sequence ran
+ *   accept_hist    device int32 [max_rounds, B] out (or NULL): accept count of round r, for the
+ *                  sequences that ran it
+ *   n_new_max      >= K + 1 and >= the first round's prior_len - cache length (the drafter's
+ *                  initial catch-up); at most cache->cap
+ * The drafter cache advances as in df_draft_round. The first call with a given set of
+ * arguments builds and keeps the loop graph; later calls with the same arguments relaunch it. */
+int df_generate(const df_dflash_config *cfg, const df_dflash_weights *w, const df_kv_cache *cache,
+                const df_synthetic_verifier *v, float *prior_cap, int32_t *prior_len,
+                int32_t *out_tokens, int32_t *out_len, const int32_t *prompt_len,
+                int max_new_tokens, int max_rounds, int B, int K, int n_new_max,
+                const int32_t *eos, int n_eos, int32_t *rounds, int32_t *accept_hist, void *ws,
+                size_t ws_bytes, int32_t *d_status, df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * MTP (NextN) draft step, mtp.rs `MtpWeights::forward_draft_with_hidden`, chained n_steps
  * times (the returned hidden feeds the next step with the embedding of the step's argmax).
  * ---------------------------------------------------------------------------------------- */

@@ -46,6 +46,11 @@ class DFlashWeights(ctypes.Structure):
                 ("layers", POINTER(LayerWeights)), ("embed", c_void_p), ("lm_head", c_void_p)]
 
 
+class SyntheticVerifier(ctypes.Structure):
+    _fields_ = [("ref", c_void_p), ("agree", c_void_p), ("table", c_void_p), ("n_comb", c_int32),
+                ("sel", c_int32 * 16), ("max_len", c_int32)]
+
+
 class KvCache(ctypes.Structure):
     _fields_ = [("k", POINTER(c_void_p)), ("v", POINTER(c_void_p)), ("seq_len", c_void_p),
                 ("cap", c_int32), ("batch", c_int32), ("n_layers", c_int32)]
@@ -109,6 +114,11 @@ _SIGS = [
                                   c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_size_t, c_void_p, c_void_p]),
     ("df_accept_stochastic_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
+    ("df_generate_workspace_bytes", c_size_t, [POINTER(DFlashConfig), c_int, c_int, c_int]),
+    ("df_generate", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), POINTER(KvCache),
+                            POINTER(SyntheticVerifier), c_void_p, c_void_p, c_void_p, c_void_p,
+                            c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_int,
+                            c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     ("accept_stochastic", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
                                   c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
@@ -416,3 +426,31 @@ def accept_stochastic(draft_logits, target_logits, drafts, temperature: float, u
                                    _p(out["committed"]), _p(out["n_committed"]), _p(out["accept"]),
                                    _p(out["hit_eos"]), _p(out["rollback"]), _p(ws), ws.numel(),
                                    _p(d_status), _stream(stream)))
+
+
+def generate_workspace_bytes(model: "DFlashModel", B: int, K: int, n_new_max: int) -> int:
+    return int(lib().df_generate_workspace_bytes(ctypes.byref(model.cfg), B, K, n_new_max))
+
+
+def generate(model: "DFlashModel", ref, agree, table, sel, prior_cap, prior_len, out_tokens,
+             out_len, prompt_len, max_new_tokens: int, max_rounds: int, K: int, n_new_max: int,
+             eos, rounds, ws, accept_hist=None, d_status=None, stream=None):
+    """The device generate loop (see include/dflash.h, df_generate). ref/agree [B, max_len],
+    table [B, n_comb, max_len, H], sel: list of capture-layer indices of the drafter's target
+    layers; the state tensors are device tensors updated in place."""
+    B, max_len = ref.shape
+    v = SyntheticVerifier()
+    v.ref = ref.data_ptr()
+    v.agree = None if agree is None else agree.data_ptr()
+    v.table = table.data_ptr()
+    v.n_comb = table.shape[1]
+    for i, c in enumerate(sel):
+        v.sel[i] = int(c)
+    v.max_len = max_len
+    n_eos = 0 if eos is None else eos.numel()
+    _check(lib().df_generate(ctypes.byref(model.cfg), ctypes.byref(model.weights),
+                             ctypes.byref(model.cache_c), ctypes.byref(v), _p(prior_cap),
+                             _p(prior_len), _p(out_tokens), _p(out_len), _p(prompt_len),
+                             max_new_tokens, max_rounds, B, K, n_new_max, _p(eos), n_eos,
+                             _p(rounds), _p(accept_hist), _p(ws), ws.numel(), _p(d_status),
+                             _stream(stream)))

@@ -986,6 +986,218 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
 
 }  // extern "C"
 
+// ================================================================ multi-round generate loop
+namespace df {
+namespace {
+
+// Round scratch of the loop, after the round's own workspace.
+struct LoopWs {
+    float *th;
+    int32_t *ints;
+};
+
+size_t loop_extra_bytes(const df_dflash_config *c, int B, int K, int n_new_max) {
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    cv.take<float>((size_t)B * std::max(n_new_max, 1) * c->n_target_layers * c->hidden);
+    cv.take<int32_t>((size_t)B * (4 * (K + 1) + 8) + 8);
+    return cv.off;
+}
+
+// One cached executable graph: the loop is rebuilt only when an argument changes.
+struct LoopGraph {
+    std::mutex mu;
+    uint64_t key = 0;
+    bool have = false;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaStream_t cap = nullptr;
+};
+LoopGraph g_loop;
+
+uint64_t fnv(uint64_t h, const void *p, size_t n) {
+    const unsigned char *c = static_cast<const unsigned char *>(p);
+    for (size_t i = 0; i < n; ++i) h = (h ^ c[i]) * 1099511628211ull;
+    return h;
+}
+
+}  // namespace
+}  // namespace df
+
+extern "C" {
+
+size_t df_generate_workspace_bytes(const df_dflash_config *cfg, int B, int K, int n_new_max) {
+    if (check_cfg(cfg) != DF_OK || B <= 0 || K < 1 || n_new_max < K + 1) return 0;
+    const size_t fwd = df_dflash_workspace_bytes(cfg, B, K + 1, n_new_max);
+    return fwd ? fwd + loop_extra_bytes(cfg, B, K, n_new_max) : 0;
+}
+
+int df_generate(const df_dflash_config *cfg, const df_dflash_weights *w, const df_kv_cache *cache,
+                const df_synthetic_verifier *v, float *prior_cap, int32_t *prior_len,
+                int32_t *out_tokens, int32_t *out_len, const int32_t *prompt_len,
+                int max_new_tokens, int max_rounds, int B, int K, int n_new_max,
+                const int32_t *eos, int n_eos, int32_t *rounds, int32_t *accept_hist, void *ws,
+                size_t ws_bytes, int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_cfg(cfg));
+    DF_TRY(check_weights(cfg, w));
+    REQ(B > 0 && B <= 1024 && K >= 1, DF_ESHAPE, "B=%d K=%d (B <= 1024, K >= 1)", B, K);
+    REQ(n_new_max >= K + 1 && cache && n_new_max <= cache->cap, DF_ESHAPE,
+        "n_new_max=%d (K+1 <= n_new_max <= cache cap)", n_new_max);
+    DF_TRY(check_cache(cache, cfg->n_layers, B, cfg->head_dim));
+    REQ(v && v->ref && v->table && v->max_len > K + 2, DF_EINVAL, "synthetic verifier");
+    REQ(v->n_comb >= 1 && cfg->n_target_layers <= kLoopMaxTargetLayers, DF_ESHAPE,
+        "n_comb=%d, n_target_layers=%d (<= %d)", v->n_comb, cfg->n_target_layers,
+        kLoopMaxTargetLayers);
+    for (int l = 0; l < cfg->n_target_layers; ++l)
+        REQ(v->sel[l] >= 0 && v->sel[l] < v->n_comb, DF_ESHAPE, "sel[%d]=%d outside the %d captured layers",
+            l, v->sel[l], v->n_comb);
+    REQ(prior_cap && prior_len && out_tokens && out_len && prompt_len && rounds, DF_EINVAL,
+        "NULL loop state");
+    REQ(max_rounds >= 0 && max_new_tokens >= 0, DF_ESHAPE, "max_rounds / max_new_tokens");
+    REQ(n_eos >= 0 && (n_eos == 0 || eos), DF_EINVAL, "eos list");
+    DF_TRY(get_ws(ws, ws_bytes, df_generate_workspace_bytes(cfg, B, K, n_new_max)));
+    const int blk = K + 1;
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    DFlashWs W;
+    carve_dflash(cv, W, cfg, B, blk, n_new_max, cache->cap, true);
+    float *th = cv.take<float>((size_t)B * n_new_max * cfg->n_target_layers * cfg->hidden);
+    int32_t *ints = cv.take<int32_t>((size_t)B * (4 * blk + 8) + 8);
+    REQ(cv.ok, DF_EWORKSPACE, "workspace too small");
+    LoopArgs a;
+    memset(static_cast<void *>(&a), 0, sizeof(a));   // padding too: the bytes key the graph cache
+    a.th = th;
+    a.ref = v->ref;
+    a.agree = v->agree;
+    a.table = v->table;
+    a.n_comb = v->n_comb;
+    for (int l = 0; l < cfg->n_target_layers; ++l) a.sel[l] = v->sel[l];
+    a.max_len = v->max_len;
+    a.prior_cap = prior_cap;
+    a.prior_len = prior_len;
+    a.out = out_tokens;
+    a.out_len = out_len;
+    a.prompt_len = prompt_len;
+    a.rounds = rounds;
+    a.accept_hist = accept_hist;
+    a.max_rounds = max_rounds;
+    a.max_new = max_new_tokens;
+    a.cache_seq = cache->seq_len;
+    a.B = B;
+    a.K = K;
+    a.H = cfg->hidden;
+    a.n_tl = cfg->n_target_layers;
+    a.n_new_max = n_new_max;
+    a.argmax = ints;
+    a.target = ints + (size_t)B * blk;
+    a.committed = ints + (size_t)2 * B * blk;
+    a.n_new = ints + (size_t)3 * B * blk;
+    a.last_token = a.n_new + B;
+    a.n_committed = a.last_token + B;
+    a.accept = a.n_committed + B;
+    a.hit = a.accept + B;
+    a.rollback = a.hit + B;
+    a.done = a.rollback + B;
+    a.round_ctr = a.done + B;
+    a.eos = eos;
+    a.n_eos = n_eos;
+    a.status = d_status;
+
+    // the cache key: every argument the graph bakes in
+    uint64_t key = 1469598103934665603ull;
+    key = fnv(key, cfg, sizeof(*cfg));
+    key = fnv(key, w, sizeof(*w));
+    key = fnv(key, w->layers, sizeof(df_layer_weights) * cfg->n_layers);
+    key = fnv(key, cache, sizeof(*cache));
+    key = fnv(key, cache->k, sizeof(float *) * cfg->n_layers);
+    key = fnv(key, cache->v, sizeof(float *) * cfg->n_layers);
+    key = fnv(key, &a, sizeof(a));
+    key = fnv(key, &ws, sizeof(ws));
+    key = fnv(key, &stream, sizeof(stream));
+    cudaStream_t user = (cudaStream_t)stream;
+    std::lock_guard<std::mutex> lk(g_loop.mu);
+    if (!(g_loop.have && g_loop.key == key)) {
+        if (g_loop.have) {
+            cudaGraphExecDestroy(g_loop.exec);
+            cudaGraphDestroy(g_loop.graph);
+            g_loop.have = false;
+        }
+        if (!g_loop.cap) {
+            cudaError_t e = cudaStreamCreateWithFlags(&g_loop.cap, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return fail(DF_ECUDA, "loop capture stream: %s", cudaGetErrorString(e));
+        }
+        cudaStream_t cs = g_loop.cap;
+        cudaGraph_t g = nullptr;
+        cudaError_t e = cudaGraphCreate(&g, 0);
+        cudaGraphConditionalHandle h = 0;
+        if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&h, g, 1, cudaGraphCondAssignDefault);
+        a.cond = h;
+        // the init kernel, then a while node whose body is one round
+        if (e == cudaSuccess)
+            e = cudaStreamBeginCaptureToGraph(cs, g, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) {
+            if (g) cudaGraphDestroy(g);
+            return fail(DF_ECUDA, "loop graph set-up: %s", cudaGetErrorString(e));
+        }
+        int rc = launch_loop_init(a, cs);
+        cudaGraph_t got = nullptr;
+        e = cudaStreamEndCapture(cs, &got);
+        if (rc != DF_OK || e != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return rc != DF_OK ? rc : fail(DF_ECUDA, "loop init capture: %s", cudaGetErrorString(e));
+        }
+        cudaGraphNode_t init_node = nullptr;
+        size_t n_nodes = 1;
+        e = cudaGraphGetNodes(g, &init_node, &n_nodes);
+        cudaGraphNodeParams cp = {};
+        cp.type = cudaGraphNodeTypeConditional;
+        cp.conditional.handle = h;
+        cp.conditional.type = cudaGraphCondTypeWhile;
+        cp.conditional.size = 1;
+        cudaGraphNode_t cnode = nullptr;
+        if (e == cudaSuccess) e = cudaGraphAddNode(&cnode, g, &init_node, nullptr, 1, &cp);
+        cudaGraph_t body = e == cudaSuccess ? cp.conditional.phGraph_out[0] : nullptr;
+        if (e == cudaSuccess)
+            e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return fail(DF_ECUDA, "loop while node: %s", cudaGetErrorString(e));
+        }
+        rc = launch_loop_prepare(a, cs);
+        if (rc == DF_OK)
+            rc = dflash_forward_impl(cfg, w, cache, nullptr, a.last_token, a.th, a.n_new, n_new_max,
+                                     B, blk, W.h_final, W.xp_head, W, d_status, cs);
+        if (rc == DF_OK)
+            rc = lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
+                              a.argmax, nullptr, nullptr, W.tc, cs);
+        if (rc == DF_OK) rc = launch_loop_verify(a, cs);
+        if (rc == DF_OK)
+            rc = launch_accept(a.argmax + 1, blk, a.target, B, K, eos, n_eos, a.committed,
+                               a.n_committed, a.accept, a.hit, a.rollback, nullptr, d_status, cs);
+        if (rc == DF_OK) rc = launch_loop_append(a, cs);
+        if (rc == DF_OK) rc = launch_loop_commit(a, cs);
+        e = cudaStreamEndCapture(cs, &body);
+        if (rc != DF_OK || e != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return rc != DF_OK ? rc : fail(DF_ECUDA, "loop body capture: %s", cudaGetErrorString(e));
+        }
+        cudaGraphExec_t ex = nullptr;
+        e = cudaGraphInstantiate(&ex, g, 0);
+        if (e != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return fail(DF_ECUDA, "loop graph instantiate: %s", cudaGetErrorString(e));
+        }
+        g_loop.graph = g;
+        g_loop.exec = ex;
+        g_loop.key = key;
+        g_loop.have = true;
+    }
+    cudaError_t e = cudaGraphLaunch(g_loop.exec, user);
+    if (e != cudaSuccess) return fail(DF_ECUDA, "loop graph launch: %s", cudaGetErrorString(e));
+    return DF_OK;
+}
+
+}  // extern "C"
+
 // ================================================================ MTP draft step
 namespace df {
 namespace {

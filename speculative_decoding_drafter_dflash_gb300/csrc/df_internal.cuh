@@ -373,6 +373,40 @@ struct SampleArgs {
 int sample_chunks(int V);
 int launch_accept_stochastic(const SampleArgs &a, cudaStream_t s);
 
+// Multi-round generate loop around the draft round (k_loop.cu).
+constexpr int kLoopMaxTargetLayers = 16;
+struct LoopArgs {
+    // synthetic verifier
+    const int32_t *ref = nullptr;        // [B, max_len]
+    const uint8_t *agree = nullptr;      // [B, max_len] or null
+    const float *table = nullptr;        // [B, n_comb, max_len, H]
+    int n_comb = 0;
+    int sel[kLoopMaxTargetLayers] = {};  // drafter target layer l = captured layer sel[l]
+    int max_len = 0;
+    // caller state
+    float *prior_cap = nullptr;          // [B, n_comb, max_len, H]
+    int32_t *prior_len = nullptr, *out = nullptr, *out_len = nullptr;
+    const int32_t *prompt_len = nullptr;
+    int32_t *rounds = nullptr, *accept_hist = nullptr;
+    int max_rounds = 0, max_new = 0;
+    int32_t *cache_seq = nullptr;        // drafter cache lengths
+    int B = 0, K = 0, H = 0, n_tl = 0, n_new_max = 0;
+    // round scratch
+    float *th = nullptr;                 // [B, n_new_max, n_tl * H]
+    int32_t *n_new = nullptr, *last_token = nullptr, *argmax = nullptr, *target = nullptr;
+    int32_t *committed = nullptr, *n_committed = nullptr, *accept = nullptr, *hit = nullptr;
+    int32_t *rollback = nullptr, *done = nullptr, *round_ctr = nullptr;
+    const int32_t *eos = nullptr;
+    int n_eos = 0;
+    cudaGraphConditionalHandle cond = 0;
+    int32_t *status = nullptr;
+};
+int launch_loop_init(const LoopArgs &a, cudaStream_t s);
+int launch_loop_prepare(const LoopArgs &a, cudaStream_t s);
+int launch_loop_verify(const LoopArgs &a, cudaStream_t s);
+int launch_loop_append(const LoopArgs &a, cudaStream_t s);
+int launch_loop_commit(const LoopArgs &a, cudaStream_t s);
+
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
                        int32_t *status, cudaStream_t s);
 int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
