@@ -338,7 +338,6 @@ void attn_plan(AttnArgs &a, int max_keys);
 size_t attn_part_floats(const AttnArgs &a);
 int launch_attn(const AttnArgs &a, cudaStream_t s);
 bool attn_tc_supported(int d, int rows);
-int attn_tc_max_keys(int d, int rows);
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
 
 // Non-greedy accept step (speculative sampling) over B sequences of K drafts and vocab V.

@@ -595,24 +595,19 @@ size_t attn_part_floats(const AttnArgs &a) {
 
 // Keys per chunk: a whole number of tiles, about one CTA per SM (two waves when sequences x
 // KV heads alone nearly fill the GPU). Head dims 128 and 256 with up to 32 query rows per KV
-// head run on the tensor cores when a chunk fits the tensor-core kernel's score memory;
-// everything else runs on the CUDA cores.
+// head run on the tensor cores (128-key tiles); everything else runs on the CUDA cores.
 void attn_plan(AttnArgs &a, int max_keys) {
     const int R = a.blk * (a.nq / a.nkv);
     const int heads = a.B * a.nkv;
     const int waves = heads > 38 ? 2 : 1;
     const int want = std::max(1, (waves * kNumSMs + heads - 1) / heads);
-    for (int tc = attn_tc_supported(a.d, R) ? 1 : 0; tc >= 0; --tc) {
-        const int TK = tc ? 128 : kTileBytes / (2 * a.d * 4);
-        const int tiles = std::max(1, (max_keys + TK - 1) / TK);
-        const int n = std::min(want, tiles);
-        const int per = (tiles + n - 1) / n;
-        if (tc && per * TK > attn_tc_max_keys(a.d, R)) continue;
-        a.tc = tc;
-        a.chunk = per * TK;
-        a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
-        return;
-    }
+    a.tc = attn_tc_supported(a.d, R) ? 1 : 0;
+    const int TK = a.tc ? 128 : kTileBytes / (2 * a.d * 4);
+    const int tiles = std::max(1, (max_keys + TK - 1) / TK);
+    const int n = std::min(want, tiles);
+    const int per = (tiles + n - 1) / n;
+    a.chunk = per * TK;
+    a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
 }
 
 template <int D, int RPL>

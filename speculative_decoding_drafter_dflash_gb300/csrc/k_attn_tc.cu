@@ -15,12 +15,13 @@
 // accumulation in TMEM):
 //   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (one TMEM block per tile)
 //   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (per 128-dim half)
-// The whole chunk's scores stay in TMEM (at most (512 - halves*NP)/NP tiles), so the softmax
-// maximum is exact per chunk and no running rescale is needed: pass 1 takes the row maxima,
-// pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory) right before its
-// P.V MMAs. Values are transposed while they are split, so both products read K-major operands.
+// A chunk's scores stay in TMEM, up to (512 - halves*NP)/NP tiles per pass, so the softmax
+// maximum is exact per pass: pass 1 takes the row maxima, pass 2 turns each tile into
+// probabilities (BF16 hi/lo in shared memory) right before its P.V MMAs. A longer chunk runs in
+// several passes whose (max, sum, o) are merged in registers, rescaled once per pass. Values are
+// transposed while they are split, so both products read K-major operands.
 //
-// 256 threads: every warp converts; thread 0 issues the TMA loads and the MMAs and refills a
+// 288 threads: warps 0-7 convert; warp 8 issues the TMA loads and the MMAs and refills a
 // buffer once the MMAs reading it are done; warps w and w + 4 share TMEM lane quarter w % 4 and
 // split the rows in the softmax and the read-out. Block rows (keys past the cache rows) come from
 // kb/vb with plain loads during the split; keys past the chunk are written as zeros.
@@ -43,7 +44,7 @@ constexpr int kAtomBytes = 128 * 128;         // one 64-element-wide column bloc
 
 template <int D, int NP, int NBUF>
 constexpr bool attn_tc_smem_bound() {
-    return 1024 + NBUF * 2 * kOpBytes + (D / 128) * 2 * NP * 256 + 2 * NP * 256 + 8 * NP * 4 +
+    return 1024 + NBUF * 2 * kOpBytes + (D / 128) * 2 * NP * 256 + 2 * NP * 256 + 9 * NP * 4 +
                3 * NBUF * 8 + 16 <= 232448;
 }
 
@@ -112,7 +113,8 @@ struct AttnTcParams {
     AttnArgs a;
 };
 
-template <int D, int NP, int NBUF>
+// MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
+template <int D, int NP, int NBUF, bool MP>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
     constexpr int NH = D / 128;               // 128-wide halves of the head dimension
     constexpr int NPH = NP / 2;               // rows per thread in the softmax and read-out
@@ -125,7 +127,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint8_t *qsm = sm + NBUF * 2 * kOpBytes;            // [NH][hi, lo] Q operands
     uint8_t *psm = qsm + NH * 2 * kQBytes;              // [hi, lo] P operand (second buffer)
     float *red = reinterpret_cast<float *>(psm + 2 * kQBytes);   // [4][NP] maxima, [4][NP] sums
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + 8 * NP); // [NBUF] staging landed
+    float *mrun = red + 8 * NP;                                  // [NP] running row maxima
+    uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NBUF] staging landed
     uint64_t *mdone = full + NBUF;                               // [NBUF] MMAs of the unit done
     uint64_t *conv = mdone + NBUF;                               // [NBUF] unit split, ready for MMA
     uint32_t *tslot = reinterpret_cast<uint32_t *>(conv + NBUF);
@@ -149,18 +152,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int n_tiles = (c1 - c0 + kTcKeys - 1) / kTcKeys;
     const size_t head_off = (size_t)b * a.nkv + g;
     float *part = a.part + ((head_off * a.n_chunks + chunk) * (size_t)R) * (D + 2);
-    if (n_tiles == 0 || n_tiles * NP + NH * NP > kTmemCols) {
-        if (n_tiles != 0 && tid == 0) set_status(a.status, DF_ESHAPE);
+    if (n_tiles == 0) {
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
         return;
     }
-    const int nK = n_tiles * NH, nU = 2 * nK;
+    // A chunk longer than the score memory runs in passes of at most max_tp tiles; each pass
+    // has an exact maximum and its output is merged into running (max, sum, o) registers.
+    const int max_tp = (kTmemCols - NH * NP) / NP;
+    const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
+    if (!MP && n_tiles > max_tp) {           // the host plans single-pass launches within bounds
+        if (tid == 0) set_status(a.status, DF_ESHAPE);
+        for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
+        return;
+    }
+    const int tpp = (n_tiles + n_pass - 1) / n_pass;    // tiles per pass (the last may be short)
+    const int upp = 2 * tpp * NH;                        // units per full pass
+    const int nU = 2 * n_tiles * NH;
+    const bool multi = MP && n_pass > 1;
     const uint64_t pol = policy_evict_first();
-    // Unit u: K (u < nK) or V of tile t, 128-wide half h, staged by one TMA box of 128 rows.
+    // Unit u of pass p: the pass's K units (tile-major, then 128-wide half), then its V units.
+    struct UnitInfo {
+        int t0, nt, v, t, h;
+    };
+    auto decode = [&](int u) -> UnitInfo {
+        const int p = min(u / upp, n_pass - 1);
+        UnitInfo x;
+        x.t0 = p * tpp;
+        x.nt = min(n_tiles, x.t0 + tpp) - x.t0;
+        int local = u - p * upp;
+        x.v = local >= x.nt * NH;
+        if (x.v) local -= x.nt * NH;
+        x.t = x.t0 + local / NH;
+        x.h = local % NH;
+        return x;
+    };
+    // Unit u: K or V of tile t, 128-wide half h, staged by one TMA box of 128 rows.
     auto issue = [&](int u) {
-        const bool isV = u >= nK;
-        const int j = isV ? u - nK : u;
-        const int t = j / NH, h = j % NH, bf = u % NBUF;
+        const UnitInfo x = decode(u);
+        const bool isV = x.v;
+        const int t = x.t, h = x.h, bf = u % NBUF;
         mbar_expect_tx(&full[bf], (uint32_t)(2 * kOpBytes));
         tma_load_2d(kvb + (size_t)bf * 2 * kOpBytes, isV ? &P.vmap : &P.kmap, &full[bf], h * 128,
                     (int)(head_off * a.cap) + c0 + t * kTcKeys, pol);
@@ -216,19 +246,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int ocol = n_tiles * NP;            // O^T accumulators after the score tiles
-    // P operand of tile t: two buffers in turn. Buffer 0 reuses the Q operands' space (every
-    // score MMA has completed before the first P is written), buffer 1 follows it.
-    auto p_buf = [&](int t) -> uint32_t { return smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes); };
+    const int ocol = tpp * NP;                // O^T accumulators after a pass's score tiles
+    // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
+    // (every score MMA has completed before the first P is written), buffer 1 following it.
+    // Several passes: Q stays live, so one buffer after the Q operands.
+    auto p_buf = [&](int t) -> uint32_t {
+        return multi ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
+    };
 
     // In-place conversion of a staged unit: every thread reads its 64 F32 values (block rows
     // from kb/vb, zeros past the chunk's last key), the CTA synchronises, then the values go back
     // as BF16 hi (first 32 KB) and lo (second 32 KB) in the swizzled K-major operand layout.
     float xv[64];
     auto read_unit = [&](int u) {
-        const bool isV = u >= nK;
-        const int j = isV ? u - nK : u;
-        const int t = j / NH, h = j % NH;
+        const UnitInfo x = decode(u);
+        const bool isV = x.v;
+        const int t = x.t, h = x.h;
         const float *st = reinterpret_cast<const float *>(kvb + (size_t)(u % NBUF) * 2 * kOpBytes);
         const float *blkp = isV ? a.vb : a.kb;
         const int kbase = c0 + t * kTcKeys;
@@ -264,7 +297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     };
     auto write_unit = [&](int u) {
         const uint32_t hi = smem_u32(kvb + (size_t)(u % NBUF) * 2 * kOpBytes), lo = hi + kOpBytes;
-        if (u < nK) {
+        if (!decode(u).v) {
 #pragma unroll
             for (int it = 0; it < 16; ++it) {
                 const int kr = it * 8 + warp;
@@ -327,8 +360,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         return !(a.causal_block && key >= S_cache && key - S_cache > row / rep);
     };
     float Mrow[NPH], lsum[NPH];
+    float lrun[MP ? NPH : 1], orun[MP ? NH : 1][MP ? NPH : 1];
 #pragma unroll
     for (int r = 0; r < NPH; ++r) lsum[r] = 0.f;
+    if constexpr (MP) {
+#pragma unroll
+        for (int r = 0; r < NPH; ++r) {
+            lrun[r] = 0.f;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) orun[h][r] = 0.f;
+        }
+    }
+    if (tid < NP) mrun[tid] = -INFINITY;
 
     if (warp == kConvThreads / 32) {
         // TMA / MMA issuer: MMAs of unit u once its split has landed; then refill its buffer.
@@ -338,14 +381,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 if (!mbar_wait(&conv[u % NBUF], ph, abort_flag, a.status)) break;
                 tc_fence_after();
                 const uint32_t ahi = smem_u32(kvb + (size_t)(u % NBUF) * 2 * kOpBytes), alo = ahi + kOpBytes;
-                if (u < nK) {
-                    const int t = u / NH, h = u % NH;
-                    const uint32_t qhi = smem_u32(qsm + (2 * h) * kQBytes), qlo = qhi + kQBytes;
-                    mma3(tmem + t * NP, ahi, alo, qhi, qlo, h > 0);
+                const UnitInfo x = decode(u);
+                if (!x.v) {
+                    const uint32_t qhi = smem_u32(qsm + (2 * x.h) * kQBytes), qlo = qhi + kQBytes;
+                    mma3(tmem + (x.t - x.t0) * NP, ahi, alo, qhi, qlo, x.h > 0);
                 } else {
-                    const int t = (u - nK) / NH, h = (u - nK) % NH;
-                    const uint32_t phi = p_buf(t), plo = phi + kQBytes;
-                    mma3(tmem + ocol + h * NP, ahi, alo, phi, plo, t > 0);
+                    const uint32_t phi = p_buf(x.t), plo = phi + kQBytes;
+                    mma3(tmem + ocol + x.h * NP, ahi, alo, phi, plo, x.t > x.t0);
                 }
                 mma_commit(&mdone[u % NBUF]);
                 if (u + NBUF < nU) {
@@ -357,18 +399,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         __syncwarp();
     } else {
         for (int u = 0; u < nU; ++u) {
-            if (u >= nK && (u - nK) % NH == 0) {
-                const int t = (u - nK) / NH;
-                if (t == 0) {
-                    // softmax pass 1: exact row maxima over the chunk
-                    wait_mma(nK - 1);
+            const UnitInfo x = decode(u);
+            if (x.v && x.h == 0) {
+                const int t = x.t, tl = t - x.t0;
+                if (tl == 0) {
+                    // softmax pass 1: exact row maxima over the pass's tiles
+                    wait_mma((u / upp) * upp + x.nt * NH - 1);
                     float mx[NPH];
 #pragma unroll
                     for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
-                    for (int tt = 0; tt < n_tiles; ++tt) {
+                    for (int tt = 0; tt < x.nt; ++tt) {
                         float s[NPH];
                         tmem_rows<NPH>(tmem + lane_addr + tt * NP + r0, s);
-                        const int key = c0 + tt * kTcKeys + lq * 32 + lane;
+                        const int key = c0 + (x.t0 + tt) * kTcKeys + lq * 32 + lane;
 #pragma unroll
                         for (int r = 0; r < NPH; ++r)
                             if (row_ok(key, r0 + r)) mx[r] = fmaxf(mx[r], s[r] * scale);
@@ -383,7 +426,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     for (int r = 0; r < NPH; ++r)
                         Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                         fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
-                } else if (t >= 2) {
+                } else if (multi) {
+                    wait_mma(u - 1);   // one P buffer: the previous tile's P.V MMAs are done
+                } else if (tl >= 2) {
                     // P operands alternate between two buffers: the one for tile t was last read by
                     // the P.V MMAs of tile t - 2. Waiting on that older unit is only safe while
                     // its barrier cannot have completed a later phase (NBUF > NH); otherwise wait
@@ -392,7 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 // pass 2 for tile t: probabilities -> BF16 hi/lo P operand
                 float s[NPH];
-                tmem_rows<NPH>(tmem + lane_addr + t * NP + r0, s);
+                tmem_rows<NPH>(tmem + lane_addr + tl * NP + r0, s);
                 const int kt = lq * 32 + lane;
                 const int key = c0 + t * kTcKeys + kt;
                 const uint32_t phi = p_buf(t), plo = phi + kQBytes;
@@ -417,27 +462,73 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv[u % NBUF]);
+            if constexpr (MP) {
+                if (x.v && x.t == x.t0 + x.nt - 1 && x.h == NH - 1) {
+                    // end of a pass: merge its (max, sum, o) into the running values
+                    wait_mma(u);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        float o[NPH];
+                        tmem_rows<NPH>(tmem + lane_addr + ocol + h * NP + r0, o);
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r) {
+                            const float Mr = mrun[r0 + r], Mn = fmaxf(Mr, Mrow[r]);
+                            if (Mn == -INFINITY) continue;
+                            const float so = Mr == -INFINITY ? 0.f : ex2(Mr - Mn);
+                            const float sn = Mrow[r] == -INFINITY ? 0.f : ex2(Mrow[r] - Mn);
+                            orun[h][r] = orun[h][r] * so + o[r] * sn;
+                            if (h == NH - 1) {
+                                lrun[r] = lrun[r] * so + lsum[r] * sn;
+                                lsum[r] = 0.f;
+                            }
+                        }
+                    }
+                    conv_sync();                // everyone has read mrun before it moves
+                    if (lq == 0 && lane == 0)
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r) mrun[r0 + r] = fmaxf(mrun[r0 + r], Mrow[r]);
+                    conv_sync();
+                }
+            }
         }
-        wait_mma(nU - 1);
 
-        // read-out: O^T columns of this thread's rows, row sums, maxima
+        // read-out: o of this thread's rows, row sums, maxima
+        if constexpr (MP) {
 #pragma unroll
-        for (int r = 0; r < NPH; ++r) {
-            const float l = warp_sum(lsum[r]);
-            if (lane == 0) red[4 * NP + lq * NP + r0 + r] = l;
-        }
+            for (int r = 0; r < NPH; ++r) {
+                const float l = warp_sum(lrun[r]);
+                if (lane == 0) red[4 * NP + lq * NP + r0 + r] = l;
+            }
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-            float o[NPH];
-            tmem_rows<NPH>(tmem + lane_addr + ocol + h * NP + r0, o);
-            const int d = h * 128 + lq * 32 + lane;
+            for (int h = 0; h < NH; ++h) {
+                const int d = h * 128 + lq * 32 + lane;
 #pragma unroll
-            for (int r = 0; r < NPH; ++r)
-                if (r0 + r < R) part[(size_t)(r0 + r) * (D + 2) + d] = o[r];
+                for (int r = 0; r < NPH; ++r)
+                    if (r0 + r < R) part[(size_t)(r0 + r) * (D + 2) + d] = orun[h][r];
+            }
+        } else {
+            wait_mma(nU - 1);
+#pragma unroll
+            for (int r = 0; r < NPH; ++r) {
+                const float l = warp_sum(lsum[r]);
+                if (lane == 0) red[4 * NP + lq * NP + r0 + r] = l;
+            }
+            if (lq == 0 && lane == 0)
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) mrun[r0 + r] = Mrow[r];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                float o[NPH];
+                tmem_rows<NPH>(tmem + lane_addr + ocol + h * NP + r0, o);
+                const int d = h * 128 + lq * 32 + lane;
+#pragma unroll
+                for (int r = 0; r < NPH; ++r)
+                    if (r0 + r < R) part[(size_t)(r0 + r) * (D + 2) + d] = o[r];
+            }
         }
         conv_sync();
         if (tid < R) {
-            const float M = fmaxf(fmaxf(red[tid], red[NP + tid]), fmaxf(red[2 * NP + tid], red[3 * NP + tid]));
+            const float M = mrun[tid];
             const float L = red[4 * NP + tid] + red[5 * NP + tid] + red[6 * NP + tid] + red[7 * NP + tid];
             part[(size_t)tid * (D + 2) + D] = M;
             part[(size_t)tid * (D + 2) + D + 1] = L;
@@ -454,11 +545,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 template <int D, int NP, int NBUF>
 size_t attn_tc_smem() {
     return 1024 + NBUF * 2 * (size_t)kOpBytes + (D / 128) * 2 * (size_t)NP * 256 +
-           2 * (size_t)NP * 256 + 8 * NP * sizeof(float) + 3 * NBUF * sizeof(uint64_t) + 16;
+           2 * (size_t)NP * 256 + 9 * NP * sizeof(float) + 3 * NBUF * sizeof(uint64_t) + 16;
 }
 
 template <int D, int NP, int NBUF>
 int launch_tc(const AttnArgs &a, cudaStream_t s) {
+    constexpr int max_keys_one_pass = (kTmemCols - (D / 128) * NP) / NP * kTcKeys;
     static_assert(attn_tc_smem_bound<D, NP, NBUF>(), "shared memory");
     AttnTcParams p;
     memset(&p, 0, sizeof(p));
@@ -472,7 +564,10 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
                        128, CU_TENSOR_MAP_SWIZZLE_NONE));
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF>, grid, dim3(kTcThreads),
+    if (a.chunk <= max_keys_one_pass)
+        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false>, grid,
+                        dim3(kTcThreads), attn_tc_smem<D, NP, NBUF>(), s, p);
+    return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true>, grid, dim3(kTcThreads),
                     attn_tc_smem<D, NP, NBUF>(), s, p);
 }
 
@@ -480,14 +575,9 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
 
 bool attn_tc_supported(int d, int rows) { return (d == 128 || d == 256) && rows >= 1 && rows <= 32; }
 
-int attn_tc_max_keys(int d, int rows) {
-    const int NP = rows <= 16 ? 16 : 32;
-    return (kTmemCols - (d / 128) * NP) / NP * kTcKeys;
-}
-
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     const int R = a.blk * (a.nq / a.nkv);
-    if (!attn_tc_supported(a.d, R) || a.chunk % kTcKeys != 0 || a.chunk > attn_tc_max_keys(a.d, R))
+    if (!attn_tc_supported(a.d, R) || a.chunk % kTcKeys != 0)
         return fail(DF_ESHAPE, "tensor-core attention: d=%d rows=%d chunk=%d", a.d, R, a.chunk);
     if (a.d == 128) return R <= 16 ? launch_tc<128, 16, 3>(a, s) : launch_tc<128, 32, 3>(a, s);
     return R <= 16 ? launch_tc<256, 16, 3>(a, s) : launch_tc<256, 32, 2>(a, s);

@@ -124,5 +124,12 @@ def test_attention_matches_oracle(Bn, blk, nq, nkv, d, seq, cap, block_keys, cau
     assert kernel in names
 
 
+def test_attention_long_chunks_run_in_passes():
+    """64 KV heads leave 5 chunks per head; 12000 keys then give 19-tile chunks, above the
+    15 tiles of scores TMEM holds at 32 query rows: two passes merged in registers."""
+    names = _attention_case(2, 16, 64, 32, 128, [12000, 9000], 12100, True, False, seed=77)
+    assert "attn_tc_kernel" in names
+
+
 def test_attention_no_visible_keys_gives_zeros():
     _attention_case(1, 2, 4, 2, 128, [0], 64, False, False, seed=1)
