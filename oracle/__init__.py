@@ -13,6 +13,8 @@ package never imports the CUDA library: they share no code.
 
 Pin status (what each function is checked against, in tests/test_oracle_*.py):
   decode_bf16            canonical round trip, odd length, misread signature, all 65536 patterns
+  round_bf16             hand ties to even, every finite BF16 value kept, integer rounding rule
+  BF16 KV cache          appended rows equal the F32 path's rows rounded to BF16
   rmsnorm / head_rmsnorm closed forms (constant vector, hand example), scale invariance, unit RMS
   rope                   hand example, norm preservation, R(p)R(q)=R(p+q), relative-position property
   sdpa                   brute-force float64 loops, one key, equal keys, GQA == MHA with repeated heads

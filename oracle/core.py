@@ -28,6 +28,18 @@ def decode_bf16(bits, dt=np.float32):
     return f.astype(dt, copy=False)
 
 
+def round_bf16(x, dt=np.float32):
+    """Round to the nearest BF16 value, ties to an even last mantissa bit (the value a BF16
+    store keeps), returned as floats. Finite inputs: the F32 word's low 16 bits decide
+    against the halfway point 0x8000, with the stored half's lowest bit breaking ties."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    low = u & np.uint64(0xFFFF)
+    high = u >> np.uint64(16)
+    up = (low > np.uint64(0x8000)) | ((low == np.uint64(0x8000)) & ((high & np.uint64(1)) == 1))
+    high = high + up.astype(np.uint64)
+    return decode_bf16(high.astype(np.uint16), dt)
+
+
 def decode_bf16_bytes(data: bytes, dt=np.float32):
     """Little-endian BF16 bytes -> floats; an odd byte count is rejected.
 

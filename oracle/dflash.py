@@ -31,7 +31,7 @@ from __future__ import annotations
 import numpy as np
 
 from .core import (OracleError, accept_walk, decode_bf16, head_rmsnorm, kv_rollback, linear,
-                   lm_head_argmax, rmsnorm, rope, sdpa, swiglu)
+                   lm_head_argmax, rmsnorm, rope, round_bf16, sdpa, swiglu)
 
 
 def fc_hidden_norm(cfg, w, x_new, dt=np.float32):
@@ -44,12 +44,16 @@ def fc_hidden_norm(cfg, w, x_new, dt=np.float32):
 
 
 def dflash_layer(cfg, lw, h, h_ctx, k_cache, v_cache, ctx0, dt=np.float32):
-    """One drafter decoder layer for one sequence.
+    """One drafter decoder layer for one sequence; `cfg.kv_bf16` (optional, default off)
+    selects a BF16 KV cache: every K/V value the attention reads, cached or of the block, is
+    rounded to BF16 when it is produced (the verifier of qwen35_orchestrator.rs's "Output
+    divergence" note runs its attention in BF16).
 
     h[blk, H] block residual stream; h_ctx[n_new, H] normed context rows; k_cache,
     v_cache [n_kv, cap, d] of this layer (modified in place: rows ctx0..ctx0+n_new
     receive the context K/V). Returns the new residual stream.
     """
+    bf16_kv = bool(getattr(cfg, "kv_bf16", False))
     H, nq, nkv, d = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     eps, theta, rot = cfg.rms_eps, cfg.rope_theta, cfg.rot
     blk = h.shape[0]
@@ -63,6 +67,8 @@ def dflash_layer(cfg, lw, h, h_ctx, k_cache, v_cache, ctx0, dt=np.float32):
         vc = linear(h_ctx, lw["wv"], dt)
         pos_c = np.arange(ctx0, ctx0 + n_new)
         kc = rope(kc.reshape(n_new, nkv, d), pos_c, rot, theta, dt)
+        if bf16_kv:                         # a BF16 KV cache keeps the rounded values
+            kc, vc = round_bf16(kc, dt), round_bf16(vc, dt)
         k_cache[:, ctx0:ctx0 + n_new, :] = kc.transpose(1, 0, 2)
         v_cache[:, ctx0:ctx0 + n_new, :] = vc.reshape(n_new, nkv, d).transpose(1, 0, 2)
     ctx_len = ctx0 + n_new
@@ -74,6 +80,8 @@ def dflash_layer(cfg, lw, h, h_ctx, k_cache, v_cache, ctx0, dt=np.float32):
     pos_b = np.arange(ctx_len, ctx_len + blk)
     q = rope(q.reshape(blk, nq, d), pos_b, rot, theta, dt)
     kb = rope(kb.reshape(blk, nkv, d), pos_b, rot, theta, dt)
+    if bf16_kv:                             # block K/V at the precision of the cache
+        kb, vb = round_bf16(kb, dt), round_bf16(vb, dt)
     keys = np.concatenate([np.asarray(k_cache[:, :ctx_len, :], dt).transpose(1, 0, 2), kb], 0)
     vals = np.concatenate([np.asarray(v_cache[:, :ctx_len, :], dt).transpose(1, 0, 2),
                            vb.reshape(blk, nkv, d)], 0)

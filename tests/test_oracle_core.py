@@ -306,3 +306,23 @@ def test_kv_rollback_golden(case):
             core.kv_rollback(case["seq_len"], case["n"])
     else:
         assert core.kv_rollback(case["seq_len"], case["n"]) == case["after"]
+
+
+def test_round_bf16_hand_values_and_ties_to_even():
+    one = 1.0
+    assert core.round_bf16([one + 2.0 ** -8])[0] == one                  # halfway, even stays
+    assert core.round_bf16([one + 3 * 2.0 ** -8])[0] == one + 2.0 ** -6   # halfway, odd rounds up
+    assert core.round_bf16([one + 2.0 ** -8 + 2.0 ** -20])[0] == one + 2.0 ** -7
+    assert core.round_bf16([-(one + 3 * 2.0 ** -8)])[0] == -(one + 2.0 ** -6)
+    assert core.round_bf16([0.0, -0.0, 3.0])[0] == 0.0
+
+
+def test_round_bf16_keeps_every_finite_bf16_value_and_matches_integer_rounding():
+    from tests.oracle_fixtures import bf16_bits_rne
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = core.decode_bf16(bits)
+    finite = np.isfinite(vals)
+    assert np.array_equal(core.round_bf16(vals[finite]).view(np.uint32),
+                          vals[finite].view(np.uint32))
+    x = np.random.default_rng(0).standard_normal(100000).astype(np.float32) * 100
+    assert np.array_equal(core.round_bf16(x), core.decode_bf16(bf16_bits_rne(x)))

@@ -301,3 +301,22 @@ def test_planted_mistakes_are_caught(monkeypatch):
 
     c, a, hit, rb = walk_no_free([1, 2], [4, 0, 5], ())
     assert not (1 <= len(c) <= 3)
+
+
+def test_bf16_kv_layer_stores_rounded_rows():
+    """With a BF16 KV cache the appended context rows are the F32 path's rows rounded to BF16."""
+    from oracle import dflash as odf
+    from tests.oracle_fixtures import dflash_cfg, random_dflash_weights
+    cfg = dflash_cfg(H=16, nq=2, nkv=1, d=8, I=12, V=50, K=3, n_tl=2)
+    w = random_dflash_weights(cfg, n_layers=1, seed=3)
+    rng = np.random.default_rng(4)
+    h = rng.standard_normal((4, 16)).astype(np.float32)
+    hc = rng.standard_normal((5, 16)).astype(np.float32)
+    k32, v32 = np.zeros((1, 20, 8), np.float32), np.zeros((1, 20, 8), np.float32)
+    kb, vb = np.zeros_like(k32), np.zeros_like(v32)
+    out32 = odf.dflash_layer(cfg, w["layers"][0], h, hc, k32, v32, 2)
+    cfg.kv_bf16 = True
+    out16 = odf.dflash_layer(cfg, w["layers"][0], h, hc, kb, vb, 2)
+    assert np.array_equal(kb[:, 2:7], core.round_bf16(k32[:, 2:7]))
+    assert np.array_equal(vb[:, 2:7], core.round_bf16(v32[:, 2:7]))
+    assert not np.array_equal(out16, out32) and np.max(np.abs(out16 - out32)) < 0.05
