@@ -43,8 +43,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "mtp", "moe", "attn",
-                                                     "stochastic", "generate"],
+    ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "sweep_bf16kv", "mtp",
+                                                     "moe", "attn", "stochastic", "generate"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -109,7 +109,7 @@ def round_bytes(s, n_new: int) -> int:
     """Algorithmic HBM bytes of one round: every weight once, KV read of the cache plus the
     appended rows, KV write of the appended rows, the new target hidden rows, embed rows."""
     H, d, nkv, L = s.hidden, s.head_dim, s.n_kv_heads, s.n_layers
-    kv_row = nkv * d * 4 * 2                       # K and V, F32
+    kv_row = nkv * d * (2 if getattr(s, "kv_bf16", False) else 4) * 2   # K and V
     w = s.weight_bytes() + 2 * s.vocab * H         # drafter + lm_head
     kv_read = L * (s.ctx + n_new) * kv_row
     kv_write = L * n_new * kv_row
@@ -475,8 +475,9 @@ def _graph_rate(run_once, steps: int, warmup: int = 3) -> float:
     return steps / (e0.elapsed_time(e1) / 1e3)
 
 
-def sweep_case(steps: int):
-    """Draft rounds/s over K x context x batch at the DFlash shape (one line per case)."""
+def sweep_case(steps: int, kv_bf16: bool = False):
+    """Draft rounds/s over K x context x batch at the DFlash shape (one line per case); with
+    kv_bf16 the drafter's KV cache is BF16."""
     import torch
 
     from speculative_decoding_drafter_dflash_gb300 import binding as B
@@ -489,7 +490,7 @@ def sweep_case(steps: int):
         for Bn in (1, 8):
             cache = None
             for K in (1, 3, 7, 15):
-                s = DFLASH_K15.with_(K=K, ctx=ctx, batch=Bn)
+                s = DFLASH_K15.with_(K=K, ctx=ctx, batch=Bn, kv_bf16=kv_bf16)
                 if cache is None or cache.cap < s.ctx + s.block:
                     cache = None
                     torch.cuda.empty_cache()
@@ -512,7 +513,8 @@ def sweep_case(steps: int):
 
                 rate = _graph_rate(once, steps)
                 nb = sum(round_bytes(s, n) for n in n_new) - (Bn - 1) * (s.weight_bytes() + 2 * s.vocab * s.hidden)
-                print(json.dumps({"profile_case": "sweep", "K": K, "ctx": ctx, "batch": Bn,
+                print(json.dumps({"profile_case": "sweep", "kv": "bf16" if kv_bf16 else "f32",
+                                  "K": K, "ctx": ctx, "batch": Bn,
                                   "rounds_per_s": round(rate, 1),
                                   "positions_per_s": round(rate * Bn * s.block, 1),
                                   "round_us": round(1e6 / rate, 1), "round_bytes": int(nb),
@@ -775,6 +777,8 @@ def profile_case(args):
     g = torch.Generator(device=dev).manual_seed(0)
     if args.profile_case == "sweep":
         return sweep_case(args.steps)
+    if args.profile_case == "sweep_bf16kv":
+        return sweep_case(args.steps, kv_bf16=True)
     if args.profile_case == "mtp":
         return mtp_case(args.steps)
     if args.profile_case == "moe":

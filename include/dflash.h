@@ -95,6 +95,10 @@ typedef struct {
     float rms_eps;
     float rope_theta;
     float embed_scale;        /* multiplies gathered embedding rows (1.0) */
+    int32_t kv_bf16;          /* 0: F32 KV cache; 1: BF16 KV cache (k[l], v[l] hold BF16 bit
+                                 patterns in the same layout; every K/V value the attention reads
+                                 is rounded to BF16 when produced). Needs head_dim 128 or 256 and
+                                 at most 32 query rows per KV head (block x n_q / n_kv). */
 } df_dflash_config;
 
 typedef struct {
@@ -120,8 +124,8 @@ typedef struct {
     const uint16_t *lm_head;         /* [V, H] BF16 (the target's, borrowed) */
 } df_dflash_weights;
 
-/* Per-layer F32 KV cache. Row p of sequence b, KV head h lives at
- * k[l] + ((b * n_kv + h) * cap + p) * head_dim. seq_len[b] counts the valid rows. */
+/* Per-layer KV cache, F32 (or BF16 with cfg->kv_bf16). Row p of sequence b, KV head h lives at
+ * element ((b * n_kv + h) * cap + p) * head_dim of k[l]. seq_len[b] counts the valid rows. */
 typedef struct {
     float *const *k;     /* HOST array [n_layers] of device pointers [batch, n_kv, cap, d] */
     float *const *v;     /* HOST array [n_layers], same layout */

@@ -33,7 +33,7 @@ class DFlashConfig(ctypes.Structure):
                 ("n_kv_heads", c_int32), ("head_dim", c_int32), ("intermediate", c_int32),
                 ("vocab", c_int32), ("n_target_layers", c_int32), ("rotary_dim", c_int32),
                 ("mask_token_id", c_int32), ("causal_block", c_int32), ("rms_eps", c_float),
-                ("rope_theta", c_float), ("embed_scale", c_float)]
+                ("rope_theta", c_float), ("embed_scale", c_float), ("kv_bf16", c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -199,7 +199,8 @@ class DFlashModel:
         self.cfg = DFlashConfig(shape.hidden, shape.n_layers, shape.n_q_heads, shape.n_kv_heads,
                                 shape.head_dim, shape.intermediate, shape.vocab,
                                 shape.n_target_layers, shape.rotary_dim, shape.mask_id,
-                                shape.causal_block, shape.rms_eps, shape.rope_theta, embed_scale)
+                                shape.causal_block, shape.rms_eps, shape.rope_theta, embed_scale,
+                                1 if getattr(shape, "kv_bf16", False) else 0)
         L = len(weights.layers)
         self._layers = (LayerWeights * L)()
         for i, lw in enumerate(weights.layers):

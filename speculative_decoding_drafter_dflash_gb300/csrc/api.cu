@@ -148,6 +148,9 @@ int check_cfg(const df_dflash_config *c) {
         "mask_token_id=%d outside [0, vocab)", c->mask_token_id);
     REQ(c->causal_block == 0 || c->causal_block == 1, DF_EINVAL, "causal_block=%d", c->causal_block);
     REQ(c->rms_eps >= 0.f && c->rope_theta > 0.f, DF_EINVAL, "rms_eps / rope_theta");
+    REQ(c->kv_bf16 == 0 || c->kv_bf16 == 1, DF_EINVAL, "kv_bf16=%d", c->kv_bf16);
+    REQ(!c->kv_bf16 || c->head_dim == 128 || c->head_dim == 256, DF_ESHAPE,
+        "a BF16 KV cache needs head_dim 128 or 256 (head_dim=%d)", c->head_dim);
     return DF_OK;
 }
 
@@ -285,6 +288,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
     const int I = c->intermediate;
     const int T_blk = B * blk, T_ctx = B * n_new_max, T_all = T_blk + T_ctx;
     const int fc_in = c->n_target_layers * H, qt = nq * d, kt = nkv * d, Nqkv = qt + 2 * kt;
+    REQ(!c->kv_bf16 || attn_tc_supported(d, blk * (nq / nkv)), DF_ESHAPE,
+        "a BF16 KV cache needs at most 32 query rows per KV head (block %d x %d)", blk, nq / nkv);
 
     // A projection whose split partial sums land in ws.defer; returns the split count.
     auto deferred = [&](GemmArgs g, int T, int N, const char *name, int *S) -> int {
@@ -415,6 +420,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         qa.append_block = 0;
         qa.pos_off = 0;
         qa.status = st;
+        qa.kv_bf16 = c->kv_bf16 ? 1 : 0;
         DF_TRY(launch_qk_rope(qa, s));
 
         AttnArgs at = ws.plan;
@@ -434,6 +440,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         at.ldg = 0;
         at.pack = ws.xp_o;
         at.status = st;
+        at.kv_bf16 = c->kv_bf16 ? 1 : 0;
         DF_TRY(launch_attn(at, s));
 
         GemmArgs go;

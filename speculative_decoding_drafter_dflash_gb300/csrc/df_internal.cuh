@@ -312,6 +312,7 @@ struct QkArgs {
     int n_gate_heads = 0;
     float *gate_out = nullptr;
     int ldg = 0;
+    int kv_bf16 = 0;         // cache_k/cache_v hold BF16; block K/V rounded to BF16 values
 };
 int launch_qk_rope(const QkArgs &a, cudaStream_t s);
 
@@ -328,6 +329,7 @@ struct AttnArgs {
     float *part;             // [B, nkv, n_chunks, R, d + 2] per-CTA partial (o, m, l)
     int n_chunks, chunk;     // key chunks per (sequence, KV head); keys per chunk
     int tc;                  // 1: tensor-core kernel (chunk a multiple of 128 keys)
+    int kv_bf16;             // cache_k/cache_v hold BF16 (tensor-core kernel only)
     const float *gate;       // optional [B*blk, ldg] gate pre-activation (q_total wide)
     int ldg;
     uint16_t *pack;          // packed output [2*B*blk, nq*d] (or null)

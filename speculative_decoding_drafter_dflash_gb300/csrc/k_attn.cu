@@ -168,6 +168,22 @@ __global__ void qk_rope_kernel(QkArgs a) {
             dst = cache + (((size_t)b * a.nkv + head) * a.cap + p) * d;
         }
     }
+    if (!is_q && a.kv_bf16) {
+        // BF16 KV cache: cached rows are stored as BF16, block rows keep the rounded values
+        const bool to_cache = !(is_block && !a.append_block);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (u >= ept) continue;
+            const uint16_t bits = f32_to_bf16_bits(x[u]);
+            if (to_cache) {
+                const size_t idx = (size_t)(dst - (is_k ? a.cache_k : a.cache_v)) + lane + 32 * u;
+                reinterpret_cast<uint16_t *>(is_k ? a.cache_k : a.cache_v)[idx] = bits;
+            } else {
+                dst[lane + 32 * u] = bf16_bits_to_f32(bits);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
         if (u < ept) dst[lane + 32 * u] = x[u];
@@ -623,6 +639,9 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
     if (need_merge > (size_t)kAttnStages * kTileBytes)
         return fail(DF_ESHAPE, "attention: merge buffer exceeds the stage buffers");
     dim3 grid(a.n_chunks, a.nkv, a.B);
+    if (a.kv_bf16 && !a.tc)
+        return fail(DF_ESHAPE, "a BF16 KV cache needs head_dim 128 or 256 and at most 32 query "
+                               "rows per KV head (the tensor-core attention)");
     if (a.tc) DF_TRY(launch_attn_tc(a, s));
     else DF_TRY(launch_k("attn_kernel", attn_kernel<D, RPL>, grid, dim3(kAttnThreads), smem, s, a));
     dim3 cgrid((R + 7) / 8, a.nkv, a.B);

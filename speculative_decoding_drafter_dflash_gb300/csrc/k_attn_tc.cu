@@ -45,7 +45,7 @@ constexpr int kAtomBytes = 128 * 128;         // one 64-element-wide column bloc
 template <int D, int NP, int NBUF>
 constexpr bool attn_tc_smem_bound() {
     return 1024 + NBUF * 2 * kOpBytes + (D / 128) * 2 * NP * 256 + 2 * NP * 256 + 9 * NP * 4 +
-               3 * NBUF * 8 + 16 <= 232448;
+               3 * 2 * NBUF * 8 + 16 <= 232448;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -109,13 +109,17 @@ __device__ __forceinline__ void tmem_rows(uint32_t taddr, float (&v)[NPH]) {
 }
 
 struct AttnTcParams {
-    CUtensorMap kmap, vmap;   // F32 [B * nkv * cap rows, d cols], 128 x 128 boxes, no swizzle
+    CUtensorMap kmap, vmap;   // F32 or BF16 [B * nkv * cap rows, d cols], 128 x 128 boxes
     AttnArgs a;
 };
 
 // MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
-template <int D, int NP, int NBUF, bool MP>
+// KVB: the cache holds BF16 (the split keeps only the exact hi half: two MMAs per K step, and
+// twice as many half-size staging buffers in the same shared memory).
+template <int D, int NP, int NBUF, bool MP, bool KVB>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
+    constexpr int NB = KVB ? 2 * NBUF : NBUF;          // staging buffers
+    constexpr int kUnit = KVB ? kOpBytes : 2 * kOpBytes;  // bytes of one staged unit
     constexpr int NH = D / 128;               // 128-wide halves of the head dimension
     constexpr int NPH = NP / 2;               // rows per thread in the softmax and read-out
     constexpr int kQBytes = NP * 256;         // one NP x 128 BF16 operand (Q or P, hi or lo)
@@ -123,15 +127,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                               ~uintptr_t(1023));
-    uint8_t *kvb = sm;                                  // NBUF x 64 KB: F32 staging, then hi | lo
-    uint8_t *qsm = sm + NBUF * 2 * kOpBytes;            // [NH][hi, lo] Q operands
+    uint8_t *kvb = sm;                                  // NB x 64 KB: F32 staging, then hi | lo
+    uint8_t *qsm = sm + NB * kUnit;            // [NH][hi, lo] Q operands
     uint8_t *psm = qsm + NH * 2 * kQBytes;              // [hi, lo] P operand (second buffer)
     float *red = reinterpret_cast<float *>(psm + 2 * kQBytes);   // [4][NP] maxima, [4][NP] sums
     float *mrun = red + 8 * NP;                                  // [NP] running row maxima
-    uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NBUF] staging landed
-    uint64_t *mdone = full + NBUF;                               // [NBUF] MMAs of the unit done
-    uint64_t *conv = mdone + NBUF;                               // [NBUF] unit split, ready for MMA
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(conv + NBUF);
+    uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NB] staging landed
+    uint64_t *mdone = full + NB;                               // [NB] MMAs of the unit done
+    uint64_t *conv = mdone + NB;                               // [NB] unit split, ready for MMA
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(conv + NB);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -190,9 +194,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     auto issue = [&](int u) {
         const UnitInfo x = decode(u);
         const bool isV = x.v;
-        const int t = x.t, h = x.h, bf = u % NBUF;
-        mbar_expect_tx(&full[bf], (uint32_t)(2 * kOpBytes));
-        tma_load_2d(kvb + (size_t)bf * 2 * kOpBytes, isV ? &P.vmap : &P.kmap, &full[bf], h * 128,
+        const int t = x.t, h = x.h, bf = u % NB;
+        mbar_expect_tx(&full[bf], (uint32_t)kUnit);
+        tma_load_2d(kvb + (size_t)bf * kUnit, isV ? &P.vmap : &P.kmap, &full[bf], h * 128,
                     (int)(head_off * a.cap) + c0 + t * kTcKeys, pol);
     };
 
@@ -218,14 +222,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         tmem_relinquish();
     }
     if (tid == kConvThreads) {
-        for (int i = 0; i < NBUF; ++i) {
+        for (int i = 0; i < NB; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&mdone[i], 1);
             mbar_init(&conv[i], kConvThreads / 32);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int u = 0; u < min(NBUF, nU); ++u) issue(u);
+        for (int u = 0; u < min(NB, nU); ++u) issue(u);
     }
     // Q -> hi/lo operands (rows R..NP-1 zero)
 #pragma unroll
@@ -262,7 +266,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const UnitInfo x = decode(u);
         const bool isV = x.v;
         const int t = x.t, h = x.h;
-        const float *st = reinterpret_cast<const float *>(kvb + (size_t)(u % NBUF) * 2 * kOpBytes);
+        const float *st = reinterpret_cast<const float *>(kvb + (size_t)(u % NB) * kUnit);
+        const uint16_t *stb = reinterpret_cast<const uint16_t *>(st);
+        auto stage4 = [&](int kr, int c4) -> float4 {     // 4 staged values at row kr, col c4
+            if constexpr (KVB) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(stb + kr * 128 + c4);
+                return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                   __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+            } else {
+                return *reinterpret_cast<const float4 *>(st + kr * 128 + c4);
+            }
+        };
         const float *blkp = isV ? a.vb : a.kb;
         const int kbase = c0 + t * kTcKeys;
         if (!isV) {
@@ -270,7 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             for (int it = 0; it < 16; ++it) {
                 const int kr = it * 8 + warp, key = kbase + kr;
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (key < S_cache) v = *reinterpret_cast<const float4 *>(st + kr * 128 + 4 * lane);
+                if (key < S_cache) v = stage4(kr, 4 * lane);
                 else if (key < c1)
                     v = __ldcg(reinterpret_cast<const float4 *>(
                         blkp + (head_off * a.blk + (key - S_cache)) * D + h * 128 + 4 * lane));
@@ -285,7 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (int jj = 0; jj < 8; ++jj) {
                     const int kr = 8 * ob + jj, key = kbase + kr;
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (key < S_cache) v = *reinterpret_cast<const float4 *>(st + kr * 128 + 4 * qd);
+                    if (key < S_cache) v = stage4(kr, 4 * qd);
                     else if (key < c1)
                         v = __ldcg(reinterpret_cast<const float4 *>(
                             blkp + (head_off * a.blk + (key - S_cache)) * D + h * 128 + 4 * qd));
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
     };
     auto write_unit = [&](int u) {
-        const uint32_t hi = smem_u32(kvb + (size_t)(u % NBUF) * 2 * kOpBytes), lo = hi + kOpBytes;
+        const uint32_t hi = smem_u32(kvb + (size_t)(u % NB) * kUnit), lo = hi + kOpBytes;
         if (!decode(u).v) {
 #pragma unroll
             for (int it = 0; it < 16; ++it) {
@@ -309,8 +323,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 const uint32_t o = sw_off(128, kr, 4 * lane);
                 st_shared_v2(hi + o, *reinterpret_cast<const uint32_t *>(&h01),
                              *reinterpret_cast<const uint32_t *>(&h23));
-                st_shared_v2(lo + o, *reinterpret_cast<const uint32_t *>(&l01),
-                             *reinterpret_cast<const uint32_t *>(&l23));
+                if constexpr (!KVB)
+                    st_shared_v2(lo + o, *reinterpret_cast<const uint32_t *>(&l01),
+                                 *reinterpret_cast<const uint32_t *>(&l23));
             }
         } else {
 #pragma unroll
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     split8(x, vh, vl);
                     const uint32_t o = sw_off(128, 4 * qd + i, 8 * ob);
                     st_shared_v4(hi + o, vh);
-                    st_shared_v4(lo + o, vl);
+                    if constexpr (!KVB) st_shared_v4(lo + o, vl);
                 }
             }
         }
@@ -344,11 +359,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 mma_bf16(dt, sw128_desc(a_hi + oa), sw128_desc(b_hi + ob), idesc,
                          (acc || kb || ks) ? 1u : 0u);
                 mma_bf16(dt, sw128_desc(a_hi + oa), sw128_desc(b_lo + ob), idesc, 1u);
-                mma_bf16(dt, sw128_desc(a_lo + oa), sw128_desc(b_hi + ob), idesc, 1u);
+                if constexpr (!KVB) mma_bf16(dt, sw128_desc(a_lo + oa), sw128_desc(b_hi + ob), idesc, 1u);
             }
     };
     auto wait_mma = [&](int u) {   // the MMAs of unit u (and all before it) have completed
-        mbar_wait(&mdone[u % NBUF], (uint32_t)((u / NBUF) & 1), abort_flag, a.status);
+        mbar_wait(&mdone[u % NB], (uint32_t)((u / NB) & 1), abort_flag, a.status);
         tc_fence_after();
     };
 
@@ -377,10 +392,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // TMA / MMA issuer: MMAs of unit u once its split has landed; then refill its buffer.
         if (lane == 0) {
             for (int u = 0; u < nU; ++u) {
-                const uint32_t ph = (uint32_t)((u / NBUF) & 1);
-                if (!mbar_wait(&conv[u % NBUF], ph, abort_flag, a.status)) break;
+                const uint32_t ph = (uint32_t)((u / NB) & 1);
+                if (!mbar_wait(&conv[u % NB], ph, abort_flag, a.status)) break;
                 tc_fence_after();
-                const uint32_t ahi = smem_u32(kvb + (size_t)(u % NBUF) * 2 * kOpBytes), alo = ahi + kOpBytes;
+                const uint32_t ahi = smem_u32(kvb + (size_t)(u % NB) * kUnit), alo = ahi + kOpBytes;
                 const UnitInfo x = decode(u);
                 if (!x.v) {
                     const uint32_t qhi = smem_u32(qsm + (2 * x.h) * kQBytes), qlo = qhi + kQBytes;
@@ -389,10 +404,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     const uint32_t phi = p_buf(x.t), plo = phi + kQBytes;
                     mma3(tmem + ocol + x.h * NP, ahi, alo, phi, plo, x.t > x.t0);
                 }
-                mma_commit(&mdone[u % NBUF]);
-                if (u + NBUF < nU) {
-                    if (!mbar_wait(&mdone[u % NBUF], ph, abort_flag, a.status)) break;
-                    issue(u + NBUF);
+                mma_commit(&mdone[u % NB]);
+                if (u + NB < nU) {
+                    if (!mbar_wait(&mdone[u % NB], ph, abort_flag, a.status)) break;
+                    issue(u + NB);
                 }
             }
         }
@@ -431,9 +446,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 } else if (tl >= 2) {
                     // P operands alternate between two buffers: the one for tile t was last read by
                     // the P.V MMAs of tile t - 2. Waiting on that older unit is only safe while
-                    // its barrier cannot have completed a later phase (NBUF > NH); otherwise wait
+                    // its barrier cannot have completed a later phase (NB > NH); otherwise wait
                     // on the most recent unit, which covers it.
-                    wait_mma(NBUF > NH ? u - NH - 1 : u - 1);
+                    wait_mma(NB > NH ? u - NH - 1 : u - 1);
                 }
                 // pass 2 for tile t: probabilities -> BF16 hi/lo P operand
                 float s[NPH];
@@ -454,14 +469,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     st_shared_u16(plo + o, pl);
                 }
             }
-            mbar_wait(&full[u % NBUF], (uint32_t)((u / NBUF) & 1), abort_flag, a.status);
+            mbar_wait(&full[u % NB], (uint32_t)((u / NB) & 1), abort_flag, a.status);
             read_unit(u);
             conv_sync();
             write_unit(u);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[u % NBUF]);
+            if (lane == 0) mbar_arrive(&conv[u % NB]);
             if constexpr (MP) {
                 if (x.v && x.t == x.t0 + x.nt - 1 && x.h == NH - 1) {
                     // end of a pass: merge its (max, sum, o) into the running values
@@ -545,7 +560,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 template <int D, int NP, int NBUF>
 size_t attn_tc_smem() {
     return 1024 + NBUF * 2 * (size_t)kOpBytes + (D / 128) * 2 * (size_t)NP * 256 +
-           2 * (size_t)NP * 256 + 9 * NP * sizeof(float) + 3 * NBUF * sizeof(uint64_t) + 16;
+           2 * (size_t)NP * 256 + 9 * NP * sizeof(float) + 3 * 2 * NBUF * sizeof(uint64_t) + 16;
 }
 
 template <int D, int NP, int NBUF>
@@ -558,17 +573,23 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
     if (rows + kTcKeys > 0x7fffffffull)
         return fail(DF_ESHAPE, "tensor-core attention: %llu cache rows exceed the TMA row range",
                     (unsigned long long)rows);
-    DF_TRY(make_tma_2d(&p.kmap, a.cache_k, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, rows, D, 128,
-                       128, CU_TENSOR_MAP_SWIZZLE_NONE));
-    DF_TRY(make_tma_2d(&p.vmap, a.cache_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, rows, D, 128,
-                       128, CU_TENSOR_MAP_SWIZZLE_NONE));
+    const CUtensorMapDataType dt = a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int eb = a.kv_bf16 ? 2 : 4;
+    DF_TRY(make_tma_2d(&p.kmap, a.cache_k, dt, eb, D, rows, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE));
+    DF_TRY(make_tma_2d(&p.vmap, a.cache_v, dt, eb, D, rows, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE));
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    if (a.chunk <= max_keys_one_pass)
-        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false>, grid,
-                        dim3(kTcThreads), attn_tc_smem<D, NP, NBUF>(), s, p);
-    return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true>, grid, dim3(kTcThreads),
-                    attn_tc_smem<D, NP, NBUF>(), s, p);
+    const size_t smem = attn_tc_smem<D, NP, NBUF>();
+    const bool one = a.chunk <= max_keys_one_pass;
+    if (a.kv_bf16)
+        return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true>, grid,
+                              dim3(kTcThreads), smem, s, p)
+                   : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, true>, grid,
+                              dim3(kTcThreads), smem, s, p);
+    return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false>, grid,
+                          dim3(kTcThreads), smem, s, p)
+               : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false>, grid,
+                          dim3(kTcThreads), smem, s, p);
 }
 
 }  // namespace

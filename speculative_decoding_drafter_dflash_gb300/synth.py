@@ -118,16 +118,17 @@ def dflash_weights(s: DFlashShape, seed: int = 0, device="cpu") -> DFlashWeights
 
 
 def kv_cache(n_layers: int, B: int, n_kv: int, d: int, filled: int, cap: int, seed: int,
-             device="cpu") -> KvCache:
-    """Per-layer F32 K/V of `cap` positions; the first `filled` hold N(0,1) rows."""
+             device="cpu", bf16: bool = False) -> KvCache:
+    """Per-layer F32 (or BF16) K/V of `cap` positions; the first `filled` hold N(0,1) rows."""
     g = _gen(seed, device)
     ks, vs = [], []
+    dt = torch.bfloat16 if bf16 else torch.float32
     for _ in range(n_layers):
-        k = torch.zeros((B, n_kv, cap, d), device=device, dtype=torch.float32)
+        k = torch.zeros((B, n_kv, cap, d), device=device, dtype=dt)
         v = torch.zeros_like(k)
         if filled:
-            k[:, :, :filled] = _normal(g, (B, n_kv, filled, d), 1.0, device)
-            v[:, :, :filled] = _normal(g, (B, n_kv, filled, d), 1.0, device)
+            k[:, :, :filled] = _normal(g, (B, n_kv, filled, d), 1.0, device).to(dt)
+            v[:, :, :filled] = _normal(g, (B, n_kv, filled, d), 1.0, device).to(dt)
         ks.append(k)
         vs.append(v)
     seq = torch.full((B,), filled, device=device, dtype=torch.int32)
@@ -136,7 +137,7 @@ def kv_cache(n_layers: int, B: int, n_kv: int, d: int, filled: int, cap: int, se
 
 def dflash_cache(s: DFlashShape, seed: int = 1, device="cpu", extra: int = 0) -> KvCache:
     return kv_cache(s.n_layers, s.batch, s.n_kv_heads, s.head_dim, s.ctx,
-                    s.ctx + s.block + extra, seed, device)
+                    s.ctx + s.block + extra, seed, device, bf16=s.kv_bf16)
 
 
 def accept_lengths(n: int, K: int, p: Optional[float], seed: int) -> np.ndarray:

@@ -37,6 +37,7 @@ class DFlashShape:
     w_std: float = 0.02
     norm_std: float = 0.1
     accept_p: float = 0.6       # P(accept >= j) = p**j for the geometric target
+    kv_bf16: bool = False       # BF16 KV cache (False: F32)
 
     @property
     def block(self) -> int:

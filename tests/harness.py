@@ -40,9 +40,13 @@ def mtp_weights_host(w: synth.MtpWeights):
     return out
 
 
+def _as_f32(t):
+    """Host F32 copy of a cache tensor (BF16 caches are widened exactly)."""
+    return t.detach().float().contiguous().cpu().numpy()
+
+
 def cache_host(c: synth.KvCache):
-    return [synth.host(k).copy() for k in c.k], [synth.host(v).copy() for v in c.v], \
-        synth.host(c.seq_len).copy()
+    return [_as_f32(k) for k in c.k], [_as_f32(v) for v in c.v], synth.host(c.seq_len).copy()
 
 
 def assert_argmax_parity(gpu_idx, ref_idx, ref_top1, ref_top2, what=""):
