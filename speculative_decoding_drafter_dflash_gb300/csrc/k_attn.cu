@@ -491,21 +491,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
     }
 }
 
-// Merge of the chunk partials: one warp per (query row, sequence, KV head) group of rows. Lane c
-// holds chunk c's merge weight exp2(m_c - M) / L; every partial o value of a chunk is loaded
-// before any is summed, and the sum runs in chunk order (the result does not depend on timing).
+// Merge of the chunk partials: one warp per (query row, 32-wide slice of the head dims). Lane c
+// holds chunk c's merge weight 2^(m_c - M) / L (M, L over all chunks); the partial outputs of 32
+// chunks are loaded at once per lane before any is summed, and the sum runs in chunk order (the
+// result does not depend on timing).
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
-    constexpr int RPB = 8;                   // query rows per CTA (one per warp)
-    constexpr int EPL = D / 32;              // output dims per lane
+    constexpr int SL = D / 32;               // slices per row
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y, b = blockIdx.z;
     const int rep = a.nq / a.nkv;
     const int R = a.blk * rep;
-    const int r2 = blockIdx.x * RPB + warp;
-    if (r2 >= R) return;
+    const int task = blockIdx.x * 8 + warp;
+    if (task >= R * SL) return;
+    const int r2 = task / SL, e = (task - r2 * SL) * 32 + lane;
     const size_t head_off = (size_t)b * a.nkv + g;
     const float *allp = a.part + head_off * a.n_chunks * (size_t)R * (D + 2);
     const int NC = a.n_chunks;
@@ -520,9 +521,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
     }
     L = warp_sum(L);
     const float invL = L > 0.f ? 1.f / L : 0.f;
-    float y[EPL];
-#pragma unroll
-    for (int u = 0; u < EPL; ++u) y[u] = 0.f;
+    float y = 0.f;
     for (int c0 = 0; c0 < NC; c0 += 32) {
         float wl = 0.f;
         if (c0 + lane < NC) {
@@ -530,41 +529,27 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
             wl = mc == -INFINITY ? 0.f : exp2f(mc - M) * invL;
         }
         const int cn = min(32, NC - c0);
-        for (int cb = 0; cb < cn; cb += 8) {
-            float ov[8][EPL];
+        float ov[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = c0 + cb + j;
-                const float *pc = allp + ((size_t)min(c, NC - 1) * R + r2) * (D + 2);
+        for (int j = 0; j < 32; ++j)
+            ov[j] = j < cn ? allp[((size_t)(c0 + j) * R + r2) * (D + 2) + e] : 0.f;
 #pragma unroll
-                for (int u = 0; u < EPL; ++u) ov[j][u] = (cb + j < cn) ? pc[lane + 32 * u] : 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, wl, (cb + j) & 31);
-#pragma unroll
-                for (int u = 0; u < EPL; ++u) y[u] = fmaf(wj, ov[j][u], y[u]);
-            }
-        }
+        for (int j = 0; j < 32; ++j) y = fmaf(__shfl_sync(0xffffffffu, wl, j), ov[j], y);
     }
     const int i = r2 / rep, h = g * rep + r2 % rep;
     const size_t t = (size_t)b * a.blk + i;
-#pragma unroll
-    for (int u = 0; u < EPL; ++u) {
-        const int e = lane + 32 * u;
-        float v = y[u];
-        if (a.gate) {
-            const float z = a.gate[t * a.ldg + (size_t)h * D + e];
-            v = v * (1.f / (1.f + expf(-z)));
-        }
-        const size_t col = (size_t)h * D + e;
-        if (a.out) a.out[t * (size_t)(a.nq * D) + col] = v;
-        if (a.pack) {
-            uint16_t hi, lo;
-            split_hi_lo(v, hi, lo);
-            a.pack[(2 * t) * (size_t)(a.nq * D) + col] = hi;
-            a.pack[(2 * t + 1) * (size_t)(a.nq * D) + col] = lo;
-        }
+    float v = y;
+    if (a.gate) {
+        const float z = a.gate[t * a.ldg + (size_t)h * D + e];
+        v = v * (1.f / (1.f + expf(-z)));
+    }
+    const size_t col = (size_t)h * D + e;
+    if (a.out) a.out[t * (size_t)(a.nq * D) + col] = v;
+    if (a.pack) {
+        uint16_t hi, lo;
+        split_hi_lo(v, hi, lo);
+        a.pack[(2 * t) * (size_t)(a.nq * D) + col] = hi;
+        a.pack[(2 * t + 1) * (size_t)(a.nq * D) + col] = lo;
     }
 }
 
@@ -644,7 +629,7 @@ int launch_attn_d(const AttnArgs &a, cudaStream_t s) {
                                "rows per KV head (the tensor-core attention)");
     if (a.tc) DF_TRY(launch_attn_tc(a, s));
     else DF_TRY(launch_k("attn_kernel", attn_kernel<D, RPL>, grid, dim3(kAttnThreads), smem, s, a));
-    dim3 cgrid((R + 7) / 8, a.nkv, a.B);
+    dim3 cgrid((R * (D / 32) + 7) / 8, a.nkv, a.B);
     return launch_k("attn_combine_kernel", attn_combine_kernel<D>, cgrid, dim3(256), 0, s, a);
 }
 
