@@ -181,6 +181,21 @@ def _p(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _dev(t: Optional[torch.Tensor], dtype, name: str):
+    """Pointer of a contiguous CUDA tensor of `dtype` (None passes through). A tensor of another
+    type, layout or device raises here rather than reaching a kernel that would read it with the
+    wrong element size."""
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} on "
+                        f"{t.device}" + ("" if t.is_contiguous() else " (not contiguous)"))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+F32, I32, BF16 = torch.float32, torch.int32, torch.bfloat16
+
+
 def _stream(stream):
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -215,6 +230,11 @@ class DFlashModel:
 
     def set_cache(self, cache):
         L = len(cache.k)
+        want = BF16 if self.cfg.kv_bf16 else F32
+        for i in range(L):
+            _dev(cache.k[i], want, f"cache.k[{i}]")
+            _dev(cache.v[i], want, f"cache.v[{i}]")
+        _dev(cache.seq_len, I32, "cache.seq_len")
         self._k = (c_void_p * L)(*[t.data_ptr() for t in cache.k])
         self._v = (c_void_p * L)(*[t.data_ptr() for t in cache.v])
         self.cache_c = KvCache(self._k, self._v, cache.seq_len.data_ptr(), cache.cap,
@@ -250,7 +270,9 @@ def lm_head_workspace_bytes(rows: int, H: int, V: int) -> int:
 def lm_head_argmax(W, X, idx, top1=None, top2=None, ws=None, stream=None):
     rows, H = X.shape
     V = W.shape[0]
-    _check(lib().lm_head_argmax(_p(W), _p(X), rows, H, V, _p(idx), _p(top1), _p(top2), _p(ws),
+    _check(lib().lm_head_argmax(_dev(W, BF16, "W"), _dev(X, F32, "X"), rows, H, V,
+                                _dev(idx, I32, "idx"), _dev(top1, F32, "top1"),
+                                _dev(top2, F32, "top2"), _p(ws),
                                 ws.numel() if ws is not None else 0, _stream(stream)))
 
 
@@ -261,15 +283,17 @@ def linear_workspace_bytes(T: int, N: int, K: int) -> int:
 def df_linear(W, X, Y, ws, stream=None):
     T, K = X.shape
     N = W.shape[0]
-    _check(lib().df_linear(_p(W), _p(X), T, N, K, _p(Y), _p(ws), ws.numel(), _stream(stream)))
+    _check(lib().df_linear(_dev(W, BF16, "W"), _dev(X, F32, "X"), T, N, K, _dev(Y, F32, "Y"),
+                           _p(ws), ws.numel(), _stream(stream)))
 
 
 def lm_head_argmax_noalloc(W, X, idx, top1=None, top2=None, stream=None):
     """lm_head_argmax without a workspace (fixed scratch inside the library; see dflash.h)."""
     rows, H = X.shape
     V = W.shape[0]
-    _check(lib().lm_head_argmax_noalloc(_p(W), _p(X), rows, H, V, _p(idx), _p(top1), _p(top2),
-                                        _stream(stream)))
+    _check(lib().lm_head_argmax_noalloc(_dev(W, BF16, "W"), _dev(X, F32, "X"), rows, H, V,
+                                        _dev(idx, I32, "idx"), _dev(top1, F32, "top1"),
+                                        _dev(top2, F32, "top2"), _stream(stream)))
 
 
 def accept_prefix_argmax(drafts, drafts_ld: int, target, K: int, eos, committed, n_committed,
@@ -406,8 +430,11 @@ def attention(q, cache_k, cache_v, seq_len, out, ws, kb=None, vb=None, causal_bl
     out [B, blk, nq, d]."""
     Bn, blk, nq, d = q.shape
     nkv, cap = cache_k.shape[1], cache_k.shape[2]
-    _check(lib().df_attention(_p(q), _p(cache_k), _p(cache_v), cap, _p(seq_len), _p(kb), _p(vb),
-                              Bn, blk, nq, nkv, d, 1 if causal_block else 0, _p(out), _p(ws),
+    _check(lib().df_attention(_dev(q, F32, "q"), _dev(cache_k, F32, "cache_k"),
+                              _dev(cache_v, F32, "cache_v"), cap, _dev(seq_len, I32, "seq_len"),
+                              _dev(kb, F32, "kb"), _dev(vb, F32, "vb"),
+                              Bn, blk, nq, nkv, d, 1 if causal_block else 0,
+                              _dev(out, F32, "out"), _p(ws),
                               ws.numel(), _p(d_status), _stream(stream)))
 
 

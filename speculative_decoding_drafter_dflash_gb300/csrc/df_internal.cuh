@@ -282,6 +282,7 @@ int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *t
 
 // RoPE table: cos/sin F32 [B, slots, rot/2] for block slots (pos = seq_len + n_new + i + off)
 // and context slots (pos = seq_len + j).
+constexpr int kMaxRopeHalf = 128;   // rotary dims up to 256
 int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const int32_t *n_new,
                       int n_new_max, int B, int blk, int pos_off, int rot, float theta,
                       int32_t *status, cudaStream_t s);

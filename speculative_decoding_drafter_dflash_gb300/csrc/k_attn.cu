@@ -8,8 +8,10 @@
 // with grouped KV heads), `apply_sigmoid_gate_multiply`. DFlash: tensors.rs
 // `DFlashLayerTensors::q_norm/k_norm`; the context rows of qwen35_orchestrator.rs step 3.
 #include <math.h>
+#include <string.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "df_internal.cuh"
 
@@ -17,34 +19,40 @@ namespace df {
 
 namespace {
 
-// cos/sin of pos * theta^(-2j/rot) in double precision, rounded to F32.
-__global__ void rope_table_kernel(float *cos_t, float *sin_t, const int32_t *seq_len,
-                                  const int32_t *n_new, int n_new_max, int B, int blk, int pos_off,
-                                  int rot, float theta, int32_t *status) {
+// cos/sin of pos * theta^(-2j/rot), rounded to F32. The inverse frequencies come from the host
+// in double precision (GB300's FP64 rate makes per-element exp2/log2 the slowest step of a
+// round); the angle is formed and reduced to [-pi, pi] in double, then its sine and cosine are
+// taken in F32.
+struct RopeArgs {
+    float *cos_t, *sin_t;
+    const int32_t *seq_len, *n_new;
+    int n_new_max, B, blk, pos_off, rot;
+    int32_t *status;
+    double inv[kMaxRopeHalf];
+};
+
+__global__ void rope_table_kernel(const __grid_constant__ RopeArgs a) {
     pdl_trigger();
     pdl_wait();
-    const int half = rot / 2;
-    const int slots = blk + n_new_max;
-    const int total = B * slots * half;
+    const int half = a.rot / 2;
+    const int slots = a.blk + a.n_new_max;
+    const int total = a.B * slots * half;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-        int j = i % half;
-        int s = (i / half) % slots;
-        int b = i / (half * slots);
-        int base = seq_len[b];
-        int nn = n_new ? min(max(n_new[b], 0), n_new_max) : 0;
-        if (status && j == 0 && s == 0 && n_new && (n_new[b] < 0 || n_new[b] > n_new_max))
-            set_status(status, DF_ESHAPE);
-        long long pos = s < blk ? (long long)base + nn + s + pos_off : (long long)base + (s - blk);
-        // inverse frequency theta^(-2j/rot) and the angle in double precision; the angle is
-        // reduced to [-pi, pi] in double, then its sine and cosine are taken in F32.
-        const double inv = exp2(-2.0 * (double)j / (double)rot * log2((double)theta));
-        const double ang = (double)pos * inv;
+        const int j = i % half;
+        const int s = (i / half) % slots;
+        const int b = i / (half * slots);
+        const int base = a.seq_len[b];
+        const int nn = a.n_new ? min(max(a.n_new[b], 0), a.n_new_max) : 0;
+        if (a.status && j == 0 && s == 0 && a.n_new && (a.n_new[b] < 0 || a.n_new[b] > a.n_new_max))
+            set_status(a.status, DF_ESHAPE);
+        const long long pos = s < a.blk ? (long long)base + nn + s + a.pos_off : (long long)base + (s - a.blk);
+        const double ang = (double)pos * a.inv[j];
         const double two_pi = 6.283185307179586476925286766559;
-        const double red = ang - rint(ang / two_pi) * two_pi;
+        const double red = fma(-rint(ang * (1.0 / two_pi)), two_pi, ang);
         float sn, cs;
         sincosf((float)red, &sn, &cs);
-        cos_t[i] = cs;
-        sin_t[i] = sn;
+        a.cos_t[i] = cs;
+        a.sin_t[i] = sn;
     }
 }
 
@@ -575,9 +583,22 @@ int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const 
                       int32_t *status, cudaStream_t s) {
     int total = B * (blk + n_new_max) * (rot / 2);
     if (total <= 0) return DF_OK;
+    if (rot / 2 > kMaxRopeHalf) return fail(DF_ESHAPE, "rotary dim %d above %d", rot, 2 * kMaxRopeHalf);
+    RopeArgs a;
+    memset(&a, 0, sizeof(a));
+    a.cos_t = cos_t;
+    a.sin_t = sin_t;
+    a.seq_len = seq_len;
+    a.n_new = n_new;
+    a.n_new_max = n_new_max;
+    a.B = B;
+    a.blk = blk;
+    a.pos_off = pos_off;
+    a.rot = rot;
+    a.status = status;
+    for (int j = 0; j < rot / 2; ++j) a.inv[j] = std::pow((double)theta, -2.0 * j / (double)rot);
     int threads = 256, grid = min((total + threads - 1) / threads, 4 * kNumSMs);
-    return launch_k("rope_table_kernel", rope_table_kernel, dim3(grid), dim3(threads), 0, s, cos_t,
-                    sin_t, seq_len, n_new, n_new_max, B, blk, pos_off, rot, theta, status);
+    return launch_k("rope_table_kernel", rope_table_kernel, dim3(grid), dim3(threads), 0, s, a);
 }
 
 int launch_qk_rope(const QkArgs &a, cudaStream_t s) {

@@ -90,3 +90,17 @@ def test_workspace_queries_scale(L):
     w8 = lib.df_dflash_workspace_bytes(ctypes.byref(cfg), 8, 16, 16)
     assert 0 < w1 < w8 < 1 << 31
     assert lib.df_lm_head_workspace_bytes(16, 2816, 262144) > 2 * 16 * 2816 * 2
+
+
+def test_binding_rejects_tensors_of_the_wrong_type_or_device(L):
+    # The element size a kernel reads with comes from the entry point, not from the tensor: a
+    # host tensor, or one of another dtype (a BF16 cache handed to the F32 attention), must stop
+    # in the binding. Without a GPU every tensor is a host tensor: the first argument is named.
+    import torch
+    f32 = torch.zeros((1, 2, 2, 128))
+    with pytest.raises(TypeError, match="^q: expected a contiguous CUDA"):
+        L.attention(f32, f32.to(torch.bfloat16), f32, torch.zeros(1, dtype=torch.int32), f32,
+                    torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="^W: expected a contiguous CUDA torch.bfloat16"):
+        L.df_linear(torch.zeros((4, 8)), torch.zeros((2, 8)), torch.zeros((2, 4)),
+                    torch.zeros(256, dtype=torch.uint8))
