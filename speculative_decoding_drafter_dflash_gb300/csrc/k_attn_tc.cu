@@ -8,23 +8,28 @@
 // merges the chunks. Scores follow hf2q 0.1.1 models/qwen35/mtp.rs (`sdpa` step of the draft
 // forward: softmax(q k^T / sqrt(d)) v over the visible keys).
 //
-// The cache holds F32 keys and values. Each 128-key x 128-dim piece (a "unit") lands in a
-// 64 KB shared-memory buffer by one TMA box load (three buffers in flight), is split in place
-// into hi = bf16(x) and lo = bf16(x - hi) (about 16 mantissa bits) in the 128-byte-swizzled
-// K-major layout, and is multiplied with three kind::f16 MMAs (hi.hi + hi.lo + lo.hi, F32
-// accumulation in TMEM):
-//   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (one TMEM block per tile)
-//   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (per 128-dim half)
-// A chunk's scores stay in TMEM, up to (512 - halves*NP)/NP tiles per pass, so the softmax
-// maximum is exact per pass: pass 1 takes the row maxima, pass 2 turns each tile into
-// probabilities (BF16 hi/lo in shared memory) right before its P.V MMAs. A longer chunk runs in
-// several passes whose (max, sum, o) are merged in registers, rescaled once per pass. Values are
-// transposed while they are split, so both products read K-major operands.
+// Each 128-key x 128-dim piece of K or V (a "unit") lands in shared memory by TMA with the
+// 128-byte swizzle (F32: four 32-column boxes, BF16: two 64-column boxes), so a thread reading
+// one row, or one column, of it touches every bank once. The eight converting warps turn a unit
+// into a BF16 operand in tensor memory (TMEM), where the MMA reads it as its A matrix:
+//   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (A = K: lane = key)
+//   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (A = V^T: lane = dim)
+// An F32 cache is split into hi = bf16(x) and lo = bf16(x - hi) (about 16 mantissa bits) and
+// multiplied with three MMAs per 16-wide K step (hi.hi + hi.lo + lo.hi against Q or P, whose
+// hi/lo halves sit in shared memory); a BF16 cache needs only its own values (two MMAs). The
+// converted operand never goes back to shared memory, and the staging buffer is free for the
+// next TMA load as soon as the warps have read it.
 //
-// 288 threads: warps 0-7 convert; warp 8 issues the TMA loads and the MMAs and refills a
-// buffer once the MMAs reading it are done; warps w and w + 4 share TMEM lane quarter w % 4 and
-// split the rows in the softmax and the read-out. Block rows (keys past the cache rows) come from
-// kb/vb with plain loads during the split; keys past the chunk are written as zeros.
+// A chunk's scores stay in TMEM, up to (512 - 256 - halves*NP)/NP tiles per pass (256 columns
+// hold the converted operands), so the softmax maximum is exact per pass: pass 1 takes the row
+// maxima, pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory) right before
+// its V units are converted. A longer chunk runs in several passes whose (max, sum, o) are
+// merged in registers, rescaled once per pass.
+//
+// 288 threads: warps 0-7 convert, run the softmax and read out (warps w and w + 4 share TMEM
+// lane quarter w % 4 and take one half of the columns, rows or keys); thread 0 also issues the
+// TMA loads; warp 8 issues the MMAs. Block rows (keys past the cache rows) come from kb/vb with
+// plain loads during the conversion; keys past the chunk are converted as zeros.
 #include <cuda_bf16.h>
 #include <string.h>
 
@@ -35,17 +40,20 @@ namespace df {
 
 namespace {
 
-constexpr int kConvThreads = 256;             // warps 0-7: split, softmax, read-out
-constexpr int kTcThreads = kConvThreads + 32;  // warp 8: TMA and MMA issue
+constexpr int kGroups = 4;                    // converting warps per TMEM lane quarter
+constexpr int kConvThreads = 128 * kGroups;   // warps 0-15: convert, softmax, read-out
+constexpr int kTcThreads = kConvThreads + 32;  // warp 16: MMA issue
+constexpr int kDT = 128 / kGroups;            // K values of a unit row per converting thread
 constexpr int kTcKeys = 128;                  // keys per tile
 constexpr int kTmemCols = 512;
-constexpr int kOpBytes = 128 * 128 * 2;       // one 128 x 128 BF16 operand (hi or lo): 32 KB
-constexpr int kAtomBytes = 128 * 128;         // one 64-element-wide column block of 128 rows
+constexpr int kACols = 256;                   // TMEM columns of the converted A operands
+constexpr int kF32Unit = 128 * 128 * 4;       // one staged F32 unit: 64 KB
+constexpr int kBoxBytes = 128 * 128;          // one 128-byte-wide column box of 128 rows
 
 template <int D, int NP, int NBUF>
-constexpr bool attn_tc_smem_bound() {
-    return 1024 + NBUF * 2 * kOpBytes + (D / 128) * 2 * NP * 256 + 2 * NP * 256 + 9 * NP * 4 +
-               3 * 2 * NBUF * 8 + 16 <= 232448;
+constexpr size_t attn_tc_smem_bytes() {
+    return 1024 + (size_t)NBUF * kF32Unit + (D / 128) * 2 * (size_t)NP * 256 + 2 * (size_t)NP * 256 +
+           9 * NP * 4 + 32 * 8 + 16;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -76,26 +84,41 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint4 &hi, uint4 &lo
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// Two F32 values (lower K index first) -> one word of BF16 hi halves and one of lo halves.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+    lo = *reinterpret_cast<const uint32_t *>(&lb);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
-__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t x, uint32_t y) {
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
-}
-
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// Barrier of the eight splitting warps (named barrier 1; warp 8 does not take part).
-__device__ __forceinline__ void conv_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier of the converting warps (named barrier 1; the MMA warp does not take part).
+__device__ __forceinline__ void conv_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConvThreads) : "memory");
+}
 
 template <int NPH>
 __device__ __forceinline__ void tmem_rows(uint32_t taddr, float (&v)[NPH]) {
-    if constexpr (NPH == 16) {
+    if constexpr (NPH == 4) {
+        uint32_t r[4];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+    } else if constexpr (NPH == 16) {
         uint32_t r[16];
         tmem_ld16(taddr, r);
 #pragma unroll
@@ -108,40 +131,76 @@ __device__ __forceinline__ void tmem_rows(uint32_t taddr, float (&v)[NPH]) {
     }
 }
 
+// Reduce N per-lane values over the warp's 32 lanes with N-1+5-log2(N) shuffles (halving the
+// values each step instead of reducing each one separately). Returns the reduction of value
+// `row` (see below) in every lane; lanes that share a row get the same value. MAX: max, else sum.
+template <int N, bool MAX>
+__device__ __forceinline__ float lane_reduce_rows(float (&v)[N], int lane, int &row) {
+    row = 0;
+#pragma unroll
+    for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float send = up ? v[i] : v[i + n / 2];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+        if (up) row += n / 2;
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 32 / N / 2; o >= 1; o >>= 1) {
+        const float got = __shfl_xor_sync(0xffffffffu, r, o);
+        r = MAX ? fmaxf(r, got) : r + got;
+    }
+    return r;
+}
+
 struct AttnTcParams {
-    CUtensorMap kmap, vmap;   // F32 or BF16 [B * nkv * cap rows, d cols], 128 x 128 boxes
+    CUtensorMap kmap, vmap;   // F32 or BF16 [B * nkv * cap rows, d cols], 128-byte-wide boxes
     AttnArgs a;
 };
 
 // MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
-// KVB: the cache holds BF16 (the split keeps only the exact hi half: two MMAs per K step, and
-// twice as many half-size staging buffers in the same shared memory).
+// KVB: the cache holds BF16 (no lo half: two MMAs per K step, and twice as many half-size
+// staging buffers in the same shared memory).
 template <int D, int NP, int NBUF, bool MP, bool KVB>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
-    constexpr int NB = KVB ? 2 * NBUF : NBUF;          // staging buffers
-    constexpr int kUnit = KVB ? kOpBytes : 2 * kOpBytes;  // bytes of one staged unit
-    constexpr int NH = D / 128;               // 128-wide halves of the head dimension
-    constexpr int NPH = NP / 2;               // rows per thread in the softmax and read-out
+    constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
+    constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit
+    constexpr int kBoxes = kUnit / kBoxBytes;             // TMA boxes per unit
+    constexpr int kBoxCols = 128 / kBoxes;                // elements per box row
+    constexpr int kUCols = KVB ? 64 : 128;                // TMEM columns of one converted unit
+    constexpr int NA = kACols / kUCols;                   // converted-operand regions
+    constexpr int NH = D / 128;                           // 128-wide halves of the head dim
+    constexpr int NPH = NP / kGroups;         // rows per thread in the softmax and read-out
     constexpr int kQBytes = NP * 256;         // one NP x 128 BF16 operand (Q or P, hi or lo)
     const AttnArgs &a = P.a;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                               ~uintptr_t(1023));
-    uint8_t *kvb = sm;                                  // NB x 64 KB: F32 staging, then hi | lo
-    uint8_t *qsm = sm + NB * kUnit;            // [NH][hi, lo] Q operands
+    uint8_t *stg = sm;                                  // NB staging buffers
+    uint8_t *qsm = sm + NB * kUnit;                     // [NH][hi, lo] Q operands
     uint8_t *psm = qsm + NH * 2 * kQBytes;              // [hi, lo] P operand (second buffer)
     float *red = reinterpret_cast<float *>(psm + 2 * kQBytes);   // [4][NP] maxima, [4][NP] sums
     float *mrun = red + 8 * NP;                                  // [NP] running row maxima
     uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NB] staging landed
-    uint64_t *mdone = full + NB;                               // [NB] MMAs of the unit done
-    uint64_t *conv = mdone + NB;                               // [NB] unit split, ready for MMA
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(conv + NB);
+    uint64_t *aready = full + NB;     // [NA] region converted (8 warp arrivals)
+    uint64_t *afree = aready + NA;    // [NA] MMAs reading the region done
+    uint64_t *sdone = afree + NA;     // the pass's score MMAs done
+    uint64_t *pready = sdone + 1;     // [2] P operand written (8 warp arrivals)
+    uint64_t *pfree = pready + 2;     // [2] P.V MMAs reading the P buffer done
+    uint64_t *odone = pfree + 2;      // the pass's P.V MMAs done
+    uint64_t *drain = odone + 1;      // every MMA issued has completed
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     pdl_trigger();
-    if (tid == kConvThreads) {
+    if (tid == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.kmap)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap)) : "memory");
     }
@@ -160,9 +219,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
         return;
     }
-    // A chunk longer than the score memory runs in passes of at most max_tp tiles; each pass
+    // A chunk longer than the score columns runs in passes of at most max_tp tiles; each pass
     // has an exact maximum and its output is merged into running (max, sum, o) registers.
-    const int max_tp = (kTmemCols - NH * NP) / NP;
+    const int max_tp = (kTmemCols - kACols - NH * NP) / NP;
     const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
     if (!MP && n_tiles > max_tp) {           // the host plans single-pass launches within bounds
         if (tid == 0) set_status(a.status, DF_ESHAPE);
@@ -190,14 +249,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         x.h = local % NH;
         return x;
     };
-    // Unit u: K or V of tile t, 128-wide half h, staged by one TMA box of 128 rows.
+    // Unit u: K or V of tile t, 128-wide half h, staged by kBoxes TMA boxes of 128 rows.
     auto issue = [&](int u) {
         const UnitInfo x = decode(u);
-        const bool isV = x.v;
-        const int t = x.t, h = x.h, bf = u % NB;
+        const int bf = u % NB;
+        uint8_t *dst = stg + (size_t)bf * kUnit;
         mbar_expect_tx(&full[bf], (uint32_t)kUnit);
-        tma_load_2d(kvb + (size_t)bf * kUnit, isV ? &P.vmap : &P.kmap, &full[bf], h * 128,
-                    (int)(head_off * a.cap) + c0 + t * kTcKeys, pol);
+        const int y = (int)(head_off * a.cap) + c0 + x.t * kTcKeys;
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+            tma_load_2d(dst + j * kBoxBytes, x.v ? &P.vmap : &P.kmap, &full[bf],
+                        x.h * 128 + j * kBoxCols, y, pol);
     };
 
     // Q rows are loaded before the first TMA boxes are issued, so they do not queue behind them.
@@ -221,15 +283,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         tmem_alloc(tslot, kTmemCols);
         tmem_relinquish();
     }
-    if (tid == kConvThreads) {
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&mdone[i], 1);
-            mbar_init(&conv[i], kConvThreads / 32);
+    int issued = 0;   // TMA units issued (thread 0)
+    if (tid == 0) {
+        for (int i = 0; i < NB; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&aready[i], kConvThreads / 32);
+            mbar_init(&afree[i], 1);
         }
+        mbar_init(sdone, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&pready[i], kConvThreads / 32);
+            mbar_init(&pfree[i], 1);
+        }
+        mbar_init(odone, 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int u = 0; u < min(NB, nU); ++u) issue(u);
+        for (; issued < min(NB, nU); ++issued) issue(issued);
     }
     // Q -> hi/lo operands (rows R..NP-1 zero)
 #pragma unroll
@@ -250,237 +320,258 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int ocol = tpp * NP;                // O^T accumulators after a pass's score tiles
+    const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NP);   // O^T accumulators
+    const uint32_t acol = (uint32_t)(kTmemCols - kACols);             // converted operands
     // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
     // (every score MMA has completed before the first P is written), buffer 1 following it.
     // Several passes: Q stays live, so one buffer after the Q operands.
+    auto p_idx = [&](int t) -> int { return multi ? 0 : (t & 1); };
+    auto p_phase = [&](int t) -> uint32_t { return (uint32_t)((multi ? t : (t >> 1)) & 1); };
     auto p_buf = [&](int t) -> uint32_t {
         return multi ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
     };
-
-    // In-place conversion of a staged unit: every thread reads its 64 F32 values (block rows
-    // from kb/vb, zeros past the chunk's last key), the CTA synchronises, then the values go back
-    // as BF16 hi (first 32 KB) and lo (second 32 KB) in the swizzled K-major operand layout.
-    float xv[64];
-    auto read_unit = [&](int u) {
-        const UnitInfo x = decode(u);
-        const bool isV = x.v;
-        const int t = x.t, h = x.h;
-        const float *st = reinterpret_cast<const float *>(kvb + (size_t)(u % NB) * kUnit);
-        const uint16_t *stb = reinterpret_cast<const uint16_t *>(st);
-        auto stage4 = [&](int kr, int c4) -> float4 {     // 4 staged values at row kr, col c4
-            if constexpr (KVB) {
-                const uint2 w = *reinterpret_cast<const uint2 *>(stb + kr * 128 + c4);
-                return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                                   __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-            } else {
-                return *reinterpret_cast<const float4 *>(st + kr * 128 + c4);
-            }
-        };
-        const float *blkp = isV ? a.vb : a.kb;
-        const int kbase = c0 + t * kTcKeys;
-        if (!isV) {
-#pragma unroll
-            for (int it = 0; it < 16; ++it) {
-                const int kr = it * 8 + warp, key = kbase + kr;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (key < S_cache) v = stage4(kr, 4 * lane);
-                else if (key < c1)
-                    v = __ldcg(reinterpret_cast<const float4 *>(
-                        blkp + (head_off * a.blk + (key - S_cache)) * D + h * 128 + 4 * lane));
-                xv[4 * it] = v.x; xv[4 * it + 1] = v.y; xv[4 * it + 2] = v.z; xv[4 * it + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int wi = it * 8 + warp;
-                const int ob = (wi & 3) * 4 + (lane & 3), qd = (wi >> 2) * 8 + (lane >> 2);
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int kr = 8 * ob + jj, key = kbase + kr;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (key < S_cache) v = stage4(kr, 4 * qd);
-                    else if (key < c1)
-                        v = __ldcg(reinterpret_cast<const float4 *>(
-                            blkp + (head_off * a.blk + (key - S_cache)) * D + h * 128 + 4 * qd));
-                    const int o = 32 * it + 4 * jj;
-                    xv[o] = v.x; xv[o + 1] = v.y; xv[o + 2] = v.z; xv[o + 3] = v.w;
-                }
-            }
-        }
-    };
-    auto write_unit = [&](int u) {
-        const uint32_t hi = smem_u32(kvb + (size_t)(u % NB) * kUnit), lo = hi + kOpBytes;
-        if (!decode(u).v) {
-#pragma unroll
-            for (int it = 0; it < 16; ++it) {
-                const int kr = it * 8 + warp;
-                const __nv_bfloat162 h01 = __floats2bfloat162_rn(xv[4 * it], xv[4 * it + 1]);
-                const __nv_bfloat162 h23 = __floats2bfloat162_rn(xv[4 * it + 2], xv[4 * it + 3]);
-                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-                const __nv_bfloat162 l01 = __floats2bfloat162_rn(xv[4 * it] - f01.x, xv[4 * it + 1] - f01.y);
-                const __nv_bfloat162 l23 = __floats2bfloat162_rn(xv[4 * it + 2] - f23.x, xv[4 * it + 3] - f23.y);
-                const uint32_t o = sw_off(128, kr, 4 * lane);
-                st_shared_v2(hi + o, *reinterpret_cast<const uint32_t *>(&h01),
-                             *reinterpret_cast<const uint32_t *>(&h23));
-                if constexpr (!KVB)
-                    st_shared_v2(lo + o, *reinterpret_cast<const uint32_t *>(&l01),
-                                 *reinterpret_cast<const uint32_t *>(&l23));
-            }
-        } else {
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int wi = it * 8 + warp;
-                const int ob = (wi & 3) * 4 + (lane & 3), qd = (wi >> 2) * 8 + (lane >> 2);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float x[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) x[jj] = xv[32 * it + 4 * jj + i];
-                    uint4 vh, vl;
-                    split8(x, vh, vl);
-                    const uint32_t o = sw_off(128, 4 * qd + i, 8 * ob);
-                    st_shared_v4(hi + o, vh);
-                    if constexpr (!KVB) st_shared_v4(lo + o, vl);
-                }
-            }
-        }
-    };
-    // Three MMAs per 16-wide K step: hi.hi + hi.lo + lo.hi (K = 128 in 8 steps).
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
-    auto mma3 = [&](uint32_t dt, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
-                    bool acc) {
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t oa = kb * kAtomBytes + ks * 32, ob = kb * NP * 128 + ks * 32;
-                mma_bf16(dt, sw128_desc(a_hi + oa), sw128_desc(b_hi + ob), idesc,
-                         (acc || kb || ks) ? 1u : 0u);
-                mma_bf16(dt, sw128_desc(a_hi + oa), sw128_desc(b_lo + ob), idesc, 1u);
-                if constexpr (!KVB) mma_bf16(dt, sw128_desc(a_lo + oa), sw128_desc(b_hi + ob), idesc, 1u);
-            }
-    };
-    auto wait_mma = [&](int u) {   // the MMAs of unit u (and all before it) have completed
-        mbar_wait(&mdone[u % NB], (uint32_t)((u / NB) & 1), abort_flag, a.status);
-        tc_fence_after();
-    };
-
-    const float scale = 1.4426950408889634f / sqrtf((float)D);
-    const int lq = warp & 3, r0 = (warp >> 2) * NPH;
-    const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
-    auto row_ok = [&](int key, int row) {
-        if (key >= c1 || row >= R) return false;
-        return !(a.causal_block && key >= S_cache && key - S_cache > row / rep);
-    };
-    float Mrow[NPH], lsum[NPH];
-    float lrun[MP ? NPH : 1], orun[MP ? NH : 1][MP ? NPH : 1];
-#pragma unroll
-    for (int r = 0; r < NPH; ++r) lsum[r] = 0.f;
-    if constexpr (MP) {
-#pragma unroll
-        for (int r = 0; r < NPH; ++r) {
-            lrun[r] = 0.f;
-#pragma unroll
-            for (int h = 0; h < NH; ++h) orun[h][r] = 0.f;
-        }
-    }
-    if (tid < NP) mrun[tid] = -INFINITY;
 
     if (warp == kConvThreads / 32) {
-        // TMA / MMA issuer: MMAs of unit u once its split has landed; then refill its buffer.
+        // MMA issuer: the products of unit u once its operand is in TMEM (and, for a V unit,
+        // once its tile's P is in shared memory); commits free the operand region, the P buffer,
+        // and signal the end of a pass's scores and outputs.
         if (lane == 0) {
             for (int u = 0; u < nU; ++u) {
-                const uint32_t ph = (uint32_t)((u / NB) & 1);
-                if (!mbar_wait(&conv[u % NB], ph, abort_flag, a.status)) break;
-                tc_fence_after();
-                const uint32_t ahi = smem_u32(kvb + (size_t)(u % NB) * kUnit), alo = ahi + kOpBytes;
                 const UnitInfo x = decode(u);
+                const int r = u % NA;
+                if (!mbar_wait(&aready[r], (uint32_t)((u / NA) & 1), abort_flag, a.status)) break;
+                if (x.v && x.h == 0 &&
+                    !mbar_wait(&pready[p_idx(x.t)], p_phase(x.t), abort_flag, a.status))
+                    break;
+                tc_fence_after();
+                const uint32_t ahi = tmem + acol + (uint32_t)(r * kUCols), alo = ahi + 64;
+                uint32_t d, bhi;
+                bool acc;
                 if (!x.v) {
-                    const uint32_t qhi = smem_u32(qsm + (2 * x.h) * kQBytes), qlo = qhi + kQBytes;
-                    mma3(tmem + (x.t - x.t0) * NP, ahi, alo, qhi, qlo, x.h > 0);
+                    d = tmem + (uint32_t)((x.t - x.t0) * NP);
+                    bhi = smem_u32(qsm + (2 * x.h) * kQBytes);
+                    acc = x.h > 0;
                 } else {
-                    const uint32_t phi = p_buf(x.t), plo = phi + kQBytes;
-                    mma3(tmem + ocol + x.h * NP, ahi, alo, phi, plo, x.t > x.t0);
+                    d = tmem + ocol + (uint32_t)(x.h * NP);
+                    bhi = p_buf(x.t);
+                    acc = x.t > x.t0;
                 }
-                mma_commit(&mdone[u % NB]);
-                if (u + NB < nU) {
-                    if (!mbar_wait(&mdone[u % NB], ph, abort_flag, a.status)) break;
-                    issue(u + NB);
+                const uint32_t blo = bhi + kQBytes;
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {
+                    // K step s: columns 8s.. of the operand, bytes 32*(s%4) of 64-wide block s/4
+                    const uint32_t ob = (uint32_t)((s >> 2) * NP * 128 + (s & 3) * 32);
+                    mma_bf16_ts(d, ahi + 8 * s, sw128_desc(bhi + ob), idesc, (acc || s) ? 1u : 0u);
+                    mma_bf16_ts(d, ahi + 8 * s, sw128_desc(blo + ob), idesc, 1u);
+                    if constexpr (!KVB) mma_bf16_ts(d, alo + 8 * s, sw128_desc(bhi + ob), idesc, 1u);
+                }
+                mma_commit(&afree[r]);
+                const bool last_of_tile = x.h == NH - 1;
+                const bool last_of_pass = last_of_tile && x.t == x.t0 + x.nt - 1;
+                if (!x.v) {
+                    if (last_of_pass) mma_commit(sdone);
+                } else {
+                    if (last_of_tile) mma_commit(&pfree[p_idx(x.t)]);
+                    if (last_of_pass) mma_commit(odone);
                 }
             }
+            // Every MMA this thread issued has completed once the drain barrier flips.
+            mma_commit(drain);
+            mbar_drain(drain, 0);
         }
         __syncwarp();
     } else {
+        const int lq = warp & 3, grp = warp >> 2;
+        const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
+        // Unit u -> BF16 operand in TMEM region u % NA. K unit: this thread's lane is key
+        // 32*lq + lane, its columns the dims [kDT*grp, kDT*grp + kDT) of the unit. V unit: its
+        // lane is dim 32*lq + lane, its columns the keys [kDT*grp, kDT*grp + kDT).
+        auto convert = [&](int u) {
+            const UnitInfo x = decode(u);
+            const int bf = u % NB, r = u % NA;
+            mbar_wait(&full[bf], (uint32_t)((u / NB) & 1), abort_flag, a.status);
+            if (u >= NA) {
+                mbar_wait(&afree[r], (uint32_t)(((u / NA) - 1) & 1), abort_flag, a.status);
+                tc_fence_after();
+            }
+            const uint8_t *st = stg + (size_t)bf * kUnit;
+            const int kbase = c0 + x.t * kTcKeys;
+            const float *blkp = (x.v ? a.vb : a.kb) + head_off * a.blk * (size_t)D + x.h * 128;
+            const uint32_t ta = tmem + lane_addr + acol + (uint32_t)(r * kUCols + (kDT / 2) * grp);
+            // 8 K values per step: 4 hi words at ta + 4*it, 4 lo words at ta + 64 + 4*it. Loops,
+            // not unrolled code: a CTA converts only a few units, so the instructions are fetched
+            // cold and their number, not their issue rate, sets the time.
+            if (!x.v) {
+                const int kr = lq * 32 + lane, key = kbase + kr;
+                const bool cached = key < S_cache;
+                const float *src = (!cached && key < c1) ? blkp + (size_t)(key - S_cache) * D + kDT * grp
+                                                         : nullptr;
+#pragma unroll 2
+                for (int it = 0; it < kDT / 8; ++it) {
+                    const int d0 = kDT * grp + 8 * it;            // first of the step's 8 dims
+                    uint32_t hw[4], lw[4];
+                    float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+                    if (cached) {
+                        if constexpr (KVB) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(
+                                st + (d0 >> 6) * kBoxBytes + kr * 128 + ((((d0 & 63) >> 3) ^ (kr & 7)) << 4));
+                            hw[0] = w.x; hw[1] = w.y; hw[2] = w.z; hw[3] = w.w;
+                        } else {
+                            const uint8_t *row = st + (d0 >> 5) * kBoxBytes + kr * 128;
+                            const int c = (d0 & 31) >> 2;
+                            f0 = *reinterpret_cast<const float4 *>(row + ((c ^ (kr & 7)) << 4));
+                            f1 = *reinterpret_cast<const float4 *>(row + (((c + 1) ^ (kr & 7)) << 4));
+                        }
+                    } else if (src) {
+                        f0 = __ldcg(reinterpret_cast<const float4 *>(src) + 2 * it);
+                        f1 = __ldcg(reinterpret_cast<const float4 *>(src) + 2 * it + 1);
+                    }
+                    if (!KVB || !cached) {
+                        split2(f0.x, f0.y, hw[0], lw[0]);
+                        split2(f0.z, f0.w, hw[1], lw[1]);
+                        split2(f1.x, f1.y, hw[2], lw[2]);
+                        split2(f1.z, f1.w, hw[3], lw[3]);
+                    }
+                    tmem_st4(ta + 4 * it, hw);
+                    if constexpr (!KVB) tmem_st4(ta + 64 + 4 * it, lw);
+                }
+            } else {
+                const int dd = lq * 32 + lane;                // dim within the 128-wide half
+                const int col = dd % kBoxCols;
+                const uint8_t *sb = st + (dd / kBoxCols) * kBoxBytes;
+                auto staged = [&](int kr, int k7) -> float {    // k7 = kr & 7, known statically
+                    if constexpr (KVB) {
+                        const uint16_t bits = *reinterpret_cast<const uint16_t *>(
+                            sb + kr * 128 + (((col >> 3) ^ k7) << 4) + (col & 7) * 2);
+                        return __uint_as_float((uint32_t)bits << 16);
+                    } else {
+                        return *reinterpret_cast<const float *>(
+                            sb + kr * 128 + (((col >> 2) ^ k7) << 4) + (col & 3) * 4);
+                    }
+                };
+#pragma unroll 2
+                for (int it = 0; it < kDT / 8; ++it) {
+                    const int kr0 = kDT * grp + 8 * it;           // 8 keys, kr0 % 8 == 0
+                    float v[8];
+                    if (kbase + kr0 + 7 < S_cache) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = staged(kr0 + e, e);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int key = kbase + kr0 + e;
+                            float xv = 0.f;
+                            if (key < S_cache) xv = staged(kr0 + e, e);
+                            else if (key < c1) xv = __ldcg(blkp + (size_t)(key - S_cache) * D + dd);
+                            v[e] = xv;
+                        }
+                    }
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) split2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
+                    tmem_st4(ta + 4 * it, hw);
+                    if constexpr (!KVB) tmem_st4(ta + 64 + 4 * it, lw);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aready[r]);
+            conv_sync();   // every warp has read the staging buffer: refill it
+            if (tid == 0 && issued < nU) {
+                fence_proxy_async_smem();
+                issue(issued);
+                ++issued;
+            }
+        };
+
+        const float scale = 1.4426950408889634f / sqrtf((float)D);
+        const int r0 = grp * NPH;
+        auto row_ok = [&](int key, int row) {
+            if (key >= c1 || row >= R) return false;
+            return !(a.causal_block && key >= S_cache && key - S_cache > row / rep);
+        };
+        float Mrow[NPH], lsum[NPH];
+        float lrun[MP ? NPH : 1], orun[MP ? NH : 1][MP ? NPH : 1];
+#pragma unroll
+        for (int r = 0; r < NPH; ++r) lsum[r] = 0.f;
+        if constexpr (MP) {
+#pragma unroll
+            for (int r = 0; r < NPH; ++r) {
+                lrun[r] = 0.f;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) orun[h][r] = 0.f;
+            }
+        }
+        if (tid < NP) mrun[tid] = -INFINITY;
+
         for (int u = 0; u < nU; ++u) {
             const UnitInfo x = decode(u);
+            const int p = min(u / upp, n_pass - 1);
             if (x.v && x.h == 0) {
                 const int t = x.t, tl = t - x.t0;
                 if (tl == 0) {
                     // softmax pass 1: exact row maxima over the pass's tiles
-                    wait_mma((u / upp) * upp + x.nt * NH - 1);
+                    mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
+                    tc_fence_after();
                     float mx[NPH];
 #pragma unroll
                     for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
                     for (int tt = 0; tt < x.nt; ++tt) {
-                        float s[NPH];
-                        tmem_rows<NPH>(tmem + lane_addr + tt * NP + r0, s);
+                        float sv[NPH];
+                        tmem_rows<NPH>(tmem + lane_addr + tt * NP + r0, sv);
                         const int key = c0 + (x.t0 + tt) * kTcKeys + lq * 32 + lane;
 #pragma unroll
                         for (int r = 0; r < NPH; ++r)
-                            if (row_ok(key, r0 + r)) mx[r] = fmaxf(mx[r], s[r] * scale);
+                            if (row_ok(key, r0 + r)) mx[r] = fmaxf(mx[r], sv[r] * scale);
                     }
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) {
-                        const float m = warp_max(mx[r]);
-                        if (lane == 0) red[lq * NP + r0 + r] = m;
-                    }
+                    int row;
+                    const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
+                    if ((lane & (32 / NPH - 1)) == 0) red[lq * NP + r0 + row] = m;
                     conv_sync();
 #pragma unroll
                     for (int r = 0; r < NPH; ++r)
                         Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                         fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
-                } else if (multi) {
-                    wait_mma(u - 1);   // one P buffer: the previous tile's P.V MMAs are done
-                } else if (tl >= 2) {
-                    // P operands alternate between two buffers: the one for tile t was last read by
-                    // the P.V MMAs of tile t - 2. Waiting on that older unit is only safe while
-                    // its barrier cannot have completed a later phase (NB > NH); otherwise wait
-                    // on the most recent unit, which covers it.
-                    wait_mma(NB > NH ? u - NH - 1 : u - 1);
                 }
-                // pass 2 for tile t: probabilities -> BF16 hi/lo P operand
-                float s[NPH];
-                tmem_rows<NPH>(tmem + lane_addr + tl * NP + r0, s);
+                // pass 2 for tile t: probabilities -> BF16 hi/lo P operand, once the P.V MMAs
+                // that last read this buffer are done
+                const int prev = multi ? t - 1 : t - 2;
+                if (prev >= 0) {
+                    mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
+                    tc_fence_after();
+                }
+                float sv[NPH];
+                tmem_rows<NPH>(tmem + lane_addr + tl * NP + r0, sv);
                 const int kt = lq * 32 + lane;
                 const int key = c0 + t * kTcKeys + kt;
                 const uint32_t phi = p_buf(t), plo = phi + kQBytes;
 #pragma unroll
                 for (int r = 0; r < NPH; ++r) {
                     const int row = r0 + r;
-                    float p = 0.f;
-                    if (row_ok(key, row) && Mrow[r] != -INFINITY) p = ex2(s[r] * scale - Mrow[r]);
-                    lsum[r] += p;
-                    const uint16_t ph = f32_to_bf16_bits(p);
-                    const uint16_t pl = f32_to_bf16_bits(p - bf16_bits_to_f32(ph));
+                    float pv = 0.f;
+                    if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
+                    lsum[r] += pv;
+                    const uint16_t ph = f32_to_bf16_bits(pv);
+                    const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
                     const uint32_t o = sw_off(NP, row, kt);
                     st_shared_u16(phi + o, ph);
                     st_shared_u16(plo + o, pl);
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
             }
-            mbar_wait(&full[u % NB], (uint32_t)((u / NB) & 1), abort_flag, a.status);
-            read_unit(u);
-            conv_sync();
-            write_unit(u);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[u % NB]);
-            if constexpr (MP) {
-                if (x.v && x.t == x.t0 + x.nt - 1 && x.h == NH - 1) {
-                    // end of a pass: merge its (max, sum, o) into the running values
-                    wait_mma(u);
+            convert(u);
+            if (x.v && x.h == NH - 1 && x.t == x.t0 + x.nt - 1) {
+                // end of a pass: its P.V products are complete
+                mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
+                tc_fence_after();
+                if constexpr (MP) {
+                    // merge the pass's (max, sum, o) into the running values
 #pragma unroll
                     for (int h = 0; h < NH; ++h) {
                         float o[NPH];
@@ -509,11 +600,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
         // read-out: o of this thread's rows, row sums, maxima
         if constexpr (MP) {
-#pragma unroll
-            for (int r = 0; r < NPH; ++r) {
-                const float l = warp_sum(lrun[r]);
-                if (lane == 0) red[4 * NP + lq * NP + r0 + r] = l;
-            }
+            int row;
+            const float l = lane_reduce_rows<NPH, false>(lrun, lane, row);
+            if ((lane & (32 / NPH - 1)) == 0) red[4 * NP + lq * NP + r0 + row] = l;
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
                 const int d = h * 128 + lq * 32 + lane;
@@ -522,12 +611,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     if (r0 + r < R) part[(size_t)(r0 + r) * (D + 2) + d] = orun[h][r];
             }
         } else {
-            wait_mma(nU - 1);
-#pragma unroll
-            for (int r = 0; r < NPH; ++r) {
-                const float l = warp_sum(lsum[r]);
-                if (lane == 0) red[4 * NP + lq * NP + r0 + r] = l;
-            }
+            int row;
+            const float l = lane_reduce_rows<NPH, false>(lsum, lane, row);
+            if ((lane & (32 / NPH - 1)) == 0) red[4 * NP + lq * NP + r0 + row] = l;
             if (lq == 0 && lane == 0)
 #pragma unroll
                 for (int r = 0; r < NPH; ++r) mrun[r0 + r] = Mrow[r];
@@ -548,6 +634,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             part[(size_t)tid * (D + 2) + D] = M;
             part[(size_t)tid * (D + 2) + D + 1] = L;
         }
+        if (tid == 0) {
+            // after an abort: let every TMA load still in flight land before the CTA exits
+            for (int j = max(0, issued - NB); j < issued; ++j)
+                mbar_drain(&full[j % NB], (uint32_t)((j / NB) & 1));
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -558,15 +649,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 }
 
 template <int D, int NP, int NBUF>
-size_t attn_tc_smem() {
-    return 1024 + NBUF * 2 * (size_t)kOpBytes + (D / 128) * 2 * (size_t)NP * 256 +
-           2 * (size_t)NP * 256 + 9 * NP * sizeof(float) + 3 * 2 * NBUF * sizeof(uint64_t) + 16;
-}
-
-template <int D, int NP, int NBUF>
 int launch_tc(const AttnArgs &a, cudaStream_t s) {
-    constexpr int max_keys_one_pass = (kTmemCols - (D / 128) * NP) / NP * kTcKeys;
-    static_assert(attn_tc_smem_bound<D, NP, NBUF>(), "shared memory");
+    constexpr int max_keys_one_pass = (kTmemCols - kACols - (D / 128) * NP) / NP * kTcKeys;
+    constexpr size_t smem = attn_tc_smem_bytes<D, NP, NBUF>();
+    static_assert(smem <= 232448, "shared memory");
     AttnTcParams p;
     memset(&p, 0, sizeof(p));
     const uint64_t rows = (uint64_t)a.B * a.nkv * a.cap;
@@ -575,11 +661,11 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
                     (unsigned long long)rows);
     const CUtensorMapDataType dt = a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int eb = a.kv_bf16 ? 2 : 4;
-    DF_TRY(make_tma_2d(&p.kmap, a.cache_k, dt, eb, D, rows, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE));
-    DF_TRY(make_tma_2d(&p.vmap, a.cache_v, dt, eb, D, rows, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE));
+    const uint32_t box_cols = 128 / eb;       // one 128-byte row per box row
+    DF_TRY(make_tma_2d(&p.kmap, a.cache_k, dt, eb, D, rows, D, box_cols, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    DF_TRY(make_tma_2d(&p.vmap, a.cache_v, dt, eb, D, rows, D, box_cols, 128, CU_TENSOR_MAP_SWIZZLE_128B));
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    const size_t smem = attn_tc_smem<D, NP, NBUF>();
     const bool one = a.chunk <= max_keys_one_pass;
     if (a.kv_bf16)
         return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true>, grid,
