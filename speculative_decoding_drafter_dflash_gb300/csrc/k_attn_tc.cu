@@ -14,13 +14,15 @@
 // into a BF16 operand in tensor memory (TMEM), where the MMA reads it as its A matrix:
 //   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (A = K: lane = key)
 //   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (A = V^T: lane = dim)
-// An F32 cache is split into hi = bf16(x) and lo = bf16(x - hi) (about 16 mantissa bits) and
-// multiplied with three MMAs per 16-wide K step (hi.hi + hi.lo + lo.hi against Q or P, whose
-// hi/lo halves sit in shared memory); a BF16 cache needs only its own values (two MMAs). The
-// converted operand never goes back to shared memory, and the staging buffer is free for the
-// next TMA load as soon as the warps have read it.
+// An F32 cache is split into hi = bf16(x) and lo = bf16(x - hi) (about 16 mantissa bits). Q and
+// P sit in shared memory as one operand of 2*NP rows, their hi rows stacked on their lo rows, so
+// one MMA with N = 2*NP per operand half and 16-wide K step (two for an F32 cache, one for BF16)
+// yields x.hi products in accumulator columns [0, NP) and x.lo products in [NP, 2NP); the two are
+// added when the accumulator is read (hi.hi + hi.lo + lo.hi + lo.lo). The converted operand
+// never goes back to shared memory, and the staging buffer is free for the next TMA load as soon
+// as the warps have read it.
 //
-// A chunk's scores stay in TMEM, up to (512 - 256 - halves*NP)/NP tiles per pass (256 columns
+// A chunk's scores stay in TMEM, up to (512 - 256 - halves*2NP)/2NP tiles per pass (256 columns
 // hold the converted operands), so the softmax maximum is exact per pass: pass 1 takes the row
 // maxima, pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory) right before
 // its V units are converted. A longer chunk runs in several passes whose (max, sum, o) are
@@ -176,14 +178,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     constexpr int NA = kACols / kUCols;                   // converted-operand regions
     constexpr int NH = D / 128;                           // 128-wide halves of the head dim
     constexpr int NPH = NP / kGroups;         // rows per thread in the softmax and read-out
-    constexpr int kQBytes = NP * 256;         // one NP x 128 BF16 operand (Q or P, hi or lo)
+    constexpr int kQBytes = NP * 256;         // NP rows x 128 BF16 (the hi or the lo rows)
+    constexpr int NS = 2 * NP;                // MMA N: hi rows 0..NP-1 stacked on lo rows
     const AttnArgs &a = P.a;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                               ~uintptr_t(1023));
     uint8_t *stg = sm;                                  // NB staging buffers
-    uint8_t *qsm = sm + NB * kUnit;                     // [NH][hi, lo] Q operands
-    uint8_t *psm = qsm + NH * 2 * kQBytes;              // [hi, lo] P operand (second buffer)
+    uint8_t *qsm = sm + NB * kUnit;                     // [NH] stacked hi/lo Q operands
+    uint8_t *psm = qsm + NH * 2 * kQBytes;              // stacked hi/lo P operand (second buffer)
     float *red = reinterpret_cast<float *>(psm + 2 * kQBytes);   // [4][NP] maxima, [4][NP] sums
     float *mrun = red + 8 * NP;                                  // [NP] running row maxima
     uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NB] staging landed
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
     // A chunk longer than the score columns runs in passes of at most max_tp tiles; each pass
     // has an exact maximum and its output is merged into running (max, sum, o) registers.
-    const int max_tp = (kTmemCols - kACols - NH * NP) / NP;
+    const int max_tp = (kTmemCols - kACols - NH * NS) / NS;
     const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
     if (!MP && n_tiles > max_tp) {           // the host plans single-pass launches within bounds
         if (tid == 0) set_status(a.status, DF_ESHAPE);
@@ -310,9 +313,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             uint4 hi, lo;
             split8(qx[i], hi, lo);
             const int h = d >> 7;
-            const uint32_t o = sw_off(NP, r, d & 127);
-            st_shared_v4(smem_u32(qsm + (2 * h) * kQBytes + o), hi);
-            st_shared_v4(smem_u32(qsm + (2 * h + 1) * kQBytes + o), lo);
+            uint8_t *qh = qsm + h * 2 * kQBytes;
+            st_shared_v4(smem_u32(qh + sw_off(NS, r, d & 127)), hi);
+            st_shared_v4(smem_u32(qh + sw_off(NS, NP + r, d & 127)), lo);
         }
     }
     fence_proxy_async_smem();
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NP);   // O^T accumulators
+    const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NS);   // O^T accumulators
     const uint32_t acol = (uint32_t)(kTmemCols - kACols);             // converted operands
     // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
     // (every score MMA has completed before the first P is written), buffer 1 following it.
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     auto p_buf = [&](int t) -> uint32_t {
         return multi ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
     };
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) |
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NS >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
 
     if (warp == kConvThreads / 32) {
@@ -350,21 +353,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 uint32_t d, bhi;
                 bool acc;
                 if (!x.v) {
-                    d = tmem + (uint32_t)((x.t - x.t0) * NP);
-                    bhi = smem_u32(qsm + (2 * x.h) * kQBytes);
+                    d = tmem + (uint32_t)((x.t - x.t0) * NS);
+                    bhi = smem_u32(qsm + x.h * 2 * kQBytes);
                     acc = x.h > 0;
                 } else {
-                    d = tmem + ocol + (uint32_t)(x.h * NP);
+                    d = tmem + ocol + (uint32_t)(x.h * NS);
                     bhi = p_buf(x.t);
                     acc = x.t > x.t0;
                 }
-                const uint32_t blo = bhi + kQBytes;
+                // One MMA per operand half and K step against the stacked [hi; lo] rows: the
+                // columns [0, NP) of d collect x.hi products, [NP, 2NP) x.lo products (their sum
+                // is taken when d is read).
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s) {
                     // K step s: columns 8s.. of the operand, bytes 32*(s%4) of 64-wide block s/4
-                    const uint32_t ob = (uint32_t)((s >> 2) * NP * 128 + (s & 3) * 32);
+                    const uint32_t ob = (uint32_t)((s >> 2) * NS * 128 + (s & 3) * 32);
                     mma_bf16_ts(d, ahi + 8 * s, sw128_desc(bhi + ob), idesc, (acc || s) ? 1u : 0u);
-                    mma_bf16_ts(d, ahi + 8 * s, sw128_desc(blo + ob), idesc, 1u);
                     if constexpr (!KVB) mma_bf16_ts(d, alo + 8 * s, sw128_desc(bhi + ob), idesc, 1u);
                 }
                 mma_commit(&afree[r]);
@@ -520,8 +524,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
                     for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
                     for (int tt = 0; tt < x.nt; ++tt) {
-                        float sv[NPH];
-                        tmem_rows<NPH>(tmem + lane_addr + tt * NP + r0, sv);
+                        float sv[NPH], sl[NPH];
+                        tmem_rows<NPH>(tmem + lane_addr + tt * NS + r0, sv);
+                        tmem_rows<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r) sv[r] += sl[r];
                         const int key = c0 + (x.t0 + tt) * kTcKeys + lq * 32 + lane;
 #pragma unroll
                         for (int r = 0; r < NPH; ++r)
@@ -543,11 +550,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
                     tc_fence_after();
                 }
-                float sv[NPH];
-                tmem_rows<NPH>(tmem + lane_addr + tl * NP + r0, sv);
+                float sv[NPH], sl[NPH];
+                tmem_rows<NPH>(tmem + lane_addr + tl * NS + r0, sv);
+                tmem_rows<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) sv[r] += sl[r];
                 const int kt = lq * 32 + lane;
                 const int key = c0 + t * kTcKeys + kt;
-                const uint32_t phi = p_buf(t), plo = phi + kQBytes;
+                const uint32_t pb = p_buf(t);
 #pragma unroll
                 for (int r = 0; r < NPH; ++r) {
                     const int row = r0 + r;
@@ -556,9 +566,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     lsum[r] += pv;
                     const uint16_t ph = f32_to_bf16_bits(pv);
                     const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
-                    const uint32_t o = sw_off(NP, row, kt);
-                    st_shared_u16(phi + o, ph);
-                    st_shared_u16(plo + o, pl);
+                    st_shared_u16(pb + sw_off(NS, row, kt), ph);
+                    st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -574,8 +583,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     // merge the pass's (max, sum, o) into the running values
 #pragma unroll
                     for (int h = 0; h < NH; ++h) {
-                        float o[NPH];
-                        tmem_rows<NPH>(tmem + lane_addr + ocol + h * NP + r0, o);
+                        float o[NPH], ol[NPH];
+                        tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + r0, o);
+                        tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r) o[r] += ol[r];
 #pragma unroll
                         for (int r = 0; r < NPH; ++r) {
                             const float Mr = mrun[r0 + r], Mn = fmaxf(Mr, Mrow[r]);
@@ -619,8 +631,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (int r = 0; r < NPH; ++r) mrun[r0 + r] = Mrow[r];
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-                float o[NPH];
-                tmem_rows<NPH>(tmem + lane_addr + ocol + h * NP + r0, o);
+                float o[NPH], ol[NPH];
+                tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + r0, o);
+                tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) o[r] += ol[r];
                 const int d = h * 128 + lq * 32 + lane;
 #pragma unroll
                 for (int r = 0; r < NPH; ++r)
@@ -650,7 +665,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
 template <int D, int NP, int NBUF>
 int launch_tc(const AttnArgs &a, cudaStream_t s) {
-    constexpr int max_keys_one_pass = (kTmemCols - kACols - (D / 128) * NP) / NP * kTcKeys;
+    constexpr int max_keys_one_pass = (kTmemCols - kACols - (D / 128) * 2 * NP) / (2 * NP) * kTcKeys;
     constexpr size_t smem = attn_tc_smem_bytes<D, NP, NBUF>();
     static_assert(smem <= 232448, "shared memory");
     AttnTcParams p;
