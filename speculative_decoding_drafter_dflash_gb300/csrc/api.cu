@@ -197,6 +197,7 @@ int check_cache(const df_kv_cache *k, int n_layers, int B, int d) {
 // ---------------------------------------------------------------- DFlash workspace
 struct DFlashWs {
     float *h, *defer, *q, *kb, *vb, *cos_t, *sin_t, *attn_part, *h_final;
+    float *ss_in, *ss_post;   // slice sums of squares of the deferred input / post-attention norms
     size_t defer_floats;
     uint16_t *xp_ctx, *xp_qkv, *xp_o, *xp_ffn, *xp_act, *xp_head;
     ArgTop *amax_part;
@@ -228,6 +229,8 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     const size_t T_blk = (size_t)B * blk, T_ctx = (size_t)B * n_new_max, T_all = T_blk + T_ctx;
     const size_t fc_in = (size_t)c->n_target_layers * H, qt = (size_t)nq * d, kt = (size_t)nkv * d;
     w.h = cv.take<float>(T_blk * H);
+    w.ss_in = cv.take<float>(T_blk * (size_t)pack_slices(H));
+    w.ss_post = cv.take<float>(T_blk * (size_t)pack_slices(H));
     // deferred split-K sums of one projection: S x T x N floats with S * N <= SMs * 128
     w.defer_floats = defer_floats_for((int)T_all, (long long)std::max<size_t>(qt + 2 * kt, H));
     w.defer = cv.take<float>(w.defer_floats);
@@ -277,7 +280,9 @@ int get_ws(void *ws, size_t ws_bytes, size_t need) {
 // The drafter forward. Either block_ids or (last_token, mask id) provides the block tokens.
 // fc, QKV, O and down projections leave split-K partial sums that the next kernel adds in
 // (hidden_norm pack, q/k-norm + RoPE, fused residual + RMSNorm pack); gate/up writes packed
-// SwiGLU activations directly.
+// SwiGLU activations directly. The input and post-attention RMSNorms are deferred: their row
+// prologue packs x * w and per-slice sums of squares, and the QKV (block rows) and gate/up
+// projections multiply their outputs by 1/rms.
 int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
                         const df_kv_cache *cache, const int32_t *block_ids,
                         const int32_t *last_token, const float *target_hidden,
@@ -373,8 +378,17 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         p.ldp = H;
         p.T = T_blk;
         p.K = H;
+        p.ss_out = ws.ss_in;
         p.status = st;
         DF_TRY(launch_pack(p, s));
+        // 1/rms of a deferred norm as the row scale of the projection that consumes it
+        auto row_scale = [&](GemmArgs &g, const float *ss) {
+            g.rs_ss = ss;
+            g.rs_n = pack_slices(H);
+            g.rs_rows = T_blk;
+            g.rs_inv_k = 1.f / (float)H;
+            g.rs_eps = c->rms_eps;
+        };
 
         GemmArgs g;
         g.W0 = L.wq;
@@ -388,6 +402,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.X = ws.xp_qkv;
         g.ldx = H;
         g.T = T_all;
+        row_scale(g, ws.ss_in);
         int S_qkv = 0;
         DF_TRY(deferred(g, T_all, Nqkv, "gemm_qkv", &S_qkv));
 
@@ -470,6 +485,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         pf.ldp = H;
         pf.T = T_blk;
         pf.K = H;
+        pf.ss_out = ws.ss_post;
         pf.status = st;
         DF_TRY(launch_pack(pf, s));
 
@@ -488,6 +504,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gu.ldpo = I;
         gu.status = st;
         gu.name = "gemm_gate_up";
+        row_scale(gu, ws.ss_post);
         DF_TRY(launch_gemm_tc(gu, ws.tc, s));
 
         GemmArgs gd;

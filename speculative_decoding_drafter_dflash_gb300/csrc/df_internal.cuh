@@ -198,8 +198,15 @@ struct PackArgs {
     int n_part = 0;
     size_t part_stride = 0;          // floats between splits
     int ldpart = 0;                  // floats between rows of one split
+    // Deferred RMSNorm (needs norm_w and pack, no y_out): the row is split over pack_slices(K)
+    // CTAs without a cluster; pack receives x * norm_w (the numerator only) and ss_out[t * S + j]
+    // the sum of x^2 over slice j of row t. The 1/rms factor is applied by the consuming
+    // projection as a row scale (GemmArgs::rs_*), which the linearity of the projection allows.
+    float *ss_out = nullptr;
 };
 int launch_pack(const PackArgs &a, cudaStream_t s);
+// Number of CTAs (slices) a row of K elements is split over by the row prologue.
+int pack_slices(int K);
 
 // Mixture-of-experts FFN (router, top-k, routed + shared expert SwiGLUs) over T <= 16 rows.
 constexpr int kMoeMaxRows = 16;
@@ -256,6 +263,13 @@ struct GemmArgs {
     int ldpo = 0;
     ArgTop *part = nullptr;          // EPI_ARGMAX: partial states [grid, T]
     int *n_part = nullptr;           // EPI_ARGMAX: host-visible count of partial rows written
+    // Row scale of the outputs (any epilogue): rows t < rs_rows are multiplied by
+    // 1 / sqrt((rs_ss[t*rs_n] + ... + rs_ss[t*rs_n + rs_n-1]) * rs_inv_k + rs_eps), the partial
+    // sums taken in order: the RMSNorm factor of an input row whose numerator x * w was packed
+    // by a deferred-norm row prologue. Rows at or past rs_rows are left as they are.
+    const float *rs_ss = nullptr;
+    int rs_n = 0, rs_rows = 0;
+    float rs_inv_k = 0.f, rs_eps = 0.f;
 };
 
 // Scratch of the tensor-core projections: partial tiles of tiles shared by several CTAs, and

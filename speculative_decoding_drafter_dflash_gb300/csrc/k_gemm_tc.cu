@@ -74,6 +74,9 @@ struct TcParams {
     float *scratch;
     int *counters;
     int32_t *status;
+    const float *rs_ss;
+    int rs_n, rs_rows;
+    float rs_inv_k, rs_eps;
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -158,15 +161,19 @@ struct EpiSmem {
     float *xs;      // [128][kTokChunk]
     ArgTop *wst;    // [4][kTokChunk]
     ArgTop *st;     // [T]
+    float *rs;      // [T] row scales (when rs_ss is set)
 };
 
 // Apply the epilogue op to tokens [t0, t0 + kTokChunk) of tile m for this thread's row r.
 // Every epilogue thread calls this (the SwiGLU and argmax paths synchronise the 128 threads).
 __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, int m, int r,
-                                          int q, int lane, int t0, const float (&y)[kTokChunk],
+                                          int q, int lane, int t0, const float (&y0)[kTokChunk],
                                           int split) {
     int n_out, s;
     const bool valid = tile_row(p, m, r, n_out, s);
+    float y[kTokChunk];
+#pragma unroll
+    for (int i = 0; i < kTokChunk; ++i) y[i] = p.rs_ss ? y0[i] * es.rs[min(t0 + i, p.T - 1)] : y0[i];
     if (p.epi == EPI_STORE || p.epi == EPI_RESID) {
         if (valid) {
             float *out = p.out + (size_t)split * p.part_stride;
@@ -242,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     es.xs = reinterpret_cast<float *>(tmem_slot + 4);
     es.wst = reinterpret_cast<ArgTop *>(es.xs + kBM * kTokChunk);
     es.st = es.wst + 4 * kTokChunk;
+    es.rs = reinterpret_cast<float *>(es.st + p.T);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -410,6 +418,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
     } else {
         pdl_wait();
+        if (p.rs_ss) {
+            for (int t = threadIdx.x - 64; t < p.T; t += 128) {
+                float sc = 1.f;
+                if (t < p.rs_rows) {
+                    float acc = 0.f;
+                    for (int j = 0; j < p.rs_n; ++j) acc += p.rs_ss[(size_t)t * p.rs_n + j];
+                    sc = 1.f / sqrtf(acc * p.rs_inv_k + p.rs_eps);
+                }
+                es.rs[t] = sc;
+            }
+            epi_bar();
+        }
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
         const int r = q * 32 + lane;     // tile row of this thread
         int acc = 0;
@@ -611,6 +631,11 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
     p.scratch = sc.partials;
     p.counters = sc.counters;
     p.status = a.status;
+    p.rs_ss = a.rs_ss;
+    p.rs_n = a.rs_n;
+    p.rs_rows = a.rs_rows;
+    p.rs_inv_k = a.rs_inv_k;
+    p.rs_eps = a.rs_eps;
     if (!p.splits && (size_t)p.G * 2 * T * kBM > sc.partial_floats)
         return fail(DF_EWORKSPACE, "GEMM scratch too small (%d tokens)", T);
     if (a.defer && (a.epi != EPI_STORE || a.part_stride < (size_t)T * a.ldo))
@@ -619,7 +644,7 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
         return fail(DF_EWORKSPACE, "GEMM tile counters too few (%d tiles)", p.n_tiles);
     size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 5) * 8 + 16 +
                   (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
-                  (size_t)T * sizeof(ArgTop) + 64;
+                  (size_t)T * sizeof(ArgTop) + (size_t)T * sizeof(float) + 64;
     if (G_out) *G_out = a.defer ? p.splits : p.G;
     return launch_k(a.name, gemm_tc_kernel, dim3(p.G), dim3(kThreads), smem, s, p);
 }
@@ -641,6 +666,10 @@ int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *
         if (a.out) c.out = a.out + (size_t)t0 * a.ldo;
         if (a.resid) c.resid = a.resid + (size_t)t0 * a.ldr;
         if (a.pack_out) c.pack_out = a.pack_out + (size_t)2 * t0 * a.ldpo;
+        if (a.rs_ss) {
+            c.rs_ss = a.rs_ss + (size_t)t0 * a.rs_n;
+            c.rs_rows = std::max(0, a.rs_rows - t0);
+        }
         DF_TRY(launch_chunk(c, sc, s, n_partials_out));
     }
     return DF_OK;

@@ -154,7 +154,22 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a, int 
         }
     }
     float inv = 1.f;
-    if (a.norm_w) {
+    if (a.norm_w && a.ss_out) {
+        // deferred norm: this slice's sum of squares, warps in order; no cluster exchange
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < NV; ++u)
+            ss = fmaf(x[u].x, x[u].x, fmaf(x[u].y, x[u].y, fmaf(x[u].z, x[u].z, fmaf(x[u].w, x[u].w, ss))));
+        ss = warp_sum(ss);
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        if (l == 0) red[w] = ss;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+            for (int i = 0; i < kPackThreads / 32; ++i) tot += red[i];
+            a.ss_out[(size_t)t * cl + rank] = tot;
+        }
+    } else if (a.norm_w) {
         float ss = 0.f;
 #pragma unroll
         for (int u = 0; u < NV; ++u)
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a, int 
         }
     }
     // peers may still be reading red[32] through distributed shared memory
-    if (a.norm_w && cl > 1) cg::this_cluster().sync();
+    if (a.norm_w && !a.ss_out && cl > 1) cg::this_cluster().sync();
 }
 
 bool aligned_for_vec(const PackArgs &a) {
@@ -223,18 +238,29 @@ bool aligned_for_vec(const PackArgs &a) {
 
 }  // namespace
 
+int pack_slices(int K) {
+    // Up to 8 CTAs per row, keeping at least 64 4-element groups per CTA.
+    const int K4 = K / 4;
+    int cl = 8;
+    while (cl > 1 && (K4 % cl != 0 || K4 / cl < 64)) cl >>= 1;
+    return cl;
+}
+
 int launch_pack(const PackArgs &a, cudaStream_t s) {
     if (a.T <= 0) return DF_OK;
+    if (a.ss_out && (!a.norm_w || !a.pack || a.y_out || !aligned_for_vec(a) ||
+                     (a.K / 4) / pack_slices(a.K) > 16 * kPackThreads))
+        return fail(DF_EINVAL, "deferred-norm row prologue: needs norm_w and pack, no y_out, "
+                               "16-byte aligned rows");
     if (aligned_for_vec(a)) {
-        // Split each row over up to 8 CTAs of a cluster, keeping at least 64 4-element groups
-        // per CTA.
+        // Split each row over up to 8 CTAs (a cluster, when the slices exchange their sums of
+        // squares; independent CTAs when the norm is deferred to the consumer).
         const int K4 = a.K / 4;
-        int cl = 8;
-        while (cl > 1 && (K4 % cl != 0 || K4 / cl < 64)) cl >>= 1;
+        const int cl = pack_slices(a.K);
         const int nv = (K4 / cl + kPackThreads - 1) / kPackThreads;
         const dim3 g(a.T * cl), b(kPackThreads);
         if (nv <= 16) {
-            if (cl > 1) {
+            if (cl > 1 && !a.ss_out) {
                 if (nv <= 1) return launch_kc("pack_kernel", pack_vec_kernel<1>, g, b, 0, cl, s, a, cl);
                 if (nv <= 2) return launch_kc("pack_kernel", pack_vec_kernel<2>, g, b, 0, cl, s, a, cl);
                 if (nv <= 4) return launch_kc("pack_kernel", pack_vec_kernel<4>, g, b, 0, cl, s, a, cl);
