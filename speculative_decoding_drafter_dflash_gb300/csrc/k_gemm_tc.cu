@@ -106,11 +106,12 @@ __device__ __forceinline__ int cta_of(long long x, const TcParams &p) {
 
 // The segments (tile m, K blocks [k0, k1), split index) a CTA works on, in order. Stream-K:
 // one contiguous range of the (tile, K block) space. Split mode: units blockIdx.x + i * G.
+template <bool FIX>
 struct Work {
     long long x, end;
     int u;
     __device__ __forceinline__ void init(const TcParams &p) {
-        if (p.splits) {
+        if constexpr (!FIX) {
             u = blockIdx.x;
         } else {
             x = kb_start(blockIdx.x, p);
@@ -118,7 +119,7 @@ struct Work {
         }
     }
     __device__ __forceinline__ bool next(const TcParams &p, int &m, int &k0, int &k1, int &split) {
-        if (p.splits) {
+        if constexpr (!FIX) {
             if (u >= p.n_units) return false;
             m = u / p.splits;
             split = u - m * p.splits;
@@ -166,6 +167,7 @@ struct EpiSmem {
 
 // Apply the epilogue op to tokens [t0, t0 + kTokChunk) of tile m for this thread's row r.
 // Every epilogue thread calls this (the SwiGLU and argmax paths synchronise the 128 threads).
+template <int EPI>
 __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, int m, int r,
                                           int q, int lane, int t0, const float (&y0)[kTokChunk],
                                           int split) {
@@ -174,7 +176,7 @@ __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, 
     float y[kTokChunk];
 #pragma unroll
     for (int i = 0; i < kTokChunk; ++i) y[i] = p.rs_ss ? y0[i] * es.rs[min(t0 + i, p.T - 1)] : y0[i];
-    if (p.epi == EPI_STORE || p.epi == EPI_RESID) {
+    if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
         if (valid) {
             float *out = p.out + (size_t)split * p.part_stride;
 #pragma unroll
@@ -182,12 +184,12 @@ __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, 
                 int t = t0 + i;
                 if (t < p.T) {
                     float v = y[i];
-                    if (p.epi == EPI_RESID) v += p.resid[(size_t)t * p.ldr + n_out];
+                    if constexpr (EPI == EPI_RESID) v += p.resid[(size_t)t * p.ldr + n_out];
                     out[(size_t)t * p.ldo + n_out] = v;
                 }
             }
         }
-    } else if (p.epi == EPI_SWIGLU) {
+    } else if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll
         for (int i = 0; i < kTokChunk; ++i) es.xs[r * kTokChunk + i] = y[i];
         epi_bar();
@@ -232,6 +234,11 @@ __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, 
     }
 }
 
+// EPI: the epilogue; FIX: whether a tile may be shared by several CTAs (stream-K work split,
+// partial tiles finished by the last CTA). Each launch runs one instantiation, so its code holds
+// only the paths it executes: a projection runs for a few microseconds and its instructions are
+// fetched cold, so code that is never taken still costs.
+template <int EPI, bool FIX>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // (tile, k-block) cursor: one TMA issue per k-block must stay far cheaper than the
             // ~700 cycles a 16 KB weight tile takes to stream into one SM.
             struct Cursor {
-                Work w;
+                Work<FIX> w;
                 int m, kb, k1, split, s, row0;
                 bool valid;
             };
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            Work w;
+            Work<FIX> w;
             w.init(p);
             int m, k0, k1, split;
             while (ok && w.next(p, m, k0, k1, split)) {
@@ -434,12 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int r = q * 32 + lane;     // tile row of this thread
         int acc = 0;
         uint32_t aphase = 0;
-        Work w;
+        Work<FIX> w;
         w.init(p);
         int m, k0, k1, split;
         while (w.next(p, m, k0, k1, split)) {
             if (k0 >= k1) continue;
-            const bool whole = p.splits || (k0 == 0 && k1 == p.kbt);
+            const bool whole = !FIX || (k0 == 0 && k1 == p.kbt);
             const int slot = (!p.splits && kb_start(blockIdx.x, p) / p.kbt == m) ? 0 : 1;
             const bool got = mbar_wait(&tfull[acc], aphase, abort_flag, p.status);
             if (epi_any(!got)) break;   // all four epilogue warps leave together
@@ -460,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 for (int i = 0; i < kTokChunk; ++i)
                     y[i] = __uint_as_float(v[2 * i]) + __uint_as_float(v[2 * i + 1]);
                 if (whole) {
-                    epi_apply(p, es, m, r, q, lane, c * kTokChunk, y, split);
-                } else {
+                    epi_apply<EPI>(p, es, m, r, q, lane, c * kTokChunk, y, split);
+                } else if constexpr (FIX) {
 #pragma unroll
                     for (int i = 0; i < kTokChunk; ++i) {
                         int t = c * kTokChunk + i;
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 acc = 0;
                 aphase ^= 1u;
             }
-            if (!whole) {
+            if (FIX && !whole) {
                 // Stream-K fixup: the last CTA of this tile sums the partials in CTA order.
                 __threadfence();
                 epi_bar();
@@ -516,13 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                                 for (int i = 0; i < kTokChunk; ++i) y[i] += v8[j][i];
                         }
-                        epi_apply(p, es, m, r, q, lane, c * kTokChunk, y, split);
+                        epi_apply<EPI>(p, es, m, r, q, lane, c * kTokChunk, y, split);
                     }
                     if (r == 0) p.counters[m] = 0;
                 }
             }
         }
-        if (p.epi == EPI_ARGMAX) {
+        if constexpr (EPI == EPI_ARGMAX) {
             epi_bar();
             for (int t = threadIdx.x - 64; t < p.T; t += 128)
                 p.part[(size_t)blockIdx.x * p.T + t] = es.st[t];
@@ -646,7 +653,24 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
                   (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
                   (size_t)T * sizeof(ArgTop) + (size_t)T * sizeof(float) + 64;
     if (G_out) *G_out = a.defer ? p.splits : p.G;
-    return launch_k(a.name, gemm_tc_kernel, dim3(p.G), dim3(kThreads), smem, s, p);
+    const dim3 grid(p.G), block(kThreads);
+    const bool fix = p.splits == 0;
+    switch (a.epi) {
+        case EPI_STORE:
+            return fix ? launch_k(a.name, gemm_tc_kernel<EPI_STORE, true>, grid, block, smem, s, p)
+                       : launch_k(a.name, gemm_tc_kernel<EPI_STORE, false>, grid, block, smem, s, p);
+        case EPI_RESID:
+            return fix ? launch_k(a.name, gemm_tc_kernel<EPI_RESID, true>, grid, block, smem, s, p)
+                       : launch_k(a.name, gemm_tc_kernel<EPI_RESID, false>, grid, block, smem, s, p);
+        case EPI_SWIGLU:
+            return fix ? launch_k(a.name, gemm_tc_kernel<EPI_SWIGLU, true>, grid, block, smem, s, p)
+                       : launch_k(a.name, gemm_tc_kernel<EPI_SWIGLU, false>, grid, block, smem, s, p);
+        case EPI_ARGMAX:
+            return fix ? launch_k(a.name, gemm_tc_kernel<EPI_ARGMAX, true>, grid, block, smem, s, p)
+                       : launch_k(a.name, gemm_tc_kernel<EPI_ARGMAX, false>, grid, block, smem, s, p);
+        default:
+            return fail(DF_EINVAL, "unknown projection epilogue %d", a.epi);
+    }
 }
 
 }  // namespace
