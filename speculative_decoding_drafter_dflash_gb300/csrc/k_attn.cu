@@ -95,6 +95,34 @@ __global__ void qk_rope_kernel(QkArgs a) {
                             : (is_q ? head * d
                                     : (is_k ? a.nq * d + head * d : (a.nq + a.nkv) * d + head * d));
 
+    // The norm weights and this row's cos/sin are requested before the projection partials,
+    // so they arrive in the same round trip.
+    const bool rotate = !is_gate && slot < a.nq + a.nkv;
+    float nwv[8], cv[8], sv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        nwv[u] = 1.f;
+        cv[u] = 1.f;
+        sv[u] = 0.f;
+    }
+    if (rotate) {
+        const float *nw = is_q ? a.q_norm : a.k_norm;
+        const int tslot = is_block ? i : a.blk + i;
+        const float *ct = a.cos_t + ((size_t)b * (a.blk + a.n_new_max) + tslot) * half;
+        const float *st = a.sin_t + ((size_t)b * (a.blk + a.n_new_max) + tslot) * half;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = lane + 32 * u;
+            if (u < ept) {
+                if (nw) nwv[u] = nw[e];
+                if (e < a.rot) {
+                    const int f = e < half ? e : e - half;
+                    cv[u] = ct[f];
+                    sv[u] = st[f];
+                }
+            }
+        }
+    }
     float x[8];
     if (a.part) {
         // deferred split-K: every split is loaded first, then summed in split order
@@ -127,9 +155,8 @@ __global__ void qk_rope_kernel(QkArgs a) {
         return;
     }
 
-    if (!(slot >= a.nq + a.nkv)) {   // q or k: per-head RMSNorm, then RoPE
-        const float *nw = is_q ? a.q_norm : a.k_norm;
-        if (nw) {
+    if (rotate) {   // q or k: per-head RMSNorm, then RoPE
+        if (is_q ? a.q_norm : a.k_norm) {
             float ss = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) ss = fmaf(x[u], x[u], ss);
@@ -137,21 +164,18 @@ __global__ void qk_rope_kernel(QkArgs a) {
             float inv = 1.f / sqrtf(ss / (float)d + a.eps);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (u < ept) x[u] = x[u] * inv * nw[lane + 32 * u];
+                if (u < ept) x[u] = x[u] * inv * nwv[u];
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
             if (u < ept) buf[lane + 32 * u] = x[u];
         __syncwarp();
-        const int tslot = is_block ? i : a.blk + i;
-        const float *ct = a.cos_t + ((size_t)b * (a.blk + a.n_new_max) + tslot) * half;
-        const float *st = a.sin_t + ((size_t)b * (a.blk + a.n_new_max) + tslot) * half;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             int e = lane + 32 * u;
             if (u < ept && e < a.rot) {
-                if (e < half) x[u] = buf[e] * ct[e] - buf[e + half] * st[e];
-                else x[u] = buf[e] * ct[e - half] + buf[e - half] * st[e - half];
+                if (e < half) x[u] = buf[e] * cv[u] - buf[e + half] * sv[u];
+                else x[u] = buf[e] * cv[u] + buf[e - half] * sv[u];
             }
         }
     }
@@ -518,31 +542,52 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
     const size_t head_off = (size_t)b * a.nkv + g;
     const float *allp = a.part + head_off * a.n_chunks * (size_t)R * (D + 2);
     const int NC = a.n_chunks;
-    float M = -INFINITY;
-    for (int c = lane; c < NC; c += 32) M = fmaxf(M, allp[((size_t)c * R + r2) * (D + 2) + D]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int c = lane; c < NC; c += 32) {
-        const float *pc = allp + ((size_t)c * R + r2) * (D + 2);
-        const float mc = pc[D];
-        if (mc != -INFINITY) L += pc[D + 1] * exp2f(mc - M);
-    }
-    L = warp_sum(L);
-    const float invL = L > 0.f ? 1.f / L : 0.f;
     float y = 0.f;
-    for (int c0 = 0; c0 < NC; c0 += 32) {
-        float wl = 0.f;
-        if (c0 + lane < NC) {
-            const float mc = allp[((size_t)(c0 + lane) * R + r2) * (D + 2) + D];
-            wl = mc == -INFINITY ? 0.f : exp2f(mc - M) * invL;
+    if (NC <= 32) {
+        // one round trip: every lane's (m, l) of chunk `lane` and the 32 partial outputs of its
+        // dim are requested before any is used
+        float mc = -INFINITY, lc = 0.f;
+        if (lane < NC) {
+            const float *pc = allp + ((size_t)lane * R + r2) * (D + 2);
+            mc = pc[D];
+            lc = pc[D + 1];
         }
-        const int cn = min(32, NC - c0);
         float ov[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            ov[j] = j < cn ? allp[((size_t)(c0 + j) * R + r2) * (D + 2) + e] : 0.f;
+            ov[j] = j < NC ? allp[((size_t)j * R + r2) * (D + 2) + e] : 0.f;
+        const float M = warp_max(mc);
+        const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
+        const float L = warp_sum(lc * w);
+        const float wl = L > 0.f ? w / L : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) y = fmaf(__shfl_sync(0xffffffffu, wl, j), ov[j], y);
+    } else {
+        float M = -INFINITY;
+        for (int c = lane; c < NC; c += 32) M = fmaxf(M, allp[((size_t)c * R + r2) * (D + 2) + D]);
+        M = warp_max(M);
+        float L = 0.f;
+        for (int c = lane; c < NC; c += 32) {
+            const float *pc = allp + ((size_t)c * R + r2) * (D + 2);
+            const float mc = pc[D];
+            if (mc != -INFINITY) L += pc[D + 1] * exp2f(mc - M);
+        }
+        L = warp_sum(L);
+        const float invL = L > 0.f ? 1.f / L : 0.f;
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+            float wl = 0.f;
+            if (c0 + lane < NC) {
+                const float mc = allp[((size_t)(c0 + lane) * R + r2) * (D + 2) + D];
+                wl = mc == -INFINITY ? 0.f : exp2f(mc - M) * invL;
+            }
+            const int cn = min(32, NC - c0);
+            float ov[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                ov[j] = j < cn ? allp[((size_t)(c0 + j) * R + r2) * (D + 2) + e] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) y = fmaf(__shfl_sync(0xffffffffu, wl, j), ov[j], y);
+        }
     }
     const int i = r2 / rep, h = g * rep + r2 % rep;
     const size_t t = (size_t)b * a.blk + i;
