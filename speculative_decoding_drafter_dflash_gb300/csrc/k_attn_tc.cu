@@ -160,6 +160,34 @@ __device__ __forceinline__ float lane_reduce_rows(float (&v)[N], int lane, int &
     return r;
 }
 
+// tcgen05.ld of NPH columns without the wait, so several loads share one tcgen05.wait::ld.
+template <int NPH>
+__device__ __forceinline__ void tmem_ld_nowait(uint32_t taddr, uint32_t (&r)[NPH]) {
+    if constexpr (NPH == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+    } else if constexpr (NPH == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                       "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr));
+    } else {
+        static_assert(NPH == 16, "rows per thread");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+              "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    }
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 struct AttnTcParams {
     CUtensorMap kmap, vmap;   // F32 or BF16 [B * nkv * cap rows, d cols], 128-byte-wide boxes
     AttnArgs a;
@@ -524,15 +552,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
                     for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
                     for (int tt = 0; tt < x.nt; ++tt) {
-                        float sv[NPH], sl[NPH];
-                        tmem_rows<NPH>(tmem + lane_addr + tt * NS + r0, sv);
-                        tmem_rows<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
-#pragma unroll
-                        for (int r = 0; r < NPH; ++r) sv[r] += sl[r];
+                        uint32_t sh[NPH], sl[NPH];
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
+                        tmem_ld_wait();
                         const int key = c0 + (x.t0 + tt) * kTcKeys + lq * 32 + lane;
 #pragma unroll
                         for (int r = 0; r < NPH; ++r)
-                            if (row_ok(key, r0 + r)) mx[r] = fmaxf(mx[r], sv[r] * scale);
+                            if (row_ok(key, r0 + r))
+                                mx[r] = fmaxf(mx[r], (__uint_as_float(sh[r]) + __uint_as_float(sl[r])) * scale);
                     }
                     int row;
                     const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
@@ -550,11 +578,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
                     tc_fence_after();
                 }
-                float sv[NPH], sl[NPH];
-                tmem_rows<NPH>(tmem + lane_addr + tl * NS + r0, sv);
-                tmem_rows<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                float sv[NPH];
+                {
+                    uint32_t sh[NPH], sl[NPH];
+                    tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
+                    tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int r = 0; r < NPH; ++r) sv[r] += sl[r];
+                    for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
+                }
                 const int kt = lq * 32 + lane;
                 const int key = c0 + t * kTcKeys + kt;
                 const uint32_t pb = p_buf(t);
@@ -631,11 +663,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (int r = 0; r < NPH; ++r) mrun[r0 + r] = Mrow[r];
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-                float o[NPH], ol[NPH];
-                tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + r0, o);
-                tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
+                float o[NPH];
+                {
+                    uint32_t oh[NPH], ol[NPH];
+                    tmem_ld_nowait<NPH>(tmem + lane_addr + ocol + h * NS + r0, oh);
+                    tmem_ld_nowait<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int r = 0; r < NPH; ++r) o[r] += ol[r];
+                    for (int r = 0; r < NPH; ++r) o[r] = __uint_as_float(oh[r]) + __uint_as_float(ol[r]);
+                }
                 const int d = h * 128 + lq * 32 + lane;
 #pragma unroll
                 for (int r = 0; r < NPH; ++r)
