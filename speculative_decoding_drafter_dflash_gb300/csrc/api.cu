@@ -456,6 +456,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         at.pack = ws.xp_o;
         at.status = st;
         at.kv_bf16 = c->kv_bf16 ? 1 : 0;
+        at.early_kv = 1;   // seq_len moves only at the end of the forward
         DF_TRY(launch_attn(at, s));
 
         GemmArgs go;

@@ -350,6 +350,10 @@ struct AttnArgs {
     uint16_t *pack;          // packed output [2*B*blk, nq*d] (or null)
     float *out;              // F32 output [B*blk, nq*d] (or null)
     int32_t *status;
+    // 1: seq_len is not written by any kernel of the same stream before this one (the DFlash
+    // forward advances it only at its end), so cache rows below it may be loaded before the
+    // wait for the preceding kernel.
+    int early_kv;
 };
 void attn_plan(AttnArgs &a, int max_keys);
 size_t attn_part_floats(const AttnArgs &a);

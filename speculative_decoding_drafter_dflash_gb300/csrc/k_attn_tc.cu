@@ -230,10 +230,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const size_t head_off = (size_t)b * a.nkv + g;
+    const uint64_t pol = policy_evict_first();
     pdl_trigger();
+    // Units 0 and 1 are the K units of the chunk's first two tiles when the head dim is 128 (one
+    // half per tile) and those tiles exist. Rows that predate this round do not depend on the
+    // preceding kernels, so when both the tile and (for unit 1) the chunk's second tile lie below
+    // seq_len they are requested before the wait, behind the q/k norm kernel.
+    int n_early = 0;
     if (tid == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.kmap)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap)) : "memory");
+        for (int i = 0; i < NB; ++i) mbar_init(&full[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (NH == 1 && a.early_kv) {
+            const long long old = a.seq_len[b];
+            const long long c0e = (long long)chunk * a.chunk;
+            for (int t = 0; t < min(2, NB) && (t + 1) * kTcKeys <= a.chunk &&
+                            c0e + (long long)(t + 1) * kTcKeys <= old && c0e + (t + 1) * kTcKeys <= a.cap;
+                 ++t) {
+                uint8_t *dst = stg + (size_t)t * kUnit;
+                mbar_expect_tx(&full[t], (uint32_t)kUnit);
+                const int y = (int)(head_off * a.cap + c0e) + t * kTcKeys;
+#pragma unroll
+                for (int j = 0; j < kBoxes; ++j)
+                    tma_load_2d(dst + j * kBoxBytes, &P.kmap, &full[t], j * kBoxCols, y, pol);
+                n_early = t + 1;
+            }
+        }
     }
     pdl_wait();
     const int rep = a.nq / a.nkv;
@@ -244,7 +268,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int S = S_cache + (a.kb ? a.blk : 0);
     const int c0 = min(S, chunk * a.chunk), c1 = min(S, c0 + a.chunk);
     const int n_tiles = (c1 - c0 + kTcKeys - 1) / kTcKeys;
-    const size_t head_off = (size_t)b * a.nkv + g;
     float *part = a.part + ((head_off * a.n_chunks + chunk) * (size_t)R) * (D + 2);
     if (n_tiles == 0) {
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
@@ -255,7 +278,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int max_tp = (kTmemCols - kACols - NH * NS) / NS;
     const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
     if (!MP && n_tiles > max_tp) {           // the host plans single-pass launches within bounds
-        if (tid == 0) set_status(a.status, DF_ESHAPE);
+        if (tid == 0) {
+            set_status(a.status, DF_ESHAPE);
+            for (int j = 0; j < n_early; ++j) mbar_drain(&full[j], 0);
+        }
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
         return;
     }
@@ -263,7 +289,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int upp = 2 * tpp * NH;                        // units per full pass
     const int nU = 2 * n_tiles * NH;
     const bool multi = MP && n_pass > 1;
-    const uint64_t pol = policy_evict_first();
     // Unit u of pass p: the pass's K units (tile-major, then 128-wide half), then its V units.
     struct UnitInfo {
         int t0, nt, v, t, h;
@@ -314,9 +339,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         tmem_alloc(tslot, kTmemCols);
         tmem_relinquish();
     }
-    int issued = 0;   // TMA units issued (thread 0)
+    int issued = n_early;   // TMA units issued (thread 0)
     if (tid == 0) {
-        for (int i = 0; i < NB; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < NA; ++i) {
             mbar_init(&aready[i], kConvThreads / 32);
             mbar_init(&afree[i], 1);
