@@ -24,9 +24,10 @@
 //
 // A chunk's scores stay in TMEM, up to (512 - 256 - halves*2NP)/2NP tiles per pass (256 columns
 // hold the converted operands), so the softmax maximum is exact per pass: pass 1 takes the row
-// maxima, pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory) right before
-// its V units are converted. A longer chunk runs in several passes whose (max, sum, o) are
-// merged in registers, rescaled once per pass.
+// maxima, pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory). The first V
+// units of a pass (as many as there are operand regions) are converted before the softmax, while
+// the score MMAs finish; the rest right after their tile's probabilities. A longer chunk runs in
+// several passes whose (max, sum, o) are merged in registers, rescaled once per pass.
 //
 // 288 threads: warps 0-7 convert, run the softmax and read out (warps w and w + 4 share TMEM
 // lane quarter w % 4 and take one half of the columns, rows or keys); thread 0 also issues the
@@ -563,24 +564,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         if (tid < NP) mrun[tid] = -INFINITY;
 
-        for (int u = 0; u < nU; ++u) {
-            const UnitInfo x = decode(u);
-            const int p = min(u / upp, n_pass - 1);
-            if (x.v && x.h == 0) {
-                const int t = x.t, tl = t - x.t0;
-                if (tl == 0) {
+        // Per pass: the K units, then as many V units as there are operand regions (their regions
+        // are freed by the score MMAs alone), then the softmax; the probabilities of a tile are
+        // written before its first V unit that was not converted ahead.
+        for (int p = 0; p < n_pass; ++p) {
+            const int pt0 = p * tpp, nt = min(n_tiles, pt0 + tpp) - pt0, ub = p * upp;
+            const int nK = nt * NH, nV = nK, pre = min(NA, nV), pre_tiles = (pre + NH - 1) / NH;
+            int pdone = 0;   // tiles of the pass whose P operand is written
+            for (int i = 0; i <= nK + nV; ++i) {
+                int want = pdone;
+                if (i == nK + pre) {
                     // softmax pass 1: exact row maxima over the pass's tiles
                     mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
                     tc_fence_after();
                     float mx[NPH];
 #pragma unroll
                     for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
-                    for (int tt = 0; tt < x.nt; ++tt) {
+                    for (int tt = 0; tt < nt; ++tt) {
                         uint32_t sh[NPH], sl[NPH];
                         tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
                         tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
                         tmem_ld_wait();
-                        const int key = c0 + (x.t0 + tt) * kTcKeys + lq * 32 + lane;
+                        const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
 #pragma unroll
                         for (int r = 0; r < NPH; ++r)
                             if (row_ok(key, r0 + r))
@@ -594,75 +599,79 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     for (int r = 0; r < NPH; ++r)
                         Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                         fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
+                    want = pre_tiles;
                 }
-                // pass 2 for tile t: probabilities -> BF16 hi/lo P operand, once the P.V MMAs
-                // that last read this buffer are done
-                const int prev = multi ? t - 1 : t - 2;
-                if (prev >= 0) {
-                    mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
-                    tc_fence_after();
-                }
-                float sv[NPH];
-                {
-                    uint32_t sh[NPH], sl[NPH];
-                    tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
-                    tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
-                    tmem_ld_wait();
+                if (i >= nK + pre && i < nK + nV && (i - nK) % NH == 0) want = max(want, (i - nK) / NH + 1);
+                for (; pdone < want; ++pdone) {
+                    // pass 2 for tile t: probabilities -> BF16 hi/lo P operand, once the P.V MMAs
+                    // that last read this buffer are done
+                    const int t = pt0 + pdone, tl = pdone;
+                    const int prev = multi ? t - 1 : t - 2;
+                    if (prev >= 0) {
+                        mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
+                        tc_fence_after();
+                    }
+                    float sv[NPH];
+                    {
+                        uint32_t sh[NPH], sl[NPH];
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
-                }
-                const int kt = lq * 32 + lane;
-                const int key = c0 + t * kTcKeys + kt;
-                const uint32_t pb = p_buf(t);
+                        for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
+                    }
+                    const int kt = lq * 32 + lane;
+                    const int key = c0 + t * kTcKeys + kt;
+                    const uint32_t pb = p_buf(t);
 #pragma unroll
-                for (int r = 0; r < NPH; ++r) {
-                    const int row = r0 + r;
-                    float pv = 0.f;
-                    if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
-                    lsum[r] += pv;
-                    const uint16_t ph = f32_to_bf16_bits(pv);
-                    const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
-                    st_shared_u16(pb + sw_off(NS, row, kt), ph);
-                    st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
+                    for (int r = 0; r < NPH; ++r) {
+                        const int row = r0 + r;
+                        float pv = 0.f;
+                        if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
+                        lsum[r] += pv;
+                        const uint16_t ph = f32_to_bf16_bits(pv);
+                        const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
+                        st_shared_u16(pb + sw_off(NS, row, kt), ph);
+                        st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
+                if (i == nK + nV) break;
+                convert(ub + i);
             }
-            convert(u);
-            if (x.v && x.h == NH - 1 && x.t == x.t0 + x.nt - 1) {
-                // end of a pass: its P.V products are complete
-                mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
-                tc_fence_after();
-                if constexpr (MP) {
-                    // merge the pass's (max, sum, o) into the running values
+            // end of a pass: its P.V products are complete
+            mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
+            tc_fence_after();
+            if constexpr (MP) {
+                // merge the pass's (max, sum, o) into the running values
 #pragma unroll
-                    for (int h = 0; h < NH; ++h) {
-                        float o[NPH], ol[NPH];
-                        tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + r0, o);
-                        tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
+                for (int h = 0; h < NH; ++h) {
+                    float o[NPH], ol[NPH];
+                    tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + r0, o);
+                    tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
 #pragma unroll
-                        for (int r = 0; r < NPH; ++r) o[r] += ol[r];
+                    for (int r = 0; r < NPH; ++r) o[r] += ol[r];
 #pragma unroll
-                        for (int r = 0; r < NPH; ++r) {
-                            const float Mr = mrun[r0 + r], Mn = fmaxf(Mr, Mrow[r]);
-                            if (Mn == -INFINITY) continue;
-                            const float so = Mr == -INFINITY ? 0.f : ex2(Mr - Mn);
-                            const float sn = Mrow[r] == -INFINITY ? 0.f : ex2(Mrow[r] - Mn);
-                            orun[h][r] = orun[h][r] * so + o[r] * sn;
-                            if (h == NH - 1) {
-                                lrun[r] = lrun[r] * so + lsum[r] * sn;
-                                lsum[r] = 0.f;
-                            }
+                    for (int r = 0; r < NPH; ++r) {
+                        const float Mr = mrun[r0 + r], Mn = fmaxf(Mr, Mrow[r]);
+                        if (Mn == -INFINITY) continue;
+                        const float so = Mr == -INFINITY ? 0.f : ex2(Mr - Mn);
+                        const float sn = Mrow[r] == -INFINITY ? 0.f : ex2(Mrow[r] - Mn);
+                        orun[h][r] = orun[h][r] * so + o[r] * sn;
+                        if (h == NH - 1) {
+                            lrun[r] = lrun[r] * so + lsum[r] * sn;
+                            lsum[r] = 0.f;
                         }
                     }
-                    conv_sync();                // everyone has read mrun before it moves
-                    if (lq == 0 && lane == 0)
-#pragma unroll
-                        for (int r = 0; r < NPH; ++r) mrun[r0 + r] = fmaxf(mrun[r0 + r], Mrow[r]);
-                    conv_sync();
                 }
+                conv_sync();                // everyone has read mrun before it moves
+                if (lq == 0 && lane == 0)
+#pragma unroll
+                    for (int r = 0; r < NPH; ++r) mrun[r0 + r] = fmaxf(mrun[r0 + r], Mrow[r]);
+                conv_sync();
             }
         }
 
