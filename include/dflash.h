@@ -11,8 +11,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every pointer is caller-owned. Device pointers are CUDA global memory on the current
- *    device; "host" is marked where a pointer is host memory. The library allocates and frees
- *    nothing and keeps no state between calls besides the thread-local error text.
+ *    device; "host" is marked where a pointer is host memory. The library allocates no
+ *    tensor memory; besides the thread-local error text it keeps only executable CUDA graphs
+ *    of df_generate and df_draft_round_host (keyed by every argument they bake in) and the
+ *    streams it captures them on.
  *  - BF16 tensors are passed as `const uint16_t *` holding BF16 bit patterns (little-endian,
  *    row-major `[out, in]`, as tensors.rs `upload_bf16` copies them: no transpose, no
  *    dequantisation). RMSNorm weights are F32 (tensors.rs `upload_bf16_as_f32`: a BF16 buffer
@@ -326,6 +328,13 @@ size_t df_draft_round_host_workspace_bytes(const df_dflash_config *cfg, int B, i
  * (in/out), argmax_out [B, K+1], committed [B, K+1], n_committed, accept_count, hit_eos,
  * rollback [B], status (the device status word). ws must hold
  * df_dflash_workspace_bytes(cfg, B, K+1, n_new_max) + df_draft_round_host_workspace_bytes().
+ * When every host buffer is page-locked, the copies and kernels of the call are captured once
+ * into a CUDA graph cached under all of the call's arguments (pointers, sizes, stream and the
+ * weight and cache pointers they reach; up to 16 argument sets, least recently used dropped),
+ * and a repeated call launches that graph: the buffers' contents are read at each launch, so
+ * only their addresses are fixed. The cache holds graphs, not data; pageable buffers take the
+ * stream path. Not thread-safe against a concurrent call on the same buffers (as any stream
+ * use of them).
  */
 int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
                         const df_kv_cache *cache, const int32_t *last_token,

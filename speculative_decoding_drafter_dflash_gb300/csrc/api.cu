@@ -557,6 +557,75 @@ int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V
     return launch_argmax_final(part, G, rows, idx, top1, top2, nullptr, 1, 0, s);
 }
 
+// FNV-1a over bytes: the key of a cached graph (every argument it bakes in).
+uint64_t fnv(uint64_t h, const void *p, size_t n) {
+    const unsigned char *c = static_cast<const unsigned char *>(p);
+    for (size_t i = 0; i < n; ++i) h = (h ^ c[i]) * 1099511628211ull;
+    return h;
+}
+
+// Executable graphs of the host-buffer round entry, least recently used evicted past kMax.
+struct HostRoundGraphs {
+    static constexpr int kMax = 16;
+    struct Entry {
+        uint64_t key, used;
+        cudaGraph_t graph;
+        cudaGraphExec_t exec;
+    };
+    std::mutex mu;
+    std::vector<Entry> entries;
+    uint64_t tick = 0;
+    cudaStream_t cap = nullptr;
+};
+HostRoundGraphs g_host_graphs;
+
+// Launches on `user` the graph captured from enqueue(capture stream) for this key, capturing and
+// instantiating it on first use.
+template <class F>
+int host_round_graph(uint64_t key, F &&enqueue, cudaStream_t user) {
+    HostRoundGraphs &hg = g_host_graphs;
+    std::lock_guard<std::mutex> lk(hg.mu);
+    ++hg.tick;
+    cudaGraphExec_t ex = nullptr;
+    for (auto &en : hg.entries)
+        if (en.key == key) {
+            en.used = hg.tick;
+            ex = en.exec;
+        }
+    if (!ex) {
+        if (!hg.cap) {
+            cudaError_t e = cudaStreamCreateWithFlags(&hg.cap, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return fail(DF_ECUDA, "capture stream: %s", cudaGetErrorString(e));
+        }
+        cudaError_t e = cudaStreamBeginCapture(hg.cap, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return fail(DF_ECUDA, "host round capture: %s", cudaGetErrorString(e));
+        const int rc = enqueue(hg.cap);
+        cudaGraph_t g = nullptr;
+        e = cudaStreamEndCapture(hg.cap, &g);
+        if (rc != DF_OK || e != cudaSuccess) {
+            if (g) cudaGraphDestroy(g);
+            return rc != DF_OK ? rc : fail(DF_ECUDA, "host round capture: %s", cudaGetErrorString(e));
+        }
+        e = cudaGraphInstantiate(&ex, g, 0);
+        if (e != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return fail(DF_ECUDA, "host round graph instantiate: %s", cudaGetErrorString(e));
+        }
+        if ((int)hg.entries.size() >= HostRoundGraphs::kMax) {
+            size_t lru = 0;
+            for (size_t i = 1; i < hg.entries.size(); ++i)
+                if (hg.entries[i].used < hg.entries[lru].used) lru = i;
+            cudaGraphExecDestroy(hg.entries[lru].exec);
+            cudaGraphDestroy(hg.entries[lru].graph);
+            hg.entries.erase(hg.entries.begin() + (long)lru);
+        }
+        hg.entries.push_back({key, hg.tick, g, ex});
+    }
+    const cudaError_t e = cudaGraphLaunch(ex, user);
+    if (e != cudaSuccess) return fail(DF_ECUDA, "host round graph launch: %s", cudaGetErrorString(e));
+    return DF_OK;
+}
+
 }  // namespace
 }  // namespace df
 
@@ -974,37 +1043,122 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
     int32_t *d_rb = d_he + B;
     int32_t *d_eos = d_rb + B;
     int32_t *d_st = d_eos + n_eos;
-    cudaStream_t s = (cudaStream_t)stream;
-    auto h2d = [&](void *dst, const void *src, size_t bytes) {
-        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) : cudaSuccess;
-    };
-    auto d2h = [&](void *dst, const void *src, size_t bytes) {
-        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s) : cudaSuccess;
-    };
-    cudaError_t e = cudaSuccess;
-    e = e ? e : h2d(d_last, last_token, sizeof(int32_t) * B);
-    if (n_new_max > 0) {
-        e = e ? e : h2d(d_th, target_hidden_new, sizeof(float) * B * n_new_max * fc_in);
-        e = e ? e : h2d(d_nnew, n_new, sizeof(int32_t) * B);
+    cudaStream_t user = (cudaStream_t)stream;
+    // Device addresses of the host buffers when they are page-locked and mapped (else null).
+    const void *host_bufs[] = {last_token, target_hidden_new, n_new, target_argmax, eos,
+                               target_seq_len, argmax_out, committed, n_committed, accept_count,
+                               hit_eos, rollback, status};
+    constexpr int kBufs = (int)(sizeof(host_bufs) / sizeof(host_bufs[0]));
+    void *dev_of[kBufs] = {};
+    bool pinned = true;
+    for (int i = 0; i < kBufs; ++i) {
+        if (!host_bufs[i]) continue;
+        cudaPointerAttributes pa{};
+        if (cudaPointerGetAttributes(&pa, host_bufs[i]) != cudaSuccess ||
+            pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr) {
+            pinned = false;
+            cudaGetLastError();
+            break;
+        }
+        dev_of[i] = pa.devicePointer;
     }
-    e = e ? e : h2d(d_tgt, target_argmax, sizeof(int32_t) * B * blk);
-    e = e ? e : h2d(d_tsl, target_seq_len, sizeof(int32_t) * B);
-    e = e ? e : h2d(d_eos, eos, sizeof(int32_t) * n_eos);
-    e = e ? e : cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
-    if (e != cudaSuccess) return fail(DF_ECUDA, "host round staging: %s", cudaGetErrorString(e));
-    DF_TRY(df_draft_round(cfg, w, cache, d_last, n_new_max ? d_th : nullptr,
-                          n_new_max ? d_nnew : nullptr, n_new_max, B, K, d_tgt, d_eos, n_eos,
-                          d_tsl, d_am, d_com, d_nc, d_ac, d_he, d_rb, ws, need_round, d_st,
-                          stream));
-    e = d2h(target_seq_len, d_tsl, sizeof(int32_t) * B);
-    e = e ? e : d2h(argmax_out, d_am, sizeof(int32_t) * B * blk);
-    e = e ? e : d2h(committed, d_com, sizeof(int32_t) * B * blk);
-    e = e ? e : d2h(n_committed, d_nc, sizeof(int32_t) * B);
-    e = e ? e : d2h(accept_count, d_ac, sizeof(int32_t) * B);
-    e = e ? e : d2h(hit_eos, d_he, sizeof(int32_t) * B);
-    e = e ? e : d2h(rollback, d_rb, sizeof(int32_t) * B);
-    e = e ? e : d2h(status, d_st, sizeof(int32_t));
-    e = e ? e : cudaStreamSynchronize(s);
+    // Graph form: the large target rows by one DMA copy, the small inputs and all outputs by one
+    // word-copy kernel each, reading and writing the mapped host buffers directly.
+    auto enqueue_mapped = [&](cudaStream_t s) -> int {
+        cudaError_t e = cudaSuccess;
+        if (n_new_max > 0)
+            e = cudaMemcpyAsync(d_th, target_hidden_new, sizeof(float) * B * n_new_max * fc_in,
+                                cudaMemcpyHostToDevice, s);
+        e = e ? e : cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return fail(DF_ECUDA, "host round staging: %s", cudaGetErrorString(e));
+        WordCopyList in;
+        auto add = [](WordCopyList &l, const void *src, void *dst, long long words) {
+            if (words <= 0) return;
+            l.src[l.n] = src;
+            l.dst[l.n] = dst;
+            l.words[l.n] = (int)words;
+            ++l.n;
+        };
+        add(in, dev_of[0], d_last, B);
+        if (n_new_max > 0) add(in, dev_of[2], d_nnew, B);
+        add(in, dev_of[3], d_tgt, (long long)B * blk);
+        add(in, dev_of[4], d_eos, n_eos);
+        add(in, dev_of[5], d_tsl, B);
+        DF_TRY(launch_word_copy(in, s));
+        DF_TRY(df_draft_round(cfg, w, cache, d_last, n_new_max ? d_th : nullptr,
+                              n_new_max ? d_nnew : nullptr, n_new_max, B, K, d_tgt, d_eos, n_eos,
+                              d_tsl, d_am, d_com, d_nc, d_ac, d_he, d_rb, ws, need_round, d_st,
+                              (df_stream_t)s));
+        WordCopyList out;
+        add(out, d_tsl, dev_of[5], B);
+        add(out, d_am, dev_of[6], (long long)B * blk);
+        add(out, d_com, dev_of[7], (long long)B * blk);
+        add(out, d_nc, dev_of[8], B);
+        add(out, d_ac, dev_of[9], B);
+        add(out, d_he, dev_of[10], B);
+        add(out, d_rb, dev_of[11], B);
+        add(out, d_st, dev_of[12], 1);
+        return launch_word_copy(out, s);
+    };
+    // Stream form: copies in, the round, copies out.
+    auto enqueue = [&](cudaStream_t s) -> int {
+        auto h2d = [&](void *dst, const void *src, size_t bytes) {
+            return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) : cudaSuccess;
+        };
+        auto d2h = [&](void *dst, const void *src, size_t bytes) {
+            return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s) : cudaSuccess;
+        };
+        cudaError_t e = cudaSuccess;
+        e = e ? e : h2d(d_last, last_token, sizeof(int32_t) * B);
+        if (n_new_max > 0) {
+            e = e ? e : h2d(d_th, target_hidden_new, sizeof(float) * B * n_new_max * fc_in);
+            e = e ? e : h2d(d_nnew, n_new, sizeof(int32_t) * B);
+        }
+        e = e ? e : h2d(d_tgt, target_argmax, sizeof(int32_t) * B * blk);
+        e = e ? e : h2d(d_tsl, target_seq_len, sizeof(int32_t) * B);
+        e = e ? e : h2d(d_eos, eos, sizeof(int32_t) * n_eos);
+        e = e ? e : cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return fail(DF_ECUDA, "host round staging: %s", cudaGetErrorString(e));
+        DF_TRY(df_draft_round(cfg, w, cache, d_last, n_new_max ? d_th : nullptr,
+                              n_new_max ? d_nnew : nullptr, n_new_max, B, K, d_tgt, d_eos, n_eos,
+                              d_tsl, d_am, d_com, d_nc, d_ac, d_he, d_rb, ws, need_round, d_st,
+                              (df_stream_t)s));
+        e = d2h(target_seq_len, d_tsl, sizeof(int32_t) * B);
+        e = e ? e : d2h(argmax_out, d_am, sizeof(int32_t) * B * blk);
+        e = e ? e : d2h(committed, d_com, sizeof(int32_t) * B * blk);
+        e = e ? e : d2h(n_committed, d_nc, sizeof(int32_t) * B);
+        e = e ? e : d2h(accept_count, d_ac, sizeof(int32_t) * B);
+        e = e ? e : d2h(hit_eos, d_he, sizeof(int32_t) * B);
+        e = e ? e : d2h(rollback, d_rb, sizeof(int32_t) * B);
+        e = e ? e : d2h(status, d_st, sizeof(int32_t));
+        if (e != cudaSuccess) return fail(DF_ECUDA, "host round readback: %s", cudaGetErrorString(e));
+        return DF_OK;
+    };
+    // With every host buffer page-locked the whole call is one cached CUDA graph (copies and
+    // kernels baked with these exact arguments), so a repeated call costs one graph launch and
+    // the synchronisation; pageable buffers take the stream path.
+    cudaError_t e = cudaSuccess;
+    if (!pinned) {
+        DF_TRY(enqueue(user));
+    } else {
+        uint64_t key = 1469598103934665603ull;
+        key = fnv(key, cfg, sizeof(*cfg));
+        key = fnv(key, w, sizeof(*w));
+        key = fnv(key, w->layers, sizeof(df_layer_weights) * cfg->n_layers);
+        key = fnv(key, cache, sizeof(*cache));
+        key = fnv(key, cache->k, sizeof(float *) * cfg->n_layers);
+        key = fnv(key, cache->v, sizeof(float *) * cfg->n_layers);
+        key = fnv(key, host_bufs, sizeof(host_bufs));
+        const long long scal[] = {n_new_max, B, K, n_eos, (long long)ws_bytes};
+        key = fnv(key, scal, sizeof(scal));
+        key = fnv(key, &ws, sizeof(ws));
+        key = fnv(key, &stream, sizeof(stream));
+        int dev = 0;
+        cudaGetDevice(&dev);
+        key = fnv(key, &dev, sizeof(dev));
+        DF_TRY(host_round_graph(key, enqueue_mapped, user));
+    }
+    e = cudaStreamSynchronize(user);
     if (e != cudaSuccess) return fail(DF_ECUDA, "host round readback: %s", cudaGetErrorString(e));
     return DF_OK;
 }
@@ -1039,11 +1193,6 @@ struct LoopGraph {
 };
 LoopGraph g_loop;
 
-uint64_t fnv(uint64_t h, const void *p, size_t n) {
-    const unsigned char *c = static_cast<const unsigned char *>(p);
-    for (size_t i = 0; i < n; ++i) h = (h ^ c[i]) * 1099511628211ull;
-    return h;
-}
 
 }  // namespace
 }  // namespace df

@@ -429,6 +429,14 @@ int launch_loop_commit(const LoopArgs &a, cudaStream_t s);
 
 int launch_seq_advance(int32_t *seq_len, const int32_t *n_new, int B, int delta, int cap,
                        int32_t *status, cudaStream_t s);
+// Up to 12 copies of 32-bit words (device <-> device-addressable page-locked host memory).
+struct WordCopyList {
+    const void *src[12] = {};
+    void *dst[12] = {};
+    int words[12] = {};
+    int n = 0;
+};
+int launch_word_copy(const WordCopyList &l, cudaStream_t s);
 int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
                   const int32_t *eos, int n_eos, int32_t *committed, int32_t *n_committed,
                   int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,

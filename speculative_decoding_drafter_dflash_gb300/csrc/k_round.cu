@@ -91,7 +91,25 @@ __global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32
     seq_len[b] -= k;
 }
 
+// Word copies between device memory and page-locked host memory the device can address (the
+// small inputs and outputs of the host-buffer round): one launch instead of one DMA copy each.
+__global__ void word_copy_kernel(WordCopyList l) {
+    pdl_trigger();
+    pdl_wait();
+    for (int r = 0; r < l.n; ++r) {
+        const uint32_t *src = static_cast<const uint32_t *>(l.src[r]);
+        uint32_t *dst = static_cast<uint32_t *>(l.dst[r]);
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < l.words[r]; i += gridDim.x * blockDim.x)
+            dst[i] = src[i];
+    }
+}
+
 }  // namespace
+
+int launch_word_copy(const WordCopyList &l, cudaStream_t s) {
+    if (l.n <= 0) return DF_OK;
+    return launch_k("word_copy_kernel", word_copy_kernel, dim3(1), dim3(256), 0, s, l);
+}
 
 int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1, float *top2,
                         int32_t *idx_copy, int idx_copy_ld, int idx_copy_skip, cudaStream_t s) {

@@ -191,6 +191,46 @@ def test_draft_round_tiny_end_to_end():
         assert out.committed[b, :int(out.n_committed[b])].tolist() == c
 
 
+def test_host_round_entry_matches_device_round_pinned_and_pageable():
+    # df_draft_round_host: with page-locked host buffers the call runs as a cached CUDA graph
+    # (first call captures it, later calls relaunch it with the buffers' current contents);
+    # with pageable buffers it runs on the stream. Both must give df_draft_round's results.
+    shape = TINY.with_(batch=2)
+    w, cache, inp, model = _setup(shape, [2, 4], seed=3)
+    seq0 = cache.seq_len.clone()
+    tgt = torch.randint(2, shape.vocab - 1, (shape.batch, shape.block), dtype=torch.int32,
+                        generator=torch.Generator().manual_seed(5)).to(DEV)
+    eos = torch.tensor(shape.eos_ids, dtype=torch.int32, device=DEV)
+    ws = B.alloc_workspace(model.workspace_bytes(shape.batch, shape.block, inp.n_new_max))
+    out = B.RoundOutputs(shape.batch, shape.K, DEV)
+    tsl = torch.tensor([100, 90], dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, inp.n_new_max, shape.K,
+                     tgt, eos, tsl, out, ws, st)
+    torch.cuda.synchronize()
+    ref = {k: getattr(out, k).cpu() for k in ("argmax", "committed", "n_committed", "accept",
+                                              "hit_eos", "rollback")}
+    ref["tsl"] = tsl.cpu()
+    ws_h = B.alloc_workspace(B.draft_round_host_workspace_bytes(model, shape.batch, shape.K,
+                                                                inp.n_new_max, eos.numel()))
+    for pin in (True, True, False):
+        cache.seq_len.copy_(seq0)
+        mk = (lambda t: t.cpu().pin_memory()) if pin else (lambda t: t.cpu().clone())
+        hin = dict(last=mk(inp.last_token), th=mk(inp.target_hidden), nn=mk(inp.n_new),
+                   tgt=mk(tgt), eos=mk(eos), tsl=mk(torch.tensor([100, 90], dtype=torch.int32)))
+        z = lambda *sh: mk(torch.zeros(sh, dtype=torch.int32))
+        hout = {"argmax": z(shape.batch, shape.block), "committed": z(shape.batch, shape.block),
+                "n_committed": z(shape.batch), "accept": z(shape.batch), "hit_eos": z(shape.batch),
+                "rollback": z(shape.batch), "status": z(1)}
+        B.df_draft_round_host(model, hin["last"], hin["th"], hin["nn"], inp.n_new_max, shape.K,
+                              hin["tgt"], hin["eos"], hin["tsl"], hout, ws_h)
+        assert int(hout["status"][0]) == 0
+        for k in ("argmax", "committed", "n_committed", "accept", "hit_eos", "rollback"):
+            assert torch.equal(hout[k], ref[k]), (pin, k)
+        assert torch.equal(hin["tsl"], ref["tsl"])
+        assert torch.equal(cache.seq_len.cpu(), seq0.cpu() + inp.n_new.cpu())
+
+
 def test_device_status_on_capacity_and_bad_ids():
     shape = TINY
     w, cache, inp, model = _setup(shape, [3], seed=4)
