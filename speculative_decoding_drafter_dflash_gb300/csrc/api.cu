@@ -1062,14 +1062,10 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
         }
         dev_of[i] = pa.devicePointer;
     }
-    // Graph form: the large target rows by one DMA copy, the small inputs and all outputs by one
-    // word-copy kernel each, reading and writing the mapped host buffers directly.
+    // Graph form: the small inputs and all outputs by one word-copy kernel each, the target rows
+    // read by the round's first kernel, all straight from and to the mapped host buffers.
     auto enqueue_mapped = [&](cudaStream_t s) -> int {
-        cudaError_t e = cudaSuccess;
-        if (n_new_max > 0)
-            e = cudaMemcpyAsync(d_th, target_hidden_new, sizeof(float) * B * n_new_max * fc_in,
-                                cudaMemcpyHostToDevice, s);
-        e = e ? e : cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
+        cudaError_t e = cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return fail(DF_ECUDA, "host round staging: %s", cudaGetErrorString(e));
         WordCopyList in;
         auto add = [](WordCopyList &l, const void *src, void *dst, long long words) {
@@ -1085,7 +1081,9 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
         add(in, dev_of[4], d_eos, n_eos);
         add(in, dev_of[5], d_tsl, B);
         DF_TRY(launch_word_copy(in, s));
-        DF_TRY(df_draft_round(cfg, w, cache, d_last, n_new_max ? d_th : nullptr,
+        // the row prologue reads the new target rows straight from the mapped host buffer
+        DF_TRY(df_draft_round(cfg, w, cache, d_last,
+                              n_new_max ? static_cast<const float *>(dev_of[1]) : nullptr,
                               n_new_max ? d_nnew : nullptr, n_new_max, B, K, d_tgt, d_eos, n_eos,
                               d_tsl, d_am, d_com, d_nc, d_ac, d_he, d_rb, ws, need_round, d_st,
                               (df_stream_t)s));
