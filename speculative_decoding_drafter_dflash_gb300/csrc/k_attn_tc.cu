@@ -237,28 +237,89 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // Units 0 and 1 are the K units of the chunk's first two tiles when the head dim is 128 (one
     // half per tile) and those tiles exist. Rows that predate this round do not depend on the
     // preceding kernels, so when both the tile and (for unit 1) the chunk's second tile lie below
-    // seq_len they are requested before the wait, behind the q/k norm kernel.
+    // seq_len they are requested, and converted into their TMEM operands, before the wait: only
+    // the score MMAs need q, which the preceding kernel writes.
     int n_early = 0;
+    if (NH == 1 && a.early_kv) {
+        const long long old = a.seq_len[b];
+        const long long c0e = (long long)chunk * a.chunk;
+        while (n_early < min(2, NB) && (n_early + 1) * kTcKeys <= a.chunk &&
+               c0e + (long long)(n_early + 1) * kTcKeys <= old &&
+               c0e + (long long)(n_early + 1) * kTcKeys <= a.cap)
+            ++n_early;
+    }
     if (tid == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.kmap)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap)) : "memory");
         for (int i = 0; i < NB; ++i) mbar_init(&full[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (NH == 1 && a.early_kv) {
-            const long long old = a.seq_len[b];
-            const long long c0e = (long long)chunk * a.chunk;
-            for (int t = 0; t < min(2, NB) && (t + 1) * kTcKeys <= a.chunk &&
-                            c0e + (long long)(t + 1) * kTcKeys <= old && c0e + (t + 1) * kTcKeys <= a.cap;
-                 ++t) {
-                uint8_t *dst = stg + (size_t)t * kUnit;
-                mbar_expect_tx(&full[t], (uint32_t)kUnit);
-                const int y = (int)(head_off * a.cap + c0e) + t * kTcKeys;
-#pragma unroll
-                for (int j = 0; j < kBoxes; ++j)
-                    tma_load_2d(dst + j * kBoxBytes, &P.kmap, &full[t], j * kBoxCols, y, pol);
-                n_early = t + 1;
-            }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&aready[i], kConvThreads / 32);
+            mbar_init(&afree[i], 1);
         }
+        mbar_init(sdone, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&pready[i], kConvThreads / 32);
+            mbar_init(&pfree[i], 1);
+        }
+        mbar_init(odone, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const long long c0e = (long long)chunk * a.chunk;
+        for (int t = 0; t < n_early; ++t) {
+            uint8_t *dst = stg + (size_t)t * kUnit;
+            mbar_expect_tx(&full[t], (uint32_t)kUnit);
+            const int y = (int)(head_off * a.cap + c0e) + t * kTcKeys;
+#pragma unroll
+            for (int j = 0; j < kBoxes; ++j)
+                tma_load_2d(dst + j * kBoxBytes, &P.kmap, &full[t], j * kBoxCols, y, pol);
+        }
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t acol = (uint32_t)(kTmemCols - kACols);             // converted operands
+    const int lq = warp & 3, grp = warp >> 2;
+    const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
+    if (n_early > 0 && warp < kConvThreads / 32) {
+        // the early K units: all keys are cache rows; staged rows -> BF16 operand in region u
+        for (int u = 0; u < n_early; ++u) {
+            mbar_wait(&full[u], 0u, abort_flag, a.status);
+            const uint8_t *st = stg + (size_t)u * kUnit;
+            const uint32_t ta = tmem + lane_addr + acol + (uint32_t)(u * kUCols + (kDT / 2) * grp);
+            const int kr = lq * 32 + lane;
+#pragma unroll 2
+            for (int it = 0; it < kDT / 8; ++it) {
+                const int d0 = kDT * grp + 8 * it;
+                uint32_t hw[4], lw[4];
+                if constexpr (KVB) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(
+                        st + (d0 >> 6) * kBoxBytes + kr * 128 + ((((d0 & 63) >> 3) ^ (kr & 7)) << 4));
+                    hw[0] = w.x; hw[1] = w.y; hw[2] = w.z; hw[3] = w.w;
+                } else {
+                    const uint8_t *row = st + (d0 >> 5) * kBoxBytes + kr * 128;
+                    const int c = (d0 & 31) >> 2;
+                    const float4 f0 = *reinterpret_cast<const float4 *>(row + ((c ^ (kr & 7)) << 4));
+                    const float4 f1 = *reinterpret_cast<const float4 *>(row + (((c + 1) ^ (kr & 7)) << 4));
+                    split2(f0.x, f0.y, hw[0], lw[0]);
+                    split2(f0.z, f0.w, hw[1], lw[1]);
+                    split2(f1.x, f1.y, hw[2], lw[2]);
+                    split2(f1.z, f1.w, hw[3], lw[3]);
+                }
+                tmem_st4(ta + 4 * it, hw);
+                if constexpr (!KVB) tmem_st4(ta + 64 + 4 * it, lw);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aready[u]);
+        }
+        conv_sync();   // every converting warp is done with the early staging buffers
     }
     pdl_wait();
     const int rep = a.nq / a.nkv;
@@ -272,6 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     float *part = a.part + ((head_off * a.n_chunks + chunk) * (size_t)R) * (D + 2);
     if (n_tiles == 0) {
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
         return;
     }
     // A chunk longer than the score columns runs in passes of at most max_tp tiles; each pass
@@ -279,9 +341,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int max_tp = (kTmemCols - kACols - NH * NS) / NS;
     const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
     if (!MP && n_tiles > max_tp) {           // the host plans single-pass launches within bounds
-        if (tid == 0) {
-            set_status(a.status, DF_ESHAPE);
-            for (int j = 0; j < n_early; ++j) mbar_drain(&full[j], 0);
+        if (tid == 0) set_status(a.status, DF_ESHAPE);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tmem, kTmemCols);
         }
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
         return;
@@ -336,26 +401,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             qx[i][4] = v.x; qx[i][5] = v.y; qx[i][6] = v.z; qx[i][7] = v.w;
         }
     }
-    if (warp == 0) {
-        tmem_alloc(tslot, kTmemCols);
-        tmem_relinquish();
-    }
+    // the early units' buffers are free again: the staging runs NB units ahead of them
     int issued = n_early;   // TMA units issued (thread 0)
     if (tid == 0) {
-        for (int i = 0; i < NA; ++i) {
-            mbar_init(&aready[i], kConvThreads / 32);
-            mbar_init(&afree[i], 1);
-        }
-        mbar_init(sdone, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&pready[i], kConvThreads / 32);
-            mbar_init(&pfree[i], 1);
-        }
-        mbar_init(odone, 1);
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (; issued < min(NB, nU); ++issued) issue(issued);
+        if (n_early > 0) fence_proxy_async_smem();
+        for (; issued < min(NB + n_early, nU); ++issued) issue(issued);
     }
     // Q -> hi/lo operands (rows R..NP-1 zero)
 #pragma unroll
@@ -375,9 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tslot;
     const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NS);   // O^T accumulators
-    const uint32_t acol = (uint32_t)(kTmemCols - kACols);             // converted operands
     // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
     // (every score MMA has completed before the first P is written), buffer 1 following it.
     // Several passes: Q stays live, so one buffer after the Q operands.
@@ -440,8 +488,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         __syncwarp();
     } else {
-        const int lq = warp & 3, grp = warp >> 2;
-        const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
         // Unit u -> BF16 operand in TMEM region u % NA. K unit: this thread's lane is key
         // 32*lq + lane, its columns the dims [kDT*grp, kDT*grp + kDT) of the unit. V unit: its
         // lane is dim 32*lq + lane, its columns the keys [kDT*grp, kDT*grp + kDT).
@@ -640,7 +686,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
                 }
                 if (i == nK + nV) break;
-                convert(ub + i);
+                if (ub + i >= n_early) convert(ub + i);   // the early units are converted already
             }
             // end of a pass: its P.V products are complete
             mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
