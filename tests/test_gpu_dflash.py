@@ -229,6 +229,35 @@ def test_host_round_entry_matches_device_round_pinned_and_pageable():
             assert torch.equal(hout[k], ref[k]), (pin, k)
         assert torch.equal(hin["tsl"], ref["tsl"])
         assert torch.equal(cache.seq_len.cpu(), seq0.cpu() + inp.n_new.cpu())
+    # the cached graph reads the buffers' contents at each launch: new targets in the same
+    # pinned buffers must give the device round's results for those targets
+    tgt2 = torch.flip(tgt, dims=[1]).contiguous()
+    cache.seq_len.copy_(seq0)
+    tsl2 = torch.tensor([100, 90], dtype=torch.int32, device=DEV)
+    B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, inp.n_new_max, shape.K,
+                     tgt2, eos, tsl2, out, ws, st)
+    torch.cuda.synchronize()
+    ref2 = {k: getattr(out, k).cpu() for k in ("argmax", "committed", "n_committed", "accept",
+                                               "rollback")}
+    cache.seq_len.copy_(seq0)
+    pin = lambda t: t.cpu().pin_memory()
+    hin = dict(last=pin(inp.last_token), th=pin(inp.target_hidden), nn=pin(inp.n_new),
+               tgt=pin(tgt), eos=pin(eos), tsl=pin(torch.tensor([100, 90], dtype=torch.int32)))
+    z = lambda *sh: pin(torch.zeros(sh, dtype=torch.int32))
+    hout = {"argmax": z(shape.batch, shape.block), "committed": z(shape.batch, shape.block),
+            "n_committed": z(shape.batch), "accept": z(shape.batch), "hit_eos": z(shape.batch),
+            "rollback": z(shape.batch), "status": z(1)}
+    B.df_draft_round_host(model, hin["last"], hin["th"], hin["nn"], inp.n_new_max, shape.K,
+                          hin["tgt"], hin["eos"], hin["tsl"], hout, ws_h)
+    cache.seq_len.copy_(seq0)
+    hin["tgt"].copy_(tgt2.cpu())
+    hin["tsl"].copy_(torch.tensor([100, 90], dtype=torch.int32))
+    B.df_draft_round_host(model, hin["last"], hin["th"], hin["nn"], inp.n_new_max, shape.K,
+                          hin["tgt"], hin["eos"], hin["tsl"], hout, ws_h)
+    assert int(hout["status"][0]) == 0
+    for k in ("argmax", "committed", "n_committed", "accept", "rollback"):
+        assert torch.equal(hout[k], ref2[k]), k
+    assert torch.equal(hin["tsl"], tsl2.cpu())
 
 
 def test_device_status_on_capacity_and_bad_ids():
