@@ -197,8 +197,15 @@ struct AttnTcParams {
 // MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
 // KVB: the cache holds BF16 (no lo half: two MMAs per K step, and twice as many half-size
 // staging buffers in the same shared memory).
-template <int D, int NP, int NBUF, bool MP, bool KVB>
+// VS: chunks of at most two tiles of an F32 cache with head_dim 128. Each V unit is converted in
+// place in its staging buffer into V^T as a K-major BF16 operand in shared memory (hi in the
+// first 32 KB, lo in the second), which the P.V MMAs read directly; K unit t and V unit t share
+// staging buffer t. With the TMEM regions left to the K units, the V units of tiles that predate
+// the round are converted before the wait as well, and after it only q, the scores, the softmax
+// and the products remain (plus the units of tiles holding new rows).
+template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
+    static_assert(!VS || (D == 128 && NBUF == 2 && !MP && !KVB), "in-place V operands");
     constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
     constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit
     constexpr int kBoxes = kUnit / kBoxBytes;             // TMA boxes per unit
@@ -226,13 +233,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint64_t *pfree = pready + 2;     // [2] P.V MMAs reading the P buffer done
     uint64_t *odone = pfree + 2;      // the pass's P.V MMAs done
     uint64_t *drain = odone + 1;      // every MMA issued has completed
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *vready = drain + 1;     // [2] VS: V operand of tile t written (16 warp arrivals)
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(vready + 2);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const size_t head_off = (size_t)b * a.nkv + g;
     const uint64_t pol = policy_evict_first();
+    int nis[2] = {0, 0};   // VS: TMA loads issued into staging buffers 0 and 1 (thread 0)
+    // VS: V rows [y, y + 128) of the cache into staging buffer bf (thread 0)
+    auto stage_v = [&](int bf, int y) {
+        uint8_t *dst = stg + (size_t)bf * kUnit;
+        mbar_expect_tx(&full[bf], (uint32_t)kUnit);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+            tma_load_2d(dst + j * kBoxBytes, &P.vmap, &full[bf], j * kBoxCols, y, pol);
+        ++nis[bf & 1];
+    };
     pdl_trigger();
     // Units 0 and 1 are the K units of the chunk's first two tiles when the head dim is 128 (one
     // half per tile) and those tiles exist. Rows that predate this round do not depend on the
@@ -240,9 +258,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // seq_len they are requested, and converted into their TMEM operands, before the wait: only
     // the score MMAs need q, which the preceding kernel writes.
     int n_early = 0;
+    const long long c0e = (long long)chunk * a.chunk;
     if (NH == 1 && a.early_kv) {
         const long long old = a.seq_len[b];
-        const long long c0e = (long long)chunk * a.chunk;
         while (n_early < min(2, NB) && (n_early + 1) * kTcKeys <= a.chunk &&
                c0e + (long long)(n_early + 1) * kTcKeys <= old &&
                c0e + (long long)(n_early + 1) * kTcKeys <= a.cap)
@@ -263,9 +281,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         mbar_init(odone, 1);
         mbar_init(drain, 1);
+        if (VS)
+            for (int i = 0; i < 2; ++i) mbar_init(&vready[i], kConvThreads / 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const long long c0e = (long long)chunk * a.chunk;
         for (int t = 0; t < n_early; ++t) {
             uint8_t *dst = stg + (size_t)t * kUnit;
             mbar_expect_tx(&full[t], (uint32_t)kUnit);
@@ -273,6 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
             for (int j = 0; j < kBoxes; ++j)
                 tma_load_2d(dst + j * kBoxBytes, &P.kmap, &full[t], j * kBoxCols, y, pol);
+            ++nis[t & 1];
         }
     }
     if (warp == 0) {
@@ -286,6 +306,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const uint32_t acol = (uint32_t)(kTmemCols - kACols);             // converted operands
     const int lq = warp & 3, grp = warp >> 2;
     const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
+    // VS: V unit of tile t, staged in buffer bf (phase ph) -> V^T hi/lo BF16 operand in place. The
+    // thread's row is dim 32*lq + lane, its keys [32*grp, 32*grp + 32) of the tile: all its values
+    // are read before the barrier, and written after it as 16-byte pieces of 8 keys. Keys from
+    // s_cache on come from the block rows vb (below kend) or are zero.
+    auto convert_vs = [&](int t, int bf, uint32_t ph, int kbase, int s_cache, int kend) {
+        mbar_wait(&full[bf], ph, abort_flag, a.status);
+        uint8_t *st = stg + (size_t)bf * kUnit;
+        const uint8_t *sb = st + lq * kBoxBytes + (lane & 3) * 4;   // box of dims 32*lq..
+        const int kr0 = 32 * grp, c = lane >> 2;
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            v[e] = *reinterpret_cast<const float *>(sb + (kr0 + e) * 128 + ((c ^ (e & 7)) << 4));
+        if (kbase + kr0 + 31 >= s_cache) {
+            const float *blkp = a.vb + head_off * a.blk * (size_t)D + lq * 32 + lane;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int key = kbase + kr0 + e;
+                if (key >= s_cache) v[e] = key < kend ? __ldcg(blkp + (size_t)(key - s_cache) * D) : 0.f;
+            }
+        }
+        conv_sync();   // the whole unit is in registers: overwrite it
+        const uint32_t o0 = smem_u32(st);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) split2(v[8 * q + 2 * i], v[8 * q + 2 * i + 1], hw[i], lw[i]);
+            const uint32_t o = o0 + sw_off(128, lq * 32 + lane, kr0 + 8 * q);
+            st_shared_v4(o, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+            st_shared_v4(o + kUnit / 2, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&vready[t]);
+    };
     if (n_early > 0 && warp < kConvThreads / 32) {
         // the early K units: all keys are cache rows; staged rows -> BF16 operand in region u
         for (int u = 0; u < n_early; ++u) {
@@ -320,6 +376,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             if (lane == 0) mbar_arrive(&aready[u]);
         }
         conv_sync();   // every converting warp is done with the early staging buffers
+        if constexpr (VS) {
+            // the V units of the same tiles, into the same buffers, converted in place
+            if (tid == 0) {
+                fence_proxy_async_smem();
+                for (int t = 0; t < n_early; ++t) stage_v(t, (int)(head_off * a.cap + c0e) + t * kTcKeys);
+            }
+            for (int t = 0; t < n_early; ++t) convert_vs(t, t, 1u, 0, 0x7fffffff, 0);
+        }
     }
     pdl_wait();
     const int rep = a.nq / a.nkv;
@@ -340,7 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // has an exact maximum and its output is merged into running (max, sum, o) registers.
     const int max_tp = (kTmemCols - kACols - NH * NS) / NS;
     const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
-    if (!MP && n_tiles > max_tp) {           // the host plans single-pass launches within bounds
+    if (!MP && (n_tiles > max_tp || (VS && n_tiles > 2))) {   // the host plans within bounds
         if (tid == 0) set_status(a.status, DF_ESHAPE);
         tc_fence_before();
         __syncthreads();
@@ -403,9 +467,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
     // the early units' buffers are free again: the staging runs NB units ahead of them
     int issued = n_early;   // TMA units issued (thread 0)
+    // VS: the V unit of a lone tile with nothing converted early takes the unused buffer 1 and is
+    // requested together with its K unit
+    const bool v_apart = VS && n_tiles == 1 && n_early == 0;
     if (tid == 0) {
-        if (n_early > 0) fence_proxy_async_smem();
-        for (; issued < min(NB + n_early, nU); ++issued) issue(issued);
+        if constexpr (VS) {
+            for (int t = n_early; t < n_tiles; ++t) {
+                issue(t);
+                ++nis[t];
+            }
+            if (v_apart) stage_v(1, (int)(head_off * a.cap) + c0);
+        } else {
+            if (n_early > 0) fence_proxy_async_smem();
+            for (; issued < min(NB + n_early, nU); ++issued) issue(issued);
+        }
     }
     // Q -> hi/lo operands (rows R..NP-1 zero)
 #pragma unroll
@@ -441,7 +516,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // MMA issuer: the products of unit u once its operand is in TMEM (and, for a V unit,
         // once its tile's P is in shared memory); commits free the operand region, the P buffer,
         // and signal the end of a pass's scores and outputs.
-        if (lane == 0) {
+        if (lane == 0 && VS) {
+            // VS: the score MMAs of every tile (K operands in TMEM regions t), then the P.V MMAs
+            // of tile t with V^T from its staging buffer (hi half, then lo half)
+            bool ok = true;
+            const uint32_t bq = smem_u32(qsm);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                if (!(ok = mbar_wait(&aready[t], 0u, abort_flag, a.status))) break;
+                tc_fence_after();
+                const uint32_t ahi = tmem + acol + (uint32_t)(t * kUCols), d = tmem + (uint32_t)(t * NS);
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t ob = (uint32_t)((s >> 2) * NS * 128 + (s & 3) * 32);
+                    mma_bf16_ts(d, ahi + 8 * s, sw128_desc(bq + ob), idesc, s ? 1u : 0u);
+                    mma_bf16_ts(d, ahi + 64 + 8 * s, sw128_desc(bq + ob), idesc, 1u);
+                }
+            }
+            if (ok) mma_commit(sdone);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                if (!(ok = mbar_wait(&vready[t], 0u, abort_flag, a.status) &&
+                           mbar_wait(&pready[p_idx(t)], p_phase(t), abort_flag, a.status)))
+                    break;
+                tc_fence_after();
+                const uint32_t vhi = smem_u32(stg + (size_t)(v_apart ? 1 : t) * kUnit), bp = p_buf(t);
+                const uint32_t d = tmem + ocol;
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {
+                    // K step s: keys 16s.. = bytes 32*(s%4) of the 64-key block s/4 of each operand
+                    const uint32_t ob = (uint32_t)((s >> 2) * NS * 128 + (s & 3) * 32);
+                    const uint32_t oa = (uint32_t)((s >> 2) * 128 * 128 + (s & 3) * 32);
+                    mma_bf16(d, sw128_desc(vhi + oa), sw128_desc(bp + ob), idesc, (t || s) ? 1u : 0u);
+                    mma_bf16(d, sw128_desc(vhi + kUnit / 2 + oa), sw128_desc(bp + ob), idesc, 1u);
+                }
+            }
+            if (ok) mma_commit(odone);
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        } else if (lane == 0) {
             for (int u = 0; u < nU; ++u) {
                 const UnitInfo x = decode(u);
                 const int r = u % NA;
@@ -506,7 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             // 8 K values per step: 4 hi words at ta + 4*it, 4 lo words at ta + 64 + 4*it. Loops,
             // not unrolled code: a CTA converts only a few units, so the instructions are fetched
             // cold and their number, not their issue rate, sets the time.
-            if (!x.v) {
+            if (VS || !x.v) {
                 const int kr = lq * 32 + lane, key = kbase + kr;
                 const bool cached = key < S_cache;
                 const float *src = (!cached && key < c1) ? blkp + (size_t)(key - S_cache) * D + kDT * grp
@@ -540,7 +651,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     tmem_st4(ta + 4 * it, hw);
                     if constexpr (!KVB) tmem_st4(ta + 64 + 4 * it, lw);
                 }
-            } else {
+            } else if constexpr (!VS) {
                 const int dd = lq * 32 + lane;                // dim within the 128-wide half
                 const int col = dd % kBoxCols;
                 const uint8_t *sb = st + (dd / kBoxCols) * kBoxBytes;
@@ -583,7 +694,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(&aready[r]);
             conv_sync();   // every warp has read the staging buffer: refill it
-            if (tid == 0 && issued < nU) {
+            if constexpr (VS) {
+                if (tid == 0 && !v_apart) {   // with V unit x.t
+                    fence_proxy_async_smem();
+                    stage_v(bf, (int)(head_off * a.cap) + kbase);
+                }
+            } else if (tid == 0 && issued < nU) {
                 fence_proxy_async_smem();
                 issue(issued);
                 ++issued;
@@ -610,81 +726,96 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         if (tid < NP) mrun[tid] = -INFINITY;
 
+        // softmax pass 1 of pass p (tiles pt0 .. pt0 + nt - 1): exact row maxima into Mrow
+        auto pass_max = [&](int p, int pt0, int nt) {
+            mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
+            tc_fence_after();
+            float mx[NPH];
+#pragma unroll
+            for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
+            for (int tt = 0; tt < nt; ++tt) {
+                uint32_t sh[NPH], sl[NPH];
+                tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
+                tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
+                tmem_ld_wait();
+                const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
+#pragma unroll
+                for (int r = 0; r < NPH; ++r)
+                    if (row_ok(key, r0 + r))
+                        mx[r] = fmaxf(mx[r], (__uint_as_float(sh[r]) + __uint_as_float(sl[r])) * scale);
+            }
+            int row;
+            const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
+            if ((lane & (32 / NPH - 1)) == 0) red[lq * NP + r0 + row] = m;
+            conv_sync();
+#pragma unroll
+            for (int r = 0; r < NPH; ++r)
+                Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
+                                fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
+        };
+        // pass 2 for tile t (the tl-th of its pass): probabilities -> BF16 hi/lo P operand, once
+        // the P.V MMAs that last read this buffer are done
+        auto write_p = [&](int t, int tl) {
+            const int prev = multi ? t - 1 : t - 2;
+            if (prev >= 0) {
+                mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
+                tc_fence_after();
+            }
+            float sv[NPH];
+            {
+                uint32_t sh[NPH], sl[NPH];
+                tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
+                tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                tmem_ld_wait();
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
+            }
+            const int kt = lq * 32 + lane;
+            const int key = c0 + t * kTcKeys + kt;
+            const uint32_t pb = p_buf(t);
+#pragma unroll
+            for (int r = 0; r < NPH; ++r) {
+                const int row = r0 + r;
+                float pv = 0.f;
+                if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
+                lsum[r] += pv;
+                const uint16_t ph = f32_to_bf16_bits(pv);
+                const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
+                st_shared_u16(pb + sw_off(NS, row, kt), ph);
+                st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
+        };
+
+        if constexpr (VS) {
+            // one pass: the K units not converted early (each then passes its buffer on to the V
+            // unit of its tile), those V units in place, the softmax, all P operands
+            for (int t = n_early; t < n_tiles; ++t) convert(t);
+            for (int t = n_early; t < n_tiles; ++t)
+                convert_vs(t, v_apart ? 1 : t, v_apart ? 0u : 1u, c0 + t * kTcKeys, S_cache, c1);
+            pass_max(0, 0, n_tiles);
+            for (int t = 0; t < n_tiles; ++t) write_p(t, t);
+            mbar_wait(odone, 0u, abort_flag, a.status);
+            tc_fence_after();
+        }
         // Per pass: the K units, then as many V units as there are operand regions (their regions
         // are freed by the score MMAs alone), then the softmax; the probabilities of a tile are
         // written before its first V unit that was not converted ahead.
-        for (int p = 0; p < n_pass; ++p) {
+        for (int p = 0; p < (VS ? 0 : n_pass); ++p) {
             const int pt0 = p * tpp, nt = min(n_tiles, pt0 + tpp) - pt0, ub = p * upp;
             const int nK = nt * NH, nV = nK, pre = min(NA, nV), pre_tiles = (pre + NH - 1) / NH;
             int pdone = 0;   // tiles of the pass whose P operand is written
             for (int i = 0; i <= nK + nV; ++i) {
                 int want = pdone;
                 if (i == nK + pre) {
-                    // softmax pass 1: exact row maxima over the pass's tiles
-                    mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
-                    tc_fence_after();
-                    float mx[NPH];
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
-                    for (int tt = 0; tt < nt; ++tt) {
-                        uint32_t sh[NPH], sl[NPH];
-                        tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
-                        tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
-                        tmem_ld_wait();
-                        const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
-#pragma unroll
-                        for (int r = 0; r < NPH; ++r)
-                            if (row_ok(key, r0 + r))
-                                mx[r] = fmaxf(mx[r], (__uint_as_float(sh[r]) + __uint_as_float(sl[r])) * scale);
-                    }
-                    int row;
-                    const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
-                    if ((lane & (32 / NPH - 1)) == 0) red[lq * NP + r0 + row] = m;
-                    conv_sync();
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r)
-                        Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
-                                        fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
+                    pass_max(p, pt0, nt);
                     want = pre_tiles;
                 }
                 if (i >= nK + pre && i < nK + nV && (i - nK) % NH == 0) want = max(want, (i - nK) / NH + 1);
-                for (; pdone < want; ++pdone) {
-                    // pass 2 for tile t: probabilities -> BF16 hi/lo P operand, once the P.V MMAs
-                    // that last read this buffer are done
-                    const int t = pt0 + pdone, tl = pdone;
-                    const int prev = multi ? t - 1 : t - 2;
-                    if (prev >= 0) {
-                        mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
-                        tc_fence_after();
-                    }
-                    float sv[NPH];
-                    {
-                        uint32_t sh[NPH], sl[NPH];
-                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
-                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
-                    }
-                    const int kt = lq * 32 + lane;
-                    const int key = c0 + t * kTcKeys + kt;
-                    const uint32_t pb = p_buf(t);
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) {
-                        const int row = r0 + r;
-                        float pv = 0.f;
-                        if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
-                        lsum[r] += pv;
-                        const uint16_t ph = f32_to_bf16_bits(pv);
-                        const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
-                        st_shared_u16(pb + sw_off(NS, row, kt), ph);
-                        st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
-                }
+                for (; pdone < want; ++pdone) write_p(pt0 + pdone, pdone);
                 if (i == nK + nV) break;
                 if (ub + i >= n_early) convert(ub + i);   // the early units are converted already
             }
@@ -766,8 +897,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         if (tid == 0) {
             // after an abort: let every TMA load still in flight land before the CTA exits
-            for (int j = max(0, issued - NB); j < issued; ++j)
-                mbar_drain(&full[j % NB], (uint32_t)((j / NB) & 1));
+            if constexpr (VS) {
+                for (int j = 0; j < 2; ++j)
+                    if (nis[j] > 0) mbar_drain(&full[j], (uint32_t)((nis[j] - 1) & 1));
+            } else {
+                for (int j = max(0, issued - NB); j < issued; ++j)
+                    mbar_drain(&full[j % NB], (uint32_t)((j / NB) & 1));
+            }
         }
     }
     tc_fence_before();
@@ -798,13 +934,18 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
     dim3 grid(a.n_chunks, a.nkv, a.B);
     const bool one = a.chunk <= max_keys_one_pass;
     if (a.kv_bf16)
-        return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true>, grid,
+        return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true, false>, grid,
                               dim3(kTcThreads), smem, s, p)
-                   : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, true>, grid,
+                   : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, true, false>, grid,
                               dim3(kTcThreads), smem, s, p);
-    return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false>, grid,
+    if constexpr (D == 128 && NBUF == 2) {
+        if (a.chunk <= 2 * kTcKeys)   // chunks of one or two tiles: V operands in place
+            return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, true>, grid,
+                            dim3(kTcThreads), smem, s, p);
+    }
+    return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false>, grid,
                           dim3(kTcThreads), smem, s, p)
-               : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false>, grid,
+               : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false, false>, grid,
                           dim3(kTcThreads), smem, s, p);
 }
 
