@@ -10,7 +10,7 @@
 //
 // Each 128-key x 128-dim piece of K or V (a "unit") lands in shared memory by TMA with the
 // 128-byte swizzle (F32: four 32-column boxes, BF16: two 64-column boxes), so a thread reading
-// one row, or one column, of it touches every bank once. The eight converting warps turn a unit
+// one row, or one column, of it touches every bank once. The sixteen converting warps turn a unit
 // into a BF16 operand in tensor memory (TMEM), where the MMA reads it as its A matrix:
 //   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (A = K: lane = key)
 //   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (A = V^T: lane = dim)
@@ -20,7 +20,10 @@
 // yields x.hi products in accumulator columns [0, NP) and x.lo products in [NP, 2NP); the two are
 // added when the accumulator is read (hi.hi + hi.lo + lo.hi + lo.lo). The converted operand
 // never goes back to shared memory, and the staging buffer is free for the next TMA load as soon
-// as the warps have read it.
+// as the warps have read it. Chunks of at most two tiles of an F32 cache with head_dim 128 (the
+// VS instantiation) keep V^T in shared memory instead: each V unit is split in place in its
+// staging buffer and read by the MMA through a shared-memory descriptor, which leaves TMEM to the
+// K units and lets the V units of old cache rows be prepared before the wait too.
 //
 // A chunk's scores stay in TMEM, up to (512 - 256 - halves*2NP)/2NP tiles per pass (256 columns
 // hold the converted operands), so the softmax maximum is exact per pass: pass 1 takes the row
@@ -29,10 +32,10 @@
 // the score MMAs finish; the rest right after their tile's probabilities. A longer chunk runs in
 // several passes whose (max, sum, o) are merged in registers, rescaled once per pass.
 //
-// 288 threads: warps 0-7 convert, run the softmax and read out (warps w and w + 4 share TMEM
-// lane quarter w % 4 and take one half of the columns, rows or keys); thread 0 also issues the
-// TMA loads; warp 8 issues the MMAs. Block rows (keys past the cache rows) come from kb/vb with
-// plain loads during the conversion; keys past the chunk are converted as zeros.
+// 544 threads: warps 0-15 convert, run the softmax and read out (warps w, w + 4, w + 8, w + 12
+// share TMEM lane quarter w % 4 and take one quarter of the columns, rows or keys); thread 0 also
+// issues the TMA loads; warp 16 issues the MMAs. Block rows (keys past the cache rows) come from
+// kb/vb with plain loads during the conversion; keys past the chunk are converted as zeros.
 #include <cuda_bf16.h>
 #include <string.h>
 
@@ -53,10 +56,11 @@ constexpr int kACols = 256;                   // TMEM columns of the converted A
 constexpr int kF32Unit = 128 * 128 * 4;       // one staged F32 unit: 64 KB
 constexpr int kBoxBytes = 128 * 128;          // one 128-byte-wide column box of 128 rows
 
-template <int D, int NP, int NBUF>
+// VS: no separate second P buffer (it takes the staging buffer of K unit 1).
+template <int D, int NP, int NBUF, bool VS = false>
 constexpr size_t attn_tc_smem_bytes() {
-    return 1024 + (size_t)NBUF * kF32Unit + (D / 128) * 2 * (size_t)NP * 256 + 2 * (size_t)NP * 256 +
-           9 * NP * 4 + 32 * 8 + 16;
+    return 1024 + (size_t)NBUF * kF32Unit + (D / 128) * 2 * (size_t)NP * 256 +
+           (VS ? 0 : 2 * (size_t)NP * 256) + 9 * NP * 4 + 32 * 8 + 16;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -197,15 +201,16 @@ struct AttnTcParams {
 // MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
 // KVB: the cache holds BF16 (no lo half: two MMAs per K step, and twice as many half-size
 // staging buffers in the same shared memory).
-// VS: chunks of at most two tiles of an F32 cache with head_dim 128. Each V unit is converted in
-// place in its staging buffer into V^T as a K-major BF16 operand in shared memory (hi in the
-// first 32 KB, lo in the second), which the P.V MMAs read directly; K unit t and V unit t share
-// staging buffer t. With the TMEM regions left to the K units, the V units of tiles that predate
-// the round are converted before the wait as well, and after it only q, the scores, the softmax
-// and the products remain (plus the units of tiles holding new rows).
+// VS: chunks of at most two tiles of an F32 cache with head_dim 128, three staging buffers. Each
+// V unit is converted in place in its staging buffer into V^T as a K-major BF16 operand in shared
+// memory (hi in the first 32 KB, lo in the second), which the P.V MMAs read directly. K unit t
+// lands in buffer t, V unit 0 in buffer 2 (requested with the K units) and V unit 1 in buffer 0
+// once K unit 0 is in TMEM. With the TMEM regions left to the K units, the V units of tiles that
+// predate the round are converted before the wait as well, and after it only q, the scores, the
+// softmax and the products remain (plus the units of tiles holding new rows).
 template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
-    static_assert(!VS || (D == 128 && NBUF == 2 && !MP && !KVB), "in-place V operands");
+    static_assert(!VS || (D == 128 && NBUF == 3 && !MP && !KVB), "in-place V operands");
     constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
     constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit
     constexpr int kBoxes = kUnit / kBoxBytes;             // TMA boxes per unit
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint8_t *stg = sm;                                  // NB staging buffers
     uint8_t *qsm = sm + NB * kUnit;                     // [NH] stacked hi/lo Q operands
     uint8_t *psm = qsm + NH * 2 * kQBytes;              // stacked hi/lo P operand (second buffer)
-    float *red = reinterpret_cast<float *>(psm + 2 * kQBytes);   // [4][NP] maxima, [4][NP] sums
+    float *red = reinterpret_cast<float *>(psm + (VS ? 0 : 2 * kQBytes));   // [4][NP] maxima, [4][NP] sums
     float *mrun = red + 8 * NP;                                  // [NP] running row maxima
     uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NB] staging landed
     uint64_t *aready = full + NB;     // [NA] region converted (8 warp arrivals)
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const size_t head_off = (size_t)b * a.nkv + g;
     const uint64_t pol = policy_evict_first();
-    int nis[2] = {0, 0};   // VS: TMA loads issued into staging buffers 0 and 1 (thread 0)
+    int nis[4] = {0, 0, 0, 0};   // VS: TMA loads issued into each staging buffer (thread 0)
     // VS: V rows [y, y + 128) of the cache into staging buffer bf (thread 0)
     auto stage_v = [&](int bf, int y) {
         uint8_t *dst = stg + (size_t)bf * kUnit;
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
             tma_load_2d(dst + j * kBoxBytes, &P.vmap, &full[bf], j * kBoxCols, y, pol);
-        ++nis[bf & 1];
+        ++nis[bf & 3];
     };
     pdl_trigger();
     // Units 0 and 1 are the K units of the chunk's first two tiles when the head dim is 128 (one
@@ -292,8 +297,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
             for (int j = 0; j < kBoxes; ++j)
                 tma_load_2d(dst + j * kBoxBytes, &P.kmap, &full[t], j * kBoxCols, y, pol);
-            ++nis[t & 1];
+            ++nis[t & 3];
         }
+        if (VS && n_early > 0) stage_v(2, (int)(head_off * a.cap + c0e));   // V unit 0
     }
     if (warp == 0) {
         tmem_alloc(tslot, kTmemCols);
@@ -374,15 +380,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aready[u]);
+            if (VS && u == 0 && n_early == 2) {
+                conv_sync();   // K unit 0 is read: buffer 0 takes V unit 1
+                if (tid == 0) {
+                    fence_proxy_async_smem();
+                    stage_v(0, (int)(head_off * a.cap + c0e) + kTcKeys);
+                }
+            }
         }
         conv_sync();   // every converting warp is done with the early staging buffers
         if constexpr (VS) {
-            // the V units of the same tiles, into the same buffers, converted in place
-            if (tid == 0) {
-                fence_proxy_async_smem();
-                for (int t = 0; t < n_early; ++t) stage_v(t, (int)(head_off * a.cap + c0e) + t * kTcKeys);
-            }
-            for (int t = 0; t < n_early; ++t) convert_vs(t, t, 1u, 0, 0x7fffffff, 0);
+            // the V units of the same tiles, converted in place
+            for (int t = 0; t < n_early; ++t) convert_vs(t, t ? 0 : 2, (uint32_t)t, 0, 0x7fffffff, 0);
         }
     }
     pdl_wait();
@@ -467,16 +476,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
     // the early units' buffers are free again: the staging runs NB units ahead of them
     int issued = n_early;   // TMA units issued (thread 0)
-    // VS: the V unit of a lone tile with nothing converted early takes the unused buffer 1 and is
-    // requested together with its K unit
-    const bool v_apart = VS && n_tiles == 1 && n_early == 0;
     if (tid == 0) {
         if constexpr (VS) {
+            // the units not requested before the wait: K units into buffers t, V unit 0 into
+            // buffer 2, V unit 1 into buffer 0 when K unit 0 was converted before the wait
             for (int t = n_early; t < n_tiles; ++t) {
                 issue(t);
                 ++nis[t];
             }
-            if (v_apart) stage_v(1, (int)(head_off * a.cap) + c0);
+            if (n_early == 0) stage_v(2, (int)(head_off * a.cap) + c0);
+            if (n_early == 1 && n_tiles == 2) {
+                fence_proxy_async_smem();
+                stage_v(0, (int)(head_off * a.cap) + c0 + kTcKeys);
+            }
         } else {
             if (n_early > 0) fence_proxy_async_smem();
             for (; issued < min(NB + n_early, nU); ++issued) issue(issued);
@@ -503,10 +515,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NS);   // O^T accumulators
     // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
     // (every score MMA has completed before the first P is written), buffer 1 following it.
-    // Several passes: Q stays live, so one buffer after the Q operands.
+    // Several passes: Q stays live, so one buffer after the Q operands. VS: buffer 1 is the staging
+    // buffer of K unit 1, read into TMEM before the score MMAs complete.
     auto p_idx = [&](int t) -> int { return multi ? 0 : (t & 1); };
     auto p_phase = [&](int t) -> uint32_t { return (uint32_t)((multi ? t : (t >> 1)) & 1); };
     auto p_buf = [&](int t) -> uint32_t {
+        if (VS) return (t & 1) ? smem_u32(stg + kUnit) : smem_u32(qsm);
         return multi ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
     };
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NS >> 3) << 17) |
@@ -538,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                            mbar_wait(&pready[p_idx(t)], p_phase(t), abort_flag, a.status)))
                     break;
                 tc_fence_after();
-                const uint32_t vhi = smem_u32(stg + (size_t)(v_apart ? 1 : t) * kUnit), bp = p_buf(t);
+                const uint32_t vhi = smem_u32(stg + (size_t)(t ? 0 : 2) * kUnit), bp = p_buf(t);
                 const uint32_t d = tmem + ocol;
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s) {
@@ -695,9 +709,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             if (lane == 0) mbar_arrive(&aready[r]);
             conv_sync();   // every warp has read the staging buffer: refill it
             if constexpr (VS) {
-                if (tid == 0 && !v_apart) {   // with V unit x.t
+                if (tid == 0 && x.t == 0 && n_tiles == 2) {   // with V unit 1
                     fence_proxy_async_smem();
-                    stage_v(bf, (int)(head_off * a.cap) + kbase);
+                    stage_v(0, (int)(head_off * a.cap) + c0 + kTcKeys);
                 }
             } else if (tid == 0 && issued < nU) {
                 fence_proxy_async_smem();
@@ -726,7 +740,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         if (tid < NP) mrun[tid] = -INFINITY;
 
-        // softmax pass 1 of pass p (tiles pt0 .. pt0 + nt - 1): exact row maxima into Mrow
+        // VS: softmax pass 1 of the chunk's tiles pt0 .. pt0 + nt - 1: exact row maxima into Mrow
+        // (the loop below keeps its own copy, which compiles to fewer spills there)
         auto pass_max = [&](int p, int pt0, int nt) {
             mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
             tc_fence_after();
@@ -753,8 +768,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                 fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
         };
-        // pass 2 for tile t (the tl-th of its pass): probabilities -> BF16 hi/lo P operand, once
-        // the P.V MMAs that last read this buffer are done
+        // VS: pass 2 for tile t (the tl-th of its pass): probabilities -> BF16 hi/lo P operand,
+        // once the P.V MMAs that last read this buffer are done
         auto write_p = [&](int t, int tl) {
             const int prev = multi ? t - 1 : t - 2;
             if (prev >= 0) {
@@ -795,7 +810,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             // unit of its tile), those V units in place, the softmax, all P operands
             for (int t = n_early; t < n_tiles; ++t) convert(t);
             for (int t = n_early; t < n_tiles; ++t)
-                convert_vs(t, v_apart ? 1 : t, v_apart ? 0u : 1u, c0 + t * kTcKeys, S_cache, c1);
+                convert_vs(t, t ? 0 : 2, (uint32_t)t, c0 + t * kTcKeys, S_cache, c1);
             pass_max(0, 0, n_tiles);
             for (int t = 0; t < n_tiles; ++t) write_p(t, t);
             mbar_wait(odone, 0u, abort_flag, a.status);
@@ -811,11 +826,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             for (int i = 0; i <= nK + nV; ++i) {
                 int want = pdone;
                 if (i == nK + pre) {
-                    pass_max(p, pt0, nt);
+                    // softmax pass 1: exact row maxima over the pass's tiles
+                    mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
+                    tc_fence_after();
+                    float mx[NPH];
+#pragma unroll
+                    for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
+                    for (int tt = 0; tt < nt; ++tt) {
+                        uint32_t sh[NPH], sl[NPH];
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
+                        tmem_ld_wait();
+                        const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r)
+                            if (row_ok(key, r0 + r))
+                                mx[r] = fmaxf(mx[r], (__uint_as_float(sh[r]) + __uint_as_float(sl[r])) * scale);
+                    }
+                    int row;
+                    const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
+                    if ((lane & (32 / NPH - 1)) == 0) red[lq * NP + r0 + row] = m;
+                    conv_sync();
+#pragma unroll
+                    for (int r = 0; r < NPH; ++r)
+                        Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
+                                        fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
                     want = pre_tiles;
                 }
                 if (i >= nK + pre && i < nK + nV && (i - nK) % NH == 0) want = max(want, (i - nK) / NH + 1);
-                for (; pdone < want; ++pdone) write_p(pt0 + pdone, pdone);
+                for (; pdone < want; ++pdone) {
+                    // pass 2 for tile t: probabilities -> BF16 hi/lo P operand, once the P.V MMAs
+                    // that last read this buffer are done
+                    const int t = pt0 + pdone, tl = pdone;
+                    const int prev = multi ? t - 1 : t - 2;
+                    if (prev >= 0) {
+                        mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
+                        tc_fence_after();
+                    }
+                    float sv[NPH];
+                    {
+                        uint32_t sh[NPH], sl[NPH];
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
+                    }
+                    const int kt = lq * 32 + lane;
+                    const int key = c0 + t * kTcKeys + kt;
+                    const uint32_t pb = p_buf(t);
+#pragma unroll
+                    for (int r = 0; r < NPH; ++r) {
+                        const int row = r0 + r;
+                        float pv = 0.f;
+                        if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
+                        lsum[r] += pv;
+                        const uint16_t ph = f32_to_bf16_bits(pv);
+                        const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
+                        st_shared_u16(pb + sw_off(NS, row, kt), ph);
+                        st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
+                }
                 if (i == nK + nV) break;
                 if (ub + i >= n_early) convert(ub + i);   // the early units are converted already
             }
@@ -898,7 +973,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (tid == 0) {
             // after an abort: let every TMA load still in flight land before the CTA exits
             if constexpr (VS) {
-                for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < 3; ++j)
                     if (nis[j] > 0) mbar_drain(&full[j], (uint32_t)((nis[j] - 1) & 1));
             } else {
                 for (int j = max(0, issued - NB); j < issued; ++j)
@@ -938,10 +1013,13 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
                               dim3(kTcThreads), smem, s, p)
                    : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, true, false>, grid,
                               dim3(kTcThreads), smem, s, p);
-    if constexpr (D == 128 && NBUF == 2) {
-        if (a.chunk <= 2 * kTcKeys)   // chunks of one or two tiles: V operands in place
-            return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, true>, grid,
-                            dim3(kTcThreads), smem, s, p);
+    if constexpr (D == 128) {
+        if (a.chunk <= 2 * kTcKeys) {   // chunks of one or two tiles: V operands in place
+            constexpr size_t smem_vs = attn_tc_smem_bytes<D, NP, 3, true>();
+            static_assert(smem_vs <= 232448, "shared memory");
+            return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, 3, false, false, true>, grid,
+                            dim3(kTcThreads), smem_vs, s, p);
+        }
     }
     return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false>, grid,
                           dim3(kTcThreads), smem, s, p)
