@@ -73,6 +73,34 @@ def test_mtp_tensor_core_attention(d, nq, nkv, kv_len, steps):
     assert list(synth.host(r["cache"].seq_len)) == list(r["ref"][4])
 
 
+def _tc_chunk_keys(B, nkv, max_keys, sms=152):
+    """Keys per attention chunk as the library plans them: a whole number of 128-key tiles,
+    about one CTA per SM (two waves above 38 sequence x KV-head pairs)."""
+    heads = B * nkv
+    waves = 2 if heads > 38 else 1
+    want = max(1, (waves * sms + heads - 1) // heads)
+    tiles = max(1, (max_keys + 127) // 128)
+    n = min(want, tiles)
+    return (tiles + n - 1) // n * 128
+
+
+@pytest.mark.parametrize("ctx,n_new,causal", [
+    (3960, [5], 0),    # chunks 0-14: both tiles' K and V converted before the wait; chunk 15:
+                       # tile 0 straddles the old context end, nothing early, block rows in both
+    (3960, [5], 1),
+    (4000, [16], 0),   # chunk 15: tile 0 early, tile 1 new context + block rows
+])
+def test_dflash_forward_two_tile_chunks_in_place_v(ctx, n_new, causal):
+    """Chunks of two 128-key tiles (head_dim 128, F32 cache) take the in-place V^T operand path;
+    the three ways a chunk splits into early and late units, against the oracle."""
+    shape = TINY.with_(head_dim=128, n_q_heads=16, n_kv_heads=8, K=15, ctx=ctx)
+    assert _tc_chunk_keys(1, 8, ctx + 2 * shape.block) == 256
+    r, names = _kernels(lambda: _run_forward(shape, n_new, seed=ctx + causal, causal=causal))
+    assert "attn_tc_kernel" in names
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+
+
 # ---------------------------------------------------------------- df_attention on its own
 ATTN_TOL = 1e-4   # hi/lo BF16 operands carry ~16 mantissa bits; the CUDA-core path is plain F32
 
@@ -122,6 +150,15 @@ def _attention_case(Bn, blk, nq, nkv, d, seq, cap, block_keys, causal, seed):
 def test_attention_matches_oracle(Bn, blk, nq, nkv, d, seq, cap, block_keys, causal, kernel):
     names = _attention_case(Bn, blk, nq, nkv, d, seq, cap, block_keys, causal, seed=d + cap)
     assert kernel in names
+
+
+@pytest.mark.parametrize("seq,causal", [([4000], False), ([3900], False), ([3900], True)])
+def test_attention_two_tile_chunks_in_place_v(seq, causal):
+    """256-key chunks of 8 KV heads: every chunk converts its units after the (absent) wait; the
+    last holds two tiles with block rows in the second (seq 4000) or a single tile (seq 3900)."""
+    assert _tc_chunk_keys(1, 8, 4096 + 16) == 256
+    names = _attention_case(1, 16, 16, 8, 128, seq, 4096, True, causal, seed=seq[0] + causal)
+    assert "attn_tc_kernel" in names
 
 
 def test_attention_long_chunks_run_in_passes():
