@@ -229,7 +229,7 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     const size_t T_blk = (size_t)B * blk, T_ctx = (size_t)B * n_new_max, T_all = T_blk + T_ctx;
     const size_t fc_in = (size_t)c->n_target_layers * H, qt = (size_t)nq * d, kt = (size_t)nkv * d;
     w.h = cv.take<float>(T_blk * H);
-    w.ss_in = cv.take<float>(T_blk * (size_t)pack_slices(H));
+    w.ss_in = cv.take<float>(T_all * (size_t)pack_slices(H));   // block rows, then context rows
     w.ss_post = cv.take<float>(T_blk * (size_t)pack_slices(H));
     // deferred split-K sums of one projection: S x T x N floats with S * N <= SMs * 128
     w.defer_floats = defer_floats_for((int)T_all, (long long)std::max<size_t>(qt + 2 * kt, H));
@@ -311,7 +311,9 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
     DF_TRY(launch_rope_table(ws.cos_t, ws.sin_t, cache->seq_len, n_new, n_new_max, B, blk, 0, rot,
                              c->rope_theta, st, s));
     if (T_ctx > 0) {
-        // Context stream: h_ctx = rmsnorm(X_new fc^T) * hidden_norm, packed after the block rows.
+        // Context stream: h_ctx = rmsnorm(X_new fc^T) * hidden_norm, packed after the block rows
+        // with the norm deferred (x * hidden_norm packed, 1/rms applied by every layer's QKV
+        // projection from the sums of squares stored after the block rows' ones).
         PackArgs p;
         p.src = target_hidden;
         p.lds = fc_in;
@@ -346,6 +348,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         q.K = H;
         q.nvalid = n_new;
         q.rows_per_seq = n_new_max;
+        q.ss_out = ws.ss_in + (size_t)T_blk * pack_slices(H);
         q.status = st;
         DF_TRY(launch_pack(q, s));
     }
@@ -403,6 +406,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         g.ldx = H;
         g.T = T_all;
         row_scale(g, ws.ss_in);
+        g.rs_rows = T_all;   // the context rows' deferred hidden norm as well
         int S_qkv = 0;
         DF_TRY(deferred(g, T_all, Nqkv, "gemm_qkv", &S_qkv));
 
