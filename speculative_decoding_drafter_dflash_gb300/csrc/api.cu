@@ -257,12 +257,11 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
                                               (long long)(qt + 2 * kt), (long long)H});
         carve_tc(cv, w.tc, (int)T_all, rows);
     }
+    w.h_final = nullptr;   // the round defers the final norm to the lm_head (no h_final)
     if (round) {
-        w.h_final = cv.take<float>(T_blk * H);
         w.xp_head = cv.take<uint16_t>(2 * T_blk * H);
         w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * T_blk);
     } else {
-        w.h_final = nullptr;
         w.xp_head = nullptr;
         w.amax_part = nullptr;
     }
@@ -535,6 +534,9 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
     pfin.y_out = h_final;
     pfin.ldy = H;
     pfin.pack = final_pack;
+    // Without h_final (the draft round) the final norm is deferred to the lm_head: x * final_norm
+    // is packed, its sums of squares reuse the post-attention ones (the last gate/up has read them)
+    if (!h_final) pfin.ss_out = ws.ss_post;
     pfin.ldp = H;
     pfin.T = T_blk;
     pfin.K = H;
@@ -543,8 +545,11 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
     return launch_seq_advance(cache->seq_len, n_new, B, 0, cache->cap, st, s);
 }
 
+// rs_ss: the packed rows carry a deferred RMSNorm (slice sums of squares, as the row prologue
+// writes them); the logits are scaled by 1/rms per row before the argmax.
 int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
-                 int32_t *idx, float *top1, float *top2, const TcScratch &tc, cudaStream_t s) {
+                 int32_t *idx, float *top1, float *top2, const TcScratch &tc, cudaStream_t s,
+                 const float *rs_ss = nullptr, float rs_eps = 0.f) {
     GemmArgs g;
     g.W0 = Wlm;
     g.n0 = V;
@@ -556,6 +561,13 @@ int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V
     g.epi = EPI_ARGMAX;
     g.part = part;
     g.name = "gemm_lm_head_argmax";
+    if (rs_ss) {
+        g.rs_ss = rs_ss;
+        g.rs_n = pack_slices(H);
+        g.rs_rows = rows;
+        g.rs_inv_k = 1.f / (float)H;
+        g.rs_eps = rs_eps;
+    }
     int G = 0;
     DF_TRY(launch_gemm_tc(g, tc, s, &G));
     return launch_argmax_final(part, G, rows, idx, top1, top2, nullptr, 1, 0, s);
@@ -995,7 +1007,7 @@ int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
     DF_TRY(dflash_forward_impl(cfg, w, cache, nullptr, last_token, target_hidden_new, n_new,
                                n_new_max, B, blk, W.h_final, W.xp_head, W, d_status, s));
     DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
-                        argmax_out, nullptr, nullptr, W.tc, s));
+                        argmax_out, nullptr, nullptr, W.tc, s, W.ss_post, cfg->rms_eps));
     return launch_accept(argmax_out + 1, blk, target_argmax, B, K, eos, n_eos, committed,
                          n_committed, accept_count, hit_eos, rollback, target_seq_len, d_status, s);
 }
@@ -1344,7 +1356,7 @@ int df_generate(const df_dflash_config *cfg, const df_dflash_weights *w, const d
                                      B, blk, W.h_final, W.xp_head, W, d_status, cs);
         if (rc == DF_OK)
             rc = lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
-                              a.argmax, nullptr, nullptr, W.tc, cs);
+                              a.argmax, nullptr, nullptr, W.tc, cs, W.ss_post, cfg->rms_eps);
         if (rc == DF_OK) rc = launch_loop_verify(a, cs);
         if (rc == DF_OK)
             rc = launch_accept(a.argmax + 1, blk, a.target, B, K, eos, n_eos, a.committed,
