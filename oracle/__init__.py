@@ -22,7 +22,13 @@ Pin status (what each function is checked against, in tests/test_oracle_*.py):
   argmax_top2            planted maxima, ties to the lowest index, brute-force scan
   accept_walk            hand examples + brute force over all short draft/target pairs
   kv_rollback            hand examples, overflow rejection
-  dflash forward / mtp   special cases with closed forms (zero projections, one key), float64 shadow
+  qk_norm_rope           one-head hand example (norm first, then the turn)
+  dflash forward / mtp   special cases with closed forms (zero projections, one key), whole-layer
+                         closed forms with 2-dim heads (norm weights that do not commute with the
+                         rotation fix "q/k norm, then RoPE"; identity / reversal projections; the
+                         SwiGLU fed by the post-attention norm), float64 shadow, and planted slips
+                         of the composition (norm order, FFN input norm, positions, eh halves,
+                         gate placement, final-norm weight) that those pins catch
   moe routing            hand example, top-k weights sum to one, one-expert reduction to dense
   stochastic accept      hand draws, exact identity (committed token ~ target softmax) with a
                          planted wrong residual, Monte-Carlo run of the walk, greedy limit at

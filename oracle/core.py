@@ -152,6 +152,21 @@ def rope(x, pos, rotary_dim, theta, dt=np.float32):
     return out
 
 
+def qk_norm_rope(x, w, pos, n_heads, head_dim, eps, rotary_dim, theta, dt=np.float32):
+    """Projected q or k rows x[T, n_heads*head_dim] (one row may come unbatched) ->
+    [T, n_heads, head_dim], T = len(pos): per-head RMSNorm
+    with the shared `[head_dim]` weight first, then RoPE at the rows' positions pos[T].
+
+    mtp.rs, `forward_full_attention`: the per-head q/k RMSNorm is applied to the projections and
+    `apply_imrope` rotates the normed heads; tensors.rs, `DFlashLayerTensors::q_norm` / `k_norm`
+    (qwen3-style per-head norms of the drafter layer).
+    """
+    T = np.size(pos)
+    x = np.asarray(x, dtype=dt).reshape(T, n_heads * head_dim)
+    normed = head_rmsnorm(x, w, n_heads, head_dim, eps, dt)
+    return rope(normed.reshape(T, n_heads, head_dim), pos, rotary_dim, theta, dt)
+
+
 # ---------------------------------------------------------------------------
 # Attention
 # ---------------------------------------------------------------------------

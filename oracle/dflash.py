@@ -30,8 +30,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .core import (OracleError, accept_walk, decode_bf16, head_rmsnorm, kv_rollback, linear,
-                   lm_head_argmax, rmsnorm, rope, round_bf16, sdpa, swiglu)
+from .core import (OracleError, accept_walk, decode_bf16, kv_rollback, linear, lm_head_argmax,
+                   qk_norm_rope, rmsnorm, round_bf16, sdpa, swiglu)
 
 
 def fc_hidden_norm(cfg, w, x_new, dt=np.float32):
@@ -63,10 +63,10 @@ def dflash_layer(cfg, lw, h, h_ctx, k_cache, v_cache, ctx0, dt=np.float32):
         raise OracleError("KV cache capacity exceeded")
     # Context stream: K/V of the newly committed rows, appended at their positions.
     if n_new:
-        kc = head_rmsnorm(linear(h_ctx, lw["wk"], dt), lw["k_norm"], nkv, d, eps, dt)
-        vc = linear(h_ctx, lw["wv"], dt)
         pos_c = np.arange(ctx0, ctx0 + n_new)
-        kc = rope(kc.reshape(n_new, nkv, d), pos_c, rot, theta, dt)
+        kc = qk_norm_rope(linear(h_ctx, lw["wk"], dt), lw["k_norm"], pos_c, nkv, d, eps, rot,
+                          theta, dt)
+        vc = linear(h_ctx, lw["wv"], dt)
         if bf16_kv:                         # a BF16 KV cache keeps the rounded values
             kc, vc = round_bf16(kc, dt), round_bf16(vc, dt)
         k_cache[:, ctx0:ctx0 + n_new, :] = kc.transpose(1, 0, 2)
@@ -74,12 +74,10 @@ def dflash_layer(cfg, lw, h, h_ctx, k_cache, v_cache, ctx0, dt=np.float32):
     ctx_len = ctx0 + n_new
     # Block stream.
     xn = rmsnorm(h, lw["input_norm"], eps, dt)
-    q = head_rmsnorm(linear(xn, lw["wq"], dt), lw["q_norm"], nq, d, eps, dt)
-    kb = head_rmsnorm(linear(xn, lw["wk"], dt), lw["k_norm"], nkv, d, eps, dt)
-    vb = linear(xn, lw["wv"], dt)
     pos_b = np.arange(ctx_len, ctx_len + blk)
-    q = rope(q.reshape(blk, nq, d), pos_b, rot, theta, dt)
-    kb = rope(kb.reshape(blk, nkv, d), pos_b, rot, theta, dt)
+    q = qk_norm_rope(linear(xn, lw["wq"], dt), lw["q_norm"], pos_b, nq, d, eps, rot, theta, dt)
+    kb = qk_norm_rope(linear(xn, lw["wk"], dt), lw["k_norm"], pos_b, nkv, d, eps, rot, theta, dt)
+    vb = linear(xn, lw["wv"], dt)
     if bf16_kv:                             # block K/V at the precision of the cache
         kb, vb = round_bf16(kb, dt), round_bf16(vb, dt)
     keys = np.concatenate([np.asarray(k_cache[:, :ctx_len, :], dt).transpose(1, 0, 2), kb], 0)

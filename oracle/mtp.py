@@ -25,8 +25,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .core import (OracleError, decode_bf16, head_rmsnorm, linear, lm_head_argmax, rmsnorm, rope,
-                   sdpa, sigmoid, silu, swiglu)
+from .core import (OracleError, decode_bf16, linear, lm_head_argmax, qk_norm_rope, rmsnorm, sdpa,
+                   sigmoid, swiglu)
 
 
 def moe_route(x, router_bits, top_k, dt=np.float32):
@@ -71,11 +71,9 @@ def mtp_step(cfg, w, k_cache, v_cache, pos, prev_hidden, token, dt=np.float32):
     x = (linear(rmsnorm(e, w["enorm"], 1e-6, dt), w["eh_embed"], dt)
          + linear(rmsnorm(np.asarray(prev_hidden, dt), w["hnorm"], 1e-6, dt), w["eh_hidden"], dt))
     xn = rmsnorm(x, w["attn_norm"], eps, dt)
-    q = head_rmsnorm(linear(xn, w["wq"], dt), w["q_norm"], nq, d, eps, dt)
-    k = head_rmsnorm(linear(xn, w["wk"], dt), w["k_norm"], nkv, d, eps, dt)
+    q = qk_norm_rope(linear(xn, w["wq"], dt), w["q_norm"], [pos], nq, d, eps, rot, theta, dt)
+    k = qk_norm_rope(linear(xn, w["wk"], dt), w["k_norm"], [pos], nkv, d, eps, rot, theta, dt)
     v = linear(xn, w["wv"], dt)
-    q = rope(q.reshape(1, nq, d), [pos], rot, theta, dt)
-    k = rope(k.reshape(1, nkv, d), [pos], rot, theta, dt)
     k_cache[:, pos, :] = k[0]
     v_cache[:, pos, :] = v.reshape(nkv, d)
     keys = np.asarray(k_cache[:, :pos + 1, :], dt).transpose(1, 0, 2)

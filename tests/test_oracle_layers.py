@@ -6,6 +6,7 @@ planted mistakes that the pins must catch. No expected value here comes from the
 CUDA library.
 """
 import copy
+import inspect
 import math
 
 import numpy as np
@@ -257,6 +258,222 @@ def test_moe_single_expert_reduces_to_dense():
     assert np.allclose(out, want, rtol=1e-12)
 
 
+# --------------------------------------------------------------- whole-layer closed forms
+#
+# Two-dimensional heads (head_dim 2, so RoPE turns the one pair of a head by `position`
+# radians), identity projections and norm weights that differ inside a rotation pair: the
+# per-head norm weight then does not commute with the rotation, so the order "q/k RMSNorm,
+# then RoPE" is fixed by the expected value. Every expected value below is worked out with
+# scalar arithmetic on Python floats, following the layer as the pages describe it
+# (tensors.rs `DFlashLayerTensors`: q_norm / k_norm per head, post_attention_layernorm between
+# the attention residual and the MLP; mtp.rs `forward_full_attention`: per-head norm then
+# `apply_imrope`; `forward_ffn_residual`: post-attention norm feeds the FFN, whose output is
+# added to the attention residual).
+
+Q_NORM2 = [1.9, 0.4]
+K_NORM2 = [0.6, 1.7]
+
+
+def _nrm(x, w, eps=1e-6):
+    """RMSNorm of one row, element by element."""
+    ms = sum(v * v for v in x) / len(x)
+    r = 1.0 / math.sqrt(ms + eps)
+    return [v * r * g for v, g in zip(x, w)]
+
+
+def _turn(pair, angle):
+    """Rotation of the pair (x0, x1) by `angle` radians: the rotate-half RoPE of a 2-dim head
+    (inverse frequency theta^0 = 1)."""
+    c, s = math.cos(angle), math.sin(angle)
+    return [pair[0] * c - pair[1] * s, pair[1] * c + pair[0] * s]
+
+
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def _attend(q, keys, vals):
+    """softmax(q . k / sqrt(2)) weighted sum of the value rows, for one 2-dim query."""
+    sc = [(q[0] * k[0] + q[1] * k[1]) / math.sqrt(2.0) for k in keys]
+    m = max(sc)
+    e = [math.exp(v - m) for v in sc]
+    z = sum(e)
+    return [sum(e[j] * vals[j][t] for j in range(len(vals))) / z for t in range(2)]
+
+
+def _reverse_bits(n):
+    """BF16 [n, n] reversal permutation (row i selects input n-1-i)."""
+    w = fx.zeros_bits(n, n)
+    for i in range(n):
+        w[i, n - 1 - i] = fx.ONE
+    return w
+
+
+def _dflash_two_dim_case():
+    """One drafter layer, H = 4, two q heads sharing one KV head of dim 2, identity q/k/v, gate,
+    up and down projections, Wo the reversal permutation J; two cached rows, one new context
+    row, a block of two."""
+    cfg = fx.dflash_cfg(H=4, nq=2, nkv=1, d=2, I=4, V=10, K=1, n_tl=2)
+    w = fx.random_dflash_weights(cfg, seed=21)
+    lw = w["layers"][0]
+    lw["q_norm"] = np.array(Q_NORM2, np.float32)
+    lw["k_norm"] = np.array(K_NORM2, np.float32)
+    lw["post_norm"] = np.array([1.5, 0.7, 1.2, 0.9], np.float32)
+    for name, (r, c) in dict(wq=(4, 4), wk=(2, 4), wv=(2, 4), wg=(4, 4), wu=(4, 4),
+                             wd=(4, 4)).items():
+        lw[name] = fx.eye_bits(r, c)
+    lw["wo"] = _reverse_bits(4)
+    w["fc"] = fx.eye_bits(4, 8)
+    rng = np.random.default_rng(22)
+    ks, vs = fx.random_cache(1, 1, 1, 2, 2, 6, seed=23, dtype=np.float64)
+    X = rng.standard_normal((1, 1, 8))
+    ids = np.array([[3, 9]])
+    return cfg, w, ks, vs, X, ids
+
+
+def _dflash_two_dim_expected(w, ks, vs, X, ids):
+    lw = w["layers"][0]
+    f = lambda a: [float(v) for v in np.asarray(a).reshape(-1)]
+    k_cached = [f(ks[0][0, 0, j]) for j in range(2)]
+    v_cached = [f(vs[0][0, 0, j]) for j in range(2)]
+    # context row (position 2): h_ctx = rmsnorm(X[:4]) * hidden_norm; K = rope(norm(h_ctx[:2]))
+    hc = _nrm(f(X[0, 0, :4]), f(w["hidden_norm"]))
+    kc = _turn(_nrm(hc[:2], f(lw["k_norm"])), 2.0)
+    vc = hc[:2]
+    # block rows at positions 3 and 4 (after the one appended context row)
+    e = [f(core.decode_bf16(w["embed"][t], np.float64)) for t in ids[0]]
+    xn = [_nrm(r, f(lw["input_norm"])) for r in e]
+    kb = [_turn(_nrm(xn[i][:2], f(lw["k_norm"])), 3.0 + i) for i in range(2)]
+    vb = [xn[i][:2] for i in range(2)]
+    keys = k_cached + [kc] + kb
+    vals = v_cached + [vc] + vb
+    out = []
+    for i in range(2):
+        o = []
+        for hq in range(2):
+            q = _turn(_nrm(xn[i][2 * hq:2 * hq + 2], f(lw["q_norm"])), 3.0 + i)
+            o += _attend(q, keys, vals)
+        h1 = [e[i][t] + o[3 - t] for t in range(4)]            # Wo = J
+        x2 = _nrm(h1, f(lw["post_norm"]))
+        h2 = [a + _silu(z) * z for a, z in zip(h1, x2)]
+        out.append(_nrm(h2, f(w["final_norm"])))
+    return np.array(out), kc, vc
+
+
+def test_dflash_layer_closed_form_two_dim_heads():
+    """Whole drafter layer with every projection the identity: context K/V normed then rotated
+    at the row's absolute position, block q/k normed then rotated at ctx_len + i, attention over
+    cache + context + block (not causal), residual, SwiGLU on the post-attention norm, final
+    norm."""
+    cfg, w, ks, vs, X, ids = _dflash_two_dim_case()
+    want, kc, vc = _dflash_two_dim_expected(w, copy.deepcopy(ks), copy.deepcopy(vs), X, ids)
+    out, seq = dflash.dflash_block_forward(cfg, w, ks, vs, [2], ids, X, [1], np.float64)
+    assert list(seq) == [3]
+    assert np.allclose(ks[0][0, 0, 2], kc, rtol=1e-12, atol=1e-14)
+    assert np.allclose(vs[0][0, 0, 2], vc, rtol=1e-12, atol=1e-14)
+    assert np.allclose(out[0], want, rtol=1e-10, atol=1e-12)
+
+
+def test_dflash_swiglu_reads_post_attention_norm():
+    """Wo = 0 leaves h = E[ids] after attention; Wg = Wu = Wd = I then give
+    h_final = rmsnorm(e + silu(x2) x2, final_norm) with x2 = rmsnorm(e, post_norm)."""
+    cfg = fx.dflash_cfg(H=16, I=16)
+    w = fx.random_dflash_weights(cfg, seed=31)
+    lw = w["layers"][0]
+    lw["wo"] = fx.zeros_bits(16, cfg.q_total)
+    lw["wg"], lw["wu"], lw["wd"] = fx.eye_bits(16, 16), fx.eye_bits(16, 16), fx.eye_bits(16, 16)
+    rng = np.random.default_rng(32)
+    ks, vs = fx.random_cache(1, 1, cfg.n_kv_heads, cfg.head_dim, 3, 8)
+    ids = _ids(cfg, 1, rng)
+    X = rng.standard_normal((1, 1, cfg.fc_in))
+    out, _ = dflash.dflash_block_forward(cfg, w, ks, vs, [3], ids, X, [1], np.float64)
+    for i, t in enumerate(ids[0]):
+        e = [float(v) for v in core.decode_bf16(w["embed"][t], np.float64)]
+        x2 = _nrm(e, [float(g) for g in lw["post_norm"]])
+        h2 = [a + _silu(z) * z for a, z in zip(e, x2)]
+        want = _nrm(h2, [float(g) for g in w["final_norm"]])
+        assert np.allclose(out[0, i], want, rtol=1e-10, atol=1e-12)
+
+
+def _mtp_two_dim_case():
+    """MTP step, H = 4, two q heads sharing one KV head of dim 2, eh_embed = I, eh_hidden and Wo
+    the reversal permutation J, identity q/k/v/gate and SwiGLU projections, two cached rows."""
+    cfg = fx.mtp_cfg(H=4, nq=2, nkv=1, d=2, I=4, V=10)
+    w = fx.random_mtp_weights(cfg, seed=41)
+    w["q_norm"] = np.array(Q_NORM2, np.float32)
+    w["k_norm"] = np.array(K_NORM2, np.float32)
+    w["post_norm"] = np.array([1.5, 0.7, 1.2, 0.9], np.float32)
+    w["eh_embed"] = fx.eye_bits(4, 4)
+    w["eh_hidden"] = _reverse_bits(4)
+    for name, (r, c) in dict(wq=(4, 4), wk=(2, 4), wv=(2, 4), w_gate=(4, 4), wg=(4, 4),
+                             wu=(4, 4), wd=(4, 4)).items():
+        w[name] = fx.eye_bits(r, c)
+    w["wo"] = _reverse_bits(4)
+    rng = np.random.default_rng(42)
+    kc = np.zeros((1, 4, 2))
+    vc = np.zeros((1, 4, 2))
+    kc[0, :2] = rng.standard_normal((2, 2))
+    vc[0, :2] = rng.standard_normal((2, 2))
+    prev = rng.standard_normal(4)
+    return cfg, w, kc, vc, prev
+
+
+def test_mtp_step_closed_form_two_dim_heads():
+    """Whole MTP step at position 2: x = enorm(e) + J hnorm(h_prev); q/k normed then rotated by
+    2 rad; attention over the two cached rows and the new one; output times sigmoid(gate);
+    h1 = x + J o; hidden = h1 + SwiGLU(rmsnorm(h1, post_norm)); argmax of the shared head."""
+    cfg, w, kc, vc, prev = _mtp_two_dim_case()
+    f = lambda a: [float(v) for v in np.asarray(a).reshape(-1)]
+    k_cached = [f(kc[0, j]) for j in range(2)]
+    v_cached = [f(vc[0, j]) for j in range(2)]
+    hidden, idx, _, _, _ = mtp.mtp_step(cfg, w, kc, vc, 2, prev, 7, np.float64)
+    e = f(core.decode_bf16(w["embed"][7], np.float64))
+    ne = _nrm(e, f(w["enorm"]))
+    nh = _nrm(f(prev), f(w["hnorm"]))
+    x = [ne[i] + nh[3 - i] for i in range(4)]
+    xn = _nrm(x, f(w["attn_norm"]))
+    k2 = _turn(_nrm(xn[:2], f(w["k_norm"])), 2.0)
+    v2 = xn[:2]
+    o = []
+    for hq in range(2):
+        q = _turn(_nrm(xn[2 * hq:2 * hq + 2], f(w["q_norm"])), 2.0)
+        o += _attend(q, k_cached + [k2], v_cached + [v2])
+    og = [a / (1.0 + math.exp(-g)) for a, g in zip(o, xn)]
+    h1 = [x[i] + og[3 - i] for i in range(4)]                   # Wo = J
+    x2 = _nrm(h1, f(w["post_norm"]))
+    want = [a + _silu(z) * z for a, z in zip(h1, x2)]
+    assert np.allclose(kc[0, 2], k2, rtol=1e-12, atol=1e-14)
+    assert np.allclose(vc[0, 2], v2, rtol=1e-12, atol=1e-14)
+    assert np.allclose(hidden, want, rtol=1e-10, atol=1e-12)
+    xh = _nrm(want, f(w["shared_head_norm"]))
+    lm = core.decode_bf16(w["lm_head"], np.float64)
+    logits = [sum(float(lm[v, j]) * xh[j] for j in range(4)) for v in range(cfg.vocab)]
+    assert idx == max(range(cfg.vocab), key=lambda v: (logits[v], -v))
+
+
+def test_mtp_dense_ffn_reads_post_attention_norm():
+    """Wo = 0 makes h1 = x; with eh_embed = I, eh_hidden = J and Wg = Wu = Wd = I,
+    hidden = x + silu(x2) x2 with x = enorm(e) + J hnorm(h_prev), x2 = rmsnorm(x, post_norm)."""
+    cfg = fx.mtp_cfg(H=16, I=16)
+    w = fx.random_mtp_weights(cfg, seed=51)
+    w["wo"] = fx.zeros_bits(16, cfg.q_total)
+    w["eh_embed"] = fx.eye_bits(16, 16)
+    w["eh_hidden"] = _reverse_bits(16)
+    w["wg"], w["wu"], w["wd"] = fx.eye_bits(16, 16), fx.eye_bits(16, 16), fx.eye_bits(16, 16)
+    rng = np.random.default_rng(52)
+    kc = rng.standard_normal((1, 6, 8))
+    vc = rng.standard_normal((1, 6, 8))
+    prev = rng.standard_normal(16)
+    hidden, _, _, _, _ = mtp.mtp_step(cfg, w, kc, vc, 4, prev, 5, np.float64)
+    f = lambda a: [float(v) for v in np.asarray(a).reshape(-1)]
+    ne = _nrm(f(core.decode_bf16(w["embed"][5], np.float64)), f(w["enorm"]))
+    nh = _nrm(f(prev), f(w["hnorm"]))
+    x = [ne[i] + nh[15 - i] for i in range(16)]
+    x2 = _nrm(x, f(w["post_norm"]))
+    want = [a + _silu(z) * z for a, z in zip(x, x2)]
+    assert np.allclose(hidden, want, rtol=1e-10, atol=1e-12)
+
+
 # --------------------------------------------------------------- planted mistakes
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -320,3 +537,98 @@ def test_bf16_kv_layer_stores_rounded_rows():
     assert np.array_equal(kb[:, 2:7], core.round_bf16(k32[:, 2:7]))
     assert np.array_equal(vb[:, 2:7], core.round_bf16(v32[:, 2:7]))
     assert not np.array_equal(out16, out32) and np.max(np.abs(out16 - out32)) < 0.05
+
+
+def _mutant(module, name, edits):
+    """`module.name` recompiled from its source with each (old, new) text edit applied once: a
+    plausible slip planted in the oracle (on the CPU) to show that some pin fails."""
+    src = inspect.getsource(getattr(module, name))
+    for old, new in edits:
+        assert src.count(old) == 1, old
+        src = src.replace(old, new)
+    ns = dict(vars(module))
+    exec(compile(src, module.__file__, "exec"), ns)
+    return ns[name]
+
+
+def _rope_then_norm(x, w, pos, n_heads, head_dim, eps, rotary_dim, theta, dt=np.float32):
+    """The planted slip of the q/k step: RoPE first, per-head RMSNorm after it."""
+    T = np.size(pos)
+    x = np.asarray(x, dt).reshape(T, n_heads, head_dim)
+    turned = core.rope(x, pos, rotary_dim, theta, dt).reshape(T, n_heads * head_dim)
+    return core.head_rmsnorm(turned, w, n_heads, head_dim, eps, dt).reshape(T, n_heads, head_dim)
+
+
+DFLASH_PINS = (test_dflash_layer_closed_form_two_dim_heads,
+               test_dflash_swiglu_reads_post_attention_norm)
+MTP_PINS = (test_mtp_step_closed_form_two_dim_heads, test_mtp_dense_ffn_reads_post_attention_norm)
+
+LAYER_SLIPS = [
+    # the drafter's SwiGLU fed by the input norm instead of the post-attention norm
+    ("swiglu_input_norm", dflash, "dflash_layer",
+     [('rmsnorm(h, lw["post_norm"]', 'rmsnorm(h, lw["input_norm"]')], DFLASH_PINS),
+    # the drafter's context K normed with the q weight
+    ("context_k_q_norm", dflash, "dflash_layer",
+     [('lw["k_norm"], pos_c', 'lw["q_norm"], pos_c')], DFLASH_PINS[:1]),
+    # block rows rotated at positions counted before the context append
+    ("block_positions_before_append", dflash, "dflash_layer",
+     [("pos_b = np.arange(ctx_len, ctx_len + blk)", "pos_b = np.arange(ctx0, ctx0 + blk)")],
+     DFLASH_PINS[:1]),
+    # the final norm taken with the hidden (fc) norm weight
+    ("final_norm_weight", dflash, "dflash_block_forward",
+     [('rmsnorm(h, w["final_norm"]', 'rmsnorm(h, w["hidden_norm"]')], DFLASH_PINS),
+    # the MTP FFN fed by the attention-input norm instead of the post-attention norm
+    ("mtp_ffn_attn_norm", mtp, "mtp_step",
+     [('fin = rmsnorm(h1, w["post_norm"]', 'fin = rmsnorm(h1, w["attn_norm"]')], MTP_PINS),
+    # the MTP FFN fed by x (before the attention residual) instead of h1
+    ("mtp_ffn_before_attention", mtp, "mtp_step",
+     [("fin = rmsnorm(h1,", "fin = rmsnorm(x,")], MTP_PINS[:1]),
+    # the two eh_proj halves swapped
+    ("mtp_eh_halves_swapped", mtp, "mtp_step",
+     [('w["eh_embed"]', 'w["@@"]'), ('w["eh_hidden"]', 'w["eh_embed"]'),
+      ('w["@@"]', 'w["eh_hidden"]')], MTP_PINS),
+    # the sigmoid gate applied after the output projection instead of before it
+    ("mtp_gate_after_wo", mtp, "mtp_step",
+     [("o = o * sigmoid(linear(xn, w[\"w_gate\"], dt), dt)", "pass"),
+      ('h1 = x + linear(o, w["wo"], dt)',
+       'h1 = x + linear(o, w["wo"], dt) * sigmoid(linear(xn, w["w_gate"], dt), dt)')],
+     MTP_PINS[:1]),
+]
+
+
+@pytest.mark.parametrize("slip", LAYER_SLIPS, ids=[s[0] for s in LAYER_SLIPS])
+def test_planted_layer_composition_mistakes_are_caught(monkeypatch, slip):
+    """Each slip in the composition of the drafter layer or the MTP step fails a closed-form
+    pin above; the unmodified oracle passes the same pins."""
+    _, module, name, edits, pins = slip
+    monkeypatch.setattr(module, name, _mutant(module, name, edits))
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            pin()
+    monkeypatch.undo()
+    for pin in pins:
+        pin()
+
+
+def test_planted_rope_before_norm_is_caught(monkeypatch):
+    """RoPE before the per-head q/k norm, in the drafter (block and context rows) and in the
+    MTP step: the norm weight does not commute with the rotation, so the two-dim-head closed
+    forms fail."""
+    monkeypatch.setattr(dflash, "qk_norm_rope", _rope_then_norm)
+    with pytest.raises(AssertionError):
+        test_dflash_layer_closed_form_two_dim_heads()
+    monkeypatch.setattr(mtp, "qk_norm_rope", _rope_then_norm)
+    with pytest.raises(AssertionError):
+        test_mtp_step_closed_form_two_dim_heads()
+    monkeypatch.undo()
+    test_dflash_layer_closed_form_two_dim_heads()
+    test_mtp_step_closed_form_two_dim_heads()
+
+
+def test_qk_norm_rope_order_on_one_head():
+    """One 2-dim head [1, 0] with norm weight [2, 1] at position pi/2: normed first it is
+    [2, 0] (RMS of [1, 0] is 1/sqrt(2), so the normed head is [sqrt(2)*2, 0] up to eps), then
+    turned by pi/2 to [0, 2 sqrt(2)]; turned first and normed after it would be [0, sqrt(2)]."""
+    y = core.qk_norm_rope(np.array([[1.0, 0.0]]), np.array([2.0, 1.0]), [math.pi / 2], 1, 2, 0.0,
+                          2, 1e4, np.float64)
+    assert np.allclose(y.reshape(-1), [0.0, 2.0 * math.sqrt(2.0)], atol=1e-12)
