@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from . import stochastic
 from .core import (OracleError, accept_walk, decode_bf16, kv_rollback, linear, lm_head_argmax,
                    qk_norm_rope, rmsnorm, round_bf16, sdpa, swiglu)
 
@@ -141,4 +142,37 @@ def draft_round(cfg, w, cache_k, cache_v, seq_len, block_ids, target_hidden, n_n
         res["hit_eos"].append(hit)
         res["rollback"].append(rb)
         res["target_seq_len"].append(kv_rollback(target_seq_len[b], rb))
+    return res
+
+
+def draft_round_stochastic(cfg, w, cache_k, cache_v, seq_len, block_ids, target_hidden, n_new,
+                           target_logits, temperature, u_draft, u_accept, u_sample, eos,
+                           target_seq_len, dt=np.float32):
+    """The non-greedy draft round (qwen35_orchestrator.rs, module doc "Non-greedy
+    (Metropolis-Hastings) is out of scope here": stochastic acceptance replaces the greedy walk
+    at step 11): the drafter forward, the lm_head logits of every block position, each draft
+    i = 1..K drawn from softmax(logits_i / T) with u_draft[b, i-1], then the speculative-sampling
+    accept step against the verifier's logits target_logits [B, K+1, V] with u_accept [B, K]
+    and u_sample [B], and the rollback of the verifier's KV by K - accept_count.
+    """
+    h_final, seq = dflash_block_forward(cfg, w, cache_k, cache_v, seq_len, block_ids,
+                                        target_hidden, n_new, dt)
+    B, blk, H = h_final.shape
+    K = blk - 1
+    logits = np.stack([linear(h_final[b], w["lm_head"], dt) for b in range(B)])   # [B, blk, V]
+    res = dict(h_final=h_final, seq_len=seq, logits=logits, drafts=[], committed=[], accept=[],
+               hit_eos=[], rollback=[], target_seq_len=[], info=[])
+    for b in range(B):
+        drafts = [stochastic.sample_draft(logits[b, 1 + i], temperature, u_draft[b][i])
+                  for i in range(K)]
+        c, a, hit, rb, info = stochastic.accept_stochastic(logits[b, 1:], target_logits[b], drafts,
+                                                           temperature, u_accept[b], u_sample[b],
+                                                           eos)
+        res["drafts"].append(drafts)
+        res["committed"].append(c)
+        res["accept"].append(a)
+        res["hit_eos"].append(hit)
+        res["rollback"].append(rb)
+        res["target_seq_len"].append(kv_rollback(target_seq_len[b], rb))
+        res["info"].append(info)
     return res

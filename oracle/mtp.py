@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from . import stochastic
 from .core import (OracleError, decode_bf16, linear, lm_head_argmax, qk_norm_rope, rmsnorm, sdpa,
                    sigmoid, swiglu)
 
@@ -92,6 +93,7 @@ def mtp_step(cfg, w, k_cache, v_cache, pos, prev_hidden, token, dt=np.float32):
         f = swiglu(fin, w["wg"], w["wu"], w["wd"], dt)
     hidden = h1 + f
     xh = rmsnorm(hidden, w["shared_head_norm"], eps, dt)
+    info["head_in"] = xh
     idx, t1, t2 = lm_head_argmax(xh[None, :], w["lm_head"], dt)
     return hidden, int(idx[0]), float(t1[0]), float(t2[0]), info
 
@@ -116,3 +118,26 @@ def mtp_forward_draft(cfg, w, cache_k, cache_v, seq_len, prev_hidden, tokens, n_
             hid[s, b], am[s, b], t1s[s, b], t2s[s, b] = h, tok, t1, t2
             infos.append(info)
     return hid, am, t1s, t2s, seq, infos
+
+
+def mtp_forward_draft_sampled(cfg, w, cache_k, cache_v, seq_len, prev_hidden, tokens, n_steps,
+                              temperature, u_draft, dt=np.float32):
+    """Chained MTP draft at temperature T > 0 (the MTP K=1 path of the non-greedy variant,
+    qwen35_orchestrator.rs module doc "Non-greedy (Metropolis-Hastings) is out of scope here"):
+    every step's draft is drawn from softmax(logits / T) with u_draft[s, b] and fed to the next
+    step in place of the argmax. Returns hidden [n_steps, B, H], drafts [n_steps, B],
+    logits [n_steps, B, V] and the new seq_len."""
+    B = len(tokens)
+    hid = np.zeros((n_steps, B, cfg.hidden), dtype=dt)
+    drafts = np.zeros((n_steps, B), dtype=np.int64)
+    logits = np.zeros((n_steps, B, cfg.vocab), dtype=dt)
+    seq = np.asarray(seq_len, dtype=np.int64).copy()
+    for b in range(B):
+        h, tok = np.asarray(prev_hidden[b], dt), int(tokens[b])
+        for s in range(n_steps):
+            h, _, _, _, info = mtp_step(cfg, w, cache_k[b], cache_v[b], int(seq[b]), h, tok, dt)
+            seq[b] += 1
+            lg = linear(info["head_in"], w["lm_head"], dt)
+            tok = stochastic.sample_draft(lg, temperature, u_draft[s][b])
+            hid[s, b], drafts[s, b], logits[s, b] = h, tok, lg
+    return hid, drafts, logits, seq

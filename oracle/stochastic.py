@@ -11,9 +11,10 @@ spell the rule out; it is read as the standard speculative-sampling acceptance t
   at the first rejection a, the committed token is drawn from max(0, p_a - q_a) (normalised);
   if every draft is accepted (a = K), it is drawn from p_K (the verifier's next position).
 
-Under this rule the committed token at every position is distributed exactly as the target's
-p (the identity the pins check). A draw from weights w with a uniform u is the smallest index
-j whose running sum w_0 + ... + w_j exceeds u * sum(w). The committed list, its EOS cut and
+Under this rule, with every draft x_i itself drawn from q_i (`sample_draft`), the committed
+token at every position is distributed exactly as the target's p (the identity the pins check).
+A draw from weights w with a uniform u is the smallest index j whose running sum
+w_0 + ... + w_j exceeds u * sum(w). The committed list, its EOS cut and
 rollback = K - a follow the greedy walk (core.accept_walk). All arithmetic in float64.
 """
 from __future__ import annotations
@@ -51,6 +52,13 @@ def draw_margin(w, u):
     j = draw_index(w, u)
     lo = c[j - 1] if j > 0 else 0.0
     return float(min(t - lo, c[j] - t) / c[-1])
+
+
+def sample_draft(logits, temperature, u):
+    """A draft token drawn from q = softmax(logits / T) with the uniform u in [0, 1): the
+    drafter's side of the non-greedy path (each drafted position is a sample of the drafter's
+    distribution rather than its argmax; the acceptance test below divides by that q)."""
+    return draw_index(softmax_t(logits, temperature), u)
 
 
 def residual(p, q):
