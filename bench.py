@@ -43,8 +43,12 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--batch", type=int, default=1, help="sequences of --profile-case round")
+    ap.add_argument("--ctx", type=int, default=0, help="cache rows of --profile-case round")
+    ap.add_argument("--trace-dump", default=None, help="--profile-case trace: save the records")
+
     ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "sweep_bf16kv", "mtp",
-                                                     "moe", "attn", "stochastic", "generate"],
+                                                     "moe", "attn", "stochastic", "generate", "trace"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -155,6 +159,123 @@ def oracle_rounds(s, hw, ks, vs, seq, host_inputs, targets, n: int, budget_s: fl
         if time.perf_counter() - t0 > budget_s:
             break
     return done, time.perf_counter() - t0
+
+
+def _openblas():
+    """numpy's OpenBLAS library handle, found among the loaded libraries (None if absent)."""
+    import ctypes
+    import re
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted(set(re.findall(r"(/\S*openblas\S*\.so\S*)", f.read())))
+    except OSError:
+        return None
+    for path in libs:
+        try:
+            return ctypes.CDLL(path)
+        except OSError:
+            continue
+    return None
+
+
+def _blas_fn(kind: str):
+    lib = _openblas()
+    if lib is None:
+        return None
+    for name in (f"scipy_openblas_{kind}_num_threads64_", f"scipy_openblas_{kind}_num_threads",
+                 f"openblas_{kind}_num_threads64_", f"openblas_{kind}_num_threads"):
+        if hasattr(lib, name):
+            return getattr(lib, name)
+    return None
+
+
+def blas_threads():
+    """Threads numpy's BLAS uses now (None when it cannot be asked)."""
+    import numpy  # noqa: F401  (loads the BLAS library)
+    fn = _blas_fn("get")
+    return int(fn()) if fn is not None else None
+
+
+def set_blas_threads(n: int) -> bool:
+    import numpy  # noqa: F401
+    fn = _blas_fn("set")
+    if fn is None:
+        return False
+    import ctypes
+    fn.argtypes = [ctypes.c_int]
+    fn(int(n))
+    return True
+
+
+def _median_ms(fn, want: int, budget_s: float):
+    times, t_all = [], time.perf_counter()
+    while len(times) < want:
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    return statistics.median(times) * 1e3, len(times)
+
+
+def cpu_legs(dflash_state, budget_s: float, dev):
+    """The CPU oracle on the tiny DFlash shape, the DFlash K=15 round and a 3-step dense MTP
+    chain, with every core and with one BLAS thread (median ms of >= 3 rounds, >= 100 for the
+    tiny shape, each leg bounded by budget_s). Inputs are drawn on the GPU and copied to the
+    host, as for the main leg; dflash_state is the main leg's host state, reused."""
+    from oracle import dflash as odf
+    from oracle import mtp as omtp
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15, MTP_DENSE, TINY
+    h = synth.host
+    legs = {}
+    # tiny DFlash round
+    s = TINY
+    w = synth.dflash_weights(s, seed=0, device=dev)
+    cache = synth.dflash_cache(s, seed=1, device=dev)
+    inp = synth.dflash_round_inputs(s, [3], seed=2, device=dev)
+    hw, ks, vs, seq, hinp = oracle_round_setup(s, w, cache, [inp])
+    ids, th, nn = hinp[0]
+    tgt = np.zeros((1, s.block), dtype=np.int32)
+    runs = {"tiny": (s.name, "round", 100,
+                     lambda: odf.draft_round(s, hw, ks, vs, seq, ids, th, nn, tgt, s.eos_ids,
+                                             [1 << 30]))}
+    # DFlash K=15 round (the main leg's weights and inputs)
+    s2 = DFLASH_K15
+    hw2, ks2, vs2, seq2, hinp2, tg2 = dflash_state
+    ids2, th2, nn2 = hinp2[0]
+    runs["dflash"] = (s2.name, "round", 3,
+                      lambda: odf.draft_round(s2, hw2, ks2, vs2, seq2, ids2, th2, nn2, tg2[0],
+                                              s2.eos_ids, [1 << 30]))
+    # dense MTP, one chain of 3 steps
+    s3 = MTP_DENSE
+    w3 = synth.mtp_weights(s3, seed=0, device=dev)
+    hw3 = {n: (None if getattr(w3, n) is None else h(getattr(w3, n))) for n in (
+        "enorm", "hnorm", "eh_embed", "eh_hidden", "attn_norm", "post_norm", "q_norm", "k_norm",
+        "wq", "wk", "wv", "w_gate", "wo", "shared_head_norm", "embed", "lm_head", "wg", "wu", "wd",
+        "router", "exp_g", "exp_u", "exp_d", "sh_g", "sh_u", "sh_d", "sh_gate")}
+    del w3
+    c3 = synth.mtp_cache(s3, 3, seed=1, device=dev)
+    k3, v3, q3 = h(c3.k[0]), h(c3.v[0]), h(c3.seq_len).copy()
+    p3, t3 = synth.mtp_inputs(s3, seed=2, device=dev)
+    p3, t3 = h(p3), h(t3)
+    del c3
+    runs["mtp3"] = (s3.name, "3-step chain", 3,
+                    lambda: omtp.mtp_forward_draft(s3, hw3, k3.copy(), v3.copy(), q3, p3, t3, 3))
+    all_threads = blas_threads()
+    for name, (wl, per, want, fn) in runs.items():
+        leg = {"workload": wl, "per": per}
+        fn()                                                   # warm-up
+        for label, n in (("all_cores", all_threads), ("one_thread", 1)):
+            if label == "one_thread" and not set_blas_threads(1):
+                leg[label] = "unavailable: numpy's BLAS thread count cannot be set"
+                continue
+            ms, k = _median_ms(fn, want, budget_s)
+            leg[label] = {"ms": round(ms, 3), "rounds": k, "blas_threads": blas_threads()}
+            if all_threads:
+                set_blas_threads(all_threads)
+        legs[name] = leg
+    return legs
 
 
 def max_over_ranks(seconds: float, world: int, device=None) -> float:
@@ -357,19 +478,27 @@ def run_native(args, rank, world, local_rank):
         oracle_rounds(s, hw, ks, vs, seq, hinp, tg, 1, 1e9)      # warm the BLAS / page cache
         n, secs = oracle_rounds(s, hw, ks, vs, seq, hinp, tg, 50, args.cpu_seconds)
         cpu = {"value": round(n / secs, 4), "unit": "rounds/s", "cores": cores(), "kind": "oracle",
-               "sample": f"{n} full rounds of this workload by the NumPy F32 oracle ({secs:.1f} s)"}
+               "sample": f"{n} full rounds of this workload by the NumPy F32 oracle ({secs:.1f} s)",
+               "blas_threads": blas_threads(),
+               "legs": cpu_legs((hw, ks, vs, seq, hinp, tg), max(3.0, args.cpu_seconds / 3), dev)}
+        del hw, ks, vs
 
     if rank != 0:
         return None
     return {
         "metric": METRIC, "value": round(value, 3), "unit": "rounds/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 hi/lo pair, f32 accumulate",
         "data": "synthetic",
         "config": {"workload": s.name, "batch_per_gpu": 1, "K": s.K, "block": s.block,
                    "ctx": s.ctx, "hidden": s.hidden, "layers": s.n_layers, "heads": "16q/8kv x 128",
                    "intermediate": s.intermediate, "vocab": s.vocab,
                    "weights": "bf16", "activations_kv": "f32", "accumulate": "f32",
+                   "arithmetic": "bf16 weights x f32 activations carried into tcgen05 kind::f16 "
+                                 "as a bf16 hi/lo pair (~16 mantissa bits); attention splits the "
+                                 "f32 KV the same way (lo x lo dropped); f32 accumulate, softmax "
+                                 "and norms",
                    "n_new_per_variant": n_new, "accept_per_variant": [int(a) for a in acc],
                    "l2": "no flush: each round streams 2.6 GB of weights, 20x the 129 MB L2",
                    "cuda_graph": not args.no_graph, "parallelism": f"replicas x{world}"},
@@ -764,10 +893,118 @@ def generate_case(steps: int):
         del cache, ws, table, prior
 
 
+TRACE_NAMES = {1: "rope_table", 2: "qk_rope", 3: "attn", 4: "attn_combine", 5: "seq_advance",
+               6: "attn_tc", 15: "pack", 16: "pack", 17: "argmax_final", 18: "accept",
+               19: "rollback", 20: "word_copy"}
+
+
+def trace_case(args):
+    """In-graph timeline of the draft round from the trace build (per-CTA global-timer spans of
+    every kernel): CUDA-graph rounds of the workload, each launch's first start, last end and the
+    time it adds to the round's critical path, summed per kernel over the rounds' layers."""
+    from speculative_decoding_drafter_dflash_gb300 import build as bld
+    os.environ["DFLASH_LIB"] = bld.build(trace=True)
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+    s = DFLASH_K15.with_(batch=args.batch, ctx=args.ctx or DFLASH_K15.ctx)
+    Bn, dev = s.batch, torch.device("cuda", 0)
+    acc, n_new = variants(s)
+    nmax = s.block
+    w = synth.dflash_weights(s, seed=0, device=dev)
+    cache = synth.dflash_cache(s, seed=1, device=dev)
+    model = B.DFlashModel(s, w, cache)
+    ws = B.alloc_workspace(model.workspace_bytes(Bn, s.block, nmax), dev)
+    out = B.RoundOutputs(Bn, s.K, dev)
+    eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
+    tsl = torch.full((Bn,), 1 << 30, dtype=torch.int32, device=dev)
+    tgt = torch.zeros((Bn, s.block), dtype=torch.int32, device=dev)
+    inp = synth.dflash_round_inputs(s, [nmax] * Bn, seed=10, device=dev)
+    inp.n_new = torch.tensor([n_new[b % N_VARIANTS] for b in range(Bn)], dtype=torch.int32,
+                             device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, nmax, s.K, tgt, eos,
+                         tsl, out, ws, stream=stream)
+        B.kv_rollback(cache.seq_len, inp.n_new, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    B.profile_enable(True)                       # the launch names, in order, of one round
+    with torch.cuda.stream(stream):
+        step()
+    names = [n for n, _ in B.profile_read()]
+    B.profile_enable(False)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    rounds = max(3, min(args.steps, 20))
+    B.trace_reset()
+    for _ in range(rounds):
+        g.replay()
+    torch.cuda.synchronize()
+    kid, sm, t0, t1 = B.trace_read()
+    if args.trace_dump:
+        np.savez(args.trace_dump, kid=kid, sm=sm, t0=t0, t1=t1, names=np.array(names))
+    # Every kernel waits for its predecessor's grid to complete before its CTAs finish, so the
+    # launches follow one another in the order of their CTAs' end times (their start times
+    # interleave: a successor's CTAs become resident early and wait).
+    order = np.argsort(t1, kind="stable")
+    kid, t0, t1 = kid[order], t0[order].astype(np.int64), t1[order].astype(np.int64)
+    groups = []                                  # [kid, first start, last end, ctas]
+    for k, a, b in zip(kid.tolist(), t0.tolist(), t1.tolist()):
+        if groups and groups[-1][0] == k:
+            g_ = groups[-1]
+            g_[1] = min(g_[1], a)
+            g_[2] = max(g_[2], b)
+            g_[3] += 1
+        else:
+            groups.append([k, a, b, 1])
+    per = len(names)
+    ok = len(groups) == per * rounds
+    # Each launch is charged the time by which it moves the end of the timeline (the idle time
+    # before it included), so the charges add up to the span of the replays.
+    agg, crit_total, timeline = {}, 0.0, []
+    prev_end = groups[0][1] if groups else 0
+    for i, (k, a, b, n) in enumerate(groups):
+        name = names[i % per] if ok else (TRACE_NAMES.get(k) or f"gemm_epi{(k - 100) // 2}")
+        exposed = max(0, b - prev_end)
+        if per <= i < 2 * per:                  # the second replay, launch by launch
+            timeline.append({"launch": name, "ctas": n,
+                             "first_start_us": round((a - groups[per][1]) / 1e3, 2),
+                             "end_us": round((b - groups[per][1]) / 1e3, 2),
+                             "after_previous_us": round(exposed / 1e3, 2)})
+        prev_end = max(prev_end, b)
+        e = agg.setdefault(name, [0, 0.0, 0.0, 0])
+        e[0] += 1
+        e[1] += (b - max(a, b - exposed)) / 1e3
+        e[2] += exposed / 1e3
+        e[3] = n
+        crit_total += exposed / 1e3
+    span = (groups[-1][2] - groups[0][1]) / 1e3 / rounds
+    table = {k: {"launches_per_round": v[0] // rounds, "span_us_each": round(v[1] / v[0], 2),
+                 "critical_us_per_round": round(v[2] / rounds, 2), "ctas": v[3]}
+             for k, v in sorted(agg.items(), key=lambda kv: -kv[1][2])}
+    print(json.dumps({"profile_case": "trace", "workload": s.name, "batch": Bn, "ctx": s.ctx,
+                      "rounds": rounds, "launches_per_round": per, "grouped_ok": ok,
+                      "round_us": round(span, 1),
+                      "critical_us_per_round": round(crit_total / rounds, 1), "kernels": table,
+                      "timeline": timeline}))
+
+
 def profile_case(args):
     """A small, self-contained case for ncu: the full-size lm_head argmax (1.48 GB of weights,
     larger than L2) over the 16 block rows, 2 warm-up launches then 3 profiled ones; or one
     eager round of the workload."""
+    if args.profile_case == "trace":              # loads the trace build: before the binding
+        return trace_case(args)
     import torch
 
     from speculative_decoding_drafter_dflash_gb300 import binding as B
@@ -827,20 +1064,23 @@ def profile_case(args):
     else:
         # Per-kernel GPU time inside eager rounds of the workload (library event profiler).
         from speculative_decoding_drafter_dflash_gb300 import synth
+        s = s.with_(batch=args.batch, ctx=args.ctx or s.ctx)
+        Bn = s.batch
         acc, n_new = variants(s)
         nmax = s.block
         w = synth.dflash_weights(s, seed=0, device=dev)
         cache = synth.dflash_cache(s, seed=1, device=dev)
         model = B.DFlashModel(s, w, cache)
-        ws = B.alloc_workspace(model.workspace_bytes(1, s.block, nmax), dev)
-        out = B.RoundOutputs(1, s.K, dev)
+        ws = B.alloc_workspace(model.workspace_bytes(Bn, s.block, nmax), dev)
+        out = B.RoundOutputs(Bn, s.K, dev)
         eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
-        tsl = torch.full((1,), 1 << 30, dtype=torch.int32, device=dev)
-        tgt = torch.zeros((1, s.block), dtype=torch.int32, device=dev)
+        tsl = torch.full((Bn,), 1 << 30, dtype=torch.int32, device=dev)
+        tgt = torch.zeros((Bn, s.block), dtype=torch.int32, device=dev)
         inputs = []
         for v in range(N_VARIANTS):
-            inp = synth.dflash_round_inputs(s, [nmax], seed=10 + v, device=dev)
-            inp.n_new = torch.tensor([n_new[v]], dtype=torch.int32, device=dev)
+            inp = synth.dflash_round_inputs(s, [nmax] * Bn, seed=10 + v, device=dev)
+            inp.n_new = torch.tensor([n_new[(v + b) % N_VARIANTS] for b in range(Bn)],
+                                     dtype=torch.int32, device=dev)
             inputs.append(inp)
 
         def one(v):

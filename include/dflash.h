@@ -78,6 +78,17 @@ uint64_t df_kernel_launches(void);
 int df_profile_enable(int on);
 int df_profile_read(float *us, int max_entries, char *names, size_t names_bytes);
 
+/* Trace builds only (libdflash_trace.so, built with build.py --trace; other builds return
+ * DF_EINVAL): every CTA of every kernel records its kernel id (TK_* of the library's internal
+ * list; projections 100 + 2 * epilogue + stream-K), its SM and the global-timer nanoseconds at
+ * which it started and its thread 0 left, into one device buffer of 2^20 records, so the
+ * launches of a CUDA graph replay can be timed one by one with their overlaps.
+ * df_trace_reset clears the buffer (synchronous); df_trace_read synchronises the device and
+ * copies up to max_records records out, returning their number. */
+int df_trace_reset(void);
+int df_trace_read(uint32_t *kid, uint32_t *sm, unsigned long long *t0, unsigned long long *t1,
+                  int max_records);
+
 /* ------------------------------------------------------------------------------------------
  * DFlash drafter (tensors.rs `DFlashLayerTensors`, `DFlashModelTensors`; dflash config fields
  * seen in qwen35_orchestrator.rs: target_layer_ids, mask_token_id, hidden_size, head_dim).
@@ -287,6 +298,40 @@ int accept_stochastic(const float *draft_logits, const float *target_logits, int
                       int32_t *d_status, df_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Sampled drafts: one token per row drawn from q = softmax(logits[r] / T) with the uniform
+ * u[r]: the smallest j whose running sum q_0 + ... + q_j exceeds u[r] (the drafter's side of
+ * the non-greedy path of qwen35_orchestrator.rs's module doc, "Non-greedy (Metropolis-Hastings)
+ * is out of scope here": each drafted position is a sample of the drafter's distribution, which
+ * the accept step above then divides by). The weights are computed to ~1e-14 relative and summed
+ * in float-float / float64, so a draw differs from a float64 reference only where u * total is
+ * within ~1e-12 of a cumulative boundary.
+ * ---------------------------------------------------------------------------------------- */
+/* Workspace (chunk statistics, draw partial sums, counters); allocate it zeroed. */
+size_t df_sample_softmax_workspace_bytes(int R, int V);
+
+/*   logits       device F32 [R, V], 16-byte aligned; V a positive multiple of 4, V <= 2^21
+ *   temperature  > 0 (DF_EINVAL otherwise)
+ *   u            device F32 [R] uniforms in [0, 1)
+ *   tokens       device int32 [R] out
+ * A row whose weights sum to zero (all logits -inf) sets DF_EINVAL in d_status. */
+int sample_softmax(const float *logits, int R, int V, float temperature, const float *u,
+                   int32_t *tokens, void *ws, size_t ws_bytes, int32_t *d_status,
+                   df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Failure-detection test hook (no counterpart on the pages). Every barrier wait of the
+ * tensor-core projection kernel is bounded: after the limit it raises the CTA's abort flag,
+ * writes DF_ETIMEOUT to the call's status word, lets every role leave, waits (bounded) for the
+ * TMA loads it issued and frees its tensor memory, so the context stays usable. This call sets,
+ * for the projections launched after it from any thread, the limit in SM cycles (0 restores the
+ * default of ~2 s) and, with withhold_first != 0, makes every CTA's TMA producer skip the load of
+ * its first pipeline stage, so the MMA warp's wait runs out. Outputs of calls made while
+ * withholding are meaningless. Returns DF_EINVAL for a negative limit, or for withholding without
+ * a positive limit. Reset with (0, 0).
+ * ---------------------------------------------------------------------------------------- */
+int df_test_wait_hook(long long wait_cycles, int withhold_first);
+
+/* ------------------------------------------------------------------------------------------
  * KV rollback (qwen35_orchestrator.rs step 8, `rollback_kv`): seq_len[b] -= n[b]. Cache rows
  * are not touched. If n[b] < 0 or n[b] > seq_len[b], seq_len[b] is left unchanged and
  * DF_ECAPACITY is written to d_status.
@@ -315,6 +360,34 @@ int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
                    int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
                    int32_t *rollback, void *ws, size_t ws_bytes, int32_t *d_status,
                    df_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Non-greedy DFlash draft round (temperature T > 0): the drafter forward of df_draft_round, the
+ * lm_head logits of every block row, draft i = 1..K drawn from softmax(logits_i / T)
+ * (sample_softmax's rule) with u_draft[b, i-1], then accept_stochastic against the verifier's
+ * logits and the rollback of target_seq_len by K - accept_count (qwen35_orchestrator.rs, module
+ * doc "Non-greedy (Metropolis-Hastings) is out of scope here": the stochastic acceptance takes
+ * the place of the greedy walk at step 11).
+ *   target_logits   device F32 [B, K+1, V]: verifier logits at positions 0..K (16-byte aligned)
+ *   u_draft, u_accept device F32 [B, K]; u_sample device F32 [B]: uniforms in [0, 1)
+ *   logits_out      device F32 [B, K+1, V] out: the drafter's logits of every block row
+ *                   (row 0 = last_token's position; rows 1..K are the drafts' q)
+ *   drafts_out      device int32 [B, K] out: the sampled drafts
+ *   committed, n_committed, accept_count, hit_eos, rollback, target_seq_len: as df_draft_round
+ * 1 <= K <= 64; V a multiple of 4. The drafter cache advances as in df_draft_round.
+ * ---------------------------------------------------------------------------------------- */
+size_t df_draft_round_stochastic_workspace_bytes(const df_dflash_config *cfg, int B, int K,
+                                                 int n_new_max);
+int df_draft_round_stochastic(const df_dflash_config *cfg, const df_dflash_weights *w,
+                              const df_kv_cache *cache, const int32_t *last_token,
+                              const float *target_hidden_new, const int32_t *n_new,
+                              int n_new_max, int B, int K, const float *target_logits,
+                              float temperature, const float *u_draft, const float *u_accept,
+                              const float *u_sample, const int32_t *eos, int n_eos,
+                              int32_t *target_seq_len, float *logits_out, int32_t *drafts_out,
+                              int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                              int32_t *hit_eos, int32_t *rollback, void *ws, size_t ws_bytes,
+                              int32_t *d_status, df_stream_t stream);
 
 /* Bytes of the host-buffer round's staging area (device), in addition to the round's own. */
 size_t df_draft_round_host_workspace_bytes(const df_dflash_config *cfg, int B, int K,
@@ -449,6 +522,23 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
                       int B, int n_steps, float *hidden_out, int32_t *argmax_out,
                       float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
                       df_stream_t stream);
+
+/* The MTP K=1 path at temperature T > 0 (qwen35_orchestrator.rs module doc, "Non-greedy
+ * (Metropolis-Hastings) is out of scope here": the stochastic acceptance is wired through the
+ * MTP K=1 path): as mtp_forward_draft, but every step's token is drawn from
+ * softmax(logits / T) with u_draft[s, b] (sample_softmax's rule) and fed to the next step.
+ *   temperature  > 0 (DF_EINVAL otherwise)
+ *   u_draft      device F32 [n_steps, B] uniforms in [0, 1)
+ *   draft_out    device int32 [n_steps, B] out: the drawn tokens
+ *   logits_out   device F32 [n_steps, B, V] out (required): every step's logits, the q of the
+ *                accept step; V a multiple of 4
+ * Workspace: df_mtp_workspace_bytes. */
+int mtp_forward_draft_sampled(const df_mtp_config *cfg, const df_mtp_weights *w,
+                              const df_kv_cache *cache, const float *prev_hidden,
+                              const int32_t *token, int B, int n_steps, float temperature,
+                              const float *u_draft, float *hidden_out, int32_t *draft_out,
+                              float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
+                              df_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Mixture-of-experts FFN of the MTP block on its own (mtp.rs `MtpFfnWeightsGpu::Moe`; the

@@ -15,7 +15,8 @@ from typing import List, Optional, Sequence
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdflash.so")
+# DFLASH_LIB selects another build of the same library (the debug build, libdflash_debug.so).
+LIB_PATH = os.environ.get("DFLASH_LIB") or os.path.join(_PKG, "libdflash.so")
 
 DF_OK, DF_EINVAL, DF_ESHAPE, DF_ECAPACITY, DF_EWORKSPACE, DF_ECUDA, DF_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 STATUS_NAMES = {0: "DF_OK", -1: "DF_EINVAL", -2: "DF_ESHAPE", -3: "DF_ECAPACITY",
@@ -123,6 +124,24 @@ _SIGS = [
                                   c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
                                   c_void_p]),
+    ("df_test_wait_hook", c_int, [ctypes.c_longlong, c_int]),
+    ("df_trace_reset", c_int, []),
+    ("df_trace_read", c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int]),
+    ("df_sample_softmax_workspace_bytes", c_size_t, [c_int, c_int]),
+    ("sample_softmax", c_int, [c_void_p, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p,
+                               c_size_t, c_void_p, c_void_p]),
+    ("df_draft_round_stochastic_workspace_bytes", c_size_t, [POINTER(DFlashConfig), c_int, c_int,
+                                                             c_int]),
+    ("df_draft_round_stochastic", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights),
+                                          POINTER(KvCache), c_void_p, c_void_p, c_void_p, c_int,
+                                          c_int, c_int, c_void_p, c_float, c_void_p, c_void_p,
+                                          c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
+    ("mtp_forward_draft_sampled", c_int, [POINTER(MtpConfig), POINTER(MtpWeights),
+                                          POINTER(KvCache), c_void_p, c_void_p, c_int, c_int,
+                                          c_float, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_size_t, c_void_p, c_void_p]),
     ("df_attention_workspace_bytes", c_size_t, [c_int] * 6),
     ("df_attention", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
                              c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
@@ -410,6 +429,20 @@ def mtp_forward_draft(model: MtpModel, prev_hidden, token, n_steps: int, hidden_
                                    ws.numel(), _p(d_status), _stream(stream)))
 
 
+def mtp_forward_draft_sampled(model: MtpModel, prev_hidden, token, n_steps: int,
+                              temperature: float, u_draft, hidden_out, draft_out, logits_out, ws,
+                              d_status=None, stream=None):
+    """The sampled MTP chain: u_draft [n_steps, B]; draft_out [n_steps, B] int32 and
+    logits_out [n_steps, B, V] are outputs."""
+    B = token.shape[0]
+    _check(lib().mtp_forward_draft_sampled(
+        ctypes.byref(model.cfg), ctypes.byref(model.weights), ctypes.byref(model.cache_c),
+        _dev(prev_hidden, F32, "prev_hidden"), _dev(token, I32, "token"), B, n_steps,
+        float(temperature), _dev(u_draft, F32, "u_draft"), _dev(hidden_out, F32, "hidden_out"),
+        _dev(draft_out, I32, "draft_out"), _dev(logits_out, F32, "logits_out"), _p(ws),
+        ws.numel(), _p(d_status), _stream(stream)))
+
+
 def moe_ffn(model: MtpModel, x, out, ws, expert_ids=None, expert_w=None, d_status=None,
             stream=None):
     """The MoE FFN alone: out[T, H] from normalised rows x[T, H]; optional expert_ids
@@ -454,6 +487,70 @@ def accept_stochastic(draft_logits, target_logits, drafts, temperature: float, u
                                    _p(out["committed"]), _p(out["n_committed"]), _p(out["accept"]),
                                    _p(out["hit_eos"]), _p(out["rollback"]), _p(ws), ws.numel(),
                                    _p(d_status), _stream(stream)))
+
+
+def trace_reset():
+    _check(lib().df_trace_reset())
+
+
+def trace_read(max_records: int = 1 << 20):
+    """[(kernel id, SM, start ns, end ns)] of the CTAs recorded since trace_reset() (trace
+    builds only)."""
+    import numpy as np
+    kid = np.zeros(max_records, np.uint32)
+    sm = np.zeros(max_records, np.uint32)
+    t0 = np.zeros(max_records, np.uint64)
+    t1 = np.zeros(max_records, np.uint64)
+    n = lib().df_trace_read(kid.ctypes.data, sm.ctypes.data, t0.ctypes.data, t1.ctypes.data,
+                            max_records)
+    if n < 0:
+        _check(n)
+    return kid[:n], sm[:n], t0[:n], t1[:n]
+
+
+def test_wait_hook(wait_cycles: int, withhold_first: bool):
+    """Failure-detection test hook of the projection kernel (see include/dflash.h)."""
+    _check(lib().df_test_wait_hook(int(wait_cycles), 1 if withhold_first else 0))
+
+
+def sample_softmax_workspace_bytes(R: int, V: int) -> int:
+    return int(lib().df_sample_softmax_workspace_bytes(R, V))
+
+
+def sample_softmax(logits, temperature: float, u, tokens, ws, d_status=None, stream=None):
+    """logits [R, V] F32, u [R] F32 uniforms; tokens [R] int32 out: one draw per row from
+    softmax(logits / T)."""
+    R, V = logits.shape
+    _check(lib().sample_softmax(_dev(logits, F32, "logits"), R, V, float(temperature),
+                                _dev(u, F32, "u"), _dev(tokens, I32, "tokens"), _p(ws), ws.numel(),
+                                _p(d_status), _stream(stream)))
+
+
+def draft_round_stochastic_workspace_bytes(model: "DFlashModel", B: int, K: int,
+                                           n_new_max: int) -> int:
+    return int(lib().df_draft_round_stochastic_workspace_bytes(ctypes.byref(model.cfg), B, K,
+                                                               n_new_max))
+
+
+def df_draft_round_stochastic(model: "DFlashModel", last_token, target_hidden_new, n_new,
+                              n_new_max: int, K: int, target_logits, temperature: float, u_draft,
+                              u_accept, u_sample, eos, target_seq_len, logits_out, drafts_out,
+                              out: "RoundOutputs", ws, d_status=None, stream=None):
+    """The non-greedy round: target_logits [B, K+1, V]; u_draft, u_accept [B, K]; u_sample [B];
+    logits_out [B, K+1, V] and drafts_out [B, K] are outputs, as are out.committed etc.
+    (out.argmax is not written)."""
+    B = last_token.shape[0]
+    n_eos = 0 if eos is None else eos.numel()
+    _check(lib().df_draft_round_stochastic(
+        ctypes.byref(model.cfg), ctypes.byref(model.weights), ctypes.byref(model.cache_c),
+        _dev(last_token, I32, "last_token"), _dev(target_hidden_new, F32, "target_hidden_new"),
+        _dev(n_new, I32, "n_new"), n_new_max, B, K, _dev(target_logits, F32, "target_logits"),
+        float(temperature), _dev(u_draft, F32, "u_draft"), _dev(u_accept, F32, "u_accept"),
+        _dev(u_sample, F32, "u_sample"), _dev(eos, I32, "eos"), n_eos,
+        _dev(target_seq_len, I32, "target_seq_len"), _dev(logits_out, F32, "logits_out"),
+        _dev(drafts_out, I32, "drafts_out"), _p(out.committed), _p(out.n_committed),
+        _p(out.accept), _p(out.hit_eos), _p(out.rollback), _p(ws), ws.numel(), _p(d_status),
+        _stream(stream)))
 
 
 def generate_workspace_bytes(model: "DFlashModel", B: int, K: int, n_new_max: int) -> int:

@@ -17,6 +17,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdflash.so")
+# The debug build: device-side index checks that write DF_EINVAL to the status word (DF_DEBUG).
+DEBUG_LIB = os.path.join(PKG, "libdflash_debug.so")
+# The trace build: per-CTA kernel spans in one device buffer (DF_TRACE; relocatable device code).
+TRACE_LIB = os.path.join(PKG, "libdflash_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -35,21 +39,28 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, debug: bool = False,
+          trace: bool = False) -> str:
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    lib = DEBUG_LIB if debug else (TRACE_LIB if trace else LIB)
+    objdir = os.path.join(BUILD, "debug" if debug else "trace") if (debug or trace) else BUILD
+    os.makedirs(objdir, exist_ok=True)
     srcs = sources()
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     deps.append(os.path.join(INCLUDE, "dflash.h"))
-    if not force and os.path.exists(LIB):
-        t_lib = os.path.getmtime(LIB)
+    if not force and os.path.exists(lib):
+        t_lib = os.path.getmtime(lib)
         if all(os.path.getmtime(d) <= t_lib for d in deps):
-            return LIB
+            return lib
     flags = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
              "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC] + ARCH
+    if debug:
+        flags.append("-DDF_DEBUG=1")
+    if trace:
+        flags += ["-DDF_TRACE=1", "-rdc=true"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,15 +72,17 @@ def build(verbose: bool = False, force: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
     cuda_lib = os.path.join(_cuda_home(nvcc), "lib64")
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, "-shared", "-cudart", "shared", "-o", tmp] + objs + ARCH + [
+    tmp = lib + ".tmp"
+    cmd = [nvcc, "-shared", "-cudart", "shared", "-o", tmp] + (["-rdc=true"] if trace else []) + \
+        objs + ARCH + [
         "-Xlinker", f"-rpath={cuda_lib}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, force="--force" in sys.argv))
+    print(build(verbose=True, force="--force" in sys.argv, debug="--debug" in sys.argv,
+                trace="--trace" in sys.argv))

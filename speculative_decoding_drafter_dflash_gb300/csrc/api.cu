@@ -29,6 +29,23 @@ int fail(int code, const char *fmt, ...) {
 }
 
 // ---------------------------------------------------------------- launch set-up
+int sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char *e = getenv("DF_PDL");
@@ -107,7 +124,6 @@ int cuda_check(const char *what, cudaStream_t s) {
 
 namespace {
 
-constexpr int kArgmaxGridMax = 4 * kNumSMs;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -198,6 +214,7 @@ int check_cache(const df_kv_cache *k, int n_layers, int B, int d) {
 struct DFlashWs {
     float *h, *defer, *q, *kb, *vb, *cos_t, *sin_t, *attn_part, *h_final;
     float *ss_in, *ss_post;   // slice sums of squares of the deferred input / post-attention norms
+    int ss_slots;             // slots per row of ss_in / ss_post (one per 128-column tile of H)
     size_t defer_floats;
     uint16_t *xp_ctx, *xp_qkv, *xp_o, *xp_ffn, *xp_act, *xp_head;
     ArgTop *amax_part;
@@ -206,21 +223,23 @@ struct DFlashWs {
     TcScratch tc;
 };
 
-int n_counters_for(long long rows) { return (int)(rows / 64 + 256); }
-
 // Room for the split partial sums of a projection with N outputs over T tokens: the splits S
 // satisfy S * ceil(N / 128) <= SMs, so S * N < (SMs + S) * 128.
 size_t defer_floats_for(int T, long long N) {
-    return (size_t)T * (size_t)(2 * kNumSMs * 128 + N);
+    return (size_t)T * (size_t)(2 * (size_t)sm_count() * 128 + N);
 }
 
-void carve_tc(Carve &cv, TcScratch &tc, int max_tokens, long long max_rows) {
-    tc.partial_floats = tc_partial_floats(max_tokens);
+// ctas: the projection grid (every SM by default).
+void carve_tc(Carve &cv, TcScratch &tc, int max_tokens, long long max_rows, int ctas = 0) {
+    tc.max_ctas = ctas > 0 ? ctas : sm_count();
+    tc.partial_floats = tc_partial_floats(max_tokens, tc.max_ctas);
     tc.partials = cv.take<float>(tc.partial_floats);
     tc.n_counters = n_counters_for(max_rows);
     tc.counters = cv.take<int>((size_t)tc.n_counters);
-    tc.max_ctas = kNumSMs;
 }
+
+// Argmax partials of an lm_head over `rows` rows: one per (projection CTA, row).
+size_t argmax_parts(int rows) { return (size_t)sm_count() * (size_t)rows; }
 
 void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int blk, int n_new_max,
                   int cap, bool round) {
@@ -229,8 +248,9 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     const size_t T_blk = (size_t)B * blk, T_ctx = (size_t)B * n_new_max, T_all = T_blk + T_ctx;
     const size_t fc_in = (size_t)c->n_target_layers * H, qt = (size_t)nq * d, kt = (size_t)nkv * d;
     w.h = cv.take<float>(T_blk * H);
-    w.ss_in = cv.take<float>(T_all * (size_t)pack_slices(H));   // block rows, then context rows
-    w.ss_post = cv.take<float>(T_blk * (size_t)pack_slices(H));
+    w.ss_slots = std::max((H + 127) / 128, pack_slices(H));
+    w.ss_in = cv.take<float>(T_all * (size_t)w.ss_slots);   // block rows, then context rows
+    w.ss_post = cv.take<float>(T_blk * (size_t)w.ss_slots);
     // deferred split-K sums of one projection: S x T x N floats with S * N <= SMs * 128
     w.defer_floats = defer_floats_for((int)T_all, (long long)std::max<size_t>(qt + 2 * kt, H));
     w.defer = cv.take<float>(w.defer_floats);
@@ -260,7 +280,7 @@ void carve_dflash(Carve &cv, DFlashWs &w, const df_dflash_config *c, int B, int 
     w.h_final = nullptr;   // the round defers the final norm to the lm_head (no h_final)
     if (round) {
         w.xp_head = cv.take<uint16_t>(2 * T_blk * H);
-        w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * T_blk);
+        w.amax_part = cv.take<ArgTop>(argmax_parts((int)T_blk));
     } else {
         w.xp_head = nullptr;
         w.amax_part = nullptr;
@@ -347,7 +367,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         q.K = H;
         q.nvalid = n_new;
         q.rows_per_seq = n_new_max;
-        q.ss_out = ws.ss_in + (size_t)T_blk * pack_slices(H);
+        q.ss_out = ws.ss_in + (size_t)T_blk * ws.ss_slots;
+        q.ss_ld = ws.ss_slots;
         q.status = st;
         DF_TRY(launch_pack(q, s));
     }
@@ -381,12 +402,13 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         p.T = T_blk;
         p.K = H;
         p.ss_out = ws.ss_in;
+        p.ss_ld = ws.ss_slots;
         p.status = st;
         DF_TRY(launch_pack(p, s));
         // 1/rms of a deferred norm as the row scale of the projection that consumes it
         auto row_scale = [&](GemmArgs &g, const float *ss) {
             g.rs_ss = ss;
-            g.rs_n = pack_slices(H);
+            g.rs_n = ws.ss_slots;
             g.rs_rows = T_blk;
             g.rs_inv_k = 1.f / (float)H;
             g.rs_eps = c->rms_eps;
@@ -470,28 +492,30 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         go.X = ws.xp_o;
         go.ldx = qt;
         go.T = T_blk;
-        int S_o = 0;
-        DF_TRY(deferred(go, T_blk, H, "gemm_o", &S_o));
-
-        // h += O-projection partials (fused residual add), then post-attention RMSNorm
-        PackArgs pf;
-        pf.src = ws.h;
-        pf.lds = H;
-        pf.part = ws.defer;
-        pf.n_part = S_o;
-        pf.part_stride = (size_t)T_blk * H;
-        pf.ldpart = H;
-        pf.h_out = ws.h;
-        pf.ldh = H;
-        pf.norm_w = L.post_attn_norm;
-        pf.eps = c->rms_eps;
-        pf.pack = ws.xp_ffn;
-        pf.ldp = H;
-        pf.T = T_blk;
-        pf.K = H;
-        pf.ss_out = ws.ss_post;
-        pf.status = st;
-        DF_TRY(launch_pack(pf, s));
+        {
+            // h += O-projection partials (fused residual add), then post-attention RMSNorm
+            int S_o = 0;
+            DF_TRY(deferred(go, T_blk, H, "gemm_o", &S_o));
+            PackArgs pf;
+            pf.src = ws.h;
+            pf.lds = H;
+            pf.part = ws.defer;
+            pf.n_part = S_o;
+            pf.part_stride = (size_t)T_blk * H;
+            pf.ldpart = H;
+            pf.h_out = ws.h;
+            pf.ldh = H;
+            pf.norm_w = L.post_attn_norm;
+            pf.eps = c->rms_eps;
+            pf.pack = ws.xp_ffn;
+            pf.ldp = H;
+            pf.T = T_blk;
+            pf.K = H;
+            pf.ss_out = ws.ss_post;
+            pf.ss_ld = ws.ss_slots;
+            pf.status = st;
+            DF_TRY(launch_pack(pf, s));
+        }
 
         GemmArgs gu;
         gu.W0 = L.w_gate;
@@ -509,7 +533,6 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gu.status = st;
         gu.name = "gemm_gate_up";
         row_scale(gu, ws.ss_post);
-        DF_TRY(launch_gemm_tc(gu, ws.tc, s));
 
         GemmArgs gd;
         gd.W0 = L.w_down;
@@ -519,6 +542,7 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gd.X = ws.xp_act;
         gd.ldx = I;
         gd.T = T_blk;
+        DF_TRY(launch_gemm_tc(gu, ws.tc, s));
         DF_TRY(deferred(gd, T_blk, H, "gemm_down", &S_down));
     }
     // h += last down-projection partials, then the final norm
@@ -536,20 +560,29 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
     pfin.pack = final_pack;
     // Without h_final (the draft round) the final norm is deferred to the lm_head: x * final_norm
     // is packed, its sums of squares reuse the post-attention ones (the last gate/up has read them)
-    if (!h_final) pfin.ss_out = ws.ss_post;
+    if (!h_final) {
+        pfin.ss_out = ws.ss_post;
+        pfin.ss_ld = ws.ss_slots;
+    }
     pfin.ldp = H;
     pfin.T = T_blk;
     pfin.K = H;
     pfin.status = st;
-    DF_TRY(launch_pack(pfin, s));
-    return launch_seq_advance(cache->seq_len, n_new, B, 0, cache->cap, st, s);
+    // the drafter cache advances by n_new here: the last layer's kernels have read seq_len
+    pfin.adv_seq = cache->seq_len;
+    pfin.adv_n = n_new;
+    pfin.adv_B = B;
+    pfin.adv_cap = cache->cap;
+    return launch_pack(pfin, s);
 }
 
 // rs_ss: the packed rows carry a deferred RMSNorm (slice sums of squares, as the row prologue
 // writes them); the logits are scaled by 1/rms per row before the argmax.
-int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
-                 int32_t *idx, float *top1, float *top2, const TcScratch &tc, cudaStream_t s,
-                 const float *rs_ss = nullptr, float rs_eps = 0.f) {
+// The lm_head projection with the running-argmax epilogue; G receives the number of partial
+// states per row it leaves in `part`.
+int lm_head_gemm(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
+                 const TcScratch &tc, cudaStream_t s, const float *rs_ss, float rs_eps, int rs_n,
+                 int *G) {
     GemmArgs g;
     g.W0 = Wlm;
     g.n0 = V;
@@ -563,7 +596,31 @@ int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V
     g.name = "gemm_lm_head_argmax";
     if (rs_ss) {
         g.rs_ss = rs_ss;
-        g.rs_n = pack_slices(H);
+        g.rs_n = rs_n > 0 ? rs_n : pack_slices(H);
+        g.rs_rows = rows;
+        g.rs_inv_k = 1.f / (float)H;
+        g.rs_eps = rs_eps;
+    }
+    return launch_gemm_tc(g, tc, s, G);
+}
+
+int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
+                 int32_t *idx, float *top1, float *top2, const TcScratch &tc, cudaStream_t s,
+                 const float *rs_ss = nullptr, float rs_eps = 0.f, int rs_n = 0) {
+    GemmArgs g;
+    g.W0 = Wlm;
+    g.n0 = V;
+    g.N = V;
+    g.K = H;
+    g.X = xp;
+    g.ldx = H;
+    g.T = rows;
+    g.epi = EPI_ARGMAX;
+    g.part = part;
+    g.name = "gemm_lm_head_argmax";
+    if (rs_ss) {
+        g.rs_ss = rs_ss;
+        g.rs_n = rs_n > 0 ? rs_n : pack_slices(H);
         g.rs_rows = rows;
         g.rs_inv_k = 1.f / (float)H;
         g.rs_eps = rs_eps;
@@ -647,7 +704,51 @@ int host_round_graph(uint64_t key, F &&enqueue, cudaStream_t user) {
 
 using namespace df;
 
+#if DF_TRACE
+namespace df {
+__device__ TraceRec g_trace[kTraceMax];
+__device__ unsigned g_trace_n;
+}  // namespace df
+#endif
+
 extern "C" {
+
+int df_trace_reset(void) {
+#if DF_TRACE
+    const unsigned zero = 0;
+    cudaError_t e = cudaMemcpyToSymbol(df::g_trace_n, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(DF_ECUDA, "df_trace_reset: %s", cudaGetErrorString(e));
+    return DF_OK;
+#else
+    return fail(DF_EINVAL, "df_trace_reset: this library is not a trace build");
+#endif
+}
+
+int df_trace_read(uint32_t *kid, uint32_t *sm, unsigned long long *t0, unsigned long long *t1,
+                  int max_records) {
+#if DF_TRACE
+    if (!kid || !sm || !t0 || !t1 || max_records < 0)
+        return fail(DF_EINVAL, "df_trace_read: NULL output");
+    cudaError_t e = cudaDeviceSynchronize();
+    unsigned n = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&n, df::g_trace_n, sizeof(n));
+    if (e != cudaSuccess) return fail(DF_ECUDA, "df_trace_read: %s", cudaGetErrorString(e));
+    n = std::min<unsigned>(std::min(n, kTraceMax), (unsigned)max_records);
+    std::vector<TraceRec> rec(n);
+    if (n) e = cudaMemcpyFromSymbol(rec.data(), df::g_trace, sizeof(TraceRec) * n);
+    if (e != cudaSuccess) return fail(DF_ECUDA, "df_trace_read: %s", cudaGetErrorString(e));
+    for (unsigned i = 0; i < n; ++i) {
+        kid[i] = rec[i].kid;
+        sm[i] = rec[i].sm;
+        t0[i] = rec[i].t0;
+        t1[i] = rec[i].t1;
+    }
+    return (int)n;
+#else
+    (void)kid, (void)sm, (void)t0, (void)t1, (void)max_records;
+    return fail(DF_EINVAL, "df_trace_read: this library is not a trace build");
+#endif
+}
 
 const char *df_last_error(void) { return g_err; }
 
@@ -730,12 +831,7 @@ int dflash_block_forward(const df_dflash_config *cfg, const df_dflash_weights *w
 size_t df_lm_head_workspace_bytes(int rows, int H, int V) {
     if (rows <= 0 || H <= 0 || V <= 0) return 0;
     if (rows > kMaxTcTokens) return 0;
-    Carve cv{nullptr, 0, ~size_t(0), true};
-    cv.take<uint16_t>((size_t)2 * rows * H);
-    cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
-    TcScratch tc;
-    carve_tc(cv, tc, rows, V);
-    return cv.off;
+    return lm_head_scratch_bytes_for(rows, H, V, sm_count());
 }
 
 int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
@@ -748,10 +844,11 @@ int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, in
     REQ(idx, DF_EINVAL, "idx is NULL");
     DF_TRY(get_ws(ws, ws_bytes, df_lm_head_workspace_bytes(rows, H, V)));
     Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    const int ctas = sm_count();
     uint16_t *xp = cv.take<uint16_t>((size_t)2 * rows * H);
-    ArgTop *part = cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    ArgTop *part = cv.take<ArgTop>((size_t)ctas * rows);
     TcScratch tc;
-    carve_tc(cv, tc, rows, V);
+    carve_tc(cv, tc, rows, V, ctas);
     cudaStream_t s = (cudaStream_t)stream;
     PackArgs p;
     p.src = X;
@@ -867,19 +964,11 @@ int df_attention(const float *q, const float *cache_k, const float *cache_v, int
     return launch_attn(a, (cudaStream_t)stream);
 }
 
-static void carve_sample(Carve &cv, SampleArgs &a, int B, int K, int V) {
-    a.n_chunks = sample_chunks(V);
-    a.stats = cv.take<MaxSum>((size_t)B * (2 * K + 1) * a.n_chunks);
-    a.state = cv.take<SampleState>((size_t)B);
-    a.csum = cv.take<float>((size_t)B * a.n_chunks);
-    a.counters = cv.take<int>((size_t)B);
-}
-
 size_t df_accept_stochastic_workspace_bytes(int B, int K, int V) {
-    if (B <= 0 || K < 1 || K > 64 || V <= 0 || V % 4 != 0) return 0;
+    if (B <= 0 || K < 1 || K > kSampleMaxK || V <= 0 || V % 4 != 0) return 0;
     Carve cv{nullptr, 0, ~size_t(0), true};
     SampleArgs a;
-    carve_sample(cv, a, B, K, V);
+    carve_sample_scratch(cv, a, B, K, V);
     return cv.off;
 }
 
@@ -903,14 +992,15 @@ int accept_stochastic(const float *draft_logits, const float *target_logits, int
     DF_TRY(get_ws(ws, ws_bytes, df_accept_stochastic_workspace_bytes(B, K, V)));
     SampleArgs a;
     Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
-    carve_sample(cv, a, B, K, V);
+    carve_sample_scratch(cv, a, B, K, V);
     a.draft = draft_logits;
+    a.draft_ld = K;
     a.target = target_logits;
     a.V = V;
     a.B = B;
     a.K = K;
     a.T = temperature;
-    a.scale = (float)(1.4426950408889634 / (double)temperature);
+    sample_constants(a);
     a.drafts = drafts;
     a.u_accept = u_accept;
     a.u_sample = u_sample;
@@ -923,6 +1013,42 @@ int accept_stochastic(const float *draft_logits, const float *target_logits, int
     a.rollback = rollback;
     a.status = d_status;
     return launch_accept_stochastic(a, (cudaStream_t)stream);
+}
+
+size_t df_sample_softmax_workspace_bytes(int R, int V) {
+    if (R <= 0 || V <= 0 || V % 4 != 0) return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    SampleArgs a;
+    carve_sample_scratch(cv, a, R, 1, V);
+    return cv.off;
+}
+
+int sample_softmax(const float *logits, int R, int V, float temperature, const float *u,
+                   int32_t *tokens, void *ws, size_t ws_bytes, int32_t *d_status,
+                   df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(R > 0, DF_ESHAPE, "R=%d", R);
+    REQ(V > 0 && V % 4 == 0, DF_ESHAPE, "V=%d (a positive multiple of 4)", V);
+    REQ(temperature > 0.f, DF_EINVAL, "temperature=%g (temperature 0 is the argmax)",
+        (double)temperature);
+    REQ(logits && u && tokens, DF_EINVAL, "NULL input or output");
+    DF_TRY(check_bf16(logits, "logits"));      // 16-byte alignment
+    DF_TRY(get_ws(ws, ws_bytes, df_sample_softmax_workspace_bytes(R, V)));
+    SampleArgs a;
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    carve_sample_scratch(cv, a, R, 1, V);
+    a.draft = logits;
+    a.draft_ld = 1;
+    a.V = V;
+    a.B = R;
+    a.K = 1;
+    a.T = temperature;
+    sample_constants(a);
+    a.sample_mode = 1;
+    a.u_draft = u;
+    a.drafts_out = tokens;
+    a.status = d_status;
+    return launch_sample_drafts(a, (cudaStream_t)stream);
 }
 
 int accept_prefix_argmax(const int32_t *drafts, int drafts_ld, const int32_t *target, int B,
@@ -1006,10 +1132,124 @@ int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
     cudaStream_t s = (cudaStream_t)stream;
     DF_TRY(dflash_forward_impl(cfg, w, cache, nullptr, last_token, target_hidden_new, n_new,
                                n_new_max, B, blk, W.h_final, W.xp_head, W, d_status, s));
-    DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
-                        argmax_out, nullptr, nullptr, W.tc, s, W.ss_post, cfg->rms_eps));
-    return launch_accept(argmax_out + 1, blk, target_argmax, B, K, eos, n_eos, committed,
-                         n_committed, accept_count, hit_eos, rollback, target_seq_len, d_status, s);
+    if (blk > 32) {
+        DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
+                            argmax_out, nullptr, nullptr, W.tc, s, W.ss_post, cfg->rms_eps,
+                            W.ss_slots));
+        return launch_accept(argmax_out + 1, blk, target_argmax, B, K, eos, n_eos, committed,
+                             n_committed, accept_count, hit_eos, rollback, target_seq_len,
+                             d_status, s);
+    }
+    // the lm_head's argmax partials, then the argmax merge and the accept walk in one launch
+    int G = 0;
+    DF_TRY(lm_head_gemm(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
+                        W.tc, s, W.ss_post, cfg->rms_eps, W.ss_slots, &G));
+    return launch_argmax_accept(W.amax_part, G, B, blk, argmax_out, target_argmax, eos, n_eos,
+                                committed, n_committed, accept_count, hit_eos, rollback,
+                                target_seq_len, d_status, s);
+}
+
+size_t df_draft_round_stochastic_workspace_bytes(const df_dflash_config *cfg, int B, int K,
+                                                 int n_new_max) {
+    if (check_cfg(cfg) != DF_OK || B <= 0 || K < 1 || K > kSampleMaxK || n_new_max < 0 ||
+        cfg->vocab % 4 != 0)
+        return 0;
+    Carve cv{nullptr, 0, ~size_t(0), true};
+    DFlashWs w;
+    carve_dflash(cv, w, cfg, B, K + 1, n_new_max, 1 << 20, true);
+    SampleArgs a;
+    carve_sample_scratch(cv, a, B, K, cfg->vocab);
+    return cv.off;
+}
+
+int df_draft_round_stochastic(const df_dflash_config *cfg, const df_dflash_weights *w,
+                              const df_kv_cache *cache, const int32_t *last_token,
+                              const float *target_hidden_new, const int32_t *n_new,
+                              int n_new_max, int B, int K, const float *target_logits,
+                              float temperature, const float *u_draft, const float *u_accept,
+                              const float *u_sample, const int32_t *eos, int n_eos,
+                              int32_t *target_seq_len, float *logits_out, int32_t *drafts_out,
+                              int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                              int32_t *hit_eos, int32_t *rollback, void *ws, size_t ws_bytes,
+                              int32_t *d_status, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_cfg(cfg));
+    DF_TRY(check_weights(cfg, w));
+    REQ(B > 0 && K >= 1 && K <= kSampleMaxK, DF_ESHAPE, "B=%d K=%d (1 <= K <= %d)", B, K,
+        kSampleMaxK);
+    REQ(cfg->vocab % 4 == 0, DF_ESHAPE, "vocab=%d (a multiple of 4)", cfg->vocab);
+    REQ(temperature > 0.f, DF_EINVAL, "temperature=%g (temperature 0 is df_draft_round)",
+        (double)temperature);
+    const int blk = K + 1;
+    REQ(n_new_max >= 0 && n_new_max <= (cache ? cache->cap : 0), DF_ESHAPE, "n_new_max=%d",
+        n_new_max);
+    DF_TRY(check_cache(cache, cfg->n_layers, B, cfg->head_dim));
+    REQ(last_token && target_logits && u_draft && u_accept && u_sample && target_seq_len &&
+            logits_out && drafts_out && committed && n_committed && accept_count && hit_eos &&
+            rollback,
+        DF_EINVAL, "NULL round input or output");
+    REQ(n_new_max == 0 || (target_hidden_new && n_new), DF_EINVAL,
+        "target_hidden_new / n_new is NULL");
+    REQ(n_eos >= 0 && (n_eos == 0 || eos), DF_EINVAL, "eos list");
+    DF_TRY(check_f32(target_logits, "target_logits"));
+    DF_TRY(check_f32(logits_out, "logits_out"));
+    DF_TRY(get_ws(ws, ws_bytes, df_draft_round_stochastic_workspace_bytes(cfg, B, K, n_new_max)));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    DFlashWs W;
+    carve_dflash(cv, W, cfg, B, blk, n_new_max, cache->cap, true);
+    SampleArgs a;
+    carve_sample_scratch(cv, a, B, K, cfg->vocab);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int H = cfg->hidden, V = cfg->vocab;
+    DF_TRY(dflash_forward_impl(cfg, w, cache, nullptr, last_token, target_hidden_new, n_new,
+                               n_new_max, B, blk, W.h_final, W.xp_head, W, d_status, s));
+    // logits of every block row (final norm deferred to the row scale, as in the greedy round)
+    GemmArgs gl;
+    gl.W0 = w->lm_head;
+    gl.n0 = V;
+    gl.N = V;
+    gl.K = H;
+    gl.X = W.xp_head;
+    gl.ldx = H;
+    gl.T = B * blk;
+    gl.epi = EPI_STORE;
+    gl.out = logits_out;
+    gl.ldo = V;
+    gl.status = d_status;
+    gl.name = "gemm_lm_head_logits";
+    gl.rs_ss = W.ss_post;
+    gl.rs_n = W.ss_slots;
+    gl.rs_rows = B * blk;
+    gl.rs_inv_k = 1.f / (float)H;
+    gl.rs_eps = cfg->rms_eps;
+    DF_TRY(launch_gemm_tc(gl, W.tc, s));
+    // drafts i = 1..K drawn from softmax(logits / T), then the accept step
+    a.draft = logits_out + V;
+    a.draft_ld = blk;
+    a.target = target_logits;
+    a.V = V;
+    a.B = B;
+    a.K = K;
+    a.T = temperature;
+    sample_constants(a);
+    a.sample_mode = 1;
+    a.u_draft = u_draft;
+    a.drafts_out = drafts_out;
+    a.status = d_status;
+    DF_TRY(launch_sample_drafts(a, s));
+    a.sample_mode = 0;
+    a.drafts = drafts_out;
+    a.u_accept = u_accept;
+    a.u_sample = u_sample;
+    a.eos = eos;
+    a.n_eos = n_eos;
+    a.committed = committed;
+    a.n_committed = n_committed;
+    a.accept_count = accept_count;
+    a.hit_eos = hit_eos;
+    a.rollback = rollback;
+    DF_TRY(launch_accept_stochastic(a, s));
+    return launch_rollback(target_seq_len, rollback, B, d_status, s);
 }
 
 size_t df_draft_round_host_workspace_bytes(const df_dflash_config *cfg, int B, int K,
@@ -1356,7 +1596,8 @@ int df_generate(const df_dflash_config *cfg, const df_dflash_weights *w, const d
                                      B, blk, W.h_final, W.xp_head, W, d_status, cs);
         if (rc == DF_OK)
             rc = lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
-                              a.argmax, nullptr, nullptr, W.tc, cs, W.ss_post, cfg->rms_eps);
+                              a.argmax, nullptr, nullptr, W.tc, cs, W.ss_post, cfg->rms_eps,
+                              W.ss_slots);
         if (rc == DF_OK) rc = launch_loop_verify(a, cs);
         if (rc == DF_OK)
             rc = launch_accept(a.argmax + 1, blk, a.target, B, K, eos, n_eos, a.committed,
@@ -1540,7 +1781,7 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     w.xp_ffn = cv.take<uint16_t>((size_t)2 * B * H);
     w.xp_act = cv.take<uint16_t>((size_t)2 * B * std::max<size_t>(I, 1));
     w.xp_head = cv.take<uint16_t>((size_t)2 * B * H);
-    w.amax_part = cv.take<ArgTop>((size_t)kArgmaxGridMax * B);
+    w.amax_part = cv.take<ArgTop>(argmax_parts(B));
     if (c->n_experts) carve_moe(cv, w.moe, c, B);
     else w.moe = MoeWs{};
     long long rows = std::max<long long>({(long long)c->vocab, 2LL * (long long)I,
@@ -1558,15 +1799,25 @@ size_t df_mtp_workspace_bytes(const df_mtp_config *cfg, int B) {
     Carve cv{nullptr, 0, ~size_t(0), true};
     MtpWs w;
     carve_mtp(cv, w, cfg, B, 1 << 20);
+    SampleArgs a;
+    carve_sample_scratch(cv, a, B, 1, cfg->vocab);
     return cv.off;
 }
 
-int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
-                      const df_kv_cache *cache, const float *prev_hidden, const int32_t *token,
-                      int B, int n_steps, float *hidden_out, int32_t *argmax_out,
-                      float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
-                      df_stream_t stream) {
-    g_err[0] = 0;
+}  // extern "C"
+
+namespace df {
+namespace {
+
+// The chained MTP draft. temperature == 0: each step's token is the lm_head argmax (and the
+// last step's logits are stored when logits_out is given). temperature > 0: every step stores
+// its logits in logits_out [n_steps, B, V] and its token is drawn from softmax(logits / T) with
+// u_draft [n_steps, B]; argmax_out then receives the drawn tokens.
+int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cache *cache,
+             const float *prev_hidden, const int32_t *token, int B, int n_steps,
+             float *hidden_out, int32_t *argmax_out, float *logits_out, float temperature,
+             const float *u_draft, void *ws, size_t ws_bytes, int32_t *d_status,
+             df_stream_t stream) {
     DF_TRY(check_mtp_cfg(cfg));
     DF_TRY(check_mtp_weights(cfg, w));
     REQ(B > 0 && n_steps >= 1, DF_ESHAPE, "B=%d n_steps=%d", B, n_steps);
@@ -1574,10 +1825,18 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
     REQ(prev_hidden && token && hidden_out && argmax_out, DF_EINVAL, "NULL MTP input or output");
     REQ(cfg->n_experts == 0 || B <= kMoeMaxRows, DF_ESHAPE, "MoE MTP takes B <= %d (B=%d)",
         kMoeMaxRows, B);
+    const bool sampled = temperature > 0.f;
+    if (sampled) {
+        REQ(logits_out && u_draft, DF_EINVAL, "a sampled MTP draft needs logits_out and u_draft");
+        REQ(cfg->vocab % 4 == 0, DF_ESHAPE, "vocab=%d (a multiple of 4)", cfg->vocab);
+        DF_TRY(check_f32(logits_out, "logits_out"));
+    }
     DF_TRY(get_ws(ws, ws_bytes, df_mtp_workspace_bytes(cfg, B)));
     Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
     MtpWs W;
     carve_mtp(cv, W, cfg, B, cache->cap);
+    SampleArgs sa;
+    carve_sample_scratch(cv, sa, B, 1, cfg->vocab);
     cudaStream_t s = (cudaStream_t)stream;
     const int H = cfg->hidden, d = cfg->head_dim, nq = cfg->n_q_heads, nkv = cfg->n_kv_heads;
     const int rot = cfg->rotary_dim ? cfg->rotary_dim : d;
@@ -1808,6 +2067,37 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         // shared head: RMSNorm then lm_head argmax (mtp.rs `forward_ffn_residual`,
         // `forward_shared_head`)
         DF_TRY(launch_pack(pk, s));
+        if (sampled) {
+            // this step's logits, then its draft drawn from softmax(logits / T)
+            float *lg = logits_out + (size_t)st * B * cfg->vocab;
+            GemmArgs gl;
+            gl.W0 = w->lm_head;
+            gl.n0 = cfg->vocab;
+            gl.N = cfg->vocab;
+            gl.K = H;
+            gl.X = W.xp_head;
+            gl.ldx = H;
+            gl.T = B;
+            gl.epi = EPI_STORE;
+            gl.out = lg;
+            gl.ldo = cfg->vocab;
+            gl.status = d_status;
+            gl.name = "gemm_logits";
+            DF_TRY(launch_gemm_tc(gl, W.tc, s));
+            sa.draft = lg;
+            sa.draft_ld = 1;
+            sa.V = cfg->vocab;
+            sa.B = B;
+            sa.K = 1;
+            sa.T = temperature;
+            sample_constants(sa);
+            sa.sample_mode = 1;
+            sa.u_draft = u_draft + (size_t)st * B;
+            sa.drafts_out = argmax_out + (size_t)st * B;
+            sa.status = d_status;
+            DF_TRY(launch_sample_drafts(sa, s));
+            continue;
+        }
         DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B, H, cfg->vocab, W.amax_part,
                             argmax_out + (size_t)st * B, nullptr, nullptr, W.tc, s));
         if (logits_out && st == n_steps - 1) {
@@ -1827,6 +2117,34 @@ int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
         }
     }
     return launch_seq_advance(cache->seq_len, nullptr, B, n_steps, cache->cap, d_status, s);
+}
+
+}  // namespace
+}  // namespace df
+
+extern "C" {
+
+int mtp_forward_draft(const df_mtp_config *cfg, const df_mtp_weights *w,
+                      const df_kv_cache *cache, const float *prev_hidden, const int32_t *token,
+                      int B, int n_steps, float *hidden_out, int32_t *argmax_out,
+                      float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
+                      df_stream_t stream) {
+    g_err[0] = 0;
+    return mtp_impl(cfg, w, cache, prev_hidden, token, B, n_steps, hidden_out, argmax_out,
+                    logits_out, 0.f, nullptr, ws, ws_bytes, d_status, stream);
+}
+
+int mtp_forward_draft_sampled(const df_mtp_config *cfg, const df_mtp_weights *w,
+                              const df_kv_cache *cache, const float *prev_hidden,
+                              const int32_t *token, int B, int n_steps, float temperature,
+                              const float *u_draft, float *hidden_out, int32_t *draft_out,
+                              float *logits_out, void *ws, size_t ws_bytes, int32_t *d_status,
+                              df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(temperature > 0.f, DF_EINVAL, "temperature=%g (temperature 0 is mtp_forward_draft)",
+        (double)temperature);
+    return mtp_impl(cfg, w, cache, prev_hidden, token, B, n_steps, hidden_out, draft_out,
+                    logits_out, temperature, u_draft, ws, ws_bytes, d_status, stream);
 }
 
 size_t df_moe_workspace_bytes(const df_mtp_config *cfg, int T) {
@@ -1876,28 +2194,19 @@ int df_moe_ffn(const df_mtp_config *cfg, const df_mtp_weights *w, const float *x
 // scratch carved from a caller-given region instead of a workspace argument.
 namespace df {
 
-size_t lm_head_scratch_bytes(int rows, int H, int V) {
-    if (rows <= 0 || rows > kMaxTcTokens || H <= 0 || V <= 0) return 0;
-    Carve cv{nullptr, 0, ~size_t(0), true};
-    cv.take<uint16_t>((size_t)2 * rows * H);
-    cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
-    TcScratch tc;
-    carve_tc(cv, tc, rows, V);
-    return cv.off;
-}
-
+// The lm_head argmax with its scratch at `scratch` and a grid of `ctas` CTAs.
 int lm_head_run(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
-                float *top1, float *top2, char *scratch, size_t scratch_bytes, bool zero_counters,
-                cudaStream_t s) {
+                float *top1, float *top2, char *scratch, size_t scratch_bytes, int ctas,
+                bool zero_counters, cudaStream_t s) {
     g_err[0] = 0;
     DF_TRY(check_bf16(W, "W"));
     DF_TRY(check_f32(X, "X"));
     REQ(idx, DF_EINVAL, "idx is NULL");
     Carve cv{scratch, 0, scratch_bytes, true};
     uint16_t *xp = cv.take<uint16_t>((size_t)2 * rows * H);
-    ArgTop *part = cv.take<ArgTop>((size_t)kArgmaxGridMax * rows);
+    ArgTop *part = cv.take<ArgTop>((size_t)ctas * rows);
     TcScratch tc;
-    carve_tc(cv, tc, rows, V);
+    carve_tc(cv, tc, rows, V, ctas);
     REQ(cv.ok, DF_EWORKSPACE, "scratch of %zu bytes is too small", scratch_bytes);
     if (zero_counters) {
         cudaError_t e = cudaMemsetAsync(tc.counters, 0, sizeof(int) * (size_t)tc.n_counters, s);

@@ -26,7 +26,12 @@ int cuda_check(const char *what, cudaStream_t s);
         if (df_rc_ != DF_OK) return df_rc_; \
     } while (0)
 
-constexpr int kNumSMs = 152;
+// SMs of the current device (queried once per device; kDefaultSMs, GB300's count, when no device
+// is visible, e.g. for workspace-size queries on a machine without a GPU). Grids, split counts,
+// scratch sizes and the attention chunk plan are derived from it, so a workspace sized on one
+// device is checked again against the device it runs on.
+constexpr int kDefaultSMs = 152;
+int sm_count();
 
 // ---------------------------------------------------------------- launches
 // Every kernel is launched with programmatic dependent launch: it may start while its
@@ -104,6 +109,74 @@ __device__ __forceinline__ void split_hi_lo(float y, uint16_t &hi, uint16_t &lo)
 
 __device__ __forceinline__ void set_status(int32_t *st, int code) {
     if (st) atomicCAS(st, 0, code);
+}
+
+// Trace builds (build.py --trace: -DDF_TRACE=1 with relocatable device code, a separate
+// libdflash_trace.so): every kernel's CTAs record (kernel id, SM, start, end) in nanoseconds of
+// the global timer into one device buffer, read back by df_trace_read; the launches of a CUDA
+// graph replay can then be timed one by one, overlap included. Normal builds record nothing.
+#ifndef DF_TRACE
+#define DF_TRACE 0
+#endif
+enum TraceKid : uint32_t {
+    TK_ROPE_TABLE = 1, TK_QK_ROPE, TK_ATTN, TK_ATTN_COMBINE, TK_SEQ_ADVANCE, TK_ATTN_TC,
+    TK_LOOP_INIT, TK_LOOP_PREPARE, TK_LOOP_VERIFY, TK_LOOP_APPEND, TK_LOOP_COMMIT, TK_MOE_ROUTER,
+    TK_MOE_GATE_UP, TK_MOE_DOWN, TK_PACK, TK_PACK_VEC, TK_ARGMAX_FINAL, TK_ACCEPT, TK_ROLLBACK,
+    TK_WORD_COPY, TK_SAMPLE_STATS, TK_SAMPLE_WALK, TK_SAMPLE_NORM, TK_SAMPLE_DRAW,
+    TK_GEMM = 100   // + 2 * epilogue + (stream-K fix-up ? 1 : 0)
+};
+struct TraceRec {
+    uint32_t kid, sm;
+    unsigned long long t0, t1;
+};
+constexpr unsigned kTraceMax = 1u << 20;
+#if DF_TRACE
+extern __device__ TraceRec g_trace[kTraceMax];
+extern __device__ unsigned g_trace_n;
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ uint32_t sm_id() {
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+    return v;
+}
+// Records the CTA's span when thread 0 leaves the kernel (its destructor runs at every return).
+struct TraceScope {
+    unsigned long long t0;
+    uint32_t kid;
+    __device__ explicit TraceScope(uint32_t k) : t0(global_ns()), kid(k) {}
+    __device__ ~TraceScope() {
+        if (threadIdx.x == 0 && threadIdx.y == 0) {
+            const unsigned i = atomicAdd(&g_trace_n, 1u);
+            if (i < kTraceMax) g_trace[i] = TraceRec{kid, sm_id(), t0, global_ns()};
+        }
+    }
+};
+#define DF_TRACE_KERNEL(kid) ::df::TraceScope df_trace_scope_((uint32_t)(kid))
+#else
+#define DF_TRACE_KERNEL(kid) \
+    do {                     \
+    } while (0)
+#endif
+
+// Debug builds (build.py --debug: -DDF_DEBUG=1, a separate libdflash_debug.so) check the
+// indices of stores whose positions come from device data or from index arithmetic over a
+// launch's geometry; a failed check writes DF_EINVAL to the call's status word and the access
+// is skipped. In normal builds the check is compiled out (always true).
+#ifndef DF_DEBUG
+#define DF_DEBUG 0
+#endif
+__device__ __forceinline__ bool df_in_bounds(bool ok, int32_t *status) {
+#if DF_DEBUG
+    if (!ok) set_status(status, DF_EINVAL);
+    return ok;
+#else
+    (void)status;
+    return true;
+#endif
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -199,10 +272,17 @@ struct PackArgs {
     size_t part_stride = 0;          // floats between splits
     int ldpart = 0;                  // floats between rows of one split
     // Deferred RMSNorm (needs norm_w and pack, no y_out): the row is split over pack_slices(K)
-    // CTAs without a cluster; pack receives x * norm_w (the numerator only) and ss_out[t * S + j]
-    // the sum of x^2 over slice j of row t. The 1/rms factor is applied by the consuming
-    // projection as a row scale (GemmArgs::rs_*), which the linearity of the projection allows.
+    // CTAs without a cluster; pack receives x * norm_w (the numerator only) and ss_out[t * L + j]
+    // the sum of x^2 over slice j of row t, L = ss_ld (pack_slices(K) when 0; slots past the
+    // slices are written as zeros). The 1/rms factor is applied by the consuming projection as
+    // a row scale (GemmArgs::rs_*), which the linearity of the projection allows.
     float *ss_out = nullptr;
+    int ss_ld = 0;
+    // Optional side job of CTA 0: seq_len[b] += n_new[b] for b < adv_B (capacity-checked as
+    // launch_seq_advance), when nothing later in the stream reads the old lengths.
+    int32_t *adv_seq = nullptr;
+    const int32_t *adv_n = nullptr;
+    int adv_B = 0, adv_cap = 0;
 };
 int launch_pack(const PackArgs &a, cudaStream_t s);
 // Number of CTAs (slices) a row of K elements is split over by the row prologue.
@@ -280,14 +360,28 @@ struct TcScratch {
     size_t partial_floats = 0;
     int *counters = nullptr;
     int n_counters = 0;
-    int max_ctas = kNumSMs;
+    int max_ctas = 0;        // CTAs of a launch (set by the carve)
 };
-inline size_t tc_partial_floats(int max_tokens) {
-    int t = max_tokens < kMaxTcTokens ? max_tokens : kMaxTcTokens;
-    return (size_t)kNumSMs * 2 * 128 * (size_t)(t > 0 ? t : 1);
+// Byte size of a carve of `bytes` (every carve starts on a 256-byte boundary).
+constexpr size_t carve_round(size_t bytes) { return (bytes + 255) & ~size_t(255); }
+// Partial tiles of a stream-K projection over at most max_tokens tokens with `ctas` CTAs.
+constexpr size_t tc_partial_floats(int max_tokens, int ctas) {
+    return (size_t)ctas * 2 * 128 *
+           (size_t)((max_tokens < kMaxTcTokens ? max_tokens : kMaxTcTokens) > 0
+                        ? (max_tokens < kMaxTcTokens ? max_tokens : kMaxTcTokens)
+                        : 1);
+}
+// Arrival counters of a projection with at most max_rows output rows.
+constexpr int n_counters_for(long long max_rows) { return (int)(max_rows / 64 + 256); }
+// Bytes of the scratch of an lm_head argmax over `rows` rows with `ctas` CTAs: packed rows, the
+// per-CTA argmax partials, the projection's partial tiles and counters (carved in this order).
+constexpr size_t lm_head_scratch_bytes_for(int rows, int H, int V, int ctas) {
+    return carve_round((size_t)2 * rows * H * 2) + carve_round((size_t)ctas * rows * sizeof(ArgTop)) +
+           carve_round(tc_partial_floats(rows, ctas) * 4) + carve_round((size_t)n_counters_for(V) * 4);
 }
 int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s,
                    int *n_partials_out = nullptr);
+
 
 // Reduce EPI_ARGMAX partials [G, T] into idx/top1/top2 [T].
 int launch_argmax_final(const ArgTop *part, int G, int T, int32_t *idx, float *top1,
@@ -361,22 +455,31 @@ int launch_attn(const AttnArgs &a, cudaStream_t s);
 bool attn_tc_supported(int d, int rows);
 int launch_attn_tc(const AttnArgs &a, cudaStream_t s);
 
-// Non-greedy accept step (speculative sampling) over B sequences of K drafts and vocab V.
+// Non-greedy path over B sequences of K drafts and vocab V: drafts drawn from the drafter's
+// softmax (sample mode) and the speculative-sampling accept step (accept mode).
 constexpr int kSampleMaxK = 64;
 struct MaxSum {
     float m, s;              // max of x, sum of exp(x - m)
 };
 struct SampleState {
     int acc;                 // accepted drafts
-    float mp, sp, mq, sq;    // max and 1 / sum of the rows the committed token is drawn from
+    float mp, mq;            // row maxima (x units) of the rows the committed token is drawn from
 };
 struct SampleArgs {
-    const float *draft = nullptr;    // [B, K, V] drafter logits (block positions 1..K)
+    const float *draft = nullptr;    // drafter logits: row i of sequence b at (b * draft_ld + i) * V
+    int draft_ld = 0;                // rows between sequences (K for a [B, K, V] tensor)
     const float *target = nullptr;   // [B, K+1, V] verifier logits (positions 0..K)
     int V = 0, B = 0, K = 0;
     float T = 1.f;                   // temperature > 0
     float scale = 1.f;               // log2(e) / T
-    const int32_t *drafts = nullptr; // [B, K]
+    // float-float constants of the draw weights (sample_constants): log2(e) / T, ln 2, and
+    // 2^(k/32) for k = -16..16
+    float sc_hi = 0.f, sc_lo = 0.f, ln2_hi = 0.f, ln2_lo = 0.f;
+    float2 exp2_tab[33] = {};
+    int sample_mode = 0;             // 1: draw drafts [B, K] from the drafter rows
+    const float *u_draft = nullptr;  // sample mode: [B, K] uniforms in [0, 1)
+    int32_t *drafts_out = nullptr;   // sample mode: [B, K]
+    const int32_t *drafts = nullptr; // accept mode: [B, K]
     const float *u_accept = nullptr; // [B, K] uniforms in [0, 1)
     const float *u_sample = nullptr; // [B]
     const int32_t *eos = nullptr;
@@ -384,14 +487,20 @@ struct SampleArgs {
     int32_t *committed = nullptr, *n_committed = nullptr, *accept_count = nullptr;
     int32_t *hit_eos = nullptr, *rollback = nullptr;
     int n_chunks = 0;
-    MaxSum *stats = nullptr;         // [B, 2K+1, n_chunks]
+    MaxSum *stats = nullptr;         // [B, 2K+1, n_chunks] (sample mode: [B, K, n_chunks])
     SampleState *state = nullptr;    // [B]
-    float *csum = nullptr;           // [B, n_chunks]
-    int *counters = nullptr;         // [B], zero between calls
+    double *dsum = nullptr;          // [B, n_chunks, 2]: exp sums of the draw's p and q rows
+    double *csum = nullptr;          // [B * K, n_chunks]: draw weights per chunk
+    int *counters = nullptr;         // [B * K], zero between calls
     int32_t *status = nullptr;
 };
 int sample_chunks(int V);
+// Scratch of either mode for B sequences of K drafts: carved in this order by the callers.
+void carve_sample_scratch(Carve &cv, SampleArgs &a, int B, int K, int V);
+// scale and the float-float constants from a.T (> 0)
+void sample_constants(SampleArgs &a);
 int launch_accept_stochastic(const SampleArgs &a, cudaStream_t s);
+int launch_sample_drafts(const SampleArgs &a, cudaStream_t s);
 
 // Multi-round generate loop around the draft round (k_loop.cu).
 constexpr int kLoopMaxTargetLayers = 16;
@@ -442,5 +551,11 @@ int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, i
                   int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,
                   int32_t *target_seq_len, int32_t *status, cudaStream_t s);
 int launch_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *status, cudaStream_t s);
+// argmax_final + accept in one launch for blocks of 2..32 rows (one CTA per sequence).
+int launch_argmax_accept(const ArgTop *part, int G, int B, int blk, int32_t *argmax_out,
+                         const int32_t *target, const int32_t *eos, int n_eos,
+                         int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                         int32_t *hit_eos, int32_t *rollback, int32_t *target_seq_len,
+                         int32_t *status, cudaStream_t s);
 
 }  // namespace df

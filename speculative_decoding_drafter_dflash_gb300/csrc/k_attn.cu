@@ -32,6 +32,7 @@ struct RopeArgs {
 };
 
 __global__ void rope_table_kernel(const __grid_constant__ RopeArgs a) {
+    DF_TRACE_KERNEL(TK_ROPE_TABLE);
     pdl_trigger();
     pdl_wait();
     const int half = a.rot / 2;
@@ -59,6 +60,7 @@ __global__ void rope_table_kernel(const __grid_constant__ RopeArgs a) {
 // One warp per (token row, head slot). Slots: [0, nq) q heads, [nq, nq+nkv) k heads,
 // [nq+nkv, nq+2nkv) v heads. Rows [0, B*blk) are block rows, the rest context rows.
 __global__ void qk_rope_kernel(QkArgs a) {
+    DF_TRACE_KERNEL(TK_QK_ROPE);
     extern __shared__ float smem[];
     pdl_trigger();
     pdl_wait();
@@ -279,6 +281,7 @@ __device__ __forceinline__ void attn_wait(uint64_t *bar, uint32_t parity, int32_
 // (o, m, l) per query row; attn_combine_kernel merges the chunks.
 template <int D, int RPL>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
+    DF_TRACE_KERNEL(TK_ATTN);
     constexpr int LPR = D / 32;
     constexpr int DL = 32;
     constexpr int RPW = 32 / LPR;                  // row sets per warp
@@ -529,6 +532,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnArgs a) {
 // result does not depend on timing).
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
+    DF_TRACE_KERNEL(TK_ATTN_COMBINE);
     constexpr int SL = D / 32;               // slices per row
     pdl_trigger();
     pdl_wait();
@@ -608,6 +612,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
 
 __global__ void seq_advance_kernel(int32_t *seq_len, const int32_t *n_new, int B, int delta,
                                    int cap, int32_t *status) {
+    DF_TRACE_KERNEL(TK_SEQ_ADVANCE);
     pdl_trigger();
     pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -642,7 +647,7 @@ int launch_rope_table(float *cos_t, float *sin_t, const int32_t *seq_len, const 
     a.rot = rot;
     a.status = status;
     for (int j = 0; j < rot / 2; ++j) a.inv[j] = std::pow((double)theta, -2.0 * j / (double)rot);
-    int threads = 256, grid = min((total + threads - 1) / threads, 4 * kNumSMs);
+    int threads = 256, grid = min((total + threads - 1) / threads, 4 * sm_count());
     return launch_k("rope_table_kernel", rope_table_kernel, dim3(grid), dim3(threads), 0, s, a);
 }
 
@@ -667,7 +672,7 @@ void attn_plan(AttnArgs &a, int max_keys) {
     const int R = a.blk * (a.nq / a.nkv);
     const int heads = a.B * a.nkv;
     const int waves = heads > 38 ? 2 : 1;
-    const int want = std::max(1, (waves * kNumSMs + heads - 1) / heads);
+    const int want = std::max(1, (waves * sm_count() + heads - 1) / heads);
     a.tc = attn_tc_supported(a.d, R) ? 1 : 0;
     const int TK = a.tc ? 128 : kTileBytes / (2 * a.d * 4);
     const int tiles = std::max(1, (max_keys + TK - 1) / TK);

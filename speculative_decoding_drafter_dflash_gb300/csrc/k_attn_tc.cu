@@ -210,6 +210,7 @@ struct AttnTcParams {
 // softmax and the products remain (plus the units of tiles holding new rows).
 template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
+    DF_TRACE_KERNEL(TK_ATTN_TC);
     static_assert(!VS || (D == 128 && NBUF == 3 && !MP && !KVB), "in-place V operands");
     constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
     constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit

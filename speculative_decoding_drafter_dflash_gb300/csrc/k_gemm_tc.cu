@@ -29,6 +29,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "df_internal.cuh"
 #include "tc_ptx.cuh"
@@ -77,7 +78,10 @@ struct TcParams {
     const float *rs_ss;
     int rs_n, rs_rows;
     float rs_inv_k, rs_eps;
+    long long wait_cycles;   // limit of every barrier wait (kTimeoutCycles unless a test sets it)
+    int withhold_first;      // test hook: the producer never loads its first stage
 };
+
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -240,6 +244,7 @@ __device__ __forceinline__ void epi_apply(const TcParams &p, const EpiSmem &es, 
 // fetched cold, so code that is never taken still costs.
 template <int EPI, bool FIX>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+    DF_TRACE_KERNEL(TK_GEMM + 2 * EPI + (FIX ? 1 : 0));
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -338,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             cursor_init(cur);
             int pre = 0;
             while (cur.valid && pre < p.stages) {
-                mbar_expect_tx(&full[pre], p.stage_bytes);
-                load_a(cur, pre);
+                if (!(p.withhold_first && pre == 0)) {
+                    mbar_expect_tx(&full[pre], p.stage_bytes);
+                    load_a(cur, pre);
+                }
                 advance(cur);
                 ++pre;
             }
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 Cursor cb;
                 cursor_init(cb);
                 for (int i = 0; i < pre; ++i) {
-                    load_b(cb, i);
+                    if (!(p.withhold_first && i == 0)) load_b(cb, i);
                     advance(cb);
                 }
             }
@@ -357,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             long long issued = pre;
             bool ok = true;
             while (cur.valid) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.wait_cycles)) {
                     ok = false;
                     break;
                 }
@@ -371,11 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     phase ^= 1u;
                 }
             }
-            if (!ok) {
-                // Let every load already issued land before the CTA can exit.
+            (void)ok;
+            {
+                // Every load issued lands before the CTA can exit, whether or not the MMA warp
+                // consumed it (the last use of each stage; a withheld first load was never
+                // issued). In a normal run these have landed by the time the loop ends.
                 long long first = issued > p.stages ? issued - p.stages : 0;
-                for (long long j = first; j < issued; ++j)
-                    mbar_drain(&full[j % p.stages], (uint32_t)((j / p.stages) & 1));
+                for (long long j = first; j < issued; ++j) {
+                    if (p.withhold_first && j == 0) continue;
+                    mbar_drain(&full[j % p.stages], (uint32_t)((j / p.stages) & 1), p.wait_cycles);
+                }
             }
         }
     } else if (warp == 1) {
@@ -388,11 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int m, k0, k1, split;
             while (ok && w.next(p, m, k0, k1, split)) {
                 if (k0 >= k1) continue;
-                if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status)) break;
+                if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, p.wait_cycles))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * p.acc_cols);
                 for (int kb = k0; kb < k1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
             // Every MMA this thread issued has completed once the drain barrier flips.
             mma_commit(drain);
-            mbar_drain(drain, 0);
+            mbar_drain(drain, 0, p.wait_cycles);
         }
     } else {
         pdl_wait();
@@ -448,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             if (k0 >= k1) continue;
             const bool whole = !FIX || (k0 == 0 && k1 == p.kbt);
             const int slot = (!p.splits && kb_start(blockIdx.x, p) / p.kbt == m) ? 0 : 1;
-            const bool got = mbar_wait(&tfull[acc], aphase, abort_flag, p.status);
+            const bool got = mbar_wait(&tfull[acc], aphase, abort_flag, p.status, p.wait_cycles);
             if (epi_any(!got)) break;   // all four epilogue warps leave together
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.acc_cols);
@@ -553,8 +566,14 @@ int make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uin
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_out) {
-    TcParams p;
+// Failure-detection test hook (df_test_wait_hook): a shorter wait limit, and every CTA's first
+// stage withheld so the MMA warp's wait runs out. Zero in normal use.
+std::atomic<long long> g_hook_wait_cycles{0};
+std::atomic<int> g_hook_withhold{0};
+
+// The kernel parameters of one projection (at most kMaxTcTokens tokens) and its dynamic shared
+// memory; launches nothing.
+int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &smem_out) {
     memset(&p, 0, sizeof(p));
     const int T = a.T;
     int NC = ((2 * T + 15) / 16) * 16;
@@ -643,15 +662,27 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
     p.rs_rows = a.rs_rows;
     p.rs_inv_k = a.rs_inv_k;
     p.rs_eps = a.rs_eps;
+    {
+        const long long w = g_hook_wait_cycles.load(std::memory_order_relaxed);
+        p.wait_cycles = w > 0 ? w : kTimeoutCycles;
+        p.withhold_first = g_hook_withhold.load(std::memory_order_relaxed);
+    }
     if (!p.splits && (size_t)p.G * 2 * T * kBM > sc.partial_floats)
         return fail(DF_EWORKSPACE, "GEMM scratch too small (%d tokens)", T);
     if (a.defer && (a.epi != EPI_STORE || a.part_stride < (size_t)T * a.ldo))
         return fail(DF_EINVAL, "deferred split-K needs a plain store into S x T x ldo floats");
     if (p.n_tiles > sc.n_counters)
         return fail(DF_EWORKSPACE, "GEMM tile counters too few (%d tiles)", p.n_tiles);
-    size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 5) * 8 + 16 +
-                  (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
-                  (size_t)T * sizeof(ArgTop) + (size_t)T * sizeof(float) + 64;
+    smem_out = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 5) * 8 + 16 +
+               (size_t)kBM * kTokChunk * 4 + 4 * kTokChunk * sizeof(ArgTop) +
+               (size_t)T * sizeof(ArgTop) + (size_t)T * sizeof(float) + 64;
+    return DF_OK;
+}
+
+int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_out) {
+    TcParams p;
+    size_t smem = 0;
+    DF_TRY(build_params(a, sc, p, smem));
     if (G_out) *G_out = a.defer ? p.splits : p.G;
     const dim3 grid(p.G), block(kThreads);
     const bool fix = p.splits == 0;
@@ -714,6 +745,20 @@ int get_encode() {
     return DF_OK;
 }
 }  // namespace
+
+}  // namespace df
+
+extern "C" int df_test_wait_hook(long long wait_cycles, int withhold_first) {
+    if (wait_cycles < 0 || (withhold_first && wait_cycles == 0))
+        return df::fail(DF_EINVAL, "df_test_wait_hook: wait_cycles=%lld withhold_first=%d "
+                                   "(withholding needs a positive wait limit)",
+                        wait_cycles, withhold_first);
+    df::g_hook_wait_cycles.store(wait_cycles, std::memory_order_relaxed);
+    df::g_hook_withhold.store(withhold_first ? 1 : 0, std::memory_order_relaxed);
+    return DF_OK;
+}
+
+namespace df {
 
 int make_tma_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem_bytes,
                 uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols, uint32_t box_rows,

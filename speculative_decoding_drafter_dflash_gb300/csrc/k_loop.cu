@@ -22,6 +22,7 @@ __device__ __forceinline__ bool is_eos(const LoopArgs &a, int tok) {
 // One CTA, a thread per sequence: the page returns at once when the first token is an EOS id
 // or the budget is zero; the loop runs while some sequence is active.
 __global__ void loop_init_kernel(LoopArgs a) {
+    DF_TRACE_KERNEL(TK_LOOP_INIT);
     pdl_trigger();
     pdl_wait();
     bool active = false;
@@ -47,6 +48,7 @@ __global__ void loop_init_kernel(LoopArgs a) {
 // n_new = prior_len - drafter cache length (the positions the drafter has not consumed), and the
 // concatenation of the drafter's target layers for those rows. Grid (B * n_new_max, n_tl).
 __global__ void __launch_bounds__(256) loop_prepare_kernel(LoopArgs a) {
+    DF_TRACE_KERNEL(TK_LOOP_PREPARE);
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x / a.n_new_max, j = blockIdx.x - b * a.n_new_max, l = blockIdx.y;
@@ -71,6 +73,7 @@ __global__ void __launch_bounds__(256) loop_prepare_kernel(LoopArgs a) {
 // Synthetic verifier: its greedy token after verify position p0 + j is the draft x_j where it
 // agrees (j < K), else ref[p0 + j + 1]. Grid B, K+1 threads or more.
 __global__ void loop_verify_kernel(LoopArgs a) {
+    DF_TRACE_KERNEL(TK_LOOP_VERIFY);
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x;
@@ -93,6 +96,7 @@ __device__ __forceinline__ bool stops(const LoopArgs &a, int b, int len, int n) 
 // verifier's capture = its table rows) join the captured prefix at prior_len (= p0). Skipped
 // when the sequence stops, as the page breaks before this step. Grid (B * (K+1), n_comb).
 __global__ void __launch_bounds__(256) loop_append_kernel(LoopArgs a) {
+    DF_TRACE_KERNEL(TK_LOOP_APPEND);
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x / (a.K + 1), j = blockIdx.x - b * (a.K + 1), c = blockIdx.y;
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(256) loop_append_kernel(LoopArgs a) {
 // Bookkeeping, one CTA with a thread per sequence: committed tokens appended, lengths, stop
 // flags, per-sequence rounds and accept history; then the loop condition.
 __global__ void loop_commit_kernel(LoopArgs a) {
+    DF_TRACE_KERNEL(TK_LOOP_COMMIT);
     pdl_trigger();
     pdl_wait();
     const int r = *a.round_ctr;
@@ -118,7 +123,9 @@ __global__ void loop_commit_kernel(LoopArgs a) {
         if (a.done[b]) continue;
         const int len = a.out_len[b], n = a.n_committed[b];
         int32_t *o = a.out + (size_t)b * a.max_len;
-        for (int i = 0; i < n && len + i < a.max_len; ++i) o[len + i] = a.committed[(size_t)b * (a.K + 1) + i];
+        for (int i = 0; i < n && len + i < a.max_len; ++i)
+            if (df_in_bounds(len + i >= 0 && i <= a.K, a.status))
+                o[len + i] = a.committed[(size_t)b * (a.K + 1) + i];
         const bool stop = stops(a, b, len, n);
         int nl = min(len + n, a.max_len);
         if (stop) {

@@ -48,6 +48,7 @@ __device__ __forceinline__ uint4 ld_w(const uint16_t *p, bool ok) {
 // Router: one warp per weight row (E router rows, then the shared-expert gate row), against
 // all T input rows at once. The last CTA to arrive selects the experts.
 __global__ void __launch_bounds__(kMoeThreads) moe_router_kernel(MoeArgs a) {
+    DF_TRACE_KERNEL(TK_MOE_ROUTER);
     __shared__ int s_last;
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kMoeThreads) moe_router_kernel(MoeArgs a) {
 
 // Gate/up: one warp per (row t, slot j, intermediate index r). act[t, j, r] = silu(g) * u.
 __global__ void __launch_bounds__(kMoeThreads) moe_gate_up_kernel(MoeArgs a) {
+    DF_TRACE_KERNEL(TK_MOE_GATE_UP);
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int S = a.k + 1, Imax = max(a.Ie, a.Is);
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(kMoeThreads) moe_gate_up_kernel(MoeArgs a) {
 // Down: one warp per (slot j, row t, block of kDownRows output rows).
 // part[j, t, h] = weight[t, j] * (down_j[h, :] . act[t, j, :]).
 __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(MoeArgs a) {
+    DF_TRACE_KERNEL(TK_MOE_DOWN);
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int S = a.k + 1, Imax = max(a.Ie, a.Is);

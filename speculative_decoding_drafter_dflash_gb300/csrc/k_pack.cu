@@ -16,6 +16,20 @@ namespace {
 
 constexpr int kPackThreads = 256;
 
+// The capacity-checked length advance a pack launch may carry (CTA 0, after the wait).
+__device__ __forceinline__ void pack_side_advance(const PackArgs &a) {
+    if (!a.adv_seq || blockIdx.x != 0) return;
+    for (int b = threadIdx.x; b < a.adv_B; b += blockDim.x) {
+        const int add = a.adv_n ? a.adv_n[b] : 0;
+        long long nv = (long long)a.adv_seq[b] + add;
+        if (add < 0 || nv > a.adv_cap) {
+            set_status(a.status, DF_ECAPACITY);
+            nv = min(max(nv, 0LL), (long long)a.adv_cap);
+        }
+        a.adv_seq[b] = (int32_t)nv;
+    }
+}
+
 __device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v);
     int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -37,9 +51,11 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // raw (h_out), computes rmsnorm(row) * w when a weight is given (else the row itself),
 // optionally stores that (y_out), and packs it into two BF16 rows (hi, lo).
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
+    DF_TRACE_KERNEL(TK_PACK);
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
+    pack_side_advance(a);
     const int t = blockIdx.x;
     const int K = a.K;
     const int s = t / a.rows_per_seq, j = t - s * a.rows_per_seq;
@@ -92,10 +108,12 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackArgs a) {
 // memory, in rank order, so every CTA of a row applies the same factor.
 template <int NV>
 __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a, int cl) {
+    DF_TRACE_KERNEL(TK_PACK_VEC);
     constexpr int G = NV <= 2 ? 8 : 4;   // split partials loaded per round
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
+    pack_side_advance(a);
     const int t = blockIdx.x / cl, rank = blockIdx.x - t * cl;
     const int K = a.K, K4 = K >> 2, per4 = K4 / cl, base4 = rank * per4;
     const int s = t / a.rows_per_seq, j = t - s * a.rows_per_seq;
@@ -167,7 +185,10 @@ __global__ void __launch_bounds__(kPackThreads) pack_vec_kernel(PackArgs a, int 
         if (threadIdx.x == 0) {
             float tot = 0.f;
             for (int i = 0; i < kPackThreads / 32; ++i) tot += red[i];
-            a.ss_out[(size_t)t * cl + rank] = tot;
+            const int ld = a.ss_ld > 0 ? a.ss_ld : cl;
+            a.ss_out[(size_t)t * ld + rank] = tot;
+            if (rank == 0)
+                for (int j = cl; j < ld; ++j) a.ss_out[(size_t)t * ld + j] = 0.f;
         }
     } else if (a.norm_w) {
         float ss = 0.f;
@@ -249,7 +270,8 @@ int pack_slices(int K) {
 int launch_pack(const PackArgs &a, cudaStream_t s) {
     if (a.T <= 0) return DF_OK;
     if (a.ss_out && (!a.norm_w || !a.pack || a.y_out || !aligned_for_vec(a) ||
-                     (a.K / 4) / pack_slices(a.K) > 16 * kPackThreads))
+                     (a.K / 4) / pack_slices(a.K) > 16 * kPackThreads ||
+                     (a.ss_ld > 0 && a.ss_ld < pack_slices(a.K))))
         return fail(DF_EINVAL, "deferred-norm row prologue: needs norm_w and pack, no y_out, "
                                "16-byte aligned rows");
     if (aligned_for_vec(a)) {

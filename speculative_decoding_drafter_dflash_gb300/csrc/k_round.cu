@@ -15,6 +15,7 @@ namespace {
 // largest value, the lowest index among equal values, and the second-largest value).
 __global__ void argmax_final_kernel(const ArgTop *part, int G, int T, int32_t *idx, float *top1,
                                     float *top2, int32_t *idx_copy, int ld, int skip) {
+    DF_TRACE_KERNEL(TK_ARGMAX_FINAL);
     pdl_trigger();
     pdl_wait();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -41,23 +42,19 @@ __global__ void argmax_final_kernel(const ArgTop *part, int G, int T, int32_t *i
     }
 }
 
-// One thread per sequence.
-__global__ void accept_kernel(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
-                              const int32_t *eos, int n_eos, int32_t *committed,
-                              int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
-                              int32_t *rollback, int32_t *target_seq_len, int32_t *status) {
-    pdl_trigger();
-    pdl_wait();
-    int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    const int32_t *dr = drafts + (size_t)b * ld;
-    const int32_t *tg = target + (size_t)b * (K + 1);
+// The greedy walk of one sequence over its drafts dr[0..K) and the verifier's argmaxes tg[0..K]:
+// accepted prefix, free token, EOS cut, -1 fill, rollback of the verifier's KV length.
+__device__ void accept_walk_one(const int32_t *dr, const int32_t *tg, int b, int K,
+                                const int32_t *eos, int n_eos, int32_t *committed,
+                                int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                                int32_t *rollback, int32_t *target_seq_len, int32_t *status) {
     int a = 0;
     while (a < K && dr[a] == tg[a]) ++a;
     int32_t *out = committed + (size_t)b * (K + 1);
     int n = 0, hit = 0;
     for (int i = 0; i <= a; ++i) {
         int tok = i < a ? dr[i] : tg[a];
+        if (!df_in_bounds(n <= K, status)) break;
         out[n++] = tok;
         bool is_eos = false;
         for (int e = 0; e < n_eos; ++e) is_eos |= (tok == eos[e]);
@@ -78,7 +75,60 @@ __global__ void accept_kernel(const int32_t *drafts, int ld, const int32_t *targ
     }
 }
 
+// The round's tail in one launch, one CTA per sequence: warp i merges the lm_head argmax
+// partials of block row i (as argmax_final_kernel), then thread 0 walks the drafts (rows 1..K)
+// against the verifier's argmaxes.
+__global__ void argmax_accept_kernel(const ArgTop *part, int G, int blk, int32_t *argmax_out,
+                                     const int32_t *target, const int32_t *eos, int n_eos,
+                                     int32_t *committed, int32_t *n_committed,
+                                     int32_t *accept_count, int32_t *hit_eos, int32_t *rollback,
+                                     int32_t *target_seq_len, int32_t *status) {
+    DF_TRACE_KERNEL(TK_ARGMAX_FINAL);
+    __shared__ int32_t idx[32];
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = gridDim.x * blk;
+    if (w < blk) {
+        const int t = b * blk + w;
+        ArgTop r = argtop_empty(0x7fffffff);
+        for (int g = lane; g < G; g += 32) r = argtop_merge(r, part[(size_t)g * T + t]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            ArgTop x;
+            x.v1 = __shfl_xor_sync(0xffffffffu, r.v1, o);
+            x.i1 = __shfl_xor_sync(0xffffffffu, r.i1, o);
+            x.v2 = __shfl_xor_sync(0xffffffffu, r.v2, o);
+            r = argtop_merge(r, x);
+        }
+        if (lane == 0) {
+            idx[w] = r.i1;
+            argmax_out[t] = r.i1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        accept_walk_one(idx + 1, target + (size_t)b * blk, b, blk - 1, eos, n_eos, committed,
+                        n_committed, accept_count, hit_eos, rollback, target_seq_len, status);
+}
+
+// One thread per sequence.
+__global__ void accept_kernel(const int32_t *drafts, int ld, const int32_t *target, int B, int K,
+                              const int32_t *eos, int n_eos, int32_t *committed,
+                              int32_t *n_committed, int32_t *accept_count, int32_t *hit_eos,
+                              int32_t *rollback, int32_t *target_seq_len, int32_t *status) {
+    DF_TRACE_KERNEL(TK_ACCEPT);
+    pdl_trigger();
+    pdl_wait();
+    int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    accept_walk_one(drafts + (size_t)b * ld, target + (size_t)b * (K + 1), b, K, eos, n_eos,
+                    committed, n_committed, accept_count, hit_eos, rollback, target_seq_len,
+                    status);
+}
+
 __global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32_t *status) {
+    DF_TRACE_KERNEL(TK_ROLLBACK);
     pdl_trigger();
     pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -94,6 +144,7 @@ __global__ void rollback_kernel(int32_t *seq_len, const int32_t *n, int B, int32
 // Word copies between device memory and page-locked host memory the device can address (the
 // small inputs and outputs of the host-buffer round): one launch instead of one DMA copy each.
 __global__ void word_copy_kernel(WordCopyList l) {
+    DF_TRACE_KERNEL(TK_WORD_COPY);
     pdl_trigger();
     pdl_wait();
     for (int r = 0; r < l.n; ++r) {
@@ -126,6 +177,18 @@ int launch_accept(const int32_t *drafts, int ld, const int32_t *target, int B, i
     return launch_k("accept_kernel", accept_kernel, dim3((B + 127) / 128), dim3(128), 0, s, drafts,
                     ld, target, B, K, eos, n_eos, committed, n_committed, accept_count, hit_eos,
                     rollback, target_seq_len, status);
+}
+
+int launch_argmax_accept(const ArgTop *part, int G, int B, int blk, int32_t *argmax_out,
+                         const int32_t *target, const int32_t *eos, int n_eos,
+                         int32_t *committed, int32_t *n_committed, int32_t *accept_count,
+                         int32_t *hit_eos, int32_t *rollback, int32_t *target_seq_len,
+                         int32_t *status, cudaStream_t s) {
+    if (B <= 0) return DF_OK;
+    if (blk < 2 || blk > 32) return fail(DF_ESHAPE, "fused argmax + accept takes 2..32 rows");
+    return launch_k("argmax_accept_kernel", argmax_accept_kernel, dim3(B), dim3(32 * blk), 0, s,
+                    part, G, blk, argmax_out, target, eos, n_eos, committed, n_committed,
+                    accept_count, hit_eos, rollback, target_seq_len, status);
 }
 
 int launch_rollback(int32_t *seq_len, const int32_t *n, int B, int32_t *status, cudaStream_t s) {

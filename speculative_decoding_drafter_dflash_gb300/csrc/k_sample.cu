@@ -1,20 +1,27 @@
-// Non-greedy accept step (speculative sampling): qwen35_orchestrator.rs, module doc
-// "Non-greedy (Metropolis-Hastings) is out of scope here" (stochastic acceptance wired through
-// the MTP K=1 path; for DFlash it replaces `step_round_from_argmaxes` at step 11). The rule,
-// which the page does not spell out, is read as the standard speculative-sampling test: with
-// p_i = softmax(target_i / T) and q_i = softmax(draft_i / T), draft x_i is accepted when
+// Non-greedy path: drafts drawn from the drafter's softmax and the speculative-sampling accept
+// step. qwen35_orchestrator.rs, module doc "Non-greedy (Metropolis-Hastings) is out of scope
+// here" (stochastic acceptance wired through the MTP K=1 path; for DFlash it replaces
+// `step_round_from_argmaxes` at step 11). The rule, which the page does not spell out, is read
+// as the standard speculative-sampling test: with p_i = softmax(target_i / T) and
+// q_i = softmax(draft_i / T), each draft x_i is itself a draw from q_i; it is accepted when
 // u_i q_i(x_i) < p_i(x_i); at the first rejection a the committed token is drawn from
 // max(0, p_a - q_a), and when every draft is accepted from p_K. A draw from weights w with a
 // uniform u is the smallest index j whose running sum exceeds u * sum(w).
 //
-// Three kernels, all reading the logits with 128-bit loads:
-//   stats : per (row, 2048-wide chunk) the maximum of x = l log2(e) / T and the sum of
-//           2^(x - max) (hardware ex2)
-//   walk  : one warp per sequence merges the chunk statistics of its 2K+1 rows (in chunk order)
-//           and runs the accept test at the drafted tokens
-//   draw  : per (sequence, chunk) the sum of the draw weights; the last chunk CTA of a sequence
-//           locates the chunk and then the index where the running sum crosses u * total, and
-//           writes the committed tokens (EOS cut, -1 fill) as the greedy walk does.
+// Kernels, all reading the logits with 128-bit loads (x = logit * log2(e) / T):
+//   stats : per (row, 2048-wide chunk) the maximum of x and the sum of 2^(x - max) (F32,
+//           hardware ex2): the accept tests and the shift of every draw
+//   walk  : one CTA per sequence merges its rows' chunk statistics and runs the K accept tests
+//   norm  : per (sequence, chunk) the sums of 2^(x - M) of the draw's p and q rows
+//   draw  : per (draw, chunk) the sum of the draw weights; the last chunk CTA of a draw locates
+//           the chunk, the thread and the index where the running sum crosses u * total
+//
+// The draw weights are computed to ~1e-14 relative (a float-float 2^x: the exponent split
+// into an integer, a 1/32 step from a table and a short Taylor series) and summed as
+// float-float pairs inside a warp and in float64 beyond it, so a draw agrees with a float64
+// reference except where u * total lies within ~1e-12 of a cumulative boundary.
+#include <cmath>
+
 #include "df_internal.cuh"
 
 namespace df {
@@ -24,6 +31,7 @@ namespace {
 constexpr int kSThreads = 256;
 constexpr int kEPT = 8;                     // logits per thread (two 128-bit loads)
 constexpr int kSChunk = kSThreads * kEPT;   // logits per chunk CTA
+constexpr int kMaxChunks = 1024;            // V <= 2^21
 
 using MS = MaxSum;
 
@@ -52,17 +60,102 @@ __device__ __forceinline__ MS warp_ms(MS v) {
     return v;
 }
 
-// Row rho of sequence b: rho <= K is target row rho, rho > K is draft row rho - K - 1.
+// ------------------------------------------------------------------ float-float arithmetic
+// A value hi + lo with |lo| <= ulp(hi) / 2 (Dekker / Knuth error-free transformations).
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ FF two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+
+__device__ __forceinline__ FF fast_two_sum(float a, float b) {   // |a| >= |b| or a == 0
+    const float s = a + b;
+    return {s, b - (s - a)};
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const FF s = two_sum(a.hi, b.hi);
+    return fast_two_sum(s.hi, s.lo + (a.lo + b.lo));
+}
+
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+    const float p = a.hi * b.hi;
+    const float e = fmaf(a.hi, b.hi, -p);
+    return fast_two_sum(p, fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e)));
+}
+
+__device__ __forceinline__ double ff_to_double(FF a) { return (double)a.hi + (double)a.lo; }
+
+__device__ __forceinline__ FF warp_ff_sum(FF v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        FF w;
+        w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = ff_add(v, w);
+    }
+    return v;
+}
+
+// 2^(l * scale - M) for a logit l: scale = sc_hi + sc_lo, M an F32 shift (the row maximum of
+// the F32 products, so the result is <= ~1). The product and the shift are carried exactly as
+// a float-float d; d = n + k/32 + r with integer n, |k| <= 16, |r| <= 1/64; 2^(k/32) comes from
+// the table (float-float, computed on the host in double), 2^r = exp(r ln 2) from the Taylor
+// series to the 6th power (|r ln 2| < 0.011, the next term < 4e-18).
+__device__ __forceinline__ FF weight_ff(float l, float M, const SampleArgs &a) {
+    const float p_hi = l * a.sc_hi;
+    const float p_lo = fmaf(l, a.sc_lo, fmaf(l, a.sc_hi, -p_hi));
+    FF d = two_sum(p_hi, -M);
+    d = fast_two_sum(d.hi, d.lo + p_lo);
+    if (!(d.hi > -126.f)) return {0.f, 0.f};          // below 2^-126 of the row maximum
+    const float nf = rintf(d.hi);
+    FF f = two_sum(d.hi - nf, d.lo);                   // d.hi - nf is exact
+    const float kf = rintf(f.hi * 32.f);
+    FF r = two_sum(fmaf(kf, -0.03125f, f.hi), f.lo);   // f.hi - k/32 is exact
+    const float g_hi = r.hi * a.ln2_hi;
+    const float g_lo = fmaf(r.hi, a.ln2_lo, fmaf(r.lo, a.ln2_hi, fmaf(r.hi, a.ln2_hi, -g_hi)));
+    const float sq_hi = g_hi * g_hi;
+    const float sq_lo = fmaf(g_hi, g_hi, -sq_hi) + 2.f * g_hi * g_lo;
+    const float tail =
+        sq_hi * g_hi *
+        (1.f / 6.f + g_hi * (1.f / 24.f + g_hi * (1.f / 120.f + g_hi * (1.f / 720.f))));
+    FF E = two_sum(g_hi, 0.5f * sq_hi);
+    E = fast_two_sum(E.hi, E.lo + (g_lo + 0.5f * sq_lo + tail));
+    const float2 t = a.exp2_tab[min(max((int)kf + 16, 0), 32)];
+    const float m_hi = t.x * E.hi;
+    const float m_lo = fmaf(t.x, E.hi, -m_hi) + fmaf(t.x, E.lo, t.y * E.hi);
+    FF w = two_sum(t.x, m_hi);
+    w = fast_two_sum(w.hi, w.lo + (t.y + m_lo));
+    const float s = __int_as_float(((int)nf + 127) << 23);   // 2^n, n in [-126, 0]
+    return {w.hi * s, w.lo * s};
+}
+
+__device__ __forceinline__ const float *draft_row(const SampleArgs &a, int b, int i) {
+    return a.draft + ((size_t)b * a.draft_ld + i) * a.V;
+}
+
+// Row rho of sequence b in the statistics. Accept mode: rho <= K is target row rho, rho > K is
+// draft row rho - K - 1. Sample mode: draft row rho.
 __device__ __forceinline__ const float *row_ptr(const SampleArgs &a, int b, int rho) {
+    if (a.sample_mode) return draft_row(a, b, rho);
     if (rho <= a.K) return a.target + ((size_t)b * (a.K + 1) + rho) * a.V;
-    return a.draft + ((size_t)b * a.K + (rho - a.K - 1)) * a.V;
+    return draft_row(a, b, rho - a.K - 1);
+}
+
+__device__ __forceinline__ int stat_rows(const SampleArgs &a) {
+    return a.sample_mode ? a.K : 2 * a.K + 1;
 }
 
 __global__ void __launch_bounds__(kSThreads) sample_stats_kernel(SampleArgs a) {
+    DF_TRACE_KERNEL(TK_SAMPLE_STATS);
     __shared__ MS red[kSThreads / 32];
     pdl_trigger();
     pdl_wait();
-    const int c = blockIdx.x, rows = 2 * a.K + 1;
+    const int c = blockIdx.x, rows = stat_rows(a);
     const int b = blockIdx.y / rows, rho = blockIdx.y - b * rows;
     const float *row = row_ptr(a, b, rho);
     const int j0 = c * kSChunk + threadIdx.x * kEPT;
@@ -96,10 +189,25 @@ __global__ void __launch_bounds__(kSThreads) sample_stats_kernel(SampleArgs a) {
     }
 }
 
+// Row maximum from the chunk statistics (exact: a maximum of maxima).
+__device__ float row_max(const SampleArgs &a, const MS *p) {
+    __shared__ float wm[kSThreads / 32];
+    float m = -INFINITY;
+    for (int c = threadIdx.x; c < a.n_chunks; c += kSThreads) m = fmaxf(m, p[c].m);
+    m = warp_max(m);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = wm[0];
+    for (int w = 1; w < kSThreads / 32; ++w) r = fmaxf(r, wm[w]);
+    return r;
+}
+
 // One CTA per sequence: warps merge the chunk statistics of the 2K+1 rows (lanes over chunks in
 // a fixed order), then thread i runs the accept test of draft i, all in parallel; the accept
 // count is the first failing i.
 __global__ void __launch_bounds__(kSThreads) sample_walk_kernel(SampleArgs a) {
+    DF_TRACE_KERNEL(TK_SAMPLE_WALK);
     __shared__ MS rs[2 * kSampleMaxK + 1];
     __shared__ int rej[kSampleMaxK];
     pdl_trigger();
@@ -133,81 +241,188 @@ __global__ void __launch_bounds__(kSThreads) sample_walk_kernel(SampleArgs a) {
                 acc = i;
                 break;
             }
-        // the draw: residual of row acc, or the target's next position when all were accepted
-        const MS sp = rs[acc];
-        const MS sq = acc < a.K ? rs[a.K + 1 + acc] : MS{-INFINITY, 0.f};
         SampleState st;
         st.acc = acc;
-        st.mp = sp.m;
-        st.sp = 1.f / sp.s;
-        st.mq = sq.m;
-        st.sq = acc < a.K ? 1.f / sq.s : 0.f;
+        st.mp = rs[acc].m;
+        st.mq = acc < a.K ? rs[a.K + 1 + acc].m : 0.f;
         a.state[b] = st;
         a.accept_count[b] = acc;
         a.rollback[b] = a.K - acc;
     }
 }
 
-// Draw weight of index j for sequence b (residual when acc < K, else the target's softmax).
-__device__ __forceinline__ float draw_weight(const SampleArgs &a, const SampleState &st, float lt,
-                                             float ld) {
-    const float p = ex2f(lt * a.scale - st.mp) * st.sp;
-    if (st.acc >= a.K) return p;
-    const float q = ex2f(ld * a.scale - st.mq) * st.sq;
-    return fmaxf(0.f, p - q);
+// What one draw reads: its p row (and, for a residual draw, its q row), their shifts, and the
+// float-float reciprocals of their exp sums (residual draws only).
+struct DrawJob {
+    const float *p, *q;
+    float mp, mq;
+    FF ip, iq;
+    float u;
+};
+
+// Accept mode: the draw of sequence b (residual of row acc, or the target's row K).
+__device__ DrawJob accept_job(const SampleArgs &a, int b) {
+    const SampleState st = a.state[b];
+    DrawJob j;
+    j.p = a.target + ((size_t)b * (a.K + 1) + st.acc) * a.V;
+    j.q = st.acc < a.K ? draft_row(a, b, st.acc) : nullptr;
+    j.mp = st.mp;
+    j.mq = st.mq;
+    j.u = a.u_sample[b];
+    j.ip = j.iq = {0.f, 0.f};
+    return j;
 }
 
-__global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
-    __shared__ float wsum[kSThreads / 32];
-    __shared__ float tsum[kSThreads];
-    __shared__ int s_last, s_chunk;
-    __shared__ float s_base, s_target;
+// Sums of 2^(x - M) of the draw's p and q rows over one chunk (residual draws only).
+__global__ void __launch_bounds__(kSThreads) sample_norm_kernel(SampleArgs a) {
+    DF_TRACE_KERNEL(TK_SAMPLE_NORM);
+    __shared__ double wsum[2][kSThreads / 32];
     pdl_trigger();
     pdl_wait();
     const int c = blockIdx.x, b = blockIdx.y;
-    const SampleState st = a.state[b];
-    const float *tp = row_ptr(a, b, st.acc);
-    const float *dq = st.acc < a.K ? row_ptr(a, b, a.K + 1 + st.acc) : nullptr;
-    auto chunk_weights = [&](int cc, int t_idx, float (&w)[kEPT]) {
-        const int j0 = cc * kSChunk + t_idx * kEPT;
+    const DrawJob jb = accept_job(a, b);
+    if (!jb.q) return;
+    const int j0 = c * kSChunk + threadIdx.x * kEPT;
+    FF sp{0.f, 0.f}, sq{0.f, 0.f};
 #pragma unroll
-        for (int h = 0; h < kEPT / 4; ++h) {
-            float4 lt = make_float4(0.f, 0.f, 0.f, 0.f), ld = lt;
-            const bool ok = j0 + 4 * h < a.V;
-            if (ok) {
-                lt = __ldcg(reinterpret_cast<const float4 *>(tp + j0 + 4 * h));
-                if (dq) ld = __ldcg(reinterpret_cast<const float4 *>(dq + j0 + 4 * h));
-            }
-            w[4 * h] = ok ? draw_weight(a, st, lt.x, ld.x) : 0.f;
-            w[4 * h + 1] = ok ? draw_weight(a, st, lt.y, ld.y) : 0.f;
-            w[4 * h + 2] = ok ? draw_weight(a, st, lt.z, ld.z) : 0.f;
-            w[4 * h + 3] = ok ? draw_weight(a, st, lt.w, ld.w) : 0.f;
+    for (int h = 0; h < kEPT / 4; ++h) {
+        if (j0 + 4 * h < a.V) {
+            const float4 lp = __ldcg(reinterpret_cast<const float4 *>(jb.p + j0 + 4 * h));
+            const float4 lq = __ldcg(reinterpret_cast<const float4 *>(jb.q + j0 + 4 * h));
+            sp = ff_add(sp, weight_ff(lp.x, jb.mp, a));
+            sp = ff_add(sp, weight_ff(lp.y, jb.mp, a));
+            sp = ff_add(sp, weight_ff(lp.z, jb.mp, a));
+            sp = ff_add(sp, weight_ff(lp.w, jb.mp, a));
+            sq = ff_add(sq, weight_ff(lq.x, jb.mq, a));
+            sq = ff_add(sq, weight_ff(lq.y, jb.mq, a));
+            sq = ff_add(sq, weight_ff(lq.z, jb.mq, a));
+            sq = ff_add(sq, weight_ff(lq.w, jb.mq, a));
         }
-    };
-    float w[kEPT];
-    chunk_weights(c, threadIdx.x, w);
-    float s = 0.f;
+    }
+    sp = warp_ff_sum(sp);
+    sq = warp_ff_sum(sq);
+    if ((threadIdx.x & 31) == 0) {
+        wsum[0][threadIdx.x >> 5] = ff_to_double(sp);
+        wsum[1][threadIdx.x >> 5] = ff_to_double(sq);
+    }
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        double t = 0.0;
+        for (int w = 0; w < kSThreads / 32; ++w) t += wsum[threadIdx.x][w];
+        a.dsum[((size_t)b * a.n_chunks + c) * 2 + threadIdx.x] = t;
+    }
+}
+
+// Float-float reciprocal of a positive double.
+__device__ __forceinline__ FF ff_recip(double s) {
+    const double r = 1.0 / s;
+    const float hi = (float)r;
+    return {hi, (float)(r - (double)hi)};
+}
+
+// The weights of thread t_idx's kEPT logits of chunk cc.
+__device__ __forceinline__ void chunk_weights(const SampleArgs &a, const DrawJob &jb, int cc,
+                                              int t_idx, FF (&w)[kEPT]) {
+    const int j0 = cc * kSChunk + t_idx * kEPT;
 #pragma unroll
-    for (int i = 0; i < kEPT; ++i) s += w[i];
-    s = warp_sum(s);
-    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = s;
+    for (int h = 0; h < kEPT / 4; ++h) {
+        const bool ok = j0 + 4 * h < a.V;
+        float4 lp = make_float4(0.f, 0.f, 0.f, 0.f), lq = lp;
+        if (ok) {
+            lp = __ldcg(reinterpret_cast<const float4 *>(jb.p + j0 + 4 * h));
+            if (jb.q) lq = __ldcg(reinterpret_cast<const float4 *>(jb.q + j0 + 4 * h));
+        }
+        const float lpv[4] = {lp.x, lp.y, lp.z, lp.w}, lqv[4] = {lq.x, lq.y, lq.z, lq.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            FF v{0.f, 0.f};
+            if (ok) {
+                v = weight_ff(lpv[e], jb.mp, a);
+                if (jb.q) {
+                    // max(0, p - q) with p = 2^(x - mp) / S_p and q = 2^(y - mq) / S_q
+                    const FF pn = ff_mul(v, jb.ip);
+                    const FF qn = ff_mul(weight_ff(lqv[e], jb.mq, a), jb.iq);
+                    v = ff_add(pn, FF{-qn.hi, -qn.lo});
+                    if (!(v.hi > 0.f)) v = {0.f, 0.f};
+                }
+            }
+            w[4 * h + e] = v;
+        }
+    }
+}
+
+__device__ __forceinline__ FF thread_sum(const FF (&w)[kEPT]) {
+    FF s{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kEPT; ++i) s = ff_add(s, w[i]);
+    return s;
+}
+
+// grid (chunks, draws). Accept mode: draw b of sequence b, then the committed tokens.
+// Sample mode: draw b * K + i is draft i of sequence b, from softmax(draft row i / T).
+__global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
+    DF_TRACE_KERNEL(TK_SAMPLE_DRAW);
+    __shared__ double wsum[kSThreads / 32];
+    __shared__ double tsum[kSThreads];
+    __shared__ double s_norm[2];
+    __shared__ float s_max;
+    __shared__ int s_last, s_chunk;
+    __shared__ double s_base, s_target;
+    pdl_trigger();
+    pdl_wait();
+    const int c = blockIdx.x, job = blockIdx.y;
+    DrawJob jb;
+    if (a.sample_mode) {
+        const int b = job / a.K, i = job - b * a.K;
+        jb.p = draft_row(a, b, i);
+        jb.q = nullptr;
+        const float M = row_max(a, a.stats + (size_t)job * a.n_chunks);
+        if (threadIdx.x == 0) s_max = M;
+        __syncthreads();
+        jb.mp = s_max;
+        jb.mq = 0.f;
+        jb.u = a.u_draft[job];
+        jb.ip = jb.iq = {0.f, 0.f};
+    } else {
+        jb = accept_job(a, job);
+        if (jb.q) {
+            // S_p and S_q from the chunk sums of the norm kernel, in chunk order
+            if (threadIdx.x < 2) {
+                const double *ds = a.dsum + (size_t)job * a.n_chunks * 2;
+                double t = 0.0;
+                for (int cc = 0; cc < a.n_chunks; ++cc) t += __ldcg(ds + 2 * cc + threadIdx.x);
+                s_norm[threadIdx.x] = t;
+            }
+            __syncthreads();
+            if (!(s_norm[0] > 0.0) || !(s_norm[1] > 0.0)) {
+                set_status(a.status, DF_EINVAL);
+                jb.q = nullptr;   // degenerate input: draw from p
+            } else {
+                jb.ip = ff_recip(s_norm[0]);
+                jb.iq = ff_recip(s_norm[1]);
+            }
+        }
+    }
+    FF w[kEPT];
+    chunk_weights(a, jb, c, threadIdx.x, w);
+    const FF ts = warp_ff_sum(thread_sum(w));
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ff_to_double(ts);
     __syncthreads();
     if (threadIdx.x == 0) {
-        float t = 0.f;
+        double t = 0.0;
         for (int i = 0; i < kSThreads / 32; ++i) t += wsum[i];
-        a.csum[(size_t)b * a.n_chunks + c] = t;
+        a.csum[(size_t)job * a.n_chunks + c] = t;
     }
-    // last chunk CTA of the sequence locates the draw
+    // the last chunk CTA of the draw locates it
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&a.counters[b], 1) == a.n_chunks - 1;
+    if (threadIdx.x == 0) s_last = atomicAdd(&a.counters[job], 1) == a.n_chunks - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (threadIdx.x == 0) a.counters[b] = 0;   // leave the counter at zero for the next call
-    // chunk sums into shared memory (parallel loads), then one thread scans them in order
-    const float *cs = a.csum + (size_t)b * a.n_chunks;
-    float tot = 0.f, run = 0.f, base = 0.f, base_last = 0.f, target = 0.f;
+    if (threadIdx.x == 0) a.counters[job] = 0;   // left at zero for the next call
+    const double *cs = a.csum + (size_t)job * a.n_chunks;
+    double tot = 0.0, run = 0.0, base = 0.0, base_last = 0.0, target = 0.0;
     int cstar = -1, last_pos = 0;
     for (int c0 = 0; c0 < a.n_chunks; c0 += kSThreads) {
         const int n = min(kSThreads, a.n_chunks - c0);
@@ -217,7 +432,7 @@ __global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
         if (threadIdx.x == 0)
             for (int i = 0; i < n; ++i) tot += tsum[i];
     }
-    if (threadIdx.x == 0) target = a.u_sample[b] * tot;
+    if (threadIdx.x == 0) target = (double)jb.u * tot;
     for (int c0 = 0; c0 < a.n_chunks; c0 += kSThreads) {
         const int n = min(kSThreads, a.n_chunks - c0);
         __syncthreads();
@@ -225,8 +440,8 @@ __global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
         __syncthreads();
         if (threadIdx.x == 0)
             for (int i = 0; i < n; ++i) {
-                const float v = tsum[i];
-                if (v > 0.f) {
+                const double v = tsum[i];
+                if (v > 0.0) {
                     last_pos = c0 + i;
                     base_last = run;
                 }
@@ -245,74 +460,110 @@ __global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
         s_chunk = cstar;
         s_base = base;
         s_target = target;
-        if (!(tot > 0.f)) set_status(a.status, DF_EINVAL);
+        if (!(tot > 0.0)) set_status(a.status, DF_EINVAL);
     }
     __syncthreads();
-    chunk_weights(s_chunk, threadIdx.x, w);
-    float mine = 0.f;
-#pragma unroll
-    for (int i = 0; i < kEPT; ++i) mine += w[i];
-    tsum[threadIdx.x] = mine;
+    chunk_weights(a, jb, s_chunk, threadIdx.x, w);
+    tsum[threadIdx.x] = ff_to_double(thread_sum(w));
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // running sum over the chunk's threads in index order, then inside the found thread
-        float run = s_base;
-        int tok = -1, last_pos = -1;
-        for (int t = 0; t < kSThreads && tok < 0; ++t) {
-            const float v = tsum[t];
-            if (v > 0.f) last_pos = t;
-            if (run + v > s_target) tok = t;
-            else run += v;
-        }
-        int idx;
-        if (tok < 0) tok = last_pos < 0 ? 0 : last_pos;
-        // thread tok's weights (recomputed by thread 0 with the same loads and arithmetic)
-        {
-            const int j0 = s_chunk * kSChunk + tok * kEPT;
-            float wv[kEPT];
-            chunk_weights(s_chunk, tok, wv);
-            float r = run;
-            idx = -1;
-            int lastj = j0;
-            for (int i = 0; i < kEPT; ++i) {
-                if (j0 + i >= a.V) break;
-                if (wv[i] > 0.f) lastj = j0 + i;
-                if (r + wv[i] > s_target) {
-                    idx = j0 + i;
-                    break;
-                }
-                r += wv[i];
-            }
-            if (idx < 0) idx = lastj;
-        }
-        // committed tokens: accepted drafts, then the drawn token, cut after the first EOS
-        int32_t *out = a.committed + (size_t)b * (a.K + 1);
-        int n = 0, hit = 0;
-        for (int i = 0; i <= st.acc; ++i) {
-            const int tkn = i < st.acc ? a.drafts[(size_t)b * a.K + i] : idx;
-            out[n++] = tkn;
-            bool is_eos = false;
-            for (int e = 0; e < a.n_eos; ++e) is_eos |= (tkn == a.eos[e]);
-            if (is_eos) {
-                hit = 1;
+    if (threadIdx.x != 0) return;
+    // running sum over the chunk's threads in index order, then inside the found thread
+    double r = s_base;
+    int tok = -1, last_t = -1;
+    for (int t = 0; t < kSThreads && tok < 0; ++t) {
+        const double v = tsum[t];
+        if (v > 0.0) last_t = t;
+        if (r + v > s_target) tok = t;
+        else r += v;
+    }
+    if (tok < 0) tok = last_t < 0 ? 0 : last_t;
+    int idx = -1;
+    {
+        const int j0 = s_chunk * kSChunk + tok * kEPT;
+        FF wv[kEPT];
+        chunk_weights(a, jb, s_chunk, tok, wv);
+        int lastj = j0;
+        for (int i = 0; i < kEPT; ++i) {
+            if (j0 + i >= a.V) break;
+            const double v = ff_to_double(wv[i]);
+            if (v > 0.0) lastj = j0 + i;
+            if (r + v > s_target) {
+                idx = j0 + i;
                 break;
             }
+            r += v;
         }
-        for (int i = n; i <= a.K; ++i) out[i] = -1;
-        a.n_committed[b] = n;
-        a.hit_eos[b] = hit;
+        if (idx < 0) idx = lastj;
     }
+    if (!df_in_bounds(idx >= 0 && idx < a.V, a.status)) idx = 0;
+    if (a.sample_mode) {
+        a.drafts_out[job] = idx;
+        return;
+    }
+    // committed tokens: accepted drafts, then the drawn token, cut after the first EOS
+    const int b = job, acc = a.state[b].acc;
+    int32_t *out = a.committed + (size_t)b * (a.K + 1);
+    int n = 0, hit = 0;
+    for (int i = 0; i <= acc; ++i) {
+        const int tkn = i < acc ? a.drafts[(size_t)b * a.K + i] : idx;
+        if (!df_in_bounds(n <= a.K, a.status)) break;
+        out[n++] = tkn;
+        bool is_eos = false;
+        for (int e = 0; e < a.n_eos; ++e) is_eos |= (tkn == a.eos[e]);
+        if (is_eos) {
+            hit = 1;
+            break;
+        }
+    }
+    for (int i = n; i <= a.K; ++i) out[i] = -1;
+    a.n_committed[b] = n;
+    a.hit_eos[b] = hit;
 }
 
 }  // namespace
 
 int sample_chunks(int V) { return (V + kSChunk - 1) / kSChunk; }
 
+void carve_sample_scratch(Carve &cv, SampleArgs &a, int B, int K, int V) {
+    a.n_chunks = sample_chunks(V);
+    a.stats = cv.take<MaxSum>((size_t)B * (2 * K + 1) * a.n_chunks);
+    a.state = cv.take<SampleState>((size_t)B);
+    a.dsum = cv.take<double>((size_t)B * a.n_chunks * 2);
+    a.csum = cv.take<double>((size_t)B * K * a.n_chunks);
+    a.counters = cv.take<int>((size_t)B * K);
+}
+
+void sample_constants(SampleArgs &a) {
+    const double scale = 1.4426950408889634 / (double)a.T;   // log2(e) / T
+    a.scale = (float)scale;
+    a.sc_hi = (float)scale;
+    a.sc_lo = (float)(scale - (double)a.sc_hi);
+    const double ln2 = 0.69314718055994530942;
+    a.ln2_hi = (float)ln2;
+    a.ln2_lo = (float)(ln2 - (double)a.ln2_hi);
+    for (int k = -16; k <= 16; ++k) {
+        const double v = std::exp2((double)k / 32.0);
+        a.exp2_tab[k + 16].x = (float)v;
+        a.exp2_tab[k + 16].y = (float)(v - (double)(float)v);
+    }
+}
+
 int launch_accept_stochastic(const SampleArgs &a, cudaStream_t s) {
+    if (a.n_chunks > kMaxChunks) return fail(DF_ESHAPE, "vocabulary of %d is too large", a.V);
     DF_TRY(launch_k("sample_stats_kernel", sample_stats_kernel,
                     dim3(a.n_chunks, a.B * (2 * a.K + 1)), dim3(kSThreads), 0, s, a));
     DF_TRY(launch_k("sample_walk_kernel", sample_walk_kernel, dim3(a.B), dim3(kSThreads), 0, s, a));
+    DF_TRY(launch_k("sample_norm_kernel", sample_norm_kernel, dim3(a.n_chunks, a.B),
+                    dim3(kSThreads), 0, s, a));
     return launch_k("sample_draw_kernel", sample_draw_kernel, dim3(a.n_chunks, a.B),
+                    dim3(kSThreads), 0, s, a);
+}
+
+int launch_sample_drafts(const SampleArgs &a, cudaStream_t s) {
+    if (a.n_chunks > kMaxChunks) return fail(DF_ESHAPE, "vocabulary of %d is too large", a.V);
+    DF_TRY(launch_k("sample_stats_kernel", sample_stats_kernel, dim3(a.n_chunks, a.B * a.K),
+                    dim3(kSThreads), 0, s, a));
+    return launch_k("sample_draw_kernel", sample_draw_kernel, dim3(a.n_chunks, a.B * a.K),
                     dim3(kSThreads), 0, s, a);
 }
 

@@ -48,15 +48,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait on a barrier phase. Gives up (returns false) when another role has aborted or
-// after kTimeoutCycles, in which case it raises the CTA's abort flag and DF_ETIMEOUT.
+// after `limit` cycles, in which case it raises the CTA's abort flag and DF_ETIMEOUT.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
+                                          int32_t *status, long long limit = kTimeoutCycles) {
     long long t0 = clock64();
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 63u) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 set_status(status, DF_ETIMEOUT);
                 return false;
@@ -66,10 +66,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // Bounded wait used while tearing down after an abort (ignores the abort flag).
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity,
+                                           long long limit = kTimeoutCycles) {
     long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kTimeoutCycles) return;
+        if (clock64() - t0 > limit) return;
     }
 }
 

@@ -351,3 +351,41 @@ def test_batched_round_b8_ctx1024():
     torch.cuda.synchronize()
     ri, r1, r2 = ocore.lm_head_argmax(r["ref"].reshape(-1, shape.hidden), r["hw"]["lm_head"])
     assert_argmax_parity(idx.cpu().numpy(), ri, r1, r2, "B=8 argmax")
+
+
+@pytest.mark.slow
+def test_batched_draft_round_b8_ctx1024():
+    """df_draft_round itself at 8 sequences (128 lm_head rows whose final norm is the lm_head's
+    row scale), K=15, context 1024, ragged new-row counts: every argmax (gap-gated), the accept
+    walks, rollbacks and cache lengths against the oracle."""
+    shape = DFLASH_K15.with_(batch=8, ctx=1024)
+    n_new = [1, 16, 3, 7, 2, 11, 5, 9]
+    acc = np.array([0, 1, 2, 3, 4, 5, 15, 7])
+    w, cache, inp, model = _setup(shape, n_new, seed=6)
+    hw = dflash_weights_host(w)
+    ks, vs, seq0 = cache_host(cache)
+    ref_h, seq_ref = odf.dflash_block_forward(shape, hw, ks, vs, seq0, synth.host(inp.block_ids),
+                                              synth.host(inp.target_hidden), synth.host(inp.n_new))
+    ri, r1, r2 = ocore.lm_head_argmax(ref_h.reshape(-1, shape.hidden), hw["lm_head"])
+    Bn, blk = shape.batch, shape.block
+    tgt = synth.targets_from_drafts(ri.reshape(Bn, blk)[:, 1:], acc, shape.vocab, seed=2)
+    ws = B.alloc_workspace(model.workspace_bytes(Bn, blk, inp.n_new_max))
+    out = B.RoundOutputs(Bn, shape.K, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    eos = torch.tensor(shape.eos_ids, dtype=torch.int32, device=DEV)
+    tsl = torch.full((Bn,), 5000, dtype=torch.int32, device=DEV)
+    B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, inp.n_new_max, shape.K,
+                     torch.tensor(tgt, device=DEV), eos, tsl, out, ws, st)
+    torch.cuda.synchronize()
+    assert int(st) == 0
+    am = out.argmax.cpu().numpy()
+    assert_argmax_parity(am, ri, r1, r2, "B=8 round argmax")
+    assert list(synth.host(cache.seq_len)) == list(seq_ref)
+    gap = (r1 - r2).reshape(Bn, blk)
+    for b in range(Bn):
+        if np.all(gap[b] > 1e-2):
+            c, a, hit, rb = ocore.accept_walk(ri.reshape(Bn, blk)[b, 1:], tgt[b], shape.eos_ids)
+            assert int(out.accept[b]) == a and int(out.rollback[b]) == rb, f"sequence {b}"
+            assert int(synth.host(tsl)[b]) == 5000 - rb
+            n = int(out.n_committed[b])
+            assert out.committed[b, :n].cpu().numpy().tolist() == c

@@ -13,7 +13,7 @@ from speculative_decoding_drafter_dflash_gb300 import binding as B
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 DECISION_MARGIN = 1e-4    # relative distance of u q(x) from p(x) below which a test is skipped
-DRAW_TOL = 2e-5           # of the total weight: F32 running sums over up to 262144 weights
+DRAW_TOL = 1e-9           # of the total weight: float-float weights, float64 running sums
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -60,9 +60,9 @@ def _run(tl, dl, drafts, ua, us, T, eos=(1,)):
 
 def _check(tl, dl, drafts, ua, us, T, got, eos=(1,)):
     """Accept counts and rollbacks bit-exact where the accept test is clear of its threshold;
-    the drawn token must be a valid draw: its weight positive and u * W within
-    DRAW_TOL * W of its cumulative interval (the GPU sums the weights in F32 in another order).
-    Returns how many sequences drew exactly the oracle's token."""
+    the drawn token equal to the oracle's wherever u * W lies more than DRAW_TOL * W from a
+    cumulative boundary, and otherwise a valid draw (positive weight, u * W within 2 DRAW_TOL * W
+    of its interval). Returns how many sequences drew exactly the oracle's token."""
     Bn, K, V = dl.shape
     tlh, dlh = tl.cpu().numpy(), dl.cpu().numpy()
     dh, uah, ush = drafts.cpu().numpy(), ua.cpu().numpy(), us.cpu().numpy()
@@ -87,8 +87,10 @@ def _check(tl, dl, drafts, ua, us, T, got, eos=(1,)):
         c = np.cumsum(w)
         t = float(ush[b]) * c[-1]
         lo = c[tok - 1] if tok > 0 else 0.0
-        assert w[tok] > 0 and lo - DRAW_TOL * c[-1] <= t <= c[tok] + DRAW_TOL * c[-1], \
+        assert w[tok] > 0 and lo - 2 * DRAW_TOL * c[-1] <= t <= c[tok] + 2 * DRAW_TOL * c[-1], \
             f"sequence {b}: token {tok} is not a draw of u={ush[b]}"
+        if info["draw_margin"] > DRAW_TOL:
+            assert tok == committed[a], f"sequence {b}: drew {tok}, oracle {committed[a]}"
         exact += int(tok == committed[a])
         want_hit = int(tok in set(eos))
         assert got["hit_eos"][b] == want_hit and n == a + 1
@@ -102,8 +104,7 @@ def test_accept_stochastic_matches_oracle(Bn, K, V, T, seed):
     got, st, _, _ = _run(tl, dl, drafts, ua, us, T)
     assert st == 0
     exact = _check(tl, dl, drafts, ua, us, T, got)
-    if V <= 4096:                                    # large weights per token: the same draw
-        assert exact >= Bn - 1
+    assert exact >= Bn - 1          # a draw within 1e-9 of a boundary is a rare event
 
 
 def test_identical_distributions_accept_every_draft():

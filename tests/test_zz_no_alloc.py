@@ -4,15 +4,17 @@ The no-allocation entry point serves callers that cannot allocate device memory 
 plug-in host that owns every allocation, or a loop that cannot take cudaMalloc's implicit
 synchronisation): it keeps its scratch in a fixed array inside the library. Two calls in a row
 with different inputs must each agree with the workspace-based entry point, which also shows
-that nothing left in the shared array by the first call leaks into the second. This file is
-named to run last; it also passes alone in a fresh process.
+that nothing left in the shared array by the first call leaks into the second; a small case is
+also checked straight against the CPU oracle's lm_head argmax. This file is named to run last;
+it also passes alone in a fresh process.
 """
 import numpy as np
 import pytest
 import torch
 
+from oracle import core as ocore
 from speculative_decoding_drafter_dflash_gb300 import binding as B
-from tests.harness import GAP_MIN, REL_TOL, rel_err
+from tests.harness import GAP_MIN, REL_TOL, assert_argmax_parity, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -67,10 +69,31 @@ def test_noalloc_matches_workspace_entry_point_twice():
         _agree(ref, got)
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
-    W = torch.zeros((64, 256), dtype=torch.bfloat16, device=DEV)
-    X = torch.zeros((17, 256), device=DEV)
-    idx = torch.empty(17, dtype=torch.int32, device=DEV)
+def test_noalloc_matches_oracle():
+    """H = 256, V = 4096, 5 rows: indices equal the oracle's wherever its top-1/top-2 gap
+    exceeds GAP_MIN, top values within REL_TOL."""
+    g = torch.Generator(device=DEV).manual_seed(12)
+    V, H, rows = 4096, 256, 5
+    W = (torch.randn((V, H), generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+    X = torch.randn((rows, H), generator=g, device=DEV)
+    for _ in range(2):
+        idx, t1, t2 = _noalloc(W, X)
+        torch.cuda.synchronize()
+        bits = W.view(torch.int16).cpu().numpy().view(np.uint16)
+        ri, r1, r2 = ocore.lm_head_argmax(X.cpu().numpy(), bits)
+        assert_argmax_parity(idx.cpu().numpy(), ri, r1, r2, "noalloc")
+        assert rel_err(t1.cpu().numpy(), r1) <= REL_TOL and rel_err(t2.cpu().numpy(), r2) <= REL_TOL
+
+
+@pytest.mark.parametrize("rows,H,V", [(17, 256, 64), (4, 260, 64), (4, 8200, 64), (4, 256, 524289)])
+def test_noalloc_rejects_sizes_beyond_its_scratch(rows, H, V):
+    """More than 16 rows, H not a multiple of 8 or above 8192, V above 524288: refused on the
+    host before any launch (W is only as large as the rows the shape check needs)."""
+    W = torch.zeros((min(V, 64), H), dtype=torch.bfloat16, device=DEV)
+    X = torch.zeros((rows, H), device=DEV)
+    idx = torch.empty(rows, dtype=torch.int32, device=DEV)
     with pytest.raises(B.DFlashError) as e:
-        B.lm_head_argmax_noalloc(W, X, idx)
+        rc = B.lib().lm_head_argmax_noalloc(B._p(W), B._p(X), rows, H, V, B._p(idx), None, None,
+                                             B._stream(None))
+        B._check(rc)
     assert e.value.code == B.DF_ESHAPE
