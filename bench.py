@@ -1036,10 +1036,15 @@ def profile_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": "lm_head", "idx0": int(idx[0])}))
     elif args.profile_case == "gemms":
-        # Every projection shape of one drafter layer (+ fc) timed alone with CUDA events.
+        # Every projection shape of one drafter layer (+ fc) timed alone with CUDA events, for
+        # --batch sequences of 16 block rows (the QKV shape adds as many context rows); the
+        # lm_head shape only at batch 1. --steps timed calls per shape after 3 warm-up calls.
         H, I, qt, kt = s.hidden, s.intermediate, s.q_total, s.kv_total
-        shapes = [("fc", 16, H, s.fc_in), ("qkv", 32, qt + 2 * kt, H), ("o", 16, H, qt),
-                  ("gate_up", 16, 2 * I, H), ("down", 16, H, I), ("lm_head_store", 16, s.vocab, H)]
+        b = max(1, args.batch)
+        shapes = [("fc", 16 * b, H, s.fc_in), ("qkv", 32 * b, qt + 2 * kt, H), ("o", 16 * b, H, qt),
+                  ("gate_up", 16 * b, 2 * I, H), ("down", 16 * b, H, I)]
+        if b == 1:
+            shapes.append(("lm_head_store", 16, s.vocab, H))
         res = {}
         for name, T, N, K in shapes:
             W = (torch.randn((N, K), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
@@ -1049,7 +1054,7 @@ def profile_case(args):
             for _ in range(3):
                 B.df_linear(W, X, Y, ws)
             evs = []
-            for _ in range(20):
+            for _ in range(max(1, min(args.steps, 20))):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 B.df_linear(W, X, Y, ws)
