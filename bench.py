@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--trace-dump", default=None, help="--profile-case trace: save the records")
 
     ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "sweep_bf16kv", "mtp",
-                                                     "moe", "attn", "stochastic", "generate", "trace"],
+                                                     "moe", "attn", "stochastic", "sampled", "generate", "trace"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -826,12 +826,135 @@ def stochastic_case(steps: int):
         torch.cuda.synchronize()
         us_ = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
         nb = Bn * (2 * K + 1) * V * 4
+        flush.fill_(1)
+        B.profile_enable(True)          # one more call, each launch bracketed by events
+        B.accept_stochastic(dl, tl, drafts, T, ua, us, eos, out, ws)
+        torch.cuda.synchronize()
+        per = [[n, round(t, 2)] for n, t in B.profile_read()]
+        B.profile_enable(False)
         print(json.dumps({"profile_case": "stochastic", "workload": f"accept-k{K}-v{V}-b{Bn}",
                           "us": round(us_, 2), "logit_bytes": nb,
                           "gbs": round(nb / us_ / 1e3, 1),
                           "frac_of_measured_hbm": round(nb / us_ / 1e3 / hbm_peak, 4),
-                          "mean_accept": float(out["accept"].float().mean())}), flush=True)
+                          "mean_accept": float(out["accept"].float().mean()),
+                          "per_launch_us_with_event_overhead": per}), flush=True)
         del tl, dl, ws
+
+
+def sampled_case(steps: int):
+    """The non-greedy path at full size: sample_softmax over the 15 drafter rows of a round
+    (V=262144, after an L2-evicting write), the whole non-greedy DFlash round (K=15, ctx 4096,
+    T=1) against the greedy round on the same inputs, both as CUDA graphs, and the sampled dense
+    MTP chain (1 and 3 steps) against the argmax chain."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15, MTP_DENSE
+    dev = torch.device("cuda", 0)
+    hbm_peak, _ = peaks()
+    g = torch.Generator(device=dev).manual_seed(0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = DFLASH_K15
+    K, V = s.K, s.vocab
+    # sample_softmax alone
+    lg = torch.randn((K, V), generator=g, device=dev)
+    u = torch.rand((K,), generator=g, device=dev)
+    tok = torch.empty((K,), dtype=torch.int32, device=dev)
+    ws = B.alloc_workspace(B.sample_softmax_workspace_bytes(K, V), dev)
+    for _ in range(3):
+        B.sample_softmax(lg, 1.0, u, tok, ws)
+    times = []
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        B.sample_softmax(lg, 1.0, u, tok, ws)
+        e1.record()
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    us_ = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
+    nb = K * V * 4                # one pass over every logit (plus one 8 KB chunk per draw)
+    flush.fill_(1)
+    B.profile_enable(True)
+    B.sample_softmax(lg, 1.0, u, tok, ws)
+    torch.cuda.synchronize()
+    per = [[n, round(t, 2)] for n, t in B.profile_read()]
+    B.profile_enable(False)
+    print(json.dumps({"profile_case": "sampled", "workload": f"sample-softmax-{K}x{V}",
+                      "us": round(us_, 2), "bytes": nb, "gbs": round(nb / us_ / 1e3, 1),
+                      "frac_of_measured_hbm": round(nb / us_ / 1e3 / hbm_peak, 4),
+                      "per_launch_us_with_event_overhead": per}), flush=True)
+    del lg, ws
+    # the non-greedy round against the greedy round
+    acc, n_new = variants(s)
+    w = synth.dflash_weights(s, seed=0, device=dev)
+    cache = synth.dflash_cache(s, seed=1, device=dev)
+    model = B.DFlashModel(s, w, cache)
+    inp = synth.dflash_round_inputs(s, [s.block], seed=10, device=dev)
+    inp.n_new = torch.tensor([n_new[0]], dtype=torch.int32, device=dev)
+    eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
+    tsl = torch.full((1,), 1 << 30, dtype=torch.int32, device=dev)
+    out = B.RoundOutputs(1, K, dev)
+    tl = torch.randn((1, K + 1, V), generator=g, device=dev)
+    ud, ua = torch.rand((1, K), generator=g, device=dev), torch.rand((1, K), generator=g, device=dev)
+    us = torch.rand((1,), generator=g, device=dev)
+    logits = torch.empty((1, K + 1, V), device=dev)
+    drafts = torch.empty((1, K), dtype=torch.int32, device=dev)
+    ws_s = B.alloc_workspace(B.draft_round_stochastic_workspace_bytes(model, 1, K, s.block), dev)
+    ws_g = B.alloc_workspace(model.workspace_bytes(1, s.block, s.block), dev)
+    tgt = torch.zeros((1, s.block), dtype=torch.int32, device=dev)
+
+    def stochastic(stream):
+        B.df_draft_round_stochastic(model, inp.last_token, inp.target_hidden, inp.n_new, s.block,
+                                    K, tl, 1.0, ud, ua, us, eos, tsl, logits, drafts, out, ws_s,
+                                    stream=stream)
+        B.kv_rollback(cache.seq_len, inp.n_new, stream=stream)
+
+    def greedy(stream):
+        B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, s.block, K, tgt,
+                         eos, tsl, out, ws_g, stream=stream)
+        B.kv_rollback(cache.seq_len, inp.n_new, stream=stream)
+
+    rs = _graph_rate(stochastic, steps)
+    rg = _graph_rate(greedy, steps)
+    print(json.dumps({"profile_case": "sampled", "workload": s.name, "round": "T=1 sampled drafts",
+                      "rounds_per_s": round(rs, 1), "round_us": round(1e6 / rs, 1),
+                      "greedy_rounds_per_s": round(rg, 1), "greedy_round_us": round(1e6 / rg, 1),
+                      "extra_us": round(1e6 / rs - 1e6 / rg, 1)}), flush=True)
+    del w, cache, model, ws_s, ws_g, logits, tl
+    torch.cuda.empty_cache()
+    # the sampled dense MTP chain against the argmax chain
+    m = MTP_DENSE
+    w = synth.mtp_weights(m, seed=0, device=dev)
+    for n_steps in (1, 3):
+        cache = synth.mtp_cache(m, n_steps, seed=1, device=dev)
+        prev, tk = synth.mtp_inputs(m, seed=2, device=dev)
+        model = B.MtpModel(m, w, cache)
+        wsm = B.alloc_workspace(model.workspace_bytes(1), dev)
+        hid = torch.empty((n_steps, 1, m.hidden), device=dev)
+        am = torch.empty((n_steps, 1), dtype=torch.int32, device=dev)
+        lgm = torch.empty((n_steps, 1, m.vocab), device=dev)
+        um = torch.rand((n_steps, 1), generator=g, device=dev)
+        nback = torch.tensor([n_steps], dtype=torch.int32, device=dev)
+
+        def sampled(stream):
+            B.mtp_forward_draft_sampled(model, prev, tk, n_steps, 1.0, um, hid, am, lgm, wsm,
+                                        stream=stream)
+            B.kv_rollback(cache.seq_len, nback, stream=stream)
+
+        def argmax(stream):
+            B.mtp_forward_draft(model, prev, tk, n_steps, hid, am, wsm, stream=stream)
+            B.kv_rollback(cache.seq_len, nback, stream=stream)
+
+        r1, r0 = _graph_rate(sampled, steps), _graph_rate(argmax, steps)
+        print(json.dumps({"profile_case": "sampled", "workload": m.name, "n_steps": n_steps,
+                          "sampled_call_us": round(1e6 / r1, 1), "argmax_call_us": round(1e6 / r0, 1),
+                          "extra_us_per_step": round((1e6 / r1 - 1e6 / r0) / n_steps, 1)}),
+              flush=True)
+        del cache, model, wsm, lgm
+    del w
+    torch.cuda.empty_cache()
 
 
 def generate_case(steps: int):
@@ -1026,6 +1149,8 @@ def profile_case(args):
         return stochastic_case(args.steps)
     if args.profile_case == "generate":
         return generate_case(args.steps)
+    if args.profile_case == "sampled":
+        return sampled_case(args.steps)
     if args.profile_case == "lm_head":
         W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)

@@ -303,7 +303,7 @@ int accept_stochastic(const float *draft_logits, const float *target_logits, int
  * the non-greedy path of qwen35_orchestrator.rs's module doc, "Non-greedy (Metropolis-Hastings)
  * is out of scope here": each drafted position is a sample of the drafter's distribution, which
  * the accept step above then divides by). The weights are computed to ~1e-14 relative and summed
- * in float-float / float64, so a draw differs from a float64 reference only where u * total is
+ * as float-float pairs, so a draw differs from a float64 reference only where u * total is
  * within ~1e-12 of a cumulative boundary.
  * ---------------------------------------------------------------------------------------- */
 /* Workspace (chunk statistics, draw partial sums, counters); allocate it zeroed. */

@@ -123,6 +123,7 @@ enum TraceKid : uint32_t {
     TK_LOOP_INIT, TK_LOOP_PREPARE, TK_LOOP_VERIFY, TK_LOOP_APPEND, TK_LOOP_COMMIT, TK_MOE_ROUTER,
     TK_MOE_GATE_UP, TK_MOE_DOWN, TK_PACK, TK_PACK_VEC, TK_ARGMAX_FINAL, TK_ACCEPT, TK_ROLLBACK,
     TK_WORD_COPY, TK_SAMPLE_STATS, TK_SAMPLE_WALK, TK_SAMPLE_NORM, TK_SAMPLE_DRAW,
+    TK_SAMPLE_FUSED,
     TK_GEMM = 100   // + 2 * epilogue + (stream-K fix-up ? 1 : 0)
 };
 struct TraceRec {
@@ -489,8 +490,8 @@ struct SampleArgs {
     int n_chunks = 0;
     MaxSum *stats = nullptr;         // [B, 2K+1, n_chunks] (sample mode: [B, K, n_chunks])
     SampleState *state = nullptr;    // [B]
-    double *dsum = nullptr;          // [B, n_chunks, 2]: exp sums of the draw's p and q rows
-    double *csum = nullptr;          // [B * K, n_chunks]: draw weights per chunk
+    float2 *dsum = nullptr;          // [B, n_chunks, 2]: exp sums of the draw's p and q rows (hi, lo)
+    float2 *csum = nullptr;          // [B * K, n_chunks]: draw weights per chunk (hi, lo)
     int *counters = nullptr;         // [B * K], zero between calls
     int32_t *status = nullptr;
 };

@@ -8,18 +8,24 @@
 // max(0, p_a - q_a), and when every draft is accepted from p_K. A draw from weights w with a
 // uniform u is the smallest index j whose running sum exceeds u * sum(w).
 //
-// Kernels, all reading the logits with 128-bit loads (x = logit * log2(e) / T):
+// Kernels, all reading the logits with 128-bit loads (x = logit * log2(e) / T).
+// Accept step (four launches):
 //   stats : per (row, 2048-wide chunk) the maximum of x and the sum of 2^(x - max) (F32,
-//           hardware ex2): the accept tests and the shift of every draw
+//           hardware ex2): the accept tests and the shift of the draw
 //   walk  : one CTA per sequence merges its rows' chunk statistics and runs the K accept tests
 //   norm  : per (sequence, chunk) the sums of 2^(x - M) of the draw's p and q rows
-//   draw  : per (draw, chunk) the sum of the draw weights; the last chunk CTA of a draw locates
-//           the chunk, the thread and the index where the running sum crosses u * total
+//   draw  : per (sequence, chunk) the sum of the draw weights; the last chunk CTA of a draw
+//           locates the chunk, then the index, where the running sum crosses u * total
+// Drafts (one launch):
+//   fused : per (draft, chunk) the chunk maximum and the sum of the weights shifted by it; the
+//           last chunk CTA of a draft rescales the chunk sums to the row maximum and locates
+//           the token the same way
 //
 // The draw weights are computed to ~1e-14 relative (a float-float 2^x: the exponent split
-// into an integer, a 1/32 step from a table and a short Taylor series) and summed as
-// float-float pairs inside a warp and in float64 beyond it, so a draw agrees with a float64
-// reference except where u * total lies within ~1e-12 of a cumulative boundary.
+// into an integer, a 1/32 step from a table and a short Taylor series) and summed and scanned as
+// float-float pairs throughout (no float64: this part runs it at a small fraction of the F32
+// rate), so a draw agrees with a float64 reference except where u * total lies within ~1e-12
+// of a cumulative boundary.
 #include <cmath>
 
 #include "df_internal.cuh"
@@ -88,8 +94,6 @@ __device__ __forceinline__ FF ff_mul(FF a, FF b) {
     return fast_two_sum(p, fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e)));
 }
 
-__device__ __forceinline__ double ff_to_double(FF a) { return (double)a.hi + (double)a.lo; }
-
 __device__ __forceinline__ FF warp_ff_sum(FF v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -101,21 +105,18 @@ __device__ __forceinline__ FF warp_ff_sum(FF v) {
     return v;
 }
 
-// 2^(l * scale - M) for a logit l: scale = sc_hi + sc_lo, M an F32 shift (the row maximum of
-// the F32 products, so the result is <= ~1). The product and the shift are carried exactly as
-// a float-float d; d = n + k/32 + r with integer n, |k| <= 16, |r| <= 1/64; 2^(k/32) comes from
-// the table (float-float, computed on the host in double), 2^r = exp(r ln 2) from the Taylor
-// series to the 6th power (|r ln 2| < 0.011, the next term < 4e-18).
-__device__ __forceinline__ FF weight_ff(float l, float M, const SampleArgs &a) {
-    const float p_hi = l * a.sc_hi;
-    const float p_lo = fmaf(l, a.sc_lo, fmaf(l, a.sc_hi, -p_hi));
-    FF d = two_sum(p_hi, -M);
-    d = fast_two_sum(d.hi, d.lo + p_lo);
-    if (!(d.hi > -126.f)) return {0.f, 0.f};          // below 2^-126 of the row maximum
+// 2^d for a float-float d (d.hi <= ~0; 0 below 2^-126). d = n + k/32 + r with integer n,
+// |k| <= 16, |r| <= 1/64; 2^(k/32) comes from the table (float-float, computed on the host in
+// double), 2^r = exp(r ln 2) from the Taylor series to the 6th power (|r ln 2| < 0.011, the next
+// term < 4e-18). The fast_two_sum steps are exact: d.hi - n and f.hi - k/32 are 0 or at least
+// one ulp of the word whose half-ulp bounds the low part, |g| > g^2 / 2, and the table entry
+// (>= 0.7) exceeds its product with |E| < 0.012.
+__device__ __forceinline__ FF exp2_ff(FF d, const SampleArgs &a, const float2 *tab) {
+    if (!(d.hi > -126.f)) return {0.f, 0.f};
     const float nf = rintf(d.hi);
-    FF f = two_sum(d.hi - nf, d.lo);                   // d.hi - nf is exact
+    const FF f = fast_two_sum(d.hi - nf, d.lo);        // d.hi - nf is exact
     const float kf = rintf(f.hi * 32.f);
-    FF r = two_sum(fmaf(kf, -0.03125f, f.hi), f.lo);   // f.hi - k/32 is exact
+    const FF r = fast_two_sum(fmaf(kf, -0.03125f, f.hi), f.lo);   // f.hi - k/32 is exact
     const float g_hi = r.hi * a.ln2_hi;
     const float g_lo = fmaf(r.hi, a.ln2_lo, fmaf(r.lo, a.ln2_hi, fmaf(r.hi, a.ln2_hi, -g_hi)));
     const float sq_hi = g_hi * g_hi;
@@ -123,31 +124,38 @@ __device__ __forceinline__ FF weight_ff(float l, float M, const SampleArgs &a) {
     const float tail =
         sq_hi * g_hi *
         (1.f / 6.f + g_hi * (1.f / 24.f + g_hi * (1.f / 120.f + g_hi * (1.f / 720.f))));
-    FF E = two_sum(g_hi, 0.5f * sq_hi);
+    FF E = fast_two_sum(g_hi, 0.5f * sq_hi);
     E = fast_two_sum(E.hi, E.lo + (g_lo + 0.5f * sq_lo + tail));
-    const float2 t = a.exp2_tab[min(max((int)kf + 16, 0), 32)];
+    const float2 t = tab[min(max((int)kf + 16, 0), 32)];
     const float m_hi = t.x * E.hi;
     const float m_lo = fmaf(t.x, E.hi, -m_hi) + fmaf(t.x, E.lo, t.y * E.hi);
-    FF w = two_sum(t.x, m_hi);
+    FF w = fast_two_sum(t.x, m_hi);
     w = fast_two_sum(w.hi, w.lo + (t.y + m_lo));
     const float s = __int_as_float(((int)nf + 127) << 23);   // 2^n, n in [-126, 0]
     return {w.hi * s, w.lo * s};
+}
+
+// 2^(l * scale - M) for a logit l: scale = sc_hi + sc_lo, M an F32 shift at least the largest
+// F32 product l * sc_hi it is used with (so the result is <= ~1). The product and the shift are
+// carried exactly as a float-float exponent.
+__device__ __forceinline__ FF weight_ff(float l, float M, const SampleArgs &a,
+                                        const float2 *tab) {
+    const float p_hi = l * a.sc_hi;
+    const float p_lo = fmaf(l, a.sc_lo, fmaf(l, a.sc_hi, -p_hi));
+    FF d = two_sum(p_hi, -M);
+    d = fast_two_sum(d.hi, d.lo + p_lo);
+    return exp2_ff(d, a, tab);
 }
 
 __device__ __forceinline__ const float *draft_row(const SampleArgs &a, int b, int i) {
     return a.draft + ((size_t)b * a.draft_ld + i) * a.V;
 }
 
-// Row rho of sequence b in the statistics. Accept mode: rho <= K is target row rho, rho > K is
-// draft row rho - K - 1. Sample mode: draft row rho.
+// Row rho of sequence b in the accept step's statistics: rho <= K is target row rho, rho > K is
+// draft row rho - K - 1.
 __device__ __forceinline__ const float *row_ptr(const SampleArgs &a, int b, int rho) {
-    if (a.sample_mode) return draft_row(a, b, rho);
     if (rho <= a.K) return a.target + ((size_t)b * (a.K + 1) + rho) * a.V;
     return draft_row(a, b, rho - a.K - 1);
-}
-
-__device__ __forceinline__ int stat_rows(const SampleArgs &a) {
-    return a.sample_mode ? a.K : 2 * a.K + 1;
 }
 
 __global__ void __launch_bounds__(kSThreads) sample_stats_kernel(SampleArgs a) {
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kSThreads) sample_stats_kernel(SampleArgs a) {
     __shared__ MS red[kSThreads / 32];
     pdl_trigger();
     pdl_wait();
-    const int c = blockIdx.x, rows = stat_rows(a);
+    const int c = blockIdx.x, rows = 2 * a.K + 1;
     const int b = blockIdx.y / rows, rho = blockIdx.y - b * rows;
     const float *row = row_ptr(a, b, rho);
     const int j0 = c * kSChunk + threadIdx.x * kEPT;
@@ -187,20 +195,6 @@ __global__ void __launch_bounds__(kSThreads) sample_stats_kernel(SampleArgs a) {
         for (int w = 1; w < kSThreads / 32; ++w) r = ms_merge(r, red[w]);
         a.stats[(size_t)blockIdx.y * gridDim.x + c] = r;
     }
-}
-
-// Row maximum from the chunk statistics (exact: a maximum of maxima).
-__device__ float row_max(const SampleArgs &a, const MS *p) {
-    __shared__ float wm[kSThreads / 32];
-    float m = -INFINITY;
-    for (int c = threadIdx.x; c < a.n_chunks; c += kSThreads) m = fmaxf(m, p[c].m);
-    m = warp_max(m);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
-    __syncthreads();
-    float r = wm[0];
-    for (int w = 1; w < kSThreads / 32; ++w) r = fmaxf(r, wm[w]);
-    return r;
 }
 
 // One CTA per sequence: warps merge the chunk statistics of the 2K+1 rows (lanes over chunks in
@@ -252,11 +246,11 @@ __global__ void __launch_bounds__(kSThreads) sample_walk_kernel(SampleArgs a) {
 }
 
 // What one draw reads: its p row (and, for a residual draw, its q row), their shifts, and the
-// float-float reciprocals of their exp sums (residual draws only).
+// float-float exp sums of both rows (residual draws only).
 struct DrawJob {
     const float *p, *q;
     float mp, mq;
-    FF ip, iq;
+    FF Sp, Sq;   // residual draws: the exp sums of the p and q rows
     float u;
 };
 
@@ -269,19 +263,79 @@ __device__ DrawJob accept_job(const SampleArgs &a, int b) {
     j.mp = st.mp;
     j.mq = st.mq;
     j.u = a.u_sample[b];
-    j.ip = j.iq = {0.f, 0.f};
+    j.Sp = j.Sq = {0.f, 0.f};
     return j;
+}
+
+// ------------------------------------------------------------------ block-wide float-float
+// Warp sums and scans in a fixed order, then the 8 warp values in warp order; every CTA that
+// runs them on the same data gets the same bits.
+__device__ __forceinline__ FF ff_block_sum(FF v, FF *sh) {
+    v = warp_ff_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    __syncthreads();
+    FF t{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kSThreads / 32; ++w) t = ff_add(t, sh[w]);
+    return t;
+}
+
+// Exclusive prefix (thread order) of v over the CTA; *total = the sum over all threads.
+__device__ __forceinline__ FF ff_block_exscan(FF v, FF *sh, FF *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    FF inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        FF n;
+        n.hi = __shfl_up_sync(0xffffffffu, inc.hi, o);
+        n.lo = __shfl_up_sync(0xffffffffu, inc.lo, o);
+        if (lane >= o) inc = ff_add(n, inc);
+    }
+    FF ex;
+    ex.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    ex.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (lane == 0) ex = {0.f, 0.f};
+    __syncthreads();
+    if (lane == 31) sh[warp] = inc;
+    __syncthreads();
+    FF off{0.f, 0.f}, t{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kSThreads / 32; ++w) {
+        if (w < warp) off = ff_add(off, sh[w]);
+        t = ff_add(t, sh[w]);
+    }
+    *total = t;
+    return ff_add(off, ex);
+}
+
+__device__ __forceinline__ bool ff_gt(FF a, FF b) {
+    return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ FF ldcg_ff(const float2 *p) {
+    const float2 v = __ldcg(p);
+    return {v.x, v.y};
+}
+
+// The 2^(k/32) table of the draw weights, copied from the kernel parameters into shared memory
+// (lanes index it with different k).
+__device__ __forceinline__ void load_tab(const SampleArgs &a, float2 *tab) {
+    if (threadIdx.x < 33) tab[threadIdx.x] = a.exp2_tab[threadIdx.x];
+    __syncthreads();
 }
 
 // Sums of 2^(x - M) of the draw's p and q rows over one chunk (residual draws only).
 __global__ void __launch_bounds__(kSThreads) sample_norm_kernel(SampleArgs a) {
     DF_TRACE_KERNEL(TK_SAMPLE_NORM);
-    __shared__ double wsum[2][kSThreads / 32];
+    __shared__ float2 tab[33];
+    __shared__ FF red[kSThreads / 32];
     pdl_trigger();
     pdl_wait();
     const int c = blockIdx.x, b = blockIdx.y;
     const DrawJob jb = accept_job(a, b);
     if (!jb.q) return;
+    load_tab(a, tab);
     const int j0 = c * kSChunk + threadIdx.x * kEPT;
     FF sp{0.f, 0.f}, sq{0.f, 0.f};
 #pragma unroll
@@ -289,40 +343,31 @@ __global__ void __launch_bounds__(kSThreads) sample_norm_kernel(SampleArgs a) {
         if (j0 + 4 * h < a.V) {
             const float4 lp = __ldcg(reinterpret_cast<const float4 *>(jb.p + j0 + 4 * h));
             const float4 lq = __ldcg(reinterpret_cast<const float4 *>(jb.q + j0 + 4 * h));
-            sp = ff_add(sp, weight_ff(lp.x, jb.mp, a));
-            sp = ff_add(sp, weight_ff(lp.y, jb.mp, a));
-            sp = ff_add(sp, weight_ff(lp.z, jb.mp, a));
-            sp = ff_add(sp, weight_ff(lp.w, jb.mp, a));
-            sq = ff_add(sq, weight_ff(lq.x, jb.mq, a));
-            sq = ff_add(sq, weight_ff(lq.y, jb.mq, a));
-            sq = ff_add(sq, weight_ff(lq.z, jb.mq, a));
-            sq = ff_add(sq, weight_ff(lq.w, jb.mq, a));
+            sp = ff_add(sp, weight_ff(lp.x, jb.mp, a, tab));
+            sp = ff_add(sp, weight_ff(lp.y, jb.mp, a, tab));
+            sp = ff_add(sp, weight_ff(lp.z, jb.mp, a, tab));
+            sp = ff_add(sp, weight_ff(lp.w, jb.mp, a, tab));
+            sq = ff_add(sq, weight_ff(lq.x, jb.mq, a, tab));
+            sq = ff_add(sq, weight_ff(lq.y, jb.mq, a, tab));
+            sq = ff_add(sq, weight_ff(lq.z, jb.mq, a, tab));
+            sq = ff_add(sq, weight_ff(lq.w, jb.mq, a, tab));
         }
     }
-    sp = warp_ff_sum(sp);
-    sq = warp_ff_sum(sq);
-    if ((threadIdx.x & 31) == 0) {
-        wsum[0][threadIdx.x >> 5] = ff_to_double(sp);
-        wsum[1][threadIdx.x >> 5] = ff_to_double(sq);
-    }
-    __syncthreads();
-    if (threadIdx.x < 2) {
-        double t = 0.0;
-        for (int w = 0; w < kSThreads / 32; ++w) t += wsum[threadIdx.x][w];
-        a.dsum[((size_t)b * a.n_chunks + c) * 2 + threadIdx.x] = t;
+    sp = ff_block_sum(sp, red);
+    sq = ff_block_sum(sq, red);
+    if (threadIdx.x == 0) {
+        float2 *d = a.dsum + ((size_t)b * a.n_chunks + c) * 2;
+        d[0] = make_float2(sp.hi, sp.lo);
+        d[1] = make_float2(sq.hi, sq.lo);
     }
 }
 
-// Float-float reciprocal of a positive double.
-__device__ __forceinline__ FF ff_recip(double s) {
-    const double r = 1.0 / s;
-    const float hi = (float)r;
-    return {hi, (float)(r - (double)hi)};
-}
-
-// The weights of thread t_idx's kEPT logits of chunk cc.
-__device__ __forceinline__ void chunk_weights(const SampleArgs &a, const DrawJob &jb, int cc,
-                                              int t_idx, FF (&w)[kEPT]) {
+// The draw weights of thread t_idx's kEPT logits of chunk cc. Residual draws use
+// max(0, p - q) scaled by S_p S_q (a draw is unchanged by a positive scale):
+// 2^(x - mp) S_q - 2^(y - mq) S_p.
+__device__ __forceinline__ void chunk_weights(const SampleArgs &a, const float2 *tab,
+                                              const DrawJob &jb, int cc, int t_idx,
+                                              FF (&w)[kEPT]) {
     const int j0 = cc * kSChunk + t_idx * kEPT;
 #pragma unroll
     for (int h = 0; h < kEPT / 4; ++h) {
@@ -337,11 +382,10 @@ __device__ __forceinline__ void chunk_weights(const SampleArgs &a, const DrawJob
         for (int e = 0; e < 4; ++e) {
             FF v{0.f, 0.f};
             if (ok) {
-                v = weight_ff(lpv[e], jb.mp, a);
+                v = weight_ff(lpv[e], jb.mp, a, tab);
                 if (jb.q) {
-                    // max(0, p - q) with p = 2^(x - mp) / S_p and q = 2^(y - mq) / S_q
-                    const FF pn = ff_mul(v, jb.ip);
-                    const FF qn = ff_mul(weight_ff(lqv[e], jb.mq, a), jb.iq);
+                    const FF pn = ff_mul(v, jb.Sq);
+                    const FF qn = ff_mul(weight_ff(lqv[e], jb.mq, a, tab), jb.Sp);
                     v = ff_add(pn, FF{-qn.hi, -qn.lo});
                     if (!(v.hi > 0.f)) v = {0.f, 0.f};
                 }
@@ -358,62 +402,124 @@ __device__ __forceinline__ FF thread_sum(const FF (&w)[kEPT]) {
     return s;
 }
 
-// grid (chunks, draws). Accept mode: draw b of sequence b, then the committed tokens.
-// Sample mode: draw b * K + i is draft i of sequence b, from softmax(draft row i / T).
+// The last CTA of a draw, step 1: thread t owns chunks [t * per, (t + 1) * per) (thread order
+// is chunk order) and wcs(cc) gives chunk cc's weight sum. Finds the first chunk whose running
+// sum exceeds u * total, or, when rounding puts the target past the total, the last chunk with
+// weight; returns it with the running sum before it (*base) and the target.
+template <typename ChunkW>
+__device__ __forceinline__ int locate_chunk(int n_chunks, ChunkW wcs, float u, FF *red,
+                                            int *s_pick, int *s_pick_last, FF *s_base,
+                                            FF *base, FF *target, FF *total) {
+    const int per = (n_chunks + kSThreads - 1) / kSThreads;   // <= kMaxChunks / kSThreads
+    FF cv[kMaxChunks / kSThreads];
+    FF mine{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kMaxChunks / kSThreads; ++i) {
+        const int cc = threadIdx.x * per + i;
+        cv[i] = (i < per && cc < n_chunks) ? wcs(cc) : FF{0.f, 0.f};
+        mine = ff_add(mine, cv[i]);
+    }
+    if (threadIdx.x == 0) {
+        *s_pick = INT_MAX;
+        *s_pick_last = -1;
+        *s_base = {0.f, 0.f};
+    }
+    FF run = ff_block_exscan(mine, red, total);   // its barriers order the resets above
+    *target = ff_mul(*total, FF{u, 0.f});
+    int pick = INT_MAX, pick_last = -1;
+    FF base_pick{0.f, 0.f}, base_last{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kMaxChunks / kSThreads; ++i) {
+        const int cc = threadIdx.x * per + i;
+        if (i < per && cc < n_chunks) {
+            const FF nx = ff_add(run, cv[i]);
+            if (cv[i].hi > 0.f) {
+                pick_last = cc;
+                base_last = run;
+            }
+            if (pick == INT_MAX && ff_gt(nx, *target)) {
+                pick = cc;
+                base_pick = run;
+            }
+            run = nx;
+        }
+    }
+    atomicMin(s_pick, pick);
+    atomicMax(s_pick_last, pick_last);
+    __syncthreads();
+    const bool found = *s_pick != INT_MAX;
+    const int cstar = found ? *s_pick : max(*s_pick_last, 0);
+    if (found ? pick == cstar : pick_last == cstar) *s_base = found ? base_pick : base_last;
+    __syncthreads();
+    *base = *s_base;
+    return cstar;
+}
+
+// Step 2: thread t holds weights w of indices j0 .. j0 + kEPT - 1 of the chunk (thread order is
+// index order); the running sum at index j is base + fac * (the chunk's weights up to j). The
+// first index whose running sum exceeds the target, else the last index with weight, else -1.
+__device__ __forceinline__ int locate_in_chunk(const FF (&w)[kEPT], int j0, int V, FF base,
+                                               FF fac, FF target, FF *red, int *s_pick,
+                                               int *s_pick_last) {
+    __syncthreads();   // the step-1 readers of *s_pick are done
+    if (threadIdx.x == 0) {
+        *s_pick = INT_MAX;
+        *s_pick_last = -1;
+    }
+    FF ctot;
+    FF run = ff_block_exscan(thread_sum(w), red, &ctot);
+    int pick = INT_MAX, pick_last = -1;
+#pragma unroll
+    for (int i = 0; i < kEPT; ++i) {
+        if (j0 + i < V) {
+            const FF nx = ff_add(run, w[i]);
+            if (w[i].hi > 0.f) pick_last = j0 + i;
+            if (pick == INT_MAX && ff_gt(ff_add(base, ff_mul(fac, nx)), target)) pick = j0 + i;
+            run = nx;
+        }
+    }
+    atomicMin(s_pick, pick);
+    atomicMax(s_pick_last, pick_last);
+    __syncthreads();
+    return *s_pick != INT_MAX ? *s_pick : *s_pick_last;
+}
+
+// Accept mode, grid (chunks, B): the draw of sequence b, then its committed tokens. Every chunk
+// CTA writes its chunk's weight sum; the last one to finish locates the chunk, then the token.
 __global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
     DF_TRACE_KERNEL(TK_SAMPLE_DRAW);
-    __shared__ double wsum[kSThreads / 32];
-    __shared__ double tsum[kSThreads];
-    __shared__ double s_norm[2];
-    __shared__ float s_max;
-    __shared__ int s_last, s_chunk;
-    __shared__ double s_base, s_target;
+    __shared__ float2 tab[33];
+    __shared__ FF red[kSThreads / 32];
+    __shared__ int s_last, s_pick, s_pick_last;
+    __shared__ FF s_base;
     pdl_trigger();
     pdl_wait();
+    load_tab(a, tab);
     const int c = blockIdx.x, job = blockIdx.y;
-    DrawJob jb;
-    if (a.sample_mode) {
-        const int b = job / a.K, i = job - b * a.K;
-        jb.p = draft_row(a, b, i);
-        jb.q = nullptr;
-        const float M = row_max(a, a.stats + (size_t)job * a.n_chunks);
-        if (threadIdx.x == 0) s_max = M;
-        __syncthreads();
-        jb.mp = s_max;
-        jb.mq = 0.f;
-        jb.u = a.u_draft[job];
-        jb.ip = jb.iq = {0.f, 0.f};
-    } else {
-        jb = accept_job(a, job);
-        if (jb.q) {
-            // S_p and S_q from the chunk sums of the norm kernel, in chunk order
-            if (threadIdx.x < 2) {
-                const double *ds = a.dsum + (size_t)job * a.n_chunks * 2;
-                double t = 0.0;
-                for (int cc = 0; cc < a.n_chunks; ++cc) t += __ldcg(ds + 2 * cc + threadIdx.x);
-                s_norm[threadIdx.x] = t;
-            }
-            __syncthreads();
-            if (!(s_norm[0] > 0.0) || !(s_norm[1] > 0.0)) {
-                set_status(a.status, DF_EINVAL);
-                jb.q = nullptr;   // degenerate input: draw from p
-            } else {
-                jb.ip = ff_recip(s_norm[0]);
-                jb.iq = ff_recip(s_norm[1]);
-            }
+    DrawJob jb = accept_job(a, job);
+    if (jb.q) {
+        // S_p and S_q from the norm kernel's chunk sums; every CTA of the draw runs the same
+        // reduction, so all of them scale the weights identically
+        FF sp{0.f, 0.f}, sq{0.f, 0.f};
+        const float2 *ds = a.dsum + (size_t)job * a.n_chunks * 2;
+        for (int cc = threadIdx.x; cc < a.n_chunks; cc += kSThreads) {
+            sp = ff_add(sp, ldcg_ff(ds + 2 * cc));
+            sq = ff_add(sq, ldcg_ff(ds + 2 * cc + 1));
+        }
+        sp = ff_block_sum(sp, red);
+        sq = ff_block_sum(sq, red);
+        if (!(sp.hi > 0.f) || !(sq.hi > 0.f)) {
+            if (threadIdx.x == 0) set_status(a.status, DF_EINVAL);
+            jb.q = nullptr;   // degenerate input: draw from p
+        } else {
+            jb.Sp = sp;
+            jb.Sq = sq;
         }
     }
     FF w[kEPT];
-    chunk_weights(a, jb, c, threadIdx.x, w);
-    const FF ts = warp_ff_sum(thread_sum(w));
-    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ff_to_double(ts);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int i = 0; i < kSThreads / 32; ++i) t += wsum[i];
-        a.csum[(size_t)job * a.n_chunks + c] = t;
-    }
-    // the last chunk CTA of the draw locates it
+    chunk_weights(a, tab, jb, c, threadIdx.x, w);
+    const FF cs_own = ff_block_sum(thread_sum(w), red);
+    if (threadIdx.x == 0) a.csum[(size_t)job * a.n_chunks + c] = make_float2(cs_own.hi, cs_own.lo);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) s_last = atomicAdd(&a.counters[job], 1) == a.n_chunks - 1;
@@ -421,85 +527,18 @@ __global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
     if (!s_last) return;
     __threadfence();
     if (threadIdx.x == 0) a.counters[job] = 0;   // left at zero for the next call
-    const double *cs = a.csum + (size_t)job * a.n_chunks;
-    double tot = 0.0, run = 0.0, base = 0.0, base_last = 0.0, target = 0.0;
-    int cstar = -1, last_pos = 0;
-    for (int c0 = 0; c0 < a.n_chunks; c0 += kSThreads) {
-        const int n = min(kSThreads, a.n_chunks - c0);
-        __syncthreads();
-        if ((int)threadIdx.x < n) tsum[threadIdx.x] = __ldcg(cs + c0 + threadIdx.x);
-        __syncthreads();
-        if (threadIdx.x == 0)
-            for (int i = 0; i < n; ++i) tot += tsum[i];
-    }
-    if (threadIdx.x == 0) target = (double)jb.u * tot;
-    for (int c0 = 0; c0 < a.n_chunks; c0 += kSThreads) {
-        const int n = min(kSThreads, a.n_chunks - c0);
-        __syncthreads();
-        if ((int)threadIdx.x < n) tsum[threadIdx.x] = __ldcg(cs + c0 + threadIdx.x);
-        __syncthreads();
-        if (threadIdx.x == 0)
-            for (int i = 0; i < n; ++i) {
-                const double v = tsum[i];
-                if (v > 0.0) {
-                    last_pos = c0 + i;
-                    base_last = run;
-                }
-                if (cstar < 0 && run + v > target) {
-                    cstar = c0 + i;
-                    base = run;
-                }
-                run += v;
-            }
-    }
-    if (threadIdx.x == 0) {
-        if (cstar < 0) {                    // rounding put the target past the total
-            cstar = last_pos;
-            base = base_last;
-        }
-        s_chunk = cstar;
-        s_base = base;
-        s_target = target;
-        if (!(tot > 0.0)) set_status(a.status, DF_EINVAL);
-    }
-    __syncthreads();
-    chunk_weights(a, jb, s_chunk, threadIdx.x, w);
-    tsum[threadIdx.x] = ff_to_double(thread_sum(w));
-    __syncthreads();
+    const float2 *cs = a.csum + (size_t)job * a.n_chunks;
+    FF base, target, tot;
+    const int cstar = locate_chunk(
+        a.n_chunks, [&](int cc) { return ldcg_ff(cs + cc); }, jb.u, red, &s_pick,
+        &s_pick_last, &s_base, &base, &target, &tot);
+    if (threadIdx.x == 0 && !(tot.hi > 0.f)) set_status(a.status, DF_EINVAL);
+    chunk_weights(a, tab, jb, cstar, threadIdx.x, w);
+    int idx = locate_in_chunk(w, cstar * kSChunk + threadIdx.x * kEPT, a.V, base, FF{1.f, 0.f},
+                              target, red, &s_pick, &s_pick_last);
     if (threadIdx.x != 0) return;
-    // running sum over the chunk's threads in index order, then inside the found thread
-    double r = s_base;
-    int tok = -1, last_t = -1;
-    for (int t = 0; t < kSThreads && tok < 0; ++t) {
-        const double v = tsum[t];
-        if (v > 0.0) last_t = t;
-        if (r + v > s_target) tok = t;
-        else r += v;
-    }
-    if (tok < 0) tok = last_t < 0 ? 0 : last_t;
-    int idx = -1;
-    {
-        const int j0 = s_chunk * kSChunk + tok * kEPT;
-        FF wv[kEPT];
-        chunk_weights(a, jb, s_chunk, tok, wv);
-        int lastj = j0;
-        for (int i = 0; i < kEPT; ++i) {
-            if (j0 + i >= a.V) break;
-            const double v = ff_to_double(wv[i]);
-            if (v > 0.0) lastj = j0 + i;
-            if (r + v > s_target) {
-                idx = j0 + i;
-                break;
-            }
-            r += v;
-        }
-        if (idx < 0) idx = lastj;
-    }
+    if (idx < 0) idx = cstar * kSChunk;
     if (!df_in_bounds(idx >= 0 && idx < a.V, a.status)) idx = 0;
-    if (a.sample_mode) {
-        a.drafts_out[job] = idx;
-        return;
-    }
     // committed tokens: accepted drafts, then the drawn token, cut after the first EOS
     const int b = job, acc = a.state[b].acc;
     int32_t *out = a.committed + (size_t)b * (a.K + 1);
@@ -520,6 +559,95 @@ __global__ void __launch_bounds__(kSThreads) sample_draw_kernel(SampleArgs a) {
     a.hit_eos[b] = hit;
 }
 
+// Sample mode, one pass: grid (chunks, B * K), draw b * K + i is draft i of sequence b, from
+// softmax(draft row i / T). Each chunk CTA takes its own maximum m_c as the shift and writes m_c
+// and S_c = sum of 2^(x - m_c); the last CTA of the draw rescales the chunk sums by
+// 2^(m_c - M) (M the row maximum), locates the chunk, and recomputes that chunk's weights with
+// the same shift for the token.
+__global__ void __launch_bounds__(kSThreads) sample_fused_kernel(SampleArgs a) {
+    DF_TRACE_KERNEL(TK_SAMPLE_FUSED);
+    __shared__ float2 tab[33];
+    __shared__ FF red[kSThreads / 32];
+    __shared__ float wm[kSThreads / 32];
+    __shared__ int s_last, s_pick, s_pick_last;
+    __shared__ FF s_base;
+    pdl_trigger();
+    pdl_wait();
+    load_tab(a, tab);
+    const int c = blockIdx.x, job = blockIdx.y;
+    const int b = job / a.K, i = job - b * a.K;
+    const float *row = draft_row(a, b, i);
+    const float u = a.u_draft[job];
+    float *cm = &a.stats[(size_t)job * a.n_chunks].m;   // m_c, stride sizeof(MaxSum) / 4
+    constexpr int kMS = sizeof(MaxSum) / sizeof(float);
+    float2 *cs = a.csum + (size_t)job * a.n_chunks;
+    auto load = [&](int cc, float (&l)[kEPT]) {
+        const int j0 = cc * kSChunk + threadIdx.x * kEPT;
+#pragma unroll
+        for (int h = 0; h < kEPT / 4; ++h) {
+            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (j0 + 4 * h < a.V) v = __ldcg(reinterpret_cast<const float4 *>(row + j0 + 4 * h));
+            l[4 * h] = v.x;
+            l[4 * h + 1] = v.y;
+            l[4 * h + 2] = v.z;
+            l[4 * h + 3] = v.w;
+        }
+    };
+    float l[kEPT];
+    load(c, l);
+    float m = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kEPT; ++e) m = fmaxf(m, l[e] * a.sc_hi);
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float mc = wm[0];
+#pragma unroll
+    for (int w_ = 1; w_ < kSThreads / 32; ++w_) mc = fmaxf(mc, wm[w_]);
+    FF w[kEPT];
+#pragma unroll
+    for (int e = 0; e < kEPT; ++e) w[e] = weight_ff(l[e], mc, a, tab);
+    FF sc;
+    ff_block_exscan(thread_sum(w), red, &sc);
+    if (threadIdx.x == 0) {
+        cm[(size_t)c * kMS] = mc;
+        cs[c] = make_float2(sc.hi, sc.lo);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&a.counters[job], 1) == a.n_chunks - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) a.counters[job] = 0;   // left at zero for the next call
+    // the row maximum M over the chunk maxima (exact), then each chunk's scale 2^(m_c - M)
+    float M = -INFINITY;
+    for (int cc = threadIdx.x; cc < a.n_chunks; cc += kSThreads) M = fmaxf(M, __ldcg(cm + (size_t)cc * kMS));
+    M = warp_max(M);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = wm[0];
+#pragma unroll
+    for (int w_ = 1; w_ < kSThreads / 32; ++w_) M = fmaxf(M, wm[w_]);
+    auto fac = [&](int cc) { return exp2_ff(two_sum(__ldcg(cm + (size_t)cc * kMS), -M), a, tab); };
+    FF base, target, tot;
+    const int cstar = locate_chunk(
+        a.n_chunks, [&](int cc) { return ff_mul(ldcg_ff(cs + cc), fac(cc)); }, u, red, &s_pick,
+        &s_pick_last, &s_base, &base, &target, &tot);
+    if (threadIdx.x == 0 && !(tot.hi > 0.f)) set_status(a.status, DF_EINVAL);
+    const float mstar = __ldcg(cm + (size_t)cstar * kMS);
+    load(cstar, l);
+#pragma unroll
+    for (int e = 0; e < kEPT; ++e) w[e] = weight_ff(l[e], mstar, a, tab);
+    int idx = locate_in_chunk(w, cstar * kSChunk + threadIdx.x * kEPT, a.V, base, fac(cstar),
+                              target, red, &s_pick, &s_pick_last);
+    if (threadIdx.x != 0) return;
+    if (idx < 0) idx = cstar * kSChunk;
+    if (!df_in_bounds(idx >= 0 && idx < a.V, a.status)) idx = 0;
+    a.drafts_out[job] = idx;
+}
+
 }  // namespace
 
 int sample_chunks(int V) { return (V + kSChunk - 1) / kSChunk; }
@@ -528,8 +656,8 @@ void carve_sample_scratch(Carve &cv, SampleArgs &a, int B, int K, int V) {
     a.n_chunks = sample_chunks(V);
     a.stats = cv.take<MaxSum>((size_t)B * (2 * K + 1) * a.n_chunks);
     a.state = cv.take<SampleState>((size_t)B);
-    a.dsum = cv.take<double>((size_t)B * a.n_chunks * 2);
-    a.csum = cv.take<double>((size_t)B * K * a.n_chunks);
+    a.dsum = cv.take<float2>((size_t)B * a.n_chunks * 2);
+    a.csum = cv.take<float2>((size_t)B * K * a.n_chunks);
     a.counters = cv.take<int>((size_t)B * K);
 }
 
@@ -561,9 +689,7 @@ int launch_accept_stochastic(const SampleArgs &a, cudaStream_t s) {
 
 int launch_sample_drafts(const SampleArgs &a, cudaStream_t s) {
     if (a.n_chunks > kMaxChunks) return fail(DF_ESHAPE, "vocabulary of %d is too large", a.V);
-    DF_TRY(launch_k("sample_stats_kernel", sample_stats_kernel, dim3(a.n_chunks, a.B * a.K),
-                    dim3(kSThreads), 0, s, a));
-    return launch_k("sample_draw_kernel", sample_draw_kernel, dim3(a.n_chunks, a.B * a.K),
+    return launch_k("sample_fused_kernel", sample_fused_kernel, dim3(a.n_chunks, a.B * a.K),
                     dim3(kSThreads), 0, s, a);
 }
 

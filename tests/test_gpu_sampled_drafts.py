@@ -4,8 +4,8 @@ sampled MTP chain (`mtp_forward_draft_sampled`).
 
 A draw from the same logits must equal the oracle's float64 draw wherever u * total lies more
 than DRAW_TOL (a fraction of the total) from a cumulative boundary: the kernels compute the
-weights to ~1e-14 relative and sum them in float-float / float64. Where the drafter's own logits
-feed a draw, the GPU's logits are compared with the oracle's within the float tolerance and the
+weights to ~1e-14 relative and sum and scan them as float-float pairs. Where the drafter's own
+logits feed a draw, the GPU's logits are compared with the oracle's within the float tolerance and the
 draw is checked on the GPU's logits (the integer decision is taken on the kernel's floats); the
 drafts must also equal the oracle's own where its draw margin exceeds LOGIT_DRAW_TOL, which
 covers the logit differences of the whole forward."""

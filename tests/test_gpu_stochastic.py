@@ -13,7 +13,7 @@ from speculative_decoding_drafter_dflash_gb300 import binding as B
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 DECISION_MARGIN = 1e-4    # relative distance of u q(x) from p(x) below which a test is skipped
-DRAW_TOL = 1e-9           # of the total weight: float-float weights, float64 running sums
+DRAW_TOL = 1e-9           # of the total weight: float-float weights and running sums
 
 
 @pytest.fixture(scope="module", autouse=True)
