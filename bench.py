@@ -1016,6 +1016,8 @@ def generate_case(steps: int):
         del cache, ws, table, prior
 
 
+TRACE_MARK = 1000                # kids of the in-kernel trace marks: TRACE_MARK + phase
+GEMM_MARKS = (11, 12, 13)        # phases marked by the projection kernel; the others by attention
 TRACE_NAMES = {1: "rope_table", 2: "qk_rope", 3: "attn", 4: "attn_combine", 5: "seq_advance",
                6: "attn_tc", 15: "pack", 16: "pack", 17: "argmax_final", 18: "accept",
                19: "rollback", 20: "word_copy"}
@@ -1076,6 +1078,9 @@ def trace_case(args):
     kid, sm, t0, t1 = B.trace_read()
     if args.trace_dump:
         np.savez(args.trace_dump, kid=kid, sm=sm, t0=t0, t1=t1, names=np.array(names))
+    is_mark = kid >= TRACE_MARK
+    mk, mt = kid[is_mark] - TRACE_MARK, t0[is_mark].astype(np.int64)
+    kid, sm, t0, t1 = kid[~is_mark], sm[~is_mark], t0[~is_mark], t1[~is_mark]
     # Every kernel waits for its predecessor's grid to complete before its CTAs finish, so the
     # launches follow one another in the order of their CTAs' end times (their start times
     # interleave: a successor's CTAs become resident early and wait).
@@ -1112,6 +1117,32 @@ def trace_case(args):
         e[3] = n
         crit_total += exposed / 1e3
     span = (groups[-1][2] - groups[0][1]) / 1e3 / rounds
+    # Points inside the kernels (trace marks): each belongs to the first launch of its kernel
+    # family that ends at or after it; reported as us after the end of the launch before that
+    # one (median over CTAs and launches, and the median over launches of the last CTA's).
+    phases = {}
+    for fam, sel in (("attn", lambda k: k == 6), ("gemm", lambda k: k >= 100)):
+        gi = [i for i, g_ in enumerate(groups) if sel(g_[0]) and i > 0]
+        if not gi:
+            continue
+        ends = np.array([groups[i][2] for i in gi], dtype=np.int64)
+        for ph in sorted(set(mk.tolist())):
+            if (ph in GEMM_MARKS) != (fam == "gemm"):
+                continue
+            t = mt[mk == ph]
+            j = np.searchsorted(ends, t, side="left")
+            ok_ = j < len(gi)
+            t, j = t[ok_], j[ok_]
+            rel = {}
+            for tt, jj in zip(t.tolist(), j.tolist()):
+                i = gi[jj]
+                name = names[i % per] if ok else fam
+                rel.setdefault(name, {}).setdefault(i, []).append((tt - groups[i - 1][2]) / 1e3)
+            for name, per_launch in rel.items():
+                allv = [v for vs in per_launch.values() for v in vs]
+                phases.setdefault(name, {})[str(ph)] = {
+                    "median_us": round(float(np.median(allv)), 2),
+                    "last_cta_us": round(float(np.median([max(vs) for vs in per_launch.values()])), 2)}
     table = {k: {"launches_per_round": v[0] // rounds, "span_us_each": round(v[1] / v[0], 2),
                  "critical_us_per_round": round(v[2] / rounds, 2), "ctas": v[3]}
              for k, v in sorted(agg.items(), key=lambda kv: -kv[1][2])}
@@ -1119,7 +1150,7 @@ def trace_case(args):
                       "rounds": rounds, "launches_per_round": per, "grouped_ok": ok,
                       "round_us": round(span, 1),
                       "critical_us_per_round": round(crit_total / rounds, 1), "kernels": table,
-                      "timeline": timeline}))
+                      "phases_after_previous_launch": phases, "timeline": timeline}))
 
 
 def profile_case(args):

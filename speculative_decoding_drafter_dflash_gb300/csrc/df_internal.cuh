@@ -131,6 +131,12 @@ struct TraceRec {
     unsigned long long t0, t1;
 };
 constexpr unsigned kTraceMax = 1u << 20;
+constexpr uint32_t kTraceMark = 1000;   // kids of DF_TRACE_MARK points: kTraceMark + phase
+// Phases: attention 1 (past the wait), 2 (Q operand written), 7 (score MMAs issued), 6 (score
+// MMAs done, warp 0), 15 (the same, warp 15), 10 (first score tile read from TMEM), 14 (row
+// maxima of warp 0 reduced), 3 (row maxima of all warps), 0 (first tile's scores read again), 8
+// (first P operand written), 4 (all P operands), 5 (P.V done), 9 (partial outputs stored);
+// projection 11 (producer past the wait), 12 (an accumulator ready), 13 (epilogue done).
 #if DF_TRACE
 extern __device__ TraceRec g_trace[kTraceMax];
 extern __device__ unsigned g_trace_n;
@@ -144,22 +150,48 @@ __device__ __forceinline__ uint32_t sm_id() {
     asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
     return v;
 }
-// Records the CTA's span when thread 0 leaves the kernel (its destructor runs at every return).
+// Records the CTA's span when thread 0 leaves the kernel (its destructor runs at every return),
+// followed by the CTA's trace marks: points inside the kernel that any one thread stamps into a
+// shared-memory slot per phase (no global traffic until the end, so marking barely perturbs the
+// kernel); a mark stamped twice keeps the later time. Marks are stamped only after the kernel's
+// first CTA-wide barrier, which orders them after the slots are cleared.
+constexpr int kTraceMarks = 16;
 struct TraceScope {
     unsigned long long t0;
     uint32_t kid;
-    __device__ explicit TraceScope(uint32_t k) : t0(global_ns()), kid(k) {}
+    unsigned long long *marks;
+    __device__ TraceScope(uint32_t k, unsigned long long *m) : t0(global_ns()), kid(k), marks(m) {
+        if (threadIdx.y == 0 && threadIdx.x < kTraceMarks) m[threadIdx.x] = 0ull;
+    }
     __device__ ~TraceScope() {
         if (threadIdx.x == 0 && threadIdx.y == 0) {
-            const unsigned i = atomicAdd(&g_trace_n, 1u);
+            unsigned n = 0;
+            for (int p = 0; p < kTraceMarks; ++p) n += marks[p] != 0ull;
+            const unsigned i = atomicAdd(&g_trace_n, 1u + n);
+            const uint32_t cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
             if (i < kTraceMax) g_trace[i] = TraceRec{kid, sm_id(), t0, global_ns()};
+            unsigned j = i + 1;
+            for (int p = 0; p < kTraceMarks; ++p)
+                if (marks[p] != 0ull) {
+                    if (j < kTraceMax) g_trace[j] = TraceRec{kTraceMark + p, cta, marks[p], 0ull};
+                    ++j;
+                }
         }
     }
 };
-#define DF_TRACE_KERNEL(kid) ::df::TraceScope df_trace_scope_((uint32_t)(kid))
+#define DF_TRACE_KERNEL(kid)                                          \
+    __shared__ unsigned long long df_trace_marks_[::df::kTraceMarks]; \
+    ::df::TraceScope df_trace_scope_((uint32_t)(kid), df_trace_marks_)
+#define DF_TRACE_MARK(who, phase)                              \
+    do {                                                       \
+        if (who) df_trace_marks_[(phase)] = ::df::global_ns(); \
+    } while (0)
 #else
 #define DF_TRACE_KERNEL(kid) \
     do {                     \
+    } while (0)
+#define DF_TRACE_MARK(who, phase) \
+    do {                          \
     } while (0)
 #endif
 

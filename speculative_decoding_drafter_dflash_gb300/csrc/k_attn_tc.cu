@@ -396,6 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
     }
     pdl_wait();
+    DF_TRACE_MARK(tid == 0, 1);
     const int rep = a.nq / a.nkv;
     const int R = a.blk * rep;
     const int nn = a.n_new ? min(max(a.n_new[b], 0), a.n_new_max) : 0;
@@ -513,6 +514,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    DF_TRACE_MARK(tid == 0, 2);
     const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NS);   // O^T accumulators
     // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
     // (every score MMA has completed before the first P is written), buffer 1 following it.
@@ -547,6 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     mma_bf16_ts(d, ahi + 64 + 8 * s, sw128_desc(bq + ob), idesc, 1u);
                 }
             }
+            DF_TRACE_MARK(true, 7);
             if (ok) mma_commit(sdone);
             for (int t = 0; t < n_tiles && ok; ++t) {
                 if (!(ok = mbar_wait(&vready[t], 0u, abort_flag, a.status) &&
@@ -746,14 +749,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         auto pass_max = [&](int p, int pt0, int nt) {
             mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
             tc_fence_after();
+            DF_TRACE_MARK(tid == 0, 6);
             float mx[NPH];
 #pragma unroll
             for (int r = 0; r < NPH; ++r) mx[r] = -INFINITY;
+            DF_TRACE_MARK(tid == kConvThreads - 32, 15);
             for (int tt = 0; tt < nt; ++tt) {
                 uint32_t sh[NPH], sl[NPH];
                 tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
                 tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
                 tmem_ld_wait();
+                DF_TRACE_MARK(tid == 0 && tt == 0, 10);
                 const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
 #pragma unroll
                 for (int r = 0; r < NPH; ++r)
@@ -763,6 +769,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             int row;
             const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
             if ((lane & (32 / NPH - 1)) == 0) red[lq * NP + r0 + row] = m;
+            DF_TRACE_MARK(tid == 0, 14);
             conv_sync();
 #pragma unroll
             for (int r = 0; r < NPH; ++r)
@@ -783,6 +790,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
                 tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
                 tmem_ld_wait();
+                DF_TRACE_MARK(tid == 0 && t == 0, 0);
 #pragma unroll
                 for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
             }
@@ -813,9 +821,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             for (int t = n_early; t < n_tiles; ++t)
                 convert_vs(t, t ? 0 : 2, (uint32_t)t, c0 + t * kTcKeys, S_cache, c1);
             pass_max(0, 0, n_tiles);
-            for (int t = 0; t < n_tiles; ++t) write_p(t, t);
+            DF_TRACE_MARK(tid == 0, 3);
+            for (int t = 0; t < n_tiles; ++t) {
+                write_p(t, t);
+                DF_TRACE_MARK(tid == 0 && t == 0, 8);
+            }
+            DF_TRACE_MARK(tid == 0, 4);
             mbar_wait(odone, 0u, abort_flag, a.status);
             tc_fence_after();
+            DF_TRACE_MARK(tid == 0, 5);
         }
         // Per pass: the K units, then as many V units as there are operand regions (their regions
         // are freed by the score MMAs alone), then the softmax; the probabilities of a tile are
@@ -964,6 +978,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     if (r0 + r < R) part[(size_t)(r0 + r) * (D + 2) + d] = o[r];
             }
         }
+        DF_TRACE_MARK(tid == 0, 9);
         conv_sync();
         if (tid < R) {
             const float M = mrun[tid];

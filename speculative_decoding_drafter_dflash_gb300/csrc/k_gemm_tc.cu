@@ -351,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 ++pre;
             }
             pdl_wait();
+            DF_TRACE_MARK(true, 11);
             {
                 Cursor cb;
                 cursor_init(cb);
@@ -463,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const int slot = (!p.splits && kb_start(blockIdx.x, p) / p.kbt == m) ? 0 : 1;
             const bool got = mbar_wait(&tfull[acc], aphase, abort_flag, p.status, p.wait_cycles);
             if (epi_any(!got)) break;   // all four epilogue warps leave together
+            DF_TRACE_MARK(threadIdx.x == 64, 12);
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.acc_cols);
             const int n_chunks = (p.T + kTokChunk - 1) / kTokChunk;
@@ -547,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (int t = threadIdx.x - 64; t < p.T; t += 128)
                 p.part[(size_t)blockIdx.x * p.T + t] = es.st[t];
         }
+        DF_TRACE_MARK(threadIdx.x == 64, 13);
     }
     tc_fence_before();
     __syncthreads();
