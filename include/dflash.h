@@ -35,6 +35,10 @@
  *  - Dimensions: every K dimension of a projection (hidden, intermediate, n_q_heads*head_dim,
  *    n_target_layers*hidden) must be a multiple of 8; head_dim a multiple of 32 and <= 256;
  *    rotary_dim even and <= head_dim; n_q_heads a multiple of n_kv_heads.
+ *  - Weights (row-major or tiled) are read-only inputs that must be complete when a call is
+ *    enqueued: a projection requests its first weight tiles before it waits for the kernel ahead
+ *    of it on the stream (programmatic dependent launch), so weights written by kernels on the
+ *    same stream need a stream synchronisation or an event wait before the call.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
@@ -135,7 +139,38 @@ typedef struct {
     const df_layer_weights *layers;  /* HOST array [n_layers] */
     const uint16_t *embed;           /* [V, H] BF16 token embedding (the target's, borrowed) */
     const uint16_t *lm_head;         /* [V, H] BF16 (the target's, borrowed) */
+    const void *tiled;               /* NULL, or the projection and lm_head weights re-laid out by
+                                        df_dflash_tile_weights from these same matrices: the
+                                        projections then read their weights from it (the matrices
+                                        above must stay valid: they still describe the shapes) */
 } df_dflash_weights;
+
+/*
+ * Tiled weights. The projections read their weights as 128-row x 64-column BF16 tiles; from the
+ * row-major [out, in] matrices each tile arrives as 128 strided 128-byte rows, from a tiled copy
+ * as one contiguous block laid out exactly as the tensor cores read it (the 128-byte-swizzled
+ * image: row r of a tile at byte r * 128, its 16-byte piece j at (j ^ (r % 8)) * 16; tile
+ * (m, kb) of a matrix at byte (m * kbt + kb) * 16384, kbt = ceil(in / 64); rows and columns past
+ * the matrix zero). Two K blocks are then moved per bulk copy, which on this part streams at the
+ * HBM rate where 16 KB tensor-map copies do not. A one-time device-to-device conversion at model
+ * load; the copy takes as many bytes as the matrices (padded to whole tiles).
+ *
+ * df_dflash_tiled_bytes: bytes of a DFlash model's tiled copy (fc, every layer's QKV, O,
+ *   gate/up (gate and up rows paired 64 + 64 per tile), down, then the lm_head); 0 on an invalid
+ *   config.
+ * df_dflash_tile_weights: fills `tiled` (device, >= df_dflash_tiled_bytes, 1024-byte aligned,
+ *   owned by the caller) from w's matrices on `stream`; set w->tiled = tiled afterwards, and
+ *   synchronise `stream` before the first call that reads it (see the weights convention above).
+ *   DF_EWORKSPACE when too small, DF_EINVAL on a bad pointer.
+ * df_tiled_matrix_bytes / df_tile_matrix: the same for one [N, K] matrix (K a multiple of 8),
+ *   e.g. an lm_head for lm_head_argmax_tiled.
+ */
+size_t df_dflash_tiled_bytes(const df_dflash_config *cfg);
+int df_dflash_tile_weights(const df_dflash_config *cfg, const df_dflash_weights *w, void *tiled,
+                           size_t tiled_bytes, df_stream_t stream);
+size_t df_tiled_matrix_bytes(int N, int K);
+int df_tile_matrix(const uint16_t *W, int N, int K, void *tiled, size_t tiled_bytes,
+                   df_stream_t stream);
 
 /* Per-layer KV cache, F32 (or BF16 with cfg->kv_bf16). Row p of sequence b, KV head h lives at
  * element ((b * n_kv + h) * cap + p) * head_dim of k[l]. seq_len[b] counts the valid rows. */
@@ -186,6 +221,12 @@ size_t df_lm_head_workspace_bytes(int rows, int H, int V);
  *   top2  device F32 [rows] out or NULL: the second largest (== top1 when the max is tied) */
 int lm_head_argmax(const uint16_t *W, const float *X, int rows, int H, int V, int32_t *idx,
                    float *top1, float *top2, void *ws, size_t ws_bytes, df_stream_t stream);
+
+/* lm_head_argmax reading the tiled copy of W (df_tile_matrix, V x H): same outputs, same
+ * workspace; W_tiled device, 1024-byte aligned. */
+int lm_head_argmax_tiled(const void *W_tiled, const float *X, int rows, int H, int V,
+                         int32_t *idx, float *top1, float *top2, void *ws, size_t ws_bytes,
+                         df_stream_t stream);
 
 /*
  * lm_head_argmax_noalloc — lm_head_argmax for callers that cannot allocate device memory:

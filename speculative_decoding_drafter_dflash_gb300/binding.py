@@ -44,7 +44,8 @@ class LayerWeights(ctypes.Structure):
 
 class DFlashWeights(ctypes.Structure):
     _fields_ = [("fc", c_void_p), ("hidden_norm", c_void_p), ("final_norm", c_void_p),
-                ("layers", POINTER(LayerWeights)), ("embed", c_void_p), ("lm_head", c_void_p)]
+                ("layers", POINTER(LayerWeights)), ("embed", c_void_p), ("lm_head", c_void_p),
+                ("tiled", c_void_p)]
 
 
 class SyntheticVerifier(ctypes.Structure):
@@ -91,6 +92,13 @@ _SIGS = [
                                c_void_p, c_void_p, c_size_t, c_void_p]),
     ("lm_head_argmax_noalloc", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                        c_void_p, c_void_p]),
+    ("lm_head_argmax_tiled", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_size_t, c_void_p]),
+    ("df_dflash_tiled_bytes", c_size_t, [POINTER(DFlashConfig)]),
+    ("df_dflash_tile_weights", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), c_void_p,
+                                       c_size_t, c_void_p]),
+    ("df_tiled_matrix_bytes", c_size_t, [c_int, c_int]),
+    ("df_tile_matrix", c_int, [c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     ("df_linear_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
     ("df_linear", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
                           c_void_p]),
@@ -228,7 +236,10 @@ class DFlashModel:
     """C structs for a DFlash drafter: config, weight pointers, KV cache. Keeps the tensors
     and ctypes arrays alive for the lifetime of the object."""
 
-    def __init__(self, shape, weights, cache, embed_scale: float = 1.0):
+    def __init__(self, shape, weights, cache, embed_scale: float = 1.0, tiled: bool = True):
+        """tiled: also lay the projection and lm_head weights out as tiles
+        (df_dflash_tile_weights) and let the kernels read those; False reads the row-major
+        matrices."""
         self.shape = shape
         self.cfg = DFlashConfig(shape.hidden, shape.n_layers, shape.n_q_heads, shape.n_kv_heads,
                                 shape.head_dim, shape.intermediate, shape.vocab,
@@ -243,8 +254,22 @@ class DFlashModel:
                 lw.wg, lw.wu, lw.wd)))
         self.weights = DFlashWeights(weights.fc.data_ptr(), weights.hidden_norm.data_ptr(),
                                      weights.final_norm.data_ptr(), self._layers,
-                                     weights.embed.data_ptr(), weights.lm_head.data_ptr())
+                                     weights.embed.data_ptr(), weights.lm_head.data_ptr(), None)
         self._w = weights
+        self._tiled = None
+        if tiled:
+            n = int(lib().df_dflash_tiled_bytes(ctypes.byref(self.cfg)))
+            if n == 0:   # an invalid config: the tiling call reports why, with its code
+                _check(lib().df_dflash_tile_weights(ctypes.byref(self.cfg),
+                                                    ctypes.byref(self.weights), None, 0,
+                                                    _stream(None)))
+                _check(DF_EINVAL)
+            buf, ptr = _aligned_buffer(n, weights.fc.device)
+            _check(lib().df_dflash_tile_weights(ctypes.byref(self.cfg), ctypes.byref(self.weights),
+                                                ptr, n, _stream(None)))
+            torch.cuda.synchronize(weights.fc.device)
+            self.weights.tiled = ptr
+            self._tiled = buf
         self.set_cache(cache)
 
     def set_cache(self, cache):
@@ -262,6 +287,41 @@ class DFlashModel:
 
     def workspace_bytes(self, B: int, block: int, n_new_max: int) -> int:
         return int(lib().df_dflash_workspace_bytes(ctypes.byref(self.cfg), B, block, n_new_max))
+
+
+def _aligned_buffer(nbytes: int, device, align: int = 1024):
+    """A device byte buffer and the first `align`-aligned address in it with nbytes behind it."""
+    buf = torch.empty(int(nbytes) + align, dtype=torch.uint8, device=device)
+    ptr = (buf.data_ptr() + align - 1) // align * align
+    return buf, ptr
+
+
+class TiledMatrix:
+    """The tiled copy of one BF16 [N, K] matrix (df_tile_matrix), e.g. an lm_head."""
+
+    def __init__(self, W, stream=None):
+        N, K = W.shape
+        n = int(lib().df_tiled_matrix_bytes(N, K))
+        self.buf, self.ptr = _aligned_buffer(n, W.device)
+        self.N, self.K, self.nbytes = N, K, n
+        _check(lib().df_tile_matrix(_dev(W, BF16, "W"), N, K, self.ptr, n, _stream(stream)))
+        # complete before any projection reads it (projections prefetch weights ahead of their
+        # predecessor kernels)
+        torch.cuda.synchronize(W.device)
+
+    def bytes_view(self) -> torch.Tensor:
+        off = self.ptr - self.buf.data_ptr()
+        return self.buf[off:off + self.nbytes]
+
+
+def lm_head_argmax_tiled(Wt: TiledMatrix, X, idx, top1=None, top2=None, ws=None, stream=None):
+    rows, H = X.shape
+    if H != Wt.K:
+        raise ValueError(f"X has {H} columns, the tiled matrix {Wt.K}")
+    _check(lib().lm_head_argmax_tiled(Wt.ptr, _dev(X, F32, "X"), rows, H, Wt.N,
+                                      _dev(idx, I32, "idx"), _dev(top1, F32, "top1"),
+                                      _dev(top2, F32, "top2"), _p(ws),
+                                      ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:

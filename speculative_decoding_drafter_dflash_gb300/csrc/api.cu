@@ -297,6 +297,91 @@ int get_ws(void *ws, size_t ws_bytes, size_t need) {
 }
 
 // The drafter forward. Either block_ids or (last_token, mask id) provides the block tokens.
+// ------------------------------------------------------------------ projection weights
+// The weight operand (matrices, segments, K split, SwiGLU pairing) of each DFlash projection,
+// shared by the forward and by the tiling of the weights; the forward adds activations,
+// epilogue and outputs. Without weights (sizing from the config alone) the matrices are stand-in
+// pointers that are never read.
+enum DfProj { DP_FC, DP_QKV, DP_O, DP_GATE_UP, DP_DOWN, DP_LM_HEAD };
+
+GemmArgs dflash_proj(const df_dflash_config *c, const df_dflash_weights *W, int layer, int which) {
+    static const uint16_t kStandIn[8] = {};
+    const uint16_t *z = kStandIn;
+    const int H = c->hidden, qt = c->n_q_heads * c->head_dim, kt = c->n_kv_heads * c->head_dim;
+    const df_layer_weights *L = (W && layer >= 0) ? &W->layers[layer] : nullptr;
+    GemmArgs g;
+    switch (which) {
+        case DP_FC:
+            g.W0 = W ? W->fc : z;
+            g.n0 = H;
+            g.N = H;
+            g.K = c->n_target_layers * H;
+            break;
+        case DP_QKV:
+            g.W0 = L ? L->wq : z;
+            g.n0 = qt;
+            g.W1 = L ? L->wk : z;
+            g.n1 = kt;
+            g.W2 = L ? L->wv : z;
+            g.n2 = kt;
+            g.N = qt + 2 * kt;
+            g.K = H;
+            break;
+        case DP_O:
+            g.W0 = L ? L->wo : z;
+            g.n0 = H;
+            g.N = H;
+            g.K = qt;
+            break;
+        case DP_GATE_UP:
+            g.W0 = L ? L->w_gate : z;
+            g.n0 = c->intermediate;
+            g.W1 = L ? L->w_up : z;
+            g.n1 = c->intermediate;
+            g.N = c->intermediate;
+            g.K = H;
+            g.epi = EPI_SWIGLU;
+            break;
+        case DP_DOWN:
+            g.W0 = L ? L->w_down : z;
+            g.n0 = H;
+            g.N = H;
+            g.K = c->intermediate;
+            break;
+        default:   // DP_LM_HEAD
+            g.W0 = W ? W->lm_head : z;
+            g.n0 = c->vocab;
+            g.N = c->vocab;
+            g.K = H;
+            break;
+    }
+    return g;
+}
+
+// Tiled layout of a DFlash model's weights: fc, then per layer QKV, O, gate/up, down, then the
+// lm_head, each projection's tiles starting on a 1024-byte boundary. Projection i of that order
+// (i = 0 fc, 1 + 4 l + j layer l's j-th, 1 + 4 n_layers the lm_head) starts at the returned
+// offset; i = 2 + 4 n_layers gives the total.
+size_t dflash_tiled_offset(const df_dflash_config *c, int i) {
+    size_t off = 0;
+    for (int k = 0; k < i; ++k) {
+        const int layer = k == 0 ? -1 : (k - 1) / 4;
+        const int which = k == 0 ? DP_FC : (k == 1 + 4 * c->n_layers ? DP_LM_HEAD : DP_QKV + (k - 1) % 4);
+        const size_t b = tiled_projection_bytes(dflash_proj(c, nullptr, k == 1 + 4 * c->n_layers ? -1 : layer, which));
+        off += (b + 1023) & ~size_t(1023);
+    }
+    return off;
+}
+
+// The tiled operand of projection `which` of `layer` when the weights carry a tiled copy.
+const uint8_t *dflash_tiled(const df_dflash_config *c, const df_dflash_weights *W, int layer,
+                            int which) {
+    if (!W || !W->tiled) return nullptr;
+    const int i = which == DP_FC ? 0 : which == DP_LM_HEAD ? 1 + 4 * c->n_layers
+                                                           : 1 + 4 * layer + (which - DP_QKV);
+    return static_cast<const uint8_t *>(W->tiled) + dflash_tiled_offset(c, i);
+}
+
 // fc, QKV, O and down projections leave split-K partial sums that the next kernel adds in
 // (hidden_norm pack, q/k-norm + RoPE, fused residual + RMSNorm pack); gate/up writes packed
 // SwiGLU activations directly. The input and post-attention RMSNorms are deferred: their row
@@ -344,11 +429,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         p.rows_per_seq = n_new_max;
         p.status = st;
         DF_TRY(launch_pack(p, s));
-        GemmArgs g;
-        g.W0 = W->fc;
-        g.n0 = H;
-        g.N = H;
-        g.K = fc_in;
+        GemmArgs g = dflash_proj(c, W, -1, DP_FC);
+        g.At = dflash_tiled(c, W, -1, DP_FC);
         g.X = ws.xp_ctx;
         g.ldx = fc_in;
         g.T = T_ctx;
@@ -414,15 +496,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
             g.rs_eps = c->rms_eps;
         };
 
-        GemmArgs g;
-        g.W0 = L.wq;
-        g.n0 = qt;
-        g.W1 = L.wk;
-        g.n1 = kt;
-        g.W2 = L.wv;
-        g.n2 = kt;
-        g.N = Nqkv;
-        g.K = H;
+        GemmArgs g = dflash_proj(c, W, l, DP_QKV);
+        g.At = dflash_tiled(c, W, l, DP_QKV);
         g.X = ws.xp_qkv;
         g.ldx = H;
         g.T = T_all;
@@ -484,11 +559,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         at.early_kv = 1;   // seq_len moves only at the end of the forward
         DF_TRY(launch_attn(at, s));
 
-        GemmArgs go;
-        go.W0 = L.wo;
-        go.n0 = H;
-        go.N = H;
-        go.K = qt;
+        GemmArgs go = dflash_proj(c, W, l, DP_O);
+        go.At = dflash_tiled(c, W, l, DP_O);
         go.X = ws.xp_o;
         go.ldx = qt;
         go.T = T_blk;
@@ -517,13 +589,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
             DF_TRY(launch_pack(pf, s));
         }
 
-        GemmArgs gu;
-        gu.W0 = L.w_gate;
-        gu.n0 = I;
-        gu.W1 = L.w_up;
-        gu.n1 = I;
-        gu.N = I;
-        gu.K = H;
+        GemmArgs gu = dflash_proj(c, W, l, DP_GATE_UP);
+        gu.At = dflash_tiled(c, W, l, DP_GATE_UP);
         gu.X = ws.xp_ffn;
         gu.ldx = H;
         gu.T = T_blk;
@@ -534,11 +601,8 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
         gu.name = "gemm_gate_up";
         row_scale(gu, ws.ss_post);
 
-        GemmArgs gd;
-        gd.W0 = L.w_down;
-        gd.n0 = H;
-        gd.N = H;
-        gd.K = I;
+        GemmArgs gd = dflash_proj(c, W, l, DP_DOWN);
+        gd.At = dflash_tiled(c, W, l, DP_DOWN);
         gd.X = ws.xp_act;
         gd.ldx = I;
         gd.T = T_blk;
@@ -582,9 +646,10 @@ int dflash_forward_impl(const df_dflash_config *c, const df_dflash_weights *W,
 // states per row it leaves in `part`.
 int lm_head_gemm(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
                  const TcScratch &tc, cudaStream_t s, const float *rs_ss, float rs_eps, int rs_n,
-                 int *G) {
+                 int *G, const uint8_t *At = nullptr) {
     GemmArgs g;
     g.W0 = Wlm;
+    g.At = At;
     g.n0 = V;
     g.N = V;
     g.K = H;
@@ -606,9 +671,11 @@ int lm_head_gemm(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V
 
 int lm_head_impl(const uint16_t *Wlm, const uint16_t *xp, int rows, int H, int V, ArgTop *part,
                  int32_t *idx, float *top1, float *top2, const TcScratch &tc, cudaStream_t s,
-                 const float *rs_ss = nullptr, float rs_eps = 0.f, int rs_n = 0) {
+                 const float *rs_ss = nullptr, float rs_eps = 0.f, int rs_n = 0,
+                 const uint8_t *At = nullptr) {
     GemmArgs g;
     g.W0 = Wlm;
+    g.At = At;
     g.n0 = V;
     g.N = V;
     g.K = H;
@@ -792,6 +859,88 @@ int df_profile_read(float *us, int max_entries, char *names, size_t names_bytes)
         ++k;
     }
     return k;
+}
+
+size_t df_dflash_tiled_bytes(const df_dflash_config *cfg) {
+    if (check_cfg(cfg) != DF_OK) return 0;
+    g_err[0] = 0;
+    return dflash_tiled_offset(cfg, 2 + 4 * cfg->n_layers);
+}
+
+int df_dflash_tile_weights(const df_dflash_config *cfg, const df_dflash_weights *w, void *tiled,
+                           size_t tiled_bytes, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_cfg(cfg));
+    DF_TRY(check_weights(cfg, w));
+    const size_t need = dflash_tiled_offset(cfg, 2 + 4 * cfg->n_layers);
+    REQ(tiled && tiled_bytes >= need, DF_EWORKSPACE, "tiled weights need %zu bytes, have %zu",
+        need, tiled_bytes);
+    REQ((reinterpret_cast<uintptr_t>(tiled) & 1023u) == 0, DF_EINVAL,
+        "tiled weights must be 1024-byte aligned");
+    uint8_t *base = static_cast<uint8_t *>(tiled);
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int i = 0; i < 2 + 4 * cfg->n_layers; ++i) {
+        const bool lm = i == 1 + 4 * cfg->n_layers;
+        const int layer = (i == 0 || lm) ? -1 : (i - 1) / 4;
+        const int which = i == 0 ? DP_FC : lm ? DP_LM_HEAD : DP_QKV + (i - 1) % 4;
+        const size_t off = dflash_tiled_offset(cfg, i), end = dflash_tiled_offset(cfg, i + 1);
+        DF_TRY(tile_projection(dflash_proj(cfg, w, layer, which), base + off, end - off, s));
+    }
+    return DF_OK;
+}
+
+size_t df_tiled_matrix_bytes(int N, int K) {
+    if (N <= 0 || K <= 0) return 0;
+    GemmArgs g;
+    g.W0 = reinterpret_cast<const uint16_t *>(&g);   // shape only
+    g.n0 = N;
+    g.N = N;
+    g.K = K;
+    return tiled_projection_bytes(g);
+}
+
+int df_tile_matrix(const uint16_t *W, int N, int K, void *tiled, size_t tiled_bytes,
+                   df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(N > 0 && K > 0 && K % 8 == 0, DF_ESHAPE, "N=%d K=%d (K a multiple of 8)", N, K);
+    DF_TRY(check_bf16(W, "W"));
+    GemmArgs g;
+    g.W0 = W;
+    g.n0 = N;
+    g.N = N;
+    g.K = K;
+    return tile_projection(g, static_cast<uint8_t *>(tiled), tiled_bytes, (cudaStream_t)stream);
+}
+
+int lm_head_argmax_tiled(const void *W_tiled, const float *X, int rows, int H, int V,
+                         int32_t *idx, float *top1, float *top2, void *ws, size_t ws_bytes,
+                         df_stream_t stream) {
+    g_err[0] = 0;
+    REQ(rows > 0 && rows <= kMaxTcTokens && H > 0 && H % 8 == 0 && V > 0, DF_ESHAPE,
+        "rows=%d (1..%d) H=%d V=%d (H %% 8 == 0)", rows, kMaxTcTokens, H, V);
+    REQ(W_tiled && (reinterpret_cast<uintptr_t>(W_tiled) & 1023u) == 0, DF_EINVAL,
+        "W_tiled is NULL or not 1024-byte aligned");
+    DF_TRY(check_f32(X, "X"));
+    REQ(idx, DF_EINVAL, "idx is NULL");
+    DF_TRY(get_ws(ws, ws_bytes, df_lm_head_workspace_bytes(rows, H, V)));
+    Carve cv{static_cast<char *>(ws), 0, ws_bytes, true};
+    const int ctas = sm_count();
+    uint16_t *xp = cv.take<uint16_t>((size_t)2 * rows * H);
+    ArgTop *part = cv.take<ArgTop>((size_t)ctas * rows);
+    TcScratch tc;
+    carve_tc(cv, tc, rows, V, ctas);
+    cudaStream_t s = (cudaStream_t)stream;
+    PackArgs p;
+    p.src = X;
+    p.lds = H;
+    p.pack = xp;
+    p.ldp = H;
+    p.T = rows;
+    p.K = H;
+    DF_TRY(launch_pack(p, s));
+    // the row-major pointer only describes the shape when the tiled copy is given
+    return lm_head_impl(static_cast<const uint16_t *>(W_tiled), xp, rows, H, V, part, idx, top1,
+                        top2, tc, s, nullptr, 0.f, 0, static_cast<const uint8_t *>(W_tiled));
 }
 
 size_t df_dflash_workspace_bytes(const df_dflash_config *cfg, int B, int block, int n_new_max) {
@@ -1135,7 +1284,7 @@ int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
     if (blk > 32) {
         DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
                             argmax_out, nullptr, nullptr, W.tc, s, W.ss_post, cfg->rms_eps,
-                            W.ss_slots));
+                            W.ss_slots, dflash_tiled(cfg, w, -1, DP_LM_HEAD)));
         return launch_accept(argmax_out + 1, blk, target_argmax, B, K, eos, n_eos, committed,
                              n_committed, accept_count, hit_eos, rollback, target_seq_len,
                              d_status, s);
@@ -1143,7 +1292,8 @@ int df_draft_round(const df_dflash_config *cfg, const df_dflash_weights *w,
     // the lm_head's argmax partials, then the argmax merge and the accept walk in one launch
     int G = 0;
     DF_TRY(lm_head_gemm(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
-                        W.tc, s, W.ss_post, cfg->rms_eps, W.ss_slots, &G));
+                        W.tc, s, W.ss_post, cfg->rms_eps, W.ss_slots, &G,
+                        dflash_tiled(cfg, w, -1, DP_LM_HEAD)));
     return launch_argmax_accept(W.amax_part, G, B, blk, argmax_out, target_argmax, eos, n_eos,
                                 committed, n_committed, accept_count, hit_eos, rollback,
                                 target_seq_len, d_status, s);
@@ -1204,11 +1354,8 @@ int df_draft_round_stochastic(const df_dflash_config *cfg, const df_dflash_weigh
     DF_TRY(dflash_forward_impl(cfg, w, cache, nullptr, last_token, target_hidden_new, n_new,
                                n_new_max, B, blk, W.h_final, W.xp_head, W, d_status, s));
     // logits of every block row (final norm deferred to the row scale, as in the greedy round)
-    GemmArgs gl;
-    gl.W0 = w->lm_head;
-    gl.n0 = V;
-    gl.N = V;
-    gl.K = H;
+    GemmArgs gl = dflash_proj(cfg, w, -1, DP_LM_HEAD);
+    gl.At = dflash_tiled(cfg, w, -1, DP_LM_HEAD);
     gl.X = W.xp_head;
     gl.ldx = H;
     gl.T = B * blk;
@@ -1597,7 +1744,7 @@ int df_generate(const df_dflash_config *cfg, const df_dflash_weights *w, const d
         if (rc == DF_OK)
             rc = lm_head_impl(w->lm_head, W.xp_head, B * blk, cfg->hidden, cfg->vocab, W.amax_part,
                               a.argmax, nullptr, nullptr, W.tc, cs, W.ss_post, cfg->rms_eps,
-                              W.ss_slots);
+                              W.ss_slots, dflash_tiled(cfg, w, -1, DP_LM_HEAD));
         if (rc == DF_OK) rc = launch_loop_verify(a, cs);
         if (rc == DF_OK)
             rc = launch_accept(a.argmax + 1, blk, a.target, B, K, eos, n_eos, a.committed,

@@ -123,7 +123,7 @@ enum TraceKid : uint32_t {
     TK_LOOP_INIT, TK_LOOP_PREPARE, TK_LOOP_VERIFY, TK_LOOP_APPEND, TK_LOOP_COMMIT, TK_MOE_ROUTER,
     TK_MOE_GATE_UP, TK_MOE_DOWN, TK_PACK, TK_PACK_VEC, TK_ARGMAX_FINAL, TK_ACCEPT, TK_ROLLBACK,
     TK_WORD_COPY, TK_SAMPLE_STATS, TK_SAMPLE_WALK, TK_SAMPLE_NORM, TK_SAMPLE_DRAW,
-    TK_SAMPLE_FUSED,
+    TK_SAMPLE_FUSED, TK_TILE,
     TK_GEMM = 100   // + 2 * epilogue + (stream-K fix-up ? 1 : 0)
 };
 struct TraceRec {
@@ -355,6 +355,9 @@ struct GemmArgs {
     // Optional split along K for segment 0: columns [K1, K) read from Wk2 [n0, K-K1].
     const uint16_t *Wk2 = nullptr;
     int K1 = 0;
+    // Optional tiled copy of the same weights (tile_projection): when set the kernel reads its
+    // A operands from it, two K blocks per bulk copy; W0.. still define the shape.
+    const uint8_t *At = nullptr;
     int N = 0, K = 0;
     const uint16_t *X = nullptr;     // packed activations [2T, ldx]
     int ldx = 0, T = 0;
@@ -412,6 +415,12 @@ constexpr size_t lm_head_scratch_bytes_for(int rows, int H, int V, int ctas) {
     return carve_round((size_t)2 * rows * H * 2) + carve_round((size_t)ctas * rows * sizeof(ArgTop)) +
            carve_round(tc_partial_floats(rows, ctas) * 4) + carve_round((size_t)n_counters_for(V) * 4);
 }
+// Tiled weight layout of a projection (the A operands of GemmArgs a: its segments, K split and
+// SwiGLU pairing): 128-row x 64-column BF16 tiles, tile (m, kb) at byte (m * kbt + kb) * 16384,
+// each stored exactly as the 128-byte-swizzled shared-memory image the MMA reads (row r at
+// r * 128, its 16-byte piece j at ((j ^ (r % 8)) * 16)), rows and columns past the matrix zero.
+size_t tiled_projection_bytes(const GemmArgs &a);
+int tile_projection(const GemmArgs &a, uint8_t *out, size_t out_bytes, cudaStream_t s);
 int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s,
                    int *n_partials_out = nullptr);
 

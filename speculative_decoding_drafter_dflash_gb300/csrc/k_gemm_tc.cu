@@ -4,7 +4,9 @@
 // activations to ~16 mantissa bits and the two columns of a token are summed in F32 in the
 // epilogue.
 //
-//   A (weights, M = 128 rows x K)   TMA, 128-byte swizzle, K-major, 64-wide K blocks
+//   A (weights, M = 128 rows x K)   TMA, 128-byte swizzle, K-major, 64-wide K blocks; or, from
+//                                   a tiled copy of the weights (tile_projection), one bulk
+//                                   copy of two K blocks (32 KB) per pipeline stage
 //   B (packed x, N = 2T rows x K)   TMA, same layout; rows past 2T are zero-filled by TMA
 //   D (F32, 128 lanes x N columns)  TMEM, two accumulators so the epilogue of one tile
 //                                   overlaps the MMAs of the next
@@ -43,10 +45,19 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;                    // BF16 elements per K block: one 128-byte row
 constexpr int kABytes = kBM * kBK * 2;     // 16 KB
 constexpr int kTokChunk = 8;               // tokens per TMEM load (16 columns)
+// K blocks per pipeline stage when the weights are tiled: up to 4 (one 64 KB weight copy and one
+// activation copy per stage), as many as leave two stages in the shared-memory budget. This
+// part's TMA unit moves roughly one copy per ~0.4 us per SM whatever its size up to 64 KB, so a
+// 16 KB weight tile per copy caps a CTA near 40 GB/s, below its share of HBM; 32-64 KB copies
+// stream at the HBM rate.
+constexpr int kTiledKpgMax = 4;
+constexpr int kStageBudget = 200 * 1024;
 
 struct TcParams {
     CUtensorMap amap[4];
     CUtensorMap bmap[2];
+    CUtensorMap bmap3;       // tiled weights, K a multiple of 64: kpg K blocks' activations
+    int b3;                  // 1: bmap3 is used (else one 2-D activation copy per K block)
     int n_seg;
     int seg_rows[4];
     int seg_tile0[5];
@@ -80,6 +91,8 @@ struct TcParams {
     float rs_inv_k, rs_eps;
     long long wait_cycles;   // limit of every barrier wait (kTimeoutCycles unless a test sets it)
     int withhold_first;      // test hook: the producer never loads its first stage
+    const uint8_t *At;       // tiled weights (tile (m, kb) at (m * kbt + kb) * 16 KB) or null
+    int kpg;                 // K blocks per pipeline stage (1 unless At is set)
 };
 
 
@@ -313,15 +326,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 while (c.valid && c.kb >= c.k1) c.valid = c.w.next(p, c.m, c.kb, c.k1, c.split);
                 if (c.valid) seg_setup(c);
             };
+            // K blocks of the stage at the cursor: up to kpg, within the current segment
+            auto group = [&](const Cursor &c) { return min(p.kpg, c.k1 - c.kb); };
             auto advance = [&](Cursor &c) {
-                if (++c.kb < c.k1) return;
+                c.kb += group(c);
+                if (c.kb < c.k1) return;
                 do {
                     c.valid = c.w.next(p, c.m, c.kb, c.k1, c.split);
                 } while (c.valid && c.kb >= c.k1);
                 if (c.valid) seg_setup(c);
             };
+            // Stage layout: the group's A tiles (16 KB each), then its B slices (NC rows each).
+            auto stage_tx = [&](const Cursor &c) {
+                // the 3-D activation box always holds kpg K blocks (past K they are zero)
+                return (uint32_t)group(c) * kABytes +
+                       (uint32_t)(p.b3 ? p.kpg : group(c)) * (uint32_t)(p.NC * 128);
+            };
             auto load_a = [&](const Cursor &c, int stage) {
                 uint8_t *a = stage_base + (size_t)stage * p.stage_bytes;
+                if (p.At) {
+                    const uint8_t *src = p.At + ((size_t)c.m * p.kbt + c.kb) * kABytes;
+                    bulk_load(a, src, (uint32_t)group(c) * kABytes, &full[stage], pol_w);
+                    return;
+                }
                 const int ks = (p.k_seg == 2 && c.kb >= p.kb_seg0) ? 1 : 0;
                 const int kx = (ks ? c.kb - p.kb_seg0 : c.kb) * kBK;
                 if (p.pair) {
@@ -332,10 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             };
             auto load_b = [&](const Cursor &c, int stage) {
-                uint8_t *b = stage_base + (size_t)stage * p.stage_bytes + kABytes;
-                const int ks = (p.k_seg == 2 && c.kb >= p.kb_seg0) ? 1 : 0;
-                const int kx = (ks ? c.kb - p.kb_seg0 : c.kb) * kBK;
-                tma_load_2d(b, &p.bmap[ks], &full[stage], kx, 0, pol_x);
+                uint8_t *b = stage_base + (size_t)stage * p.stage_bytes + (size_t)p.kpg * kABytes;
+                if (p.b3) {
+                    tma_load_3d(b, &p.bmap3, &full[stage], 0, 0, c.kb, pol_x);
+                    return;
+                }
+                const int n = group(c);
+                for (int j = 0; j < n; ++j) {
+                    const int kb = c.kb + j;
+                    const int ks = (p.k_seg == 2 && kb >= p.kb_seg0) ? 1 : 0;
+                    const int kx = (ks ? kb - p.kb_seg0 : kb) * kBK;
+                    tma_load_2d(b + (size_t)j * p.NC * 128, &p.bmap[ks], &full[stage], kx, 0, pol_x);
+                }
             };
             // Weights do not depend on earlier kernels: the first stages' weight tiles are
             // requested before waiting for the predecessor grid, activation tiles after.
@@ -344,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int pre = 0;
             while (cur.valid && pre < p.stages) {
                 if (!(p.withhold_first && pre == 0)) {
-                    mbar_expect_tx(&full[pre], p.stage_bytes);
+                    mbar_expect_tx(&full[pre], stage_tx(cur));
                     load_a(cur, pre);
                 }
                 advance(cur);
@@ -369,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&full[stage], p.stage_bytes);
+                mbar_expect_tx(&full[stage], stage_tx(cur));
                 load_a(cur, stage);
                 load_b(cur, stage);
                 advance(cur);
@@ -405,21 +440,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * p.acc_cols);
-                for (int kb = k0; kb < k1; ++kb) {
+                for (int kb = k0; kb < k1;) {
+                    const int n = min(p.kpg, k1 - kb);
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(stage_base + (size_t)stage * p.stage_bytes);
-                    const uint64_t adesc = sw128_desc(a_addr);
-                    const uint64_t bdesc = sw128_desc(a_addr + kABytes);
+                    const uint32_t b_addr = a_addr + (uint32_t)(p.kpg * kABytes);
+                    for (int j = 0; j < n; ++j) {
+                        const uint64_t adesc = sw128_desc(a_addr + (uint32_t)(j * kABytes));
+                        const uint64_t bdesc = sw128_desc(b_addr + (uint32_t)(j * p.NC * 128));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // advance 16 BF16 (32 bytes) along K inside the swizzled 128-byte row
-                        mma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), p.idesc,
-                                 (kb > k0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // advance 16 BF16 (32 bytes) along K inside the swizzled 128-byte row
+                            mma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), p.idesc,
+                                     (kb > k0 || j > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
+                    kb += n;
                     mma_commit(&empty[stage]);
                     if (++stage == p.stages) {
                         stage = 0;
@@ -593,20 +633,27 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
     const int K1 = a.K - K0;
     p.kb_seg0 = ceil_div(K0, kBK);
     p.kbt = p.kb_seg0 + (a.Wk2 ? ceil_div(K1, kBK) : 0);
+    // With tiled weights the A operands come by bulk copies: the row-major pointers only
+    // describe the segments and no A tensor map is made.
+    const bool maps = a.At == nullptr;
     if (p.pair) {
         p.n_seg = 1;
         p.seg_rows[0] = a.N;
         p.n_tiles = ceil_div(a.N, 64);
-        DF_TRY(make_map(&p.amap[0], a.W0, a.K, a.N, a.K, kBK, 64));
-        DF_TRY(make_map(&p.amap[1], a.W1, a.K, a.N, a.K, kBK, 64));
+        if (maps) {
+            DF_TRY(make_map(&p.amap[0], a.W0, a.K, a.N, a.K, kBK, 64));
+            DF_TRY(make_map(&p.amap[1], a.W1, a.K, a.N, a.K, kBK, 64));
+        }
     } else if (a.Wk2) {
         p.n_seg = 1;
         p.seg_rows[0] = a.n0;
         p.seg_tile0[0] = 0;
         p.seg_col0[0] = 0;
         p.n_tiles = ceil_div(a.n0, kBM);
-        DF_TRY(make_map(&p.amap[0], a.W0, K0, a.n0, K0, kBK, kBM));
-        DF_TRY(make_map(&p.amap[1], a.Wk2, K1, a.n0, K1, kBK, kBM));
+        if (maps) {
+            DF_TRY(make_map(&p.amap[0], a.W0, K0, a.n0, K0, kBK, kBM));
+            DF_TRY(make_map(&p.amap[1], a.Wk2, K1, a.n0, K1, kBK, kBM));
+        }
     } else {
         const uint16_t *W[4] = {a.W0, a.W1, a.W2, a.W3};
         const int rows[4] = {a.n0, a.n1, a.n2, a.n3};
@@ -616,7 +663,7 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
             p.seg_rows[ns] = rows[i];
             p.seg_tile0[ns] = tiles;
             p.seg_col0[ns] = col;
-            DF_TRY(make_map(&p.amap[ns], W[i], a.K, rows[i], a.K, kBK, kBM));
+            if (maps) DF_TRY(make_map(&p.amap[ns], W[i], a.K, rows[i], a.K, kBK, kBM));
             tiles += ceil_div(rows[i], kBM);
             col += rows[i];
             ++ns;
@@ -644,8 +691,29 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
     } else {
         p.G = (int)std::min<long long>(sc.max_ctas, p.total_kb);
     }
-    p.stage_bytes = kABytes + NC * 128;
-    p.stages = std::min(8, (int)((200 * 1024) / p.stage_bytes));
+    p.At = a.At;
+    p.kpg = 1;
+    if (a.At) {
+        if (a.Wk2) return fail(DF_ESHAPE, "tiled weights of a projection split along K");
+        if ((reinterpret_cast<uintptr_t>(a.At) & 1023u) != 0)
+            return fail(DF_EINVAL, "tiled weights must be 1024-byte aligned (%p)", (const void *)a.At);
+        const int per_kb = kABytes + NC * 128;
+        p.kpg = kTiledKpgMax;
+        while (p.kpg > 1 && kStageBudget / (p.kpg * per_kb) < 2) --p.kpg;
+        // the activations of kpg consecutive K blocks: dims (64 columns, 2T rows, K blocks) with
+        // the K-block step of 128 bytes, so one box lands as kpg swizzled NC-row slices. Only
+        // when K is whole K blocks: this view has no column bound inside a row, so a ragged last
+        // block would read past the row (there one copy per K block keeps the 2-D map's bound).
+        p.b3 = K0 % kBK == 0 ? 1 : 0;
+        if (p.b3)
+            DF_TRY(make_tma_3d(&p.bmap3, a.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kBK, 2 * T,
+                               (uint64_t)(K0 / kBK), (uint64_t)a.ldx * 2, kBK * 2, kBK, NC,
+                               p.kpg));
+    }
+    p.stage_bytes = (uint32_t)p.kpg * (kABytes + NC * 128);
+    p.stages = std::min(a.At ? 5 : 8, (int)(kStageBudget / p.stage_bytes));
+    if (p.stages < 2)
+        return fail(DF_ESHAPE, "GEMM stage of %u bytes leaves fewer than two stages", p.stage_bytes);
     p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NC >> 3) << 17) |
               ((uint32_t)(kBM >> 4) << 24);
     p.epi = a.epi;
@@ -682,6 +750,93 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
     return DF_OK;
 }
 
+// ------------------------------------------------------------------ tiled weights
+struct TileArgs {
+    const uint16_t *W[4];
+    int rows[4];
+    int tile0[5];
+    int n_seg;
+    int K0, kbt, pair, N, n_tiles;
+    uint8_t *out;
+};
+
+// The A-operand tiles of a projection, with the segment and pairing rules of build_params
+// (a projection split along K, whose two column ranges come from two matrices, is not tiled).
+int tile_plan(const GemmArgs &a, TileArgs &t) {
+    memset(&t, 0, sizeof(t));
+    if (a.N <= 0 || a.K <= 0) return fail(DF_ESHAPE, "tiled weights of an empty projection");
+    if (a.Wk2) return fail(DF_ESHAPE, "tiled weights of a projection split along K");
+    t.pair = a.epi == EPI_SWIGLU;
+    t.N = a.N;
+    t.K0 = a.K;
+    t.kbt = ceil_div(a.K, kBK);
+    if (t.pair) {
+        t.n_seg = 2;
+        t.W[0] = a.W0;
+        t.W[1] = a.W1;
+        t.rows[0] = t.rows[1] = a.N;
+        t.n_tiles = ceil_div(a.N, 64);
+    } else {
+        const uint16_t *W[4] = {a.W0, a.W1, a.W2, a.W3};
+        const int rows[4] = {a.n0, a.n1, a.n2, a.n3};
+        for (int i = 0; i < 4; ++i) {
+            if (rows[i] <= 0 || W[i] == nullptr) continue;
+            t.W[t.n_seg] = W[i];
+            t.rows[t.n_seg] = rows[i];
+            t.tile0[t.n_seg] = t.n_tiles;
+            t.n_tiles += ceil_div(rows[i], kBM);
+            ++t.n_seg;
+        }
+    }
+    t.tile0[t.n_seg] = t.n_tiles;
+    if (t.n_tiles <= 0) return fail(DF_ESHAPE, "tiled weights of an empty projection");
+    return DF_OK;
+}
+
+// One thread per 16-byte piece of the tiled copy: piece j of row r of tile (m, kb) holds
+// columns kb*64 + 8j .. +7 of the row's source and lands at (j ^ (r % 8)) * 16 in the row.
+__global__ void __launch_bounds__(256) tile_weights_kernel(TileArgs t) {
+    DF_TRACE_KERNEL(TK_TILE);
+    pdl_trigger();
+    pdl_wait();
+    const long long total = (long long)t.n_tiles * t.kbt * 1024;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long blk = i >> 10;
+        const int r = (int)((i >> 3) & 127), j = (int)(i & 7);
+        const int m = (int)(blk / t.kbt), kb = (int)(blk - (long long)m * t.kbt);
+        const uint16_t *W = nullptr;
+        long long row = 0;
+        if (t.pair) {
+            row = (long long)m * 64 + (r & 63);
+            if (row < t.N) W = r < 64 ? t.W[0] : t.W[1];
+        } else {
+            int s = 0;
+            while (s + 1 < t.n_seg && m >= t.tile0[s + 1]) ++s;
+            row = (long long)(m - t.tile0[s]) * kBM + r;
+            if (row < t.rows[s]) W = t.W[s];
+        }
+        const int col = kb * kBK + 8 * j, cols = t.K0;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (W && col < cols) {
+            const uint16_t *src = W + row * cols + col;
+            if (col + 8 <= cols && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+                v = *reinterpret_cast<const uint4 *>(src);
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t lo = col + 2 * q < cols ? src[2 * q] : 0u;
+                    const uint32_t hi = col + 2 * q + 1 < cols ? src[2 * q + 1] : 0u;
+                    w[q] = lo | (hi << 16);
+                }
+                v = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        *reinterpret_cast<uint4 *>(t.out + blk * kABytes + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+    }
+}
+
 int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_out) {
     TcParams p;
     size_t smem = 0;
@@ -708,6 +863,29 @@ int launch_chunk(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *G_
 }
 
 }  // namespace
+
+size_t tiled_projection_bytes(const GemmArgs &a) {
+    TileArgs t;
+    if (tile_plan(a, t) != DF_OK) return 0;
+    return (size_t)t.n_tiles * t.kbt * kABytes;
+}
+
+int tile_projection(const GemmArgs &a, uint8_t *out, size_t out_bytes, cudaStream_t s) {
+    TileArgs t;
+    DF_TRY(tile_plan(a, t));
+    const size_t need = (size_t)t.n_tiles * t.kbt * kABytes;
+    if (out == nullptr || out_bytes < need)
+        return fail(DF_EWORKSPACE, "tiled weights need %zu bytes, have %zu", need, out_bytes);
+    if ((reinterpret_cast<uintptr_t>(out) & 1023u) != 0)
+        return fail(DF_EINVAL, "tiled weights must be 1024-byte aligned (%p)", (void *)out);
+    for (int i = 0; i < t.n_seg; ++i)
+        if (t.W[i] == nullptr) return fail(DF_EINVAL, "tiled weights: NULL weight segment");
+    t.out = out;
+    const long long total = (long long)t.n_tiles * t.kbt * 1024;
+    const long long grid = std::min<long long>((total + 255) / 256, 16LL * sm_count());
+    return launch_k("tile_weights_kernel", tile_weights_kernel, dim3((unsigned)grid), dim3(256), 0, s,
+                    t);
+}
 
 int launch_gemm_tc(const GemmArgs &a, const TcScratch &sc, cudaStream_t s, int *n_partials_out) {
     if (a.N <= 0 || a.T <= 0) {
@@ -762,6 +940,25 @@ extern "C" int df_test_wait_hook(long long wait_cycles, int withhold_first) {
 }
 
 namespace df {
+
+int make_tma_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem_bytes,
+                uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1, uint64_t stride2,
+                uint32_t b0, uint32_t b1, uint32_t b2) {
+    DF_TRY(get_encode());
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || stride1 % 16 != 0 || stride2 % 16 != 0 ||
+        b0 * elem_bytes > 128)
+        return fail(DF_EINVAL, "3-D TMA operand misaligned (base %p, strides %llu / %llu)", base,
+                    (unsigned long long)stride1, (unsigned long long)stride2);
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1, stride2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DF_ECUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+    return DF_OK;
+}
 
 int make_tma_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem_bytes,
                 uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols, uint32_t box_rows,
