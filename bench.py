@@ -45,10 +45,12 @@ def parse():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--batch", type=int, default=1, help="sequences of --profile-case round")
     ap.add_argument("--ctx", type=int, default=0, help="cache rows of --profile-case round")
+    ap.add_argument("--vocab", type=int, default=0, help="lm_head rows of --profile-case lm_head")
     ap.add_argument("--trace-dump", default=None, help="--profile-case trace: save the records")
 
     ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "sweep_bf16kv", "mtp",
-                                                     "moe", "attn", "stochastic", "sampled", "generate", "trace"],
+                                                     "moe", "attn", "stochastic", "sampled", "generate", "trace",
+                                                     "layout"],
                     default=None,
                     help="run a few launches of one case for an ncu capture and exit")
     return ap.parse_args()
@@ -1025,6 +1027,92 @@ TRACE_NAMES = {1: "rope_table", 2: "qk_rope", 3: "attn", 4: "attn_combine", 5: "
                19: "rollback", 20: "word_copy"}
 
 
+def layout_case(args):
+    """Row-major against tiled weights on the same GPU: the lm_head + argmax alone (20 launches
+    after 3 warm-up, CUDA events) and the whole draft round as a CUDA graph (30 replays), both
+    layouts alternated three times; --batch / --ctx set the round's workload."""
+    import torch
+
+    from speculative_decoding_drafter_dflash_gb300 import binding as B
+    from speculative_decoding_drafter_dflash_gb300 import synth
+    from speculative_decoding_drafter_dflash_gb300.workloads import DFLASH_K15
+    dev = torch.device("cuda", 0)
+    s = DFLASH_K15.with_(batch=args.batch, ctx=args.ctx or DFLASH_K15.ctx)
+    w = synth.dflash_weights(s, seed=0, device=dev)
+    res = {}
+    rows = s.block
+    X = torch.randn((rows, s.hidden), device=dev)
+    idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    ws = B.alloc_workspace(B.lm_head_workspace_bytes(rows, s.hidden, s.vocab), dev)
+    Wt = B.TiledMatrix(w.lm_head)
+
+    def lm(tiled):
+        if tiled:
+            B.lm_head_argmax_tiled(Wt, X, idx, ws=ws)
+        else:
+            B.lm_head_argmax(w.lm_head, X, idx, ws=ws)
+
+    for _ in range(3):
+        for tiled in (False, True):
+            for _ in range(3):
+                lm(tiled)
+            ev = []
+            for _ in range(20):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                lm(tiled)
+                b.record()
+                ev.append((a, b))
+            torch.cuda.synchronize()
+            key = "lm_head_tiled_us" if tiled else "lm_head_rowmajor_us"
+            res.setdefault(key, []).append(
+                round(statistics.mean(x.elapsed_time(y) for x, y in ev) * 1e3, 2))
+    del Wt
+    inp = synth.dflash_round_inputs(s, [s.block] * s.batch, seed=10, device=dev)
+    inp.n_new = torch.tensor([3] * s.batch, dtype=torch.int32, device=dev)
+    eos = torch.tensor(s.eos_ids, dtype=torch.int32, device=dev)
+    tsl = torch.full((s.batch,), 1 << 30, dtype=torch.int32, device=dev)
+    tgt = torch.zeros((s.batch, s.block), dtype=torch.int32, device=dev)
+    graphs, keep = {}, []
+    for tiled in (False, True):
+        cache = synth.dflash_cache(s, seed=1, device=dev)
+        model = B.DFlashModel(s, w, cache, tiled=tiled)
+        wsr = B.alloc_workspace(model.workspace_bytes(s.batch, s.block, s.block), dev)
+        out = B.RoundOutputs(s.batch, s.K, dev)
+        st = torch.cuda.Stream(dev)
+
+        def step(model=model, wsr=wsr, out=out, cache=cache, st=st):
+            B.df_draft_round(model, inp.last_token, inp.target_hidden, inp.n_new, s.block, s.K,
+                             tgt, eos, tsl, out, wsr, stream=st)
+            B.kv_rollback(cache.seq_len, inp.n_new, stream=st)
+
+        with torch.cuda.stream(st):
+            step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            step()
+        graphs[tiled] = (g, st)
+        keep.append((model, wsr, out, cache))
+    for _ in range(3):
+        for tiled in (False, True):
+            g, st = graphs[tiled]
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(st):
+                a.record(st)
+                for _ in range(30):
+                    g.replay()
+                b.record(st)
+            torch.cuda.synchronize()
+            key = "round_tiled_us" if tiled else "round_rowmajor_us"
+            res.setdefault(key, []).append(round(a.elapsed_time(b) * 1e3 / 30, 1))
+    print(json.dumps({"profile_case": "layout", "workload": s.name, "batch": s.batch,
+                      "ctx": s.ctx, **res}))
+
+
 def trace_case(args):
     """In-graph timeline of the draft round from the trace build (per-CTA global-timer spans of
     every kernel): CUDA-graph rounds of the workload, each launch's first start, last end and the
@@ -1184,11 +1272,14 @@ def profile_case(args):
         return generate_case(args.steps)
     if args.profile_case == "sampled":
         return sampled_case(args.steps)
+    if args.profile_case == "layout":
+        return layout_case(args)
     if args.profile_case == "lm_head":
-        W = (torch.randn((s.vocab, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
+        V = args.vocab or s.vocab
+        W = (torch.randn((V, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
         X = torch.randn((s.block, s.hidden), generator=g, device=dev)
         idx = torch.empty(s.block, dtype=torch.int32, device=dev)
-        ws = B.alloc_workspace(B.lm_head_workspace_bytes(s.block, s.hidden, s.vocab), dev)
+        ws = B.alloc_workspace(B.lm_head_workspace_bytes(s.block, s.hidden, V), dev)
         Wt = B.TiledMatrix(W)          # the round reads the lm_head from its tiled copy
         for _ in range(5):
             B.lm_head_argmax_tiled(Wt, X, idx, ws=ws)
