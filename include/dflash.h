@@ -546,7 +546,18 @@ typedef struct {
     const uint16_t *sh_gate_mlp, *sh_up;    /* [Is, H] */
     const uint16_t *sh_down;                /* [H, Is] */
     const uint16_t *sh_expert_gate;         /* [1, H]: sigmoid gate of the shared expert */
+    const void *tiled;                      /* NULL, or the tiled copy by df_mtp_tile_weights */
 } df_mtp_weights;
+
+/* Tiled weights of an MTP block (the layout of the DFlash tiled weights above): eh_proj (its two
+ * halves as one K range), QKV with the output gate rows, O, the dense gate/up (paired) and down
+ * when there are no experts, and the lm_head. The experts and the router stay row-major.
+ * df_mtp_tiled_bytes: 0 on an invalid config or weights. df_mtp_tile_weights: fills `tiled`
+ * (device, 1024-byte aligned, >= df_mtp_tiled_bytes) on `stream`; set w->tiled = tiled and
+ * synchronise before the first call that reads it. DF_EWORKSPACE / DF_EINVAL as above. */
+size_t df_mtp_tiled_bytes(const df_mtp_config *cfg, const df_mtp_weights *w);
+int df_mtp_tile_weights(const df_mtp_config *cfg, const df_mtp_weights *w, void *tiled,
+                        size_t tiled_bytes, df_stream_t stream);
 
 size_t df_mtp_workspace_bytes(const df_mtp_config *cfg, int B);
 

@@ -71,7 +71,7 @@ class MtpWeights(ctypes.Structure):
         "enorm", "hnorm", "eh_embed", "eh_hidden", "attn_norm", "post_attn_norm", "q_norm",
         "k_norm", "wq", "wk", "wv", "w_gate", "wo", "shared_head_norm", "embed", "lm_head",
         "w_gate_mlp", "w_up", "w_down", "router", "exp_gate", "exp_up", "exp_down",
-        "sh_gate_mlp", "sh_up", "sh_down", "sh_expert_gate")]
+        "sh_gate_mlp", "sh_up", "sh_down", "sh_expert_gate", "tiled")]
 
 
 _lib = None
@@ -98,6 +98,9 @@ _SIGS = [
     ("df_dflash_tile_weights", c_int, [POINTER(DFlashConfig), POINTER(DFlashWeights), c_void_p,
                                        c_size_t, c_void_p]),
     ("df_tiled_matrix_bytes", c_size_t, [c_int, c_int]),
+    ("df_mtp_tiled_bytes", c_size_t, [POINTER(MtpConfig), POINTER(MtpWeights)]),
+    ("df_mtp_tile_weights", c_int, [POINTER(MtpConfig), POINTER(MtpWeights), c_void_p, c_size_t,
+                                    c_void_p]),
     ("df_tile_matrix", c_int, [c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     ("df_linear_workspace_bytes", c_size_t, [c_int, c_int, c_int]),
     ("df_linear", c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
@@ -454,7 +457,9 @@ def df_draft_round_host(model: DFlashModel, last_token, target_hidden_new, n_new
 class MtpModel:
     """C structs of an MTP block: config + weight pointers + the one-layer KV slot."""
 
-    def __init__(self, shape, w, cache):
+    def __init__(self, shape, w, cache, tiled: bool = True):
+        """tiled: also lay the projection and lm_head weights out as tiles
+        (df_mtp_tile_weights) and let the kernels read those."""
         self.shape = shape
         self.cfg = MtpConfig(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                              shape.vocab, shape.intermediate, shape.n_experts, shape.top_k,
@@ -465,8 +470,22 @@ class MtpModel:
             "enorm", "hnorm", "eh_embed", "eh_hidden", "attn_norm", "post_norm", "q_norm",
             "k_norm", "wq", "wk", "wv", "w_gate", "wo", "shared_head_norm", "embed", "lm_head",
             "wg", "wu", "wd", "router", "exp_g", "exp_u", "exp_d", "sh_g", "sh_u", "sh_d",
-            "sh_gate")])
+            "sh_gate")], None)
         self._w = w
+        self._tiled = None
+        if tiled:
+            n = int(lib().df_mtp_tiled_bytes(ctypes.byref(self.cfg), ctypes.byref(self.weights)))
+            if n == 0:   # invalid config or weights: the tiling call reports why
+                _check(lib().df_mtp_tile_weights(ctypes.byref(self.cfg),
+                                                 ctypes.byref(self.weights), None, 0,
+                                                 _stream(None)))
+                _check(DF_EINVAL)
+            buf, p_ = _aligned_buffer(n, w.lm_head.device)
+            _check(lib().df_mtp_tile_weights(ctypes.byref(self.cfg), ctypes.byref(self.weights),
+                                             p_, n, _stream(None)))
+            torch.cuda.synchronize(w.lm_head.device)
+            self.weights.tiled = p_
+            self._tiled = buf
         self._k = (c_void_p * 1)(cache.k[0].data_ptr())
         self._v = (c_void_p * 1)(cache.v[0].data_ptr())
         self.cache_c = KvCache(self._k, self._v, cache.seq_len.data_ptr(), cache.cap,

@@ -1936,10 +1936,114 @@ void carve_mtp(Carve &cv, MtpWs &w, const df_mtp_config *c, int B, int cap) {
     carve_tc(cv, w.tc, B, rows);
 }
 
+// The weight operand of each MTP projection (the dense FFN only without experts), shared by the
+// step and by the tiling of the weights.
+enum MtpProj { MP_EH, MP_QKV, MP_O, MP_GATE_UP, MP_DOWN, MP_LM_HEAD, MP_COUNT };
+
+bool mtp_has(const df_mtp_config *c, int which) {
+    return !((which == MP_GATE_UP || which == MP_DOWN) && c->n_experts > 0);
+}
+
+GemmArgs mtp_proj(const df_mtp_config *c, const df_mtp_weights *w, int which) {
+    const int H = c->hidden, d = c->head_dim, qt = c->n_q_heads * d, kt = c->n_kv_heads * d;
+    GemmArgs g;
+    switch (which) {
+        case MP_EH:
+            g.W0 = w->eh_embed;
+            g.n0 = H;
+            g.Wk2 = w->eh_hidden;
+            g.K1 = H;
+            g.N = H;
+            g.K = 2 * H;
+            break;
+        case MP_QKV:
+            g.W0 = w->wq;
+            g.n0 = qt;
+            g.W1 = w->wk;
+            g.n1 = kt;
+            g.W2 = w->wv;
+            g.n2 = kt;
+            g.W3 = w->w_gate;
+            g.n3 = w->w_gate ? qt : 0;
+            g.N = qt + 2 * kt + g.n3;
+            g.K = H;
+            break;
+        case MP_O:
+            g.W0 = w->wo;
+            g.n0 = H;
+            g.N = H;
+            g.K = qt;
+            break;
+        case MP_GATE_UP:
+            g.W0 = w->w_gate_mlp;
+            g.n0 = c->intermediate;
+            g.W1 = w->w_up;
+            g.n1 = c->intermediate;
+            g.N = c->intermediate;
+            g.K = H;
+            g.epi = EPI_SWIGLU;
+            break;
+        case MP_DOWN:
+            g.W0 = w->w_down;
+            g.n0 = H;
+            g.N = H;
+            g.K = c->intermediate;
+            break;
+        default:   // MP_LM_HEAD
+            g.W0 = w->lm_head;
+            g.n0 = c->vocab;
+            g.N = c->vocab;
+            g.K = H;
+            break;
+    }
+    return g;
+}
+
+// Tiled layout of an MTP block's weights: eh_proj, QKV (+ output gate), O, the dense gate/up and
+// down (when there are no experts), the lm_head; each on a 1024-byte boundary. Offset of
+// projection `which` (MP_COUNT: the total).
+size_t mtp_tiled_offset(const df_mtp_config *c, const df_mtp_weights *w, int which) {
+    size_t off = 0;
+    for (int k = 0; k < which; ++k)
+        if (mtp_has(c, k)) off += (tiled_projection_bytes(mtp_proj(c, w, k)) + 1023) & ~size_t(1023);
+    return off;
+}
+
+const uint8_t *mtp_tiled(const df_mtp_config *c, const df_mtp_weights *w, int which) {
+    if (!w->tiled) return nullptr;
+    return static_cast<const uint8_t *>(w->tiled) + mtp_tiled_offset(c, w, which);
+}
+
 }  // namespace
 }  // namespace df
 
 extern "C" {
+
+size_t df_mtp_tiled_bytes(const df_mtp_config *cfg, const df_mtp_weights *w) {
+    if (check_mtp_cfg(cfg) != DF_OK || check_mtp_weights(cfg, w) != DF_OK) return 0;
+    g_err[0] = 0;
+    return mtp_tiled_offset(cfg, w, MP_COUNT);
+}
+
+int df_mtp_tile_weights(const df_mtp_config *cfg, const df_mtp_weights *w, void *tiled,
+                        size_t tiled_bytes, df_stream_t stream) {
+    g_err[0] = 0;
+    DF_TRY(check_mtp_cfg(cfg));
+    DF_TRY(check_mtp_weights(cfg, w));
+    const size_t need = mtp_tiled_offset(cfg, w, MP_COUNT);
+    REQ(tiled && tiled_bytes >= need, DF_EWORKSPACE, "tiled weights need %zu bytes, have %zu",
+        need, tiled_bytes);
+    REQ((reinterpret_cast<uintptr_t>(tiled) & 1023u) == 0, DF_EINVAL,
+        "tiled weights must be 1024-byte aligned");
+    uint8_t *base = static_cast<uint8_t *>(tiled);
+    for (int k = 0; k < MP_COUNT; ++k) {
+        if (!mtp_has(cfg, k)) continue;
+        const size_t off = mtp_tiled_offset(cfg, w, k);
+        const size_t len = tiled_projection_bytes(mtp_proj(cfg, w, k));
+        DF_TRY(tile_projection(mtp_proj(cfg, w, k), base + off, len, (cudaStream_t)stream));
+    }
+    return DF_OK;
+}
 
 size_t df_mtp_workspace_bytes(const df_mtp_config *cfg, int B) {
     if (check_mtp_cfg(cfg) != DF_OK || B <= 0) return 0;
@@ -2032,13 +2136,8 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
         ph.T = B;
         ph.K = H;
         DF_TRY(launch_pack(ph, s));
-        GemmArgs ge;
-        ge.W0 = w->eh_embed;
-        ge.n0 = H;
-        ge.Wk2 = w->eh_hidden;
-        ge.K1 = H;
-        ge.N = H;
-        ge.K = 2 * H;
+        GemmArgs ge = mtp_proj(cfg, w, MP_EH);
+        ge.At = mtp_tiled(cfg, w, MP_EH);
         ge.X = W.xp_e;
         ge.ldx = H;
         ge.X2 = W.xp_h;
@@ -2062,17 +2161,8 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
         pa.T = B;
         pa.K = H;
         DF_TRY(launch_pack(pa, s));
-        GemmArgs gq;
-        gq.W0 = w->wq;
-        gq.n0 = qt;
-        gq.W1 = w->wk;
-        gq.n1 = kt;
-        gq.W2 = w->wv;
-        gq.n2 = kt;
-        gq.W3 = w->w_gate;
-        gq.n3 = n_gate * d;
-        gq.N = Nq4;
-        gq.K = H;
+        GemmArgs gq = mtp_proj(cfg, w, MP_QKV);
+        gq.At = mtp_tiled(cfg, w, MP_QKV);
         gq.X = W.xp_attn;
         gq.ldx = H;
         gq.T = B;
@@ -2131,11 +2221,8 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
         at.pack = W.xp_o;
         at.status = d_status;
         DF_TRY(launch_attn(at, s));
-        GemmArgs go;
-        go.W0 = w->wo;
-        go.n0 = H;
-        go.N = H;
-        go.K = qt;
+        GemmArgs go = mtp_proj(cfg, w, MP_O);
+        go.At = mtp_tiled(cfg, w, MP_O);
         go.X = W.xp_o;
         go.ldx = qt;
         go.T = B;
@@ -2181,26 +2268,17 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
             pk.part = W.moe.part;
             pk.n_part = cfg->top_k + 1;
         } else {
-            GemmArgs gu;
-            gu.W0 = w->w_gate_mlp;
-            gu.n0 = I;
-            gu.W1 = w->w_up;
-            gu.n1 = I;
-            gu.N = I;
-            gu.K = H;
+            GemmArgs gu = mtp_proj(cfg, w, MP_GATE_UP);
+            gu.At = mtp_tiled(cfg, w, MP_GATE_UP);
             gu.X = W.xp_ffn;
             gu.ldx = H;
             gu.T = B;
-            gu.epi = EPI_SWIGLU;
             gu.pack_out = W.xp_act;
             gu.ldpo = I;
             gu.name = "gemm_gate_up";
             DF_TRY(launch_gemm_tc(gu, W.tc, s));
-            GemmArgs gd;
-            gd.W0 = w->w_down;
-            gd.n0 = H;
-            gd.N = H;
-            gd.K = I;
+            GemmArgs gd = mtp_proj(cfg, w, MP_DOWN);
+            gd.At = mtp_tiled(cfg, w, MP_DOWN);
             gd.X = W.xp_act;
             gd.ldx = I;
             gd.T = B;
@@ -2217,11 +2295,8 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
         if (sampled) {
             // this step's logits, then its draft drawn from softmax(logits / T)
             float *lg = logits_out + (size_t)st * B * cfg->vocab;
-            GemmArgs gl;
-            gl.W0 = w->lm_head;
-            gl.n0 = cfg->vocab;
-            gl.N = cfg->vocab;
-            gl.K = H;
+            GemmArgs gl = mtp_proj(cfg, w, MP_LM_HEAD);
+            gl.At = mtp_tiled(cfg, w, MP_LM_HEAD);
             gl.X = W.xp_head;
             gl.ldx = H;
             gl.T = B;
@@ -2246,13 +2321,11 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
             continue;
         }
         DF_TRY(lm_head_impl(w->lm_head, W.xp_head, B, H, cfg->vocab, W.amax_part,
-                            argmax_out + (size_t)st * B, nullptr, nullptr, W.tc, s));
+                            argmax_out + (size_t)st * B, nullptr, nullptr, W.tc, s, nullptr, 0.f,
+                            0, mtp_tiled(cfg, w, MP_LM_HEAD)));
         if (logits_out && st == n_steps - 1) {
-            GemmArgs gl;
-            gl.W0 = w->lm_head;
-            gl.n0 = cfg->vocab;
-            gl.N = cfg->vocab;
-            gl.K = H;
+            GemmArgs gl = mtp_proj(cfg, w, MP_LM_HEAD);
+            gl.At = mtp_tiled(cfg, w, MP_LM_HEAD);
             gl.X = W.xp_head;
             gl.ldx = H;
             gl.T = B;

@@ -694,7 +694,6 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
     p.At = a.At;
     p.kpg = 1;
     if (a.At) {
-        if (a.Wk2) return fail(DF_ESHAPE, "tiled weights of a projection split along K");
         if ((reinterpret_cast<uintptr_t>(a.At) & 1023u) != 0)
             return fail(DF_EINVAL, "tiled weights must be 1024-byte aligned (%p)", (const void *)a.At);
         const int per_kb = kABytes + NC * 128;
@@ -702,9 +701,10 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
         while (p.kpg > 1 && kStageBudget / (p.kpg * per_kb) < 2) --p.kpg;
         // the activations of kpg consecutive K blocks: dims (64 columns, 2T rows, K blocks) with
         // the K-block step of 128 bytes, so one box lands as kpg swizzled NC-row slices. Only
-        // when K is whole K blocks: this view has no column bound inside a row, so a ragged last
-        // block would read past the row (there one copy per K block keeps the 2-D map's bound).
-        p.b3 = K0 % kBK == 0 ? 1 : 0;
+        // with one activation matrix whose K is whole K blocks: this view has no column bound
+        // inside a row, so a ragged last block would read past the row (there, and with a K
+        // split, one 2-D copy per K block from its own map).
+        p.b3 = (!a.Wk2 && K0 % kBK == 0) ? 1 : 0;
         if (p.b3)
             DF_TRY(make_tma_3d(&p.bmap3, a.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kBK, 2 * T,
                                (uint64_t)(K0 / kBK), (uint64_t)a.ldx * 2, kBK * 2, kBK, NC,
@@ -756,26 +756,34 @@ struct TileArgs {
     int rows[4];
     int tile0[5];
     int n_seg;
-    int K0, kbt, pair, N, n_tiles;
+    const uint16_t *Wk2;     // K split: K blocks from kb_seg0 on read columns of Wk2
+    int K0, K1, kb_seg0, kbt, pair, N, n_tiles;
     uint8_t *out;
 };
 
-// The A-operand tiles of a projection, with the segment and pairing rules of build_params
-// (a projection split along K, whose two column ranges come from two matrices, is not tiled).
+// The A-operand tiles of a projection, with the segment, K-split and pairing rules of
+// build_params: K blocks [0, kb_seg0) from the first K0 columns, the rest from Wk2.
 int tile_plan(const GemmArgs &a, TileArgs &t) {
     memset(&t, 0, sizeof(t));
     if (a.N <= 0 || a.K <= 0) return fail(DF_ESHAPE, "tiled weights of an empty projection");
-    if (a.Wk2) return fail(DF_ESHAPE, "tiled weights of a projection split along K");
     t.pair = a.epi == EPI_SWIGLU;
     t.N = a.N;
-    t.K0 = a.K;
-    t.kbt = ceil_div(a.K, kBK);
+    t.K0 = a.Wk2 ? a.K1 : a.K;
+    t.K1 = a.K - t.K0;
+    t.Wk2 = a.Wk2;
+    t.kb_seg0 = ceil_div(t.K0, kBK);
+    t.kbt = t.kb_seg0 + (a.Wk2 ? ceil_div(t.K1, kBK) : 0);
     if (t.pair) {
         t.n_seg = 2;
         t.W[0] = a.W0;
         t.W[1] = a.W1;
         t.rows[0] = t.rows[1] = a.N;
         t.n_tiles = ceil_div(a.N, 64);
+    } else if (a.Wk2) {
+        t.n_seg = 1;
+        t.W[0] = a.W0;
+        t.rows[0] = a.n0;
+        t.n_tiles = ceil_div(a.n0, kBM);
     } else {
         const uint16_t *W[4] = {a.W0, a.W1, a.W2, a.W3};
         const int rows[4] = {a.n0, a.n1, a.n2, a.n3};
@@ -816,7 +824,15 @@ __global__ void __launch_bounds__(256) tile_weights_kernel(TileArgs t) {
             row = (long long)(m - t.tile0[s]) * kBM + r;
             if (row < t.rows[s]) W = t.W[s];
         }
-        const int col = kb * kBK + 8 * j, cols = t.K0;
+        int col, cols;
+        if (t.Wk2 && kb >= t.kb_seg0) {
+            if (W) W = t.Wk2;
+            col = (kb - t.kb_seg0) * kBK + 8 * j;
+            cols = t.K1;
+        } else {
+            col = kb * kBK + 8 * j;
+            cols = t.K0;
+        }
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (W && col < cols) {
             const uint16_t *src = W + row * cols + col;

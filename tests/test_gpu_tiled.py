@@ -151,3 +151,33 @@ def test_full_size_round_tiled_bitwise():
     b = _round(DFLASH_K15, True)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def _mtp(shape, tiled, steps=2, seed=0):
+    w = synth.mtp_weights(shape, seed=seed, device=DEV)
+    cache = synth.mtp_cache(shape, steps, seed=seed + 1, device=DEV)
+    prev, tok = synth.mtp_inputs(shape, seed=seed + 2, device=DEV)
+    model = B.MtpModel(shape, w, cache, tiled=tiled)
+    ws = B.alloc_workspace(model.workspace_bytes(shape.batch))
+    hid = torch.empty((steps, shape.batch, shape.hidden), device=DEV)
+    am = torch.empty((steps, shape.batch), dtype=torch.int32, device=DEV)
+    lg = torch.empty((shape.batch, shape.vocab), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.mtp_forward_draft(model, prev, tok, steps, hid, am, ws, logits_out=lg, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st) == 0
+    return hid.cpu(), am.cpu(), lg.cpu(), cache.k[0].cpu()
+
+
+@pytest.mark.parametrize("which", ["dense", "dense_no_gate", "moe"])
+def test_mtp_tiled_bitwise(which):
+    """eh_proj (one tiled K range over its two halves, activations by one copy per K block),
+    QKV with and without the output-gate rows, the dense gate/up and down, the lm_head argmax
+    and logits: the tiled MTP step equals the row-major one bit for bit."""
+    from speculative_decoding_drafter_dflash_gb300.workloads import MTP_MOE_TINY, MTP_TINY
+    shape = {"dense": MTP_TINY.with_(batch=2), "dense_no_gate": MTP_TINY.with_(gate=False),
+             "moe": MTP_MOE_TINY}[which]
+    a = _mtp(shape, False)
+    b = _mtp(shape, True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
