@@ -194,7 +194,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 struct AttnTcParams {
-    CUtensorMap kmap, vmap;   // F32 or BF16 [B * nkv * cap rows, d cols], 128-byte-wide boxes
+    // F32 or BF16 [B * nkv * cap rows, d cols] viewed as (128-byte column group, row, group):
+    // one box of 128 rows x all the groups of a unit brings the whole unit in one copy, landing
+    // as its 128-byte-wide swizzled boxes one after another
+    CUtensorMap kmap, vmap;
     AttnArgs a;
 };
 
@@ -252,9 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     auto stage_v = [&](int bf, int y) {
         uint8_t *dst = stg + (size_t)bf * kUnit;
         mbar_expect_tx(&full[bf], (uint32_t)kUnit);
-#pragma unroll
-        for (int j = 0; j < kBoxes; ++j)
-            tma_load_2d(dst + j * kBoxBytes, &P.vmap, &full[bf], j * kBoxCols, y, pol);
+        tma_load_3d(dst, &P.vmap, &full[bf], 0, y, 0, pol);
         ++nis[bf & 3];
     };
     pdl_trigger();
@@ -295,9 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             uint8_t *dst = stg + (size_t)t * kUnit;
             mbar_expect_tx(&full[t], (uint32_t)kUnit);
             const int y = (int)(head_off * a.cap + c0e) + t * kTcKeys;
-#pragma unroll
-            for (int j = 0; j < kBoxes; ++j)
-                tma_load_2d(dst + j * kBoxBytes, &P.kmap, &full[t], j * kBoxCols, y, pol);
+            tma_load_3d(dst, &P.kmap, &full[t], 0, y, 0, pol);
             ++nis[t & 3];
         }
         if (VS && n_early > 0) stage_v(2, (int)(head_off * a.cap + c0e));   // V unit 0
@@ -446,17 +445,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         x.h = local % NH;
         return x;
     };
-    // Unit u: K or V of tile t, 128-wide half h, staged by kBoxes TMA boxes of 128 rows.
+    // Unit u: K or V of tile t, 128-wide half h: one TMA copy of 128 rows x kBoxes column groups.
     auto issue = [&](int u) {
         const UnitInfo x = decode(u);
         const int bf = u % NB;
         uint8_t *dst = stg + (size_t)bf * kUnit;
         mbar_expect_tx(&full[bf], (uint32_t)kUnit);
         const int y = (int)(head_off * a.cap) + c0 + x.t * kTcKeys;
-#pragma unroll
-        for (int j = 0; j < kBoxes; ++j)
-            tma_load_2d(dst + j * kBoxBytes, x.v ? &P.vmap : &P.kmap, &full[bf],
-                        x.h * 128 + j * kBoxCols, y, pol);
+        tma_load_3d(dst, x.v ? &P.vmap : &P.kmap, &full[bf], 0, y, x.h * kBoxes, pol);
     };
 
     // Q rows are loaded before the first TMA boxes are issued, so they do not queue behind them.
@@ -1019,8 +1015,12 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
     const CUtensorMapDataType dt = a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int eb = a.kv_bf16 ? 2 : 4;
     const uint32_t box_cols = 128 / eb;       // one 128-byte row per box row
-    DF_TRY(make_tma_2d(&p.kmap, a.cache_k, dt, eb, D, rows, D, box_cols, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-    DF_TRY(make_tma_2d(&p.vmap, a.cache_v, dt, eb, D, rows, D, box_cols, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    // a unit: 128 rows x 128 columns (F32: four 32-column groups, BF16: two 64-column groups)
+    const uint32_t unit_groups = (uint32_t)(128 / box_cols);
+    DF_TRY(make_tma_3d(&p.kmap, a.cache_k, dt, eb, box_cols, rows, (uint64_t)D / box_cols,
+                       (uint64_t)D * eb, 128, box_cols, 128, unit_groups));
+    DF_TRY(make_tma_3d(&p.vmap, a.cache_v, dt, eb, box_cols, rows, (uint64_t)D / box_cols,
+                       (uint64_t)D * eb, 128, box_cols, 128, unit_groups));
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
     const bool one = a.chunk <= max_keys_one_pass;
