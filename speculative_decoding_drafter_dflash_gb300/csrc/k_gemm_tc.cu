@@ -46,7 +46,8 @@ constexpr int kBK = 64;                    // BF16 elements per K block: one 128
 constexpr int kABytes = kBM * kBK * 2;     // 16 KB
 constexpr int kTokChunk = 8;               // tokens per TMEM load (16 columns)
 // K blocks per pipeline stage when the weights are tiled: up to 4 (one 64 KB weight copy and one
-// activation copy per stage), as many as leave two stages in the shared-memory budget. This
+// activation copy per stage) for up to 32 tokens, as many as leave two stages in the
+// shared-memory budget. This
 // part's TMA unit moves roughly one copy per ~0.4 us per SM whatever its size up to 64 KB, so a
 // 16 KB weight tile per copy caps a CTA near 40 GB/s, below its share of HBM; 32-64 KB copies
 // stream at the HBM rate.
@@ -697,7 +698,10 @@ int build_params(const GemmArgs &a, const TcScratch &sc, TcParams &p, size_t &sm
         if ((reinterpret_cast<uintptr_t>(a.At) & 1023u) != 0)
             return fail(DF_EINVAL, "tiled weights must be 1024-byte aligned (%p)", (const void *)a.At);
         const int per_kb = kABytes + NC * 128;
-        p.kpg = kTiledKpgMax;
+        // Grouped K blocks pay off while the activation slices are small (up to 32 tokens);
+        // at 128 tokens each K block brings 32 KB of activations, and four single-K-block stages
+        // measured faster than two stages of two (batch-8 round 1327 -> 1293 us).
+        p.kpg = NC <= 64 ? kTiledKpgMax : 1;
         while (p.kpg > 1 && kStageBudget / (p.kpg * per_kb) < 2) --p.kpg;
         // the activations of kpg consecutive K blocks: dims (64 columns, 2T rows, K blocks) with
         // the K-block step of 128 bytes, so one box lands as kpg swizzled NC-row slices. Only
