@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the oracle's CPU sample time")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--batch", type=int, default=1, help="sequences of --profile-case round")
+    ap.add_argument("--batch", type=int, default=1, help="sequences of --profile-case round, trace, layout, gemms and lm_head")
     ap.add_argument("--ctx", type=int, default=0, help="cache rows of --profile-case round")
     ap.add_argument("--vocab", type=int, default=0, help="lm_head rows of --profile-case lm_head")
     ap.add_argument("--trace-dump", default=None, help="--profile-case trace: save the records")
@@ -1276,10 +1276,11 @@ def profile_case(args):
         return layout_case(args)
     if args.profile_case == "lm_head":
         V = args.vocab or s.vocab
+        rows = s.block * max(1, args.batch)          # --batch 8: the 128 rows of 8 sequences
         W = (torch.randn((V, s.hidden), generator=g, device=dev) * s.w_std).to(torch.bfloat16)
-        X = torch.randn((s.block, s.hidden), generator=g, device=dev)
-        idx = torch.empty(s.block, dtype=torch.int32, device=dev)
-        ws = B.alloc_workspace(B.lm_head_workspace_bytes(s.block, s.hidden, V), dev)
+        X = torch.randn((rows, s.hidden), generator=g, device=dev)
+        idx = torch.empty(rows, dtype=torch.int32, device=dev)
+        ws = B.alloc_workspace(B.lm_head_workspace_bytes(rows, s.hidden, V), dev)
         Wt = B.TiledMatrix(W)          # the round reads the lm_head from its tiled copy
         for _ in range(5):
             B.lm_head_argmax_tiled(Wt, X, idx, ws=ws)
