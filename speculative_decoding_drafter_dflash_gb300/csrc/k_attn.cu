@@ -665,19 +665,42 @@ size_t attn_part_floats(const AttnArgs &a) {
     return (size_t)a.B * a.nkv * a.n_chunks * R * (size_t)(a.d + 2);
 }
 
-// Keys per chunk: a whole number of tiles, about one CTA per SM (two waves when sequences x
-// KV heads alone nearly fill the GPU). Head dims 128 and 256 with up to 32 query rows per KV
-// head run on the tensor cores (128-key tiles); everything else runs on the CUDA cores.
+// Keys per chunk: a whole number of tiles. Head dims 128 and 256 with up to 32 query rows per KV
+// head run on the tensor cores (128-key tiles, one CTA per SM); everything else runs on the CUDA
+// cores (about one CTA per SM, two waves when sequences x KV heads alone nearly fill the GPU).
+// Tensor-core chunks: every CTA streams its chunk at about the same rate, so a launch lasts its
+// number of waves times (tiles per chunk + a fixed cost of about one tile for the CTA's start,
+// q operand and partial write-out); the plan takes the chunk length that minimises that product,
+// the longer chunk on a tie (fewer partials to merge). A last wave of a few CTAs costs as much as
+// a full one, which the plain one-CTA-per-SM rule ignores (8 sequences x 8 KV heads: 5 chunks
+// are 320 CTAs, three waves on 152 SMs; 7 chunks fill the same three waves with shorter chunks).
 void attn_plan(AttnArgs &a, int max_keys) {
     const int R = a.blk * (a.nq / a.nkv);
     const int heads = a.B * a.nkv;
-    const int waves = heads > 38 ? 2 : 1;
-    const int want = std::max(1, (waves * sm_count() + heads - 1) / heads);
     a.tc = attn_tc_supported(a.d, R) ? 1 : 0;
     const int TK = a.tc ? 128 : kTileBytes / (2 * a.d * 4);
     const int tiles = std::max(1, (max_keys + TK - 1) / TK);
-    const int n = std::min(want, tiles);
-    const int per = (tiles + n - 1) / n;
+    int per;
+    if (a.tc) {
+        constexpr long long kChunkFixedTiles = 1;
+        const long long sms = sm_count();
+        long long best = -1;
+        per = tiles;
+        for (int p = tiles; p >= 1; --p) {
+            const long long nc = (tiles + p - 1) / p;
+            const long long waves = (heads * nc + sms - 1) / sms;
+            const long long cost = waves * (p + kChunkFixedTiles);
+            if (best < 0 || cost < best) {
+                best = cost;
+                per = p;
+            }
+        }
+    } else {
+        const int waves = heads > 38 ? 2 : 1;
+        const int want = std::max(1, (waves * sm_count() + heads - 1) / heads);
+        const int n = std::min(want, tiles);
+        per = (tiles + n - 1) / n;
+    }
     a.chunk = per * TK;
     a.n_chunks = std::max(1, (max_keys + a.chunk - 1) / a.chunk);
 }

@@ -1051,7 +1051,7 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     const int R = a.blk * (a.nq / a.nkv);
     if (!attn_tc_supported(a.d, R) || a.chunk % kTcKeys != 0)
         return fail(DF_ESHAPE, "tensor-core attention: d=%d rows=%d chunk=%d", a.d, R, a.chunk);
-    if (a.d == 128) return R <= 16 ? launch_tc<128, 16, 2>(a, s) : launch_tc<128, 32, 2>(a, s);
+    if (a.d == 128) return R <= 16 ? launch_tc<128, 16, 3>(a, s) : launch_tc<128, 32, 3>(a, s);
     return R <= 16 ? launch_tc<256, 16, 3>(a, s) : launch_tc<256, 32, 2>(a, s);
 }
 

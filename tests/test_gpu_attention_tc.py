@@ -74,14 +74,16 @@ def test_mtp_tensor_core_attention(d, nq, nkv, kv_len, steps):
 
 
 def _tc_chunk_keys(B, nkv, max_keys, sms=152):
-    """Keys per attention chunk as the library plans them: a whole number of 128-key tiles,
-    about one CTA per SM (two waves above 38 sequence x KV-head pairs)."""
+    """Keys per attention chunk as the library plans them: the whole number of 128-key tiles
+    that minimises waves x (tiles per chunk + 1), one CTA per SM, the longer chunk on a tie."""
     heads = B * nkv
-    waves = 2 if heads > 38 else 1
-    want = max(1, (waves * sms + heads - 1) // heads)
     tiles = max(1, (max_keys + 127) // 128)
-    n = min(want, tiles)
-    return (tiles + n - 1) // n * 128
+    best, per = None, tiles
+    for p in range(tiles, 0, -1):
+        waves = (heads * ((tiles + p - 1) // p) + sms - 1) // sms
+        if best is None or waves * (p + 1) < best:
+            best, per = waves * (p + 1), p
+    return per * 128
 
 
 @pytest.mark.parametrize("ctx,n_new,causal", [
@@ -162,8 +164,9 @@ def test_attention_two_tile_chunks_in_place_v(seq, causal):
 
 
 def test_attention_long_chunks_run_in_passes():
-    """64 KV heads leave 5 chunks per head; 12000 keys then give 19-tile chunks, above the
-    15 tiles of scores TMEM holds at 32 query rows: two passes merged in registers."""
+    """64 KV heads over 12116 keys: 7 chunks of 14 tiles (three waves), above the 3 tiles of
+    scores TMEM holds next to the operands at 32 query rows: five passes merged in registers."""
+    assert _tc_chunk_keys(2, 32, 12100 + 16) == 14 * 128
     names = _attention_case(2, 16, 64, 32, 128, [12000, 9000], 12100, True, False, seed=77)
     assert "attn_tc_kernel" in names
 
