@@ -136,7 +136,9 @@ constexpr uint32_t kTraceMark = 1000;   // kids of DF_TRACE_MARK points: kTraceM
 // MMAs done, warp 0), 15 (the same, warp 15), 10 (first score tile read from TMEM), 14 (row
 // maxima of warp 0 reduced), 3 (row maxima of all warps), 0 (first tile's scores read again), 8
 // (first P operand written), 4 (all P operands), 5 (P.V done), 9 (partial outputs stored);
-// projection 11 (producer past the wait), 12 (an accumulator ready), 13 (epilogue done).
+// multi-pass attention 16 + p (pass p < 4 merged), 20 (pass 1: last K unit converted), 21
+// (pass 1: row maxima), 22 (pass 1: last P operand written); projection 11 (producer past the
+// wait), 12 (an accumulator ready), 13 (epilogue done).
 #if DF_TRACE
 extern __device__ TraceRec g_trace[kTraceMax];
 extern __device__ unsigned g_trace_n;
@@ -155,7 +157,7 @@ __device__ __forceinline__ uint32_t sm_id() {
 // shared-memory slot per phase (no global traffic until the end, so marking barely perturbs the
 // kernel); a mark stamped twice keeps the later time. Marks are stamped only after the kernel's
 // first CTA-wide barrier, which orders them after the slots are cleared.
-constexpr int kTraceMarks = 16;
+constexpr int kTraceMarks = 24;
 struct TraceScope {
     unsigned long long t0;
     uint32_t kid;

@@ -863,6 +863,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                         Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                         fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
                     want = pre_tiles;
+                    DF_TRACE_MARK(tid == 0 && p == 1, 21);
                 }
                 if (i >= nK + pre && i < nK + nV && (i - nK) % NH == 0) want = max(want, (i - nK) / NH + 1);
                 for (; pdone < want; ++pdone) {
@@ -904,7 +905,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 if (i == nK + nV) break;
                 if (ub + i >= n_early) convert(ub + i);   // the early units are converted already
+                DF_TRACE_MARK(tid == 0 && p == 1 && i == nK - 1, 20);
             }
+            DF_TRACE_MARK(tid == 0 && p == 1, 22);
             // end of a pass: its P.V products are complete
             mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
             tc_fence_after();
@@ -936,6 +939,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     for (int r = 0; r < NPH; ++r) mrun[r0 + r] = fmaxf(mrun[r0 + r], Mrow[r]);
                 conv_sync();
             }
+            DF_TRACE_MARK(tid == 0 && p < 4, 16 + p);
         }
 
         // read-out: o of this thread's rows, row sums, maxima
