@@ -204,6 +204,13 @@ struct AttnTcParams {
 // MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
 // KVB: the cache holds BF16 (no lo half: two MMAs per K step, and twice as many half-size
 // staging buffers in the same shared memory).
+// ST: chunks longer than two tiles of an F32 cache with head_dim 128, streamed tile by tile (no
+// passes): units in the order K0, K1, V0, K2, V1, ..., so the score MMAs of tile t + 1 run while
+// the warps take the softmax of tile t; scores alternate between two TMEM buffers; the output
+// accumulator stays in TMEM across the tiles with a lazily moved reference maximum per row (it is
+// raised, and the accumulator and row sums rescaled, only when a tile's maximum exceeds it by more
+// than 2^8, so the probabilities stay below 2^8 and no tile waits for a rescale in the usual
+// case); (o, m, l) are then the partials of the chunk against that reference.
 // VS: chunks of at most two tiles of an F32 cache with head_dim 128, three staging buffers. Each
 // V unit is converted in place in its staging buffer into V^T as a K-major BF16 operand in shared
 // memory (hi in the first 32 KB, lo in the second), which the P.V MMAs read directly. K unit t
@@ -211,10 +218,11 @@ struct AttnTcParams {
 // once K unit 0 is in TMEM. With the TMEM regions left to the K units, the V units of tiles that
 // predate the round are converted before the wait as well, and after it only q, the scores, the
 // softmax and the products remain (plus the units of tiles holding new rows).
-template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS>
+template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS, bool ST = false>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
     DF_TRACE_KERNEL(TK_ATTN_TC);
     static_assert(!VS || (D == 128 && NBUF == 3 && !MP && !KVB), "in-place V operands");
+    static_assert(!ST || (D == 128 && !MP && !KVB && !VS), "streamed tiles");
     constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
     constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit
     constexpr int kBoxes = kUnit / kBoxBytes;             // TMA boxes per unit
@@ -242,7 +250,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint64_t *pfree = pready + 2;     // [2] P.V MMAs reading the P buffer done
     uint64_t *odone = pfree + 2;      // the pass's P.V MMAs done
     uint64_t *drain = odone + 1;      // every MMA issued has completed
-    uint64_t *vready = drain + 1;     // [2] VS: V operand of tile t written (16 warp arrivals)
+    uint64_t *vready = drain + 1;     // [2] VS: V operand of tile t written (16 warp arrivals);
+                                      // ST: score MMAs of the tiles t with t % 2 == i done
     uint32_t *tslot = reinterpret_cast<uint32_t *>(vready + 2);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
 
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const long long c0e = (long long)chunk * a.chunk;
     if (NH == 1 && a.early_kv) {
         const long long old = a.seq_len[b];
-        while (n_early < min(2, NB) && (n_early + 1) * kTcKeys <= a.chunk &&
+        while (n_early < min(ST ? 1 : 2, NB) && (n_early + 1) * kTcKeys <= a.chunk &&
                c0e + (long long)(n_early + 1) * kTcKeys <= old &&
                c0e + (long long)(n_early + 1) * kTcKeys <= a.cap)
             ++n_early;
@@ -290,6 +299,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         mbar_init(drain, 1);
         if (VS)
             for (int i = 0; i < 2; ++i) mbar_init(&vready[i], kConvThreads / 32);
+        if (ST)
+            for (int i = 0; i < 2; ++i) mbar_init(&vready[i], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int t = 0; t < n_early; ++t) {
@@ -414,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // has an exact maximum and its output is merged into running (max, sum, o) registers.
     const int max_tp = (kTmemCols - kACols - NH * NS) / NS;
     const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
-    if (!MP && (n_tiles > max_tp || (VS && n_tiles > 2))) {   // the host plans within bounds
+    if (!MP && !ST && (n_tiles > max_tp || (VS && n_tiles > 2))) {   // the host plans within bounds
         if (tid == 0) set_status(a.status, DF_ESHAPE);
         tc_fence_before();
         __syncthreads();
@@ -434,8 +445,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         int t0, nt, v, t, h;
     };
     auto decode = [&](int u) -> UnitInfo {
-        const int p = min(u / upp, n_pass - 1);
         UnitInfo x;
+        if constexpr (ST) {
+            // K0, then per tile t: K(t + 1) when it exists, V(t)
+            x.t0 = 0;
+            x.nt = n_tiles;
+            x.h = 0;
+            const int t = (u - 1) >> 1;
+            if (u == 0) {
+                x.v = 0;
+                x.t = 0;
+            } else if (((u - 1) & 1) == 0 && t + 1 < n_tiles) {
+                x.v = 0;
+                x.t = t + 1;
+            } else {
+                x.v = 1;
+                x.t = t;
+            }
+            return x;
+        }
+        const int p = min(u / upp, n_pass - 1);
         x.t0 = p * tpp;
         x.nt = min(n_tiles, x.t0 + tpp) - x.t0;
         int local = u - p * upp;
@@ -516,11 +545,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // (every score MMA has completed before the first P is written), buffer 1 following it.
     // Several passes: Q stays live, so one buffer after the Q operands. VS: buffer 1 is the staging
     // buffer of K unit 1, read into TMEM before the score MMAs complete.
-    auto p_idx = [&](int t) -> int { return multi ? 0 : (t & 1); };
-    auto p_phase = [&](int t) -> uint32_t { return (uint32_t)((multi ? t : (t >> 1)) & 1); };
+    auto p_idx = [&](int t) -> int { return (multi || ST) ? 0 : (t & 1); };
+    auto p_phase = [&](int t) -> uint32_t { return (uint32_t)(((multi || ST) ? t : (t >> 1)) & 1); };
     auto p_buf = [&](int t) -> uint32_t {
         if (VS) return (t & 1) ? smem_u32(stg + kUnit) : smem_u32(qsm);
-        return multi ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
+        return (multi || ST) ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
     };
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NS >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
@@ -579,7 +608,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 uint32_t d, bhi;
                 bool acc;
                 if (!x.v) {
-                    d = tmem + (uint32_t)((x.t - x.t0) * NS);
+                    d = tmem + (uint32_t)((ST ? (x.t & 1) : (x.t - x.t0)) * NS);
                     bhi = smem_u32(qsm + x.h * 2 * kQBytes);
                     acc = x.h > 0;
                 } else {
@@ -601,7 +630,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 const bool last_of_tile = x.h == NH - 1;
                 const bool last_of_pass = last_of_tile && x.t == x.t0 + x.nt - 1;
                 if (!x.v) {
-                    if (last_of_pass) mma_commit(sdone);
+                    if (ST) mma_commit(&vready[x.t & 1]);
+                    else if (last_of_pass) mma_commit(sdone);
                 } else {
                     if (last_of_tile) mma_commit(&pfree[p_idx(x.t)]);
                     if (last_of_pass) mma_commit(odone);
@@ -830,7 +860,98 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // Per pass: the K units, then as many V units as there are operand regions (their regions
         // are freed by the score MMAs alone), then the softmax; the probabilities of a tile are
         // written before its first V unit that was not converted ahead.
-        for (int p = 0; p < (VS ? 0 : n_pass); ++p) {
+        if constexpr (ST) {
+            constexpr float kTau = 8.f;   // log2 units: probabilities stay below 2^8
+            float mref[NPH];
+#pragma unroll
+            for (int r = 0; r < NPH; ++r) mref[r] = -INFINITY;
+            if (n_early == 0) convert(0);                          // K0
+            for (int t = 0; t < n_tiles; ++t) {
+                const bool more = t + 1 < n_tiles;
+                if (more) convert(2 * t + 1);                      // K(t + 1)
+                convert(more ? 2 * t + 2 : 2 * t + 1);             // V(t)
+                // scores of tile t -> its row maxima (max over the four lane quarters)
+                mbar_wait(&vready[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, a.status);
+                tc_fence_after();
+                float sv[NPH], mx[NPH];
+                {
+                    uint32_t sh[NPH], sl[NPH];
+                    tmem_ld_nowait<NPH>(tmem + lane_addr + (t & 1) * NS + r0, sh);
+                    tmem_ld_nowait<NPH>(tmem + lane_addr + (t & 1) * NS + NP + r0, sl);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
+                }
+                const int kt = lq * 32 + lane;
+                const int key = c0 + t * kTcKeys + kt;
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) mx[r] = row_ok(key, r0 + r) ? sv[r] * scale : -INFINITY;
+                int row;
+                const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
+                float *rb = red + (t & 1) * 4 * NP;   // alternate: a fast warp may reach tile t + 1
+                if ((lane & (32 / NPH - 1)) == 0) rb[lq * NP + r0 + row] = m;
+                conv_sync();
+                float mn[NPH];
+#pragma unroll
+                for (int r = 0; r < NPH; ++r)
+                    mn[r] = fmaxf(fmaxf(rb[r0 + r], rb[NP + r0 + r]), fmaxf(rb[2 * NP + r0 + r], rb[3 * NP + r0 + r]));
+                // the P.V MMAs of tile t - 1 are done: the P buffer and the accumulator are free
+                if (t > 0) {
+                    mbar_wait(&pfree[0], (uint32_t)((t - 1) & 1), abort_flag, a.status);
+                    tc_fence_after();
+                }
+                bool resc = false;   // the same for every lane: the warp's lanes share its rows
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) resc |= mref[r] != -INFINITY && mn[r] > mref[r] + kTau;
+                if (resc) {
+                    float oh[NPH], ol[NPH];
+                    tmem_rows<NPH>(tmem + lane_addr + ocol + r0, oh);
+                    tmem_rows<NPH>(tmem + lane_addr + ocol + NP + r0, ol);
+                    uint32_t wh[NPH], wl[NPH];
+#pragma unroll
+                    for (int r = 0; r < NPH; ++r) {
+                        const float f = (mref[r] != -INFINITY && mn[r] > mref[r] + kTau) ? ex2(mref[r] - mn[r]) : 1.f;
+                        wh[r] = __float_as_uint(oh[r] * f);
+                        wl[r] = __float_as_uint(ol[r] * f);
+                        lsum[r] *= f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < NPH; j += 4) {
+                        const uint32_t h4[4] = {wh[j], wh[j + 1], wh[j + 2], wh[j + 3]};
+                        const uint32_t l4[4] = {wl[j], wl[j + 1], wl[j + 2], wl[j + 3]};
+                        tmem_st4(tmem + lane_addr + ocol + r0 + j, h4);
+                        tmem_st4(tmem + lane_addr + ocol + NP + r0 + j, l4);
+                    }
+                    tmem_wait_st();
+                }
+#pragma unroll
+                for (int r = 0; r < NPH; ++r)
+                    if (mref[r] == -INFINITY || mn[r] > mref[r] + kTau) mref[r] = mn[r];
+                // probabilities of tile t against the reference -> BF16 hi/lo P operand
+                const uint32_t pb = p_buf(t);
+#pragma unroll
+                for (int r = 0; r < NPH; ++r) {
+                    const int rr = r0 + r;
+                    float pv = 0.f;
+                    if (row_ok(key, rr) && mref[r] != -INFINITY) pv = ex2(sv[r] * scale - mref[r]);
+                    lsum[r] += pv;
+                    const uint16_t ph = f32_to_bf16_bits(pv);
+                    const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
+                    st_shared_u16(pb + sw_off(NS, rr, kt), ph);
+                    st_shared_u16(pb + sw_off(NS, NP + rr, kt), pl);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pready[0]);
+            }
+#pragma unroll
+            for (int r = 0; r < NPH; ++r) Mrow[r] = mref[r];
+            mbar_wait(odone, 0u, abort_flag, a.status);
+            tc_fence_after();
+            conv_sync();   // every warp has read the last tile's maxima: the read-out reuses red
+        }
+        for (int p = 0; p < ((VS || ST) ? 0 : n_pass); ++p) {
             const int pt0 = p * tpp, nt = min(n_tiles, pt0 + tpp) - pt0, ub = p * upp;
             const int nK = nt * NH, nV = nK, pre = min(NA, nV), pre_tiles = (pre + NH - 1) / NH;
             int pdone = 0;   // tiles of the pass whose P operand is written
@@ -1040,11 +1161,15 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
             return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, 3, false, false, true>, grid,
                             dim3(kTcThreads), smem_vs, s, p);
         }
+        // longer chunks: streamed tile by tile
+        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false, true>,
+                        grid, dim3(kTcThreads), smem, s, p);
+    } else {
+        return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false>, grid,
+                              dim3(kTcThreads), smem, s, p)
+                   : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false, false>, grid,
+                              dim3(kTcThreads), smem, s, p);
     }
-    return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false>, grid,
-                          dim3(kTcThreads), smem, s, p)
-               : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false, false>, grid,
-                          dim3(kTcThreads), smem, s, p);
 }
 
 }  // namespace

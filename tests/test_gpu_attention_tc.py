@@ -103,6 +103,19 @@ def test_dflash_forward_two_tile_chunks_in_place_v(ctx, n_new, causal):
     assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
 
 
+def test_dflash_forward_streamed_chunks_batched():
+    """8 sequences x 8 KV heads over 63 tiles: 7 chunks of 9 tiles streamed tile by tile inside
+    the forward (the first K unit of a chunk below the old context end converted before the
+    wait; new context rows and block rows in the last chunk), against the oracle."""
+    shape = TINY.with_(head_dim=128, n_q_heads=16, n_kv_heads=8, K=15, ctx=8000, batch=8)
+    assert _tc_chunk_keys(8, 8, 8000 + 2 * shape.block) == 9 * 128
+    n_new = [3, 0, 16, 1, 7, 2, 5, 9]
+    r, names = _kernels(lambda: _run_forward(shape, n_new, seed=41))
+    assert "attn_tc_kernel" in names
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+
+
 # ---------------------------------------------------------------- df_attention on its own
 ATTN_TOL = 1e-4   # hi/lo BF16 operands carry ~16 mantissa bits; the CUDA-core path is plain F32
 
@@ -163,12 +176,62 @@ def test_attention_two_tile_chunks_in_place_v(seq, causal):
     assert "attn_tc_kernel" in names
 
 
-def test_attention_long_chunks_run_in_passes():
-    """64 KV heads over 12116 keys: 7 chunks of 14 tiles (three waves), above the 3 tiles of
-    scores TMEM holds next to the operands at 32 query rows: five passes merged in registers."""
+def test_attention_long_chunks_streamed():
+    """64 KV heads over 12116 keys: 7 chunks of 14 tiles (three waves), streamed tile by tile at
+    32 query rows (two score buffers, the output accumulated in TMEM across the tiles)."""
     assert _tc_chunk_keys(2, 32, 12100 + 16) == 14 * 128
     names = _attention_case(2, 16, 64, 32, 128, [12000, 9000], 12100, True, False, seed=77)
     assert "attn_tc_kernel" in names
+
+
+@pytest.mark.parametrize("Bn,blk,nq,nkv,seq,cap,causal,chunk_tiles", [
+    (1, 16, 16, 8, [5000], 5100, False, 3),            # 32 rows, 3-tile chunks, block rows last
+    (1, 16, 16, 8, [4990], 5100, True, 3),             # causal block, ragged last tile
+    (8, 2, 16, 8, [3000, 1, 2999, 0, 1500, 2048, 7, 2500], 3000, False, 12),  # 4 rows per head
+])
+def test_attention_streamed_chunks(Bn, blk, nq, nkv, seq, cap, causal, chunk_tiles):
+    """Chunks longer than two tiles of an F32 cache with head_dim 128: every chunk streamed tile
+    by tile, ragged sequence ends, empty sequences, block rows in the last chunk."""
+    assert _tc_chunk_keys(Bn, nkv, cap + blk) == chunk_tiles * 128
+    names = _attention_case(Bn, blk, nq, nkv, 128, seq, cap, True, causal, seed=cap + blk + causal)
+    assert "attn_tc_kernel" in names
+
+
+def test_attention_streamed_rescales_the_accumulator():
+    """Keys whose scores grow along the cache (for the first query row each 128-key tile's
+    maximum lies ~11 log2 units above the previous one's, beyond the 2^8 the reference may lag
+    by), so the streamed form raises its reference maximum and rescales the output accumulator
+    and row sums at every tile; 64 KV heads make 5-tile chunks. q and the keys are BF16 values
+    (exact in the hi half), so scores up to ~70 stay exact to F32 accumulation and the float64
+    softmax bounds the error as tightly as for unit-sized scores."""
+    from oracle import core
+    Bn, blk, nq, nkv, d, S, cap = 2, 16, 64, 32, 128, 1200, 1200
+    assert _tc_chunk_keys(Bn, nkv, cap + blk) == 5 * 128
+    g = torch.Generator(device="cuda").manual_seed(5)
+    bf = lambda x: x.to(torch.bfloat16).float()
+    q = bf(torch.randn((Bn, blk, nq, d), generator=g, device="cuda"))
+    direction = q[0, 0, 0] / q[0, 0, 0].norm()
+    ramp = torch.arange(cap, device="cuda", dtype=torch.float32) * (0.7 / 128.0) * d ** 0.5
+    ck = torch.randn((Bn, nkv, cap, d), generator=g, device="cuda") * 0.1
+    ck = bf(ck + ramp[None, None, :, None] * direction)
+    cv = torch.randn((Bn, nkv, cap, d), generator=g, device="cuda")
+    kb = bf(torch.randn((Bn, nkv, blk, d), generator=g, device="cuda"))
+    vb = torch.randn((Bn, nkv, blk, d), generator=g, device="cuda")
+    sl = torch.full((Bn,), S, dtype=torch.int32, device="cuda")
+    out = torch.full((Bn, blk, nq, d), float("nan"), device="cuda")
+    ws = B.alloc_workspace(B.attention_workspace_bytes(Bn, blk, nq, nkv, d, cap))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attention(q, ck, cv, sl, out, ws, kb, vb, False, st)
+    torch.cuda.synchronize()
+    assert int(st) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    qh, kh, vh = synth.host(q), synth.host(ck), synth.host(cv)
+    for b in range(Bn):
+        keys = np.concatenate([kh[b, :, :S].transpose(1, 0, 2), synth.host(kb)[b].transpose(1, 0, 2)])
+        vals = np.concatenate([vh[b, :, :S].transpose(1, 0, 2), synth.host(vb)[b].transpose(1, 0, 2)])
+        ref = core.sdpa(qh[b], keys, vals, None, np.float64)
+        assert rel_err(got[b], ref) <= ATTN_TOL, f"sequence {b}"
 
 
 def test_attention_no_visible_keys_gives_zeros():
