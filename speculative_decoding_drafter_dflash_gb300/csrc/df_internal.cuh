@@ -136,8 +136,9 @@ constexpr uint32_t kTraceMark = 1000;   // kids of DF_TRACE_MARK points: kTraceM
 // MMAs done, warp 0), 15 (the same, warp 15), 10 (first score tile read from TMEM), 14 (row
 // maxima of warp 0 reduced), 3 (row maxima of all warps), 0 (first tile's scores read again), 8
 // (first P operand written), 4 (all P operands), 5 (P.V done), 9 (partial outputs stored);
-// multi-pass attention 16 + p (pass p < 4 merged), 20 (pass 1: last K unit converted), 21
-// (pass 1: row maxima), 22 (pass 1: last P operand written); projection 11 (producer past the
+// streamed attention, tile 4: 16 (its iteration starts), 17 (K of tile 5 converted), 18 (V of
+// tile 4 converted), 19 (its scores ready), 20 (its row maxima), 21 (P.V of tile 3 done), 22 (its
+// P operand written), and 23 (the iteration of tile 5 starts); projection 11 (producer past the
 // wait), 12 (an accumulator ready), 13 (epilogue done).
 #if DF_TRACE
 extern __device__ TraceRec g_trace[kTraceMax];

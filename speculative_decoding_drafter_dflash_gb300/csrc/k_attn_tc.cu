@@ -9,8 +9,11 @@
 // forward: softmax(q k^T / sqrt(d)) v over the visible keys).
 //
 // Each 128-key x 128-dim piece of K or V (a "unit") lands in shared memory by TMA with the
-// 128-byte swizzle (F32: four 32-column boxes, BF16: two 64-column boxes), so a thread reading
-// one row, or one column, of it touches every bank once. The sixteen converting warps turn a unit
+// 128-byte swizzle (F32: four 32-column groups, BF16: two 64-column groups): a K unit group by
+// group (each group's 128 rows as one 16 KB box), so a thread reading one key row touches every
+// bank once; a V unit row by row (each row's groups as consecutive 128-byte lines), so the copy
+// reads whole cache rows in address order and a warp reading one dim of a key still touches
+// every bank once. The sixteen converting warps turn a unit
 // into a BF16 operand in tensor memory (TMEM), where the MMA reads it as its A matrix:
 //   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (A = K: lane = key)
 //   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (A = V^T: lane = dim)
@@ -194,9 +197,9 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 struct AttnTcParams {
-    // F32 or BF16 [B * nkv * cap rows, d cols] viewed as (128-byte column group, row, group):
-    // one box of 128 rows x all the groups of a unit brings the whole unit in one copy, landing
-    // as its 128-byte-wide swizzled boxes one after another
+    // F32 or BF16 [B * nkv * cap rows, d cols]. kmap views it as (column in group, row, group):
+    // one box of 128 rows x all the groups of a unit lands as the groups' 128-row boxes one after
+    // another. vmap views it as (column in group, group, row): the box lands row-major.
     CUtensorMap kmap, vmap;
     AttnArgs a;
 };
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     auto stage_v = [&](int bf, int y) {
         uint8_t *dst = stg + (size_t)bf * kUnit;
         mbar_expect_tx(&full[bf], (uint32_t)kUnit);
-        tma_load_3d(dst, &P.vmap, &full[bf], 0, y, 0, pol);
+        tma_load_3d(dst, &P.vmap, &full[bf], 0, 0, y, pol);
         ++nis[bf & 3];
     };
     pdl_trigger();
@@ -330,12 +333,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     auto convert_vs = [&](int t, int bf, uint32_t ph, int kbase, int s_cache, int kend) {
         mbar_wait(&full[bf], ph, abort_flag, a.status);
         uint8_t *st = stg + (size_t)bf * kUnit;
-        const uint8_t *sb = st + lq * kBoxBytes + (lane & 3) * 4;   // box of dims 32*lq..
+        // V rows staged row-major: key kr's column group lq (dims 32*lq..) is 128-byte line
+        // 4*kr + lq, swizzled by the line index (kr0 is a multiple of 8)
+        const uint8_t *sb = st + lq * 128 + (lane & 3) * 4;
         const int kr0 = 32 * grp, c = lane >> 2;
         float v[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-            v[e] = *reinterpret_cast<const float *>(sb + (kr0 + e) * 128 + ((c ^ (e & 7)) << 4));
+            v[e] = *reinterpret_cast<const float *>(sb + (kr0 + e) * 512 + ((c ^ ((4 * e + lq) & 7)) << 4));
         if (kbase + kr0 + 31 >= s_cache) {
             const float *blkp = a.vb + head_off * a.blk * (size_t)D + lq * 32 + lane;
 #pragma unroll
@@ -481,7 +486,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         uint8_t *dst = stg + (size_t)bf * kUnit;
         mbar_expect_tx(&full[bf], (uint32_t)kUnit);
         const int y = (int)(head_off * a.cap) + c0 + x.t * kTcKeys;
-        tma_load_3d(dst, x.v ? &P.vmap : &P.kmap, &full[bf], 0, y, x.h * kBoxes, pol);
+        if (x.v) tma_load_3d(dst, &P.vmap, &full[bf], 0, x.h * kBoxes, y, pol);
+        else tma_load_3d(dst, &P.kmap, &full[bf], 0, y, x.h * kBoxes, pol);
     };
 
     // Q rows are loaded before the first TMA boxes are issued, so they do not queue behind them.
@@ -697,16 +703,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
             } else if constexpr (!VS) {
                 const int dd = lq * 32 + lane;                // dim within the 128-wide half
-                const int col = dd % kBoxCols;
-                const uint8_t *sb = st + (dd / kBoxCols) * kBoxBytes;
+                const int col = dd % kBoxCols, gsel = dd / kBoxCols;
+                // V rows staged row-major: key kr's column group gsel is 128-byte line
+                // kBoxes * kr + gsel, swizzled by the line index
+                const uint8_t *sb = st + gsel * 128;
                 auto staged = [&](int kr, int k7) -> float {    // k7 = kr & 7, known statically
+                    const int x = (kBoxes * k7 + gsel) & 7;
                     if constexpr (KVB) {
                         const uint16_t bits = *reinterpret_cast<const uint16_t *>(
-                            sb + kr * 128 + (((col >> 3) ^ k7) << 4) + (col & 7) * 2);
+                            sb + kr * (kBoxes * 128) + (((col >> 3) ^ x) << 4) + (col & 7) * 2);
                         return __uint_as_float((uint32_t)bits << 16);
                     } else {
                         return *reinterpret_cast<const float *>(
-                            sb + kr * 128 + (((col >> 2) ^ k7) << 4) + (col & 3) * 4);
+                            sb + kr * (kBoxes * 128) + (((col >> 2) ^ x) << 4) + (col & 3) * 4);
                     }
                 };
 #pragma unroll 2
@@ -868,11 +877,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             if (n_early == 0) convert(0);                          // K0
             for (int t = 0; t < n_tiles; ++t) {
                 const bool more = t + 1 < n_tiles;
+                DF_TRACE_MARK(tid == 0 && t == 4, 16);
+                DF_TRACE_MARK(tid == 0 && t == 5, 23);
                 if (more) convert(2 * t + 1);                      // K(t + 1)
+                DF_TRACE_MARK(tid == 0 && t == 4, 17);
                 convert(more ? 2 * t + 2 : 2 * t + 1);             // V(t)
+                DF_TRACE_MARK(tid == 0 && t == 4, 18);
                 // scores of tile t -> its row maxima (max over the four lane quarters)
                 mbar_wait(&vready[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, a.status);
                 tc_fence_after();
+                DF_TRACE_MARK(tid == 0 && t == 4, 19);
                 float sv[NPH], mx[NPH];
                 {
                     uint32_t sh[NPH], sl[NPH];
@@ -891,6 +905,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 float *rb = red + (t & 1) * 4 * NP;   // alternate: a fast warp may reach tile t + 1
                 if ((lane & (32 / NPH - 1)) == 0) rb[lq * NP + r0 + row] = m;
                 conv_sync();
+                DF_TRACE_MARK(tid == 0 && t == 4, 20);
                 float mn[NPH];
 #pragma unroll
                 for (int r = 0; r < NPH; ++r)
@@ -900,6 +915,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     mbar_wait(&pfree[0], (uint32_t)((t - 1) & 1), abort_flag, a.status);
                     tc_fence_after();
                 }
+                DF_TRACE_MARK(tid == 0 && t == 4, 21);
                 bool resc = false;   // the same for every lane: the warp's lanes share its rows
 #pragma unroll
                 for (int r = 0; r < NPH; ++r) resc |= mref[r] != -INFINITY && mn[r] > mref[r] + kTau;
@@ -944,6 +960,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pready[0]);
+                DF_TRACE_MARK(tid == 0 && t == 4, 22);
             }
 #pragma unroll
             for (int r = 0; r < NPH; ++r) Mrow[r] = mref[r];
@@ -984,7 +1001,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                         Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                         fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
                     want = pre_tiles;
-                    DF_TRACE_MARK(tid == 0 && p == 1, 21);
                 }
                 if (i >= nK + pre && i < nK + nV && (i - nK) % NH == 0) want = max(want, (i - nK) / NH + 1);
                 for (; pdone < want; ++pdone) {
@@ -1026,9 +1042,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 if (i == nK + nV) break;
                 if (ub + i >= n_early) convert(ub + i);   // the early units are converted already
-                DF_TRACE_MARK(tid == 0 && p == 1 && i == nK - 1, 20);
             }
-            DF_TRACE_MARK(tid == 0 && p == 1, 22);
             // end of a pass: its P.V products are complete
             mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
             tc_fence_after();
@@ -1060,7 +1074,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     for (int r = 0; r < NPH; ++r) mrun[r0 + r] = fmaxf(mrun[r0 + r], Mrow[r]);
                 conv_sync();
             }
-            DF_TRACE_MARK(tid == 0 && p < 4, 16 + p);
         }
 
         // read-out: o of this thread's rows, row sums, maxima
@@ -1144,8 +1157,10 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
     const uint32_t unit_groups = (uint32_t)(128 / box_cols);
     DF_TRY(make_tma_3d(&p.kmap, a.cache_k, dt, eb, box_cols, rows, (uint64_t)D / box_cols,
                        (uint64_t)D * eb, 128, box_cols, 128, unit_groups));
-    DF_TRY(make_tma_3d(&p.vmap, a.cache_v, dt, eb, box_cols, rows, (uint64_t)D / box_cols,
-                       (uint64_t)D * eb, 128, box_cols, 128, unit_groups));
+    // V: the same unit as (column in group, group, row), so a copy reads whole cache rows in
+    // address order; it lands row-major (each row's groups as consecutive 128-byte lines)
+    DF_TRY(make_tma_3d(&p.vmap, a.cache_v, dt, eb, box_cols, (uint64_t)D / box_cols, rows, 128,
+                       (uint64_t)D * eb, box_cols, unit_groups, 128));
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
     const bool one = a.chunk <= max_keys_one_pass;
