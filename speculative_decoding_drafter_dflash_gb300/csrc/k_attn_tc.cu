@@ -207,7 +207,7 @@ struct AttnTcParams {
 // MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
 // KVB: the cache holds BF16 (no lo half: two MMAs per K step, and twice as many half-size
 // staging buffers in the same shared memory).
-// ST: chunks longer than two tiles of an F32 cache with head_dim 128, streamed tile by tile (no
+// ST: chunks longer than two tiles of a cache with head_dim 128, streamed tile by tile (no
 // passes): units in the order K0, K1, V0, K2, V1, ..., so the score MMAs of tile t + 1 run while
 // the warps take the softmax of tile t; scores alternate between two TMEM buffers; the output
 // accumulator stays in TMEM across the tiles with a lazily moved reference maximum per row (it is
@@ -225,7 +225,7 @@ template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS, bool ST = false>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
     DF_TRACE_KERNEL(TK_ATTN_TC);
     static_assert(!VS || (D == 128 && NBUF == 3 && !MP && !KVB), "in-place V operands");
-    static_assert(!ST || (D == 128 && !MP && !KVB && !VS), "streamed tiles");
+    static_assert(!ST || (D == 128 && !MP && !VS), "streamed tiles");
     constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
     constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit
     constexpr int kBoxes = kUnit / kBoxBytes;             // TMA boxes per unit
@@ -1164,11 +1164,17 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
     const bool one = a.chunk <= max_keys_one_pass;
-    if (a.kv_bf16)
+    if (a.kv_bf16) {
+        if constexpr (D == 128) {
+            if (a.chunk > 2 * kTcKeys)   // longer chunks: streamed tile by tile
+                return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true, false, true>,
+                                grid, dim3(kTcThreads), smem, s, p);
+        }
         return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true, false>, grid,
                               dim3(kTcThreads), smem, s, p)
                    : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, true, false>, grid,
                               dim3(kTcThreads), smem, s, p);
+    }
     if constexpr (D == 128) {
         if (a.chunk <= 2 * kTcKeys) {   // chunks of one or two tiles: V operands in place
             constexpr size_t smem_vs = attn_tc_smem_bytes<D, NP, 3, true>();

@@ -53,8 +53,9 @@ def test_bf16_kv_forward_matches_oracle(d, nq, nkv, K, ctx, n_new, causal):
         assert np.array_equal(kb, r["ks"][l][0, :, :s0])
 
 
-def test_bf16_kv_batched_multi_pass_chunks():
-    """Two sequences x 16 KV heads with 12000 cached keys: 19-tile chunks, two passes."""
+def test_bf16_kv_batched_streamed_chunks():
+    """Two sequences x 16 KV heads with 12000 cached keys: 4 chunks of 24 tiles per head (128
+    CTAs, one wave), streamed tile by tile with BF16 units (four TMEM operand regions)."""
     shape = TINY.with_(head_dim=128, n_q_heads=32, n_kv_heads=16, K=15, ctx=12000, batch=2,
                        kv_bf16=True)
     r = _run_forward(shape, [4, 1], seed=91)
