@@ -8,12 +8,12 @@
 // merges the chunks. Scores follow hf2q 0.1.1 models/qwen35/mtp.rs (`sdpa` step of the draft
 // forward: softmax(q k^T / sqrt(d)) v over the visible keys).
 //
-// Each 128-key x 128-dim piece of K or V (a "unit") lands in shared memory by TMA with the
-// 128-byte swizzle (F32: four 32-column groups, BF16: two 64-column groups): a K unit group by
-// group (each group's 128 rows as one 16 KB box), so a thread reading one key row touches every
-// bank once; a V unit row by row (each row's groups as consecutive 128-byte lines), so the copy
-// reads whole cache rows in address order and a warp reading one dim of a key still touches
-// every bank once. The sixteen converting warps turn a unit
+// Each 128-key x 128-dim piece of K or V (a "unit") lands in shared memory by TMA. A K unit
+// comes with the 128-byte swizzle (F32: four 32-column groups, BF16: two 64-column groups)
+// group by group (each group's 128 rows as one box), so a thread reading one key row touches
+// every bank once. A V unit of head_dim 128 is 128 whole cache rows, one contiguous run: one
+// bulk copy, landing as copied (a warp reading one dim of 32 keys reads consecutive words);
+// for head_dim 256 each 128-wide half comes row by row with the swizzle. The sixteen converting warps turn a unit
 // into a BF16 operand in tensor memory (TMEM), where the MMA reads it as its A matrix:
 //   scores  S^T [128 keys x NP rows]  = K [128 x d] . Q^T          (A = K: lane = key)
 //   output  O^T [128 dims x NP rows] += V^T [128 x 128 keys] . P^T  (A = V^T: lane = dim)
@@ -199,7 +199,8 @@ __device__ __forceinline__ void tmem_ld_wait() {
 struct AttnTcParams {
     // F32 or BF16 [B * nkv * cap rows, d cols]. kmap views it as (column in group, row, group):
     // one box of 128 rows x all the groups of a unit lands as the groups' 128-row boxes one after
-    // another. vmap views it as (column in group, group, row): the box lands row-major.
+    // another. vmap (head_dim 256) views it as (column in group, group, row): the box lands
+    // row-major.
     CUtensorMap kmap, vmap;
     AttnArgs a;
 };
@@ -263,11 +264,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const size_t head_off = (size_t)b * a.nkv + g;
     const uint64_t pol = policy_evict_first();
     int nis[4] = {0, 0, 0, 0};   // VS: TMA loads issued into each staging buffer (thread 0)
+    // V unit of cache rows [y, y + 128) (head_dim 128: one contiguous run of rows) by one bulk
+    // copy, cut at the end of the cache; rows past it are never read (keys past the cache rows
+    // come from the block rows or are zero). Other head dims: a 128-wide half through vmap.
+    auto load_v = [&](uint8_t *dst, uint64_t *bar, long long y, int h) {
+        if constexpr (D == 128) {
+            constexpr uint32_t kRow = 128 * (KVB ? 2 : 4);
+            const long long left = (long long)a.B * a.nkv * a.cap - y;
+            const uint32_t bytes = (uint32_t)min(max(left, 0LL), 128LL) * kRow;
+            mbar_expect_tx(bar, bytes);
+            if (bytes) bulk_load(dst, reinterpret_cast<const uint8_t *>(a.cache_v) + (size_t)y * kRow, bytes, bar, pol);
+        } else {
+            mbar_expect_tx(bar, (uint32_t)kUnit);
+            tma_load_3d(dst, &P.vmap, bar, 0, h * kBoxes, (int)y, pol);
+        }
+    };
     // VS: V rows [y, y + 128) of the cache into staging buffer bf (thread 0)
     auto stage_v = [&](int bf, int y) {
-        uint8_t *dst = stg + (size_t)bf * kUnit;
-        mbar_expect_tx(&full[bf], (uint32_t)kUnit);
-        tma_load_3d(dst, &P.vmap, &full[bf], 0, 0, y, pol);
+        load_v(stg + (size_t)bf * kUnit, &full[bf], y, 0);
         ++nis[bf & 3];
     };
     pdl_trigger();
@@ -333,14 +347,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     auto convert_vs = [&](int t, int bf, uint32_t ph, int kbase, int s_cache, int kend) {
         mbar_wait(&full[bf], ph, abort_flag, a.status);
         uint8_t *st = stg + (size_t)bf * kUnit;
-        // V rows staged row-major: key kr's column group lq (dims 32*lq..) is 128-byte line
-        // 4*kr + lq, swizzled by the line index (kr0 is a multiple of 8)
-        const uint8_t *sb = st + lq * 128 + (lane & 3) * 4;
-        const int kr0 = 32 * grp, c = lane >> 2;
+        // V rows staged as copied (row kr at 512 * kr); the warp reads 32 consecutive dims
+        const uint8_t *sb = st + (lq * 32 + lane) * 4;
+        const int kr0 = 32 * grp;
         float v[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-            v[e] = *reinterpret_cast<const float *>(sb + (kr0 + e) * 512 + ((c ^ ((4 * e + lq) & 7)) << 4));
+        for (int e = 0; e < 32; ++e) v[e] = *reinterpret_cast<const float *>(sb + (kr0 + e) * 512);
         if (kbase + kr0 + 31 >= s_cache) {
             const float *blkp = a.vb + head_off * a.blk * (size_t)D + lq * 32 + lane;
 #pragma unroll
@@ -484,10 +496,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const UnitInfo x = decode(u);
         const int bf = u % NB;
         uint8_t *dst = stg + (size_t)bf * kUnit;
-        mbar_expect_tx(&full[bf], (uint32_t)kUnit);
         const int y = (int)(head_off * a.cap) + c0 + x.t * kTcKeys;
-        if (x.v) tma_load_3d(dst, &P.vmap, &full[bf], 0, x.h * kBoxes, y, pol);
-        else tma_load_3d(dst, &P.kmap, &full[bf], 0, y, x.h * kBoxes, pol);
+        if (x.v) {
+            load_v(dst, &full[bf], y, x.h);
+        } else {
+            mbar_expect_tx(&full[bf], (uint32_t)kUnit);
+            tma_load_3d(dst, &P.kmap, &full[bf], 0, y, x.h * kBoxes, pol);
+        }
     };
 
     // Q rows are loaded before the first TMA boxes are issued, so they do not queue behind them.
@@ -708,6 +723,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 // kBoxes * kr + gsel, swizzled by the line index
                 const uint8_t *sb = st + gsel * 128;
                 auto staged = [&](int kr, int k7) -> float {    // k7 = kr & 7, known statically
+                    if constexpr (D == 128) {   // one bulk copy: row kr as copied, unswizzled
+                        if constexpr (KVB) {
+                            const uint16_t bits = *reinterpret_cast<const uint16_t *>(st + kr * 256 + dd * 2);
+                            return __uint_as_float((uint32_t)bits << 16);
+                        } else {
+                            return *reinterpret_cast<const float *>(st + kr * 512 + dd * 4);
+                        }
+                    }
                     const int x = (kBoxes * k7 + gsel) & 7;
                     if constexpr (KVB) {
                         const uint16_t bits = *reinterpret_cast<const uint16_t *>(
