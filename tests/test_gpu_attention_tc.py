@@ -234,5 +234,15 @@ def test_attention_streamed_rescales_the_accumulator():
         assert rel_err(got[b], ref) <= ATTN_TOL, f"sequence {b}"
 
 
+def test_attention_head_dim_256_long_chunks_run_in_passes():
+    """8 sequences x 2 KV heads of head_dim 256 (MTP MoE heads) over 16000 keys: 9 chunks of 14
+    tiles per head (144 CTAs), above the 6 tiles of scores TMEM holds next to the operands and
+    both output halves at 16 query rows: three passes merged in registers."""
+    assert _tc_chunk_keys(8, 2, 16000) == 14 * 128
+    seq = [16000, 15999, 12000, 1, 0, 8191, 14336, 13001]
+    names = _attention_case(8, 1, 16, 2, 256, seq, 16000, False, False, seed=256)
+    assert "attn_tc_kernel" in names
+
+
 def test_attention_no_visible_keys_gives_zeros():
     _attention_case(1, 2, 4, 2, 128, [0], 64, False, False, seed=1)
