@@ -28,12 +28,12 @@
 // staging buffer and read by the MMA through a shared-memory descriptor, which leaves TMEM to the
 // K units and lets the V units of old cache rows be prepared before the wait too.
 //
-// A chunk's scores stay in TMEM, up to (512 - 256 - halves*2NP)/2NP tiles per pass (256 columns
-// hold the converted operands), so the softmax maximum is exact per pass: pass 1 takes the row
-// maxima, pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory). The first V
-// units of a pass (as many as there are operand regions) are converted before the softmax, while
-// the score MMAs finish; the rest right after their tile's probabilities. A longer chunk runs in
-// several passes whose (max, sum, o) are merged in registers, rescaled once per pass.
+// A chunk of one or two tiles keeps all its scores in TMEM (256 columns hold the converted
+// operands, the rest the scores and the output), so its softmax maximum is exact: pass 1 takes
+// the row maxima, pass 2 turns each tile into probabilities (BF16 hi/lo in shared memory). The
+// first V units (as many as there are operand regions) are converted before the softmax, while
+// the score MMAs finish; the rest right after their tile's probabilities. Longer chunks stream
+// tile by tile (ST below).
 //
 // 544 threads: warps 0-15 convert, run the softmax and read out (warps w, w + 4, w + 8, w + 12
 // share TMEM lane quarter w % 4 and take one quarter of the columns, rows or keys); thread 0 also
@@ -205,10 +205,9 @@ struct AttnTcParams {
     AttnArgs a;
 };
 
-// MP: the chunk may need several passes (instantiated only for chunks longer than one pass).
 // KVB: the cache holds BF16 (no lo half: two MMAs per K step, and twice as many half-size
 // staging buffers in the same shared memory).
-// ST: chunks longer than two tiles of a cache with head_dim 128, streamed tile by tile (no
+// ST: chunks longer than two tiles, streamed tile by tile (no
 // passes): units in the order K0, K1, V0, K2, V1, ..., so the score MMAs of tile t + 1 run while
 // the warps take the softmax of tile t; scores alternate between two TMEM buffers; the output
 // accumulator stays in TMEM across the tiles with a lazily moved reference maximum per row (it is
@@ -222,11 +221,11 @@ struct AttnTcParams {
 // once K unit 0 is in TMEM. With the TMEM regions left to the K units, the V units of tiles that
 // predate the round are converted before the wait as well, and after it only q, the scores, the
 // softmax and the products remain (plus the units of tiles holding new rows).
-template <int D, int NP, int NBUF, bool MP, bool KVB, bool VS, bool ST = false>
+template <int D, int NP, int NBUF, bool KVB, bool VS, bool ST = false>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
     DF_TRACE_KERNEL(TK_ATTN_TC);
-    static_assert(!VS || (D == 128 && NBUF == 3 && !MP && !KVB), "in-place V operands");
-    static_assert(!ST || (D == 128 && !MP && !VS), "streamed tiles");
+    static_assert(!VS || (D == 128 && NBUF == 3 && !KVB), "in-place V operands");
+    static_assert(!ST || !VS, "streamed tiles");
     constexpr int NB = KVB ? 2 * NBUF : NBUF;            // staging buffers
     constexpr int kUnit = KVB ? kF32Unit / 2 : kF32Unit;  // bytes of one staged unit
     constexpr int kBoxes = kUnit / kBoxBytes;             // TMA boxes per unit
@@ -245,7 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint8_t *qsm = sm + NB * kUnit;                     // [NH] stacked hi/lo Q operands
     uint8_t *psm = qsm + NH * 2 * kQBytes;              // stacked hi/lo P operand (second buffer)
     float *red = reinterpret_cast<float *>(psm + (VS ? 0 : 2 * kQBytes));   // [4][NP] maxima, [4][NP] sums
-    float *mrun = red + 8 * NP;                                  // [NP] running row maxima
+    float *mrun = red + 8 * NP;                                  // [NP] row maxima of the partials
     uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NB] staging landed
     uint64_t *aready = full + NB;     // [NA] region converted (8 warp arrivals)
     uint64_t *afree = aready + NA;    // [NA] MMAs reading the region done
@@ -438,11 +437,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (warp == 0) tmem_dealloc(tmem, kTmemCols);
         return;
     }
-    // A chunk longer than the score columns runs in passes of at most max_tp tiles; each pass
-    // has an exact maximum and its output is merged into running (max, sum, o) registers.
+    // One pass holds at most max_tp tiles of scores; longer chunks are streamed (ST).
     const int max_tp = (kTmemCols - kACols - NH * NS) / NS;
-    const int n_pass = MP ? (n_tiles + max_tp - 1) / max_tp : 1;
-    if (!MP && !ST && (n_tiles > max_tp || (VS && n_tiles > 2))) {   // the host plans within bounds
+    if (!ST && (n_tiles > max_tp || (VS && n_tiles > 2))) {   // the host plans within bounds
         if (tid == 0) set_status(a.status, DF_ESHAPE);
         tc_fence_before();
         __syncthreads();
@@ -453,26 +450,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         for (int i = tid; i < R * (D + 2); i += kTcThreads) part[i] = (i % (D + 2)) == D ? -INFINITY : 0.f;
         return;
     }
-    const int tpp = (n_tiles + n_pass - 1) / n_pass;    // tiles per pass (the last may be short)
-    const int upp = 2 * tpp * NH;                        // units per full pass
     const int nU = 2 * n_tiles * NH;
-    const bool multi = MP && n_pass > 1;
-    // Unit u of pass p: the pass's K units (tile-major, then 128-wide half), then its V units.
+    // Unit u: the chunk's K units (tile-major, then 128-wide half), then its V units (ST: below).
     struct UnitInfo {
         int t0, nt, v, t, h;
     };
     auto decode = [&](int u) -> UnitInfo {
         UnitInfo x;
         if constexpr (ST) {
-            // K0, then per tile t: K(t + 1) when it exists, V(t)
+            // slots K0, then per tile t: K(t + 1) when it exists, V(t); a slot is NH units, one
+            // per 128-wide half of the head dim
             x.t0 = 0;
             x.nt = n_tiles;
-            x.h = 0;
-            const int t = (u - 1) >> 1;
-            if (u == 0) {
+            x.h = u % NH;
+            const int sl = u / NH;
+            const int t = (sl - 1) >> 1;
+            if (sl == 0) {
                 x.v = 0;
                 x.t = 0;
-            } else if (((u - 1) & 1) == 0 && t + 1 < n_tiles) {
+            } else if (((sl - 1) & 1) == 0 && t + 1 < n_tiles) {
                 x.v = 0;
                 x.t = t + 1;
             } else {
@@ -481,10 +477,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             }
             return x;
         }
-        const int p = min(u / upp, n_pass - 1);
-        x.t0 = p * tpp;
-        x.nt = min(n_tiles, x.t0 + tpp) - x.t0;
-        int local = u - p * upp;
+        x.t0 = 0;
+        x.nt = n_tiles;
+        int local = u;
         x.v = local >= x.nt * NH;
         if (x.v) local -= x.nt * NH;
         x.t = x.t0 + local / NH;
@@ -564,13 +559,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const uint32_t ocol = (uint32_t)(kTmemCols - kACols - NH * NS);   // O^T accumulators
     // P operand of tile t. One pass: two buffers in turn, buffer 0 reusing the Q operands' space
     // (every score MMA has completed before the first P is written), buffer 1 following it.
-    // Several passes: Q stays live, so one buffer after the Q operands. VS: buffer 1 is the staging
+    // Streamed: Q stays live, so one buffer after the Q operands. VS: buffer 1 is the staging
     // buffer of K unit 1, read into TMEM before the score MMAs complete.
-    auto p_idx = [&](int t) -> int { return (multi || ST) ? 0 : (t & 1); };
-    auto p_phase = [&](int t) -> uint32_t { return (uint32_t)(((multi || ST) ? t : (t >> 1)) & 1); };
+    auto p_idx = [&](int t) -> int { return ST ? 0 : (t & 1); };
+    auto p_phase = [&](int t) -> uint32_t { return (uint32_t)((ST ? t : (t >> 1)) & 1); };
     auto p_buf = [&](int t) -> uint32_t {
         if (VS) return (t & 1) ? smem_u32(stg + kUnit) : smem_u32(qsm);
-        return (multi || ST) ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
+        return ST ? smem_u32(psm) : smem_u32(qsm) + (uint32_t)((t & 1) * 2 * kQBytes);
     };
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NS >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
@@ -651,8 +646,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 const bool last_of_tile = x.h == NH - 1;
                 const bool last_of_pass = last_of_tile && x.t == x.t0 + x.nt - 1;
                 if (!x.v) {
-                    if (ST) mma_commit(&vready[x.t & 1]);
-                    else if (last_of_pass) mma_commit(sdone);
+                    if (ST) {
+                        if (last_of_tile) mma_commit(&vready[x.t & 1]);
+                    } else if (last_of_pass) {
+                        mma_commit(sdone);
+                    }
                 } else {
                     if (last_of_tile) mma_commit(&pfree[p_idx(x.t)]);
                     if (last_of_pass) mma_commit(odone);
@@ -789,17 +787,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             return !(a.causal_block && key >= S_cache && key - S_cache > row / rep);
         };
         float Mrow[NPH], lsum[NPH];
-        float lrun[MP ? NPH : 1], orun[MP ? NH : 1][MP ? NPH : 1];
 #pragma unroll
         for (int r = 0; r < NPH; ++r) lsum[r] = 0.f;
-        if constexpr (MP) {
-#pragma unroll
-            for (int r = 0; r < NPH; ++r) {
-                lrun[r] = 0.f;
-#pragma unroll
-                for (int h = 0; h < NH; ++h) orun[h][r] = 0.f;
-            }
-        }
         if (tid < NP) mrun[tid] = -INFINITY;
 
         // VS: softmax pass 1 of the chunk's tiles pt0 .. pt0 + nt - 1: exact row maxima into Mrow
@@ -837,7 +826,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // VS: pass 2 for tile t (the tl-th of its pass): probabilities -> BF16 hi/lo P operand,
         // once the P.V MMAs that last read this buffer are done
         auto write_p = [&](int t, int tl) {
-            const int prev = multi ? t - 1 : t - 2;
+            const int prev = t - 2;
             if (prev >= 0) {
                 mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
                 tc_fence_after();
@@ -889,22 +878,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tc_fence_after();
             DF_TRACE_MARK(tid == 0, 5);
         }
-        // Per pass: the K units, then as many V units as there are operand regions (their regions
-        // are freed by the score MMAs alone), then the softmax; the probabilities of a tile are
-        // written before its first V unit that was not converted ahead.
         if constexpr (ST) {
             constexpr float kTau = 8.f;   // log2 units: probabilities stay below 2^8
             float mref[NPH];
 #pragma unroll
             for (int r = 0; r < NPH; ++r) mref[r] = -INFINITY;
-            if (n_early == 0) convert(0);                          // K0
+            auto convert_slot = [&](int sl) {
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+                    if (sl * NH + h >= n_early) convert(sl * NH + h);   // early units: done
+            };
+            convert_slot(0);                                       // K0
             for (int t = 0; t < n_tiles; ++t) {
                 const bool more = t + 1 < n_tiles;
                 DF_TRACE_MARK(tid == 0 && t == 4, 16);
                 DF_TRACE_MARK(tid == 0 && t == 5, 23);
-                if (more) convert(2 * t + 1);                      // K(t + 1)
+                if (more) convert_slot(2 * t + 1);                 // K(t + 1)
                 DF_TRACE_MARK(tid == 0 && t == 4, 17);
-                convert(more ? 2 * t + 2 : 2 * t + 1);             // V(t)
+                convert_slot(more ? 2 * t + 2 : 2 * t + 1);        // V(t)
                 DF_TRACE_MARK(tid == 0 && t == 4, 18);
                 // scores of tile t -> its row maxima (max over the four lane quarters)
                 mbar_wait(&vready[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, a.status);
@@ -943,23 +934,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
                 for (int r = 0; r < NPH; ++r) resc |= mref[r] != -INFINITY && mn[r] > mref[r] + kTau;
                 if (resc) {
-                    float oh[NPH], ol[NPH];
-                    tmem_rows<NPH>(tmem + lane_addr + ocol + r0, oh);
-                    tmem_rows<NPH>(tmem + lane_addr + ocol + NP + r0, ol);
-                    uint32_t wh[NPH], wl[NPH];
+                    float f[NPH];
 #pragma unroll
                     for (int r = 0; r < NPH; ++r) {
-                        const float f = (mref[r] != -INFINITY && mn[r] > mref[r] + kTau) ? ex2(mref[r] - mn[r]) : 1.f;
-                        wh[r] = __float_as_uint(oh[r] * f);
-                        wl[r] = __float_as_uint(ol[r] * f);
-                        lsum[r] *= f;
+                        f[r] = (mref[r] != -INFINITY && mn[r] > mref[r] + kTau) ? ex2(mref[r] - mn[r]) : 1.f;
+                        lsum[r] *= f[r];
                     }
 #pragma unroll
-                    for (int j = 0; j < NPH; j += 4) {
-                        const uint32_t h4[4] = {wh[j], wh[j + 1], wh[j + 2], wh[j + 3]};
-                        const uint32_t l4[4] = {wl[j], wl[j + 1], wl[j + 2], wl[j + 3]};
-                        tmem_st4(tmem + lane_addr + ocol + r0 + j, h4);
-                        tmem_st4(tmem + lane_addr + ocol + NP + r0 + j, l4);
+                    for (int h = 0; h < NH; ++h) {
+                        const uint32_t oc = ocol + (uint32_t)(h * NS);
+                        float oh[NPH], ol[NPH];
+                        tmem_rows<NPH>(tmem + lane_addr + oc + r0, oh);
+                        tmem_rows<NPH>(tmem + lane_addr + oc + NP + r0, ol);
+                        uint32_t wh[NPH], wl[NPH];
+#pragma unroll
+                        for (int r = 0; r < NPH; ++r) {
+                            wh[r] = __float_as_uint(oh[r] * f[r]);
+                            wl[r] = __float_as_uint(ol[r] * f[r]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < NPH; j += 4) {
+                            const uint32_t h4[4] = {wh[j], wh[j + 1], wh[j + 2], wh[j + 3]};
+                            const uint32_t l4[4] = {wl[j], wl[j + 1], wl[j + 2], wl[j + 3]};
+                            tmem_st4(tmem + lane_addr + oc + r0 + j, h4);
+                            tmem_st4(tmem + lane_addr + oc + NP + r0 + j, l4);
+                        }
                     }
                     tmem_wait_st();
                 }
@@ -991,15 +990,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tc_fence_after();
             conv_sync();   // every warp has read the last tile's maxima: the read-out reuses red
         }
-        for (int p = 0; p < ((VS || ST) ? 0 : n_pass); ++p) {
-            const int pt0 = p * tpp, nt = min(n_tiles, pt0 + tpp) - pt0, ub = p * upp;
+        // One pass (one or two tiles): the K units, then as many V units as there are operand
+        // regions (their regions are freed by the score MMAs alone), then the softmax; the
+        // probabilities of a tile are written before its first V unit that was not converted
+        // ahead.
+        if constexpr (!VS && !ST) {
+            const int nt = n_tiles;
             const int nK = nt * NH, nV = nK, pre = min(NA, nV), pre_tiles = (pre + NH - 1) / NH;
-            int pdone = 0;   // tiles of the pass whose P operand is written
+            int pdone = 0;   // tiles whose P operand is written
             for (int i = 0; i <= nK + nV; ++i) {
                 int want = pdone;
                 if (i == nK + pre) {
-                    // softmax pass 1: exact row maxima over the pass's tiles
-                    mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
+                    // softmax pass 1: exact row maxima over the chunk's tiles
+                    mbar_wait(sdone, 0u, abort_flag, a.status);
                     tc_fence_after();
                     float mx[NPH];
 #pragma unroll
@@ -1009,7 +1012,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                         tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + r0, sh);
                         tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
                         tmem_ld_wait();
-                        const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
+                        const int key = c0 + tt * kTcKeys + lq * 32 + lane;
 #pragma unroll
                         for (int r = 0; r < NPH; ++r)
                             if (row_ok(key, r0 + r))
@@ -1029,8 +1032,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (; pdone < want; ++pdone) {
                     // pass 2 for tile t: probabilities -> BF16 hi/lo P operand, once the P.V MMAs
                     // that last read this buffer are done
-                    const int t = pt0 + pdone, tl = pdone;
-                    const int prev = multi ? t - 1 : t - 2;
+                    const int t = pdone;
+                    const int prev = t - 2;
                     if (prev >= 0) {
                         mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
                         tc_fence_after();
@@ -1038,8 +1041,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     float sv[NPH];
                     {
                         uint32_t sh[NPH], sl[NPH];
-                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
-                        tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + t * NS + r0, sh);
+                        tmem_ld_nowait<NPH>(tmem + lane_addr + t * NS + NP + r0, sl);
                         tmem_ld_wait();
 #pragma unroll
                         for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
@@ -1064,54 +1067,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     if (lane == 0) mbar_arrive(&pready[p_idx(t)]);
                 }
                 if (i == nK + nV) break;
-                if (ub + i >= n_early) convert(ub + i);   // the early units are converted already
+                if (i >= n_early) convert(i);   // the early units are converted already
             }
-            // end of a pass: its P.V products are complete
-            mbar_wait(odone, (uint32_t)(p & 1), abort_flag, a.status);
+            // its P.V products are complete
+            mbar_wait(odone, 0u, abort_flag, a.status);
             tc_fence_after();
-            if constexpr (MP) {
-                // merge the pass's (max, sum, o) into the running values
-#pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    float o[NPH], ol[NPH];
-                    tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + r0, o);
-                    tmem_rows<NPH>(tmem + lane_addr + ocol + h * NS + NP + r0, ol);
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) o[r] += ol[r];
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) {
-                        const float Mr = mrun[r0 + r], Mn = fmaxf(Mr, Mrow[r]);
-                        if (Mn == -INFINITY) continue;
-                        const float so = Mr == -INFINITY ? 0.f : ex2(Mr - Mn);
-                        const float sn = Mrow[r] == -INFINITY ? 0.f : ex2(Mrow[r] - Mn);
-                        orun[h][r] = orun[h][r] * so + o[r] * sn;
-                        if (h == NH - 1) {
-                            lrun[r] = lrun[r] * so + lsum[r] * sn;
-                            lsum[r] = 0.f;
-                        }
-                    }
-                }
-                conv_sync();                // everyone has read mrun before it moves
-                if (lq == 0 && lane == 0)
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) mrun[r0 + r] = fmaxf(mrun[r0 + r], Mrow[r]);
-                conv_sync();
-            }
         }
 
         // read-out: o of this thread's rows, row sums, maxima
-        if constexpr (MP) {
-            int row;
-            const float l = lane_reduce_rows<NPH, false>(lrun, lane, row);
-            if ((lane & (32 / NPH - 1)) == 0) red[4 * NP + lq * NP + r0 + row] = l;
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                const int d = h * 128 + lq * 32 + lane;
-#pragma unroll
-                for (int r = 0; r < NPH; ++r)
-                    if (r0 + r < R) part[(size_t)(r0 + r) * (D + 2) + d] = orun[h][r];
-            }
-        } else {
+        {
             int row;
             const float l = lane_reduce_rows<NPH, false>(lsum, lane, row);
             if ((lane & (32 / NPH - 1)) == 0) red[4 * NP + lq * NP + r0 + row] = l;
@@ -1186,33 +1150,26 @@ int launch_tc(const AttnArgs &a, cudaStream_t s) {
                        (uint64_t)D * eb, box_cols, unit_groups, 128));
     p.a = a;
     dim3 grid(a.n_chunks, a.nkv, a.B);
-    const bool one = a.chunk <= max_keys_one_pass;
-    if (a.kv_bf16) {
-        if constexpr (D == 128) {
-            if (a.chunk > 2 * kTcKeys)   // longer chunks: streamed tile by tile
-                return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true, false, true>,
-                                grid, dim3(kTcThreads), smem, s, p);
-        }
-        return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, true, false>, grid,
-                              dim3(kTcThreads), smem, s, p)
-                   : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, true, false>, grid,
-                              dim3(kTcThreads), smem, s, p);
-    }
+    // Chunks of more than two tiles stream tile by tile; shorter ones run in one pass (one or two
+    // tiles of scores fit TMEM beside the operands for every head dim and row count here), with
+    // the V operands in place for an F32 cache with head_dim 128.
+    static_assert(max_keys_one_pass >= 2 * kTcKeys, "two tiles in one pass");
+    if (a.chunk > 2 * kTcKeys)
+        return a.kv_bf16 ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false, true>,
+                                    grid, dim3(kTcThreads), smem, s, p)
+                         : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, true>,
+                                    grid, dim3(kTcThreads), smem, s, p);
+    if (a.kv_bf16)
+        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false>, grid,
+                        dim3(kTcThreads), smem, s, p);
     if constexpr (D == 128) {
-        if (a.chunk <= 2 * kTcKeys) {   // chunks of one or two tiles: V operands in place
-            constexpr size_t smem_vs = attn_tc_smem_bytes<D, NP, 3, true>();
-            static_assert(smem_vs <= 232448, "shared memory");
-            return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, 3, false, false, true>, grid,
-                            dim3(kTcThreads), smem_vs, s, p);
-        }
-        // longer chunks: streamed tile by tile
-        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false, true>,
-                        grid, dim3(kTcThreads), smem, s, p);
+        constexpr size_t smem_vs = attn_tc_smem_bytes<D, NP, 3, true>();
+        static_assert(smem_vs <= 232448, "shared memory");
+        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, 3, false, true>, grid,
+                        dim3(kTcThreads), smem_vs, s, p);
     } else {
-        return one ? launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false, false>, grid,
-                              dim3(kTcThreads), smem, s, p)
-                   : launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, true, false, false>, grid,
-                              dim3(kTcThreads), smem, s, p);
+        return launch_k("attn_tc_kernel", attn_tc_kernel<D, NP, NBUF, false, false>, grid,
+                        dim3(kTcThreads), smem, s, p);
     }
 }
 

@@ -234,13 +234,23 @@ def test_attention_streamed_rescales_the_accumulator():
         assert rel_err(got[b], ref) <= ATTN_TOL, f"sequence {b}"
 
 
-def test_attention_head_dim_256_long_chunks_run_in_passes():
+def test_attention_head_dim_256_long_chunks_streamed():
     """8 sequences x 2 KV heads of head_dim 256 (MTP MoE heads) over 16000 keys: 9 chunks of 14
-    tiles per head (144 CTAs), above the 6 tiles of scores TMEM holds next to the operands and
-    both output halves at 16 query rows: three passes merged in registers."""
+    tiles per head (144 CTAs), streamed tile by tile with both 128-wide halves of every K and V
+    tile, at 16 query rows."""
     assert _tc_chunk_keys(8, 2, 16000) == 14 * 128
     seq = [16000, 15999, 12000, 1, 0, 8191, 14336, 13001]
     names = _attention_case(8, 1, 16, 2, 256, seq, 16000, False, False, seed=256)
+    assert "attn_tc_kernel" in names
+
+
+def test_attention_head_dim_256_32_rows_streamed():
+    """head_dim 256 at 32 query rows (16 block rows x 2 query heads per KV head): two staging
+    buffers, the output halves and both score buffers fill TMEM; 3-tile chunks streamed, with
+    block rows, against the oracle."""
+    assert _tc_chunk_keys(8, 2, 3000 + 16) == 3 * 128
+    seq = [3000, 2999, 1, 0, 2500, 1777, 3000, 129]
+    names = _attention_case(8, 16, 4, 2, 256, seq, 3000, True, False, seed=2560)
     assert "attn_tc_kernel" in names
 
 

@@ -63,6 +63,16 @@ def test_bf16_kv_batched_streamed_chunks():
     assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
 
 
+def test_bf16_kv_head_dim_256_streamed_chunks():
+    """head_dim 256 with a BF16 cache: 8 sequences x 2 KV heads over ~6000 keys, 6-tile chunks
+    streamed tile by tile (both halves of each tile, four TMEM operand regions)."""
+    shape = TINY.with_(head_dim=256, n_q_heads=4, n_kv_heads=2, K=15, ctx=6000, batch=8,
+                       kv_bf16=True)
+    r = _run_forward(shape, [4, 1, 16, 0, 7, 3, 9, 2], seed=93)
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+
+
 def test_bf16_kv_rejects_unsupported_head_dim():
     shape = TINY.with_(kv_bf16=True)                  # head_dim 64
     with pytest.raises(B.DFlashError) as e:
