@@ -236,6 +236,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     constexpr int NPH = NP / kGroups;         // rows per thread in the softmax and read-out
     constexpr int kQBytes = NP * 256;         // NP rows x 128 BF16 (the hi or the lo rows)
     constexpr int NS = 2 * NP;                // MMA N: hi rows 0..NP-1 stacked on lo rows
+    // Unit conversion loops: a streamed chunk converts many units, so its loops are unrolled
+    // fully (more loads in flight per thread); the short forms convert a few units each and keep
+    // their code small (it is fetched cold).
+    constexpr int kConvUnroll = ST ? 4 : 2;
     const AttnArgs &a = P.a;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
@@ -678,14 +682,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             const float *blkp = (x.v ? a.vb : a.kb) + head_off * a.blk * (size_t)D + x.h * 128;
             const uint32_t ta = tmem + lane_addr + acol + (uint32_t)(r * kUCols + (kDT / 2) * grp);
             // 8 K values per step: 4 hi words at ta + 4*it, 4 lo words at ta + 64 + 4*it. Loops,
-            // not unrolled code: a CTA converts only a few units, so the instructions are fetched
-            // cold and their number, not their issue rate, sets the time.
+            // not unrolled code, where a CTA converts only a few units (its instructions are
+            // fetched cold and their number, not their issue rate, sets the time); unrolled when
+            // streaming (kConvUnroll).
             if (VS || !x.v) {
                 const int kr = lq * 32 + lane, key = kbase + kr;
                 const bool cached = key < S_cache;
                 const float *src = (!cached && key < c1) ? blkp + (size_t)(key - S_cache) * D + kDT * grp
                                                          : nullptr;
-#pragma unroll 2
+#pragma unroll kConvUnroll
                 for (int it = 0; it < kDT / 8; ++it) {
                     const int d0 = kDT * grp + 8 * it;            // first of the step's 8 dims
                     uint32_t hw[4], lw[4];
@@ -739,7 +744,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                             sb + kr * (kBoxes * 128) + (((col >> 2) ^ x) << 4) + (col & 3) * 4);
                     }
                 };
-#pragma unroll 2
+#pragma unroll kConvUnroll
                 for (int it = 0; it < kDT / 8; ++it) {
                     const int kr0 = kDT * grp + 8 * it;           // 8 keys, kr0 % 8 == 0
                     float v[8];
