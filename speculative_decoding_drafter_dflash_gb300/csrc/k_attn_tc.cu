@@ -252,10 +252,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint64_t *full = reinterpret_cast<uint64_t *>(mrun + NP);    // [NB] staging landed
     uint64_t *aready = full + NB;     // [NA] region converted (8 warp arrivals)
     uint64_t *afree = aready + NA;    // [NA] MMAs reading the region done
-    uint64_t *sdone = afree + NA;     // the pass's score MMAs done
+    uint64_t *sdone = afree + NA;     // one pass: every score MMA of the chunk done
     uint64_t *pready = sdone + 1;     // [2] P operand written (8 warp arrivals)
     uint64_t *pfree = pready + 2;     // [2] P.V MMAs reading the P buffer done
-    uint64_t *odone = pfree + 2;      // the pass's P.V MMAs done
+    uint64_t *odone = pfree + 2;      // every P.V MMA of the chunk done
     uint64_t *drain = odone + 1;      // every MMA issued has completed
     uint64_t *vready = drain + 1;     // [2] VS: V operand of tile t written (16 warp arrivals);
                                       // ST: score MMAs of the tiles t with t % 2 == i done
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     if (warp == kConvThreads / 32) {
         // MMA issuer: the products of unit u once its operand is in TMEM (and, for a V unit,
         // once its tile's P is in shared memory); commits free the operand region, the P buffer,
-        // and signal the end of a pass's scores and outputs.
+        // and signal the end of the chunk's scores (streamed: of each tile's) and outputs.
         if (lane == 0 && VS) {
             // VS: the score MMAs of every tile (K operands in TMEM regions t), then the P.V MMAs
             // of tile t with V^T from its staging buffer (hi half, then lo half)
@@ -648,16 +648,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 mma_commit(&afree[r]);
                 const bool last_of_tile = x.h == NH - 1;
-                const bool last_of_pass = last_of_tile && x.t == x.t0 + x.nt - 1;
+                const bool last_of_chunk = last_of_tile && x.t == x.t0 + x.nt - 1;
                 if (!x.v) {
                     if (ST) {
                         if (last_of_tile) mma_commit(&vready[x.t & 1]);
-                    } else if (last_of_pass) {
+                    } else if (last_of_chunk) {
                         mma_commit(sdone);
                     }
                 } else {
                     if (last_of_tile) mma_commit(&pfree[p_idx(x.t)]);
-                    if (last_of_pass) mma_commit(odone);
+                    if (last_of_chunk) mma_commit(odone);
                 }
             }
             // Every MMA this thread issued has completed once the drain barrier flips.
@@ -796,10 +796,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         for (int r = 0; r < NPH; ++r) lsum[r] = 0.f;
         if (tid < NP) mrun[tid] = -INFINITY;
 
-        // VS: softmax pass 1 of the chunk's tiles pt0 .. pt0 + nt - 1: exact row maxima into Mrow
-        // (the loop below keeps its own copy, which compiles to fewer spills there)
-        auto pass_max = [&](int p, int pt0, int nt) {
-            mbar_wait(sdone, (uint32_t)(p & 1), abort_flag, a.status);
+        // VS: softmax pass 1 over the chunk's nt tiles: exact row maxima into Mrow (the one-pass
+        // loop below keeps its own copy, which compiles to fewer spills there)
+        auto pass_max = [&](int nt) {
+            mbar_wait(sdone, 0u, abort_flag, a.status);
             tc_fence_after();
             DF_TRACE_MARK(tid == 0, 6);
             float mx[NPH];
@@ -812,7 +812,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 tmem_ld_nowait<NPH>(tmem + lane_addr + tt * NS + NP + r0, sl);
                 tmem_ld_wait();
                 DF_TRACE_MARK(tid == 0 && tt == 0, 10);
-                const int key = c0 + (pt0 + tt) * kTcKeys + lq * 32 + lane;
+                const int key = c0 + tt * kTcKeys + lq * 32 + lane;
 #pragma unroll
                 for (int r = 0; r < NPH; ++r)
                     if (row_ok(key, r0 + r))
@@ -828,19 +828,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 Mrow[r] = fmaxf(fmaxf(red[r0 + r], red[NP + r0 + r]),
                                 fmaxf(red[2 * NP + r0 + r], red[3 * NP + r0 + r]));
         };
-        // VS: pass 2 for tile t (the tl-th of its pass): probabilities -> BF16 hi/lo P operand,
-        // once the P.V MMAs that last read this buffer are done
-        auto write_p = [&](int t, int tl) {
-            const int prev = t - 2;
-            if (prev >= 0) {
-                mbar_wait(&pfree[p_idx(t)], p_phase(prev), abort_flag, a.status);
-                tc_fence_after();
-            }
+        // VS: pass 2 for tile t (0 or 1; each P buffer is written once): probabilities -> BF16
+        // hi/lo P operand
+        auto write_p = [&](int t) {
             float sv[NPH];
             {
                 uint32_t sh[NPH], sl[NPH];
-                tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + r0, sh);
-                tmem_ld_nowait<NPH>(tmem + lane_addr + tl * NS + NP + r0, sl);
+                tmem_ld_nowait<NPH>(tmem + lane_addr + t * NS + r0, sh);
+                tmem_ld_nowait<NPH>(tmem + lane_addr + t * NS + NP + r0, sl);
                 tmem_ld_wait();
                 DF_TRACE_MARK(tid == 0 && t == 0, 0);
 #pragma unroll
@@ -872,10 +867,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             for (int t = n_early; t < n_tiles; ++t) convert(t);
             for (int t = n_early; t < n_tiles; ++t)
                 convert_vs(t, t ? 0 : 2, (uint32_t)t, c0 + t * kTcKeys, S_cache, c1);
-            pass_max(0, 0, n_tiles);
+            pass_max(n_tiles);
             DF_TRACE_MARK(tid == 0, 3);
             for (int t = 0; t < n_tiles; ++t) {
-                write_p(t, t);
+                write_p(t);
                 DF_TRACE_MARK(tid == 0 && t == 0, 8);
             }
             DF_TRACE_MARK(tid == 0, 4);
