@@ -334,6 +334,18 @@ def test_full_size_round_k15_ctx4096():
 
 
 @pytest.mark.slow
+def test_full_size_forward_ctx32768_streamed_attention():
+    """The DFlash shape at a 32K-key context: every layer's attention streams 14-tile chunks (19
+    chunks x 8 KV heads, one wave) with the new context rows and the block rows in the last
+    chunk; h_final and the appended cache length against the oracle."""
+    shape = DFLASH_K15.with_(ctx=32768)
+    r = _run_forward(shape, [5], seed=6)
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+    assert list(synth.host(r["cache"].seq_len)) == list(r["seq_ref"])
+
+
+@pytest.mark.slow
 def test_batched_round_b8_ctx1024():
     """The batched sweep shape: 8 sequences x 16 block rows (128 lm_head rows, 256 projection
     tokens with the context rows), K=15, context 1024, ragged new-row counts."""
