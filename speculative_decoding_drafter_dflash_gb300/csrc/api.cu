@@ -1550,6 +1550,7 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
         key = fnv(key, cache->k, sizeof(float *) * cfg->n_layers);
         key = fnv(key, cache->v, sizeof(float *) * cfg->n_layers);
         key = fnv(key, host_bufs, sizeof(host_bufs));
+        key = fnv(key, dev_of, sizeof(dev_of));   // a buffer pinned again maps elsewhere
         const long long scal[] = {n_new_max, B, K, n_eos, (long long)ws_bytes};
         key = fnv(key, scal, sizeof(scal));
         key = fnv(key, &ws, sizeof(ws));
