@@ -1468,10 +1468,8 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
     // Graph form: the small inputs and all outputs by one word-copy kernel each, the target rows
     // read by the round's first kernel, all straight from and to the mapped host buffers.
     auto enqueue_mapped = [&](cudaStream_t s) -> int {
-        cudaError_t e = cudaMemsetAsync(d_st, 0, sizeof(int32_t), s);
-        if (e != cudaSuccess) return fail(DF_ECUDA, "host round staging: %s", cudaGetErrorString(e));
         WordCopyList in;
-        auto add = [](WordCopyList &l, const void *src, void *dst, long long words) {
+        auto add = [](WordCopyList &l, const void *src, void *dst, long long words) {   // src null: zeros
             if (words <= 0) return;
             l.src[l.n] = src;
             l.dst[l.n] = dst;
@@ -1483,6 +1481,7 @@ int df_draft_round_host(const df_dflash_config *cfg, const df_dflash_weights *w,
         add(in, dev_of[3], d_tgt, (long long)B * blk);
         add(in, dev_of[4], d_eos, n_eos);
         add(in, dev_of[5], d_tsl, B);
+        add(in, nullptr, d_st, 1);   // the status word starts at DF_OK
         DF_TRY(launch_word_copy(in, s));
         // the row prologue reads the new target rows straight from the mapped host buffer
         DF_TRY(df_draft_round(cfg, w, cache, d_last,

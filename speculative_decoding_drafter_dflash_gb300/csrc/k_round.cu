@@ -148,10 +148,10 @@ __global__ void word_copy_kernel(WordCopyList l) {
     pdl_trigger();
     pdl_wait();
     for (int r = 0; r < l.n; ++r) {
-        const uint32_t *src = static_cast<const uint32_t *>(l.src[r]);
+        const uint32_t *src = static_cast<const uint32_t *>(l.src[r]);   // null: zeros
         uint32_t *dst = static_cast<uint32_t *>(l.dst[r]);
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < l.words[r]; i += gridDim.x * blockDim.x)
-            dst[i] = src[i];
+            dst[i] = src ? src[i] : 0u;
     }
 }
 
