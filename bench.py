@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--batch", type=int, default=1, help="sequences of --profile-case round, trace, layout, gemms and lm_head")
     ap.add_argument("--ctx", type=int, default=0, help="cache rows of --profile-case round")
-    ap.add_argument("--vocab", type=int, default=0, help="lm_head rows of --profile-case lm_head")
+    ap.add_argument("--vocab", type=int, default=0, help="lm_head rows of --profile-case lm_head and round")
+    ap.add_argument("--layers", type=int, default=0, help="drafter layers of --profile-case round")
     ap.add_argument("--trace-dump", default=None, help="--profile-case trace: save the records")
 
     ap.add_argument("--profile-case", choices=["lm_head", "round", "gemms", "sweep", "sweep_bf16kv", "mtp",
@@ -1318,9 +1319,11 @@ def profile_case(args):
             del W, X, Y, ws
         print(json.dumps({"profile_case": "gemms", "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count, **res}))
     else:
-        # Per-kernel GPU time inside eager rounds of the workload (library event profiler).
+        # Per-kernel GPU time inside eager rounds of the workload (library event profiler);
+        # --layers and --vocab shrink the model for captures that replay every kernel.
         from speculative_decoding_drafter_dflash_gb300 import synth
-        s = s.with_(batch=args.batch, ctx=args.ctx or s.ctx)
+        s = s.with_(batch=args.batch, ctx=args.ctx or s.ctx, n_layers=args.layers or s.n_layers,
+                    vocab=args.vocab or s.vocab)
         Bn = s.batch
         acc, n_new = variants(s)
         nmax = s.block
