@@ -45,6 +45,14 @@ __device__ __forceinline__ uint4 ld_w(const uint16_t *p, bool ok) {
     return ok ? ld_stream_u4(p) : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Asks L2 for n_bytes of weights at p, one 128-byte line per lane and step (no registers held):
+// used before a kernel's wait on its predecessor, for weights that do not depend on it.
+__device__ __forceinline__ void prefetch_l2(const void *p, size_t n_bytes, int lane) {
+    const char *c = static_cast<const char *>(p);
+    for (size_t off = (size_t)lane * 128; off < n_bytes; off += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+}
+
 // Router: one warp per weight row (E router rows, then the shared-expert gate row), against
 // all T input rows at once. The last CTA to arrive selects the experts.
 __global__ void __launch_bounds__(kMoeThreads) moe_router_kernel(MoeArgs a) {
@@ -165,14 +173,21 @@ __global__ void __launch_bounds__(kMoeThreads) moe_router_kernel(MoeArgs a) {
 // Gate/up: one warp per (row t, slot j, intermediate index r). act[t, j, r] = silu(g) * u.
 __global__ void __launch_bounds__(kMoeThreads) moe_gate_up_kernel(MoeArgs a) {
     DF_TRACE_KERNEL(TK_MOE_GATE_UP);
-    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int S = a.k + 1, Imax = max(a.Ie, a.Is);
     const long long task = (long long)blockIdx.x * kMoeWarps + warp;
     const int r = (int)(task % Imax);
     const long long q = task / Imax;
     const int j = (int)(q % S), t = (int)(q / S);
+    // The shared expert does not depend on the router: its rows are requested before the wait.
+    if (t < a.T && j == a.k && r < a.Is) {
+        prefetch_l2(a.sh_g + (size_t)r * a.H, (size_t)a.H * 2, lane);
+        prefetch_l2(a.sh_u + (size_t)r * a.H, (size_t)a.H * 2, lane);
+    }
     pdl_wait();
+    // Released only past the wait: when the down kernel starts, the router (which wrote the
+    // expert choice) has completed, so down can request its experts' rows before its own wait.
+    pdl_trigger();
     if (t >= a.T) return;
     const int I = j < a.k ? a.Ie : a.Is;
     if (r >= I) return;
@@ -226,9 +241,21 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(MoeArgs a) {
     const int hb = (int)(task % nhb);
     const long long q = task / nhb;
     const int t = (int)(q % a.T), j = (int)(q / a.T);
+    const int I = j < a.k ? a.Ie : a.Is;
+    const int h0 = hb * kDownRows;
+    if (j < S && h0 < a.H) {
+        // The router has completed (the gate/up kernel releases this one only past its own
+        // wait): request this warp's rows of the chosen expert before waiting for the
+        // activations. The choice is read again after the wait; a stale one costs a prefetch.
+        const uint16_t *b = a.sh_d;
+        if (j < a.k) {
+            const int e = __ldcg(a.sel + (size_t)t * a.k + j);
+            b = e >= 0 && e < a.E ? a.exp_down + (size_t)e * a.H * a.Ie : nullptr;
+        }
+        if (b) prefetch_l2(b + (size_t)h0 * I, (size_t)min(kDownRows, a.H - h0) * I * 2, lane);
+    }
     pdl_wait();
     if (j >= S) return;
-    const int I = j < a.k ? a.Ie : a.Is;
     const uint16_t *base;
     if (j < a.k) {
         const int e = a.sel[(size_t)t * a.k + j];
@@ -241,7 +268,6 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(MoeArgs a) {
         base = a.sh_d;
     }
     const float *act = a.act + ((size_t)t * S + j) * Imax;
-    const int h0 = hb * kDownRows;
     const int nch = I >> 3;
     float acc[kDownRows];
 #pragma unroll
