@@ -51,7 +51,7 @@ namespace {
 
 constexpr int kGroups = 4;                    // converting warps per TMEM lane quarter
 constexpr int kConvThreads = 128 * kGroups;   // warps 0-15: convert, softmax, read-out
-constexpr int kTcThreads = kConvThreads + 32;  // warp 16: MMA issue
+constexpr int kTcThreads = kConvThreads + 64;  // warp 16: MMA issue; warp 17: TMA issue
 constexpr int kDT = 128 / kGroups;            // K values of a unit row per converting thread
 constexpr int kTcKeys = 128;                  // keys per tile
 constexpr int kTmemCols = 512;
@@ -259,7 +259,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     uint64_t *drain = odone + 1;      // every MMA issued has completed
     uint64_t *vready = drain + 1;     // [2] VS: V operand of tile t written (16 warp arrivals);
                                       // ST: score MMAs of the tiles t with t % 2 == i done
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(vready + 2);
+    uint64_t *bempty = vready + 2;    // [NB] staging buffer read by every converting warp (16
+                                      // warp arrivals): the TMA warp may refill it
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bempty + NB);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -321,6 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             for (int i = 0; i < 2; ++i) mbar_init(&vready[i], kConvThreads / 32);
         if (ST)
             for (int i = 0; i < 2; ++i) mbar_init(&vready[i], 1);
+        for (int i = 0; i < NB; ++i) mbar_init(&bempty[i], kConvThreads / 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int t = 0; t < n_early; ++t) {
@@ -410,7 +413,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&aready[u]);
+            if (lane == 0) {
+                mbar_arrive(&aready[u]);
+                if constexpr (!VS) mbar_arrive(&bempty[u]);
+            }
             if (VS && u == 0 && n_early == 2) {
                 conv_sync();   // K unit 0 is read: buffer 0 takes V unit 1
                 if (tid == 0) {
@@ -521,8 +527,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             qx[i][4] = v.x; qx[i][5] = v.y; qx[i][6] = v.z; qx[i][7] = v.w;
         }
     }
-    // the early units' buffers are free again: the staging runs NB units ahead of them
+    // the early units' buffers are free again: the staging runs NB units ahead of them (the
+    // first NB by thread 0 here, the others by the TMA warp)
     int issued = n_early;   // TMA units issued (thread 0)
+    const int n_first = max(n_early, min(NB + n_early, nU));
     if (tid == 0) {
         if constexpr (VS) {
             // the units not requested before the wait: K units into buffers t, V unit 0 into
@@ -665,6 +673,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             mbar_drain(drain, 0);
         }
         __syncwarp();
+    } else if (warp == kConvThreads / 32 + 1) {
+        // TMA issuer: the units after the first NB, each into its staging buffer once every
+        // converting warp has read the unit before it there. Issuing here keeps a copy that
+        // waits for room in the copy engine off the converting warps' path.
+        if constexpr (!VS) {
+            if (lane == 0) {
+                int u = n_first;
+                for (; u < nU; ++u) {
+                    if (!mbar_wait(&bempty[u % NB], (uint32_t)(((u / NB) - 1) & 1), abort_flag, a.status))
+                        break;
+                    issue(u);
+                }
+                // after an abort: let every copy still in flight land before the CTA exits
+                for (int j = max(0, u - NB); j < u; ++j) mbar_drain(&full[j % NB], (uint32_t)((j / NB) & 1));
+            }
+            __syncwarp();
+        }
     } else {
         // Unit u -> BF16 operand in TMEM region u % NA. K unit: this thread's lane is key
         // 32*lq + lane, its columns the dims [kDT*grp, kDT*grp + kDT) of the unit. V unit: its
@@ -772,16 +797,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aready[r]);
-            conv_sync();   // every warp has read the staging buffer: refill it
             if constexpr (VS) {
+                conv_sync();   // every warp has read the staging buffer: refill it
                 if (tid == 0 && x.t == 0 && n_tiles == 2) {   // with V unit 1
                     fence_proxy_async_smem();
                     stage_v(0, (int)(head_off * a.cap) + c0 + kTcKeys);
                 }
-            } else if (tid == 0 && issued < nU) {
-                fence_proxy_async_smem();
-                issue(issued);
-                ++issued;
+            } else {
+                // this warp has read the staging buffer; the TMA warp refills it once all have
+                if (lane == 0) mbar_arrive(&bempty[bf]);
             }
         };
 
@@ -1112,9 +1136,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             if constexpr (VS) {
                 for (int j = 0; j < 3; ++j)
                     if (nis[j] > 0) mbar_drain(&full[j], (uint32_t)((nis[j] - 1) & 1));
-            } else {
-                for (int j = max(0, issued - NB); j < issued; ++j)
-                    mbar_drain(&full[j % NB], (uint32_t)((j / NB) & 1));
             }
         }
     }
