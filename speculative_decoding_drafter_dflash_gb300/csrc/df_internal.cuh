@@ -138,8 +138,11 @@ constexpr uint32_t kTraceMark = 1000;   // kids of DF_TRACE_MARK points: kTraceM
 // (first P operand written), 4 (all P operands), 5 (P.V done), 9 (partial outputs stored);
 // streamed attention, tile 4: 16 (its iteration starts), 17 (K of tile 5 converted), 18 (V of
 // tile 4 converted), 19 (its scores ready), 20 (its row maxima), 21 (P.V of tile 3 done), 22 (its
-// P operand written), and 23 (the iteration of tile 5 starts); projection 11 (producer past the
-// wait), 12 (an accumulator ready), 13 (epilogue done).
+// P operand written), and 23 (the iteration of tile 5 starts); inside those two conversions (the
+// ids of the one-pass points, which a streamed launch never reaches) 3, 4, 5 (K of tile 5: copy
+// landed, its TMEM region free, converted) and 7, 8, 0 (the same for V of tile 4), and the TMA
+// warp's issue of those two units, 14 / 6 (K: before / after) and 15 / 10 (V); projection 11
+// (producer past the wait), 12 (an accumulator ready), 13 (epilogue done).
 #if DF_TRACE
 extern __device__ TraceRec g_trace[kTraceMax];
 extern __device__ unsigned g_trace_n;

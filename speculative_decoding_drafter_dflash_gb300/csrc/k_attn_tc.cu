@@ -35,10 +35,13 @@
 // the score MMAs finish; the rest right after their tile's probabilities. Longer chunks stream
 // tile by tile (ST below).
 //
-// 544 threads: warps 0-15 convert, run the softmax and read out (warps w, w + 4, w + 8, w + 12
-// share TMEM lane quarter w % 4 and take one quarter of the columns, rows or keys); thread 0 also
-// issues the TMA loads; warp 16 issues the MMAs. Block rows (keys past the cache rows) come from
-// kb/vb with plain loads during the conversion; keys past the chunk are converted as zeros.
+// 576 threads: warps 0-15 convert, run the softmax and read out (warps w, w + 4, w + 8, w + 12
+// share TMEM lane quarter w % 4 and take one quarter of the columns, rows or keys); warp 16
+// issues the MMAs; thread 0 issues the first TMA loads and warp 17 the others, each once every
+// converting warp has arrived on its buffer's "read" barrier (an issue can wait for room in the
+// copy engine; here that wait is off the converting warps' path). VS keeps thread 0 issuing its
+// few loads. Block rows (keys past the cache rows) come from kb/vb with plain loads during the
+// conversion; keys past the chunk are converted as zeros.
 #include <cuda_bf16.h>
 #include <string.h>
 
@@ -113,7 +116,7 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// Barrier of the converting warps (named barrier 1; the MMA warp does not take part).
+// Barrier of the converting warps (named barrier 1; the MMA and TMA warps do not take part).
 __device__ __forceinline__ void conv_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConvThreads) : "memory");
 }
@@ -683,7 +686,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (; u < nU; ++u) {
                     if (!mbar_wait(&bempty[u % NB], (uint32_t)(((u / NB) - 1) & 1), abort_flag, a.status))
                         break;
+                    DF_TRACE_MARK(ST && u == 9, 14);
+                    DF_TRACE_MARK(ST && u == 10, 15);
                     issue(u);
+                    DF_TRACE_MARK(ST && u == 9, 6);
+                    DF_TRACE_MARK(ST && u == 10, 10);
                 }
                 // after an abort: let every copy still in flight land before the CTA exits
                 for (int j = max(0, u - NB); j < u; ++j) mbar_drain(&full[j % NB], (uint32_t)((j / NB) & 1));
@@ -698,10 +705,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             const UnitInfo x = decode(u);
             const int bf = u % NB, r = u % NA;
             mbar_wait(&full[bf], (uint32_t)((u / NB) & 1), abort_flag, a.status);
+            DF_TRACE_MARK(ST && tid == 0 && u == 9, 3);
+            DF_TRACE_MARK(ST && tid == 0 && u == 10, 7);
             if (u >= NA) {
                 mbar_wait(&afree[r], (uint32_t)(((u / NA) - 1) & 1), abort_flag, a.status);
                 tc_fence_after();
             }
+            DF_TRACE_MARK(ST && tid == 0 && u == 9, 4);
+            DF_TRACE_MARK(ST && tid == 0 && u == 10, 8);
             const uint8_t *st = stg + (size_t)bf * kUnit;
             const int kbase = c0 + x.t * kTcKeys;
             const float *blkp = (x.v ? a.vb : a.kb) + head_off * a.blk * (size_t)D + x.h * 128;
@@ -794,6 +805,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
             }
             tmem_wait_st();
+            DF_TRACE_MARK(ST && tid == 0 && u == 9, 5);
+            DF_TRACE_MARK(ST && tid == 0 && u == 10, 0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aready[r]);
