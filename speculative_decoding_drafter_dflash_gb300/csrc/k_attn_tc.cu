@@ -121,6 +121,18 @@ __device__ __forceinline__ void conv_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConvThreads) : "memory");
 }
 
+// The same barrier, returning whether p holds in any converting thread.
+__device__ __forceinline__ bool conv_sync_or(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n barrier.cta.red.or.pred b, 1, %2, a;\n"
+        " selp.u32 %0, 1, 0, b;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)p), "n"(kConvThreads)
+        : "memory");
+    return r != 0;
+}
+
 template <int NPH>
 __device__ __forceinline__ void tmem_rows(uint32_t taddr, float (&v)[NPH]) {
     if constexpr (NPH == 4) {
@@ -949,18 +961,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 const int kt = lq * 32 + lane;
                 const int key = c0 + t * kTcKeys + kt;
+                // Does any score of the tile lie more than kTau above its row's reference (or give
+                // a row its first one)? Only then are the rows' maxima gathered across the four
+                // lane quarters; otherwise the reference stands and the tile needs no exchange.
+                bool need = false;
 #pragma unroll
-                for (int r = 0; r < NPH; ++r) mx[r] = row_ok(key, r0 + r) ? sv[r] * scale : -INFINITY;
-                int row;
-                const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
-                float *rb = red + (t & 1) * 4 * NP;   // alternate: a fast warp may reach tile t + 1
-                if ((lane & (32 / NPH - 1)) == 0) rb[lq * NP + r0 + row] = m;
-                conv_sync();
+                for (int r = 0; r < NPH; ++r) {
+                    mx[r] = row_ok(key, r0 + r) ? sv[r] * scale : -INFINITY;
+                    need |= mx[r] != -INFINITY && (mref[r] == -INFINITY || mx[r] > mref[r] + kTau);
+                }
+                const bool raise = conv_sync_or(need);   // the same in every converting warp
                 DF_TRACE_MARK(tid == 0 && t == 4, 20);
                 float mn[NPH];
+                if (raise) {
+                    int row;
+                    const float m = lane_reduce_rows<NPH, true>(mx, lane, row);
+                    float *rb = red + (t & 1) * 4 * NP;   // alternate: a fast warp may reach tile t + 1
+                    if ((lane & (32 / NPH - 1)) == 0) rb[lq * NP + r0 + row] = m;
+                    conv_sync();
 #pragma unroll
-                for (int r = 0; r < NPH; ++r)
-                    mn[r] = fmaxf(fmaxf(rb[r0 + r], rb[NP + r0 + r]), fmaxf(rb[2 * NP + r0 + r], rb[3 * NP + r0 + r]));
+                    for (int r = 0; r < NPH; ++r)
+                        mn[r] = fmaxf(fmaxf(rb[r0 + r], rb[NP + r0 + r]), fmaxf(rb[2 * NP + r0 + r], rb[3 * NP + r0 + r]));
+                }
                 // the P.V MMAs of tile t - 1 are done: the P buffer and the accumulator are free
                 if (t > 0) {
                     mbar_wait(&pfree[0], (uint32_t)((t - 1) & 1), abort_flag, a.status);
@@ -968,8 +990,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 DF_TRACE_MARK(tid == 0 && t == 4, 21);
                 bool resc = false;   // the same for every lane: the warp's lanes share its rows
+                if (raise) {
 #pragma unroll
-                for (int r = 0; r < NPH; ++r) resc |= mref[r] != -INFINITY && mn[r] > mref[r] + kTau;
+                    for (int r = 0; r < NPH; ++r) resc |= mref[r] != -INFINITY && mn[r] > mref[r] + kTau;
+                }
                 if (resc) {
                     float f[NPH];
 #pragma unroll
@@ -999,9 +1023,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     }
                     tmem_wait_st();
                 }
+                if (raise) {
 #pragma unroll
-                for (int r = 0; r < NPH; ++r)
-                    if (mref[r] == -INFINITY || mn[r] > mref[r] + kTau) mref[r] = mn[r];
+                    for (int r = 0; r < NPH; ++r)
+                        if (mref[r] == -INFINITY || mn[r] > mref[r] + kTau) mref[r] = mn[r];
+                }
                 // probabilities of tile t against the reference -> BF16 hi/lo P operand
                 const uint32_t pb = p_buf(t);
 #pragma unroll
