@@ -1028,18 +1028,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     for (int r = 0; r < NPH; ++r)
                         if (mref[r] == -INFINITY || mn[r] > mref[r] + kTau) mref[r] = mn[r];
                 }
-                // probabilities of tile t against the reference -> BF16 hi/lo P operand
-                const uint32_t pb = p_buf(t);
+                // probabilities of tile t against the reference -> BF16 hi/lo P operand, two rows
+                // per packed conversion (the same roundings as one row at a time)
+                const uint32_t prow = p_buf(t) + (uint32_t)((kt >> 6) * NS * 128 + ((kt & 7) << 1));
+                const int kc = (kt & 63) >> 3;   // the key's 16-byte piece of a 128-byte row
 #pragma unroll
-                for (int r = 0; r < NPH; ++r) {
-                    const int rr = r0 + r;
-                    float pv = 0.f;
-                    if (row_ok(key, rr) && mref[r] != -INFINITY) pv = ex2(sv[r] * scale - mref[r]);
-                    lsum[r] += pv;
-                    const uint16_t ph = f32_to_bf16_bits(pv);
-                    const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
-                    st_shared_u16(pb + sw_off(NS, rr, kt), ph);
-                    st_shared_u16(pb + sw_off(NS, NP + rr, kt), pl);
+                for (int r = 0; r < NPH; r += 2) {
+                    float pv[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        pv[i] = 0.f;
+                        if (row_ok(key, r0 + r + i) && mref[r + i] != -INFINITY)
+                            pv[i] = ex2(sv[r + i] * scale - mref[r + i]);
+                        lsum[r + i] += pv[i];
+                    }
+                    uint32_t hw, lw;
+                    split2(pv[0], pv[1], hw, lw);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int rr = r0 + r + i;   // (NP + rr) & 7 == rr & 7: NP is a multiple of 8
+                        const uint32_t o = prow + (uint32_t)(rr * 128 + ((kc ^ (rr & 7)) << 4));
+                        st_shared_u16(o, (uint16_t)(i ? hw >> 16 : hw & 0xffffu));
+                        st_shared_u16(o + NP * 128, (uint16_t)(i ? lw >> 16 : lw & 0xffffu));
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
