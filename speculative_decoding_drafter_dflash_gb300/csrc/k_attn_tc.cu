@@ -843,6 +843,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         float Mrow[NPH], lsum[NPH];
 #pragma unroll
         for (int r = 0; r < NPH; ++r) lsum[r] = 0.f;
+        // Probabilities of one tile (this thread's rows' scores sv at key kt of the tile) against
+        // the row references ref -> the BF16 hi/lo P operand at pb, two rows per packed
+        // conversion (the roundings of one row at a time); adds them to the row sums.
+        auto store_p = [&](uint32_t pb, int kt, int key, const float (&sv)[NPH], const float (&ref)[NPH]) {
+            const uint32_t prow = pb + (uint32_t)((kt >> 6) * NS * 128 + ((kt & 7) << 1));
+            const int kc = (kt & 63) >> 3;   // the key's 16-byte piece of a 128-byte row
+#pragma unroll
+            for (int r = 0; r < NPH; r += 2) {
+                float pv[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    pv[i] = 0.f;
+                    if (row_ok(key, r0 + r + i) && ref[r + i] != -INFINITY) pv[i] = ex2(sv[r + i] * scale - ref[r + i]);
+                    lsum[r + i] += pv[i];
+                }
+                uint32_t hw, lw;
+                split2(pv[0], pv[1], hw, lw);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int rr = r0 + r + i;   // (NP + rr) & 7 == rr & 7: NP is a multiple of 8
+                    const uint32_t o = prow + (uint32_t)(rr * 128 + ((kc ^ (rr & 7)) << 4));
+                    st_shared_u16(o, (uint16_t)(i ? hw >> 16 : hw & 0xffffu));
+                    st_shared_u16(o + NP * 128, (uint16_t)(i ? lw >> 16 : lw & 0xffffu));
+                }
+            }
+        };
         if (tid < NP) mrun[tid] = -INFINITY;
 
         // VS: softmax pass 1 over the chunk's nt tiles: exact row maxima into Mrow (the one-pass
@@ -891,19 +917,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
             }
             const int kt = lq * 32 + lane;
-            const int key = c0 + t * kTcKeys + kt;
-            const uint32_t pb = p_buf(t);
-#pragma unroll
-            for (int r = 0; r < NPH; ++r) {
-                const int row = r0 + r;
-                float pv = 0.f;
-                if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
-                lsum[r] += pv;
-                const uint16_t ph = f32_to_bf16_bits(pv);
-                const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
-                st_shared_u16(pb + sw_off(NS, row, kt), ph);
-                st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
-            }
+            store_p(p_buf(t), kt, c0 + t * kTcKeys + kt, sv, Mrow);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -1028,30 +1042,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                     for (int r = 0; r < NPH; ++r)
                         if (mref[r] == -INFINITY || mn[r] > mref[r] + kTau) mref[r] = mn[r];
                 }
-                // probabilities of tile t against the reference -> BF16 hi/lo P operand, two rows
-                // per packed conversion (the same roundings as one row at a time)
-                const uint32_t prow = p_buf(t) + (uint32_t)((kt >> 6) * NS * 128 + ((kt & 7) << 1));
-                const int kc = (kt & 63) >> 3;   // the key's 16-byte piece of a 128-byte row
-#pragma unroll
-                for (int r = 0; r < NPH; r += 2) {
-                    float pv[2];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        pv[i] = 0.f;
-                        if (row_ok(key, r0 + r + i) && mref[r + i] != -INFINITY)
-                            pv[i] = ex2(sv[r + i] * scale - mref[r + i]);
-                        lsum[r + i] += pv[i];
-                    }
-                    uint32_t hw, lw;
-                    split2(pv[0], pv[1], hw, lw);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int rr = r0 + r + i;   // (NP + rr) & 7 == rr & 7: NP is a multiple of 8
-                        const uint32_t o = prow + (uint32_t)(rr * 128 + ((kc ^ (rr & 7)) << 4));
-                        st_shared_u16(o, (uint16_t)(i ? hw >> 16 : hw & 0xffffu));
-                        st_shared_u16(o + NP * 128, (uint16_t)(i ? lw >> 16 : lw & 0xffffu));
-                    }
-                }
+                // probabilities of tile t against the reference -> BF16 hi/lo P operand
+                store_p(p_buf(t), kt, key, sv, mref);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -1122,19 +1114,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                         for (int r = 0; r < NPH; ++r) sv[r] = __uint_as_float(sh[r]) + __uint_as_float(sl[r]);
                     }
                     const int kt = lq * 32 + lane;
-                    const int key = c0 + t * kTcKeys + kt;
-                    const uint32_t pb = p_buf(t);
-#pragma unroll
-                    for (int r = 0; r < NPH; ++r) {
-                        const int row = r0 + r;
-                        float pv = 0.f;
-                        if (row_ok(key, row) && Mrow[r] != -INFINITY) pv = ex2(sv[r] * scale - Mrow[r]);
-                        lsum[r] += pv;
-                        const uint16_t ph = f32_to_bf16_bits(pv);
-                        const uint16_t pl = f32_to_bf16_bits(pv - bf16_bits_to_f32(ph));
-                        st_shared_u16(pb + sw_off(NS, row, kt), ph);
-                        st_shared_u16(pb + sw_off(NS, NP + row, kt), pl);
-                    }
+                    store_p(p_buf(t), kt, c0 + t * kTcKeys + kt, sv, Mrow);
                     fence_proxy_async_smem();
                     tc_fence_before();
                     __syncwarp();
