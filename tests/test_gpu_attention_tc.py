@@ -234,6 +234,52 @@ def test_attention_streamed_rescales_the_accumulator():
         assert rel_err(got[b], ref) <= ATTN_TOL, f"sequence {b}"
 
 
+def test_attention_streamed_late_spike_raises_the_reference():
+    """Scores of unit size except one key in the middle of a streamed chunk (tile 2 of its
+    5-tile chunk), whose score lies ~24 log2 units above the others for the query rows that point
+    along it and as far below for those that point away: the reference maximum stands for two
+    tiles, then only some rows exceed it by more than the margin, so the vote for gathering the
+    row maxima across lane quarters passes after tiles that skipped it, and rows that do not
+    raise keep their reference. q and the keys are BF16 values (exact in the hi half)."""
+    from oracle import core
+    Bn, blk, nq, nkv, d, S, cap = 2, 16, 64, 32, 128, 1200, 1200
+    assert _tc_chunk_keys(Bn, nkv, cap + blk) == 5 * 128
+    spike = 640 + 2 * 128 + 37           # chunk 1, tile 2
+    g = torch.Generator(device="cuda").manual_seed(11)
+    bf = lambda x: x.to(torch.bfloat16).float()
+    q = bf(torch.randn((Bn, blk, nq, d), generator=g, device="cuda"))
+    ck = torch.randn((Bn, nkv, cap, d), generator=g, device="cuda") * 0.5
+    # the spike key of every head points along the first query row of the head's first q head
+    for h in range(nkv):
+        u = q[:, 0, h * (nq // nkv)]
+        ck[:, h, spike] = u / u.norm(dim=-1, keepdim=True) * (24.0 / 1.4427 * d ** 0.5 / 11.3)
+    ck = bf(ck)
+    cv = torch.randn((Bn, nkv, cap, d), generator=g, device="cuda")
+    kb = bf(torch.randn((Bn, nkv, blk, d), generator=g, device="cuda"))
+    vb = torch.randn((Bn, nkv, blk, d), generator=g, device="cuda")
+    sl = torch.full((Bn,), S, dtype=torch.int32, device="cuda")
+    out = torch.full((Bn, blk, nq, d), float("nan"), device="cuda")
+    ws = B.alloc_workspace(B.attention_workspace_bytes(Bn, blk, nq, nkv, d, cap))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.attention(q, ck, cv, sl, out, ws, kb, vb, False, st)
+    torch.cuda.synchronize()
+    assert int(st) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    qh, kh, vh = synth.host(q), synth.host(ck), synth.host(cv)
+    for b in range(Bn):
+        keys = np.concatenate([kh[b, :, :S].transpose(1, 0, 2), synth.host(kb)[b].transpose(1, 0, 2)])
+        vals = np.concatenate([vh[b, :, :S].transpose(1, 0, 2), synth.host(vb)[b].transpose(1, 0, 2)])
+        ref = core.sdpa(qh[b], keys, vals, None, np.float64)
+        assert rel_err(got[b], ref) <= ATTN_TOL, f"sequence {b}"
+        # the case does what it is for: the aimed rows' spike score tops every earlier key of
+        # its chunk by more than the 8 log2 units the reference may lag
+        for h in range(nkv):
+            sc = kh[b, h, 640:spike + 1].astype(np.float64) @ qh[b, 0, h * (nq // nkv)].astype(np.float64)
+            sc *= 1.4426950408889634 / np.sqrt(d)
+            assert sc[-1] > sc[:-1].max() + 8.0
+
+
 def test_attention_head_dim_256_long_chunks_streamed():
     """8 sequences x 2 KV heads of head_dim 256 (MTP MoE heads) over 16000 keys: 9 chunks of 14
     tiles per head (144 CTAs), streamed tile by tile with both 128-wide halves of every K and V
