@@ -63,6 +63,17 @@ def test_bf16_kv_batched_streamed_chunks():
     assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
 
 
+def test_bf16_kv_three_tile_chunks_fill_every_buffer_once():
+    """One sequence x 8 KV heads over 6000 cached keys (6032 planned keys: 16 chunks of 3 tiles,
+    one wave): a streamed BF16 chunk then has as many units (6) as staging buffers, so every copy
+    is requested before the conversions start and the TMA-issuer warp has no refill to make."""
+    shape = TINY.with_(head_dim=128, n_q_heads=16, n_kv_heads=8, K=15, ctx=6000, batch=1,
+                       kv_bf16=True)
+    r = _run_forward(shape, [9], seed=97)
+    assert r["st"] == 0
+    assert rel_err(r["h_final"].cpu().numpy(), r["ref"]) <= REL_TOL
+
+
 def test_bf16_kv_head_dim_256_streamed_chunks():
     """head_dim 256 with a BF16 cache: 8 sequences x 2 KV heads over ~6000 keys, 6-tile chunks
     streamed tile by tile (both halves of each tile, four TMEM operand regions)."""
