@@ -2214,6 +2214,7 @@ int mtp_impl(const df_mtp_config *cfg, const df_mtp_weights *w, const df_kv_cach
         at.n_new = nullptr;
         at.n_new_max = 0;
         at.extra_rows = st + 1;
+        at.early_kv = 1;   // seq_len moves only at the end of the chain
         at.causal_block = 0;
         at.part = W.attn_part;
         at.gate = w->w_gate ? W.gate : nullptr;

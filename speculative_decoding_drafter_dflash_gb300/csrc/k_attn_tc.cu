@@ -305,18 +305,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         ++nis[bf & 3];
     };
     pdl_trigger();
-    // Units 0 and 1 are the K units of the chunk's first two tiles when the head dim is 128 (one
-    // half per tile) and those tiles exist. Rows that predate this round do not depend on the
-    // preceding kernels, so when both the tile and (for unit 1) the chunk's second tile lie below
-    // seq_len they are requested, and converted into their TMEM operands, before the wait: only
+    // Units 0 and 1 are the chunk's first K units: the K units of its first two tiles when the
+    // head dim is 128 (one half per tile), both halves of its first tile when it is 256. Rows
+    // that predate this call do not depend on the preceding kernels, so when a unit's tile lies
+    // below seq_len it is requested, and converted into its TMEM operand, before the wait: only
     // the score MMAs need q, which the preceding kernel writes.
     int n_early = 0;
     const long long c0e = (long long)chunk * a.chunk;
-    if (NH == 1 && a.early_kv) {
+    if (a.early_kv) {
         const long long old = a.seq_len[b];
-        while (n_early < min(ST ? 1 : 2, NB) && (n_early + 1) * kTcKeys <= a.chunk &&
-               c0e + (long long)(n_early + 1) * kTcKeys <= old &&
-               c0e + (long long)(n_early + 1) * kTcKeys <= a.cap)
+        auto tile_end = [&](int u) { return (long long)(u / NH + 1) * kTcKeys; };
+        while (n_early < min(ST ? 1 : 2, NB) && tile_end(n_early) <= a.chunk &&
+               c0e + tile_end(n_early) <= old && c0e + tile_end(n_early) <= a.cap)
             ++n_early;
     }
     if (tid == 0) {
@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         for (int t = 0; t < n_early; ++t) {
             uint8_t *dst = stg + (size_t)t * kUnit;
             mbar_expect_tx(&full[t], (uint32_t)kUnit);
-            const int y = (int)(head_off * a.cap + c0e) + t * kTcKeys;
-            tma_load_3d(dst, &P.kmap, &full[t], 0, y, 0, pol);
+            const int y = (int)(head_off * a.cap + c0e) + (t / NH) * kTcKeys;
+            tma_load_3d(dst, &P.kmap, &full[t], 0, y, (t % NH) * kBoxes, pol);
             ++nis[t & 3];
         }
         if (VS && n_early > 0) stage_v(2, (int)(head_off * a.cap + c0e));   // V unit 0
