@@ -305,8 +305,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         ++nis[bf & 3];
     };
     pdl_trigger();
-    // Units 0 and 1 are the chunk's first K units: the K units of its first two tiles when the
-    // head dim is 128 (one half per tile), both halves of its first tile when it is 256. Rows
+    // Units 0 and 1 are the chunk's first K units (in every form): the K units of its first two
+    // tiles when the head dim is 128 (one half per tile), both halves of its first tile when it
+    // is 256. Rows
     // that predate this call do not depend on the preceding kernels, so when a unit's tile lies
     // below seq_len it is requested, and converted into its TMEM operand, before the wait: only
     // the score MMAs need q, which the preceding kernel writes.
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     if (a.early_kv) {
         const long long old = a.seq_len[b];
         auto tile_end = [&](int u) { return (long long)(u / NH + 1) * kTcKeys; };
-        while (n_early < min(ST ? 1 : 2, NB) && tile_end(n_early) <= a.chunk &&
+        while (n_early < min(2, NB) && tile_end(n_early) <= a.chunk &&
                c0e + tile_end(n_early) <= old && c0e + tile_end(n_early) <= a.cap)
             ++n_early;
     }
